@@ -1,0 +1,398 @@
+#!/usr/bin/env python3
+"""Benchmark: dense matrix-free MTTKRP, every mode of one workload, on GB300.
+
+One step = M_k for every mode k of the workload (one mttkrp_all_modes call),
+inputs resident in HBM.  Prints one JSON line (rank 0):
+
+  value        MTTKRP GFLOP/s over all ranks, 2*R*prod(I_n) flops per mode
+  ms_per_step  milliseconds for all modes (device time, CUDA events, max over ranks)
+  e2e          the same metric through the public API from pinned host memory,
+               host->device copies of Y and the factors and device->host copies
+               of the outputs inside the timed region
+  roofline     the main contraction kernel: algorithmic flops per launch over its
+               average CUDA-event duration, against the pipe's peak
+  cpu_baseline the fp64 oracle on a bounded sample, on this host's cores
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4] [--path auto|simt|tc]
+  python bench.py --impl reference ...   # the oracle on the host cores, same metric
+
+N > 1 (torchrun): every rank runs the whole workload on its own GPU (replicas;
+the path needs no exchange between GPUs); value counts all ranks' work over
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+SM_MAX_MHZ_FALLBACK = 2070.0
+# nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): tf32 1.1 PFLOP/s
+TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="4")
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target length of the oracle CPU-baseline sample")
+    return ap.parse_args()
+
+
+def workload_from_arg(s):
+    return synth.workload(int(s)) if s.isdigit() else synth.workload(s)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": SM_MAX_MHZ_FALLBACK}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_tensor_decomposition_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".h", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, path, src_hash):
+    """DRAM bytes per launch of the main kernel from an ncu capture summary, if it
+    was taken on the current kernel sources (else None)."""
+    fn = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(fn):
+        return None
+    for line in open(fn):
+        if line.startswith("#") or not line.strip():
+            continue
+        kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+        if kv.get("workload") == workload and kv.get("path") == path and kv.get("src") == src_hash:
+            return float(kv["bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.device_index = device_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.device_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [l.strip().split(",") for l in self.file.read().splitlines() if l.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() in ("active", "1"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU side: the oracle (test infrastructure; used only for the baseline legs)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, Y, A, seconds):
+    """Time the fp64 oracle on sampled output rows of mode 0, sized to ~seconds."""
+    import oracle
+    k = 0
+    ncols = w.numel // w.dims[k]
+    t0 = time.perf_counter()
+    oracle.mttkrp(Y, A, k, rows=[0])
+    t1 = time.perf_counter() - t0
+    rows = int(max(1, min(w.dims[k], seconds / max(t1, 1e-3))))
+    rows_list = list(range(rows))
+    t0 = time.perf_counter()
+    oracle.mttkrp(Y, A, k, rows=rows_list)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * w.R * ncols * rows
+    return {"value": flops / dt / 1e9, "unit": "GFLOP/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"mode 0, output rows 0..{rows - 1} of {w.dims[k]} "
+                      f"({rows}/{w.dims[k]} of one mode), {dt:.1f} s, fp64"}
+
+
+def run_reference(args, w):
+    """--impl reference: the oracle on this host's cores, same metric and workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    Y = synth.make_tensor(w)
+    A = synth.make_factors(w)
+    # one step = one sampled output row of every mode
+    rows = [[w.dims[k] // 2] for k in range(w.d)]
+    flops = sum(2.0 * w.R * (w.numel // w.dims[k]) for k in range(w.d))
+
+    def step():
+        for k in range(w.d):
+            oracle.mttkrp(Y, A, k, rows=rows[k])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = flops / dt / 1e9
+    line = {
+        "impl": "reference",
+        "metric": "MTTKRP GFLOP/s (2*R*prod(I_n) per mode), all modes",
+        "value": round(value, 4), "unit": "GFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "dims": list(w.dims), "R": w.R,
+                   "step": "one sampled output row of every mode (bounded sample)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle",
+                         "sample": f"output row I_k/2 of each of the {w.d} modes per step"},
+        "e2e": {"value": round(value, 4), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU side
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    import dense_tensor_decomposition_gb300 as mk
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    Y = synth.make_tensor(w)
+    A = synth.make_factors(w)
+    Yd = torch.from_numpy(Y).to(device)
+    Ad = [torch.from_numpy(a).to(device) for a in A]
+    Md = [torch.empty(w.dims[k], w.R, device=device) for k in range(w.d)]
+    plan = mk.Plan(w.dims, w.R, args.path)
+    plan.attach_workspace(device)
+    stream = torch.cuda.current_stream(device)
+
+    # inputs that fit in L2 get an L2 flush (a 512 MiB write) before every timed
+    # step; each step is then timed with its own events, flush excluded
+    flush = None
+    if Y.nbytes <= L2_BYTES:
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+
+    for _ in range(args.warmup):
+        plan.all_modes(Yd, Ad, outs=Md)
+    torch.cuda.synchronize(device)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    plan.set_timing(True)
+    launches0 = plan.launch_count()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps if flush is not None else 1)]
+    barrier()
+    torch.cuda.synchronize(device)
+    w0 = time.perf_counter()
+    if flush is None:
+        evs[0][0].record(stream)
+        for _ in range(args.steps):
+            plan.all_modes(Yd, Ad, outs=Md)
+        evs[0][1].record(stream)
+    else:
+        for s in range(args.steps):
+            flush.fill_(s & 255)
+            evs[s][0].record(stream)
+            plan.all_modes(Yd, Ad, outs=Md)
+            evs[s][1].record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    wall = time.perf_counter() - w0
+    clk = clocks.stop()
+    launches = plan.launch_count() - launches0
+    ms_total = sum(a.elapsed_time(b) for a, b in evs)
+    kern = [t for k in range(w.d) for t in plan.kernel_times(k)]
+    plan.set_timing(False)
+
+    ms_max = ms_total
+    if world > 1:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    ms_per_step = ms_max / args.steps
+    flops_step = w.d * w.flops_per_mode()
+    value = world * flops_step / (ms_per_step * 1e-3) / 1e9
+
+    # ---- end to end through the public API, from pinned host memory ----
+    Yh = torch.from_numpy(Y).pin_memory()
+    Ah = [torch.from_numpy(a).pin_memory() for a in A]
+    Mh = [torch.empty(w.dims[k], w.R).pin_memory() for k in range(w.d)]
+    h2d = Yh.numel() * 4 + sum(a.numel() * 4 for a in Ah)
+    d2h = sum(m.numel() * 4 for m in Mh)
+    plan.all_modes_from_host(Yh, Ah, (Yd, Ad, Md), Mh)
+    torch.cuda.synchronize(device)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        plan.all_modes_from_host(Yh, Ah, (Yd, Ad, Md), Mh)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * flops_step / (e2e_ms * 1e-3) / 1e9
+    checksum = float(sum(float(m.double().abs().sum()) for m in Mh))
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # ---- roofline of the main contraction kernel ----
+    peaks, peak_src = measured_peaks()
+    path = plan.mode_path(0)
+    kern_ms = statistics.mean(kern) if kern else None
+    achieved_tflops = (w.flops_per_mode() / (kern_ms * 1e-3) / 1e12) if kern_ms else None
+    props = torch.cuda.get_device_properties(device)
+    if path == "tc":
+        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * TF32_OVER_BF16 / 3.0
+        bound = "tensor"
+        peak_note = (f"3xTF32: tf32 dense peak (bf16 sustained {peak_src} x 1.1/2.25) / 3 "
+                     "tensor-core products per fp32-accurate product")
+    else:
+        sm_mhz = peaks.get("sm_max_mhz", SM_MAX_MHZ_FALLBACK)
+        peak = props.multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
+        bound = "alu"
+        peak_note = (f"fp32 FMA pipe: {props.multi_processor_count} SMs x 128 lanes x 2 flops x "
+                     f"{sm_mhz:.0f} MHz (max SM clock)")
+    src_hash = kernel_source_hash()
+    traffic = recorded_traffic(w.name, path, src_hash)
+    roofline = {"bound": bound, "achieved": round(achieved_tflops, 3) if achieved_tflops else None,
+                "peak": round(peak, 3), "unit": "TFLOP/s",
+                "frac": round(achieved_tflops / peak, 4) if achieved_tflops else None,
+                "traffic": traffic, "peak_source": peak_note,
+                "kernel_ms_mean": round(kern_ms, 4) if kern_ms else None,
+                "kernel_launches_timed": len(kern),
+                "algorithmic_bytes_per_launch": max(w.bytes_per_mode(k) for k in range(w.d)),
+                "hbm_gbs_at_algorithmic_bytes":
+                    round(max(w.bytes_per_mode(k) for k in range(w.d)) / (kern_ms * 1e-3) / 1e9, 1)
+                    if kern_ms else None}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample(w, Y, A, args.cpu_seconds)
+
+    line = {
+        "metric": "MTTKRP GFLOP/s (2*R*prod(I_n) per mode), all modes",
+        "value": round(value, 2), "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "3xtf32" if path == "tc" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "dims": list(w.dims), "R": w.R, "modes": w.d,
+                   "path": path, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2 (Y {Y.nbytes >> 20} MiB > 129 MB)"
+                         if flush is None else "L2 flushed (512 MiB write) before every step",
+                   "ms_per_mode": round(ms_per_step / w.d, 4), "wall_s_timed": round(wall, 3)},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+        "gpu_launches": launches,
+        "kernel_src": src_hash,
+        "checksum": checksum,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    w = workload_from_arg(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

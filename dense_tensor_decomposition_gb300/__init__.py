@@ -1,0 +1,297 @@
+"""Dense, matrix-free MTTKRP on one GB300 (sm_103a).
+
+A thin ctypes binding of ``libmttkrp.so`` (C ABI in ``include/mttkrp.h``):
+it only checks and marshals arguments.  Every step of the computation runs in
+the library's CUDA kernels; PyTorch supplies device memory and streams.  There
+is no CPU fallback: if the library is missing this module raises.
+
+    M_k(i, r) = sum_{(i_n), n != k} Y(i_0..i_{d-1}) prod_{n != k} A_n(i_n, r)
+
+("A Performance Portable Matrix Free Dense MTTKRP in GenTen", abstract: the
+matricized tensor times Khatri-Rao product, computed without forming the
+Khatri-Rao matrix.)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from ._build import LIB as LIB_PATH, build  # noqa: F401
+
+__all__ = ["Plan", "mttkrp", "all_modes", "MttkrpError", "build", "load_library",
+           "exported_symbols", "PATH_AUTO", "PATH_SIMT", "PATH_TC"]
+
+PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
+_PATH_NAMES = {"auto": PATH_AUTO, "simt": PATH_SIMT, "tc": PATH_TC}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MttkrpError(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str):
+        self.code = code
+        super().__init__(f"{where}: {detail} (code {code})")
+
+
+def load_library():
+    """Load libmttkrp.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "dense_tensor_decomposition_gb300.build() (needs nvcc)")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i64, ci, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        lib.mttkrp_plan.argtypes = [ci, vp, i64, ctypes.POINTER(vp)]
+        lib.mttkrp_plan.restype = ci
+        lib.mttkrp_plan_set_path.argtypes = [vp, ci]
+        lib.mttkrp_plan_set_path.restype = ci
+        lib.mttkrp_workspace_bytes.argtypes = [vp, ci]
+        lib.mttkrp_workspace_bytes.restype = sz
+        lib.mttkrp_set_workspace.argtypes = [vp, vp, sz]
+        lib.mttkrp_set_workspace.restype = ci
+        lib.mttkrp.argtypes = [vp, vp, vp, ci, vp, vp]
+        lib.mttkrp.restype = ci
+        lib.mttkrp_all_modes.argtypes = [vp, vp, vp, vp, vp]
+        lib.mttkrp_all_modes.restype = ci
+        lib.mttkrp_plan_mode_path.argtypes = [vp, ci]
+        lib.mttkrp_plan_mode_path.restype = ci
+        lib.mttkrp_plan_describe.argtypes = [vp, ci, ctypes.c_char_p, sz]
+        lib.mttkrp_plan_describe.restype = ci
+        lib.mttkrp_plan_set_timing.argtypes = [vp, ci]
+        lib.mttkrp_plan_set_timing.restype = ci
+        lib.mttkrp_plan_kernel_times.argtypes = [vp, ci, ctypes.POINTER(ctypes.c_float), ci]
+        lib.mttkrp_plan_kernel_times.restype = ci
+        lib.mttkrp_plan_launch_count.argtypes = [vp]
+        lib.mttkrp_plan_launch_count.restype = i64
+        lib.mttkrp_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        lib.mttkrp_device_status.restype = ci
+        lib.mttkrp_plan_destroy.argtypes = [vp]
+        lib.mttkrp_plan_destroy.restype = None
+        lib.mttkrp_strerror.argtypes = [ci]
+        lib.mttkrp_strerror.restype = ctypes.c_char_p
+        lib.mttkrp_last_error.argtypes = []
+        lib.mttkrp_last_error.restype = ctypes.c_char_p
+        lib.mttkrp_version.argtypes = []
+        lib.mttkrp_version.restype = ci
+        _lib = lib
+        return lib
+
+
+def exported_symbols(header: str | None = None) -> list[str]:
+    """Names of the functions declared in include/mttkrp.h."""
+    if header is None:
+        header = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                              "include", "mttkrp.h")
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mttkrp\w*)\s*\(", text)))
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        lib = load_library()
+        detail = lib.mttkrp_last_error().decode() or lib.mttkrp_strerror(rc).decode()
+        raise MttkrpError(rc, where, detail)
+
+
+def _stream_handle(device, stream=None):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Plan:
+    """Planner decisions for one tensor shape and rank, plus its workspace.
+
+    The workspace is a PyTorch uint8 tensor on the tensors' device, sized by the
+    library (``mttkrp_workspace_bytes``) and attached on first use.
+    """
+
+    def __init__(self, dims, R: int, path: str | int = "auto"):
+        self._lib = load_library()
+        self.dims = tuple(int(x) for x in dims)
+        self.R = int(R)
+        self.d = len(self.dims)
+        arr = (ctypes.c_int64 * self.d)(*self.dims)
+        h = ctypes.c_void_p()
+        _check(self._lib.mttkrp_plan(self.d, arr, self.R, ctypes.byref(h)), "mttkrp_plan")
+        self._h = h
+        self._ws = None
+        self._ws_device = None
+        self._ws_user = False
+        if path not in ("auto", PATH_AUTO):
+            self.set_path(path)
+
+    # -- planner queries -------------------------------------------------
+    def set_path(self, path):
+        p = _PATH_NAMES[path] if isinstance(path, str) else int(path)
+        _check(self._lib.mttkrp_plan_set_path(self._h, p), "mttkrp_plan_set_path")
+        if not self._ws_user:
+            self._ws = None  # requirement may have changed
+
+    def workspace_bytes(self, mode: int = -1) -> int:
+        return int(self._lib.mttkrp_workspace_bytes(self._h, mode))
+
+    def mode_path(self, mode: int) -> str:
+        p = self._lib.mttkrp_plan_mode_path(self._h, mode)
+        return {PATH_SIMT: "simt", PATH_TC: "tc"}.get(p, "invalid")
+
+    def describe(self, mode: int) -> str:
+        buf = ctypes.create_string_buffer(512)
+        n = self._lib.mttkrp_plan_describe(self._h, mode, buf, 512)
+        if n < 0:
+            raise ValueError(f"invalid mode {mode}")
+        return buf.value.decode()
+
+    def set_timing(self, enable: bool = True):
+        """Record CUDA events around every main kernel (resets earlier records)."""
+        rc = self._lib.mttkrp_plan_set_timing(self._h, int(bool(enable)))
+        if rc < 0:
+            _check(-rc, "mttkrp_plan_set_timing")
+
+    def kernel_times(self, mode: int) -> list[float]:
+        """Durations (ms) of the main kernel of `mode` recorded since set_timing()."""
+        n = self._lib.mttkrp_plan_kernel_times(self._h, mode, None, 0)
+        if n < 0:
+            _check(-n, "mttkrp_plan_kernel_times")
+        buf = (ctypes.c_float * max(n, 1))()
+        n2 = self._lib.mttkrp_plan_kernel_times(self._h, mode, buf, n)
+        if n2 < 0:
+            _check(-n2, "mttkrp_plan_kernel_times")
+        return [float(buf[i]) for i in range(n)]
+
+    def launch_count(self) -> int:
+        return int(self._lib.mttkrp_plan_launch_count(self._h))
+
+    # -- workspace ---------------------------------------------------------
+    def attach_workspace(self, device):
+        """Allocate (through PyTorch) and attach a workspace, unless the caller
+        attached its own memory with set_workspace_ptr()."""
+        import torch
+        if self._ws_user:
+            return
+        need = self.workspace_bytes(-1)
+        if self._ws is not None and self._ws_device == device and self._ws.numel() >= need:
+            return
+        self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        self._ws_device = device
+        _check(self._lib.mttkrp_set_workspace(self._h, ctypes.c_void_p(self._ws.data_ptr()),
+                                              self._ws.numel()), "mttkrp_set_workspace")
+
+    def set_workspace_ptr(self, ptr: int, nbytes: int):
+        """Attach caller-owned device memory (raw pointer) as the workspace.
+        The plan then never allocates one itself; the library checks the size."""
+        self._ws = None
+        self._ws_user = True
+        _check(self._lib.mttkrp_set_workspace(self._h, ctypes.c_void_p(ptr), nbytes),
+               "mttkrp_set_workspace")
+
+    # -- argument checks -------------------------------------------------
+    def _check_inputs(self, Y, factors, skip_mode=None):
+        import torch
+        if not isinstance(Y, torch.Tensor) or not Y.is_cuda:
+            raise TypeError("Y must be a CUDA tensor")
+        if Y.dtype != torch.float32 or tuple(Y.shape) != self.dims or not Y.is_contiguous():
+            raise ValueError(f"Y must be a contiguous float32 tensor of shape {self.dims}")
+        if len(factors) != self.d:
+            raise ValueError(f"need {self.d} factors")
+        ptrs = []
+        for n, a in enumerate(factors):
+            if a is None:
+                if n != skip_mode:
+                    raise ValueError(f"factor {n} is None")
+                ptrs.append(None)
+                continue
+            if a.device != Y.device or a.dtype != torch.float32 or not a.is_contiguous() \
+                    or tuple(a.shape) != (self.dims[n], self.R):
+                raise ValueError(f"factor {n} must be a contiguous float32 "
+                                 f"{(self.dims[n], self.R)} tensor on {Y.device}")
+            ptrs.append(a.data_ptr())
+        return (ctypes.c_void_p * self.d)(*ptrs)
+
+    def _check_out(self, out, mode, device):
+        import torch
+        shape = (self.dims[mode], self.R)
+        if out is None:
+            return torch.empty(shape, dtype=torch.float32, device=device)
+        if out.device != device or out.dtype != torch.float32 or not out.is_contiguous() \
+                or tuple(out.shape) != shape:
+            raise ValueError(f"out must be a contiguous float32 {shape} tensor on {device}")
+        return out
+
+    # -- compute -----------------------------------------------------------
+    def mttkrp(self, Y, factors, mode: int, out=None, stream=None):
+        """M_mode (I_mode x R) for device tensors; enqueued on the current stream."""
+        if not 0 <= mode < self.d:
+            raise ValueError(f"mode {mode} out of range")
+        ptrs = self._check_inputs(Y, factors, skip_mode=mode)
+        out = self._check_out(out, mode, Y.device)
+        self.attach_workspace(Y.device)
+        _check(self._lib.mttkrp(self._h, ctypes.c_void_p(Y.data_ptr()), ptrs, mode,
+                                ctypes.c_void_p(out.data_ptr()), _stream_handle(Y.device, stream)),
+               "mttkrp")
+        return out
+
+    def all_modes(self, Y, factors, outs=None, stream=None):
+        """[M_0, ..., M_{d-1}] for device tensors, one call into the library."""
+        ptrs = self._check_inputs(Y, factors)
+        if outs is None:
+            outs = [None] * self.d
+        outs = [self._check_out(o, k, Y.device) for k, o in enumerate(outs)]
+        optrs = (ctypes.c_void_p * self.d)(*[o.data_ptr() for o in outs])
+        self.attach_workspace(Y.device)
+        _check(self._lib.mttkrp_all_modes(self._h, ctypes.c_void_p(Y.data_ptr()), ptrs, optrs,
+                                          _stream_handle(Y.device, stream)), "mttkrp_all_modes")
+        return outs
+
+    def all_modes_from_host(self, Y_host, factors_host, dev_bufs, outs_host, stream=None):
+        """End-to-end call from pinned host memory: copy in, compute every mode, copy out.
+
+        dev_bufs = (Y_dev, [A_dev...], [M_dev...]) preallocated device tensors.
+        Copies are enqueued on the same stream as the kernels.
+        """
+        Y_dev, A_dev, M_dev = dev_bufs
+        Y_dev.copy_(Y_host, non_blocking=True)
+        for a_d, a_h in zip(A_dev, factors_host):
+            a_d.copy_(a_h, non_blocking=True)
+        self.all_modes(Y_dev, A_dev, outs=M_dev, stream=stream)
+        for m_h, m_d in zip(outs_host, M_dev):
+            m_h.copy_(m_d, non_blocking=True)
+        return outs_host
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.mttkrp_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+        self._ws = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def mttkrp(Y, factors, mode: int, path="auto"):
+    """One-shot MTTKRP of one mode (plans on every call)."""
+    plan = Plan(tuple(Y.shape), factors[(mode + 1) % len(factors)].shape[1], path)
+    return plan.mttkrp(Y, factors, mode)
+
+
+def all_modes(Y, factors, path="auto"):
+    plan = Plan(tuple(Y.shape), factors[0].shape[1], path)
+    return plan.all_modes(Y, factors)
+
+
+def device_status() -> int:
+    """Read and clear the kernels' device-side error word (synchronises)."""
+    w = ctypes.c_uint32(0)
+    _check(load_library().mttkrp_device_status(ctypes.byref(w)), "mttkrp_device_status")
+    return int(w.value)

@@ -1,0 +1,506 @@
+// Host side of the MTTKRP library: the C ABI of include/mttkrp.h, the planner
+// (mode classification, inner-group choice, tiles, split counts, workspace
+// layout) and the launch sequence of one mode:
+//   1. factor-product tables G (pre modes, with Y base offsets) and, for an
+//      inner group of several modes, Binner;
+//   2. the main kernel (SIMT or tensor-core path) over tiles x split ranges;
+//   3. if the contraction range was split, the fixed-order fp64 reduction.
+// Everything is enqueued on the caller's stream; nothing synchronises.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+#include "tc.h"
+
+namespace mk {
+namespace {
+
+thread_local char g_errmsg[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_errmsg, sizeof(g_errmsg), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+constexpr int64_t kMaxR = 65536;
+constexpr int64_t kMaxNumel = (int64_t)1 << 40;
+// Inner-group size the planner aims for (at least this many j values per pi).
+constexpr int64_t kInnerMin = 64;
+// Longest fp32 accumulation chain (in products) allowed in one SIMT thread; more
+// contraction work is split into ranges whose partials are summed in fp64.
+constexpr int64_t kSimtChain = 8192;
+// CTAs the SIMT grid aims for: 2 waves of 2 CTAs on each of 152 SMs.
+constexpr int64_t kSimtTargetCtas = 608;
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+void classify(const Plan& p, int k, ModeGeom& g) {
+    const int d = p.d;
+    g.k = k;
+    g.I = p.dims[k];
+    g.R = p.R;
+    g.s_k = p.strides[k];
+    int64_t Q = 1;
+    for (int n = k + 1; n < d; ++n) Q *= p.dims[n];
+    bool in_group[kMaxD] = {false};
+    int64_t J = 1, Jq = 1;
+    if (Q >= kInnerMin) {
+        // trailing modes after k until the product reaches kInnerMin
+        for (int n = d - 1; n > k && J < kInnerMin; --n) {
+            in_group[n] = true;
+            J *= p.dims[n];
+        }
+        Jq = J;
+    } else {
+        // all modes after k, then the last modes before k
+        for (int n = k + 1; n < d; ++n) in_group[n] = true;
+        J = Jq = Q;
+        for (int n = k - 1; n >= 0 && J < kInnerMin; --n) {
+            in_group[n] = true;
+            J *= p.dims[n];
+        }
+    }
+    g.J = J;
+    g.Jq = Jq;
+    g.IQ = (k > 0) ? p.strides[k - 1] : 0;
+    g.ngroup = 0;
+    g.npm = 0;
+    g.npre = 1;
+    for (int n = 0; n < d; ++n) {
+        if (n == k) continue;
+        if (in_group[n]) {
+            g.group[g.ngroup++] = n;
+        } else {
+            g.pm[g.npm++] = n;
+            g.npre *= p.dims[n];
+        }
+    }
+}
+
+void plan_simt(ModePlan& mp) {
+    const ModeGeom& g = mp.g;
+    mp.path = MTTKRP_PATH_SIMT;
+    mp.bn = g.R > 64 ? 128 : 64;
+    mp.bm = g.I >= 96 ? 128 : (g.I > 32 ? 64 : 32);
+    const int64_t tiles = cdiv(g.I, mp.bm) * cdiv(g.R, mp.bn);
+    const int64_t K = g.npre * g.J;
+    int64_t S = cdiv(K, kSimtChain);
+    const int64_t s_par = cdiv(kSimtTargetCtas, tiles);
+    if (s_par > S) S = s_par;
+    if (S > g.npre) S = g.npre;
+    if (S > 65535) S = 65535;
+    if (S < 1) S = 1;
+    mp.pre_per_split = cdiv(g.npre, S);
+    mp.splits = cdiv(g.npre, mp.pre_per_split);
+}
+
+void layout_workspace(ModePlan& mp) {
+    const ModeGeom& g = mp.g;
+    size_t off = 256;  // first 256 bytes reserved
+    mp.off_partials = off;
+    if (mp.splits > 1) off = align256(off + (size_t)mp.splits * g.I * g.R * sizeof(float));
+    mp.off_binner = off;
+    if (mp.path == MTTKRP_PATH_TC) {
+        off = align256(off + tc_binner_bytes(mp));
+    } else if (g.ngroup > 1) {
+        off = align256(off + (size_t)g.J * g.R * sizeof(float));
+    }
+    mp.off_gtab = off;
+    off = align256(off + (size_t)g.npre * g.R * sizeof(float));
+    mp.off_base = off;
+    off = align256(off + (size_t)g.npre * sizeof(int64_t));
+    mp.total = off;
+}
+
+int plan_mode(Plan& p, int k, int path) {
+    ModePlan& mp = p.mode[k];
+    memset(&mp, 0, sizeof(mp));
+    classify(p, k, mp.g);
+    if (path == MTTKRP_PATH_AUTO) path = tc_prefer(mp) ? MTTKRP_PATH_TC : MTTKRP_PATH_SIMT;
+    if (path == MTTKRP_PATH_TC) {
+        if (!tc_plan(mp)) return MTTKRP_ERR_UNSUPPORTED;
+    } else {
+        plan_simt(mp);
+        // row tiles run along gridDim.y (at most 65535)
+        if (cdiv(mp.g.I, mp.bm) > 65535) return MTTKRP_ERR_UNSUPPORTED;
+    }
+    layout_workspace(mp);
+    return MTTKRP_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+
+// Event pair for the next timed main kernel of mode k (grown on demand).
+cudaError_t timing_pair(Plan& p, int k, cudaEvent_t* e0, cudaEvent_t* e1) {
+    if (p.ev_n[k] == p.ev_cap[k]) {
+        const int cap = p.ev_cap[k] ? 2 * p.ev_cap[k] : 64;
+        cudaEvent_t* s = new (std::nothrow) cudaEvent_t[cap];
+        cudaEvent_t* t = new (std::nothrow) cudaEvent_t[cap];
+        if (!s || !t) {
+            delete[] s;
+            delete[] t;
+            return cudaErrorMemoryAllocation;
+        }
+        for (int i = 0; i < p.ev_cap[k]; ++i) {
+            s[i] = p.ev_start[k][i];
+            t[i] = p.ev_stop[k][i];
+        }
+        for (int i = p.ev_cap[k]; i < cap; ++i) s[i] = t[i] = nullptr;
+        delete[] p.ev_start[k];
+        delete[] p.ev_stop[k];
+        p.ev_start[k] = s;
+        p.ev_stop[k] = t;
+        p.ev_cap[k] = cap;
+    }
+    const int i = p.ev_n[k];
+    cudaError_t err;
+    if (p.ev_start[k][i] == nullptr && (err = cudaEventCreate(&p.ev_start[k][i])) != cudaSuccess) return err;
+    if (p.ev_stop[k][i] == nullptr && (err = cudaEventCreate(&p.ev_stop[k][i])) != cudaSuccess) return err;
+    *e0 = p.ev_start[k][i];
+    *e1 = p.ev_stop[k][i];
+    return cudaSuccess;
+}
+
+void free_events(Plan& p) {
+    for (int k = 0; k < kMaxD; ++k) {
+        for (int i = 0; i < p.ev_cap[k]; ++i) {
+            if (p.ev_start[k][i]) cudaEventDestroy(p.ev_start[k][i]);
+            if (p.ev_stop[k][i]) cudaEventDestroy(p.ev_stop[k][i]);
+        }
+        delete[] p.ev_start[k];
+        delete[] p.ev_stop[k];
+        p.ev_start[k] = p.ev_stop[k] = nullptr;
+        p.ev_cap[k] = p.ev_n[k] = 0;
+    }
+}
+
+int run_mode(Plan& p, const float* Y, const float* const* factors, int k, float* out,
+             cudaStream_t stream) {
+    ModePlan& mp = p.mode[k];
+    const ModeGeom& g = mp.g;
+    if (p.ws == nullptr && mp.total > 0)
+        return fail(MTTKRP_ERR_WORKSPACE, "no workspace attached (mode %d needs %zu bytes)", k,
+                    mp.total);
+    if (p.ws_bytes < mp.total)
+        return fail(MTTKRP_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes mode %d needs",
+                    p.ws_bytes, mp.total, k);
+    for (int n = 0; n < p.d; ++n)
+        if (n != k && factors[n] == nullptr)
+            return fail(MTTKRP_ERR_INVALID, "factor %d is NULL", n);
+    if (((reinterpret_cast<uintptr_t>(Y) | reinterpret_cast<uintptr_t>(out)) & 3) != 0)
+        return fail(MTTKRP_ERR_INVALID, "Y and out must be 4-byte aligned");
+
+    char* ws = static_cast<char*>(p.ws);
+    float* partials = reinterpret_cast<float*>(ws + mp.off_partials);
+    float* gtab = reinterpret_cast<float*>(ws + mp.off_gtab);
+    int64_t* basetab = reinterpret_cast<int64_t*>(ws + mp.off_base);
+    cudaError_t err;
+
+    // 1. G table and base offsets of the pre indices
+    {
+        ProdTableArgs a;
+        memset(&a, 0, sizeof(a));
+        a.nm = g.npm;
+        for (int t = 0; t < g.npm; ++t) {
+            a.dim[t] = p.dims[g.pm[t]];
+            a.ystride[t] = p.strides[g.pm[t]];
+            a.fac[t] = factors[g.pm[t]];
+        }
+        a.rows = g.npre;
+        a.R = g.R;
+        a.tab = gtab;
+        a.base = basetab;
+        if ((err = launch_prod_table(a, stream)) != cudaSuccess)
+            return fail(MTTKRP_ERR_CUDA, "table launch: %s", cudaGetErrorString(err));
+        ++p.launches;
+    }
+    float* dst = mp.splits > 1 ? partials : out;
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+    if (p.timing) {
+        if ((err = timing_pair(p, k, &ev0, &ev1)) != cudaSuccess)
+            return fail(MTTKRP_ERR_CUDA, "timing events: %s", cudaGetErrorString(err));
+    }
+
+    if (mp.path == MTTKRP_PATH_TC) {
+        int nlaunch = 0;
+        if (ev0) cudaEventRecord(ev0, stream);
+        int rc = tc_run(p, mp, Y, factors, gtab, basetab, ws + mp.off_binner, dst, stream, &nlaunch,
+                        ev0 ? &ev0 : nullptr, g_errmsg, sizeof(g_errmsg));
+        p.launches += nlaunch;
+        if (rc != MTTKRP_OK) return rc;
+        if (ev1) {
+            cudaEventRecord(ev1, stream);
+            ++p.ev_n[k];
+        }
+    } else {
+        // 2. Binner (only for an inner group of several modes; else the factor itself)
+        const float* binner;
+        if (g.ngroup > 1) {
+            float* bt = reinterpret_cast<float*>(ws + mp.off_binner);
+            ProdTableArgs a;
+            memset(&a, 0, sizeof(a));
+            a.nm = g.ngroup;
+            for (int t = 0; t < g.ngroup; ++t) {
+                a.dim[t] = p.dims[g.group[t]];
+                a.ystride[t] = p.strides[g.group[t]];
+                a.fac[t] = factors[g.group[t]];
+            }
+            a.rows = g.J;
+            a.R = g.R;
+            a.tab = bt;
+            a.base = nullptr;
+            if ((err = launch_prod_table(a, stream)) != cudaSuccess)
+                return fail(MTTKRP_ERR_CUDA, "table launch: %s", cudaGetErrorString(err));
+            ++p.launches;
+            binner = bt;
+        } else {
+            binner = factors[g.group[0]];
+        }
+        // 3. main kernel
+        SimtArgs a;
+        a.Y = Y;
+        a.binner = binner;
+        a.gtab = gtab;
+        a.base = basetab;
+        a.dst = dst;
+        a.dst_split_stride = g.I * g.R;
+        a.I = g.I;
+        a.R = g.R;
+        a.J = g.J;
+        a.Jq = g.Jq;
+        a.IQ = g.IQ;
+        a.s_k = g.s_k;
+        a.npre = g.npre;
+        a.pre_per_split = mp.pre_per_split;
+        bool strides4 = true;
+        for (int t = 0; t < g.npm; ++t) strides4 = strides4 && (p.strides[g.pm[t]] % 4 == 0);
+        if (g.J > g.Jq) strides4 = strides4 && (g.IQ % 4 == 0);
+        int amode = kLoadScalar;
+        if (aligned16(Y) && strides4) {
+            if (g.s_k != 1 && g.s_k % 4 == 0 && g.Jq % 4 == 0) amode = kLoadVecJ;
+            else if (g.s_k == 1 && g.I % 4 == 0) amode = kLoadVecI;
+        }
+        const bool bvec = (g.R % 4 == 0) && aligned16(binner);
+        if (ev0) cudaEventRecord(ev0, stream);
+        if ((err = launch_simt(mp.bm, mp.bn, amode, bvec, a, mp.splits, stream)) != cudaSuccess)
+            return fail(MTTKRP_ERR_CUDA, "SIMT kernel launch: %s", cudaGetErrorString(err));
+        ++p.launches;
+        if (ev1) {
+            cudaEventRecord(ev1, stream);
+            ++p.ev_n[k];
+        }
+    }
+    // 4. fixed-order reduction of the split partials
+    if (mp.splits > 1) {
+        if ((err = launch_reduce_splits(partials, mp.splits, g.I * g.R, out, stream)) != cudaSuccess)
+            return fail(MTTKRP_ERR_CUDA, "reduce launch: %s", cudaGetErrorString(err));
+        ++p.launches;
+    }
+    return MTTKRP_OK;
+}
+
+Plan* as_plan(mttkrp_plan_t h) { return reinterpret_cast<Plan*>(h); }
+
+}  // namespace
+}  // namespace mk
+
+using namespace mk;
+
+extern "C" {
+
+int mttkrp_plan(int d, const int64_t* dims, int64_t R, mttkrp_plan_t* out) {
+    g_errmsg[0] = 0;
+    if (out == nullptr) return fail(MTTKRP_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    if (d < 2 || d > kMaxD) return fail(MTTKRP_ERR_INVALID, "order d=%d outside [2, %d]", d, kMaxD);
+    if (dims == nullptr) return fail(MTTKRP_ERR_INVALID, "dims is NULL");
+    if (R < 1 || R > kMaxR) return fail(MTTKRP_ERR_INVALID, "rank R=%lld outside [1, %lld]", (long long)R, (long long)kMaxR);
+    int64_t numel = 1;
+    for (int n = 0; n < d; ++n) {
+        if (dims[n] < 1) return fail(MTTKRP_ERR_INVALID, "dims[%d]=%lld < 1", n, (long long)dims[n]);
+        if (dims[n] > kMaxNumel || numel > kMaxNumel / dims[n])
+            return fail(MTTKRP_ERR_INVALID, "tensor has more than 2^40 elements");
+        numel *= dims[n];
+    }
+    Plan* p = new (std::nothrow) Plan;
+    if (p == nullptr) return fail(MTTKRP_ERR_HOST_ALLOC, "plan allocation failed");
+    memset(p, 0, sizeof(*p));
+    p->d = d;
+    p->R = R;
+    for (int n = 0; n < d; ++n) p->dims[n] = dims[n];
+    p->strides[d - 1] = 1;
+    for (int n = d - 2; n >= 0; --n) p->strides[n] = p->strides[n + 1] * p->dims[n + 1];
+    p->forced_path = MTTKRP_PATH_AUTO;
+    for (int k = 0; k < d; ++k) {
+        int rc = plan_mode(*p, k, MTTKRP_PATH_AUTO);
+        if (rc != MTTKRP_OK) {
+            delete p;
+            return fail(rc, "planning mode %d failed", k);
+        }
+    }
+    *out = reinterpret_cast<mttkrp_plan_t>(p);
+    return MTTKRP_OK;
+}
+
+int mttkrp_plan_set_path(mttkrp_plan_t h, int path) {
+    Plan* p = as_plan(h);
+    if (p == nullptr) return fail(MTTKRP_ERR_INVALID, "plan is NULL");
+    if (path != MTTKRP_PATH_AUTO && path != MTTKRP_PATH_SIMT && path != MTTKRP_PATH_TC)
+        return fail(MTTKRP_ERR_INVALID, "unknown path %d", path);
+    ModePlan saved[kMaxD];
+    memcpy(saved, p->mode, sizeof(saved));
+    for (int k = 0; k < p->d; ++k) {
+        int rc = plan_mode(*p, k, path);
+        if (rc != MTTKRP_OK) {
+            memcpy(p->mode, saved, sizeof(saved));
+            return fail(rc, "mode %d cannot run on path %d", k, path);
+        }
+    }
+    p->forced_path = path;
+    return MTTKRP_OK;
+}
+
+size_t mttkrp_workspace_bytes(mttkrp_plan_t h, int mode) {
+    Plan* p = as_plan(h);
+    if (p == nullptr || mode < -1 || mode >= p->d) return 0;
+    if (mode >= 0) return p->mode[mode].total;
+    size_t m = 0;
+    for (int k = 0; k < p->d; ++k)
+        if (p->mode[k].total > m) m = p->mode[k].total;
+    return m;
+}
+
+int mttkrp_set_workspace(mttkrp_plan_t h, void* dptr, size_t bytes) {
+    Plan* p = as_plan(h);
+    if (p == nullptr) return fail(MTTKRP_ERR_INVALID, "plan is NULL");
+    if (dptr != nullptr && (reinterpret_cast<uintptr_t>(dptr) & 255) != 0)
+        return fail(MTTKRP_ERR_INVALID, "workspace must be 256-byte aligned");
+    p->ws = dptr;
+    p->ws_bytes = dptr ? bytes : 0;
+    return MTTKRP_OK;
+}
+
+int mttkrp(mttkrp_plan_t h, const float* Y, const float* const* factors, int mode, float* out,
+           void* stream) {
+    g_errmsg[0] = 0;
+    Plan* p = as_plan(h);
+    if (p == nullptr) return fail(MTTKRP_ERR_INVALID, "plan is NULL");
+    if (mode < 0 || mode >= p->d) return fail(MTTKRP_ERR_INVALID, "mode %d outside [0, %d)", mode, p->d);
+    if (Y == nullptr || factors == nullptr || out == nullptr)
+        return fail(MTTKRP_ERR_INVALID, "NULL tensor, factor array or output");
+    return run_mode(*p, Y, factors, mode, out, static_cast<cudaStream_t>(stream));
+}
+
+int mttkrp_all_modes(mttkrp_plan_t h, const float* Y, const float* const* factors,
+                     float* const* outs, void* stream) {
+    g_errmsg[0] = 0;
+    Plan* p = as_plan(h);
+    if (p == nullptr) return fail(MTTKRP_ERR_INVALID, "plan is NULL");
+    if (Y == nullptr || factors == nullptr || outs == nullptr)
+        return fail(MTTKRP_ERR_INVALID, "NULL tensor, factor array or output array");
+    for (int k = 0; k < p->d; ++k) {
+        if (factors[k] == nullptr) return fail(MTTKRP_ERR_INVALID, "factor %d is NULL", k);
+        if (outs[k] == nullptr) return fail(MTTKRP_ERR_INVALID, "output %d is NULL", k);
+    }
+    for (int k = 0; k < p->d; ++k) {
+        int rc = run_mode(*p, Y, factors, k, outs[k], static_cast<cudaStream_t>(stream));
+        if (rc != MTTKRP_OK) return rc;
+    }
+    return MTTKRP_OK;
+}
+
+int mttkrp_plan_mode_path(mttkrp_plan_t h, int mode) {
+    Plan* p = as_plan(h);
+    if (p == nullptr || mode < 0 || mode >= p->d) return -1;
+    return p->mode[mode].path;
+}
+
+int mttkrp_plan_describe(mttkrp_plan_t h, int mode, char* buf, size_t len) {
+    Plan* p = as_plan(h);
+    if (p == nullptr || mode < 0 || mode >= p->d) return -1;
+    const ModePlan& mp = p->mode[mode];
+    const ModeGeom& g = mp.g;
+    char groups[64] = "", pres[64] = "";
+    for (int t = 0; t < g.ngroup; ++t)
+        snprintf(groups + strlen(groups), sizeof(groups) - strlen(groups), "%s%d", t ? "," : "", g.group[t]);
+    for (int t = 0; t < g.npm; ++t)
+        snprintf(pres + strlen(pres), sizeof(pres) - strlen(pres), "%s%d", t ? "," : "", g.pm[t]);
+    char tmp[512];
+    int n = snprintf(tmp, sizeof(tmp),
+                     "mode=%d path=%s tile=%dx%d inner_group=[%s] J=%lld Jq=%lld pre_modes=[%s] "
+                     "npre=%lld splits=%lld pre_per_split=%lld workspace=%zu",
+                     mode, mp.path == MTTKRP_PATH_TC ? "tc" : "simt", mp.bm, mp.bn, groups,
+                     (long long)g.J, (long long)g.Jq, pres, (long long)g.npre,
+                     (long long)mp.splits, (long long)mp.pre_per_split, mp.total);
+    if (buf != nullptr && len > 0) {
+        strncpy(buf, tmp, len - 1);
+        buf[len - 1] = 0;
+    }
+    return n;
+}
+
+int mttkrp_device_status(uint32_t* word) {
+    if (word == nullptr) return fail(MTTKRP_ERR_INVALID, "word is NULL");
+    cudaError_t err = tc_read_and_clear_status(word);
+    if (err != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "status read: %s", cudaGetErrorString(err));
+    return MTTKRP_OK;
+}
+
+int mttkrp_plan_set_timing(mttkrp_plan_t h, int enable) {
+    Plan* p = as_plan(h);
+    if (p == nullptr) return -fail(MTTKRP_ERR_INVALID, "plan is NULL");
+    p->timing = enable ? 1 : 0;
+    for (int k = 0; k < kMaxD; ++k) p->ev_n[k] = 0;
+    return MTTKRP_OK;
+}
+
+int mttkrp_plan_kernel_times(mttkrp_plan_t h, int mode, float* ms, int max) {
+    Plan* p = as_plan(h);
+    if (p == nullptr || mode < 0 || mode >= p->d || (ms == nullptr && max > 0))
+        return -fail(MTTKRP_ERR_INVALID, "invalid plan, mode or buffer");
+    const int n = p->ev_n[mode];
+    for (int i = 0; i < n && i < max; ++i) {
+        cudaError_t err = cudaEventSynchronize(p->ev_stop[mode][i]);
+        if (err == cudaSuccess) err = cudaEventElapsedTime(&ms[i], p->ev_start[mode][i], p->ev_stop[mode][i]);
+        if (err != cudaSuccess) return -fail(MTTKRP_ERR_CUDA, "event timing: %s", cudaGetErrorString(err));
+    }
+    return n;
+}
+
+int64_t mttkrp_plan_launch_count(mttkrp_plan_t h) {
+    Plan* p = as_plan(h);
+    return p ? p->launches : -1;
+}
+
+void mttkrp_plan_destroy(mttkrp_plan_t h) {
+    Plan* p = as_plan(h);
+    if (p == nullptr) return;
+    free_events(*p);
+    delete p;
+}
+
+const char* mttkrp_strerror(int code) {
+    switch (code) {
+        case MTTKRP_OK: return "ok";
+        case MTTKRP_ERR_INVALID: return "invalid argument";
+        case MTTKRP_ERR_UNSUPPORTED: return "unsupported on the requested path";
+        case MTTKRP_ERR_WORKSPACE: return "workspace missing or too small";
+        case MTTKRP_ERR_CUDA: return "CUDA error";
+        case MTTKRP_ERR_HOST_ALLOC: return "host allocation failed";
+        case MTTKRP_ERR_DEVICE: return "device-side error (bounded wait expired)";
+        default: return "unknown error code";
+    }
+}
+
+const char* mttkrp_last_error(void) { return g_errmsg; }
+
+int mttkrp_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,111 @@
+// Internal declarations shared by the host planner and the kernel files of the
+// MTTKRP library.  Nothing here is part of the C ABI (include/mttkrp.h).
+//
+// How a mode k is computed (the matrix-free scheme: the Khatri-Rao product is
+// never formed).  Y is viewed as Y[p, i, q] with i = i_k, p the modes before k
+// and q the modes after k.  The modes other than k are split into
+//   * the inner group: the last few modes after k (when Q = prod_{n>k} I_n is
+//     large enough), or all modes after k plus the last few modes before k;
+//     its combined index j runs over J values;
+//   * the pre modes: every other mode; their combined index is pi (npre values).
+// Then  M_k(i, r) = sum_pi G(pi, r) sum_j Y(pi, i, j) Binner(j, r)  with
+//   G(pi, r)     = prod over pre modes of A_n(i_n(pi), r)          (npre x R table)
+//   Binner(j, r) = prod over inner-group modes of A_n(j_n(j), r)   (J x R table)
+// so every Khatri-Rao row is G(pi, :) * Binner(j, :), built on the fly inside
+// the kernels.  The two tables hold O(R (npre + J)) numbers, not the
+// O(R prod_{n != k} I_n) of the explicit Khatri-Rao matrix.
+//
+// Offsets into Y: element (pi, i, j) sits at base(pi) + i * s_k + off(j) with
+// off(j) = (j / Jq) * IQ + (j % Jq); Jq is the part of the inner group made of
+// modes after k (contiguous in memory) and IQ the stride of mode k-1.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/mttkrp.h"
+
+namespace mk {
+
+constexpr int kMaxD = MTTKRP_MAX_ORDER;
+
+struct ModeGeom {
+    int k;
+    int64_t I;     // rows of the output, I_k
+    int64_t R;
+    int64_t s_k;   // Y stride of mode k
+    int64_t J;     // inner-group size
+    int64_t Jq;    // part of J made of modes after k
+    int64_t IQ;    // Y stride of mode k-1 (used only when J > Jq)
+    int64_t npre;  // number of pre indices pi
+    int ngroup;
+    int group[kMaxD];  // inner-group modes, C order
+    int npm;
+    int pm[kMaxD];     // pre modes, C order
+};
+
+struct ModePlan {
+    ModeGeom g;
+    int path;           // MTTKRP_PATH_SIMT or MTTKRP_PATH_TC
+    int bm, bn;         // output tile (rows x columns)
+    int64_t splits;     // number of contiguous pi ranges (1 = split-free)
+    int64_t pre_per_split;
+    // workspace layout, byte offsets from the workspace base
+    size_t off_partials, off_binner, off_gtab, off_base, total;
+};
+
+struct Plan {
+    int d;
+    int64_t dims[kMaxD];
+    int64_t strides[kMaxD];
+    int64_t R;
+    int forced_path;
+    ModePlan mode[kMaxD];
+    void* ws;
+    size_t ws_bytes;
+    int64_t launches;  // kernels launched so far
+    // benchmark timing: event pairs around the main kernel of each mode
+    int timing;
+    int ev_cap[kMaxD];
+    int ev_n[kMaxD];
+    cudaEvent_t* ev_start[kMaxD];
+    cudaEvent_t* ev_stop[kMaxD];
+};
+
+// Product table: row t of `tab` (R wide) = prod over the nm listed modes of
+// fac[m](idx_m(t), r), idx decoded from t in C order over dim[]; base[t] (if
+// non-null) = sum_m idx_m(t) * ystride[m].  nm = 0 gives rows of ones.
+struct ProdTableArgs {
+    int nm;
+    int64_t dim[kMaxD];
+    int64_t ystride[kMaxD];
+    const float* fac[kMaxD];
+    int64_t rows;
+    int64_t R;
+    float* tab;
+    int64_t* base;
+};
+
+struct SimtArgs {
+    const float* Y;
+    const float* binner;  // J x R
+    const float* gtab;    // npre x R
+    const int64_t* base;  // npre
+    float* dst;           // out (splits == 1) or partials [splits][I][R]
+    int64_t dst_split_stride;
+    int64_t I, R, J, Jq, IQ, s_k, npre, pre_per_split;
+};
+
+// Y loader variants of the SIMT kernel
+enum { kLoadScalar = 0, kLoadVecJ = 1, kLoadVecI = 2 };
+
+cudaError_t launch_prod_table(const ProdTableArgs& a, cudaStream_t s);
+cudaError_t launch_reduce_splits(const float* part, int64_t splits, int64_t n, float* out,
+                                 cudaStream_t s);
+cudaError_t launch_simt(int bm, int bn, int amode, bool bvec, const SimtArgs& a,
+                        int64_t splits, cudaStream_t s);
+bool simt_tile_supported(int bm, int bn);
+
+}  // namespace mk

@@ -1,0 +1,25 @@
+// Tensor-core (tcgen05 / TMEM) path of the MTTKRP library: planner hooks and
+// launcher.  See tc.cu for the kernel.
+#pragma once
+
+#include "internal.h"
+
+namespace mk {
+
+// Bytes of workspace the tensor-core path needs for its pre-split inner table.
+size_t tc_binner_bytes(const ModePlan& mp);
+// Whether the planner should choose the tensor-core path for this mode.
+bool tc_prefer(const ModePlan& mp);
+// Fill tiles and split counts for the tensor-core path; false if unsupported.
+bool tc_plan(ModePlan& mp);
+// Enqueue the tensor-core work of one mode (tables are already built).
+// *nlaunch receives the number of kernels enqueued.  If start_ev is non-null,
+// *start_ev is re-recorded just before the main kernel (after the tensor-core
+// path's own preparation kernels) so that timing covers the main kernel only.
+int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const* factors,
+           const float* gtab, const int64_t* basetab, void* binner_ws, float* dst,
+           cudaStream_t stream, int* nlaunch, cudaEvent_t* start_ev, char* errbuf, size_t errlen);
+// Read and clear the device-side error word (synchronises the device).
+cudaError_t tc_read_and_clear_status(uint32_t* word);
+
+}  // namespace mk

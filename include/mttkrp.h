@@ -1,0 +1,146 @@
+/*
+ * mttkrp.h -- C ABI of the GB300 dense, matrix-free MTTKRP library.
+ *
+ * The operation ("A Performance Portable Matrix Free Dense MTTKRP in GenTen",
+ * abstract and TL;DR): for a d-way dense tensor Y of shape I_0 x ... x I_{d-1},
+ * factor matrices A_n (I_n x R) and a mode k, the matricized tensor times
+ * Khatri-Rao product
+ *
+ *     M_k(i, r) = sum_{(i_n), n != k} Y(i_0, ..., i_{d-1}) * prod_{n != k} A_n(i_n, r),
+ *
+ * i.e. M_k = Y_(k) * (Khatri-Rao product of the A_n, n != k), computed without
+ * ever forming the Khatri-Rao matrix (the matrix-free scheme of that paper,
+ * whose memory grows with R * sum_n I_n instead of R * prod_{n != k} I_n).
+ *
+ * Layouts (all fp32, all device memory, all owned by the caller):
+ *   Y        C-order contiguous (last index fastest), prod_n I_n elements.
+ *   A_n      I_n x R row-major (r fastest).  The factor of the mode being
+ *            computed is not read and may be NULL.
+ *   M_k      I_k x R row-major; overwritten (not accumulated into).
+ *   workspace  caller-allocated device scratch of mttkrp_workspace_bytes()
+ *            bytes, 256-byte aligned; holds split partial sums and small
+ *            factor-product tables.  The library itself never allocates
+ *            device memory.
+ *
+ * Execution: every compute call only enqueues kernels on the given CUDA
+ * stream (a cudaStream_t passed as void*; NULL = the legacy default stream)
+ * and returns without synchronising.  Results are bitwise reproducible from
+ * run to run for a given plan (no atomics; split partial sums are added in a
+ * fixed order in fp64).  A plan and its workspace may be used by one stream
+ * at a time; calls on one plan are not thread-safe.
+ *
+ * Errors: every int-returning call returns MTTKRP_OK (0) or one of the codes
+ * below; nothing is thrown across the ABI.  mttkrp_strerror() names a code and
+ * mttkrp_last_error() gives the calling thread's last detailed message.
+ * Argument errors are detected on the host before anything is enqueued.
+ */
+#ifndef MTTKRP_H_
+#define MTTKRP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MTTKRP_MAX_ORDER 8
+
+enum mttkrp_status {
+    MTTKRP_OK = 0,
+    MTTKRP_ERR_INVALID = 1,     /* bad argument: d, dims, R, mode, NULL, misalignment */
+    MTTKRP_ERR_UNSUPPORTED = 2, /* valid, but not handled by the requested path */
+    MTTKRP_ERR_WORKSPACE = 3,   /* no workspace set, or smaller than required */
+    MTTKRP_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+    MTTKRP_ERR_HOST_ALLOC = 5,  /* host memory for the plan could not be allocated */
+    MTTKRP_ERR_DEVICE = 6       /* a kernel reported a device-side error (bounded wait expired) */
+};
+
+/* Kernel family used for a mode.  AUTO lets the planner choose per mode. */
+enum mttkrp_path {
+    MTTKRP_PATH_AUTO = 0,
+    MTTKRP_PATH_SIMT = 1, /* fp32 FMA on the CUDA cores */
+    MTTKRP_PATH_TC = 2    /* tcgen05 tensor cores, 3xTF32 split, fp32-accurate */
+};
+
+typedef struct mttkrp_plan_s* mttkrp_plan_t;
+
+/*
+ * Create a plan for a d-way tensor (2 <= d <= MTTKRP_MAX_ORDER) with the given
+ * dims (each >= 1, product < 2^40) and rank R (1 <= R <= 65536).  Host-only:
+ * validates, classifies every mode and chooses tiles and split counts; does
+ * not touch the GPU.  *out receives an opaque handle owned by the library.
+ * Returns MTTKRP_ERR_INVALID on bad arguments, MTTKRP_ERR_HOST_ALLOC if the
+ * plan cannot be allocated.
+ */
+int mttkrp_plan(int d, const int64_t* dims, int64_t R, mttkrp_plan_t* out);
+
+/* Force a kernel family for every mode (tests and benchmarks); AUTO restores
+ * the planner's choice.  Returns MTTKRP_ERR_UNSUPPORTED if some mode cannot
+ * run on that path.  Changes the workspace requirement. */
+int mttkrp_plan_set_path(mttkrp_plan_t plan, int path);
+
+/* Device workspace bytes needed by `mode` (0 <= mode < d), or the maximum over
+ * all modes when mode == -1.  Returns 0 for an invalid plan or mode. */
+size_t mttkrp_workspace_bytes(mttkrp_plan_t plan, int mode);
+
+/* Attach caller-owned device scratch (256-byte aligned) of `bytes` bytes.
+ * The plan keeps only the pointer; the caller keeps it alive while calls that
+ * use it may still run on the GPU. */
+int mttkrp_set_workspace(mttkrp_plan_t plan, void* dptr, size_t bytes);
+
+/*
+ * M_k for one mode.  Y: device pointer (16-byte alignment enables vector
+ * loads; any 4-byte alignment works).  factors: HOST array of d device
+ * pointers (factors[mode] is ignored).  out: device pointer to I_mode x R
+ * floats.  stream: cudaStream_t as void*.  Enqueues the work and returns.
+ */
+int mttkrp(mttkrp_plan_t plan, const float* Y, const float* const* factors, int mode,
+           float* out, void* stream);
+
+/* M_k for every mode k = 0..d-1, back to back on one stream; outs is a HOST
+ * array of d device pointers (outs[k] receives I_k x R floats). */
+int mttkrp_all_modes(mttkrp_plan_t plan, const float* Y, const float* const* factors,
+                     float* const* outs, void* stream);
+
+/* Path the plan uses for `mode` (MTTKRP_PATH_SIMT or MTTKRP_PATH_TC), or -1. */
+int mttkrp_plan_mode_path(mttkrp_plan_t plan, int mode);
+
+/* Human-readable planner decisions for `mode` (tiles, split count, inner
+ * group) written into buf (NUL-terminated, truncated to len).  Returns the
+ * length the full text needs, or -1 for an invalid plan or mode. */
+int mttkrp_plan_describe(mttkrp_plan_t plan, int mode, char* buf, size_t len);
+
+/* Kernel timing for benchmarks.  When enabled (enable != 0), every call
+ * records a pair of CUDA events on its stream around the main contraction
+ * kernel of each mode; mttkrp_plan_kernel_times() waits for the recorded
+ * events and copies up to `max` durations (milliseconds, in call order) of
+ * `mode` into ms, returning how many were recorded since the last reset
+ * (enable again to reset).  Events are created by the library (no device
+ * memory is allocated).  Returns a negative value on error. */
+int mttkrp_plan_set_timing(mttkrp_plan_t plan, int enable);
+int mttkrp_plan_kernel_times(mttkrp_plan_t plan, int mode, float* ms, int max);
+
+/* Number of kernels this plan has launched since it was created. */
+int64_t mttkrp_plan_launch_count(mttkrp_plan_t plan);
+
+/* Read and clear the device-side error word that kernels set when a bounded
+ * wait expires (0 = none).  Synchronises the device.  Returns MTTKRP_OK or
+ * MTTKRP_ERR_CUDA; the word is written to *word. */
+int mttkrp_device_status(uint32_t* word);
+
+void mttkrp_plan_destroy(mttkrp_plan_t plan);
+
+const char* mttkrp_strerror(int code);
+
+/* Last detailed error message of the calling thread ("" if none). */
+const char* mttkrp_last_error(void);
+
+/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+int mttkrp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MTTKRP_H_ */

@@ -1,0 +1,147 @@
+"""The C ABI on the host: the library loads, exports every declared symbol, and
+validates arguments before touching the GPU.  No compute call reaches a kernel
+here (every call below fails validation on the host or is host-only)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import dense_tensor_decomposition_gb300 as mk
+import synth
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mk.build()
+    return mk.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = mk.exported_symbols()
+    assert len(names) >= 15
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, f"declared in include/mttkrp.h but not exported: {missing}"
+
+
+def test_version_and_strerror(lib):
+    assert lib.mttkrp_version() >= 100
+    assert lib.mttkrp_strerror(0) == b"ok"
+    for code in range(1, 7):
+        assert lib.mttkrp_strerror(code) not in (b"ok", b"unknown error code")
+    assert lib.mttkrp_strerror(99) == b"unknown error code"
+
+
+def _plan_rc(lib, dims, R):
+    arr = (ctypes.c_int64 * max(1, len(dims)))(*dims)
+    h = ctypes.c_void_p()
+    rc = lib.mttkrp_plan(len(dims), arr, R, ctypes.byref(h))
+    if rc == 0:
+        lib.mttkrp_plan_destroy(h)
+    return rc
+
+
+@pytest.mark.parametrize("dims,R", [((5,), 3), ((2,) * 9, 3), ((4, 0, 3), 2), ((4, -1), 2),
+                                    ((3, 4), 0), ((3, 4), 70000), ((1 << 21, 1 << 21), 4)])
+def test_plan_rejects_invalid(lib, dims, R):
+    assert _plan_rc(lib, dims, R) == 1
+    assert lib.mttkrp_last_error() != b""
+
+
+def test_plan_rejects_null(lib):
+    h = ctypes.c_void_p()
+    assert lib.mttkrp_plan(3, None, 4, ctypes.byref(h)) == 1
+    arr = (ctypes.c_int64 * 3)(2, 3, 4)
+    assert lib.mttkrp_plan(3, arr, 4, None) == 1
+
+
+@pytest.mark.parametrize("dims,R", [((2, 3), 1), ((7, 5, 3), 9), ((1, 1, 1), 1),
+                                    ((3,) * 8, 5), ((1000, 3), 4096)])
+def test_plan_accepts_valid(lib, dims, R):
+    assert _plan_rc(lib, dims, R) == 0
+
+
+def _parse(desc):
+    out = {}
+    for tok in desc.split():
+        k, v = tok.split("=", 1)
+        out[k] = v
+    return out
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+def test_planner_invariants_on_workloads(index):
+    w = synth.workload(index)
+    p = mk.Plan(w.dims, w.R)
+    for k in range(w.d):
+        info = _parse(p.describe(k))
+        group = [int(x) for x in info["inner_group"].strip("[]").split(",") if x]
+        pre = [int(x) for x in info["pre_modes"].strip("[]").split(",") if x]
+        # the modes other than k are split into the inner group and the pre modes
+        assert sorted(group + pre) == [n for n in range(w.d) if n != k]
+        J, npre = int(info["J"]), int(info["npre"])
+        assert J == int(np.prod([w.dims[n] for n in group]))
+        assert npre == int(np.prod([w.dims[n] for n in pre])) if pre else npre == 1
+        assert J * npre * w.dims[k] == w.numel
+        splits, pps = int(info["splits"]), int(info["pre_per_split"])
+        assert splits * pps >= npre and (splits - 1) * pps < npre
+        assert int(info["workspace"]) == p.workspace_bytes(k) > 0
+        assert p.mode_path(k) in ("simt", "tc")
+    assert p.workspace_bytes(-1) == max(p.workspace_bytes(k) for k in range(w.d))
+
+
+def test_compute_calls_validate_before_launch(lib):
+    """Errors that must be reported on the host, before any kernel is enqueued."""
+    p = mk.Plan((6, 5, 4), 3)
+    h = p._h
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: every call fails validation
+    facs = (ctypes.c_void_p * 3)(1 << 20, 1 << 20, 1 << 20)
+    outs = (ctypes.c_void_p * 3)(1 << 20, 1 << 20, 1 << 20)
+    # no workspace attached
+    assert lib.mttkrp(h, fake, facs, 0, fake, None) == 3
+    assert lib.mttkrp_all_modes(h, fake, facs, outs, None) == 3
+    # workspace too small
+    assert lib.mttkrp_set_workspace(h, ctypes.c_void_p(1 << 20), 256) == 0
+    assert lib.mttkrp(h, fake, facs, 1, fake, None) == 3
+    # misaligned workspace
+    assert lib.mttkrp_set_workspace(h, ctypes.c_void_p((1 << 20) + 8), 1 << 30) == 1
+    # mode out of range, NULL pointers
+    assert lib.mttkrp(h, fake, facs, 3, fake, None) == 1
+    assert lib.mttkrp(h, fake, facs, -1, fake, None) == 1
+    assert lib.mttkrp(h, None, facs, 0, fake, None) == 1
+    assert lib.mttkrp(h, fake, None, 0, fake, None) == 1
+    assert lib.mttkrp(h, fake, facs, 0, None, None) == 1
+    assert lib.mttkrp(None, fake, facs, 0, fake, None) == 1
+    nullfacs = (ctypes.c_void_p * 3)(1 << 20, None, 1 << 20)
+    assert lib.mttkrp_set_workspace(h, ctypes.c_void_p(1 << 20), 1 << 40) == 0
+    assert lib.mttkrp(h, fake, nullfacs, 0, fake, None) == 1
+    assert lib.mttkrp_all_modes(h, fake, nullfacs, outs, None) == 1
+    # misaligned Y
+    assert lib.mttkrp(h, ctypes.c_void_p((1 << 20) + 2), facs, 0, fake, None) == 1
+    assert p.launch_count() == 0
+
+
+def test_set_path_and_describe(lib):
+    p = mk.Plan((40, 30, 20), 16)
+    p.set_path("simt")
+    assert all(p.mode_path(k) == "simt" for k in range(3))
+    with pytest.raises(ValueError):
+        p.describe(3)
+    assert lib.mttkrp_plan_set_path(p._h, 7) == 1
+    assert lib.mttkrp_plan_mode_path(p._h, 5) == -1
+    assert lib.mttkrp_workspace_bytes(p._h, 9) == 0
+
+
+def test_timing_queries_without_gpu_work(lib):
+    p = mk.Plan((4, 5, 6), 2)
+    p.set_timing(True)
+    assert p.kernel_times(0) == []
+    assert lib.mttkrp_plan_kernel_times(p._h, 7, None, 0) < 0
+
+
+def test_python_binding_rejects_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    p = mk.Plan((4, 5, 6), 2)
+    Y = torch.zeros(4, 5, 6)
+    A = [torch.zeros(n, 2) for n in (4, 5, 6)]
+    with pytest.raises(TypeError):
+        p.mttkrp(Y, A, 0)

@@ -1,0 +1,253 @@
+"""GPU parity: the CUDA paths against the fp64 oracle on the same seeded inputs.
+
+Every comparison is element by element in relative Frobenius norm,
+||M_gpu - M_oracle||_F / ||M_oracle||_F <= 1e-5 per mode per path (the
+tolerance of the MTTKRP workloads; fp32 inputs, fp32 output).  Full-size
+workloads are compared on sampled output rows that the oracle computes one by
+one, plus (for the two structured workloads) against the closed form
+M_k = B_k (*)_{n != k} (B_n^T A_n) of an exact rank-S tensor at full size.
+All calls go through the C ABI (the ctypes binding).
+"""
+import functools
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from conftest import rel_fro
+
+torch = pytest.importorskip("torch")
+import dense_tensor_decomposition_gb300 as mk  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-5
+
+
+def available_paths():
+    paths = ["simt"]
+    try:
+        p = mk.Plan((64, 64, 64), 64)
+        p.set_path("tc")
+        paths.append("tc")
+    except mk.MttkrpError:
+        pass
+    return paths
+
+
+PATHS = available_paths() if torch.cuda.is_available() else ["simt"]
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def gpu_modes(Y, A, path, modes=None, plan=None):
+    Yd = dev(Y)
+    Ad = [dev(a) for a in A]
+    if plan is None:
+        plan = mk.Plan(Y.shape, A[0].shape[1], path)
+    modes = range(Y.ndim) if modes is None else modes
+    outs = {k: plan.mttkrp(Yd, Ad, k).cpu().numpy() for k in modes}
+    torch.cuda.synchronize()
+    return outs
+
+
+def sample_rows(I, seed, n=8):
+    rng = np.random.default_rng(seed)
+    rows = {0, I - 1, I // 2}
+    rows.update(int(x) for x in rng.integers(0, I, size=n))
+    return sorted(rows)
+
+
+@functools.lru_cache(maxsize=1)
+def workload_inputs(index, noise=True):
+    w = synth.workload(index)
+    return w, synth.make_tensor(w, noise=noise), synth.make_factors(w)
+
+
+# ---------------------------------------------------------------------------
+# the five workloads, every mode, every path
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+def test_workload_parity(index, path):
+    w, Y, A = workload_inputs(index)
+    got = gpu_modes(Y, A, path)
+    for k in range(w.d):
+        if w.numel <= 1 << 24:
+            ref = oracle.mttkrp(Y, A, k)
+            err = rel_fro(got[k], ref)
+        else:
+            rows = sample_rows(w.dims[k], seed=k)
+            ref = oracle.mttkrp(Y, A, k, rows=rows)
+            err = rel_fro(got[k][rows], ref)
+        assert err <= TOL, f"{w.name} mode {k} path {path}: rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("index", [2, 4])
+def test_closed_form_full_size(index, path):
+    """Noise-free structured workloads are exact rank-S tensors: full-size check."""
+    w, Y, A = workload_inputs(index, noise=False)
+    B = synth.generating_factors(w)
+    got = gpu_modes(Y, A, path)
+    for k in range(w.d):
+        H = np.ones((B[0].shape[1], w.R))
+        for n in range(w.d):
+            if n != k:
+                H *= B[n].T @ A[n].astype(np.float64)
+        ref = B[k] @ H
+        err = rel_fro(got[k], ref)
+        assert err <= TOL, f"{w.name} (noise-free) mode {k} path {path}: {err:.3e}"
+
+
+# ---------------------------------------------------------------------------
+# shapes with tails in every dimension and the degenerate cases
+# ---------------------------------------------------------------------------
+
+EDGE = [
+    ((2, 3), 1),
+    ((1, 1, 1), 1),
+    ((37, 41), 257),
+    ((5, 7, 9, 11), 13),
+    ((3,) * 8, 5),
+    ((130, 3, 65), 130),
+    ((1000, 2), 3),
+    ((2, 1000), 4),
+    ((64, 64, 64), 4),
+    ((20, 20, 20, 20), 128),
+    ((33, 17, 129), 64),
+    ((128, 1, 128), 32),
+    ((8, 200, 6), 200),
+    ((129, 129, 7), 129),
+]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dims,R", EDGE)
+def test_edge_shapes(dims, R, path):
+    Y, A = synth.random_case(300 + sum(dims) + R, dims, R)
+    try:
+        got = gpu_modes(Y, A, path)
+    except mk.MttkrpError as e:
+        if e.code == 2 and path != "simt":
+            pytest.skip(f"{path} does not take {dims}")
+        raise
+    for k in range(len(dims)):
+        err = rel_fro(got[k], oracle.mttkrp(Y, A, k))
+        assert err <= TOL, f"{dims} R={R} mode {k} path {path}: {err:.3e}"
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_mode_permutation_invariance(path):
+    dims, R = (7, 12, 33, 5), 37
+    Y, A = synth.random_case(41, dims, R)
+    base = gpu_modes(Y, A, path)
+    perm = [2, 0, 3, 1]
+    Yp = np.ascontiguousarray(np.transpose(Y, perm))
+    Ap = [A[p] for p in perm]
+    got = gpu_modes(Yp, Ap, path)
+    for t in range(4):
+        assert rel_fro(got[t], base[perm[t]]) <= TOL
+
+
+def test_order_two_is_matrix_product():
+    Y, A = synth.random_case(42, (300, 200), 48)
+    for path in PATHS:
+        got = gpu_modes(Y, A, path)
+        Y64 = Y.astype(np.float64)
+        assert rel_fro(got[0], Y64 @ A[1].astype(np.float64)) <= TOL
+        assert rel_fro(got[1], Y64.T @ A[0].astype(np.float64)) <= TOL
+
+
+# ---------------------------------------------------------------------------
+# pointers, buffers, determinism, errors
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("path", PATHS)
+def test_misaligned_inputs_take_scalar_loads(path):
+    dims, R = (24, 16, 32), 20
+    Y, A = synth.random_case(43, dims, R)
+    ybuf = torch.zeros(Y.size + 1, device="cuda")
+    ybuf[1:] = dev(Y.ravel())
+    Yd = ybuf[1:].view(dims)  # 4-byte but not 16-byte aligned
+    abufs = []
+    Ad = []
+    for a in A:
+        buf = torch.zeros(a.size + 1, device="cuda")
+        buf[1:] = dev(a.ravel())
+        abufs.append(buf)
+        Ad.append(buf[1:].view(a.shape))
+    plan = mk.Plan(dims, R, path)
+    for k in range(3):
+        out = plan.mttkrp(Yd, Ad, k).cpu().numpy()
+        assert rel_fro(out, oracle.mttkrp(Y, A, k)) <= TOL
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_output_guard_bands(path):
+    dims, R = (45, 30, 33), 19
+    Y, A = synth.random_case(44, dims, R)
+    Yd, Ad = dev(Y), [dev(a) for a in A]
+    plan = mk.Plan(dims, R, path)
+    for k in range(3):
+        n = dims[k] * R
+        buf = torch.full((n + 2048,), float("nan"), device="cuda")
+        out = buf[1024:1024 + n].view(dims[k], R)
+        plan.mttkrp(Yd, Ad, k, out=out)
+        torch.cuda.synchronize()
+        assert torch.isnan(buf[:1024]).all() and torch.isnan(buf[1024 + n:]).all()
+        assert rel_fro(out.cpu().numpy(), oracle.mttkrp(Y, A, k)) <= TOL
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bitwise_deterministic(path):
+    w, Y, A = workload_inputs(2)
+    Yd, Ad = dev(Y), [dev(a) for a in A]
+    plan = mk.Plan(w.dims, w.R, path)
+    a = [o.clone() for o in plan.all_modes(Yd, Ad)]
+    b = plan.all_modes(Yd, Ad)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_all_modes_matches_single_calls(path):
+    dims, R = (31, 22, 17, 9), 40
+    Y, A = synth.random_case(45, dims, R)
+    Yd, Ad = dev(Y), [dev(a) for a in A]
+    plan = mk.Plan(dims, R, path)
+    allm = [o.clone() for o in plan.all_modes(Yd, Ad)]
+    for k in range(4):
+        assert torch.equal(allm[k], plan.mttkrp(Yd, Ad, k))
+
+
+def test_undersized_workspace_is_an_error():
+    dims, R = (64, 48, 40), 32
+    Y, A = synth.random_case(46, dims, R)
+    Yd, Ad = dev(Y), [dev(a) for a in A]
+    plan = mk.Plan(dims, R)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    plan.set_workspace_ptr(small.data_ptr(), 256)
+    with pytest.raises(mk.MttkrpError) as e:
+        plan.mttkrp(Yd, Ad, 0)
+    assert e.value.code == 3
+    assert plan.launch_count() == 0
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_timing_events_and_launch_count(path):
+    dims, R = (96, 80, 64), 64
+    Y, A = synth.random_case(47, dims, R)
+    Yd, Ad = dev(Y), [dev(a) for a in A]
+    plan = mk.Plan(dims, R, path)
+    plan.set_timing(True)
+    plan.all_modes(Yd, Ad)
+    plan.all_modes(Yd, Ad)
+    for k in range(3):
+        t = plan.kernel_times(k)
+        assert len(t) == 2 and all(x > 0 for x in t)
+    assert plan.launch_count() >= 2 * 3 * 2
+    assert mk.device_status() == 0
