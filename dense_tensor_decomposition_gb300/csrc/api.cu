@@ -504,3 +504,92 @@ const char* mttkrp_last_error(void) { return g_errmsg; }
 int mttkrp_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point (mttkrp_noalloc).
+//
+// Some callers cannot call cudaMalloc: a library embedded in a host program
+// whose own allocator reserves and hands out all device memory (a framework's
+// caching allocator, an inference server's arena) and forbids foreign
+// allocations, or code on a latency-critical path where cudaMalloc/cudaFree,
+// which can block until the device is idle, are not acceptable.  For them the
+// scratch that the SIMT path needs (split partial sums, factor-product
+// tables) lives in one fixed, file-scope device array instead of a
+// caller-provided workspace.  The array is part of the library image: every
+// GPU that loads the library holds it until the process exits.
+// ---------------------------------------------------------------------------
+
+#include <mutex>
+
+namespace mk {
+
+static __device__ __align__(256) unsigned char g_static_scratch[MTTKRP_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device.  The host-side
+// name of the array is only a stand-in, never a device address, so the address
+// is looked up once per device (with that device current) and cached.
+cudaError_t static_scratch_address(void** out) {
+    int dev = -1;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (err != cudaSuccess) return err;
+        g_static_ptr[dev] = p;
+    }
+    *out = g_static_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace mk
+
+extern "C" int mttkrp_noalloc(int d, const int64_t* dims, int64_t R, const float* Y,
+                              const float* const* factors, int mode, float* out, void* stream) {
+    g_errmsg[0] = 0;
+    if (d < 2 || d > kMaxD) return fail(MTTKRP_ERR_INVALID, "order d=%d outside [2, %d]", d, kMaxD);
+    if (dims == nullptr || Y == nullptr || factors == nullptr || out == nullptr)
+        return fail(MTTKRP_ERR_INVALID, "NULL dims, tensor, factor array or output");
+    if (R < 1 || R > kMaxR) return fail(MTTKRP_ERR_INVALID, "rank R=%lld outside [1, %lld]", (long long)R, (long long)kMaxR);
+    if (mode < 0 || mode >= d) return fail(MTTKRP_ERR_INVALID, "mode %d outside [0, %d)", mode, d);
+    int64_t numel = 1;
+    for (int n = 0; n < d; ++n) {
+        if (dims[n] < 1) return fail(MTTKRP_ERR_INVALID, "dims[%d]=%lld < 1", n, (long long)dims[n]);
+        if (dims[n] > kMaxNumel || numel > kMaxNumel / dims[n])
+            return fail(MTTKRP_ERR_INVALID, "tensor has more than 2^40 elements");
+        numel *= dims[n];
+    }
+    // the plan lives on the stack: nothing is allocated, on the host or the GPU
+    Plan p;
+    memset(&p, 0, sizeof(p));
+    p.d = d;
+    p.R = R;
+    for (int n = 0; n < d; ++n) p.dims[n] = dims[n];
+    p.strides[d - 1] = 1;
+    for (int n = d - 2; n >= 0; --n) p.strides[n] = p.strides[n + 1] * p.dims[n + 1];
+    p.forced_path = MTTKRP_PATH_SIMT;
+    int rc = plan_mode(p, mode, MTTKRP_PATH_SIMT);
+    if (rc != MTTKRP_OK) return fail(rc, "mode %d cannot be planned on the SIMT path", mode);
+    const size_t need = p.mode[mode].total;
+    if (need > (size_t)MTTKRP_NOALLOC_SCRATCH_BYTES)
+        return fail(MTTKRP_ERR_WORKSPACE,
+                    "mttkrp_noalloc: this problem needs %zu bytes of scratch, more than the "
+                    "%zu-byte static scratch; use mttkrp() with a workspace instead",
+                    need, (size_t)MTTKRP_NOALLOC_SCRATCH_BYTES);
+    void* scratch = nullptr;
+    cudaError_t err = static_scratch_address(&scratch);
+    if (err != cudaSuccess)
+        return fail(MTTKRP_ERR_CUDA, "static scratch address: %s", cudaGetErrorString(err));
+    p.ws = scratch;
+    p.ws_bytes = MTTKRP_NOALLOC_SCRATCH_BYTES;
+    return run_mode(p, Y, factors, mode, out, static_cast<cudaStream_t>(stream));
+}

@@ -136,6 +136,33 @@ const char* mttkrp_strerror(int code);
 /* Last detailed error message of the calling thread ("" if none). */
 const char* mttkrp_last_error(void);
 
+/*
+ * Allocation-free MTTKRP of one mode.  (No counterpart in the paper: this is a
+ * deployment convenience of this library.)
+ *
+ * For callers that must not allocate device memory: a library embedded in a
+ * program whose own allocator owns all of the GPU's memory and forbids other
+ * allocations, or code on a latency-critical path where cudaMalloc/cudaFree,
+ * which can block until the device is idle, are not acceptable.  Same result
+ * as mttkrp() on the SIMT (CUDA-core) path, for the same d, dims, R, Y,
+ * factors (HOST array of device pointers), mode, out and stream; no plan or
+ * workspace is needed and nothing is allocated, on the host or the GPU.
+ *
+ * The scratch it needs lives in one static device array of
+ * MTTKRP_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
+ * loads the library holds until the process exits.  Problems whose scratch
+ * would be larger (those with large split partial sums, e.g. a 128^4 tensor at
+ * rank 256) are rejected with MTTKRP_ERR_WORKSPACE and a message, before any
+ * work is enqueued.  The first call on a device looks up the array's device
+ * address; make that first call before any stream capture.  Every call shares
+ * the one array and leaves its contents behind; each call writes all the
+ * scratch it reads, so nothing needs clearing, but calls that overlap on the
+ * GPU (other streams or host threads at the same time) race on it.
+ */
+#define MTTKRP_NOALLOC_SCRATCH_BYTES (32u << 20)
+int mttkrp_noalloc(int d, const int64_t* dims, int64_t R, const float* Y,
+                   const float* const* factors, int mode, float* out, void* stream);
+
 /* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
 int mttkrp_version(void);
 
