@@ -98,6 +98,22 @@ def recorded_traffic(workload, path, src_hash):
     return None
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over all ranks (x itself without torch.distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(flops_per_rank_step: float, world: int, ms_per_step_max: float) -> float:
+    """Whole-job GFLOP/s: every rank's work over the slowest rank's step time."""
+    return world * flops_per_rank_step / (ms_per_step_max * 1e-3) / 1e9
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples taken while the timed region runs."""
 
@@ -288,14 +304,10 @@ def run_ours(args, w):
     kern = [t for k in range(w.d) for t in plan.kernel_times(k)]
     plan.set_timing(False)
 
-    ms_max = ms_total
-    if world > 1:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms_total, device)
     ms_per_step = ms_max / args.steps
     flops_step = w.d * w.flops_per_mode()
-    value = world * flops_step / (ms_per_step * 1e-3) / 1e9
+    value = aggregate_throughput(flops_step, world, ms_per_step)
 
     # ---- end to end through the public API, from pinned host memory ----
     Yh = torch.from_numpy(Y).pin_memory()
@@ -313,12 +325,8 @@ def run_ours(args, w):
         plan.all_modes_from_host(Yh, Ah, (Yd, Ad, Md), Mh)
     e1.record(stream)
     torch.cuda.synchronize(device)
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * flops_step / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, device)
+    e2e_value = aggregate_throughput(flops_step, world, e2e_ms)
     checksum = float(sum(float(m.double().abs().sum()) for m in Mh))
 
     if rank != 0:

@@ -123,15 +123,26 @@ int plan_mode(Plan& p, int k, int path) {
     ModePlan& mp = p.mode[k];
     memset(&mp, 0, sizeof(mp));
     classify(p, k, mp.g);
-    if (path == MTTKRP_PATH_AUTO) path = tc_prefer(mp) ? MTTKRP_PATH_TC : MTTKRP_PATH_SIMT;
-    if (path == MTTKRP_PATH_TC) {
-        if (!tc_plan(mp)) return MTTKRP_ERR_UNSUPPORTED;
-    } else {
-        plan_simt(mp);
-        // row tiles run along gridDim.y (at most 65535)
-        if (cdiv(mp.g.I, mp.bm) > 65535) return MTTKRP_ERR_UNSUPPORTED;
+    if (path == MTTKRP_PATH_AUTO) {
+        path = MTTKRP_PATH_SIMT;
+        if (tc_prefer(mp)) {
+            ModePlan trial = mp;
+            if (tc_plan(p, trial)) path = MTTKRP_PATH_TC;
+        }
     }
-    layout_workspace(mp);
+    ModePlan& alt = p.simt_alt[k];
+    alt = mp;
+    plan_simt(alt);
+    layout_workspace(alt);
+    const bool simt_ok = cdiv(alt.g.I, alt.bm) <= 65535;  // row tiles run along gridDim.y
+    if (path == MTTKRP_PATH_TC) {
+        if (!tc_plan(p, mp)) return MTTKRP_ERR_UNSUPPORTED;
+        layout_workspace(mp);
+        if (simt_ok && alt.total > mp.total) mp.total = alt.total;
+    } else {
+        if (!simt_ok) return MTTKRP_ERR_UNSUPPORTED;
+        mp = alt;
+    }
     return MTTKRP_OK;
 }
 
@@ -183,14 +194,15 @@ void free_events(Plan& p) {
 
 int run_mode(Plan& p, const float* Y, const float* const* factors, int k, float* out,
              cudaStream_t stream) {
-    ModePlan& mp = p.mode[k];
+    const ModePlan& mp = (p.mode[k].path == MTTKRP_PATH_TC && !aligned16(Y)) ? p.simt_alt[k]
+                                                                               : p.mode[k];
     const ModeGeom& g = mp.g;
     if (p.ws == nullptr && mp.total > 0)
         return fail(MTTKRP_ERR_WORKSPACE, "no workspace attached (mode %d needs %zu bytes)", k,
                     mp.total);
-    if (p.ws_bytes < mp.total)
+    if (p.ws_bytes < p.mode[k].total)
         return fail(MTTKRP_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes mode %d needs",
-                    p.ws_bytes, mp.total, k);
+                    p.ws_bytes, p.mode[k].total, k);
     for (int n = 0; n < p.d; ++n)
         if (n != k && factors[n] == nullptr)
             return fail(MTTKRP_ERR_INVALID, "factor %d is NULL", n);
@@ -435,10 +447,10 @@ int mttkrp_plan_describe(mttkrp_plan_t h, int mode, char* buf, size_t len) {
     char tmp[512];
     int n = snprintf(tmp, sizeof(tmp),
                      "mode=%d path=%s tile=%dx%d inner_group=[%s] J=%lld Jq=%lld pre_modes=[%s] "
-                     "npre=%lld splits=%lld pre_per_split=%lld workspace=%zu",
+                     "npre=%lld splits=%lld pre_per_split=%lld workspace=%zu tc_ksteps=%d tc_inner=%d",
                      mode, mp.path == MTTKRP_PATH_TC ? "tc" : "simt", mp.bm, mp.bn, groups,
                      (long long)g.J, (long long)g.Jq, pres, (long long)g.npre,
-                     (long long)mp.splits, (long long)mp.pre_per_split, mp.total);
+                     (long long)mp.splits, (long long)mp.pre_per_split, mp.total, mp.tc_ks, mp.tc_inner);
     if (buf != nullptr && len > 0) {
         strncpy(buf, tmp, len - 1);
         buf[len - 1] = 0;

@@ -52,6 +52,10 @@ struct ModePlan {
     int bm, bn;         // output tile (rows x columns)
     int64_t splits;     // number of contiguous pi ranges (1 = split-free)
     int64_t pre_per_split;
+    // tensor-core path only
+    int tc_inner;       // 1: mode with stride 1 (Y tile arrives i-major and is transposed)
+    int tc_ks;          // K-steps of 16 contraction indices per pi
+    int tc_jq_steps;    // K-steps per value of the p-side part of the inner group
     // workspace layout, byte offsets from the workspace base
     size_t off_partials, off_binner, off_gtab, off_base, total;
 };
@@ -63,6 +67,10 @@ struct Plan {
     int64_t R;
     int forced_path;
     ModePlan mode[kMaxD];
+    // SIMT plan of every mode, used when a tensor-core mode is called with a
+    // Y pointer that the tensor-memory accelerator cannot address (not 16-byte
+    // aligned); its workspace need is included in mode[k].total
+    ModePlan simt_alt[kMaxD];
     void* ws;
     size_t ws_bytes;
     int64_t launches;  // kernels launched so far

@@ -1,5 +1,31 @@
-// Tensor-core (tcgen05 / TMEM) MTTKRP path.
+// Tensor-core (tcgen05 / TMEM) MTTKRP path: fp32-accurate 3xTF32 on the
+// 5th-generation tensor cores of sm_103a.
+//
+// Per CTA: a 128 x BN tile of M_k (rows i, columns r) and a contiguous range of
+// pre indices pi.  For every pi the contraction over the inner-group index j
+// runs in K-steps of 16:
+//   * a TMA tensor copy brings the 128 x 16 tile of Y_(k) into shared memory
+//     (K-major, 64-byte swizzle; for the innermost mode it arrives i-major and
+//     is transposed by the producer warps);
+//   * one bulk copy brings the matching pre-swizzled BN x 16 tile of the inner
+//     Khatri-Rao table, as a "hi" and a "lo" image written by the prep kernel;
+//   * two producer warps write lo(y) = y - tf32(y) next to the raw tile;
+//   * one thread issues, per 8-wide k-slice, the three products
+//     hi*hi + hi*lo + lo*hi with tcgen05.mma.kind::tf32 into a TMEM accumulator.
+// The tensor cores read fp32 operands as tf32 by truncation, so the raw fp32
+// tile serves as its own "hi" part.  TMEM accumulation rounds toward zero, so
+// after at most 8 K-steps (128 indices, 48 MMAs) the accumulator is drained:
+// eight epilogue warps read it with tcgen05.ld and add G(pi, r) * z into fp32
+// registers (round to nearest), while the MMAs continue into the second TMEM
+// buffer.  At the end each thread writes its row segment of the tile (or of
+// its split's partial).  Every wait on an mbarrier is bounded in time; on
+// expiry the kernel records an error word, stops issuing work, waits (bounded)
+// for its own copies and MMAs and frees its TMEM before returning.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstdio>
+#include <cstring>
 
 #include "tc.h"
 
@@ -9,18 +35,887 @@ namespace mk {
 // through mttkrp_device_status).
 __device__ uint32_t g_device_status = 0;
 
-size_t tc_binner_bytes(const ModePlan&) { return 0; }
+namespace {
 
-bool tc_prefer(const ModePlan&) { return false; }
+constexpr int kBM = 128;
+constexpr int kBK = 16;           // contraction indices per K-step (64-byte rows)
+constexpr int kChunkSteps = 8;    // K-steps accumulated in TMEM between drains
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (4 + kEpiWarps) * 32;
 
-bool tc_plan(ModePlan&) { return false; }
+constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s bound on every wait
+constexpr uint32_t kTf32Mask = 0xFFFFE000u;
 
-int tc_run(const Plan&, const ModePlan&, const float*, const float* const*, const float*,
-           const int64_t*, void*, float*, cudaStream_t, int* nlaunch, cudaEvent_t*, char* errbuf,
-           size_t errlen) {
+// status codes (bit flags)
+constexpr uint32_t kStatusTimeoutTma = 1u << 0;
+constexpr uint32_t kStatusTimeoutLo = 1u << 1;
+constexpr uint32_t kStatusTimeoutMma = 1u << 2;
+constexpr uint32_t kStatusTimeoutEpi = 1u << 3;
+constexpr uint32_t kStatusTimeoutDrain = 1u << 4;
+
+enum Role { kRoleJq = 0, kRoleI = 1, kRoleJp = 2, kRolePP = 3, kRolePQ = 4, kRoles = 5 };
+
+struct TcArgs {
+    CUtensorMap ymap;
+    int rank;                 // tensor-map rank (2..5)
+    int slot[kRoles];         // coordinate slot of each role, -1 if absent
+    const float* bimg;        // B images [n-tile][K-step][hi|lo][BN rows x 64 B]
+    const float* gtab;        // npre x R
+    float* dst;
+    int64_t dst_split_stride;
+    int64_t I, R;
+    int64_t npre, pre_per_split;
+    int64_t nQ;               // size of the merged q-side pre dimension
+    int KS;                   // K-steps per pi
+    int jq_steps;             // K-steps per value of jp (K-contiguous variant)
+    uint32_t* status;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok;
+}
+
+// Wait for the phase of `bar` with the given parity.  Returns false if the CTA
+// was aborted or the wait exceeded kWaitNs (then the CTA is aborted and `code`
+// is recorded in the status word).
+__device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* status, uint32_t code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = gtimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (gtimer() - t0 > kWaitNs) {
+            *abort_flag = 1;
+            atomicOr(status, code);
+            return false;
+        }
+    }
+}
+
+// Like wait_bounded but ignores the abort flag (used to drain in-flight work).
+__device__ __noinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint32_t* status) {
+    const unsigned long long t0 = gtimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (gtimer() - t0 > kWaitNs) {
+            atomicOr(status, kStatusTimeoutDrain);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load(const CUtensorMap* map, int rank, const int* c, void* dst,
+                                         uint64_t* bar) {
+    const uint64_t m = reinterpret_cast<uint64_t>(map);
+    const uint32_t d = smem_u32(dst), b = smem_u32(bar);
+    switch (rank) {
+        case 2:
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                " [%0], [%1, {%2, %3}], [%4];" ::"r"(d),
+                "l"(m), "r"(c[0]), "r"(c[1]), "r"(b)
+                : "memory");
+            break;
+        case 3:
+            asm volatile(
+                "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(d),
+                "l"(m), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(b)
+                : "memory");
+            break;
+        case 4:
+            asm volatile(
+                "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(d),
+                "l"(m), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(b)
+                : "memory");
+            break;
+        default:
+            asm volatile(
+                "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(d),
+                "l"(m), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(b)
+                : "memory");
+            break;
+    }
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// K-major, 64-byte swizzle shared-memory matrix descriptor: 8-row groups of
+// 64-byte rows, 512 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(512 >> 4) << 32;   // stride byte offset: 8 rows x 64 B
+    d |= (uint64_t)1 << 46;            // descriptor version
+    d |= (uint64_t)4 << 61;            // 64-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float tf32_lo(float x) {
+    return x - __uint_as_float(__float_as_uint(x) & kTf32Mask);
+}
+
+// byte offset of (row, k) in a K-major 64-byte-swizzled tile (16 fp32 per row)
+__device__ __forceinline__ uint32_t sw64_off(uint32_t row, uint32_t chunk) {
+    return row * 64u + (((chunk ^ (row >> 1)) & 3u) << 4);
+}
+
+// ---------------------------------------------------------------------------
+// Main kernel
+// ---------------------------------------------------------------------------
+
+template <int BN, bool INNER>
+struct Smem {
+    static constexpr uint32_t kY = kBM * kBK * 4;      // 8 KB: raw Y tile (hi, or staging if INNER)
+    static constexpr uint32_t kA = kBM * kBK * 4;      // 8 KB
+    static constexpr uint32_t kB = BN * kBK * 4;       // BN x 64 B
+    static constexpr uint32_t kStage = kY + kA + (INNER ? kA : 0) + 2 * kB;
+    static constexpr uint32_t kBarBytes = 256;
+    static constexpr uint32_t kTotal = 1024 + kStages * kStage + kBarBytes;
+};
+
+template <int BN, bool INNER>
+__global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_constant__ TcArgs a) {
+    using L = Smem<BN, INNER>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~(uintptr_t)1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * L::kStage);
+    uint64_t* tma_full = bars;                 // [kStages]
+    uint64_t* lo_full = bars + kStages;        // [kStages]
+    uint64_t* empty = bars + 2 * kStages;      // [kStages]
+    uint64_t* zfull = bars + 3 * kStages;      // [2]
+    uint64_t* zempty = zfull + 2;              // [2]
+    uint64_t* mma_done = zempty + 2;           // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int64_t m0 = (int64_t)blockIdx.y * kBM;
+    const int64_t r0 = (int64_t)blockIdx.x * BN;
+    const int64_t pre_lo = (int64_t)blockIdx.z * a.pre_per_split;
+    int64_t pre_hi = pre_lo + a.pre_per_split;
+    if (pre_hi > a.npre) pre_hi = a.npre;
+    const int64_t npi = pre_hi > pre_lo ? pre_hi - pre_lo : 0;
+    const int KS = a.KS;
+    const int64_t T = npi * KS;                          // K-steps of this CTA
+    const int cpp = (KS + kChunkSteps - 1) / kChunkSteps;  // drain chunks per pi
+    const int64_t nchunks = npi * cpp;
+    constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : 2 * BN;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&tma_full[s], 1);
+            mbar_init(&lo_full[s], 2);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&zfull[b], 1);
+            mbar_init(&zempty[b], kEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // K-step t -> (pi, coordinates)
+    auto step_coords = [&](int64_t t, int* c, int64_t* pi_out) {
+        const int64_t pi = pre_lo + t / KS;
+        const int ks = (int)(t % KS);
+        int role[kRoles];
+        if (INNER) {
+            role[kRoleJq] = ks * kBK;  // j (the contraction index) runs along dim "Jq" slot
+            role[kRoleJp] = 0;
+        } else {
+            const int jp = ks / a.jq_steps;
+            role[kRoleJq] = (ks - jp * a.jq_steps) * kBK;
+            role[kRoleJp] = jp;
+        }
+        role[kRoleI] = (int)m0;
+        role[kRolePP] = (int)(pi / a.nQ);
+        role[kRolePQ] = (int)(pi % a.nQ);
+        for (int q = 0; q < kRoles; ++q)
+            if (a.slot[q] >= 0) c[a.slot[q]] = role[q];
+        *pi_out = pi;
+    };
+
+    if (warp == 0) {
+        // ------------------------- TMA producer -------------------------
+        if (lane == 0) {
+            const uint32_t bytes = L::kY + 2 * L::kB;
+            const uint8_t* bimg = reinterpret_cast<const uint8_t*>(a.bimg);
+            int64_t issued = 0;
+            for (int64_t t = 0; t < T; ++t) {
+                const int s = (int)(t % kStages);
+                const int64_t round = t / kStages;
+                if (round > 0 &&
+                    !wait_bounded(&empty[s], (uint32_t)((round - 1) & 1), abort_flag, a.status,
+                                  kStatusTimeoutTma))
+                    break;
+                uint8_t* st = smem + s * L::kStage;
+                int c[5] = {0, 0, 0, 0, 0};
+                int64_t pi;
+                step_coords(t, c, &pi);
+                const int ks = (int)(t % KS);
+                mbar_arrive_expect_tx(&tma_full[s], bytes);
+                tma_load(&a.ymap, a.rank, c, st, &tma_full[s]);
+                const uint8_t* src =
+                    bimg + ((int64_t)blockIdx.x * KS + ks) * (int64_t)(2 * L::kB);
+                bulk_load(st + L::kY + L::kA + (INNER ? L::kA : 0), src, 2 * L::kB, &tma_full[s]);
+                issued = t + 1;
+            }
+            // wait (bounded) for copies still in flight before leaving
+            for (int64_t t = issued - 1; t >= 0 && t >= issued - kStages; --t)
+                wait_drain(&tma_full[t % kStages], (uint32_t)((t / kStages) & 1), a.status);
+        }
+    } else if (warp == 1) {
+        // ------------------------- MMA issuer -------------------------
+        if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
+                                   ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+            int64_t chunk = -1;
+            bool ok = true;
+            for (int64_t t = 0; t < T && ok; ++t) {
+                const int s = (int)(t % kStages);
+                const int64_t round = t / kStages;
+                const int ks = (int)(t % KS);
+                const bool first = (ks % kChunkSteps) == 0;
+                const bool last = ((ks % kChunkSteps) == kChunkSteps - 1) || (ks == KS - 1);
+                if (first) {
+                    ++chunk;
+                    const int64_t use = chunk >> 1;
+                    if (use > 0 && !wait_bounded(&zempty[chunk & 1], (uint32_t)((use - 1) & 1),
+                                                 abort_flag, a.status, kStatusTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                if (!wait_bounded(&tma_full[s], (uint32_t)(round & 1), abort_flag, a.status,
+                                  kStatusTimeoutMma) ||
+                    !wait_bounded(&lo_full[s], (uint32_t)(round & 1), abort_flag, a.status,
+                                  kStatusTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint8_t* st = smem + s * L::kStage;
+                const uint8_t* a_hi = INNER ? st + L::kY : st;
+                const uint8_t* a_lo = a_hi + L::kA;
+                const uint8_t* b_hi = st + L::kY + L::kA + (INNER ? L::kA : 0);
+                const uint8_t* b_lo = b_hi + L::kB;
+                const uint64_t dah = sdesc_sw64(smem_u32(a_hi));
+                const uint64_t dal = sdesc_sw64(smem_u32(a_lo));
+                const uint64_t dbh = sdesc_sw64(smem_u32(b_hi));
+                const uint64_t dbl = sdesc_sw64(smem_u32(b_lo));
+                const uint32_t dz = tmem + (uint32_t)((chunk & 1) * BN);
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const uint64_t adv = (uint64_t)((kk * 32) >> 4);  // 8 tf32 = 32 bytes
+                    mma_tf32(dz, dah + adv, dbh + adv, idesc, (first && kk == 0) ? 0u : 1u);
+                    mma_tf32(dz, dah + adv, dbl + adv, idesc, 1u);
+                    mma_tf32(dz, dal + adv, dbh + adv, idesc, 1u);
+                }
+                mma_commit(&empty[s]);
+                if (last) mma_commit(&zfull[chunk & 1]);
+            }
+            // all MMAs issued by this thread are complete before TMEM is freed
+            mma_commit(mma_done);
+            wait_drain(mma_done, 0, a.status);
+        }
+    } else if (warp < 4) {
+        // ---------------------- lo producers (64 threads) ----------------------
+        const int ptid = tid - 64;
+        for (int64_t t = 0; t < T; ++t) {
+            const int s = (int)(t % kStages);
+            const int64_t round = t / kStages;
+            if (!wait_bounded(&tma_full[s], (uint32_t)(round & 1), abort_flag, a.status,
+                              kStatusTimeoutLo))
+                break;
+            uint8_t* st = smem + s * L::kStage;
+            if (!INNER) {
+                // lo tile, elementwise at the same (swizzled) offsets as the raw tile
+                const float4* src = reinterpret_cast<const float4*>(st);
+                float4* dst = reinterpret_cast<float4*>(st + L::kY);
+#pragma unroll
+                for (int v = 0; v < (int)(L::kY / 16) / 64; ++v) {
+                    const int e = ptid + 64 * v;
+                    const float4 x = src[e];
+                    dst[e] = make_float4(tf32_lo(x.x), tf32_lo(x.y), tf32_lo(x.z), tf32_lo(x.w));
+                }
+            } else {
+                // staging tile is [16 j][128 i] (i contiguous): transpose into the
+                // K-major hi and lo tiles, 4 x 4 blocks per thread
+                const float* stg = reinterpret_cast<const float*>(st);
+                uint8_t* hi = st + L::kY;
+                uint8_t* lo = hi + L::kA;
+#pragma unroll
+                for (int v = 0; v < 2; ++v) {
+                    const int blk = ptid + 64 * v;   // 128 blocks: 32 i-blocks x 4 j-chunks
+                    const int jc = blk & 3;
+                    const int ib = blk >> 2;
+                    float4 col[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        col[q] = *reinterpret_cast<const float4*>(stg + (4 * jc + q) * kBM + 4 * ib);
+                    const float rows[4][4] = {{col[0].x, col[1].x, col[2].x, col[3].x},
+                                              {col[0].y, col[1].y, col[2].y, col[3].y},
+                                              {col[0].z, col[1].z, col[2].z, col[3].z},
+                                              {col[0].w, col[1].w, col[2].w, col[3].w}};
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        const uint32_t row = 4 * ib + p;
+                        const uint32_t off = sw64_off(row, jc);
+                        *reinterpret_cast<float4*>(hi + off) =
+                            make_float4(rows[p][0], rows[p][1], rows[p][2], rows[p][3]);
+                        *reinterpret_cast<float4*>(lo + off) =
+                            make_float4(tf32_lo(rows[p][0]), tf32_lo(rows[p][1]),
+                                        tf32_lo(rows[p][2]), tf32_lo(rows[p][3]));
+                    }
+                }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&lo_full[s]);
+        }
+    } else {
+        // ---------------------- epilogue (8 warps) ----------------------
+        constexpr int kCols = BN / 2;
+        const int quad = warp & 3;
+        const int half = (warp - 4) >> 2;
+        const int64_t row = m0 + 32 * quad + lane;
+        const int64_t c0 = r0 + half * kCols;
+        float acc[kCols];
+#pragma unroll
+        for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
+        const bool gvec = (a.R % 4 == 0);
+        for (int64_t c = 0; c < nchunks; ++c) {
+            const int b = (int)(c & 1);
+            const int64_t use = c >> 1;
+            if (!wait_bounded(&zfull[b], (uint32_t)(use & 1), abort_flag, a.status,
+                              kStatusTimeoutEpi))
+                break;
+            tc_fence_after();
+            const int64_t pi = pre_lo + c / cpp;
+            const float* grow = a.gtab + pi * a.R;
+            const uint32_t tbase = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(b * BN + half * kCols);
+#pragma unroll
+            for (int cc = 0; cc < kCols; cc += 16) {
+                uint32_t z[16];
+                tmem_ld16(tbase + cc, z);
+                tmem_ld_wait();
+                if (gvec && c0 + cc + 16 <= a.R) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 g = __ldg(reinterpret_cast<const float4*>(grow + c0 + cc) + q);
+                        acc[cc + 4 * q + 0] = fmaf(g.x, __uint_as_float(z[4 * q + 0]), acc[cc + 4 * q + 0]);
+                        acc[cc + 4 * q + 1] = fmaf(g.y, __uint_as_float(z[4 * q + 1]), acc[cc + 4 * q + 1]);
+                        acc[cc + 4 * q + 2] = fmaf(g.z, __uint_as_float(z[4 * q + 2]), acc[cc + 4 * q + 2]);
+                        acc[cc + 4 * q + 3] = fmaf(g.w, __uint_as_float(z[4 * q + 3]), acc[cc + 4 * q + 3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const float g = (c0 + cc + q < a.R) ? __ldg(grow + c0 + cc + q) : 0.f;
+                        acc[cc + q] = fmaf(g, __uint_as_float(z[q]), acc[cc + q]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&zempty[b]);
+        }
+        if (!*abort_flag && row < a.I) {
+            float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride + row * a.R + c0;
+            const bool vst = gvec && ((reinterpret_cast<uintptr_t>(a.dst) & 15) == 0);
+#pragma unroll
+            for (int e = 0; e < kCols; e += 4) {
+                if (vst && c0 + e + 4 <= a.R) {
+                    *reinterpret_cast<float4*>(dst + e) =
+                        make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (c0 + e + q < a.R) dst[e + q] = acc[e + q];
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Prep: pre-swizzled hi/lo images of the inner Khatri-Rao table
+// ---------------------------------------------------------------------------
+
+struct BImgArgs {
+    int ngroup;
+    int64_t gdim[kMaxD];
+    const float* gfac[kMaxD];
+    int64_t R, J, Jq;
+    int BN, KS, jq_steps, inner;
+    int64_t nblocks;   // n-tiles x KS
+    float* out;
+};
+
+__global__ void tc_bimage_kernel(BImgArgs a) {
+    const int64_t per_block = 2LL * a.BN * kBK;  // floats (hi + lo)
+    const int64_t n = a.nblocks * per_block;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t blk = e / per_block;
+        const int64_t w = e - blk * per_block;
+        const int half = (int)(w / (a.BN * kBK));
+        const int64_t w2 = w - (int64_t)half * a.BN * kBK;
+        const uint32_t byte = (uint32_t)(w2 * 4);
+        const uint32_t row = byte / 64u;
+        const uint32_t chunk_pos = (byte % 64u) / 16u;
+        const uint32_t elem = (byte % 16u) / 4u;
+        const uint32_t kk = ((chunk_pos ^ (row >> 1)) & 3u) * 4u + elem;
+        const int64_t nt = blk / a.KS;
+        const int ks = (int)(blk - nt * a.KS);
+        const int64_t r = nt * a.BN + row;
+        int64_t j;
+        bool valid;
+        if (a.inner) {
+            j = (int64_t)ks * kBK + kk;
+            valid = j < a.J;
+        } else {
+            const int jp = ks / a.jq_steps;
+            const int64_t jq = (int64_t)(ks - jp * a.jq_steps) * kBK + kk;
+            valid = jq < a.Jq;
+            j = (int64_t)jp * a.Jq + jq;
+        }
+        float v = 0.f;
+        if (valid && r < a.R) {
+            int64_t rem = j;
+            v = 1.f;
+            for (int m = a.ngroup - 1; m >= 0; --m) {
+                const int64_t idx = rem % a.gdim[m];
+                rem /= a.gdim[m];
+                v *= a.gfac[m][idx * a.R + r];
+            }
+        }
+        a.out[e] = half == 0 ? v : v - __uint_as_float(__float_as_uint(v) & kTf32Mask);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+int g_sm_count = 0;
+
+int sm_count() {
+    if (g_sm_count == 0) {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+            g_sm_count = n;
+        else
+            g_sm_count = 152;
+        cudaGetLastError();  // a failed query on a host without a GPU leaves no sticky error
+    }
+    return g_sm_count;
+}
+
+int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct MapGeom {
+    int rank;
+    int slot[kRoles];
+    uint64_t dim[5];
+    uint64_t stride_el[5];  // element strides; stride_el[0] = 1
+    uint32_t box[5];
+};
+
+// Tensor-map geometry of Y for mode plan mp; false if TMA cannot express it.
+bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides, int d, MapGeom& mg) {
+    const ModeGeom& g = mp.g;
+    const int k = g.k;
+    struct Dim {
+        int role;
+        int64_t size, stride;
+    } dl[kRoles];
+    int n = 0;
+    // pre modes split into the run before k and the run after k
+    int64_t sizeP = 1, strideP = 0, sizeQ = 1, strideQ = 0;
+    for (int t = 0; t < g.npm; ++t) {
+        const int m = g.pm[t];
+        if (m < k) {
+            sizeP *= dims[m];
+            strideP = strides[m];  // last (innermost) mode of the run
+        } else {
+            sizeQ *= dims[m];
+            strideQ = strides[m];
+        }
+    }
+    // the runs must be contiguous in memory (adjacent modes)
+    for (int t = 0; t + 1 < g.npm; ++t) {
+        const int m = g.pm[t], m2 = g.pm[t + 1];
+        if ((m < k) == (m2 < k) && m2 != m + 1) return false;
+    }
+    (void)d;
+    if (mp.tc_inner) {
+        dl[n++] = {kRoleJq, g.J, g.IQ};   // j (stride I) — carried in the Jq role
+        dl[n++] = {kRoleI, g.I, 1};
+    } else {
+        dl[n++] = {kRoleJq, g.Jq, 1};
+        dl[n++] = {kRoleI, g.I, g.s_k};
+        if (g.J > g.Jq) dl[n++] = {kRoleJp, g.J / g.Jq, g.IQ};
+    }
+    if (sizeP > 1) dl[n++] = {kRolePP, sizeP, strideP};
+    if (sizeQ > 1) dl[n++] = {kRolePQ, sizeQ, strideQ};
+    // the innermost (stride-1) dimension first, the others by increasing stride
+    int first = -1;
+    for (int t = 0; t < n; ++t)
+        if (dl[t].stride == 1) first = t;
+    if (first < 0) return false;
+    Dim tmp = dl[0];
+    dl[0] = dl[first];
+    dl[first] = tmp;
+    for (int t = 1; t < n; ++t)
+        for (int u = t + 1; u < n; ++u)
+            if (dl[u].stride < dl[t].stride) {
+                tmp = dl[t];
+                dl[t] = dl[u];
+                dl[u] = tmp;
+            }
+    if (n > 5) return false;
+    mg.rank = n;
+    for (int q = 0; q < kRoles; ++q) mg.slot[q] = -1;
+    for (int t = 0; t < n; ++t) {
+        mg.slot[dl[t].role] = t;
+        mg.dim[t] = (uint64_t)dl[t].size;
+        mg.stride_el[t] = (uint64_t)dl[t].stride;
+        if (dl[t].size >= ((int64_t)1 << 31)) return false;
+        if (t > 0 && ((dl[t].stride * 4) % 16 != 0 || dl[t].stride * 4 >= ((int64_t)1 << 40)))
+            return false;
+        mg.box[t] = 1;
+    }
+    if (mp.tc_inner) {
+        mg.box[mg.slot[kRoleI]] = kBM;   // slot 0: i contiguous
+        mg.box[mg.slot[kRoleJq]] = kBK;
+        if (mg.slot[kRoleI] != 0) return false;
+    } else {
+        if (mg.slot[kRoleJq] != 0) return false;
+        mg.box[0] = kBK;
+        mg.box[mg.slot[kRoleI]] = kBM;
+    }
+    return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+template <int BN, bool INNER>
+cudaError_t launch_main(const TcArgs& args, dim3 grid, cudaStream_t s) {
+    using L = Smem<BN, INNER>;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tc_mttkrp_kernel<BN, INNER>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kTotal);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    tc_mttkrp_kernel<BN, INNER><<<grid, kThreads, L::kTotal, s>>>(args);
+    return cudaGetLastError();
+}
+
+size_t bimg_bytes(const ModePlan& mp) {
+    return (size_t)cdiv64(mp.g.R, mp.bn) * mp.tc_ks * 2 * (size_t)mp.bn * kBK * sizeof(float);
+}
+
+}  // namespace
+
+size_t tc_binner_bytes(const ModePlan& mp) { return bimg_bytes(mp); }
+
+bool tc_prefer(const ModePlan& mp) {
+    // the 128-row tile must be reasonably full and the rank large enough for
+    // the tensor-core products to pay off
+    return mp.g.I >= 96 && mp.g.R >= 32;
+}
+
+bool tc_plan(const Plan& p, ModePlan& mp) {
+    const ModeGeom& g = mp.g;
+    mp.path = MTTKRP_PATH_TC;
+    mp.tc_inner = (g.s_k == 1) ? 1 : 0;
+    mp.bm = kBM;
+    mp.bn = g.R >= 192 ? 256 : (g.R > 64 ? 128 : 64);
+    if (mp.tc_inner) {
+        if (g.J > g.Jq && g.Jq != 1) return false;
+        mp.tc_jq_steps = 1;
+        mp.tc_ks = (int)cdiv64(g.J, kBK);
+    } else {
+        mp.tc_jq_steps = (int)cdiv64(g.Jq, kBK);
+        mp.tc_ks = (int)((g.J / g.Jq) * mp.tc_jq_steps);
+    }
+    if (cdiv64(g.I, kBM) > 65535 || g.npre >= ((int64_t)1 << 31)) return false;
+    MapGeom mg;
+    if (!y_map_geom(mp, p.dims, p.strides, p.d, mg)) return false;
+    // split count: fill whole waves of one CTA per SM, at least two drain
+    // chunks per CTA where possible
+    const int64_t tiles = cdiv64(g.I, kBM) * cdiv64(g.R, mp.bn);
+    const int64_t sms = sm_count();
+    const int64_t smax = g.npre;
+    int64_t best = 1;
+    double best_eff = -1.0;
+    for (int64_t S = 1; S <= smax && S * tiles <= 8 * sms; ++S) {
+        const int64_t ctas = S * tiles;
+        const double eff = (double)ctas / (double)(cdiv64(ctas, sms) * sms);
+        if (eff > best_eff + 0.02) {
+            best_eff = eff;
+            best = S;
+        }
+    }
+    mp.pre_per_split = cdiv64(g.npre, best);
+    mp.splits = cdiv64(g.npre, mp.pre_per_split);
+    return true;
+}
+
+int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const* factors,
+           const float* gtab, const int64_t* basetab, void* binner_ws, float* dst,
+           cudaStream_t stream, int* nlaunch, cudaEvent_t* start_ev, char* errbuf, size_t errlen) {
+    (void)basetab;
     *nlaunch = 0;
-    snprintf(errbuf, errlen, "tensor-core path not available");
-    return MTTKRP_ERR_UNSUPPORTED;
+    const ModeGeom& g = mp.g;
+    if ((reinterpret_cast<uintptr_t>(Y) & 15) != 0) {
+        snprintf(errbuf, errlen, "tensor-core path needs a 16-byte aligned Y");
+        return MTTKRP_ERR_INVALID;
+    }
+    MapGeom mg;
+    if (!y_map_geom(mp, p.dims, p.strides, p.d, mg)) {
+        snprintf(errbuf, errlen, "mode %d: Y view not expressible as a TMA tensor map", g.k);
+        return MTTKRP_ERR_UNSUPPORTED;
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+    if (encode == nullptr) {
+        snprintf(errbuf, errlen, "cuTensorMapEncodeTiled entry point not available");
+        return MTTKRP_ERR_CUDA;
+    }
+    TcArgs args;
+    memset(&args, 0, sizeof(args));
+    cuuint64_t gdim[5], gstride[4];
+    cuuint32_t box[5], estr[5];
+    for (int t = 0; t < mg.rank; ++t) {
+        gdim[t] = mg.dim[t];
+        box[t] = mg.box[t];
+        estr[t] = 1;
+        if (t > 0) gstride[t - 1] = mg.stride_el[t] * sizeof(float);
+    }
+    CUresult cr = encode(&args.ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)mg.rank,
+                         const_cast<float*>(Y), gdim, gstride, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         mp.tc_inner ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) {
+        snprintf(errbuf, errlen, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
+        return MTTKRP_ERR_CUDA;
+    }
+    args.rank = mg.rank;
+    for (int q = 0; q < kRoles; ++q) args.slot[q] = mg.slot[q];
+
+    // B images
+    float* bimg = static_cast<float*>(binner_ws);
+    {
+        BImgArgs b;
+        memset(&b, 0, sizeof(b));
+        b.ngroup = g.ngroup;
+        for (int t = 0; t < g.ngroup; ++t) {
+            b.gdim[t] = p.dims[g.group[t]];
+            b.gfac[t] = factors[g.group[t]];
+        }
+        b.R = g.R;
+        b.J = g.J;
+        b.Jq = g.Jq;
+        b.BN = mp.bn;
+        b.KS = mp.tc_ks;
+        b.jq_steps = mp.tc_jq_steps;
+        b.inner = mp.tc_inner;
+        b.nblocks = cdiv64(g.R, mp.bn) * mp.tc_ks;
+        b.out = bimg;
+        const int64_t n = b.nblocks * 2 * mp.bn * kBK;
+        int64_t blocks = cdiv64(n, 256);
+        if (blocks > 152 * 16) blocks = 152 * 16;
+        tc_bimage_kernel<<<(unsigned)blocks, 256, 0, stream>>>(b);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            snprintf(errbuf, errlen, "B image launch: %s", cudaGetErrorString(e));
+            return MTTKRP_ERR_CUDA;
+        }
+        ++*nlaunch;
+    }
+
+    // the pre index pi = (p-side, q-side) in C order
+    int64_t nQ = 1;
+    for (int t = 0; t < g.npm; ++t)
+        if (g.pm[t] > g.k) nQ *= p.dims[g.pm[t]];
+    args.bimg = bimg;
+    args.gtab = gtab;
+    args.dst = dst;
+    args.dst_split_stride = g.I * g.R;
+    args.I = g.I;
+    args.R = g.R;
+    args.npre = g.npre;
+    args.pre_per_split = mp.pre_per_split;
+    args.nQ = nQ;
+    args.KS = mp.tc_ks;
+    args.jq_steps = mp.tc_jq_steps;
+    args.status = tc_status_ptr();
+    if (args.status == nullptr) {
+        snprintf(errbuf, errlen, "device status word unavailable");
+        return MTTKRP_ERR_CUDA;
+    }
+    if (start_ev) cudaEventRecord(*start_ev, stream);
+    dim3 grid((unsigned)cdiv64(g.R, mp.bn), (unsigned)cdiv64(g.I, kBM), (unsigned)mp.splits);
+    cudaError_t e;
+    if (mp.tc_inner) {
+        e = mp.bn == 256 ? launch_main<256, true>(args, grid, stream)
+          : mp.bn == 128 ? launch_main<128, true>(args, grid, stream)
+                         : launch_main<64, true>(args, grid, stream);
+    } else {
+        e = mp.bn == 256 ? launch_main<256, false>(args, grid, stream)
+          : mp.bn == 128 ? launch_main<128, false>(args, grid, stream)
+                         : launch_main<64, false>(args, grid, stream);
+    }
+    if (e != cudaSuccess) {
+        snprintf(errbuf, errlen, "tensor-core kernel launch: %s", cudaGetErrorString(e));
+        return MTTKRP_ERR_CUDA;
+    }
+    ++*nlaunch;
+    return MTTKRP_OK;
+}
+
+uint32_t* tc_status_ptr() {
+    static uint32_t* ptrs[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (ptrs[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<uint32_t*>(p);
+    }
+    return ptrs[dev];
 }
 
 cudaError_t tc_read_and_clear_status(uint32_t* word) {

@@ -11,7 +11,7 @@ size_t tc_binner_bytes(const ModePlan& mp);
 // Whether the planner should choose the tensor-core path for this mode.
 bool tc_prefer(const ModePlan& mp);
 // Fill tiles and split counts for the tensor-core path; false if unsupported.
-bool tc_plan(ModePlan& mp);
+bool tc_plan(const Plan& p, ModePlan& mp);
 // Enqueue the tensor-core work of one mode (tables are already built).
 // *nlaunch receives the number of kernels enqueued.  If start_ev is non-null,
 // *start_ev is re-recorded just before the main kernel (after the tensor-core
@@ -19,6 +19,8 @@ bool tc_plan(ModePlan& mp);
 int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const* factors,
            const float* gtab, const int64_t* basetab, void* binner_ws, float* dst,
            cudaStream_t stream, int* nlaunch, cudaEvent_t* start_ev, char* errbuf, size_t errlen);
+// Device address of the error word on the current device (null on failure).
+uint32_t* tc_status_ptr();
 // Read and clear the device-side error word (synchronises the device).
 cudaError_t tc_read_and_clear_status(uint32_t* word);
 
