@@ -25,7 +25,7 @@
 #include <cstddef>
 #include <cstdint>
 
-#include "../../include/mttkrp.h"
+#include "mttkrp.h"
 
 namespace mk {
 

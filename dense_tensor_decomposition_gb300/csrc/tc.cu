@@ -39,9 +39,8 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 16;           // contraction indices per K-step (64-byte rows)
-constexpr int kChunkSteps = 8;    // K-steps accumulated in TMEM between drains
-constexpr int kStages = 4;
-constexpr int kEpiWarps = 8;
+constexpr int kChunkSteps = 8;    // at most this many K-steps accumulate in TMEM between drains
+constexpr int kEpiWarps = 16;  // 4 per TMEM lane quadrant
 constexpr int kThreads = (4 + kEpiWarps) * 32;
 
 constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s bound on every wait
@@ -112,15 +111,29 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* bar, uint32_t parity
     return ok;
 }
 
-// Wait for the phase of `bar` with the given parity.  Returns false if the CTA
-// was aborted or the wait exceeded kWaitNs (then the CTA is aborted and `code`
-// is recorded in the status word).
-__device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* status, uint32_t code) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Blocking probe: the thread is suspended (no issue slots used) until the phase
+// completes or about kSuspendNs elapse.
+constexpr uint32_t kSuspendNs = 20000;
+
+__device__ __forceinline__ uint32_t mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok;
+}
+
+// Slow path of wait_bounded: suspend-and-retry until the phase completes, the
+// CTA is aborted, or kWaitNs pass (then the CTA is aborted and `code` recorded).
+__device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                       uint32_t* status, uint32_t code) {
     const unsigned long long t0 = gtimer();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_suspend(bar, parity)) return true;
         if (*abort_flag) return false;
         if (gtimer() - t0 > kWaitNs) {
             *abort_flag = 1;
@@ -130,10 +143,18 @@ __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Wait for the phase of `bar` with the given parity; false if the CTA was
+// aborted or the wait exceeded kWaitNs.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             uint32_t* status, uint32_t code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, abort_flag, status, code);
+}
+
 // Like wait_bounded but ignores the abort flag (used to drain in-flight work).
 __device__ __noinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint32_t* status) {
     const unsigned long long t0 = gtimer();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_suspend(bar, parity)) {
         if (gtimer() - t0 > kWaitNs) {
             atomicOr(status, kStatusTimeoutDrain);
             return false;
@@ -199,15 +220,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 
 // K-major, 64-byte swizzle shared-memory matrix descriptor: 8-row groups of
-// 64-byte rows, 512 bytes apart.
+// 64-byte rows, 512 bytes apart.  Everything but the start-address field is
+// constant.
+constexpr uint64_t kDescSw64Hi = ((uint64_t)1 << 16)           // leading byte offset (unused)
+                               | ((uint64_t)(512 >> 4) << 32)  // stride byte offset: 8 rows x 64 B
+                               | ((uint64_t)1 << 46)           // descriptor version
+                               | ((uint64_t)4 << 61);          // 64-byte swizzle
+
 __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
-    d |= (uint64_t)(512 >> 4) << 32;   // stride byte offset: 8 rows x 64 B
-    d |= (uint64_t)1 << 46;            // descriptor version
-    d |= (uint64_t)4 << 61;            // 64-byte swizzle
-    return d;
+    return kDescSw64Hi | (uint64_t)((saddr & 0x3FFFFu) >> 4);
 }
 
 __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -234,6 +255,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
         : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -250,30 +278,104 @@ __device__ __forceinline__ uint32_t sw64_off(uint32_t row, uint32_t chunk) {
 // ---------------------------------------------------------------------------
 // Main kernel
 // ---------------------------------------------------------------------------
+//
+// Order of work in a CTA: the inner index range is cut into B-chunks of CK
+// K-steps whose hi|lo images stay resident in shared memory; for each chunk the
+// CTA walks all of its pi, streaming only Y tiles.  TMEM is drained after every
+// "unit" of at most kChunkSteps K-steps of one (chunk, pi) pair.
+
+#ifndef TC_GROUP
+#define TC_GROUP 1
+#endif
+#ifndef TC_STAGES
+#define TC_STAGES 5
+#endif
+#ifndef TC_STAGES_INNER
+#define TC_STAGES_INNER 3
+#endif
+#ifndef TC_BRES_KB
+#define TC_BRES_KB 128
+#endif
+#ifndef TC_BRES_INNER_KB
+#define TC_BRES_INNER_KB 128
+#endif
 
 template <int BN, bool INNER>
 struct Smem {
-    static constexpr uint32_t kY = kBM * kBK * 4;      // 8 KB: raw Y tile (hi, or staging if INNER)
-    static constexpr uint32_t kA = kBM * kBK * 4;      // 8 KB
-    static constexpr uint32_t kB = BN * kBK * 4;       // BN x 64 B
-    static constexpr uint32_t kStage = kY + kA + (INNER ? kA : 0) + 2 * kB;
+    static constexpr uint32_t kY = kBM * kBK * 4;      // 8 KB: raw Y tile (hi, or i-major staging if INNER)
+    static constexpr uint32_t kA = kBM * kBK * 4;      // 8 KB: one K-major A operand tile
+    static constexpr uint32_t kB = BN * kBK * 4;       // BN x 64 B, one K-step of B
+    static constexpr uint32_t kBRes = (uint32_t)(INNER ? TC_BRES_INNER_KB : TC_BRES_KB) * 1024;  // resident B-chunk
+    static constexpr int kCK = (int)(kBRes / (2 * kB));  // K-steps per B-chunk
+    // stages (raw Y tile + on-chip operand tile(s)), consumed in groups of
+    // kGroup: one producer arrival, one MMA wait and one MMA commit per group
+    static constexpr int kGroup = TC_GROUP;
+    static constexpr int kRaw = INNER ? TC_STAGES_INNER : TC_STAGES;
+    static constexpr int kOps = kRaw;
+    static constexpr uint32_t kOp = INNER ? 2 * kA : kA;  // lo (and transposed hi if INNER)
+    static constexpr uint32_t kG = kEpiWarps * 2 * (BN / 4) * 4;  // per-warp G rows, double-buffered
     static constexpr uint32_t kBarBytes = 256;
-    static constexpr uint32_t kTotal = 1024 + kStages * kStage + kBarBytes;
+    static constexpr uint32_t kOffRaw = kBRes;
+    static constexpr uint32_t kOffOps = kOffRaw + kRaw * kY;
+    static constexpr uint32_t kOffG = kOffOps + kOps * kOp;
+    static constexpr uint32_t kOffBars = kOffG + kG;
+    static constexpr uint32_t kTotal = 1024 + kOffBars + kBarBytes;
+    static_assert(kTotal <= 232448, "shared memory budget");
+    static_assert((kRaw + 2 * (kRaw / kGroup) + 7) * 8 + 8 <= kBarBytes, "barrier area");
+};
+
+// warp-uniform bounded wait: lane 0 waits, the result is broadcast
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* status, uint32_t code) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, status, code);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// Position in a ring of N slots used round-robin: slot, parity of the current
+// round, and whether a previous round exists (then the slot must be released
+// first, i.e. its "empty" barrier has completed with parity phase ^ 1).
+template <int N>
+struct Ring {
+    int slot = 0;
+    uint32_t phase = 0;
+    bool reused = false;
+    __device__ __forceinline__ void next() {
+        if (++slot == N) {
+            slot = 0;
+            phase ^= 1u;
+            reused = true;
+        }
+    }
 };
 
 template <int BN, bool INNER>
 __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_constant__ TcArgs a) {
     using L = Smem<BN, INNER>;
+    constexpr int CK = L::kCK;
+    constexpr int NR = L::kRaw;
+    constexpr int NO = L::kOps;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~(uintptr_t)1023);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * L::kStage);
-    uint64_t* tma_full = bars;                 // [kStages]
-    uint64_t* lo_full = bars + kStages;        // [kStages]
-    uint64_t* empty = bars + 2 * kStages;      // [kStages]
-    uint64_t* zfull = bars + 3 * kStages;      // [2]
-    uint64_t* zempty = zfull + 2;              // [2]
-    uint64_t* mma_done = zempty + 2;           // [1]
+    uint8_t* bres = smem;
+    uint8_t* raw = smem + L::kOffRaw;
+    uint8_t* ops = smem + L::kOffOps;
+    float* gsm = reinterpret_cast<float*>(smem + L::kOffG);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBars);
+    // stage s holds raw Y tile s and operand tile s; K-step t uses stage t % NR
+    // and group (t / GS) % NP
+    constexpr int GS = L::kGroup;
+    static_assert(NR == NO && NR % GS == 0, "stages come in whole groups");
+    constexpr int NP = NR / GS;
+    uint64_t* raw_full = bars;                  // [NR] TMA landed
+    uint64_t* op_full = raw_full + NR;          // [NP] producers wrote the pair's operand tiles
+    uint64_t* stage_empty = op_full + NP;       // [NP] MMAs that read the pair are done
+    uint64_t* zfull = stage_empty + NP;         // [2]
+    uint64_t* zempty = zfull + 2;               // [2]
+    uint64_t* bfull = zempty + 2;               // [1]
+    uint64_t* bempty = bfull + 1;               // [1]
+    uint64_t* mma_done = bempty + 1;            // [1]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -287,21 +389,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
     if (pre_hi > a.npre) pre_hi = a.npre;
     const int64_t npi = pre_hi > pre_lo ? pre_hi - pre_lo : 0;
     const int KS = a.KS;
-    const int64_t T = npi * KS;                          // K-steps of this CTA
-    const int cpp = (KS + kChunkSteps - 1) / kChunkSteps;  // drain chunks per pi
-    const int64_t nchunks = npi * cpp;
+    const int njc = (KS + CK - 1) / CK;           // B-chunks
+    auto chunk_len = [&](int jc) { return min(CK, KS - jc * CK); };
     constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : 2 * BN;
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&tma_full[s], 1);
-            mbar_init(&lo_full[s], 2);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < NR; ++s) mbar_init(&raw_full[s], 1);
+        for (int s = 0; s < NP; ++s) {
+            mbar_init(&op_full[s], 2);
+            mbar_init(&stage_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&zfull[b], 1);
             mbar_init(&zempty[b], kEpiWarps);
         }
+        mbar_init(bfull, 1);
+        mbar_init(bempty, 1);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -316,126 +419,184 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    // K-step t -> (pi, coordinates)
-    auto step_coords = [&](int64_t t, int* c, int64_t* pi_out) {
-        const int64_t pi = pre_lo + t / KS;
-        const int ks = (int)(t % KS);
-        int role[kRoles];
-        if (INNER) {
-            role[kRoleJq] = ks * kBK;  // j (the contraction index) runs along dim "Jq" slot
-            role[kRoleJp] = 0;
-        } else {
-            const int jp = ks / a.jq_steps;
-            role[kRoleJq] = (ks - jp * a.jq_steps) * kBK;
-            role[kRoleJp] = jp;
-        }
-        role[kRoleI] = (int)m0;
-        role[kRolePP] = (int)(pi / a.nQ);
-        role[kRolePQ] = (int)(pi % a.nQ);
-        for (int q = 0; q < kRoles; ++q)
-            if (a.slot[q] >= 0) c[a.slot[q]] = role[q];
-        *pi_out = pi;
-    };
+    const int64_t T = npi * KS;  // K-steps of this CTA
 
     if (warp == 0) {
         // ------------------------- TMA producer -------------------------
         if (lane == 0) {
-            const uint32_t bytes = L::kY + 2 * L::kB;
             const uint8_t* bimg = reinterpret_cast<const uint8_t*>(a.bimg);
+            Ring<NR> rr;
+            Ring<NP> pr;
             int64_t issued = 0;
-            for (int64_t t = 0; t < T; ++t) {
-                const int s = (int)(t % kStages);
-                const int64_t round = t / kStages;
-                if (round > 0 &&
-                    !wait_bounded(&empty[s], (uint32_t)((round - 1) & 1), abort_flag, a.status,
-                                  kStatusTimeoutTma))
+            int jc_loaded = -1;
+            bool ok = true;
+            // Replace the resident B-chunk with chunk jc once the MMAs of chunk
+            // jc - 1 are done.
+            auto load_b = [&](int jc) -> bool {
+                if (jc > 0 && !wait_bounded(bempty, (uint32_t)((jc - 1) & 1), abort_flag, a.status,
+                                            kStatusTimeoutTma))
+                    return false;
+                const int ck = chunk_len(jc);
+                mbar_arrive_expect_tx(bfull, (uint32_t)(ck * 2 * L::kB));
+                for (int q = 0; q < ck; ++q) {
+                    const int ks = jc * CK + q;
+                    const uint8_t* src = bimg + ((int64_t)blockIdx.x * KS + ks) * (int64_t)(2 * L::kB);
+                    bulk_load(bres + q * 2 * L::kB, src, 2 * L::kB, bfull);
+                }
+                jc_loaded = jc;
+                return true;
+            };
+            for (int jc = 0; jc < njc && ok; ++jc) {
+                const int ck = chunk_len(jc);
+                // A chunk boundary inside a stage pair: the MMA issuer waits for the
+                // whole pair before it finishes chunk jc - 1, so the pair's second
+                // Y tile is issued before the chunk swap (which waits for those MMAs).
+                bool b_pending = (jc > 0) && (issued % GS != 0);
+                if (!b_pending && !load_b(jc)) {
+                    ok = false;
                     break;
-                uint8_t* st = smem + s * L::kStage;
-                int c[5] = {0, 0, 0, 0, 0};
-                int64_t pi;
-                step_coords(t, c, &pi);
-                const int ks = (int)(t % KS);
-                mbar_arrive_expect_tx(&tma_full[s], bytes);
-                tma_load(&a.ymap, a.rank, c, st, &tma_full[s]);
-                const uint8_t* src =
-                    bimg + ((int64_t)blockIdx.x * KS + ks) * (int64_t)(2 * L::kB);
-                bulk_load(st + L::kY + L::kA + (INNER ? L::kA : 0), src, 2 * L::kB, &tma_full[s]);
-                issued = t + 1;
+                }
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                    const int cP = (int)(pi / a.nQ);
+                    const int cQ = (int)(pi - (int64_t)cP * a.nQ);
+                    for (int q = 0; q < ck; ++q, ++issued, rr.next()) {
+                        const int ks = jc * CK + q;
+                        if (issued % GS == 0) {
+                            if (issued > 0) pr.next();
+                            if (pr.reused && !wait_bounded(&stage_empty[pr.slot], pr.phase ^ 1u,
+                                                           abort_flag, a.status, kStatusTimeoutTma)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        int role[kRoles];
+                        if (INNER) {
+                            role[kRoleJq] = ks * kBK;
+                            role[kRoleJp] = 0;
+                        } else {
+                            const int jp = ks / a.jq_steps;
+                            role[kRoleJq] = (ks - jp * a.jq_steps) * kBK;
+                            role[kRoleJp] = jp;
+                        }
+                        role[kRoleI] = (int)m0;
+                        role[kRolePP] = cP;
+                        role[kRolePQ] = cQ;
+                        int c[5] = {0, 0, 0, 0, 0};
+#pragma unroll
+                        for (int r = 0; r < kRoles; ++r)
+                            if (a.slot[r] >= 0) c[a.slot[r]] = role[r];
+                        mbar_arrive_expect_tx(&raw_full[rr.slot], L::kY);
+                        tma_load(&a.ymap, a.rank, c, raw + rr.slot * L::kY, &raw_full[rr.slot]);
+                        if (b_pending && (issued + 1) % GS == 0) {
+                            // the group is complete
+                            b_pending = false;
+                            if (!load_b(jc)) {
+                                ok = false;
+                                ++issued;
+                                rr.next();
+                                break;
+                            }
+                        }
+                    }
+                }
             }
             // wait (bounded) for copies still in flight before leaving
-            for (int64_t t = issued - 1; t >= 0 && t >= issued - kStages; --t)
-                wait_drain(&tma_full[t % kStages], (uint32_t)((t / kStages) & 1), a.status);
+            for (int64_t u = issued - 1; u >= 0 && u >= issued - NR; --u)
+                wait_drain(&raw_full[u % NR], (uint32_t)((u / NR) & 1), a.status);
+            if (jc_loaded >= 0) wait_drain(bfull, (uint32_t)(jc_loaded & 1), a.status);
         }
     } else if (warp == 1) {
         // ------------------------- MMA issuer -------------------------
         if (lane == 0) {
             const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
                                    ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-            int64_t chunk = -1;
+            const uint32_t raw_s = smem_u32(raw);
+            const uint32_t ops_s = smem_u32(ops);
+            const uint32_t bres_s = smem_u32(bres);
+            Ring<NR> rr;
+            Ring<NP> pr;
+            int64_t t = 0;       // K-steps issued
+            int zb = 0;          // TMEM buffer of the current unit
+            uint32_t zph = 0;    // bit b: parity of the next release of buffer b
+            uint32_t zused = 0;  // bit b: buffer b was used before
             bool ok = true;
-            for (int64_t t = 0; t < T && ok; ++t) {
-                const int s = (int)(t % kStages);
-                const int64_t round = t / kStages;
-                const int ks = (int)(t % KS);
-                const bool first = (ks % kChunkSteps) == 0;
-                const bool last = ((ks % kChunkSteps) == kChunkSteps - 1) || (ks == KS - 1);
-                if (first) {
-                    ++chunk;
-                    const int64_t use = chunk >> 1;
-                    if (use > 0 && !wait_bounded(&zempty[chunk & 1], (uint32_t)((use - 1) & 1),
-                                                 abort_flag, a.status, kStatusTimeoutMma)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                }
-                if (!wait_bounded(&tma_full[s], (uint32_t)(round & 1), abort_flag, a.status,
-                                  kStatusTimeoutMma) ||
-                    !wait_bounded(&lo_full[s], (uint32_t)(round & 1), abort_flag, a.status,
-                                  kStatusTimeoutMma)) {
+            for (int jc = 0; jc < njc && ok; ++jc) {
+                const int ck = chunk_len(jc);
+                if (!wait_bounded(bfull, (uint32_t)(jc & 1), abort_flag, a.status, kStatusTimeoutMma)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                uint8_t* st = smem + s * L::kStage;
-                const uint8_t* a_hi = INNER ? st + L::kY : st;
-                const uint8_t* a_lo = a_hi + L::kA;
-                const uint8_t* b_hi = st + L::kY + L::kA + (INNER ? L::kA : 0);
-                const uint8_t* b_lo = b_hi + L::kB;
-                const uint64_t dah = sdesc_sw64(smem_u32(a_hi));
-                const uint64_t dal = sdesc_sw64(smem_u32(a_lo));
-                const uint64_t dbh = sdesc_sw64(smem_u32(b_hi));
-                const uint64_t dbl = sdesc_sw64(smem_u32(b_lo));
-                const uint32_t dz = tmem + (uint32_t)((chunk & 1) * BN);
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                    for (int q = 0; q < ck; ++q, rr.next(), ++t) {
+                        const bool first = (q % kChunkSteps) == 0;
+                        const bool last = (q % kChunkSteps) == kChunkSteps - 1 || q == ck - 1;
+                        if (first && ((zused >> zb) & 1u)) {
+                            // the epilogue has read this TMEM buffer's previous contents
+                            if (!wait_bounded(&zempty[zb], (zph >> zb) & 1u, abort_flag, a.status,
+                                              kStatusTimeoutMma)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        // the producers arrive only after the pair's TMA copies landed, so
+                        // one wait per pair covers all four tiles
+                        if (t % GS == 0) {
+                            if (t > 0) pr.next();
+                            if (!wait_bounded(&op_full[pr.slot], pr.phase, abort_flag, a.status,
+                                              kStatusTimeoutMma)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        const uint32_t op = ops_s + (uint32_t)rr.slot * L::kOp;
+                        const uint32_t a_hi = INNER ? op : raw_s + (uint32_t)rr.slot * L::kY;
+                        const uint32_t a_lo = INNER ? op + L::kA : op;
+                        const uint32_t b_hi = bres_s + (uint32_t)q * 2u * L::kB;
+                        const uint64_t dah = sdesc_sw64(a_hi);
+                        const uint64_t dal = sdesc_sw64(a_lo);
+                        const uint64_t dbh = sdesc_sw64(b_hi);
+                        const uint64_t dbl = sdesc_sw64(b_hi + L::kB);
+                        const uint32_t dz = tmem + (uint32_t)(zb * BN);
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    const uint64_t adv = (uint64_t)((kk * 32) >> 4);  // 8 tf32 = 32 bytes
-                    mma_tf32(dz, dah + adv, dbh + adv, idesc, (first && kk == 0) ? 0u : 1u);
-                    mma_tf32(dz, dah + adv, dbl + adv, idesc, 1u);
-                    mma_tf32(dz, dal + adv, dbh + adv, idesc, 1u);
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint64_t adv = (uint64_t)((kk * 32) >> 4);  // 8 tf32 = 32 bytes
+                            mma_tf32(dz, dah + adv, dbh + adv, idesc, (first && kk == 0) ? 0u : 1u);
+                            mma_tf32(dz, dah + adv, dbl + adv, idesc, 1u);
+                            mma_tf32(dz, dal + adv, dbh + adv, idesc, 1u);
+                        }
+                        if (t % GS == GS - 1 || t == T - 1) mma_commit(&stage_empty[pr.slot]);
+                        if (last) {
+                            mma_commit(&zfull[zb]);
+                            if ((zused >> zb) & 1u) zph ^= 1u << zb;
+                            zused |= 1u << zb;
+                            zb ^= 1;
+                        }
+                    }
                 }
-                mma_commit(&empty[s]);
-                if (last) mma_commit(&zfull[chunk & 1]);
+                if (ok) mma_commit(bempty);  // the B-chunk may be replaced once these finish
             }
             // all MMAs issued by this thread are complete before TMEM is freed
             mma_commit(mma_done);
             wait_drain(mma_done, 0, a.status);
         }
     } else if (warp < 4) {
-        // ---------------------- lo producers (64 threads) ----------------------
+        // ---------------------- operand producers (64 threads) ----------------------
         const int ptid = tid - 64;
-        for (int64_t t = 0; t < T; ++t) {
-            const int s = (int)(t % kStages);
-            const int64_t round = t / kStages;
-            if (!wait_bounded(&tma_full[s], (uint32_t)(round & 1), abort_flag, a.status,
-                              kStatusTimeoutLo))
+        Ring<NR> rr;
+        Ring<NP> pr;
+        for (int64_t t = 0; t < T; ++t, rr.next()) {
+            if (t % GS == 0 && t > 0) pr.next();
+            // the TMA refills a stage only after its MMAs finished, so the operand
+            // tile of this stage is free once its raw tile has landed
+            if (!warp_wait(&raw_full[rr.slot], rr.phase, abort_flag, a.status, kStatusTimeoutLo))
                 break;
-            uint8_t* st = smem + s * L::kStage;
+            const uint8_t* st = raw + rr.slot * L::kY;
+            uint8_t* op = ops + rr.slot * L::kOp;
             if (!INNER) {
                 // lo tile, elementwise at the same (swizzled) offsets as the raw tile
                 const float4* src = reinterpret_cast<const float4*>(st);
-                float4* dst = reinterpret_cast<float4*>(st + L::kY);
+                float4* dst = reinterpret_cast<float4*>(op);
 #pragma unroll
                 for (int v = 0; v < (int)(L::kY / 16) / 64; ++v) {
                     const int e = ptid + 64 * v;
@@ -446,8 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                 // staging tile is [16 j][128 i] (i contiguous): transpose into the
                 // K-major hi and lo tiles, 4 x 4 blocks per thread
                 const float* stg = reinterpret_cast<const float*>(st);
-                uint8_t* hi = st + L::kY;
-                uint8_t* lo = hi + L::kA;
+                uint8_t* hi = op;
+                uint8_t* lo = op + L::kA;
 #pragma unroll
                 for (int v = 0; v < 2; ++v) {
                     const int blk = ptid + 64 * v;   // 128 blocks: 32 i-blocks x 4 j-chunks
@@ -473,60 +634,86 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                     }
                 }
             }
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&lo_full[s]);
+            if (t % GS == GS - 1 || t == T - 1) {
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&op_full[pr.slot]);
+            }
         }
     } else {
-        // ---------------------- epilogue (8 warps) ----------------------
-        constexpr int kCols = BN / 2;
+        // ---------------------- epilogue (16 warps) ----------------------
+        // warp w reads TMEM lanes 32 * (w % 4) .. + 31 (rows) and a quarter of
+        // the tile's columns.  The G(pi, :) row of the next (chunk, pi) pair is
+        // copied into the warp's second G buffer (cp.async, no registers) while
+        // the current pair is drained.
+        constexpr int kCols = BN / 4;
         const int quad = warp & 3;
-        const int half = (warp - 4) >> 2;
+        const int part = (warp - 4) >> 2;
         const int64_t row = m0 + 32 * quad + lane;
-        const int64_t c0 = r0 + half * kCols;
+        const int64_t c0 = r0 + part * kCols;
+        float* gw = gsm + (warp - 4) * 2 * kCols;   // this warp's two G rows
         float acc[kCols];
 #pragma unroll
         for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
-        const bool gvec = (a.R % 4 == 0);
-        for (int64_t c = 0; c < nchunks; ++c) {
-            const int b = (int)(c & 1);
-            const int64_t use = c >> 1;
-            if (!wait_bounded(&zfull[b], (uint32_t)(use & 1), abort_flag, a.status,
-                              kStatusTimeoutEpi))
-                break;
-            tc_fence_after();
-            const int64_t pi = pre_lo + c / cpp;
-            const float* grow = a.gtab + pi * a.R;
-            const uint32_t tbase = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(b * BN + half * kCols);
-#pragma unroll
-            for (int cc = 0; cc < kCols; cc += 16) {
-                uint32_t z[16];
-                tmem_ld16(tbase + cc, z);
-                tmem_ld_wait();
-                if (gvec && c0 + cc + 16 <= a.R) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 g = __ldg(reinterpret_cast<const float4*>(grow + c0 + cc) + q);
-                        acc[cc + 4 * q + 0] = fmaf(g.x, __uint_as_float(z[4 * q + 0]), acc[cc + 4 * q + 0]);
-                        acc[cc + 4 * q + 1] = fmaf(g.y, __uint_as_float(z[4 * q + 1]), acc[cc + 4 * q + 1]);
-                        acc[cc + 4 * q + 2] = fmaf(g.z, __uint_as_float(z[4 * q + 2]), acc[cc + 4 * q + 2]);
-                        acc[cc + 4 * q + 3] = fmaf(g.w, __uint_as_float(z[4 * q + 3]), acc[cc + 4 * q + 3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const float g = (c0 + cc + q < a.R) ? __ldg(grow + c0 + cc + q) : 0.f;
-                        acc[cc + q] = fmaf(g, __uint_as_float(z[q]), acc[cc + q]);
-                    }
-                }
+        auto fetch_g = [&](int64_t pi, int buf) {
+            for (int e = lane; e < kCols; e += 32) {
+                const bool in = (c0 + e < a.R) && (pi < pre_hi);
+                const float* src = in ? a.gtab + pi * a.R + c0 + e : a.gtab;
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                                 smem_u32(gw + buf * kCols + e)),
+                             "l"(src), "r"(in ? 4 : 0)
+                             : "memory");
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&zempty[b]);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        fetch_g(pre_lo, 0);
+        int gb = 0;           // G buffer of the current pair
+        int zb = 0;           // TMEM buffer of the next unit
+        uint32_t zph = 0;     // bit b: parity of the next completion of zfull[b]
+        bool ok = true;
+        for (int jc = 0; jc < njc && ok; ++jc) {
+            const int ck = chunk_len(jc);
+            for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+                __syncwarp();
+                fetch_g(pi + 1 < pre_hi ? pi + 1 : pre_lo, gb ^ 1);
+                const float* g_cur = gw + gb * kCols;
+                for (int q0 = 0; q0 < ck; q0 += kChunkSteps) {
+                    if (!warp_wait(&zfull[zb], (zph >> zb) & 1u, abort_flag, a.status,
+                                   kStatusTimeoutEpi)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tbase =
+                        tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
+#pragma unroll
+                    for (int cc = 0; cc < kCols; cc += 8) {
+                        uint32_t z[8];
+                        tmem_ld8(tbase + cc, z);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const float4 g = *reinterpret_cast<const float4*>(g_cur + cc + 4 * q);
+                            acc[cc + 4 * q + 0] = fmaf(g.x, __uint_as_float(z[4 * q + 0]), acc[cc + 4 * q + 0]);
+                            acc[cc + 4 * q + 1] = fmaf(g.y, __uint_as_float(z[4 * q + 1]), acc[cc + 4 * q + 1]);
+                            acc[cc + 4 * q + 2] = fmaf(g.z, __uint_as_float(z[4 * q + 2]), acc[cc + 4 * q + 2]);
+                            acc[cc + 4 * q + 3] = fmaf(g.w, __uint_as_float(z[4 * q + 3]), acc[cc + 4 * q + 3]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&zempty[zb]);
+                    zph ^= 1u << zb;
+                    zb ^= 1;
+                }
+                gb ^= 1;
+            }
         }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
         if (!*abort_flag && row < a.I) {
             float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride + row * a.R + c0;
-            const bool vst = gvec && ((reinterpret_cast<uintptr_t>(a.dst) & 15) == 0);
+            const bool vst = (a.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.dst) & 15) == 0);
 #pragma unroll
             for (int e = 0; e < kCols; e += 4) {
                 if (vst && c0 + e + 4 <= a.R) {
