@@ -29,8 +29,10 @@ int fail(int code, const char* fmt, ...) {
 
 constexpr int64_t kMaxR = 65536;
 constexpr int64_t kMaxNumel = (int64_t)1 << 40;
-// Inner-group size the planner aims for (at least this many j values per pi).
+// Inner-group size the planner aims for (at least this many j values per pi),
+// as long as at least kMinPre pre indices remain to spread over split ranges.
 constexpr int64_t kInnerMin = 64;
+constexpr int64_t kMinPre = 64;
 // Longest fp32 accumulation chain (in products) allowed in one SIMT thread; more
 // contraction work is split into ranges whose partials are summed in fp64.
 constexpr int64_t kSimtChain = 8192;
@@ -51,9 +53,20 @@ void classify(const Plan& p, int k, ModeGeom& g) {
     for (int n = k + 1; n < d; ++n) Q *= p.dims[n];
     bool in_group[kMaxD] = {false};
     int64_t J = 1, Jq = 1;
+    const int64_t others = [&] {
+        int64_t x = 1;
+        for (int n = 0; n < d; ++n)
+            if (n != k) x *= p.dims[n];
+        return x;
+    }();
+    // grow the group by one more mode only while it is small and enough pre
+    // indices would remain afterwards (the first mode is always taken)
+    auto grow = [&](int64_t J_now, int64_t dim) {
+        return J_now == 1 || (J_now < kInnerMin && others / (J_now * dim) >= kMinPre);
+    };
     if (Q >= kInnerMin) {
-        // trailing modes after k until the product reaches kInnerMin
-        for (int n = d - 1; n > k && J < kInnerMin; --n) {
+        // trailing modes after k
+        for (int n = d - 1; n > k && grow(J, p.dims[n]); --n) {
             in_group[n] = true;
             J *= p.dims[n];
         }
@@ -62,7 +75,7 @@ void classify(const Plan& p, int k, ModeGeom& g) {
         // all modes after k, then the last modes before k
         for (int n = k + 1; n < d; ++n) in_group[n] = true;
         J = Jq = Q;
-        for (int n = k - 1; n >= 0 && J < kInnerMin; --n) {
+        for (int n = k - 1; n >= 0 && grow(J, p.dims[n]); --n) {
             in_group[n] = true;
             J *= p.dims[n];
         }
@@ -490,6 +503,8 @@ int64_t mttkrp_plan_launch_count(mttkrp_plan_t h) {
     Plan* p = as_plan(h);
     return p ? p->launches : -1;
 }
+
+int mttkrp_test_withhold_signal(int count) { return tc_set_withhold_signal(count); }
 
 void mttkrp_plan_destroy(mttkrp_plan_t h) {
     Plan* p = as_plan(h);

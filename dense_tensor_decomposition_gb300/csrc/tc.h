@@ -21,6 +21,8 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
            cudaStream_t stream, int* nlaunch, cudaEvent_t* start_ev, char* errbuf, size_t errlen);
 // Device address of the error word on the current device (null on failure).
 uint32_t* tc_status_ptr();
+// Arm the failure-detection test hook for the next `count` launches.
+int tc_set_withhold_signal(int count);
 // Read and clear the device-side error word (synchronises the device).
 cudaError_t tc_read_and_clear_status(uint32_t* word);
 

@@ -124,6 +124,15 @@ int mttkrp_plan_kernel_times(mttkrp_plan_t plan, int mode, float* ms, int max);
 /* Number of kernels this plan has launched since it was created. */
 int64_t mttkrp_plan_launch_count(mttkrp_plan_t plan);
 
+/* Test hook for failure detection: the next `count` tensor-core kernel launches
+ * withhold their first accumulator-ready signal, so the waiting warps' bounded
+ * wait expires (after about one second), the kernel records a status bit,
+ * drains its own copies and MMAs, frees its tensor memory and returns with an
+ * incomplete result.  mttkrp_device_status() then reports the bit.  No fault,
+ * trap or endless wait is involved.  count = 0 disarms it.  Returns the
+ * previous count. */
+int mttkrp_test_withhold_signal(int count);
+
 /* Read and clear the device-side error word that kernels set when a bounded
  * wait expires (0 = none).  Synchronises the device.  Returns MTTKRP_OK or
  * MTTKRP_ERR_CUDA; the word is written to *word. */
