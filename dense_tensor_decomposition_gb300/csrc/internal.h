@@ -56,6 +56,8 @@ struct ModePlan {
     int tc_inner;       // 1: mode with stride 1 (Y tile arrives i-major and is transposed)
     int tc_ks;          // K-steps of 16 contraction indices per pi
     int tc_jq_steps;    // K-steps per value of the p-side part of the inner group
+    int tc_small;       // 1: small I_k, tc_ps pre indices share one 128-row tile
+    int tc_ps;
     // workspace layout, byte offsets from the workspace base
     size_t off_partials, off_binner, off_gtab, off_base, total;
 };

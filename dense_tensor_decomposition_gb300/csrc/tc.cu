@@ -70,6 +70,10 @@ struct TcArgs {
     int KS;                   // K-steps per pi
     int jq_steps;             // K-steps per value of jp (K-contiguous variant)
     int withhold_signal;      // test hook: skip the first accumulator-ready commit
+    uint32_t y_box_bytes;     // bytes of one Y tile copy
+    // small-I variant: ps pre indices share one 128-row tile (rows slot * I + i)
+    int ps;                   // pre-index slots per tile (1 otherwise)
+    int64_t batch_len;        // slots never cross a multiple of this pre index
     uint32_t* status;
 };
 
@@ -302,12 +306,13 @@ __device__ __forceinline__ uint32_t sw64_off(uint32_t row, uint32_t chunk) {
 #define TC_BRES_INNER_KB 128
 #endif
 
-template <int BN, bool INNER>
+template <int BN, bool INNER, bool SMALL = false>
 struct Smem {
     static constexpr uint32_t kY = kBM * kBK * 4;      // 8 KB: raw Y tile (hi, or i-major staging if INNER)
     static constexpr uint32_t kA = kBM * kBK * 4;      // 8 KB: one K-major A operand tile
     static constexpr uint32_t kB = BN * kBK * 4;       // BN x 64 B, one K-step of B
-    static constexpr uint32_t kBRes = (uint32_t)(INNER ? TC_BRES_INNER_KB : TC_BRES_KB) * 1024;  // resident B-chunk
+    static constexpr uint32_t kBRes =
+        (uint32_t)(SMALL ? 96 : INNER ? TC_BRES_INNER_KB : TC_BRES_KB) * 1024;  // resident B-chunk
     static constexpr int kCK = (int)(kBRes / (2 * kB));  // K-steps per B-chunk
     // stages (raw Y tile + on-chip operand tile(s)), consumed in groups of
     // kGroup: one producer arrival, one MMA wait and one MMA commit per group
@@ -315,7 +320,8 @@ struct Smem {
     static constexpr int kRaw = INNER ? TC_STAGES_INNER : TC_STAGES;
     static constexpr int kOps = kRaw;
     static constexpr uint32_t kOp = INNER ? 2 * kA : kA;  // lo (and transposed hi if INNER)
-    static constexpr uint32_t kG = kEpiWarps * 2 * (BN / 4) * 4;  // per-warp G rows, double-buffered
+    // per-warp G rows, double-buffered (small-I variant: up to 3 rows per warp)
+    static constexpr uint32_t kG = kEpiWarps * 2 * (SMALL ? 3 : 1) * (BN / 4) * 4;
     static constexpr uint32_t kBarBytes = 256;
     static constexpr uint32_t kOffRaw = kBRes;
     static constexpr uint32_t kOffOps = kOffRaw + kRaw * kY;
@@ -323,6 +329,7 @@ struct Smem {
     static constexpr uint32_t kOffBars = kOffG + kG;
     static constexpr uint32_t kTotal = 1024 + kOffBars + kBarBytes;
     static_assert(kTotal <= 232448, "shared memory budget");
+    static_assert(!SMALL || (uint32_t)(kBM * (BN + 4) * 4) <= kOffG, "slot-reduction buffer must fit");
     static_assert((kRaw + 2 * (kRaw / kGroup) + 7) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
@@ -351,9 +358,10 @@ struct Ring {
     }
 };
 
-template <int BN, bool INNER>
+template <int BN, bool INNER, bool SMALL>
 __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_constant__ TcArgs a) {
-    using L = Smem<BN, INNER>;
+    static_assert(!(SMALL && INNER), "the small-I variant needs a K-major Y tile");
+    using L = Smem<BN, INNER, SMALL>;
     constexpr int CK = L::kCK;
     constexpr int NR = L::kRaw;
     constexpr int NO = L::kOps;
@@ -421,7 +429,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int64_t T = npi * KS;  // K-steps of this CTA
+    // Work units: one pre index, or (small-I variant) up to ps consecutive pre
+    // indices that share one tile, never crossing a multiple of batch_len.
+    auto unit_next = [&](int64_t pi) -> int64_t {
+        if (!SMALL) return pi + 1;
+        int64_t e = pi + a.ps;
+        const int64_t row_end = (pi / a.batch_len + 1) * a.batch_len;
+        if (e > row_end) e = row_end;
+        return e < pre_hi ? e : pre_hi;
+    };
+    int64_t nunits = 0;
+    if (SMALL) {
+        for (int64_t pi = pre_lo; pi < pre_hi; pi = unit_next(pi)) ++nunits;
+    } else {
+        nunits = npi;
+    }
+    const int64_t T = nunits * KS;  // K-steps of this CTA
 
     if (warp == 0) {
         // ------------------------- TMA producer -------------------------
@@ -458,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                     ok = false;
                     break;
                 }
-                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; pi = unit_next(pi)) {
                     const int cP = (int)(pi / a.nQ);
                     const int cQ = (int)(pi - (int64_t)cP * a.nQ);
                     for (int q = 0; q < ck; ++q, ++issued, rr.next()) {
@@ -487,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
 #pragma unroll
                         for (int r = 0; r < kRoles; ++r)
                             if (a.slot[r] >= 0) c[a.slot[r]] = role[r];
-                        mbar_arrive_expect_tx(&raw_full[rr.slot], L::kY);
+                        mbar_arrive_expect_tx(&raw_full[rr.slot], a.y_box_bytes);
                         tma_load(&a.ymap, a.rank, c, raw + rr.slot * L::kY, &raw_full[rr.slot]);
                         if (b_pending && (issued + 1) % GS == 0) {
                             // the group is complete
@@ -528,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                     ok = false;
                     break;
                 }
-                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; pi = unit_next(pi)) {
                     for (int q = 0; q < ck; ++q, rr.next(), ++t) {
                         const bool first = (q % kChunkSteps) == 0;
                         const bool last = (q % kChunkSteps) == kChunkSteps - 1 || q == ck - 1;
@@ -650,87 +673,185 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
         }
     } else {
         // ---------------------- epilogue (16 warps) ----------------------
-        // warp w reads TMEM lanes 32 * (w % 4) .. + 31 (rows) and a quarter of
-        // the tile's columns.  The G(pi, :) row of the next (chunk, pi) pair is
-        // copied into the warp's second G buffer (cp.async, no registers) while
-        // the current pair is drained.
-        constexpr int kCols = BN / 4;
-        const int quad = warp & 3;
-        const int part = (warp - 4) >> 2;
-        const int64_t row = m0 + 32 * quad + lane;
-        const int64_t c0 = r0 + part * kCols;
-        float* gw = gsm + (warp - 4) * 2 * kCols;   // this warp's two G rows
-        float acc[kCols];
+        if constexpr (SMALL) {
+            // Tile row (TMEM lane) slot * I + i holds pre index pi_u + slot of the
+            // unit; each warp's lanes span at most kW slots.  G rows of the next
+            // unit are copied (cp.async) while the current one is drained; at the
+            // end the slots are summed through shared memory.
+            constexpr int kCols = BN / 4;
+            constexpr int kW = 3;
+            const int quad = warp & 3;
+            const int part = (warp - 4) >> 2;
+            const int64_t c0 = r0 + part * kCols;
+            const int Iv = (int)a.I;
+            const int lg = 32 * quad + lane;
+            const int slot = lg / Iv;
+            const int s_lo = (32 * quad) / Iv;
+            float* gw = gsm + (warp - 4) * 2 * kW * kCols;
+            float acc[kCols];
 #pragma unroll
-        for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
-        auto fetch_g = [&](int64_t pi, int buf) {
-            for (int e = lane; e < kCols; e += 32) {
-                const bool in = (c0 + e < a.R) && (pi < pre_hi);
-                const float* src = in ? a.gtab + pi * a.R + c0 + e : a.gtab;
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
-                                 smem_u32(gw + buf * kCols + e)),
-                             "l"(src), "r"(in ? 4 : 0)
-                             : "memory");
-            }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-        };
-        fetch_g(pre_lo, 0);
-        int gb = 0;           // G buffer of the current pair
-        int zb = 0;           // TMEM buffer of the next unit
-        uint32_t zph = 0;     // bit b: parity of the next completion of zfull[b]
-        bool ok = true;
-        for (int jc = 0; jc < njc && ok; ++jc) {
-            const int ck = chunk_len(jc);
-            for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
-                asm volatile("cp.async.wait_group 0;" ::: "memory");
-                __syncwarp();
-                fetch_g(pi + 1 < pre_hi ? pi + 1 : pre_lo, gb ^ 1);
-                const float* g_cur = gw + gb * kCols;
-                for (int q0 = 0; q0 < ck; q0 += kChunkSteps) {
-                    if (!warp_wait(&zfull[zb], (zph >> zb) & 1u, abort_flag, a.status,
-                                   kStatusTimeoutEpi)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t tbase =
-                        tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
-#pragma unroll
-                    for (int cc = 0; cc < kCols; cc += 8) {
-                        uint32_t z[8];
-                        tmem_ld8(tbase + cc, z);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const float4 g = *reinterpret_cast<const float4*>(g_cur + cc + 4 * q);
-                            acc[cc + 4 * q + 0] = fmaf(g.x, __uint_as_float(z[4 * q + 0]), acc[cc + 4 * q + 0]);
-                            acc[cc + 4 * q + 1] = fmaf(g.y, __uint_as_float(z[4 * q + 1]), acc[cc + 4 * q + 1]);
-                            acc[cc + 4 * q + 2] = fmaf(g.z, __uint_as_float(z[4 * q + 2]), acc[cc + 4 * q + 2]);
-                            acc[cc + 4 * q + 3] = fmaf(g.w, __uint_as_float(z[4 * q + 3]), acc[cc + 4 * q + 3]);
-                        }
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&zempty[zb]);
-                    zph ^= 1u << zb;
-                    zb ^= 1;
+            for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
+            auto fetch_g = [&](int64_t pu, int buf) {
+                const int64_t pe = unit_next(pu);
+                for (int e = lane; e < kW * kCols; e += 32) {
+                    const int w = e / kCols, c = e - w * kCols;
+                    const int64_t pi = pu + s_lo + w;
+                    const bool in = (pi < pe) && (s_lo + w < a.ps) && (c0 + c < a.R);
+                    const float* src = in ? a.gtab + pi * a.R + c0 + c : a.gtab;
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                                     smem_u32(gw + buf * kW * kCols + e)),
+                                 "l"(src), "r"(in ? 4 : 0)
+                                 : "memory");
                 }
-                gb ^= 1;
+                asm volatile("cp.async.commit_group;" ::: "memory");
+            };
+            fetch_g(pre_lo, 0);
+            int gb = 0;
+            int zb = 0;
+            uint32_t zph = 0;
+            bool ok = true;
+            for (int jc = 0; jc < njc && ok; ++jc) {
+                const int ck = chunk_len(jc);
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; pi = unit_next(pi)) {
+                    asm volatile("cp.async.wait_group 0;" ::: "memory");
+                    __syncwarp();
+                    const int64_t pn = unit_next(pi);
+                    fetch_g(pn < pre_hi ? pn : pre_lo, gb ^ 1);
+                    const int srow = slot - s_lo < kW ? slot - s_lo : kW - 1;
+                    const float* g_cur = gw + gb * kW * kCols + srow * kCols;
+                    for (int q0 = 0; q0 < ck; q0 += kChunkSteps) {
+                        if (!warp_wait(&zfull[zb], (zph >> zb) & 1u, abort_flag, a.status,
+                                       kStatusTimeoutEpi)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t tbase =
+                            tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
+#pragma unroll
+                        for (int cc = 0; cc < kCols; cc += 8) {
+                            uint32_t z[8];
+                            tmem_ld8(tbase + cc, z);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                acc[cc + q] = fmaf(g_cur[cc + q], __uint_as_float(z[q]), acc[cc + q]);
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&zempty[zb]);
+                        zph ^= 1u << zb;
+                        zb ^= 1;
+                    }
+                    gb ^= 1;
+                }
             }
-        }
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        if (!*abort_flag && row < a.I) {
-            float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride + row * a.R + c0;
-            const bool vst = (a.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.dst) & 15) == 0);
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            // sum the slots: rows slot * I + i of a [128][BN + 4] buffer over the
+            // (now idle) B-chunk and stage area
+            constexpr int kSP = BN + 4;
+            float* S = reinterpret_cast<float*>(smem);
+            const bool live = !*abort_flag;
+            if (live) {
 #pragma unroll
-            for (int e = 0; e < kCols; e += 4) {
-                if (vst && c0 + e + 4 <= a.R) {
-                    *reinterpret_cast<float4*>(dst + e) =
+                for (int e = 0; e < kCols; e += 4)
+                    *reinterpret_cast<float4*>(S + lg * kSP + part * kCols + e) =
                         make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
-                } else {
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+            if (live) {
+                float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride;
+                for (int idx = tid - 128; idx < Iv * BN; idx += kEpiWarps * 32) {
+                    const int i = idx / BN, c = idx - i * BN;
+                    if (r0 + c >= a.R) continue;
+                    float sum = 0.f;
+                    for (int sl = 0; sl < a.ps; ++sl) sum += S[(sl * Iv + i) * kSP + c];
+                    dst[(int64_t)i * a.R + r0 + c] = sum;
+                }
+            }
+        } else {
+            // warp w reads TMEM lanes 32 * (w % 4) .. + 31 (rows) and a quarter of
+            // the tile's columns.  The G(pi, :) row of the next (chunk, pi) pair is
+            // copied into the warp's second G buffer (cp.async, no registers) while
+            // the current pair is drained.
+            constexpr int kCols = BN / 4;
+            const int quad = warp & 3;
+            const int part = (warp - 4) >> 2;
+            const int64_t row = m0 + 32 * quad + lane;
+            const int64_t c0 = r0 + part * kCols;
+            float* gw = gsm + (warp - 4) * 2 * kCols;   // this warp's two G rows
+            float acc[kCols];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (c0 + e + q < a.R) dst[e + q] = acc[e + q];
+            for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
+            auto fetch_g = [&](int64_t pi, int buf) {
+                for (int e = lane; e < kCols; e += 32) {
+                    const bool in = (c0 + e < a.R) && (pi < pre_hi);
+                    const float* src = in ? a.gtab + pi * a.R + c0 + e : a.gtab;
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                                     smem_u32(gw + buf * kCols + e)),
+                                 "l"(src), "r"(in ? 4 : 0)
+                                 : "memory");
+                }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+            };
+            fetch_g(pre_lo, 0);
+            int gb = 0;           // G buffer of the current pair
+            int zb = 0;           // TMEM buffer of the next unit
+            uint32_t zph = 0;     // bit b: parity of the next completion of zfull[b]
+            bool ok = true;
+            for (int jc = 0; jc < njc && ok; ++jc) {
+                const int ck = chunk_len(jc);
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                    asm volatile("cp.async.wait_group 0;" ::: "memory");
+                    __syncwarp();
+                    fetch_g(pi + 1 < pre_hi ? pi + 1 : pre_lo, gb ^ 1);
+                    const float* g_cur = gw + gb * kCols;
+                    for (int q0 = 0; q0 < ck; q0 += kChunkSteps) {
+                        if (!warp_wait(&zfull[zb], (zph >> zb) & 1u, abort_flag, a.status,
+                                       kStatusTimeoutEpi)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t tbase =
+                            tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
+#pragma unroll
+                        for (int cc = 0; cc < kCols; cc += 8) {
+                            uint32_t z[8];
+                            tmem_ld8(tbase + cc, z);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int q = 0; q < 2; ++q) {
+                                const float4 g = *reinterpret_cast<const float4*>(g_cur + cc + 4 * q);
+                                acc[cc + 4 * q + 0] = fmaf(g.x, __uint_as_float(z[4 * q + 0]), acc[cc + 4 * q + 0]);
+                                acc[cc + 4 * q + 1] = fmaf(g.y, __uint_as_float(z[4 * q + 1]), acc[cc + 4 * q + 1]);
+                                acc[cc + 4 * q + 2] = fmaf(g.z, __uint_as_float(z[4 * q + 2]), acc[cc + 4 * q + 2]);
+                                acc[cc + 4 * q + 3] = fmaf(g.w, __uint_as_float(z[4 * q + 3]), acc[cc + 4 * q + 3]);
+                            }
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&zempty[zb]);
+                        zph ^= 1u << zb;
+                        zb ^= 1;
+                    }
+                    gb ^= 1;
+                }
+            }
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            if (!*abort_flag && row < a.I) {
+                float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride + row * a.R + c0;
+                const bool vst = (a.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.dst) & 15) == 0);
+#pragma unroll
+                for (int e = 0; e < kCols; e += 4) {
+                    if (vst && c0 + e + 4 <= a.R) {
+                        *reinterpret_cast<float4*>(dst + e) =
+                            make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (c0 + e + q < a.R) dst[e + q] = acc[e + q];
+                    }
                 }
             }
         }
@@ -870,7 +991,9 @@ bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides,
     }
     if (sizeP > 1) dl[n++] = {kRolePP, sizeP, strideP};
     if (sizeQ > 1) dl[n++] = {kRolePQ, sizeQ, strideQ};
-    // the innermost (stride-1) dimension first, the others by increasing stride
+    // the innermost (stride-1) dimension first, the others by increasing stride;
+    // the small-I variant keeps (j, i, batch) as the first three dimensions so
+    // that the tile rows come out as slot * I + i
     int first = -1;
     for (int t = 0; t < n; ++t)
         if (dl[t].stride == 1) first = t;
@@ -878,7 +1001,22 @@ bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides,
     Dim tmp = dl[0];
     dl[0] = dl[first];
     dl[first] = tmp;
-    for (int t = 1; t < n; ++t)
+    int fixed = 1;
+    if (mp.tc_small) {
+        const int batch_role = sizeQ > 1 ? kRolePQ : kRolePP;
+        for (int want : {(int)kRoleI, batch_role}) {
+            for (int t = fixed; t < n; ++t)
+                if (dl[t].role == want) {
+                    tmp = dl[fixed];
+                    dl[fixed] = dl[t];
+                    dl[t] = tmp;
+                    ++fixed;
+                    break;
+                }
+        }
+        if (fixed != 3) return false;
+    }
+    for (int t = fixed; t < n; ++t)
         for (int u = t + 1; u < n; ++u)
             if (dl[u].stride < dl[t].stride) {
                 tmp = dl[t];
@@ -904,7 +1042,15 @@ bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides,
     } else {
         if (mg.slot[kRoleJq] != 0) return false;
         mg.box[0] = kBK;
-        mg.box[mg.slot[kRoleI]] = kBM;
+        if (mp.tc_small) {
+            // tc_ps consecutive pre indices along the fastest pre dimension
+            const int batch_role = sizeQ > 1 ? kRolePQ : kRolePP;
+            if (mg.slot[batch_role] < 0 || mp.tc_ps < 2 || mp.tc_ps > 256) return false;
+            mg.box[mg.slot[kRoleI]] = (uint32_t)g.I;
+            mg.box[mg.slot[batch_role]] = (uint32_t)mp.tc_ps;
+        } else {
+            mg.box[mg.slot[kRoleI]] = kBM;
+        }
     }
     return true;
 }
@@ -922,21 +1068,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <int BN, bool INNER>
+template <int BN, bool INNER, bool SMALL = false>
 cudaError_t launch_main(const TcArgs& args, dim3 grid, cudaStream_t s) {
-    using L = Smem<BN, INNER>;
+    using L = Smem<BN, INNER, SMALL>;
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaError_t e0 = cudaGetDevice(&dev);
     if (e0 != cudaSuccess) return e0;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc_mttkrp_kernel<BN, INNER>,
+        cudaError_t e = cudaFuncSetAttribute(tc_mttkrp_kernel<BN, INNER, SMALL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kTotal);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    tc_mttkrp_kernel<BN, INNER><<<grid, kThreads, L::kTotal, s>>>(args);
+    tc_mttkrp_kernel<BN, INNER, SMALL><<<grid, kThreads, L::kTotal, s>>>(args);
     return cudaGetLastError();
 }
 
@@ -944,20 +1090,29 @@ size_t bimg_bytes(const ModePlan& mp) {
     return (size_t)cdiv64(mp.g.R, mp.bn) * mp.tc_ks * 2 * (size_t)mp.bn * kBK * sizeof(float);
 }
 
+// Small I_k (16..64) with a K-major Y tile: floor(128 / I_k) pre indices are
+// stacked in one 128-row tile.
+bool small_eligible(const ModeGeom& g) {
+    return g.s_k != 1 && g.I >= 16 && g.I <= 64 && g.npre >= 2;
+}
+
 }  // namespace
 
 size_t tc_binner_bytes(const ModePlan& mp) { return bimg_bytes(mp); }
 
 bool tc_prefer(const ModePlan& mp) {
-    // the 128-row tile must be reasonably full and the rank large enough for
-    // the tensor-core products to pay off
-    return mp.g.I >= 96 && mp.g.R >= 32;
+    // the 128-row tile must be reasonably full (directly, or with several pre
+    // indices stacked in it for small I_k) and the rank large enough for the
+    // tensor-core products to pay off
+    return mp.g.R >= 32 && (mp.g.I >= 96 || small_eligible(mp.g));
 }
 
 bool tc_plan(const Plan& p, ModePlan& mp) {
     const ModeGeom& g = mp.g;
     mp.path = MTTKRP_PATH_TC;
     mp.tc_inner = (g.s_k == 1) ? 1 : 0;
+    mp.tc_small = small_eligible(g) ? 1 : 0;
+    mp.tc_ps = mp.tc_small ? (int)(kBM / g.I) : 1;
     mp.bm = kBM;
     mp.bn = g.R >= 192 ? 256 : (g.R > 64 ? 128 : 64);
     if (mp.tc_inner) {
@@ -968,12 +1123,12 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
         mp.tc_jq_steps = (int)cdiv64(g.Jq, kBK);
         mp.tc_ks = (int)((g.J / g.Jq) * mp.tc_jq_steps);
     }
-    if (cdiv64(g.I, kBM) > 65535 || g.npre >= ((int64_t)1 << 31)) return false;
+    if ((!mp.tc_small && cdiv64(g.I, kBM) > 65535) || g.npre >= ((int64_t)1 << 31)) return false;
     MapGeom mg;
     if (!y_map_geom(mp, p.dims, p.strides, p.d, mg)) return false;
     // split count: fill whole waves of one CTA per SM, at least two drain
     // chunks per CTA where possible
-    const int64_t tiles = cdiv64(g.I, kBM) * cdiv64(g.R, mp.bn);
+    const int64_t tiles = (mp.tc_small ? 1 : cdiv64(g.I, kBM)) * cdiv64(g.R, mp.bn);
     const int64_t sms = sm_count();
     const int64_t smax = g.npre;
     int64_t best = 1;
@@ -1079,6 +1234,9 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     args.nQ = nQ;
     args.KS = mp.tc_ks;
     args.jq_steps = mp.tc_jq_steps;
+    args.ps = mp.tc_small ? mp.tc_ps : 1;
+    args.batch_len = nQ > 1 ? nQ : g.npre;
+    args.y_box_bytes = (uint32_t)kBK * 4u * (mp.tc_small ? (uint32_t)(g.I * mp.tc_ps) : (uint32_t)kBM);
     {
         int n = g_withhold_signal.load();
         while (n > 0 && !g_withhold_signal.compare_exchange_weak(n, n - 1)) {
@@ -1091,9 +1249,14 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
         return MTTKRP_ERR_CUDA;
     }
     if (start_ev) cudaEventRecord(*start_ev, stream);
-    dim3 grid((unsigned)cdiv64(g.R, mp.bn), (unsigned)cdiv64(g.I, kBM), (unsigned)mp.splits);
+    dim3 grid((unsigned)cdiv64(g.R, mp.bn), mp.tc_small ? 1u : (unsigned)cdiv64(g.I, kBM),
+              (unsigned)mp.splits);
     cudaError_t e;
-    if (mp.tc_inner) {
+    if (mp.tc_small) {
+        e = mp.bn == 256 ? launch_main<256, false, true>(args, grid, stream)
+          : mp.bn == 128 ? launch_main<128, false, true>(args, grid, stream)
+                         : launch_main<64, false, true>(args, grid, stream);
+    } else if (mp.tc_inner) {
         e = mp.bn == 256 ? launch_main<256, true>(args, grid, stream)
           : mp.bn == 128 ? launch_main<128, true>(args, grid, stream)
                          : launch_main<64, true>(args, grid, stream);

@@ -141,6 +141,11 @@ EDGE = [
     ((128, 128, 64), 17),
     ((96, 40, 36), 1000),
     ((160, 4, 4, 4, 4), 48),
+    # small I_k: several pre indices stacked in one 128-row tensor-core tile
+    ((24, 30, 40, 16), 96),
+    ((16, 64, 40), 200),
+    ((60, 8, 8, 36), 64),
+    ((17, 33, 48), 130),
 ]
 
 
