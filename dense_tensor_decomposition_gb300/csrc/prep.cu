@@ -39,42 +39,56 @@ cudaError_t launch_prod_table(const ProdTableArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// out[e] = (float) sum_{s=0}^{splits-1} (double) part[s * n + e], s in increasing order.
-__global__ void reduce_splits_kernel(const float* __restrict__ part, int64_t splits, int64_t n,
-                                     float* __restrict__ out) {
-    const bool vec = (n % 4 == 0) && ((reinterpret_cast<uintptr_t>(part) & 15) == 0) &&
-                     ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    if (vec) {
-        const int64_t n4 = n / 4;
-        for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n4; e += stride) {
-            double s0 = 0.0, s1 = 0.0, s2 = 0.0, s3 = 0.0;
-            for (int64_t sp = 0; sp < splits; ++sp) {
-                const float4 v = __ldcs(reinterpret_cast<const float4*>(part + sp * n) + e);
-                s0 += (double)v.x;
-                s1 += (double)v.y;
-                s2 += (double)v.z;
-                s3 += (double)v.w;
+// out[e] = (float) sum over s of (double) part[s * n + e], summed in a fixed order
+// that depends only on (splits, n): each block owns 32 consecutive outputs (one
+// per lane); warp w adds the partials of splits [w*S/8, (w+1)*S/8) in
+// increasing s; the eight warp sums are then added in warp order.  The result
+// is therefore bitwise reproducible, and the S loads are spread over 8 warps
+// instead of one serial loop per output.
+constexpr int kRedWarps = 8;
+
+__global__ void __launch_bounds__(kRedWarps * 32)
+    reduce_splits_kernel(const float* __restrict__ part, int64_t splits, int64_t n,
+                         float* __restrict__ out) {
+    __shared__ double sums[kRedWarps][32];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int64_t s0 = splits * warp / kRedWarps;
+    const int64_t s1 = splits * (warp + 1) / kRedWarps;
+    for (int64_t base = (int64_t)blockIdx.x * 32; base < n; base += (int64_t)gridDim.x * 32) {
+        const int64_t e = base + lane;
+        double acc = 0.0;
+        if (e < n) {
+            const float* p = part + s0 * n + e;
+            int64_t sp = s0;
+            // four independent loads in flight, added in split order
+            for (; sp + 4 <= s1; sp += 4, p += 4 * n) {
+                const float a0 = __ldcs(p), a1 = __ldcs(p + n), a2 = __ldcs(p + 2 * n), a3 = __ldcs(p + 3 * n);
+                acc += (double)a0;
+                acc += (double)a1;
+                acc += (double)a2;
+                acc += (double)a3;
             }
-            reinterpret_cast<float4*>(out)[e] = make_float4((float)s0, (float)s1, (float)s2, (float)s3);
+            for (; sp < s1; ++sp, p += n) acc += (double)__ldcs(p);
         }
-    } else {
-        for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += stride) {
-            double acc = 0.0;
-            for (int64_t sp = 0; sp < splits; ++sp) acc += (double)__ldcs(part + sp * n + e);
-            out[e] = (float)acc;
+        sums[warp][lane] = acc;
+        __syncthreads();
+        if (warp == 0 && e < n) {
+            double t = 0.0;
+#pragma unroll
+            for (int w = 0; w < kRedWarps; ++w) t += sums[w][lane];
+            out[e] = (float)t;
         }
+        __syncthreads();
     }
 }
 
 cudaError_t launch_reduce_splits(const float* part, int64_t splits, int64_t n, float* out,
                                  cudaStream_t s) {
     if (n == 0) return cudaSuccess;
-    const int threads = 256;
-    int64_t work = (n % 4 == 0) ? n / 4 : n;
-    int64_t blocks = (work + threads - 1) / threads;
-    if (blocks > 152 * 8) blocks = 152 * 8;
-    reduce_splits_kernel<<<(unsigned)blocks, threads, 0, s>>>(part, splits, n, out);
+    int64_t blocks = (n + 31) / 32;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    reduce_splits_kernel<<<(unsigned)blocks, kRedWarps * 32, 0, s>>>(part, splits, n, out);
     return cudaGetLastError();
 }
 

@@ -360,7 +360,6 @@ struct Ring {
 
 template <int BN, bool INNER, bool SMALL>
 __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_constant__ TcArgs a) {
-    static_assert(!(SMALL && INNER), "the small-I variant needs a K-major Y tile");
     using L = Smem<BN, INNER, SMALL>;
     constexpr int CK = L::kCK;
     constexpr int NR = L::kRaw;
@@ -632,6 +631,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                     const int e = ptid + 64 * v;
                     const float4 x = src[e];
                     dst[e] = make_float4(tf32_lo(x.x), tf32_lo(x.y), tf32_lo(x.z), tf32_lo(x.w));
+                }
+            } else if (SMALL) {
+                // staging tile is [ps][16 j][I i] (i contiguous): transpose into
+                // K-major hi and lo rows slot * I + i; one 16-byte chunk (4 j) per
+                // item, i fastest across lanes (consecutive loads, and the stores
+                // of 8 consecutive rows hit 8 distinct bank groups)
+                const float* stg = reinterpret_cast<const float*>(st);
+                uint8_t* hi = op;
+                uint8_t* lo = op + L::kA;
+                const int Iv = (int)a.I;
+                const int items = a.ps * Iv * 4;
+                for (int u = ptid; u < items; u += 64) {
+                    const int i = u % Iv;
+                    const int rest = u / Iv;
+                    const int jc = rest & 3;
+                    const int sl = rest >> 2;
+                    const float* src = stg + (sl * kBK + 4 * jc) * Iv + i;
+                    const float4 r = make_float4(src[0], src[Iv], src[2 * Iv], src[3 * Iv]);
+                    const uint32_t off = sw64_off((uint32_t)(sl * Iv + i), (uint32_t)jc);
+                    *reinterpret_cast<float4*>(hi + off) = r;
+                    *reinterpret_cast<float4*>(lo + off) =
+                        make_float4(tf32_lo(r.x), tf32_lo(r.y), tf32_lo(r.z), tf32_lo(r.w));
                 }
             } else {
                 // staging tile is [16 j][128 i] (i contiguous): transpose into the
@@ -1004,7 +1025,9 @@ bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides,
     int fixed = 1;
     if (mp.tc_small) {
         const int batch_role = sizeQ > 1 ? kRolePQ : kRolePP;
-        for (int want : {(int)kRoleI, batch_role}) {
+        // K-major: (j, i, batch); innermost mode: (i, j, batch)
+        const int second = mp.tc_inner ? (int)kRoleJq : (int)kRoleI;
+        for (int want : {second, batch_role}) {
             for (int t = fixed; t < n; ++t)
                 if (dl[t].role == want) {
                     tmp = dl[fixed];
@@ -1036,9 +1059,17 @@ bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides,
         mg.box[t] = 1;
     }
     if (mp.tc_inner) {
-        mg.box[mg.slot[kRoleI]] = kBM;   // slot 0: i contiguous
+        if (mg.slot[kRoleI] != 0) return false;   // i contiguous
         mg.box[mg.slot[kRoleJq]] = kBK;
-        if (mg.slot[kRoleI] != 0) return false;
+        if (mp.tc_small) {
+            const int batch_role = sizeQ > 1 ? kRolePQ : kRolePP;
+            if (mg.slot[batch_role] < 0 || mp.tc_ps < 2 || mp.tc_ps > 256 || (g.I * 4) % 16 != 0)
+                return false;
+            mg.box[0] = (uint32_t)g.I;
+            mg.box[mg.slot[batch_role]] = (uint32_t)mp.tc_ps;
+        } else {
+            mg.box[0] = kBM;
+        }
     } else {
         if (mg.slot[kRoleJq] != 0) return false;
         mg.box[0] = kBK;
@@ -1090,10 +1121,11 @@ size_t bimg_bytes(const ModePlan& mp) {
     return (size_t)cdiv64(mp.g.R, mp.bn) * mp.tc_ks * 2 * (size_t)mp.bn * kBK * sizeof(float);
 }
 
-// Small I_k (16..64) with a K-major Y tile: floor(128 / I_k) pre indices are
-// stacked in one 128-row tile.
+// Small I_k (16..64): floor(128 / I_k) pre indices are stacked in one 128-row
+// tile (for the innermost mode the TMA box's i extent, I_k * 4 bytes, must be a
+// multiple of 16).
 bool small_eligible(const ModeGeom& g) {
-    return g.s_k != 1 && g.I >= 16 && g.I <= 64 && g.npre >= 2;
+    return g.I >= 16 && g.I <= 64 && g.npre >= 2 && (g.s_k != 1 || g.I % 4 == 0);
 }
 
 }  // namespace
@@ -1252,7 +1284,11 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     dim3 grid((unsigned)cdiv64(g.R, mp.bn), mp.tc_small ? 1u : (unsigned)cdiv64(g.I, kBM),
               (unsigned)mp.splits);
     cudaError_t e;
-    if (mp.tc_small) {
+    if (mp.tc_small && mp.tc_inner) {
+        e = mp.bn == 256 ? launch_main<256, true, true>(args, grid, stream)
+          : mp.bn == 128 ? launch_main<128, true, true>(args, grid, stream)
+                         : launch_main<64, true, true>(args, grid, stream);
+    } else if (mp.tc_small) {
         e = mp.bn == 256 ? launch_main<256, false, true>(args, grid, stream)
           : mp.bn == 128 ? launch_main<128, false, true>(args, grid, stream)
                          : launch_main<64, false, true>(args, grid, stream);

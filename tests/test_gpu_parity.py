@@ -146,6 +146,12 @@ EDGE = [
     ((16, 64, 40), 200),
     ((60, 8, 8, 36), 64),
     ((17, 33, 48), 130),
+    # small I_k in the innermost mode (I_k * 4 bytes a multiple of 16): the
+    # staging box holds several pre indices and is transposed into one tile
+    ((30, 40, 20), 96),
+    ((12, 50, 36), 64),
+    ((7, 9, 11, 44), 130),
+    ((5, 6, 40, 28), 260),
 ]
 
 
