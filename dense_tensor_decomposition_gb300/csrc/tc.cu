@@ -227,25 +227,31 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 
 // K-major, 64-byte swizzle shared-memory matrix descriptor: 8-row groups of
 // 64-byte rows, 512 bytes apart.  Everything but the start-address field is
-// constant.
+// constant (kDescSw64Hi holds those fields).
 constexpr uint64_t kDescSw64Hi = ((uint64_t)1 << 16)           // leading byte offset (unused)
                                | ((uint64_t)(512 >> 4) << 32)  // stride byte offset: 8 rows x 64 B
                                | ((uint64_t)1 << 46)           // descriptor version
                                | ((uint64_t)4 << 61);          // 64-byte swizzle
 
-__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
-    return kDescSw64Hi | (uint64_t)((saddr & 0x3FFFFu) >> 4);
+// Low 32 bits of the descriptor above (start address and leading byte offset);
+// the high word is the constant kDescSw64Hi >> 32.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr) {
+    return (uint32_t)kDescSw64Hi | ((saddr & 0x3FFFFu) >> 4);
 }
 
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t acc) {
+// D (+)= A * B, kind::tf32; a and b are descriptor low words (high word constant)
+__device__ __forceinline__ void mma_tf32_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                           uint32_t acc) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %3};\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], da, db, %4, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"((uint32_t)(kDescSw64Hi >> 32)), "r"(idesc), "r"(acc));
 }
 
+// arrive on `bar` once all previously issued MMAs of this thread have completed
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
@@ -266,6 +272,31 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                    "=r"(r[6]), "=r"(r[7])
                  : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+// N consecutive TMEM columns of the warp's 32 lanes (one register per column)
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
+    if constexpr (N == 32) {
+        tmem_ld32(taddr, r);
+    } else if constexpr (N == 16) {
+        tmem_ld16(taddr, r);
+    } else {
+        static_assert(N == 8, "8, 16 or 32 columns");
+        tmem_ld8(taddr, r);
+    }
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {
@@ -290,9 +321,6 @@ __device__ __forceinline__ uint32_t sw64_off(uint32_t row, uint32_t chunk) {
 // CTA walks all of its pi, streaming only Y tiles.  TMEM is drained after every
 // "unit" of at most kChunkSteps K-steps of one (chunk, pi) pair.
 
-#ifndef TC_GROUP
-#define TC_GROUP 1
-#endif
 #ifndef TC_STAGES
 #define TC_STAGES 5
 #endif
@@ -301,6 +329,9 @@ __device__ __forceinline__ uint32_t sw64_off(uint32_t row, uint32_t chunk) {
 #endif
 #ifndef TC_BRES_KB
 #define TC_BRES_KB 128
+#endif
+#ifndef TC_EPI_LD
+#define TC_EPI_LD 8
 #endif
 #ifndef TC_BRES_INNER_KB
 #define TC_BRES_INNER_KB 128
@@ -314,9 +345,8 @@ struct Smem {
     static constexpr uint32_t kBRes =
         (uint32_t)(SMALL ? 96 : INNER ? TC_BRES_INNER_KB : TC_BRES_KB) * 1024;  // resident B-chunk
     static constexpr int kCK = (int)(kBRes / (2 * kB));  // K-steps per B-chunk
-    // stages (raw Y tile + on-chip operand tile(s)), consumed in groups of
-    // kGroup: one producer arrival, one MMA wait and one MMA commit per group
-    static constexpr int kGroup = TC_GROUP;
+    // stages: raw Y tile + on-chip operand tile(s); one producer arrival, one
+    // MMA wait and one MMA commit per stage
     static constexpr int kRaw = INNER ? TC_STAGES_INNER : TC_STAGES;
     static constexpr int kOps = kRaw;
     static constexpr uint32_t kOp = INNER ? 2 * kA : kA;  // lo (and transposed hi if INNER)
@@ -330,7 +360,7 @@ struct Smem {
     static constexpr uint32_t kTotal = 1024 + kOffBars + kBarBytes;
     static_assert(kTotal <= 232448, "shared memory budget");
     static_assert(!SMALL || (uint32_t)(kBM * (BN + 4) * 4) <= kOffG, "slot-reduction buffer must fit");
-    static_assert((kRaw + 2 * (kRaw / kGroup) + 7) * 8 + 8 <= kBarBytes, "barrier area");
+    static_assert((3 * kRaw + 7) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
 // warp-uniform bounded wait: lane 0 waits, the result is broadcast
@@ -373,14 +403,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
     float* gsm = reinterpret_cast<float*>(smem + L::kOffG);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBars);
     // stage s holds raw Y tile s and operand tile s; K-step t uses stage t % NR
-    // and group (t / GS) % NP
-    constexpr int GS = L::kGroup;
-    static_assert(NR == NO && NR % GS == 0, "stages come in whole groups");
-    constexpr int NP = NR / GS;
+    static_assert(NR == NO, "one operand tile per stage");
     uint64_t* raw_full = bars;                  // [NR] TMA landed
-    uint64_t* op_full = raw_full + NR;          // [NP] producers wrote the pair's operand tiles
-    uint64_t* stage_empty = op_full + NP;       // [NP] MMAs that read the pair are done
-    uint64_t* zfull = stage_empty + NP;         // [2]
+    uint64_t* op_full = raw_full + NR;          // [NR] producers wrote the stage's operand tiles
+    uint64_t* stage_empty = op_full + NR;       // [NR] MMAs that read the stage are done
+    uint64_t* zfull = stage_empty + NR;         // [2]
     uint64_t* zempty = zfull + 2;               // [2]
     uint64_t* bfull = zempty + 2;               // [1]
     uint64_t* bempty = bfull + 1;               // [1]
@@ -403,8 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
     constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : 2 * BN;
 
     if (tid == 0) {
-        for (int s = 0; s < NR; ++s) mbar_init(&raw_full[s], 1);
-        for (int s = 0; s < NP; ++s) {
+        for (int s = 0; s < NR; ++s) {
+            mbar_init(&raw_full[s], 1);
             mbar_init(&op_full[s], 2);
             mbar_init(&stage_empty[s], 1);
         }
@@ -450,7 +477,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
         if (lane == 0) {
             const uint8_t* bimg = reinterpret_cast<const uint8_t*>(a.bimg);
             Ring<NR> rr;
-            Ring<NP> pr;
             int64_t issued = 0;
             int jc_loaded = -1;
             bool ok = true;
@@ -472,27 +498,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
             };
             for (int jc = 0; jc < njc && ok; ++jc) {
                 const int ck = chunk_len(jc);
-                // A chunk boundary inside a stage pair: the MMA issuer waits for the
-                // whole pair before it finishes chunk jc - 1, so the pair's second
-                // Y tile is issued before the chunk swap (which waits for those MMAs).
-                bool b_pending = (jc > 0) && (issued % GS != 0);
-                if (!b_pending && !load_b(jc)) {
-                    ok = false;
-                    break;
-                }
+                // The first NR Y tiles of chunk jc only need stages freed by the
+                // MMAs of chunk jc - 1, so they are issued before the chunk swap
+                // (which waits for those MMAs); later ones need chunk jc's MMAs.
+                const int64_t swap_at = issued + NR;
+                bool b_pending = true;
                 for (int64_t pi = pre_lo; pi < pre_hi && ok; pi = unit_next(pi)) {
                     const int cP = (int)(pi / a.nQ);
                     const int cQ = (int)(pi - (int64_t)cP * a.nQ);
                     for (int q = 0; q < ck; ++q, ++issued, rr.next()) {
-                        const int ks = jc * CK + q;
-                        if (issued % GS == 0) {
-                            if (issued > 0) pr.next();
-                            if (pr.reused && !wait_bounded(&stage_empty[pr.slot], pr.phase ^ 1u,
-                                                           abort_flag, a.status, kStatusTimeoutTma)) {
+                        if (b_pending && issued == swap_at) {
+                            b_pending = false;
+                            if (!load_b(jc)) {
                                 ok = false;
                                 break;
                             }
                         }
+                        if (rr.reused && !wait_bounded(&stage_empty[rr.slot], rr.phase ^ 1u, abort_flag,
+                                                       a.status, kStatusTimeoutTma)) {
+                            ok = false;
+                            break;
+                        }
+                        const int ks = jc * CK + q;
                         int role[kRoles];
                         if (INNER) {
                             role[kRoleJq] = ks * kBK;
@@ -511,18 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                             if (a.slot[r] >= 0) c[a.slot[r]] = role[r];
                         mbar_arrive_expect_tx(&raw_full[rr.slot], a.y_box_bytes);
                         tma_load(&a.ymap, a.rank, c, raw + rr.slot * L::kY, &raw_full[rr.slot]);
-                        if (b_pending && (issued + 1) % GS == 0) {
-                            // the group is complete
-                            b_pending = false;
-                            if (!load_b(jc)) {
-                                ok = false;
-                                ++issued;
-                                rr.next();
-                                break;
-                            }
-                        }
                     }
                 }
+                if (ok && b_pending && !load_b(jc)) ok = false;
             }
             // wait (bounded) for copies still in flight before leaving
             for (int64_t u = issued - 1; u >= 0 && u >= issued - NR; --u)
@@ -531,15 +549,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
         }
     } else if (warp == 1) {
         // ------------------------- MMA issuer -------------------------
+        // One thread issues.  Its per-K-step instruction latency bounds the
+        // tensor pipe's duty cycle (six MMAs of BN / 2 cycles each per step), so
+        // the loop is kept short: one wait and one commit per stage, and the
+        // descriptors' low words advance incrementally (high word constant).
         if (lane == 0) {
             const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
                                    ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
             const uint32_t raw_s = smem_u32(raw);
             const uint32_t ops_s = smem_u32(ops);
-            const uint32_t bres_s = smem_u32(bres);
-            Ring<NR> rr;
-            Ring<NP> pr;
-            int64_t t = 0;       // K-steps issued
+            const uint32_t a_hi0 = sdesc_lo(INNER ? ops_s : raw_s);
+            const uint32_t a_lo0 = sdesc_lo(INNER ? ops_s + L::kA : ops_s);
+            constexpr uint32_t kAhiStep = (INNER ? L::kOp : L::kY) >> 4;
+            constexpr uint32_t kAloStep = L::kOp >> 4;
+            const uint32_t b_w0 = sdesc_lo(smem_u32(bres));
+            constexpr uint32_t kBStep = (2 * L::kB) >> 4;   // one K-step of the B-chunk
+            constexpr uint32_t kBLo = L::kB >> 4;           // lo image after the hi image
+            int slot = 0;
+            uint32_t phase = 0;
+            uint32_t ahi = a_hi0, alo = a_lo0;
             int zb = 0;          // TMEM buffer of the current unit
             uint32_t zph = 0;    // bit b: parity of the next release of buffer b
             uint32_t zused = 0;  // bit b: buffer b was used before
@@ -551,9 +579,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                     break;
                 }
                 for (int64_t pi = pre_lo; pi < pre_hi && ok; pi = unit_next(pi)) {
-                    for (int q = 0; q < ck; ++q, rr.next(), ++t) {
-                        const bool first = (q % kChunkSteps) == 0;
-                        const bool last = (q % kChunkSteps) == kChunkSteps - 1 || q == ck - 1;
+                    uint32_t bw = b_w0;
+                    for (int q = 0; q < ck; ++q, bw += kBStep) {
+                        const int qq = q % kChunkSteps;
+                        const bool first = qq == 0;
+                        const bool last = qq == kChunkSteps - 1 || q == ck - 1;
                         if (first && ((zused >> zb) & 1u)) {
                             // the epilogue has read this TMEM buffer's previous contents
                             if (!wait_bounded(&zempty[zb], (zph >> zb) & 1u, abort_flag, a.status,
@@ -563,33 +593,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                             }
                             tc_fence_after();
                         }
-                        // the producers arrive only after the pair's TMA copies landed, so
-                        // one wait per pair covers all four tiles
-                        if (t % GS == 0) {
-                            if (t > 0) pr.next();
-                            if (!wait_bounded(&op_full[pr.slot], pr.phase, abort_flag, a.status,
-                                              kStatusTimeoutMma)) {
-                                ok = false;
-                                break;
-                            }
+                        // the producers arrive only after the stage's TMA copy landed
+                        if (!wait_bounded(&op_full[slot], phase, abort_flag, a.status, kStatusTimeoutMma)) {
+                            ok = false;
+                            break;
                         }
-                        const uint32_t op = ops_s + (uint32_t)rr.slot * L::kOp;
-                        const uint32_t a_hi = INNER ? op : raw_s + (uint32_t)rr.slot * L::kY;
-                        const uint32_t a_lo = INNER ? op + L::kA : op;
-                        const uint32_t b_hi = bres_s + (uint32_t)q * 2u * L::kB;
-                        const uint64_t dah = sdesc_sw64(a_hi);
-                        const uint64_t dal = sdesc_sw64(a_lo);
-                        const uint64_t dbh = sdesc_sw64(b_hi);
-                        const uint64_t dbl = sdesc_sw64(b_hi + L::kB);
                         const uint32_t dz = tmem + (uint32_t)(zb * BN);
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
-                            const uint64_t adv = (uint64_t)((kk * 32) >> 4);  // 8 tf32 = 32 bytes
-                            mma_tf32(dz, dah + adv, dbh + adv, idesc, (first && kk == 0) ? 0u : 1u);
-                            mma_tf32(dz, dah + adv, dbl + adv, idesc, 1u);
-                            mma_tf32(dz, dal + adv, dbh + adv, idesc, 1u);
+                            const uint32_t adv = (uint32_t)kk * 2u;  // 8 tf32 = 32 bytes
+                            mma_tf32_w(dz, ahi + adv, bw + adv, idesc, (first && kk == 0) ? 0u : 1u);
+                            mma_tf32_w(dz, ahi + adv, bw + kBLo + adv, idesc, 1u);
+                            mma_tf32_w(dz, alo + adv, bw + adv, idesc, 1u);
                         }
-                        if (t % GS == GS - 1 || t == T - 1) mma_commit(&stage_empty[pr.slot]);
+                        mma_commit(&stage_empty[slot]);
                         if (last) {
                             if (a.withhold_signal && zused == 0 && zb == 0) {
                                 // test hook: this buffer is never reported full, so the
@@ -600,6 +617,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                             if ((zused >> zb) & 1u) zph ^= 1u << zb;
                             zused |= 1u << zb;
                             zb ^= 1;
+                        }
+                        if (++slot == NR) {
+                            slot = 0;
+                            phase ^= 1u;
+                            ahi = a_hi0;
+                            alo = a_lo0;
+                        } else {
+                            ahi += kAhiStep;
+                            alo += kAloStep;
                         }
                     }
                 }
@@ -613,9 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
         // ---------------------- operand producers (64 threads) ----------------------
         const int ptid = tid - 64;
         Ring<NR> rr;
-        Ring<NP> pr;
         for (int64_t t = 0; t < T; ++t, rr.next()) {
-            if (t % GS == 0 && t > 0) pr.next();
             // the TMA refills a stage only after its MMAs finished, so the operand
             // tile of this stage is free once its raw tile has landed
             if (!warp_wait(&raw_full[rr.slot], rr.phase, abort_flag, a.status, kStatusTimeoutLo))
@@ -686,11 +710,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                     }
                 }
             }
-            if (t % GS == GS - 1 || t == T - 1) {
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&op_full[pr.slot]);
-            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&op_full[rr.slot]);
         }
     } else {
         // ---------------------- epilogue (16 warps) ----------------------
@@ -700,6 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
             // unit are copied (cp.async) while the current one is drained; at the
             // end the slots are summed through shared memory.
             constexpr int kCols = BN / 4;
+            constexpr int kLd = TC_EPI_LD < kCols ? TC_EPI_LD : kCols;  // TMEM columns per wait
             constexpr int kW = 3;
             const int quad = warp & 3;
             const int part = (warp - 4) >> 2;
@@ -750,12 +773,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                         const uint32_t tbase =
                             tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
 #pragma unroll
-                        for (int cc = 0; cc < kCols; cc += 8) {
-                            uint32_t z[8];
-                            tmem_ld8(tbase + cc, z);
+                        for (int cc = 0; cc < kCols; cc += kLd) {
+                            uint32_t z[kLd];
+                            tmem_ld_cols<kLd>(tbase + cc, z);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
+                            for (int q = 0; q < kLd; ++q)
                                 acc[cc + q] = fmaf(g_cur[cc + q], __uint_as_float(z[q]), acc[cc + q]);
                         }
                         tc_fence_before();
@@ -796,6 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
             // copied into the warp's second G buffer (cp.async, no registers) while
             // the current pair is drained.
             constexpr int kCols = BN / 4;
+            constexpr int kLd = TC_EPI_LD < kCols ? TC_EPI_LD : kCols;  // TMEM columns per wait
             const int quad = warp & 3;
             const int part = (warp - 4) >> 2;
             const int64_t row = m0 + 32 * quad + lane;
@@ -837,12 +861,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                         const uint32_t tbase =
                             tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
 #pragma unroll
-                        for (int cc = 0; cc < kCols; cc += 8) {
-                            uint32_t z[8];
-                            tmem_ld8(tbase + cc, z);
+                        for (int cc = 0; cc < kCols; cc += kLd) {
+                            uint32_t z[kLd];
+                            tmem_ld_cols<kLd>(tbase + cc, z);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int q = 0; q < 2; ++q) {
+                            for (int q = 0; q < kLd / 4; ++q) {
                                 const float4 g = *reinterpret_cast<const float4*>(g_cur + cc + 4 * q);
                                 acc[cc + 4 * q + 0] = fmaf(g.x, __uint_as_float(z[4 * q + 0]), acc[cc + 4 * q + 0]);
                                 acc[cc + 4 * q + 1] = fmaf(g.y, __uint_as_float(z[4 * q + 1]), acc[cc + 4 * q + 1]);
