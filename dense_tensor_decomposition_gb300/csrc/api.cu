@@ -460,11 +460,12 @@ int mttkrp_plan_describe(mttkrp_plan_t h, int mode, char* buf, size_t len) {
     char tmp[512];
     int n = snprintf(tmp, sizeof(tmp),
                      "mode=%d path=%s tile=%dx%d inner_group=[%s] J=%lld Jq=%lld pre_modes=[%s] "
-                     "npre=%lld splits=%lld pre_per_split=%lld workspace=%zu tc_ksteps=%d tc_inner=%d tc_slots=%d",
+                     "npre=%lld splits=%lld pre_per_split=%lld workspace=%zu tc_ksteps=%d tc_inner=%d tc_slots=%d "
+                     "tc_tmem_a=%d",
                      mode, mp.path == MTTKRP_PATH_TC ? "tc" : "simt", mp.bm, mp.bn, groups,
                      (long long)g.J, (long long)g.Jq, pres, (long long)g.npre,
                      (long long)mp.splits, (long long)mp.pre_per_split, mp.total, mp.tc_ks, mp.tc_inner,
-                     mp.tc_small ? mp.tc_ps : 1);
+                     mp.tc_small ? mp.tc_ps : 1, mp.tc_tmem);
     if (buf != nullptr && len > 0) {
         strncpy(buf, tmp, len - 1);
         buf[len - 1] = 0;

@@ -58,6 +58,7 @@ struct ModePlan {
     int tc_jq_steps;    // K-steps per value of the p-side part of the inner group
     int tc_small;       // 1: small I_k, tc_ps pre indices share one 128-row tile
     int tc_ps;
+    int tc_tmem;        // 1: A operand staged in tensor memory (128 x 224 tiles, large R)
     // workspace layout, byte offsets from the workspace base
     size_t off_partials, off_binner, off_gtab, off_base, total;
 };

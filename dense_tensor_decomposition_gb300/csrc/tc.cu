@@ -42,7 +42,20 @@ constexpr int kBM = 128;
 constexpr int kBK = 16;           // contraction indices per K-step (64-byte rows)
 constexpr int kChunkSteps = 8;    // at most this many K-steps accumulate in TMEM between drains
 constexpr int kEpiWarps = 16;  // 4 per TMEM lane quadrant
-constexpr int kThreads = (4 + kEpiWarps) * 32;
+#ifndef TC_PROD_WARPS
+#define TC_PROD_WARPS 2
+#endif
+#ifndef TC_PROD_WARPS_INNER
+#define TC_PROD_WARPS_INNER 2
+#endif
+// Warp roles: 0 TMA, 1 MMA, then the operand-producer warps, then the epilogue.
+template <bool INNER>
+struct Roles {
+    static constexpr int kProdWarps = INNER ? TC_PROD_WARPS_INNER : TC_PROD_WARPS;
+    static constexpr int kProdThreads = kProdWarps * 32;
+    static constexpr int kFirstEpi = 2 + kProdWarps;
+    static constexpr int kThreads = (kFirstEpi + kEpiWarps) * 32;
+};
 
 constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s bound on every wait
 constexpr uint32_t kTf32Mask = 0xFFFFE000u;
@@ -303,6 +316,32 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 16 consecutive TMEM columns of the warp's 32 lanes (one register per column)
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// D (+)= A * B, kind::tf32, A (M=128 rows = lanes, 8 columns of K) in tensor
+// memory, B by descriptor low word (high word constant)
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                            uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], db, %4, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"((uint32_t)(kDescSw64Hi >> 32)), "r"(idesc), "r"(acc));
+}
+
 __device__ __forceinline__ float tf32_lo(float x) {
     return x - __uint_as_float(__float_as_uint(x) & kTf32Mask);
 }
@@ -329,6 +368,15 @@ __device__ __forceinline__ uint32_t sw64_off(uint32_t row, uint32_t chunk) {
 #endif
 #ifndef TC_BRES_KB
 #define TC_BRES_KB 128
+#endif
+#ifndef TC_INNER_XPOSE
+#define TC_INNER_XPOSE 1
+#endif
+#ifndef TC_TMEM_KMAJOR
+#define TC_TMEM_KMAJOR 0
+#endif
+#ifndef TC_TMEM_MIN_R
+#define TC_TMEM_MIN_R 448
 #endif
 #ifndef TC_EPI_LD
 #define TC_EPI_LD 8
@@ -389,8 +437,11 @@ struct Ring {
 };
 
 template <int BN, bool INNER, bool SMALL>
-__global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(const __grid_constant__ TcArgs a) {
     using L = Smem<BN, INNER, SMALL>;
+    using RO = Roles<INNER>;
+    constexpr int kPT = RO::kProdThreads;
+    constexpr int kFE = RO::kFirstEpi;
     constexpr int CK = L::kCK;
     constexpr int NR = L::kRaw;
     constexpr int NO = L::kOps;
@@ -432,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
     if (tid == 0) {
         for (int s = 0; s < NR; ++s) {
             mbar_init(&raw_full[s], 1);
-            mbar_init(&op_full[s], 2);
+            mbar_init(&op_full[s], RO::kProdWarps);
             mbar_init(&stage_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -635,9 +686,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
             mma_commit(mma_done);
             wait_drain(mma_done, 0, a.status);
         }
-    } else if (warp < 4) {
+    } else if (warp < kFE) {
         // ---------------------- operand producers (64 threads) ----------------------
-        const int ptid = tid - 64;
+        const int ptid = tid - 64;   // 0 .. kPT - 1
         Ring<NR> rr;
         for (int64_t t = 0; t < T; ++t, rr.next()) {
             // the TMA refills a stage only after its MMAs finished, so the operand
@@ -651,8 +702,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                 const float4* src = reinterpret_cast<const float4*>(st);
                 float4* dst = reinterpret_cast<float4*>(op);
 #pragma unroll
-                for (int v = 0; v < (int)(L::kY / 16) / 64; ++v) {
-                    const int e = ptid + 64 * v;
+                static_assert(INNER || (L::kY / 16) % kPT == 0, "whole rounds");
+                for (int v = 0; v < (int)(L::kY / 16) / kPT; ++v) {
+                    const int e = ptid + kPT * v;
                     const float4 x = src[e];
                     dst[e] = make_float4(tf32_lo(x.x), tf32_lo(x.y), tf32_lo(x.z), tf32_lo(x.w));
                 }
@@ -666,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                 uint8_t* lo = op + L::kA;
                 const int Iv = (int)a.I;
                 const int items = a.ps * Iv * 4;
-                for (int u = ptid; u < items; u += 64) {
+                for (int u = ptid; u < items; u += kPT) {
                     const int i = u % Iv;
                     const int rest = u / Iv;
                     const int jc = rest & 3;
@@ -681,15 +733,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
             } else {
                 // staging tile is [16 j][128 i] (i contiguous): transpose into the
                 // K-major hi and lo tiles, one 4 (i) x 4 (j) block per thread and
-                // round.  (A bank-conflict-free variant that rotates each thread's
-                // row order measured slower: the selects cost more than the
-                // conflicts they remove.)
+                // round
                 const float* stg = reinterpret_cast<const float*>(st);
                 uint8_t* hi = op;
                 uint8_t* lo = op + L::kA;
 #pragma unroll
-                for (int v = 0; v < 2; ++v) {
-                    const int blk = ptid + 64 * v;   // 128 blocks: 32 i-blocks x 4 j-chunks
+                for (int v = 0; v < (128 + kPT - 1) / kPT; ++v) {
+                    const int blk = ptid + kPT * v;   // 128 blocks: 32 i-blocks x 4 j-chunks
+                    if (128 % kPT != 0 && blk >= 128) break;
                     const int jc = blk & 3;
                     const int ib = blk >> 2;
                     float4 col[4];
@@ -702,7 +753,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
                                             make_float4(col[0].w, col[1].w, col[2].w, col[3].w)};
 #pragma unroll
                     for (int p = 0; p < 4; ++p) {
-                        const uint32_t off = sw64_off(4 * ib + p, jc);
+                        // TC_INNER_XPOSE == 1: row 4 ib + p is stored at tile row
+                        // 4 ib + (p ^ (ib & 1)), so that the 8 lanes of a quarter-warp
+                        // (two i-blocks of opposite parity) hit 8 distinct bank groups;
+                        // the epilogue undoes the swap
+                        const int prow = TC_INNER_XPOSE == 1 ? (p ^ (ib & 1)) : p;
+                        const uint32_t off = sw64_off(4 * ib + prow, jc);
                         *reinterpret_cast<float4*>(hi + off) = rows[p];
                         *reinterpret_cast<float4*>(lo + off) =
                             make_float4(tf32_lo(rows[p].x), tf32_lo(rows[p].y), tf32_lo(rows[p].z),
@@ -725,13 +781,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
             constexpr int kLd = TC_EPI_LD < kCols ? TC_EPI_LD : kCols;  // TMEM columns per wait
             constexpr int kW = 3;
             const int quad = warp & 3;
-            const int part = (warp - 4) >> 2;
+            const int part = (warp - kFE) >> 2;
             const int64_t c0 = r0 + part * kCols;
             const int Iv = (int)a.I;
             const int lg = 32 * quad + lane;
             const int slot = lg / Iv;
             const int s_lo = (32 * quad) / Iv;
-            float* gw = gsm + (warp - 4) * 2 * kW * kCols;
+            float* gw = gsm + (warp - kFE) * 2 * kW * kCols;
             float acc[kCols];
 #pragma unroll
             for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
@@ -805,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
             asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
             if (live) {
                 float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride;
-                for (int idx = tid - 128; idx < Iv * BN; idx += kEpiWarps * 32) {
+                for (int idx = tid - 32 * kFE; idx < Iv * BN; idx += kEpiWarps * 32) {
                     const int i = idx / BN, c = idx - i * BN;
                     if (r0 + c >= a.R) continue;
                     float sum = 0.f;
@@ -821,10 +877,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
             constexpr int kCols = BN / 4;
             constexpr int kLd = TC_EPI_LD < kCols ? TC_EPI_LD : kCols;  // TMEM columns per wait
             const int quad = warp & 3;
-            const int part = (warp - 4) >> 2;
-            const int64_t row = m0 + 32 * quad + lane;
+            const int part = (warp - kFE) >> 2;
+            const int lr = 32 * quad + lane;   // TMEM lane = tile row
+            const int64_t row = m0 + ((INNER && TC_INNER_XPOSE == 1) ? (lr ^ ((lr >> 2) & 1)) : lr);
             const int64_t c0 = r0 + part * kCols;
-            float* gw = gsm + (warp - 4) * 2 * kCols;   // this warp's two G rows
+            float* gw = gsm + (warp - kFE) * 2 * kCols;   // this warp's two G rows
             float acc[kCols];
 #pragma unroll
             for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
@@ -908,6 +965,399 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mttkrp_kernel(const __grid_con
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-core kernel with the A operand in tensor memory (large R)
+// ---------------------------------------------------------------------------
+// Four producer warps (one per TMEM lane quadrant) read their 32 rows of each
+// raw Y tile from shared memory, one row per lane, split every value into tf32
+// hi and lo and store both into tensor memory with tcgen05.st (lane = tile row,
+// column = k).  The MMAs then read only B from shared memory: at full rate the
+// tensor core otherwise takes most of the shared-memory bandwidth and starves
+// the producers.  The innermost mode's i-contiguous tile needs no separate
+// transpose (lane = row).  The raw tile is free as soon as the producers have
+// read it, so the TMA ring is decoupled from the MMAs and runs far ahead.
+// TMEM: accumulators at columns [0, BN) and [BN, 2 BN); A slots of 32 columns
+// (hi 16 | lo 16) from column 2 BN.
+#ifndef TC_T_BN
+#define TC_T_BN 224
+#endif
+#ifndef TC_T_ASLOTS
+#define TC_T_ASLOTS 2
+#endif
+constexpr int kTBN = TC_T_BN;
+constexpr int kTASlots = TC_T_ASLOTS;
+constexpr uint32_t kTACol0 = 2 * kTBN;
+constexpr int kTProdWarps = 4;
+constexpr int kTFirstEpi = 2 + kTProdWarps;
+constexpr int kTThreads = (kTFirstEpi + kEpiWarps) * 32;
+#ifndef TC_T_STAGES
+#define TC_T_STAGES 12
+#endif
+
+struct SmemT {
+    static constexpr uint32_t kY = kBM * kBK * 4;      // 8 KB raw Y tile
+    static constexpr uint32_t kB = kTBN * kBK * 4;     // 14 KB: one K-step of B (hi or lo)
+    static constexpr int kCK = 4;                      // K-steps per B-chunk
+    static constexpr uint32_t kBRes = kCK * 2 * kB;    // 112 KB resident B-chunk
+    static constexpr int kRaw = TC_T_STAGES;
+    static constexpr uint32_t kG = kEpiWarps * 2 * (kTBN / 4) * 4;
+    static constexpr uint32_t kBarBytes = 512;
+    static constexpr uint32_t kOffRaw = kBRes;
+    static constexpr uint32_t kOffG = kOffRaw + kRaw * kY;
+    static constexpr uint32_t kOffBars = kOffG + kG;
+    static constexpr uint32_t kTotal = 1024 + kOffBars + kBarBytes;
+    static_assert(kTotal <= 232448, "shared memory budget");
+    static_assert(kB % 512 == 0, "B tiles start on a swizzle-atom boundary");
+    static_assert((2 * kRaw + 2 * kTASlots + 7) * 8 + 8 <= kBarBytes, "barrier area");
+    static_assert(2 * kTBN + 32 * kTASlots <= 512, "TMEM columns");
+};
+
+template <bool INNER>
+__global__ void __launch_bounds__(kTThreads, 1) tc_tmem_kernel(const __grid_constant__ TcArgs a) {
+    using L = SmemT;
+    constexpr int BN = kTBN;
+    constexpr int CK = L::kCK;
+    constexpr int NR = L::kRaw;
+    constexpr int NA = kTASlots;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~(uintptr_t)1023);
+    uint8_t* bres = smem;
+    uint8_t* raw = smem + L::kOffRaw;
+    float* gsm = reinterpret_cast<float*>(smem + L::kOffG);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBars);
+    uint64_t* raw_full = bars;                  // [NR] TMA landed
+    uint64_t* raw_empty = raw_full + NR;        // [NR] producers read the tile
+    uint64_t* a_full = raw_empty + NR;          // [NA] producers wrote the A slot
+    uint64_t* a_empty = a_full + NA;            // [NA] MMAs that read the A slot are done
+    uint64_t* zfull = a_empty + NA;             // [2]
+    uint64_t* zempty = zfull + 2;               // [2]
+    uint64_t* bfull = zempty + 2;               // [1]
+    uint64_t* bempty = bfull + 1;               // [1]
+    uint64_t* mma_done = bempty + 1;            // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int64_t m0 = (int64_t)blockIdx.y * kBM;
+    const int64_t r0 = (int64_t)blockIdx.x * BN;
+    const int64_t pre_lo = (int64_t)blockIdx.z * a.pre_per_split;
+    int64_t pre_hi = pre_lo + a.pre_per_split;
+    if (pre_hi > a.npre) pre_hi = a.npre;
+    const int64_t npi = pre_hi > pre_lo ? pre_hi - pre_lo : 0;
+    const int KS = a.KS;
+    const int njc = (KS + CK - 1) / CK;
+    auto chunk_len = [&](int jc) { return min(CK, KS - jc * CK); };
+    constexpr uint32_t kTmemCols = 512;
+
+    if (tid == 0) {
+        for (int s = 0; s < NR; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&raw_empty[s], kTProdWarps);
+        }
+        for (int s = 0; s < NA; ++s) {
+            mbar_init(&a_full[s], kTProdWarps);
+            mbar_init(&a_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&zfull[b], 1);
+            mbar_init(&zempty[b], kEpiWarps);
+        }
+        mbar_init(bfull, 1);
+        mbar_init(bempty, 1);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int64_t T = npi * KS;  // K-steps of this CTA
+
+    if (warp == 0) {
+        // ------------------------- TMA producer -------------------------
+        if (lane == 0) {
+            const uint8_t* bimg = reinterpret_cast<const uint8_t*>(a.bimg);
+            Ring<NR> rr;
+            int64_t issued = 0;
+            int jc_loaded = -1;
+            bool ok = true;
+            auto load_b = [&](int jc) -> bool {
+                if (jc > 0 && !wait_bounded(bempty, (uint32_t)((jc - 1) & 1), abort_flag, a.status,
+                                            kStatusTimeoutTma))
+                    return false;
+                const int ck = chunk_len(jc);
+                mbar_arrive_expect_tx(bfull, (uint32_t)(ck * 2 * L::kB));
+                for (int q = 0; q < ck; ++q) {
+                    const int ks = jc * CK + q;
+                    const uint8_t* src = bimg + ((int64_t)blockIdx.x * KS + ks) * (int64_t)(2 * L::kB);
+                    bulk_load(bres + q * 2 * L::kB, src, 2 * L::kB, bfull);
+                }
+                jc_loaded = jc;
+                return true;
+            };
+            for (int jc = 0; jc < njc && ok; ++jc) {
+                const int ck = chunk_len(jc);
+                // the first NR Y tiles of chunk jc need only work of chunk jc - 1,
+                // so they are issued before the chunk swap
+                const int64_t swap_at = issued + NR;
+                bool b_pending = true;
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                    const int cP = (int)(pi / a.nQ);
+                    const int cQ = (int)(pi - (int64_t)cP * a.nQ);
+                    for (int q = 0; q < ck; ++q, ++issued, rr.next()) {
+                        if (b_pending && issued == swap_at) {
+                            b_pending = false;
+                            if (!load_b(jc)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (rr.reused && !wait_bounded(&raw_empty[rr.slot], rr.phase ^ 1u, abort_flag,
+                                                       a.status, kStatusTimeoutTma)) {
+                            ok = false;
+                            break;
+                        }
+                        const int ks = jc * CK + q;
+                        int role[kRoles];
+                        if (INNER) {
+                            role[kRoleJq] = ks * kBK;
+                            role[kRoleJp] = 0;
+                        } else {
+                            const int jp = ks / a.jq_steps;
+                            role[kRoleJq] = (ks - jp * a.jq_steps) * kBK;
+                            role[kRoleJp] = jp;
+                        }
+                        role[kRoleI] = (int)m0;
+                        role[kRolePP] = cP;
+                        role[kRolePQ] = cQ;
+                        int c[5] = {0, 0, 0, 0, 0};
+#pragma unroll
+                        for (int r = 0; r < kRoles; ++r)
+                            if (a.slot[r] >= 0) c[a.slot[r]] = role[r];
+                        mbar_arrive_expect_tx(&raw_full[rr.slot], a.y_box_bytes);
+                        tma_load(&a.ymap, a.rank, c, raw + rr.slot * L::kY, &raw_full[rr.slot]);
+                    }
+                }
+                if (ok && b_pending && !load_b(jc)) ok = false;
+            }
+            for (int64_t u = issued - 1; u >= 0 && u >= issued - NR; --u)
+                wait_drain(&raw_full[u % NR], (uint32_t)((u / NR) & 1), a.status);
+            if (jc_loaded >= 0) wait_drain(bfull, (uint32_t)(jc_loaded & 1), a.status);
+        }
+    } else if (warp == 1) {
+        // ------------------------- MMA issuer -------------------------
+        if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
+                                   ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+            const uint32_t b_w0 = sdesc_lo(smem_u32(bres));
+            constexpr uint32_t kBStep = (2 * L::kB) >> 4;
+            constexpr uint32_t kBLo = L::kB >> 4;
+            int as = 0;
+            uint32_t aph = 0;
+            int zb = 0;
+            uint32_t zph = 0;
+            uint32_t zused = 0;
+            bool ok = true;
+            for (int jc = 0; jc < njc && ok; ++jc) {
+                const int ck = chunk_len(jc);
+                if (!wait_bounded(bfull, (uint32_t)(jc & 1), abort_flag, a.status, kStatusTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                    uint32_t bw = b_w0;
+                    for (int q = 0; q < ck; ++q, bw += kBStep) {
+                        const int qq = q % kChunkSteps;
+                        const bool first = qq == 0;
+                        const bool last = qq == kChunkSteps - 1 || q == ck - 1;
+                        if (first && ((zused >> zb) & 1u)) {
+                            if (!wait_bounded(&zempty[zb], (zph >> zb) & 1u, abort_flag, a.status,
+                                              kStatusTimeoutMma)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        if (!wait_bounded(&a_full[as], aph, abort_flag, a.status, kStatusTimeoutMma)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t ta = tmem + kTACol0 + 32u * (uint32_t)as;
+                        const uint32_t dz = tmem + (uint32_t)(zb * BN);
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint32_t adv = (uint32_t)kk * 2u;   // 8 tf32 = 32 bytes of B
+                            const uint32_t ac = (uint32_t)kk * 8u;    // 8 TMEM columns of A
+                            mma_tf32_ta(dz, ta + ac, bw + adv, idesc, (first && kk == 0) ? 0u : 1u);
+                            mma_tf32_ta(dz, ta + ac, bw + kBLo + adv, idesc, 1u);
+                            mma_tf32_ta(dz, ta + 16u + ac, bw + adv, idesc, 1u);
+                        }
+                        mma_commit(&a_empty[as]);
+                        if (last) {
+                            if (a.withhold_signal && zused == 0 && zb == 0) {
+                                // test hook: this buffer is never reported full
+                            } else {
+                                mma_commit(&zfull[zb]);
+                            }
+                            if ((zused >> zb) & 1u) zph ^= 1u << zb;
+                            zused |= 1u << zb;
+                            zb ^= 1;
+                        }
+                        if (++as == NA) {
+                            as = 0;
+                            aph ^= 1u;
+                        }
+                    }
+                }
+                if (ok) mma_commit(bempty);
+            }
+            mma_commit(mma_done);
+            wait_drain(mma_done, 0, a.status);
+        }
+    } else if (warp < kTFirstEpi) {
+        // --------------- operand producers: one TMEM lane quadrant each ---------------
+        const int quad = warp & 3;
+        const int r = 32 * quad + lane;   // tile row of this thread
+        Ring<NR> rr;
+        for (int64_t t = 0; t < T; ++t, rr.next()) {
+            if (!warp_wait(&raw_full[rr.slot], rr.phase, abort_flag, a.status, kStatusTimeoutLo)) break;
+            const uint8_t* st = raw + rr.slot * L::kY;
+            uint32_t hi[16], lo[16];
+            if (!INNER) {
+                // row r of the K-major tile: 64 bytes, 64-byte swizzled
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float4 v = *reinterpret_cast<const float4*>(st + sw64_off((uint32_t)r, (uint32_t)c));
+                    hi[4 * c + 0] = __float_as_uint(v.x);
+                    hi[4 * c + 1] = __float_as_uint(v.y);
+                    hi[4 * c + 2] = __float_as_uint(v.z);
+                    hi[4 * c + 3] = __float_as_uint(v.w);
+                }
+            } else {
+                // column r of the [16 j][128 i] staging tile
+                const float* stg = reinterpret_cast<const float*>(st);
+#pragma unroll
+                for (int j = 0; j < kBK; ++j) hi[j] = __float_as_uint(stg[j * kBM + r]);
+            }
+#pragma unroll
+            for (int e = 0; e < kBK; ++e) lo[e] = __float_as_uint(tf32_lo(__uint_as_float(hi[e])));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&raw_empty[rr.slot]);   // the tile's values are in registers
+            // A slot t % NA was last read by the MMAs of K-step t - NA
+            const int as = (int)(t % NA);
+            if (t >= NA && !warp_wait(&a_empty[as], (uint32_t)(((t / NA) - 1) & 1), abort_flag, a.status,
+                                      kStatusTimeoutLo))
+                break;
+            tc_fence_after();
+            const uint32_t ta = tmem + ((uint32_t)(32 * quad) << 16) + kTACol0 + 32u * (uint32_t)as;
+            tmem_st16(ta, hi);
+            tmem_st16(ta + 16u, lo);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[as]);
+        }
+    } else {
+        // ---------------------- epilogue (16 warps) ----------------------
+        constexpr int kCols = BN / 4;
+        const int quad = warp & 3;
+        const int part = (warp - kTFirstEpi) >> 2;
+        const int64_t row = m0 + 32 * quad + lane;
+        const int64_t c0 = r0 + part * kCols;
+        float* gw = gsm + (warp - kTFirstEpi) * 2 * kCols;
+        float acc[kCols];
+#pragma unroll
+        for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
+        auto fetch_g = [&](int64_t pi, int buf) {
+            for (int e = lane; e < kCols; e += 32) {
+                const bool in = (c0 + e < a.R) && (pi < pre_hi);
+                const float* src = in ? a.gtab + pi * a.R + c0 + e : a.gtab;
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                                 smem_u32(gw + buf * kCols + e)),
+                             "l"(src), "r"(in ? 4 : 0)
+                             : "memory");
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        fetch_g(pre_lo, 0);
+        int gb = 0;
+        int zb = 0;
+        uint32_t zph = 0;
+        bool ok = true;
+        for (int jc = 0; jc < njc && ok; ++jc) {
+            const int ck = chunk_len(jc);
+            for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+                __syncwarp();
+                fetch_g(pi + 1 < pre_hi ? pi + 1 : pre_lo, gb ^ 1);
+                const float* g_cur = gw + gb * kCols;
+                for (int q0 = 0; q0 < ck; q0 += kChunkSteps) {
+                    if (!warp_wait(&zfull[zb], (zph >> zb) & 1u, abort_flag, a.status, kStatusTimeoutEpi)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tbase =
+                        tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
+#pragma unroll
+                    for (int cc = 0; cc < kCols; cc += 8) {
+                        uint32_t z[8];
+                        tmem_ld8(tbase + cc, z);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const float4 g = *reinterpret_cast<const float4*>(g_cur + cc + 4 * q);
+                            acc[cc + 4 * q + 0] = fmaf(g.x, __uint_as_float(z[4 * q + 0]), acc[cc + 4 * q + 0]);
+                            acc[cc + 4 * q + 1] = fmaf(g.y, __uint_as_float(z[4 * q + 1]), acc[cc + 4 * q + 1]);
+                            acc[cc + 4 * q + 2] = fmaf(g.z, __uint_as_float(z[4 * q + 2]), acc[cc + 4 * q + 2]);
+                            acc[cc + 4 * q + 3] = fmaf(g.w, __uint_as_float(z[4 * q + 3]), acc[cc + 4 * q + 3]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&zempty[zb]);
+                    zph ^= 1u << zb;
+                    zb ^= 1;
+                }
+                gb ^= 1;
+            }
+        }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        if (!*abort_flag && row < a.I) {
+            float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride + row * a.R + c0;
+            const bool vst = (a.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.dst) & 15) == 0);
+#pragma unroll
+            for (int e = 0; e < kCols; e += 4) {
+                if (vst && c0 + e + 4 <= a.R) {
+                    *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (c0 + e + q < a.R) dst[e + q] = acc[e + q];
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
     }
 }
 
@@ -1123,6 +1573,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+template <bool INNER>
+cudaError_t launch_tmem(const TcArgs& args, dim3 grid, cudaStream_t s) {
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tc_tmem_kernel<INNER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)SmemT::kTotal);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    tc_tmem_kernel<INNER><<<grid, kTThreads, SmemT::kTotal, s>>>(args);
+    return cudaGetLastError();
+}
+
 template <int BN, bool INNER, bool SMALL = false>
 cudaError_t launch_main(const TcArgs& args, dim3 grid, cudaStream_t s) {
     using L = Smem<BN, INNER, SMALL>;
@@ -1137,7 +1604,7 @@ cudaError_t launch_main(const TcArgs& args, dim3 grid, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    tc_mttkrp_kernel<BN, INNER, SMALL><<<grid, kThreads, L::kTotal, s>>>(args);
+    tc_mttkrp_kernel<BN, INNER, SMALL><<<grid, Roles<INNER>::kThreads, L::kTotal, s>>>(args);
     return cudaGetLastError();
 }
 
@@ -1169,8 +1636,11 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
     mp.tc_inner = (g.s_k == 1) ? 1 : 0;
     mp.tc_small = small_eligible(g) ? 1 : 0;
     mp.tc_ps = mp.tc_small ? (int)(kBM / g.I) : 1;
+    // innermost mode with large R: A staged in tensor memory (the i-contiguous
+    // tile is transposed on the way into TMEM, no shared-memory round trip)
+    mp.tc_tmem = (!mp.tc_small && g.R >= TC_TMEM_MIN_R && (mp.tc_inner || TC_TMEM_KMAJOR)) ? 1 : 0;
     mp.bm = kBM;
-    mp.bn = g.R >= 192 ? 256 : (g.R > 64 ? 128 : 64);
+    mp.bn = mp.tc_tmem ? kTBN : g.R >= 192 ? 256 : (g.R > 64 ? 128 : 64);
     if (mp.tc_inner) {
         if (g.J > g.Jq && g.Jq != 1) return false;
         mp.tc_jq_steps = 1;
@@ -1308,7 +1778,9 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     dim3 grid((unsigned)cdiv64(g.R, mp.bn), mp.tc_small ? 1u : (unsigned)cdiv64(g.I, kBM),
               (unsigned)mp.splits);
     cudaError_t e;
-    if (mp.tc_small && mp.tc_inner) {
+    if (mp.tc_tmem) {
+        e = mp.tc_inner ? launch_tmem<true>(args, grid, stream) : launch_tmem<false>(args, grid, stream);
+    } else if (mp.tc_small && mp.tc_inner) {
         e = mp.bn == 256 ? launch_main<256, true, true>(args, grid, stream)
           : mp.bn == 128 ? launch_main<128, true, true>(args, grid, stream)
                          : launch_main<64, true, true>(args, grid, stream);

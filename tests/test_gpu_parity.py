@@ -152,6 +152,10 @@ EDGE = [
     ((12, 50, 36), 64),
     ((7, 9, 11, 44), 130),
     ((5, 6, 40, 28), 260),
+    # large R: the A operand staged in tensor memory (224-column tiles), K-major
+    # and innermost modes, row / column / contraction tails
+    ((24, 40, 136), 460),
+    ((130, 6, 7, 100), 500),
 ]
 
 
