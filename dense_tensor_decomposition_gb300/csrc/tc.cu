@@ -264,6 +264,30 @@ __device__ __forceinline__ void mma_tf32_w(uint32_t d_tmem, uint32_t a_lo, uint3
         "r"(a_lo), "r"(b_lo), "r"((uint32_t)(kDescSw64Hi >> 32)), "r"(idesc), "r"(acc));
 }
 
+// As mma_tf32_w, issued only by the lane whose `leader` is nonzero (the warp runs
+// the issue loop together, so its values stay warp-uniform)
+__device__ __forceinline__ void mma_tf32_wl(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                            uint32_t acc, uint32_t leader) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %3};\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "setp.ne.b32 e, %6, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], da, db, %4, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"((uint32_t)(kDescSw64Hi >> 32)), "r"(idesc), "r"(acc), "r"(leader));
+}
+
+// commit by the lane whose `leader` is nonzero (the lane that issued the MMAs)
+__device__ __forceinline__ void mma_commit_l(uint64_t* bar, uint32_t leader) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %1, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+            smem_u32(bar)),
+        "r"(leader)
+        : "memory");
+}
+
 // arrive on `bar` once all previously issued MMAs of this thread have completed
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -378,6 +402,9 @@ __device__ __forceinline__ uint32_t sw64_off(uint32_t row, uint32_t chunk) {
 #ifndef TC_TMEM_MIN_R
 #define TC_TMEM_MIN_R 448
 #endif
+#ifndef TC_MMA_WARP
+#define TC_MMA_WARP 1
+#endif
 #ifndef TC_EPI_LD
 #define TC_EPI_LD 8
 #endif
@@ -467,7 +494,7 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x;
-    const int warp = tid >> 5;
+    const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);   // warp-uniform
     const int lane = tid & 31;
     const int64_t m0 = (int64_t)blockIdx.y * kBM;
     const int64_t r0 = (int64_t)blockIdx.x * BN;
@@ -604,7 +631,24 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
         // tensor pipe's duty cycle (six MMAs of BN / 2 cycles each per step), so
         // the loop is kept short: one wait and one commit per stage, and the
         // descriptors' low words advance incrementally (high word constant).
-        if (lane == 0) {
+        // TC_MMA_WARP: the whole warp runs the loop (warp-uniform values; lane 0
+        // issues through a predicate), otherwise lane 0 alone
+        constexpr bool kWarpIssue = TC_MMA_WARP != 0;
+        const uint32_t leader = lane == 0 ? 1u : 0u;
+        auto mma_w = [&](uint32_t d, uint32_t aw, uint32_t bw_, uint32_t idesc_, uint32_t acc) {
+            if constexpr (kWarpIssue) mma_tf32_wl(d, aw, bw_, idesc_, acc, leader);
+            else mma_tf32_w(d, aw, bw_, idesc_, acc);
+        };
+        auto commit_w = [&](uint64_t* bar) {
+            if constexpr (kWarpIssue) mma_commit_l(bar, leader);
+            else mma_commit(bar);
+        };
+        auto wait_w = [&](uint64_t* bar, uint32_t par) -> bool {
+            bool r = wait_bounded(bar, par, abort_flag, a.status, kStatusTimeoutMma);
+            if constexpr (kWarpIssue) r = __all_sync(0xffffffffu, r);
+            return r;
+        };
+        if (kWarpIssue || lane == 0) {
             const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
                                    ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
             const uint32_t raw_s = smem_u32(raw);
@@ -625,7 +669,7 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
             bool ok = true;
             for (int jc = 0; jc < njc && ok; ++jc) {
                 const int ck = chunk_len(jc);
-                if (!wait_bounded(bfull, (uint32_t)(jc & 1), abort_flag, a.status, kStatusTimeoutMma)) {
+                if (!wait_w(bfull, (uint32_t)(jc & 1))) {
                     ok = false;
                     break;
                 }
@@ -637,15 +681,14 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
                         const bool last = qq == kChunkSteps - 1 || q == ck - 1;
                         if (first && ((zused >> zb) & 1u)) {
                             // the epilogue has read this TMEM buffer's previous contents
-                            if (!wait_bounded(&zempty[zb], (zph >> zb) & 1u, abort_flag, a.status,
-                                              kStatusTimeoutMma)) {
+                            if (!wait_w(&zempty[zb], (zph >> zb) & 1u)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
                         }
                         // the producers arrive only after the stage's TMA copy landed
-                        if (!wait_bounded(&op_full[slot], phase, abort_flag, a.status, kStatusTimeoutMma)) {
+                        if (!wait_w(&op_full[slot], phase)) {
                             ok = false;
                             break;
                         }
@@ -653,17 +696,17 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             const uint32_t adv = (uint32_t)kk * 2u;  // 8 tf32 = 32 bytes
-                            mma_tf32_w(dz, ahi + adv, bw + adv, idesc, (first && kk == 0) ? 0u : 1u);
-                            mma_tf32_w(dz, ahi + adv, bw + kBLo + adv, idesc, 1u);
-                            mma_tf32_w(dz, alo + adv, bw + adv, idesc, 1u);
+                            mma_w(dz, ahi + adv, bw + adv, idesc, (first && kk == 0) ? 0u : 1u);
+                            mma_w(dz, ahi + adv, bw + kBLo + adv, idesc, 1u);
+                            mma_w(dz, alo + adv, bw + adv, idesc, 1u);
                         }
-                        mma_commit(&stage_empty[slot]);
+                        commit_w(&stage_empty[slot]);
                         if (last) {
                             if (a.withhold_signal && zused == 0 && zb == 0) {
                                 // test hook: this buffer is never reported full, so the
                                 // epilogue's bounded wait expires and the CTA aborts
                             } else {
-                                mma_commit(&zfull[zb]);
+                                commit_w(&zfull[zb]);
                             }
                             if ((zused >> zb) & 1u) zph ^= 1u << zb;
                             zused |= 1u << zb;
@@ -680,11 +723,12 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
                         }
                     }
                 }
-                if (ok) mma_commit(bempty);  // the B-chunk may be replaced once these finish
+                if (ok) commit_w(bempty);  // the B-chunk may be replaced once these finish
             }
             // all MMAs issued by this thread are complete before TMEM is freed
-            mma_commit(mma_done);
-            wait_drain(mma_done, 0, a.status);
+            commit_w(mma_done);
+            if (lane == 0) wait_drain(mma_done, 0, a.status);
+            if (kWarpIssue) __syncwarp();
         }
     } else if (warp < kFE) {
         // ---------------------- operand producers (64 threads) ----------------------
