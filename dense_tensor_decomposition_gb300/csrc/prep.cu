@@ -2,9 +2,9 @@
 //  * prod_table_kernel builds the factor-product tables G (pre modes) and
 //    Binner (inner group) that the main kernels combine into Khatri-Rao rows
 //    on the fly, plus the Y base offset of every pre index;
-//  * reduce_splits_kernel adds the per-split partial results in a fixed order
-//    in fp64 and writes the fp32 output (no atomics anywhere, so results are
-//    bitwise reproducible).
+//  * the split reductions add the per-split partial results in a fixed order
+//    in fp64 and write the fp32 output (no atomics anywhere, so results are
+//    bitwise reproducible for a given plan).
 #include "internal.h"
 
 namespace mk {
@@ -39,56 +39,138 @@ cudaError_t launch_prod_table(const ProdTableArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// out[e] = (float) sum over s of (double) part[s * n + e], summed in a fixed order
-// that depends only on (splits, n): each block owns 32 consecutive outputs (one
-// per lane); warp w adds the partials of splits [w*S/8, (w+1)*S/8) in
-// increasing s; the eight warp sums are then added in warp order.  The result
-// is therefore bitwise reproducible, and the S loads are spread over 8 warps
-// instead of one serial loop per output.
+// out[e] = (float) sum over s of (double) part[s * n + e].  Each block owns 32
+// groups of 4 consecutive outputs (one 16-byte group per lane); warp w adds the
+// partials of splits [w*S/8, (w+1)*S/8) in increasing s with several 16-byte
+// loads in flight, and the eight warp sums are added in warp order.  The order
+// depends only on (S, n), so results are bitwise reproducible; spreading the
+// splits over warps keeps enough loads in flight both for many outputs and few
+// splits and for few outputs and many splits.
 constexpr int kRedWarps = 8;
 
+template <int V>   // V = 4: float4 groups; V = 1: scalars
 __global__ void __launch_bounds__(kRedWarps * 32)
     reduce_splits_kernel(const float* __restrict__ part, int64_t splits, int64_t n,
                          float* __restrict__ out) {
-    __shared__ double sums[kRedWarps][32];
+    __shared__ double sums[kRedWarps][32][V];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int64_t s0 = splits * warp / kRedWarps;
     const int64_t s1 = splits * (warp + 1) / kRedWarps;
-    for (int64_t base = (int64_t)blockIdx.x * 32; base < n; base += (int64_t)gridDim.x * 32) {
-        const int64_t e = base + lane;
-        double acc = 0.0;
-        if (e < n) {
-            const float* p = part + s0 * n + e;
-            int64_t sp = s0;
-            // four independent loads in flight, added in split order
-            for (; sp + 4 <= s1; sp += 4, p += 4 * n) {
-                const float a0 = __ldcs(p), a1 = __ldcs(p + n), a2 = __ldcs(p + 2 * n), a3 = __ldcs(p + 3 * n);
-                acc += (double)a0;
-                acc += (double)a1;
-                acc += (double)a2;
-                acc += (double)a3;
-            }
-            for (; sp < s1; ++sp, p += n) acc += (double)__ldcs(p);
-        }
-        sums[warp][lane] = acc;
-        __syncthreads();
-        if (warp == 0 && e < n) {
-            double t = 0.0;
+    const int64_t ng = n / V;   // groups
+    for (int64_t base = (int64_t)blockIdx.x * 32; base < ng; base += (int64_t)gridDim.x * 32) {
+        const int64_t g = base + lane;
+        double acc[V];
 #pragma unroll
-            for (int w = 0; w < kRedWarps; ++w) t += sums[w][lane];
-            out[e] = (float)t;
+        for (int c = 0; c < V; ++c) acc[c] = 0.0;
+        if (g < ng) {
+            int64_t sp = s0;
+            for (; sp + 4 <= s1; sp += 4) {
+                float v[4][V];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float* p = part + (sp + u) * n + g * V;
+                    if constexpr (V == 4) {
+                        const float4 x = __ldcs(reinterpret_cast<const float4*>(p));
+                        v[u][0] = x.x;
+                        v[u][1] = x.y;
+                        v[u][2] = x.z;
+                        v[u][3] = x.w;
+                    } else {
+                        v[u][0] = __ldcs(p);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int c = 0; c < V; ++c) acc[c] += (double)v[u][c];
+            }
+            for (; sp < s1; ++sp) {
+                const float* p = part + sp * n + g * V;
+                if constexpr (V == 4) {
+                    const float4 x = __ldcs(reinterpret_cast<const float4*>(p));
+                    acc[0] += (double)x.x;
+                    acc[1] += (double)x.y;
+                    acc[2] += (double)x.z;
+                    acc[3] += (double)x.w;
+                } else {
+                    acc[0] += (double)__ldcs(p);
+                }
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < V; ++c) sums[warp][lane][c] = acc[c];
+        __syncthreads();
+        if (warp == 0 && g < ng) {
+            double t[V];
+#pragma unroll
+            for (int c = 0; c < V; ++c) t[c] = 0.0;
+#pragma unroll
+            for (int w = 0; w < kRedWarps; ++w)
+#pragma unroll
+                for (int c = 0; c < V; ++c) t[c] += sums[w][lane][c];
+            if constexpr (V == 4)
+                reinterpret_cast<float4*>(out)[g] = make_float4((float)t[0], (float)t[1], (float)t[2], (float)t[3]);
+            else
+                out[g] = (float)t[0];
         }
         __syncthreads();
+    }
+}
+
+// One thread per 4 consecutive outputs, all splits in increasing s with four
+// 16-byte loads in flight (used when there are enough outputs to fill the GPU
+// this way; no shared memory, no block barriers).
+__global__ void __launch_bounds__(256)
+    reduce_splits_flat_kernel(const float4* __restrict__ part, int64_t splits, int64_t n4,
+                              float4* __restrict__ out) {
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n4;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
+        const float4* p = part + e;
+        int64_t sp = 0;
+        for (; sp + 4 <= splits; sp += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = __ldcs(p + (sp + u) * n4);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                a0 += (double)v[u].x;
+                a1 += (double)v[u].y;
+                a2 += (double)v[u].z;
+                a3 += (double)v[u].w;
+            }
+        }
+        for (; sp < splits; ++sp) {
+            const float4 v = __ldcs(p + sp * n4);
+            a0 += (double)v.x;
+            a1 += (double)v.y;
+            a2 += (double)v.z;
+            a3 += (double)v.w;
+        }
+        out[e] = make_float4((float)a0, (float)a1, (float)a2, (float)a3);
     }
 }
 
 cudaError_t launch_reduce_splits(const float* part, int64_t splits, int64_t n, float* out,
                                  cudaStream_t s) {
     if (n == 0) return cudaSuccess;
-    int64_t blocks = (n + 31) / 32;
+    const bool vec = n % 4 == 0 && (reinterpret_cast<uintptr_t>(part) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+    const int64_t groups = vec ? n / 4 : n;
+    if (vec && groups >= 152 * 256) {
+        int64_t blocks = (groups + 255) / 256;
+        if (blocks > 152 * 8) blocks = 152 * 8;
+        reduce_splits_flat_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(part), splits,
+                                                                   groups, reinterpret_cast<float4*>(out));
+        return cudaGetLastError();
+    }
+    int64_t blocks = (groups + 31) / 32;
     if (blocks > 152 * 16) blocks = 152 * 16;
-    reduce_splits_kernel<<<(unsigned)blocks, kRedWarps * 32, 0, s>>>(part, splits, n, out);
+    if (vec)
+        reduce_splits_kernel<4><<<(unsigned)blocks, kRedWarps * 32, 0, s>>>(part, splits, n, out);
+    else
+        reduce_splits_kernel<1><<<(unsigned)blocks, kRedWarps * 32, 0, s>>>(part, splits, n, out);
     return cudaGetLastError();
 }
 

@@ -148,7 +148,15 @@ __device__ __forceinline__ uint32_t mbar_try_wait_suspend(uint64_t* bar, uint32_
 
 // Slow path of wait_bounded: suspend-and-retry until the phase completes, the
 // CTA is aborted, or kWaitNs pass (then the CTA is aborted and `code` recorded).
-__device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+#ifndef TC_WAIT_INLINE
+#define TC_WAIT_INLINE 0
+#endif
+#if TC_WAIT_INLINE
+#define TC_WAIT_SLOW_ATTR __forceinline__
+#else
+#define TC_WAIT_SLOW_ATTR __noinline__
+#endif
+__device__ TC_WAIT_SLOW_ATTR bool wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                        uint32_t* status, uint32_t code) {
     const unsigned long long t0 = gtimer();
     while (true) {
