@@ -59,6 +59,8 @@ struct ModePlan {
     int tc_small;       // 1: small I_k, tc_ps pre indices share one 128-row tile
     int tc_ps;
     int tc_tmem;        // 1: A operand staged in tensor memory (128 x 224 tiles, large R)
+    int tc_h2;          // 1: two-term fp16 split (kind::f16, K-steps of 32); implies tc_tmem
+    int tc_kw;          // contraction indices per K-step (16, or 32 with tc_h2)
     // workspace layout, byte offsets from the workspace base
     size_t off_partials, off_binner, off_gtab, off_base, total;
 };

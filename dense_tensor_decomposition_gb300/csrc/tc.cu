@@ -23,6 +23,7 @@
 // for its own copies and MMAs and frees its TMEM before returning.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 
 #include <atomic>
 #include <cstdio>
@@ -87,6 +88,9 @@ struct TcArgs {
     // small-I variant: ps pre indices share one 128-row tile (rows slot * I + i)
     int ps;                   // pre-index slots per tile (1 otherwise)
     int64_t batch_len;        // slots never cross a multiple of this pre index
+    // two-term fp16 split only
+    const uint32_t* ymax_bits;   // max |Y| as fp32 bits (device)
+    const float* colscale;       // power-of-two scale of each Binner column (R)
     uint32_t* status;
 };
 
@@ -358,6 +362,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
         : "memory");
 }
 
+// 8 consecutive TMEM columns of the warp's 32 lanes
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -406,6 +417,9 @@ __device__ __forceinline__ uint32_t sw64_off(uint32_t row, uint32_t chunk) {
 #endif
 #ifndef TC_TMEM_KMAJOR
 #define TC_TMEM_KMAJOR 0
+#endif
+#ifndef TC_H2_MIN_R
+#define TC_H2_MIN_R 448
 #endif
 #ifndef TC_TMEM_MIN_R
 #define TC_TMEM_MIN_R 448
@@ -1414,6 +1428,434 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_tmem_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------
+// Tensor-core kernel, two-term fp16 split (A in tensor memory, large R)
+// ---------------------------------------------------------------------------
+// Each fp32 value x (Y scaled by a power of two so that max|Y| < 2^14, and each
+// Binner column likewise) is split into hi = fp16(x) and lo = fp16(x - hi); the
+// three products hi*hi + hi*lo + lo*hi (kind::f16, fp32 accumulation) carry
+// 2 x 11 significant bits, as the tf32 split does, with one K = 16 instruction
+// per product per 16 contraction indices instead of two K = 8 ones.  The
+// single MMA-issuing thread, which bounds the tf32 kernels, issues half as
+// many instructions for the same work.  Structure as the tensor-memory-A tf32
+// kernel; K-steps of 32 (128-byte rows of the raw fp32 tile, 64-byte rows of
+// the fp16 B images).
+constexpr int kBK2 = 32;
+constexpr int kChunkSteps2 = 4;   // 128 contraction indices between TMEM drains
+
+#ifndef TC_H2_STAGES
+#define TC_H2_STAGES 6
+#endif
+struct SmemH2 {
+    static constexpr uint32_t kY = kBM * kBK2 * 4;     // 16 KB raw fp32 Y tile
+    static constexpr uint32_t kB = kTBN * kBK2 * 2;    // 14 KB: one K-step of B (hi or lo, fp16)
+    static constexpr int kCK = 4;                      // K-steps per B-chunk
+    static constexpr uint32_t kBRes = kCK * 2 * kB;    // 112 KB resident B-chunk
+    static constexpr int kRaw = TC_H2_STAGES;
+    static constexpr uint32_t kG = kEpiWarps * 2 * (kTBN / 4) * 4;
+    static constexpr uint32_t kBarBytes = 512;
+    static constexpr uint32_t kOffRaw = kBRes;
+    static constexpr uint32_t kOffG = kOffRaw + kRaw * kY;
+    static constexpr uint32_t kOffBars = kOffG + kG;
+    static constexpr uint32_t kTotal = 1024 + kOffBars + kBarBytes;
+    static_assert(kTotal <= 232448, "shared memory budget");
+    static_assert(kB % 512 == 0 && kY % 1024 == 0, "swizzle-atom alignment");
+    static_assert((2 * kRaw + 2 * kTASlots + 7) * 8 + 8 <= kBarBytes, "barrier area");
+};
+
+// power of two that maps the largest magnitude m (as fp32 bits) into [2^13, 2^14)
+__device__ __forceinline__ float pow2_scale(uint32_t mbits) {
+    const int e = (int)((mbits >> 23) & 0xFFu);   // biased exponent of m
+    if (e == 0 || e == 255) return 1.f;           // zero / subnormal / non-finite: no scaling
+    int se = 127 + 13 - (e - 127);                // biased exponent of 2^(13 - (e - 127))
+    se = se < 1 ? 1 : (se > 254 ? 254 : se);
+    return __uint_as_float((uint32_t)se << 23);
+}
+__device__ __forceinline__ float pow2_unscale(uint32_t mbits) {
+    return 1.f / pow2_scale(mbits);
+}
+
+// D (+)= A * B, kind::f16, A (M=128 rows = lanes, 8 columns = 16 fp16 of K) in
+// tensor memory, B by descriptor low word (high word constant)
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                           uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"((uint32_t)(kDescSw64Hi >> 32)), "r"(idesc), "r"(acc));
+}
+
+template <bool INNER>
+__global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_constant__ TcArgs a) {
+    using L = SmemH2;
+    constexpr int BN = kTBN;
+    constexpr int CK = L::kCK;
+    constexpr int NR = L::kRaw;
+    constexpr int NA = kTASlots;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~(uintptr_t)1023);
+    uint8_t* bres = smem;
+    uint8_t* raw = smem + L::kOffRaw;
+    float* gsm = reinterpret_cast<float*>(smem + L::kOffG);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBars);
+    uint64_t* raw_full = bars;                  // [NR] TMA landed
+    uint64_t* raw_empty = raw_full + NR;        // [NR] producers read the tile
+    uint64_t* a_full = raw_empty + NR;          // [NA] producers wrote the A slot
+    uint64_t* a_empty = a_full + NA;            // [NA] MMAs that read the A slot are done
+    uint64_t* zfull = a_empty + NA;             // [2]
+    uint64_t* zempty = zfull + 2;               // [2]
+    uint64_t* bfull = zempty + 2;               // [1]
+    uint64_t* bempty = bfull + 1;               // [1]
+    uint64_t* mma_done = bempty + 1;            // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int64_t m0 = (int64_t)blockIdx.y * kBM;
+    const int64_t r0 = (int64_t)blockIdx.x * BN;
+    const int64_t pre_lo = (int64_t)blockIdx.z * a.pre_per_split;
+    int64_t pre_hi = pre_lo + a.pre_per_split;
+    if (pre_hi > a.npre) pre_hi = a.npre;
+    const int64_t npi = pre_hi > pre_lo ? pre_hi - pre_lo : 0;
+    const int KS = a.KS;
+    const int njc = (KS + CK - 1) / CK;
+    auto chunk_len = [&](int jc) { return min(CK, KS - jc * CK); };
+    constexpr uint32_t kTmemCols = 512;
+
+    if (tid == 0) {
+        for (int s = 0; s < NR; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&raw_empty[s], kTProdWarps);
+        }
+        for (int s = 0; s < NA; ++s) {
+            mbar_init(&a_full[s], kTProdWarps);
+            mbar_init(&a_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&zfull[b], 1);
+            mbar_init(&zempty[b], kEpiWarps);
+        }
+        mbar_init(bfull, 1);
+        mbar_init(bempty, 1);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int64_t T = npi * KS;  // K-steps of this CTA
+
+    if (warp == 0) {
+        // ------------------------- TMA producer -------------------------
+        if (lane == 0) {
+            const uint8_t* bimg = reinterpret_cast<const uint8_t*>(a.bimg);
+            Ring<NR> rr;
+            int64_t issued = 0;
+            int jc_loaded = -1;
+            bool ok = true;
+            auto load_b = [&](int jc) -> bool {
+                if (jc > 0 && !wait_bounded(bempty, (uint32_t)((jc - 1) & 1), abort_flag, a.status,
+                                            kStatusTimeoutTma))
+                    return false;
+                const int ck = chunk_len(jc);
+                mbar_arrive_expect_tx(bfull, (uint32_t)(ck * 2 * L::kB));
+                for (int q = 0; q < ck; ++q) {
+                    const int ks = jc * CK + q;
+                    const uint8_t* src = bimg + ((int64_t)blockIdx.x * KS + ks) * (int64_t)(2 * L::kB);
+                    bulk_load(bres + q * 2 * L::kB, src, 2 * L::kB, bfull);
+                }
+                jc_loaded = jc;
+                return true;
+            };
+            for (int jc = 0; jc < njc && ok; ++jc) {
+                const int ck = chunk_len(jc);
+                // the first NR Y tiles of chunk jc need only work of chunk jc - 1,
+                // so they are issued before the chunk swap
+                const int64_t swap_at = issued + NR;
+                bool b_pending = true;
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                    const int cP = (int)(pi / a.nQ);
+                    const int cQ = (int)(pi - (int64_t)cP * a.nQ);
+                    for (int q = 0; q < ck; ++q, ++issued, rr.next()) {
+                        if (b_pending && issued == swap_at) {
+                            b_pending = false;
+                            if (!load_b(jc)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (rr.reused && !wait_bounded(&raw_empty[rr.slot], rr.phase ^ 1u, abort_flag,
+                                                       a.status, kStatusTimeoutTma)) {
+                            ok = false;
+                            break;
+                        }
+                        const int ks = jc * CK + q;
+                        int role[kRoles];
+                        if (INNER) {
+                            role[kRoleJq] = ks * kBK2;
+                            role[kRoleJp] = 0;
+                        } else {
+                            const int jp = ks / a.jq_steps;
+                            role[kRoleJq] = (ks - jp * a.jq_steps) * kBK2;
+                            role[kRoleJp] = jp;
+                        }
+                        role[kRoleI] = (int)m0;
+                        role[kRolePP] = cP;
+                        role[kRolePQ] = cQ;
+                        int c[5] = {0, 0, 0, 0, 0};
+#pragma unroll
+                        for (int r = 0; r < kRoles; ++r)
+                            if (a.slot[r] >= 0) c[a.slot[r]] = role[r];
+                        mbar_arrive_expect_tx(&raw_full[rr.slot], a.y_box_bytes);
+                        tma_load(&a.ymap, a.rank, c, raw + rr.slot * L::kY, &raw_full[rr.slot]);
+                    }
+                }
+                if (ok && b_pending && !load_b(jc)) ok = false;
+            }
+            for (int64_t u = issued - 1; u >= 0 && u >= issued - NR; --u)
+                wait_drain(&raw_full[u % NR], (uint32_t)((u / NR) & 1), a.status);
+            if (jc_loaded >= 0) wait_drain(bfull, (uint32_t)(jc_loaded & 1), a.status);
+        }
+    } else if (warp == 1) {
+        // ------------------------- MMA issuer -------------------------
+        if (lane == 0) {
+            // kind::f16: fp16 A and B, fp32 accumulator
+            const uint32_t idesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+            const uint32_t b_w0 = sdesc_lo(smem_u32(bres));
+            constexpr uint32_t kBStep = (2 * L::kB) >> 4;
+            constexpr uint32_t kBLo = L::kB >> 4;
+            int as = 0;
+            uint32_t aph = 0;
+            int zb = 0;
+            uint32_t zph = 0;
+            uint32_t zused = 0;
+            bool ok = true;
+            for (int jc = 0; jc < njc && ok; ++jc) {
+                const int ck = chunk_len(jc);
+                if (!wait_bounded(bfull, (uint32_t)(jc & 1), abort_flag, a.status, kStatusTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                    uint32_t bw = b_w0;
+                    for (int q = 0; q < ck; ++q, bw += kBStep) {
+                        const int qq = q % kChunkSteps2;
+                        const bool first = qq == 0;
+                        const bool last = qq == kChunkSteps2 - 1 || q == ck - 1;
+                        if (first && ((zused >> zb) & 1u)) {
+                            if (!wait_bounded(&zempty[zb], (zph >> zb) & 1u, abort_flag, a.status,
+                                              kStatusTimeoutMma)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        if (!wait_bounded(&a_full[as], aph, abort_flag, a.status, kStatusTimeoutMma)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t ta = tmem + kTACol0 + 32u * (uint32_t)as;
+                        const uint32_t dz = tmem + (uint32_t)(zb * BN);
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint32_t adv = (uint32_t)kk * 2u;   // 16 fp16 = 32 bytes of B
+                            const uint32_t ac = (uint32_t)kk * 8u;    // 8 TMEM columns (16 fp16) of A
+                            mma_f16_ta(dz, ta + ac, bw + adv, idesc, (first && kk == 0) ? 0u : 1u);
+                            mma_f16_ta(dz, ta + ac, bw + kBLo + adv, idesc, 1u);
+                            mma_f16_ta(dz, ta + 16u + ac, bw + adv, idesc, 1u);
+                        }
+                        mma_commit(&a_empty[as]);
+                        if (last) {
+                            if (a.withhold_signal && zused == 0 && zb == 0) {
+                                // test hook: this buffer is never reported full
+                            } else {
+                                mma_commit(&zfull[zb]);
+                            }
+                            if ((zused >> zb) & 1u) zph ^= 1u << zb;
+                            zused |= 1u << zb;
+                            zb ^= 1;
+                        }
+                        if (++as == NA) {
+                            as = 0;
+                            aph ^= 1u;
+                        }
+                    }
+                }
+                if (ok) mma_commit(bempty);
+            }
+            mma_commit(mma_done);
+            wait_drain(mma_done, 0, a.status);
+        }
+    } else if (warp < kTFirstEpi) {
+        // --------------- operand producers: one TMEM lane quadrant each ---------------
+        const int quad = warp & 3;
+        const int r = 32 * quad + lane;   // tile row of this thread
+        const float sy = pow2_scale(*a.ymax_bits);   // Y is scaled by this power of two
+        Ring<NR> rr;
+        for (int64_t t = 0; t < T; ++t, rr.next()) {
+            if (!warp_wait(&raw_full[rr.slot], rr.phase, abort_flag, a.status, kStatusTimeoutLo)) break;
+            // A slot t % NA was last read by the MMAs of K-step t - NA
+            const int as = (int)(t % NA);
+            if (t >= NA && !warp_wait(&a_empty[as], (uint32_t)(((t / NA) - 1) & 1), abort_flag, a.status,
+                                      kStatusTimeoutLo))
+                break;
+            tc_fence_after();
+            const uint8_t* st = raw + rr.slot * L::kY;
+            const uint32_t ta = tmem + ((uint32_t)(32 * quad) << 16) + kTACol0 + 32u * (uint32_t)as;
+            // two halves of 16 contraction indices: hi to columns [8h, 8h + 8), lo to
+            // [16 + 8h, 16 + 8h + 8); column c holds k = 2c (low half) and 2c + 1
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float v[16];
+                if (!INNER) {
+                    // row r of the K-major tile: 128 bytes, 128-byte swizzled
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int cc = 4 * h + c;
+                        const float4 x = *reinterpret_cast<const float4*>(
+                            st + (uint32_t)r * 128u + ((((uint32_t)cc ^ (uint32_t)r) & 7u) << 4));
+                        v[4 * c + 0] = x.x;
+                        v[4 * c + 1] = x.y;
+                        v[4 * c + 2] = x.z;
+                        v[4 * c + 3] = x.w;
+                    }
+                } else {
+                    // column r of the [32 j][128 i] staging tile
+                    const float* stg = reinterpret_cast<const float*>(st);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = stg[(16 * h + j) * kBM + r];
+                }
+                uint32_t hi[8], lo[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float x0 = v[2 * c] * sy, x1 = v[2 * c + 1] * sy;
+                    const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+                    const __half l0 = __float2half_rn(x0 - __half2float(h0));
+                    const __half l1 = __float2half_rn(x1 - __half2float(h1));
+                    hi[c] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+                    lo[c] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+                }
+                tmem_st8(ta + 8u * (uint32_t)h, hi);
+                tmem_st8(ta + 16u + 8u * (uint32_t)h, lo);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&raw_empty[rr.slot]);   // the tile has been read
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[as]);
+        }
+    } else {
+        // ---------------------- epilogue (16 warps) ----------------------
+        constexpr int kCols = BN / 4;
+        const int quad = warp & 3;
+        const int part = (warp - kTFirstEpi) >> 2;
+        const int64_t row = m0 + 32 * quad + lane;
+        const int64_t c0 = r0 + part * kCols;
+        float* gw = gsm + (warp - kTFirstEpi) * 2 * kCols;
+        float acc[kCols];
+#pragma unroll
+        for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
+        auto fetch_g = [&](int64_t pi, int buf) {
+            for (int e = lane; e < kCols; e += 32) {
+                const bool in = (c0 + e < a.R) && (pi < pre_hi);
+                const float* src = in ? a.gtab + pi * a.R + c0 + e : a.gtab;
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                                 smem_u32(gw + buf * kCols + e)),
+                             "l"(src), "r"(in ? 4 : 0)
+                             : "memory");
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        fetch_g(pre_lo, 0);
+        int gb = 0;
+        int zb = 0;
+        uint32_t zph = 0;
+        bool ok = true;
+        for (int jc = 0; jc < njc && ok; ++jc) {
+            const int ck = chunk_len(jc);
+            for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+                __syncwarp();
+                fetch_g(pi + 1 < pre_hi ? pi + 1 : pre_lo, gb ^ 1);
+                const float* g_cur = gw + gb * kCols;
+                for (int q0 = 0; q0 < ck; q0 += kChunkSteps) {
+                    if (!warp_wait(&zfull[zb], (zph >> zb) & 1u, abort_flag, a.status, kStatusTimeoutEpi)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tbase =
+                        tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
+#pragma unroll
+                    for (int cc = 0; cc < kCols; cc += 8) {
+                        uint32_t z[8];
+                        tmem_ld8(tbase + cc, z);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const float4 g = *reinterpret_cast<const float4*>(g_cur + cc + 4 * q);
+                            acc[cc + 4 * q + 0] = fmaf(g.x, __uint_as_float(z[4 * q + 0]), acc[cc + 4 * q + 0]);
+                            acc[cc + 4 * q + 1] = fmaf(g.y, __uint_as_float(z[4 * q + 1]), acc[cc + 4 * q + 1]);
+                            acc[cc + 4 * q + 2] = fmaf(g.z, __uint_as_float(z[4 * q + 2]), acc[cc + 4 * q + 2]);
+                            acc[cc + 4 * q + 3] = fmaf(g.w, __uint_as_float(z[4 * q + 3]), acc[cc + 4 * q + 3]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&zempty[zb]);
+                    zph ^= 1u << zb;
+                    zb ^= 1;
+                }
+                gb ^= 1;
+            }
+        }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        if (!*abort_flag && row < a.I) {
+            // undo the power-of-two scales of Y and of each Binner column
+            const float inv_y = pow2_unscale(*a.ymax_bits);
+#pragma unroll
+            for (int e = 0; e < kCols; ++e) {
+                const float cs = (c0 + e < a.R) ? a.colscale[c0 + e] : 1.f;
+                acc[e] = acc[e] * inv_y * (1.f / cs);
+            }
+            float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride + row * a.R + c0;
+            const bool vst = (a.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.dst) & 15) == 0);
+#pragma unroll
+            for (int e = 0; e < kCols; e += 4) {
+                if (vst && c0 + e + 4 <= a.R) {
+                    *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (c0 + e + q < a.R) dst[e + q] = acc[e + q];
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Prep: pre-swizzled hi/lo images of the inner Khatri-Rao table
 // ---------------------------------------------------------------------------
 
@@ -1466,6 +1908,113 @@ __global__ void tc_bimage_kernel(BImgArgs a) {
             }
         }
         a.out[e] = half == 0 ? v : v - __uint_as_float(__float_as_uint(v) & kTf32Mask);
+    }
+}
+
+// max |Y| over n fp32 values as fp32 bits (non-negative floats order like their
+// bits); *out must be zero before the launch.
+__global__ void __launch_bounds__(256) absmax_kernel(const float* __restrict__ y, int64_t n,
+                                                     uint32_t* __restrict__ out) {
+    uint32_t m = 0;
+    const bool vec = (reinterpret_cast<uintptr_t>(y) & 15) == 0;
+    const int64_t n4 = vec ? n / 4 : 0;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(y) + i);
+        m = max(m, __float_as_uint(fabsf(v.x)));
+        m = max(m, __float_as_uint(fabsf(v.y)));
+        m = max(m, __float_as_uint(fabsf(v.z)));
+        m = max(m, __float_as_uint(fabsf(v.w)));
+    }
+    for (int64_t i = 4 * n4 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+        m = max(m, __float_as_uint(fabsf(y[i])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ uint32_t wm[8];
+    if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = max(m, wm[w]);
+        atomicMax(out, m);
+    }
+}
+
+// Power-of-two scale of each Binner column: max_j |Binner(j, r)| is the product
+// over the group's modes of max_i |A_n(i, r)|; the scale maps it into
+// [2^13, 2^14) (1 for a zero or non-finite column).
+struct ColScaleArgs {
+    int ngroup;
+    int64_t gdim[kMaxD];
+    const float* gfac[kMaxD];
+    int64_t R;
+    float* out;
+};
+
+__global__ void colscale_kernel(ColScaleArgs a) {
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < a.R;
+         r += (int64_t)gridDim.x * blockDim.x) {
+        float prod = 1.f;
+        for (int t = 0; t < a.ngroup; ++t) {
+            float m = 0.f;
+            for (int64_t i = 0; i < a.gdim[t]; ++i) m = fmaxf(m, fabsf(a.gfac[t][i * a.R + r]));
+            prod *= m;
+        }
+        const uint32_t bits = __float_as_uint(prod);
+        const int e = (int)((bits >> 23) & 0xFFu);
+        float s = 1.f;
+        if (e != 0 && e != 255) {
+            int se = 127 + 13 - (e - 127);
+            se = se < 1 ? 1 : (se > 254 ? 254 : se);
+            s = __uint_as_float((uint32_t)se << 23);
+        }
+        a.out[r] = s;
+    }
+}
+
+// fp16 hi|lo images of the scaled inner KRP table for the two-term fp16 split:
+// per (n-tile, K-step of 32): hi image [BN rows][32 fp16] then lo image, rows of
+// 64 bytes, 64-byte swizzled (16-byte chunk c of row n at (c ^ (n >> 1)) & 3).
+__global__ void tc_bimage_h2_kernel(BImgArgs a, const float* __restrict__ colscale) {
+    const int64_t per_block = 2LL * a.BN * kBK2;  // fp16 elements (hi + lo)
+    const int64_t n = a.nblocks * per_block;
+    __half* out = reinterpret_cast<__half*>(a.out);
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t blk = e / per_block;
+        const int64_t w = e - blk * per_block;
+        const int half = (int)(w / (a.BN * kBK2));
+        const int64_t w2 = w - (int64_t)half * a.BN * kBK2;
+        const uint32_t byte = (uint32_t)(w2 * 2);
+        const uint32_t row = byte / 64u;
+        const uint32_t chunk_pos = (byte % 64u) / 16u;
+        const uint32_t elem = (byte % 16u) / 2u;
+        const uint32_t kk = ((chunk_pos ^ (row >> 1)) & 3u) * 8u + elem;
+        const int64_t nt = blk / a.KS;
+        const int ks = (int)(blk - nt * a.KS);
+        const int64_t r = nt * a.BN + row;
+        int64_t j;
+        bool valid;
+        if (a.inner) {
+            j = (int64_t)ks * kBK2 + kk;
+            valid = j < a.J;
+        } else {
+            const int jp = ks / a.jq_steps;
+            const int64_t jq = (int64_t)(ks - jp * a.jq_steps) * kBK2 + kk;
+            valid = jq < a.Jq;
+            j = (int64_t)jp * a.Jq + jq;
+        }
+        float v = 0.f;
+        if (valid && r < a.R) {
+            int64_t rem = j;
+            v = colscale[r];
+            for (int m = a.ngroup - 1; m >= 0; --m) {
+                const int64_t idx = rem % a.gdim[m];
+                rem /= a.gdim[m];
+                v *= a.gfac[m][idx * a.R + r];
+            }
+        }
+        const __half h = __float2half_rn(v);
+        out[e] = half == 0 ? h : __float2half_rn(v - __half2float(h));
     }
 }
 
@@ -1586,7 +2135,7 @@ bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides,
     }
     if (mp.tc_inner) {
         if (mg.slot[kRoleI] != 0) return false;   // i contiguous
-        mg.box[mg.slot[kRoleJq]] = kBK;
+        mg.box[mg.slot[kRoleJq]] = (uint32_t)mp.tc_kw;
         if (mp.tc_small) {
             const int batch_role = sizeQ > 1 ? kRolePQ : kRolePP;
             if (mg.slot[batch_role] < 0 || mp.tc_ps < 2 || mp.tc_ps > 256 || (g.I * 4) % 16 != 0)
@@ -1598,7 +2147,7 @@ bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides,
         }
     } else {
         if (mg.slot[kRoleJq] != 0) return false;
-        mg.box[0] = kBK;
+        mg.box[0] = (uint32_t)mp.tc_kw;
         if (mp.tc_small) {
             // tc_ps consecutive pre indices along the fastest pre dimension
             const int batch_role = sizeQ > 1 ? kRolePQ : kRolePP;
@@ -1623,6 +2172,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     }
     return fn;
+}
+
+template <bool INNER>
+cudaError_t launch_h2(const TcArgs& args, dim3 grid, cudaStream_t s) {
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tc_h2_kernel<INNER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)SmemH2::kTotal);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    tc_h2_kernel<INNER><<<grid, kTThreads, SmemH2::kTotal, s>>>(args);
+    return cudaGetLastError();
 }
 
 template <bool INNER>
@@ -1661,8 +2227,12 @@ cudaError_t launch_main(const TcArgs& args, dim3 grid, cudaStream_t s) {
 }
 
 size_t bimg_bytes(const ModePlan& mp) {
-    return (size_t)cdiv64(mp.g.R, mp.bn) * mp.tc_ks * 2 * (size_t)mp.bn * kBK * sizeof(float);
+    // per K-step: hi and lo images of bn rows x 64 bytes (16 fp32 or 32 fp16)
+    return (size_t)cdiv64(mp.g.R, mp.bn) * mp.tc_ks * 2 * (size_t)mp.bn * 64;
 }
+
+// fp16 split: the column scales follow the images
+size_t colscale_offset(const ModePlan& mp) { return (bimg_bytes(mp) + 255) / 256 * 256; }
 
 // Small I_k (16..64): floor(128 / I_k) pre indices are stacked in one 128-row
 // tile (for the innermost mode the TMA box's i extent, I_k * 4 bytes, must be a
@@ -1673,7 +2243,9 @@ bool small_eligible(const ModeGeom& g) {
 
 }  // namespace
 
-size_t tc_binner_bytes(const ModePlan& mp) { return bimg_bytes(mp); }
+size_t tc_binner_bytes(const ModePlan& mp) {
+    return mp.tc_h2 ? colscale_offset(mp) + (size_t)mp.g.R * sizeof(float) : bimg_bytes(mp);
+}
 
 bool tc_prefer(const ModePlan& mp) {
     // the 128-row tile must be reasonably full (directly, or with several pre
@@ -1691,14 +2263,18 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
     // innermost mode with large R: A staged in tensor memory (the i-contiguous
     // tile is transposed on the way into TMEM, no shared-memory round trip)
     mp.tc_tmem = (!mp.tc_small && g.R >= TC_TMEM_MIN_R && (mp.tc_inner || TC_TMEM_KMAJOR)) ? 1 : 0;
+    // large R, any mode: the two-term fp16 split in tensor memory
+    mp.tc_h2 = (!mp.tc_small && g.R >= TC_H2_MIN_R) ? 1 : 0;
+    if (mp.tc_h2) mp.tc_tmem = 1;
+    mp.tc_kw = mp.tc_h2 ? kBK2 : kBK;
     mp.bm = kBM;
     mp.bn = mp.tc_tmem ? kTBN : g.R >= 192 ? 256 : (g.R > 64 ? 128 : 64);
     if (mp.tc_inner) {
         if (g.J > g.Jq && g.Jq != 1) return false;
         mp.tc_jq_steps = 1;
-        mp.tc_ks = (int)cdiv64(g.J, kBK);
+        mp.tc_ks = (int)cdiv64(g.J, mp.tc_kw);
     } else {
-        mp.tc_jq_steps = (int)cdiv64(g.Jq, kBK);
+        mp.tc_jq_steps = (int)cdiv64(g.Jq, mp.tc_kw);
         mp.tc_ks = (int)((g.J / g.Jq) * mp.tc_jq_steps);
     }
     if ((!mp.tc_small && cdiv64(g.I, kBM) > 65535) || g.npre >= ((int64_t)1 << 31)) return false;
@@ -1757,7 +2333,9 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     CUresult cr = encode(&args.ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)mg.rank,
                          const_cast<float*>(Y), gdim, gstride, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         mp.tc_inner ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B,
+                         mp.tc_inner ? CU_TENSOR_MAP_SWIZZLE_NONE
+                         : mp.tc_h2  ? CU_TENSOR_MAP_SWIZZLE_128B   // 32 fp32 = 128-byte rows
+                                     : CU_TENSOR_MAP_SWIZZLE_64B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) {
         snprintf(errbuf, errlen, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
@@ -1768,6 +2346,38 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
 
     // B images
     float* bimg = static_cast<float*>(binner_ws);
+    float* colscale = reinterpret_cast<float*>(static_cast<uint8_t*>(binner_ws) + colscale_offset(mp));
+    // the first bytes of the workspace (reserved region) hold max |Y| as fp32 bits
+    uint32_t* ymax = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(binner_ws) - mp.off_binner);
+    if (mp.tc_h2) {
+        cudaError_t e = cudaMemsetAsync(ymax, 0, sizeof(uint32_t), stream);
+        if (e == cudaSuccess) {
+            int64_t numel = 1;
+            for (int t = 0; t < p.d; ++t) numel *= p.dims[t];
+            int64_t blocks = cdiv64(numel / 4 + 1, 256);
+            if (blocks > 152 * 8) blocks = 152 * 8;
+            absmax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, numel, ymax);
+            e = cudaGetLastError();
+        }
+        if (e == cudaSuccess) {
+            ColScaleArgs c;
+            memset(&c, 0, sizeof(c));
+            c.ngroup = g.ngroup;
+            for (int t = 0; t < g.ngroup; ++t) {
+                c.gdim[t] = p.dims[g.group[t]];
+                c.gfac[t] = factors[g.group[t]];
+            }
+            c.R = g.R;
+            c.out = colscale;
+            colscale_kernel<<<(unsigned)cdiv64(g.R, 256), 256, 0, stream>>>(c);
+            e = cudaGetLastError();
+        }
+        if (e != cudaSuccess) {
+            snprintf(errbuf, errlen, "scale launch: %s", cudaGetErrorString(e));
+            return MTTKRP_ERR_CUDA;
+        }
+        *nlaunch += 2;
+    }
     {
         BImgArgs b;
         memset(&b, 0, sizeof(b));
@@ -1785,10 +2395,13 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
         b.inner = mp.tc_inner;
         b.nblocks = cdiv64(g.R, mp.bn) * mp.tc_ks;
         b.out = bimg;
-        const int64_t n = b.nblocks * 2 * mp.bn * kBK;
+        const int64_t n = b.nblocks * 2 * mp.bn * mp.tc_kw;
         int64_t blocks = cdiv64(n, 256);
         if (blocks > 152 * 16) blocks = 152 * 16;
-        tc_bimage_kernel<<<(unsigned)blocks, 256, 0, stream>>>(b);
+        if (mp.tc_h2)
+            tc_bimage_h2_kernel<<<(unsigned)blocks, 256, 0, stream>>>(b, colscale);
+        else
+            tc_bimage_kernel<<<(unsigned)blocks, 256, 0, stream>>>(b);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) {
             snprintf(errbuf, errlen, "B image launch: %s", cudaGetErrorString(e));
@@ -1814,7 +2427,9 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     args.jq_steps = mp.tc_jq_steps;
     args.ps = mp.tc_small ? mp.tc_ps : 1;
     args.batch_len = nQ > 1 ? nQ : g.npre;
-    args.y_box_bytes = (uint32_t)kBK * 4u * (mp.tc_small ? (uint32_t)(g.I * mp.tc_ps) : (uint32_t)kBM);
+    args.y_box_bytes = (uint32_t)mp.tc_kw * 4u * (mp.tc_small ? (uint32_t)(g.I * mp.tc_ps) : (uint32_t)kBM);
+    args.ymax_bits = ymax;
+    args.colscale = colscale;
     {
         int n = g_withhold_signal.load();
         while (n > 0 && !g_withhold_signal.compare_exchange_weak(n, n - 1)) {
@@ -1830,7 +2445,9 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     dim3 grid((unsigned)cdiv64(g.R, mp.bn), mp.tc_small ? 1u : (unsigned)cdiv64(g.I, kBM),
               (unsigned)mp.splits);
     cudaError_t e;
-    if (mp.tc_tmem) {
+    if (mp.tc_h2) {
+        e = mp.tc_inner ? launch_h2<true>(args, grid, stream) : launch_h2<false>(args, grid, stream);
+    } else if (mp.tc_tmem) {
         e = mp.tc_inner ? launch_tmem<true>(args, grid, stream) : launch_tmem<false>(args, grid, stream);
     } else if (mp.tc_small && mp.tc_inner) {
         e = mp.bn == 256 ? launch_main<256, true, true>(args, grid, stream)
