@@ -1462,6 +1462,12 @@ struct SmemH2 {
     static_assert((2 * kRaw + 2 * kTASlots + 7) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
+__device__ __forceinline__ uint32_t half2_bits(__half2 h) {
+    uint32_t u;
+    memcpy(&u, &h, sizeof(u));
+    return u;
+}
+
 // power of two that maps the largest magnitude m (as fp32 bits) into [2^13, 2^14)
 __device__ __forceinline__ float pow2_scale(uint32_t mbits) {
     const int e = (int)((mbits >> 23) & 0xFFu);   // biased exponent of m
@@ -1741,12 +1747,14 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
                 uint32_t hi[8], lo[8];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
+                    // packed conversions: hi = fp16x2(x), lo = fp16x2(x - hi) (x - hi is
+                    // exact in fp32)
                     const float x0 = v[2 * c] * sy, x1 = v[2 * c + 1] * sy;
-                    const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-                    const __half l0 = __float2half_rn(x0 - __half2float(h0));
-                    const __half l1 = __float2half_rn(x1 - __half2float(h1));
-                    hi[c] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-                    lo[c] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+                    const __half2 h = __floats2half2_rn(x0, x1);
+                    const float2 hf = __half22float2(h);
+                    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+                    hi[c] = half2_bits(h);
+                    lo[c] = half2_bits(l);
                 }
                 tmem_st8(ta + 8u * (uint32_t)h, hi);
                 tmem_st8(ta + 16u + 8u * (uint32_t)h, lo);
