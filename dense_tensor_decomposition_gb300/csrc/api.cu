@@ -420,6 +420,7 @@ int mttkrp(mttkrp_plan_t h, const float* Y, const float* const* factors, int mod
     if (mode < 0 || mode >= p->d) return fail(MTTKRP_ERR_INVALID, "mode %d outside [0, %d)", mode, p->d);
     if (Y == nullptr || factors == nullptr || out == nullptr)
         return fail(MTTKRP_ERR_INVALID, "NULL tensor, factor array or output");
+    p->ymax_ready = 0;
     return run_mode(*p, Y, factors, mode, out, static_cast<cudaStream_t>(stream));
 }
 
@@ -434,6 +435,7 @@ int mttkrp_all_modes(mttkrp_plan_t h, const float* Y, const float* const* factor
         if (factors[k] == nullptr) return fail(MTTKRP_ERR_INVALID, "factor %d is NULL", k);
         if (outs[k] == nullptr) return fail(MTTKRP_ERR_INVALID, "output %d is NULL", k);
     }
+    p->ymax_ready = 0;   // one max |Y| pass serves every mode of this call
     for (int k = 0; k < p->d; ++k) {
         int rc = run_mode(*p, Y, factors, k, outs[k], static_cast<cudaStream_t>(stream));
         if (rc != MTTKRP_OK) return rc;
@@ -461,11 +463,11 @@ int mttkrp_plan_describe(mttkrp_plan_t h, int mode, char* buf, size_t len) {
     int n = snprintf(tmp, sizeof(tmp),
                      "mode=%d path=%s tile=%dx%d inner_group=[%s] J=%lld Jq=%lld pre_modes=[%s] "
                      "npre=%lld splits=%lld pre_per_split=%lld workspace=%zu tc_ksteps=%d tc_inner=%d tc_slots=%d "
-                     "tc_tmem_a=%d",
+                     "tc_tmem_a=%d tc_fp16x2=%d",
                      mode, mp.path == MTTKRP_PATH_TC ? "tc" : "simt", mp.bm, mp.bn, groups,
                      (long long)g.J, (long long)g.Jq, pres, (long long)g.npre,
                      (long long)mp.splits, (long long)mp.pre_per_split, mp.total, mp.tc_ks, mp.tc_inner,
-                     mp.tc_small ? mp.tc_ps : 1, mp.tc_tmem);
+                     mp.tc_small ? mp.tc_ps : 1, mp.tc_tmem, mp.tc_h2);
     if (buf != nullptr && len > 0) {
         strncpy(buf, tmp, len - 1);
         buf[len - 1] = 0;

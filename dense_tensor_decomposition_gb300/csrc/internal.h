@@ -79,6 +79,8 @@ struct Plan {
     void* ws;
     size_t ws_bytes;
     int64_t launches;  // kernels launched so far
+    // max |Y| (fp16-split path) already computed for the current call's Y
+    mutable int ymax_ready;
     // benchmark timing: event pairs around the main kernel of each mode
     int timing;
     int ev_cap[kMaxD];

@@ -150,6 +150,19 @@ __device__ __forceinline__ uint32_t mbar_try_wait_suspend(uint64_t* bar, uint32_
     return ok;
 }
 
+// Non-blocking test of a phase (returns at once).
+__device__ __forceinline__ uint32_t mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok;
+}
+
 // Slow path of wait_bounded: suspend-and-retry until the phase completes, the
 // CTA is aborted, or kWaitNs pass (then the CTA is aborted and `code` recorded).
 #ifndef TC_WAIT_INLINE
@@ -419,7 +432,7 @@ __device__ __forceinline__ uint32_t sw64_off(uint32_t row, uint32_t chunk) {
 #define TC_TMEM_KMAJOR 0
 #endif
 #ifndef TC_H2_MIN_R
-#define TC_H2_MIN_R 448
+#define TC_H2_MIN_R 160
 #endif
 #ifndef TC_TMEM_MIN_R
 #define TC_TMEM_MIN_R 448
@@ -1442,6 +1455,9 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_tmem_kernel(const __grid_cons
 constexpr int kBK2 = 32;
 constexpr int kChunkSteps2 = 4;   // 128 contraction indices between TMEM drains
 
+#ifndef TC_PREFETCH
+#define TC_PREFETCH 1
+#endif
 #ifndef TC_H2_STAGES
 #define TC_H2_STAGES 6
 #endif
@@ -1468,11 +1484,17 @@ __device__ __forceinline__ uint32_t half2_bits(__half2 h) {
     return u;
 }
 
-// power of two that maps the largest magnitude m (as fp32 bits) into [2^13, 2^14)
+// Power of two that maps the largest magnitude m (fp32 bits of a non-negative
+// value) into [2^13, 2^14): fp16 holds the scaled values with room to spare,
+// and their lo parts stay normal down to 2^-11 of the largest.  m = 0 or a
+// non-finite m: 1 (nothing to scale; non-finite values propagate).  Subnormal
+// m uses the exponent of its leading bit; the scale is clamped to the fp32 range.
 __device__ __forceinline__ float pow2_scale(uint32_t mbits) {
-    const int e = (int)((mbits >> 23) & 0xFFu);   // biased exponent of m
-    if (e == 0 || e == 255) return 1.f;           // zero / subnormal / non-finite: no scaling
-    int se = 127 + 13 - (e - 127);                // biased exponent of 2^(13 - (e - 127))
+    const uint32_t m = mbits & 0x7FFFFFFFu;
+    int e = (int)(m >> 23);                       // biased exponent
+    if (m == 0 || e == 255) return 1.f;
+    if (e == 0) e = 1 - (__clz((int)m) - 9);      // subnormal: leading bit of the mantissa
+    int se = 127 + 13 - (e - 127);               // biased exponent of 2^(13 - (e - 127))
     se = se < 1 ? 1 : (se > 254 ? 254 : se);
     return __uint_as_float((uint32_t)se << 23);
 }
@@ -1644,6 +1666,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
             constexpr uint32_t kBLo = L::kB >> 4;
             int as = 0;
             uint32_t aph = 0;
+            bool a_ready = false;   // a_full[as] already observed complete (prefetched test)
             int zb = 0;
             uint32_t zph = 0;
             uint32_t zused = 0;
@@ -1668,7 +1691,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
                             }
                             tc_fence_after();
                         }
-                        if (!wait_bounded(&a_full[as], aph, abort_flag, a.status, kStatusTimeoutMma)) {
+                        if (!a_ready && !wait_bounded(&a_full[as], aph, abort_flag, a.status, kStatusTimeoutMma)) {
                             ok = false;
                             break;
                         }
@@ -1698,6 +1721,9 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
                             as = 0;
                             aph ^= 1u;
                         }
+                        // non-blocking test of the next slot; its answer is used at the
+                        // top of the next K-step, so its latency overlaps the bookkeeping
+                        a_ready = TC_PREFETCH && mbar_test_wait(&a_full[as], aph) != 0;
                     }
                 }
                 if (ok) mma_commit(bempty);
@@ -1967,15 +1993,7 @@ __global__ void colscale_kernel(ColScaleArgs a) {
             for (int64_t i = 0; i < a.gdim[t]; ++i) m = fmaxf(m, fabsf(a.gfac[t][i * a.R + r]));
             prod *= m;
         }
-        const uint32_t bits = __float_as_uint(prod);
-        const int e = (int)((bits >> 23) & 0xFFu);
-        float s = 1.f;
-        if (e != 0 && e != 255) {
-            int se = 127 + 13 - (e - 127);
-            se = se < 1 ? 1 : (se > 254 ? 254 : se);
-            s = __uint_as_float((uint32_t)se << 23);
-        }
-        a.out[r] = s;
+        a.out[r] = pow2_scale(__float_as_uint(prod));
     }
 }
 
@@ -2271,8 +2289,14 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
     // innermost mode with large R: A staged in tensor memory (the i-contiguous
     // tile is transposed on the way into TMEM, no shared-memory round trip)
     mp.tc_tmem = (!mp.tc_small && g.R >= TC_TMEM_MIN_R && (mp.tc_inner || TC_TMEM_KMAJOR)) ? 1 : 0;
-    // large R, any mode: the two-term fp16 split in tensor memory
-    mp.tc_h2 = (!mp.tc_small && g.R >= TC_H2_MIN_R) ? 1 : 0;
+    // the two-term fp16 split in tensor memory (128 x 224 tiles) does a K-step
+    // about 1.4 times faster than the tf32 kernel (128 x 256 tiles): it wins
+    // unless its narrower tiles waste more columns than that
+    {
+        const int64_t h2_cols = cdiv64(g.R, kTBN) * kTBN * 10;
+        const int64_t tf_cols = cdiv64(g.R, 256) * 256 * 14;
+        mp.tc_h2 = (!mp.tc_small && g.R >= TC_H2_MIN_R && h2_cols < tf_cols) ? 1 : 0;
+    }
     if (mp.tc_h2) mp.tc_tmem = 1;
     mp.tc_kw = mp.tc_h2 ? kBK2 : kBK;
     mp.bm = kBM;
@@ -2358,14 +2382,19 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     // the first bytes of the workspace (reserved region) hold max |Y| as fp32 bits
     uint32_t* ymax = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(binner_ws) - mp.off_binner);
     if (mp.tc_h2) {
-        cudaError_t e = cudaMemsetAsync(ymax, 0, sizeof(uint32_t), stream);
-        if (e == cudaSuccess) {
+        cudaError_t e = cudaSuccess;
+        if (!p.ymax_ready) e = cudaMemsetAsync(ymax, 0, sizeof(uint32_t), stream);
+        if (e == cudaSuccess && !p.ymax_ready) {
             int64_t numel = 1;
             for (int t = 0; t < p.d; ++t) numel *= p.dims[t];
             int64_t blocks = cdiv64(numel / 4 + 1, 256);
             if (blocks > 152 * 8) blocks = 152 * 8;
             absmax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, numel, ymax);
             e = cudaGetLastError();
+            if (e == cudaSuccess) {
+                p.ymax_ready = 1;
+                ++*nlaunch;
+            }
         }
         if (e == cudaSuccess) {
             ColScaleArgs c;
@@ -2384,7 +2413,7 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
             snprintf(errbuf, errlen, "scale launch: %s", cudaGetErrorString(e));
             return MTTKRP_ERR_CUDA;
         }
-        *nlaunch += 2;
+        ++*nlaunch;
     }
     {
         BImgArgs b;

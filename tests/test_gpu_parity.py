@@ -280,3 +280,54 @@ def test_timing_events_and_launch_count(path):
         assert len(t) == 2 and all(x > 0 for x in t)
     assert plan.launch_count() >= 2 * 3 * 2
     assert mk.device_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# value ranges for the fp16-split tensor-core kernel (power-of-two scaling)
+# ---------------------------------------------------------------------------
+
+H2_SHAPES = [((130, 40, 48), 300), ((40, 36, 128), 450)]
+
+
+def h2_modes(plan, d):
+    """Modes the plan runs on the fp16-split tensor-core kernel."""
+    return [k for k in range(d) if "tc_fp16x2=1" in plan.describe(k)]
+
+
+@pytest.mark.parametrize("dims,R", H2_SHAPES)
+@pytest.mark.parametrize("yscale,ascale", [(1e30, 1e-20), (1e-30, 1e10), (1e-38, 1.0), (3.0, 1e-12)])
+def test_scaled_values(dims, R, yscale, ascale):
+    """Magnitudes far from 1 (fp16 alone would overflow or flush them): the
+    split scales Y and each inner-table column by powers of two.  (The tf32
+    kernels take the raw fp32 tile as their hi operand, so their lo terms are
+    lost for values within 2^-11 of the fp32 normal range; only the modes that
+    run on the fp16 split are checked here.)"""
+    Y, A = synth.random_case(500 + R, dims, R)
+    Y = (Y.astype(np.float64) * yscale).astype(np.float32)
+    A = [(a.astype(np.float64) * ascale).astype(np.float32) for a in A]
+    plan = make_plan(dims, R, "auto")
+    modes = h2_modes(plan, len(dims))
+    assert modes
+    got = gpu_modes(Y, A, "auto", modes=modes, plan=plan)
+    for k in modes:
+        ref = oracle.mttkrp(Y, A, k)
+        assert np.isfinite(got[k]).all()
+        assert rel_fro(got[k], ref) <= TOL, f"{dims} k={k} scales {yscale},{ascale}"
+
+
+@pytest.mark.parametrize("dims,R", H2_SHAPES)
+def test_outlier_zero_column_and_zero_tensor(dims, R):
+    Y, A = synth.random_case(600 + R, dims, R)
+    Y = Y.copy()
+    Y.flat[12345 % Y.size] = 1.0e6          # one outlier sets the scale of Y
+    A = [a.copy() for a in A]
+    for a in A:
+        a[:, 7] = 0.0                        # an all-zero factor column
+    got = gpu_modes(Y, A, "auto")
+    for k in range(len(dims)):
+        ref = oracle.mttkrp(Y, A, k)
+        assert rel_fro(got[k], ref) <= TOL
+        assert not got[k][:, 7].any()
+    zero = gpu_modes(np.zeros_like(Y), A, "auto")
+    for k in range(len(dims)):
+        assert not zero[k].any()
