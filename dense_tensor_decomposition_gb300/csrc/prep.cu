@@ -3,8 +3,9 @@
 //    Binner (inner group) that the main kernels combine into Khatri-Rao rows
 //    on the fly, plus the Y base offset of every pre index;
 //  * the split reductions add the per-split partial results in a fixed order
-//    in fp64 and write the fp32 output (no atomics anywhere, so results are
-//    bitwise reproducible for a given plan).
+//    (compensated fp32 when every thread sums all splits of its outputs, fp64
+//    when warps share the splits) and write the fp32 output; no atomics
+//    anywhere, so results are bitwise reproducible for a given plan.
 #include "internal.h"
 
 namespace mk {
@@ -118,6 +119,15 @@ __global__ void __launch_bounds__(kRedWarps * 32)
     }
 }
 
+// Compensated fp32 addition (Neumaier): sum + c carries the exact running total
+// to about one fp32 rounding, independent of the number of terms; GB300's fp64
+// rate is too low for a bandwidth-bound sum of this size.
+__device__ __forceinline__ void kahan_add(float& sum, float& c, float x) {
+    const float t = sum + x;
+    c += fabsf(sum) >= fabsf(x) ? (sum - t) + x : (x - t) + sum;
+    sum = t;
+}
+
 // One thread per 4 consecutive outputs, all splits in increasing s with four
 // 16-byte loads in flight (used when there are enough outputs to fill the GPU
 // this way; no shared memory, no block barriers).
@@ -126,7 +136,7 @@ __global__ void __launch_bounds__(256)
                               float4* __restrict__ out) {
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n4;
          e += (int64_t)gridDim.x * blockDim.x) {
-        double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
         const float4* p = part + e;
         int64_t sp = 0;
         for (; sp + 4 <= splits; sp += 4) {
@@ -135,20 +145,20 @@ __global__ void __launch_bounds__(256)
             for (int u = 0; u < 4; ++u) v[u] = __ldcs(p + (sp + u) * n4);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                a0 += (double)v[u].x;
-                a1 += (double)v[u].y;
-                a2 += (double)v[u].z;
-                a3 += (double)v[u].w;
+                kahan_add(s0, c0, v[u].x);
+                kahan_add(s1, c1, v[u].y);
+                kahan_add(s2, c2, v[u].z);
+                kahan_add(s3, c3, v[u].w);
             }
         }
         for (; sp < splits; ++sp) {
             const float4 v = __ldcs(p + sp * n4);
-            a0 += (double)v.x;
-            a1 += (double)v.y;
-            a2 += (double)v.z;
-            a3 += (double)v.w;
+            kahan_add(s0, c0, v.x);
+            kahan_add(s1, c1, v.y);
+            kahan_add(s2, c2, v.z);
+            kahan_add(s3, c3, v.w);
         }
-        out[e] = make_float4((float)a0, (float)a1, (float)a2, (float)a3);
+        out[e] = make_float4(s0 + c0, s1 + c1, s2 + c2, s3 + c3);
     }
 }
 

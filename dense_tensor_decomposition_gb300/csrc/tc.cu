@@ -1984,17 +1984,25 @@ struct ColScaleArgs {
     float* out;
 };
 
-__global__ void colscale_kernel(ColScaleArgs a) {
-    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < a.R;
-         r += (int64_t)gridDim.x * blockDim.x) {
-        float prod = 1.f;
-        for (int t = 0; t < a.ngroup; ++t) {
-            float m = 0.f;
-            for (int64_t i = 0; i < a.gdim[t]; ++i) m = fmaxf(m, fabsf(a.gfac[t][i * a.R + r]));
+// one block per 32 columns: 8 row groups x 32 columns, reduced through shared memory
+__global__ void __launch_bounds__(256) colscale_kernel(ColScaleArgs a) {
+    __shared__ float red[8][33];
+    const int lc = threadIdx.x & 31, lr = threadIdx.x >> 5;
+    const int64_t r = (int64_t)blockIdx.x * 32 + lc;
+    float prod = 1.f;
+    for (int t = 0; t < a.ngroup; ++t) {
+        float m = 0.f;
+        if (r < a.R)
+            for (int64_t i = lr; i < a.gdim[t]; i += 8) m = fmaxf(m, fabsf(a.gfac[t][i * a.R + r]));
+        red[lr][lc] = m;
+        __syncthreads();
+        if (lr == 0) {
+            for (int q = 1; q < 8; ++q) m = fmaxf(m, red[q][lc]);
             prod *= m;
         }
-        a.out[r] = pow2_scale(__float_as_uint(prod));
+        __syncthreads();
     }
+    if (lr == 0 && r < a.R) a.out[r] = pow2_scale(__float_as_uint(prod));
 }
 
 // fp16 hi|lo images of the scaled inner KRP table for the two-term fp16 split:
@@ -2406,7 +2414,7 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
             }
             c.R = g.R;
             c.out = colscale;
-            colscale_kernel<<<(unsigned)cdiv64(g.R, 256), 256, 0, stream>>>(c);
+            colscale_kernel<<<(unsigned)cdiv64(g.R, 32), 256, 0, stream>>>(c);
             e = cudaGetLastError();
         }
         if (e != cudaSuccess) {
