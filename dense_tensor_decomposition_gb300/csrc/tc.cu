@@ -1461,13 +1461,32 @@ constexpr int kChunkSteps2 = 4;   // 128 contraction indices between TMEM drains
 #ifndef TC_H2_STAGES
 #define TC_H2_STAGES 6
 #endif
+// Tile 128 x kH2BN; TMEM: accumulators at [0, BN) and [BN, 2 BN), then kH2Slots
+// A slots of 32 columns (hi 16 | lo 16, one K-step each).  Producers and MMAs
+// hand the slots over in groups of kH2Group K-steps (one barrier round trip per
+// group), kH2Slots / kH2Group groups in flight.  Measured on 512^3, R = 2000:
+// 128 x 224 with single-step groups (two slots) is the fastest per output
+// column; 128 x 192 with four slots, in groups of one or two K-steps, was 9-11 %
+// slower per column (the MMA issuer's per-step cost does not shrink with N).
+#ifndef TC_H2_BN
+#define TC_H2_BN 224
+#endif
+#ifndef TC_H2_GROUP
+#define TC_H2_GROUP 1
+#endif
+constexpr int kH2BN = TC_H2_BN;
+constexpr int kH2Slots = (512 - 2 * kH2BN) / 32 < 4 ? (512 - 2 * kH2BN) / 32 : 4;
+constexpr int kH2Group = TC_H2_GROUP;
+constexpr uint32_t kH2ACol0 = 2 * kH2BN;
+static_assert(kH2Slots >= 2 * kH2Group, "two A-slot groups in flight");
+
 struct SmemH2 {
     static constexpr uint32_t kY = kBM * kBK2 * 4;     // 16 KB raw fp32 Y tile
-    static constexpr uint32_t kB = kTBN * kBK2 * 2;    // 14 KB: one K-step of B (hi or lo, fp16)
+    static constexpr uint32_t kB = kH2BN * kBK2 * 2;   // one K-step of B (hi or lo, fp16): BN x 64 B
     static constexpr int kCK = 4;                      // K-steps per B-chunk
     static constexpr uint32_t kBRes = kCK * 2 * kB;    // 112 KB resident B-chunk
     static constexpr int kRaw = TC_H2_STAGES;
-    static constexpr uint32_t kG = kEpiWarps * 2 * (kTBN / 4) * 4;
+    static constexpr uint32_t kG = kEpiWarps * 2 * (kH2BN / 4) * 4;
     static constexpr uint32_t kBarBytes = 512;
     static constexpr uint32_t kOffRaw = kBRes;
     static constexpr uint32_t kOffG = kOffRaw + kRaw * kY;
@@ -1475,7 +1494,7 @@ struct SmemH2 {
     static constexpr uint32_t kTotal = 1024 + kOffBars + kBarBytes;
     static_assert(kTotal <= 232448, "shared memory budget");
     static_assert(kB % 512 == 0 && kY % 1024 == 0, "swizzle-atom alignment");
-    static_assert((2 * kRaw + 2 * kTASlots + 7) * 8 + 8 <= kBarBytes, "barrier area");
+    static_assert((2 * kRaw + 2 * 2 + 7) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
 __device__ __forceinline__ uint32_t half2_bits(__half2 h) {
@@ -1517,10 +1536,10 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uin
 template <bool INNER>
 __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_constant__ TcArgs a) {
     using L = SmemH2;
-    constexpr int BN = kTBN;
+    constexpr int BN = kH2BN;
     constexpr int CK = L::kCK;
     constexpr int NR = L::kRaw;
-    constexpr int NA = kTASlots;
+    constexpr int NG = kH2Slots / kH2Group;   // A-slot groups in flight
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~(uintptr_t)1023);
@@ -1530,9 +1549,9 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBars);
     uint64_t* raw_full = bars;                  // [NR] TMA landed
     uint64_t* raw_empty = raw_full + NR;        // [NR] producers read the tile
-    uint64_t* a_full = raw_empty + NR;          // [NA] producers wrote the A slot
-    uint64_t* a_empty = a_full + NA;            // [NA] MMAs that read the A slot are done
-    uint64_t* zfull = a_empty + NA;             // [2]
+    uint64_t* a_full = raw_empty + NR;          // [NG] producers wrote the group's A slots
+    uint64_t* a_empty = a_full + NG;            // [NG] MMAs that read the group's A slots are done
+    uint64_t* zfull = a_empty + NG;             // [2]
     uint64_t* zempty = zfull + 2;               // [2]
     uint64_t* bfull = zempty + 2;               // [1]
     uint64_t* bempty = bfull + 1;               // [1]
@@ -1559,7 +1578,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
             mbar_init(&raw_full[s], 1);
             mbar_init(&raw_empty[s], kTProdWarps);
         }
-        for (int s = 0; s < NA; ++s) {
+        for (int s = 0; s < NG; ++s) {
             mbar_init(&a_full[s], kTProdWarps);
             mbar_init(&a_empty[s], 1);
         }
@@ -1664,9 +1683,9 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
             const uint32_t b_w0 = sdesc_lo(smem_u32(bres));
             constexpr uint32_t kBStep = (2 * L::kB) >> 4;
             constexpr uint32_t kBLo = L::kB >> 4;
-            int as = 0;
+            int ag = 0;             // A-slot group of the current K-step (ring of NG)
             uint32_t aph = 0;
-            bool a_ready = false;   // a_full[as] already observed complete (prefetched test)
+            bool a_ready = false;   // a_full[ag] already observed complete (prefetched test)
             int zb = 0;
             uint32_t zph = 0;
             uint32_t zused = 0;
@@ -1691,12 +1710,18 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
                             }
                             tc_fence_after();
                         }
-                        if (!a_ready && !wait_bounded(&a_full[as], aph, abort_flag, a.status, kStatusTimeoutMma)) {
-                            ok = false;
-                            break;
+                        // a group is kH2Group consecutive K-steps of one unit
+                        const bool gstart = q % kH2Group == 0;
+                        const bool gend = q % kH2Group == kH2Group - 1 || q == ck - 1;
+                        if (gstart) {
+                            if (!a_ready && !wait_bounded(&a_full[ag], aph, abort_flag, a.status, kStatusTimeoutMma)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
                         }
-                        tc_fence_after();
-                        const uint32_t ta = tmem + kTACol0 + 32u * (uint32_t)as;
+                        const uint32_t ta =
+                            tmem + kH2ACol0 + 32u * (uint32_t)(ag * kH2Group + q % kH2Group);
                         const uint32_t dz = tmem + (uint32_t)(zb * BN);
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
@@ -1706,7 +1731,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
                             mma_f16_ta(dz, ta + ac, bw + kBLo + adv, idesc, 1u);
                             mma_f16_ta(dz, ta + 16u + ac, bw + adv, idesc, 1u);
                         }
-                        mma_commit(&a_empty[as]);
+                        if (gend) mma_commit(&a_empty[ag]);
                         if (last) {
                             if (a.withhold_signal && zused == 0 && zb == 0) {
                                 // test hook: this buffer is never reported full
@@ -1717,13 +1742,15 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
                             zused |= 1u << zb;
                             zb ^= 1;
                         }
-                        if (++as == NA) {
-                            as = 0;
-                            aph ^= 1u;
+                        if (gend) {
+                            if (++ag == NG) {
+                                ag = 0;
+                                aph ^= 1u;
+                            }
+                            // non-blocking test of the next group; its answer is used at
+                            // the next group start, so its latency overlaps the bookkeeping
+                            a_ready = TC_PREFETCH && mbar_test_wait(&a_full[ag], aph) != 0;
                         }
-                        // non-blocking test of the next slot; its answer is used at the
-                        // top of the next K-step, so its latency overlaps the bookkeeping
-                        a_ready = TC_PREFETCH && mbar_test_wait(&a_full[as], aph) != 0;
                     }
                 }
                 if (ok) mma_commit(bempty);
@@ -1737,60 +1764,81 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
         const int r = 32 * quad + lane;   // tile row of this thread
         const float sy = pow2_scale(*a.ymax_bits);   // Y is scaled by this power of two
         Ring<NR> rr;
-        for (int64_t t = 0; t < T; ++t, rr.next()) {
-            if (!warp_wait(&raw_full[rr.slot], rr.phase, abort_flag, a.status, kStatusTimeoutLo)) break;
-            // A slot t % NA was last read by the MMAs of K-step t - NA
-            const int as = (int)(t % NA);
-            if (t >= NA && !warp_wait(&a_empty[as], (uint32_t)(((t / NA) - 1) & 1), abort_flag, a.status,
-                                      kStatusTimeoutLo))
-                break;
-            tc_fence_after();
-            const uint8_t* st = raw + rr.slot * L::kY;
-            const uint32_t ta = tmem + ((uint32_t)(32 * quad) << 16) + kTACol0 + 32u * (uint32_t)as;
-            // two halves of 16 contraction indices: hi to columns [8h, 8h + 8), lo to
-            // [16 + 8h, 16 + 8h + 8); column c holds k = 2c (low half) and 2c + 1
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float v[16];
-                if (!INNER) {
-                    // row r of the K-major tile: 128 bytes, 128-byte swizzled
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int cc = 4 * h + c;
-                        const float4 x = *reinterpret_cast<const float4*>(
-                            st + (uint32_t)r * 128u + ((((uint32_t)cc ^ (uint32_t)r) & 7u) << 4));
-                        v[4 * c + 0] = x.x;
-                        v[4 * c + 1] = x.y;
-                        v[4 * c + 2] = x.z;
-                        v[4 * c + 3] = x.w;
+        int ag = 0;          // A-slot group of the current K-step (ring of NG)
+        int64_t g = 0;       // groups started so far
+        bool ok = true;
+        for (int jc = 0; jc < njc && ok; ++jc) {
+            const int ck = chunk_len(jc);
+            for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                for (int q = 0; q < ck; ++q, rr.next()) {
+                    const bool gstart = q % kH2Group == 0;
+                    const bool gend = q % kH2Group == kH2Group - 1 || q == ck - 1;
+                    if (!warp_wait(&raw_full[rr.slot], rr.phase, abort_flag, a.status, kStatusTimeoutLo)) {
+                        ok = false;
+                        break;
                     }
-                } else {
-                    // column r of the [32 j][128 i] staging tile
-                    const float* stg = reinterpret_cast<const float*>(st);
+                    if (gstart) {
+                        // the group's slots were last read by the MMAs of group g - NG
+                        if (g >= NG && !warp_wait(&a_empty[ag], (uint32_t)(((g / NG) - 1) & 1), abort_flag,
+                                                  a.status, kStatusTimeoutLo)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    const uint8_t* st = raw + rr.slot * L::kY;
+                    const uint32_t ta = tmem + ((uint32_t)(32 * quad) << 16) + kH2ACol0 +
+                                        32u * (uint32_t)(ag * kH2Group + q % kH2Group);
+                    // two halves of 16 contraction indices: hi to columns [8h, 8h + 8), lo
+                    // to [16 + 8h, 16 + 8h + 8); column c holds k = 2c (low half), 2c + 1
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = stg[(16 * h + j) * kBM + r];
-                }
-                uint32_t hi[8], lo[8];
+                    for (int h = 0; h < 2; ++h) {
+                        float v[16];
+                        if (!INNER) {
+                            // row r of the K-major tile: 128 bytes, 128-byte swizzled
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    // packed conversions: hi = fp16x2(x), lo = fp16x2(x - hi) (x - hi is
-                    // exact in fp32)
-                    const float x0 = v[2 * c] * sy, x1 = v[2 * c + 1] * sy;
-                    const __half2 h = __floats2half2_rn(x0, x1);
-                    const float2 hf = __half22float2(h);
-                    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
-                    hi[c] = half2_bits(h);
-                    lo[c] = half2_bits(l);
+                            for (int c = 0; c < 4; ++c) {
+                                const int cc = 4 * h + c;
+                                const float4 x = *reinterpret_cast<const float4*>(
+                                    st + (uint32_t)r * 128u + ((((uint32_t)cc ^ (uint32_t)r) & 7u) << 4));
+                                v[4 * c + 0] = x.x;
+                                v[4 * c + 1] = x.y;
+                                v[4 * c + 2] = x.z;
+                                v[4 * c + 3] = x.w;
+                            }
+                        } else {
+                            // column r of the [32 j][128 i] staging tile
+                            const float* stg = reinterpret_cast<const float*>(st);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) v[j] = stg[(16 * h + j) * kBM + r];
+                        }
+                        uint32_t hi[8], lo[8];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            // packed conversions: hi = fp16x2(x), lo = fp16x2(x - hi)
+                            // (x - hi is exact in fp32)
+                            const float x0 = v[2 * c] * sy, x1 = v[2 * c + 1] * sy;
+                            const __half2 hh = __floats2half2_rn(x0, x1);
+                            const float2 hf = __half22float2(hh);
+                            const __half2 ll = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+                            hi[c] = half2_bits(hh);
+                            lo[c] = half2_bits(ll);
+                        }
+                        tmem_st8(ta + 8u * (uint32_t)h, hi);
+                        tmem_st8(ta + 16u + 8u * (uint32_t)h, lo);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&raw_empty[rr.slot]);   // the tile has been read
+                    if (gend) {
+                        tmem_st_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&a_full[ag]);
+                        ++g;
+                        if (++ag == NG) ag = 0;
+                    }
                 }
-                tmem_st8(ta + 8u * (uint32_t)h, hi);
-                tmem_st8(ta + 16u + 8u * (uint32_t)h, lo);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&raw_empty[rr.slot]);   // the tile has been read
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[as]);
         }
     } else {
         // ---------------------- epilogue (16 warps) ----------------------
@@ -2301,14 +2349,14 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
     // about 1.4 times faster than the tf32 kernel (128 x 256 tiles): it wins
     // unless its narrower tiles waste more columns than that
     {
-        const int64_t h2_cols = cdiv64(g.R, kTBN) * kTBN * 10;
+        const int64_t h2_cols = cdiv64(g.R, kH2BN) * kH2BN * 10;
         const int64_t tf_cols = cdiv64(g.R, 256) * 256 * 14;
         mp.tc_h2 = (!mp.tc_small && g.R >= TC_H2_MIN_R && h2_cols < tf_cols) ? 1 : 0;
     }
     if (mp.tc_h2) mp.tc_tmem = 1;
     mp.tc_kw = mp.tc_h2 ? kBK2 : kBK;
     mp.bm = kBM;
-    mp.bn = mp.tc_tmem ? kTBN : g.R >= 192 ? 256 : (g.R > 64 ? 128 : 64);
+    mp.bn = mp.tc_h2 ? kH2BN : mp.tc_tmem ? kTBN : g.R >= 192 ? 256 : (g.R > 64 ? 128 : 64);
     if (mp.tc_inner) {
         if (g.J > g.Jq && g.Jq != 1) return false;
         mp.tc_jq_steps = 1;
