@@ -173,18 +173,29 @@ __device__ __forceinline__ uint32_t mbar_test_wait(uint64_t* bar, uint32_t parit
 #else
 #define TC_WAIT_SLOW_ATTR __noinline__
 #endif
-__device__ TC_WAIT_SLOW_ATTR bool wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                       uint32_t* status, uint32_t code) {
-    const unsigned long long t0 = gtimer();
+// The clock is first read after one suspension has run out without the phase
+// completing, so a wait that ends within the first suspension (the common case)
+// costs no timer read; the bound is kWaitNs plus one suspension.
+__device__ __forceinline__ bool wait_slow_body(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                               uint32_t* status, uint32_t code) {
+    unsigned long long t0 = 0;
+    bool timing = false;
     while (true) {
         if (mbar_try_wait_suspend(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (gtimer() - t0 > kWaitNs) {
+        if (!timing) {
+            t0 = gtimer();
+            timing = true;
+        } else if (gtimer() - t0 > kWaitNs) {
             *abort_flag = 1;
             atomicOr(status, code);
             return false;
         }
     }
+}
+__device__ TC_WAIT_SLOW_ATTR bool wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                       uint32_t* status, uint32_t code) {
+    return wait_slow_body(bar, parity, abort_flag, status, code);
 }
 
 // Wait for the phase of `bar` with the given parity; false if the CTA was
@@ -196,15 +207,33 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
 }
 
 // Like wait_bounded but ignores the abort flag (used to drain in-flight work).
-__device__ __noinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint32_t* status) {
-    const unsigned long long t0 = gtimer();
+__device__ __forceinline__ bool wait_drain_body(uint64_t* bar, uint32_t parity, uint32_t* status) {
+    unsigned long long t0 = 0;
+    bool timing = false;
     while (!mbar_try_wait_suspend(bar, parity)) {
-        if (gtimer() - t0 > kWaitNs) {
+        if (!timing) {
+            t0 = gtimer();
+            timing = true;
+        } else if (gtimer() - t0 > kWaitNs) {
             atomicOr(status, kStatusTimeoutDrain);
             return false;
         }
     }
     return true;
+}
+__device__ __noinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint32_t* status) {
+    return wait_drain_body(bar, parity, status);
+}
+
+// Fully inlined forms for kernels that change their register allotment with
+// setmaxnreg: ptxas cannot allocate registers around calls in such kernels.
+__device__ __forceinline__ bool wait_bounded_inl(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                 uint32_t* status, uint32_t code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow_body(bar, parity, abort_flag, status, code);
+}
+__device__ __forceinline__ bool wait_drain_inl(uint64_t* bar, uint32_t parity, uint32_t* status) {
+    return wait_drain_body(bar, parity, status);
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
@@ -217,6 +246,18 @@ __device__ __forceinline__ void tc_fence_before() {
 
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// TMA box coordinates from the role values: c[p] = role[r] for slot[r] == p,
+// 0 where no role maps (static indexing only, so everything stays in registers)
+__device__ __forceinline__ void tma_coords(const int* slot, const int* role, int* c) {
+#pragma unroll
+    for (int p = 0; p < 5; ++p) {
+        int v = 0;
+#pragma unroll
+        for (int r = 0; r < kRoles; ++r) v = slot[r] == p ? role[r] : v;
+        c[p] = v;
+    }
 }
 
 __device__ __forceinline__ void tma_load(const CUtensorMap* map, int rank, const int* c, void* dst,
@@ -327,6 +368,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
           "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t* r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
@@ -478,6 +525,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
                                           uint32_t* status, uint32_t code) {
     bool ok = true;
     if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, status, code);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+__device__ __forceinline__ bool warp_wait_inl(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              uint32_t* status, uint32_t code) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = wait_bounded_inl(bar, parity, abort_flag, status, code);
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
@@ -645,10 +698,8 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
                         role[kRoleI] = (int)m0;
                         role[kRolePP] = cP;
                         role[kRolePQ] = cQ;
-                        int c[5] = {0, 0, 0, 0, 0};
-#pragma unroll
-                        for (int r = 0; r < kRoles; ++r)
-                            if (a.slot[r] >= 0) c[a.slot[r]] = role[r];
+                        int c[5];
+                        tma_coords(a.slot, role, c);
                         mbar_arrive_expect_tx(&raw_full[rr.slot], a.y_box_bytes);
                         tma_load(&a.ymap, a.rank, c, raw + rr.slot * L::kY, &raw_full[rr.slot]);
                     }
@@ -1222,10 +1273,8 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_tmem_kernel(const __grid_cons
                         role[kRoleI] = (int)m0;
                         role[kRolePP] = cP;
                         role[kRolePQ] = cQ;
-                        int c[5] = {0, 0, 0, 0, 0};
-#pragma unroll
-                        for (int r = 0; r < kRoles; ++r)
-                            if (a.slot[r] >= 0) c[a.slot[r]] = role[r];
+                        int c[5];
+                        tma_coords(a.slot, role, c);
                         mbar_arrive_expect_tx(&raw_full[rr.slot], a.y_box_bytes);
                         tma_load(&a.ymap, a.rank, c, raw + rr.slot * L::kY, &raw_full[rr.slot]);
                     }
@@ -1474,6 +1523,47 @@ constexpr int kChunkSteps2 = 4;   // 128 contraction indices between TMEM drains
 #ifndef TC_H2_GROUP
 #define TC_H2_GROUP 1
 #endif
+#ifndef TC_H2_EPI_LD
+#define TC_H2_EPI_LD 8   // TMEM columns per epilogue load (4 or 8)
+#endif
+// Warp roles.  With the register split (default) the CTA is six warpgroups:
+// producers (warps 0-3, one per TMEM lane quadrant), control (TMA warp 4, MMA
+// warp 5, two idle warps), and four epilogue warpgroups (warps 8-23).  The
+// control and producer warpgroups give registers back (setmaxnreg.dec) and the
+// epilogue warpgroups take them (setmaxnreg.inc), so that the epilogue's
+// register-resident accumulators do not spill.  The launch allots 80 registers
+// a thread (768 threads); the split uses 128 x (56 + 72 + 4 x 88) = 61440 of
+// the 61440 allotted, and the host refuses the launch if the kernel was built
+// with fewer than 80.  Without the split: TMA warp 0, MMA warp 1, producers
+// 2-5, epilogue 6-21.
+#ifndef TC_H2_REGSPLIT
+#define TC_H2_REGSPLIT 1
+#endif
+#if TC_H2_REGSPLIT
+constexpr int kH2ProdWarp0 = 0, kH2TmaWarp = 4, kH2MmaWarp = 5, kH2FirstEpi = 8;
+#else
+constexpr int kH2ProdWarp0 = 2, kH2TmaWarp = 0, kH2MmaWarp = 1, kH2FirstEpi = 6;
+#endif
+constexpr int kH2Threads = (kH2FirstEpi + kEpiWarps) * 32;
+constexpr int kH2RegsCtl = 56, kH2RegsProd = 72, kH2RegsEpi = 88;
+constexpr int kH2RegsLaunch = 80;   // registers a thread the split needs at launch
+static_assert(!TC_H2_REGSPLIT ||
+                  128 * (kH2RegsCtl + kH2RegsProd + 4 * kH2RegsEpi) <= kH2Threads * kH2RegsLaunch,
+              "register split exceeds the launch allotment");
+static_assert(!TC_H2_REGSPLIT || kH2Threads == 768, "six warpgroups");
+
+template <int N>
+__device__ __forceinline__ void h2_regs_dec() {
+#if TC_H2_REGSPLIT
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+#endif
+}
+template <int N>
+__device__ __forceinline__ void h2_regs_inc() {
+#if TC_H2_REGSPLIT
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+#endif
+}
 constexpr int kH2BN = TC_H2_BN;
 constexpr int kH2Slots = (512 - 2 * kH2BN) / 32 < 4 ? (512 - 2 * kH2BN) / 32 : 4;
 constexpr int kH2Group = TC_H2_GROUP;
@@ -1517,8 +1607,11 @@ __device__ __forceinline__ float pow2_scale(uint32_t mbits) {
     se = se < 1 ? 1 : (se > 254 ? 254 : se);
     return __uint_as_float((uint32_t)se << 23);
 }
-__device__ __forceinline__ float pow2_unscale(uint32_t mbits) {
-    return 1.f / pow2_scale(mbits);
+// 1 / x for x = 2^k with a biased exponent in [1, 254] (what pow2_scale
+// returns), exactly: 2^-k, subnormal (2^-127) for the largest x
+__device__ __forceinline__ float pow2_recip(float x) {
+    const uint32_t e = __float_as_uint(x) >> 23;
+    return __uint_as_float(e <= 253u ? (254u - e) << 23 : 0x00400000u);
 }
 
 // D (+)= A * B, kind::f16, A (M=128 rows = lanes, 8 columns = 16 fp16 of K) in
@@ -1534,7 +1627,7 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uin
 }
 
 template <bool INNER>
-__global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(kH2Threads, 1) tc_h2_kernel(const __grid_constant__ TcArgs a) {
     using L = SmemH2;
     constexpr int BN = kH2BN;
     constexpr int CK = L::kCK;
@@ -1592,7 +1685,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {
+    if (warp == kH2MmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
                      "r"(kTmemCols));
@@ -1604,161 +1697,166 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
     const uint32_t tmem = *tmem_slot;
     const int64_t T = npi * KS;  // K-steps of this CTA
 
-    if (warp == 0) {
-        // ------------------------- TMA producer -------------------------
-        if (lane == 0) {
-            const uint8_t* bimg = reinterpret_cast<const uint8_t*>(a.bimg);
-            Ring<NR> rr;
-            int64_t issued = 0;
-            int jc_loaded = -1;
-            bool ok = true;
-            auto load_b = [&](int jc) -> bool {
-                if (jc > 0 && !wait_bounded(bempty, (uint32_t)((jc - 1) & 1), abort_flag, a.status,
-                                            kStatusTimeoutTma))
-                    return false;
-                const int ck = chunk_len(jc);
-                mbar_arrive_expect_tx(bfull, (uint32_t)(ck * 2 * L::kB));
-                for (int q = 0; q < ck; ++q) {
-                    const int ks = jc * CK + q;
-                    const uint8_t* src = bimg + ((int64_t)blockIdx.x * KS + ks) * (int64_t)(2 * L::kB);
-                    bulk_load(bres + q * 2 * L::kB, src, 2 * L::kB, bfull);
-                }
-                jc_loaded = jc;
-                return true;
-            };
-            for (int jc = 0; jc < njc && ok; ++jc) {
-                const int ck = chunk_len(jc);
-                // the first NR Y tiles of chunk jc need only work of chunk jc - 1,
-                // so they are issued before the chunk swap
-                const int64_t swap_at = issued + NR;
-                bool b_pending = true;
-                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
-                    const int cP = (int)(pi / a.nQ);
-                    const int cQ = (int)(pi - (int64_t)cP * a.nQ);
-                    for (int q = 0; q < ck; ++q, ++issued, rr.next()) {
-                        if (b_pending && issued == swap_at) {
-                            b_pending = false;
-                            if (!load_b(jc)) {
-                                ok = false;
-                                break;
-                            }
-                        }
-                        if (rr.reused && !wait_bounded(&raw_empty[rr.slot], rr.phase ^ 1u, abort_flag,
-                                                       a.status, kStatusTimeoutTma)) {
-                            ok = false;
-                            break;
-                        }
+    const bool prod_warp = warp >= kH2ProdWarp0 && warp < kH2ProdWarp0 + kTProdWarps;
+    if (!prod_warp && warp < kH2FirstEpi) {
+        // control warpgroup: TMA warp, MMA warp (and, with the register split,
+        // two idle warps)
+        h2_regs_dec<kH2RegsCtl>();
+        if (warp == kH2TmaWarp) {
+            // ------------------------- TMA producer -------------------------
+            if (lane == 0) {
+                const uint8_t* bimg = reinterpret_cast<const uint8_t*>(a.bimg);
+                Ring<NR> rr;
+                int64_t issued = 0;
+                int jc_loaded = -1;
+                bool ok = true;
+                auto load_b = [&](int jc) -> bool {
+                    if (jc > 0 && !wait_bounded_inl(bempty, (uint32_t)((jc - 1) & 1), abort_flag, a.status,
+                                                kStatusTimeoutTma))
+                        return false;
+                    const int ck = chunk_len(jc);
+                    mbar_arrive_expect_tx(bfull, (uint32_t)(ck * 2 * L::kB));
+                    for (int q = 0; q < ck; ++q) {
                         const int ks = jc * CK + q;
-                        int role[kRoles];
-                        if (INNER) {
-                            role[kRoleJq] = ks * kBK2;
-                            role[kRoleJp] = 0;
-                        } else {
-                            const int jp = ks / a.jq_steps;
-                            role[kRoleJq] = (ks - jp * a.jq_steps) * kBK2;
-                            role[kRoleJp] = jp;
-                        }
-                        role[kRoleI] = (int)m0;
-                        role[kRolePP] = cP;
-                        role[kRolePQ] = cQ;
-                        int c[5] = {0, 0, 0, 0, 0};
-#pragma unroll
-                        for (int r = 0; r < kRoles; ++r)
-                            if (a.slot[r] >= 0) c[a.slot[r]] = role[r];
-                        mbar_arrive_expect_tx(&raw_full[rr.slot], a.y_box_bytes);
-                        tma_load(&a.ymap, a.rank, c, raw + rr.slot * L::kY, &raw_full[rr.slot]);
+                        const uint8_t* src = bimg + ((int64_t)blockIdx.x * KS + ks) * (int64_t)(2 * L::kB);
+                        bulk_load(bres + q * 2 * L::kB, src, 2 * L::kB, bfull);
                     }
-                }
-                if (ok && b_pending && !load_b(jc)) ok = false;
-            }
-            for (int64_t u = issued - 1; u >= 0 && u >= issued - NR; --u)
-                wait_drain(&raw_full[u % NR], (uint32_t)((u / NR) & 1), a.status);
-            if (jc_loaded >= 0) wait_drain(bfull, (uint32_t)(jc_loaded & 1), a.status);
-        }
-    } else if (warp == 1) {
-        // ------------------------- MMA issuer -------------------------
-        if (lane == 0) {
-            // kind::f16: fp16 A and B, fp32 accumulator
-            const uint32_t idesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-            const uint32_t b_w0 = sdesc_lo(smem_u32(bres));
-            constexpr uint32_t kBStep = (2 * L::kB) >> 4;
-            constexpr uint32_t kBLo = L::kB >> 4;
-            int ag = 0;             // A-slot group of the current K-step (ring of NG)
-            uint32_t aph = 0;
-            bool a_ready = false;   // a_full[ag] already observed complete (prefetched test)
-            int zb = 0;
-            uint32_t zph = 0;
-            uint32_t zused = 0;
-            bool ok = true;
-            for (int jc = 0; jc < njc && ok; ++jc) {
-                const int ck = chunk_len(jc);
-                if (!wait_bounded(bfull, (uint32_t)(jc & 1), abort_flag, a.status, kStatusTimeoutMma)) {
-                    ok = false;
-                    break;
-                }
-                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
-                    uint32_t bw = b_w0;
-                    for (int q = 0; q < ck; ++q, bw += kBStep) {
-                        const int qq = q % kChunkSteps2;
-                        const bool first = qq == 0;
-                        const bool last = qq == kChunkSteps2 - 1 || q == ck - 1;
-                        if (first && ((zused >> zb) & 1u)) {
-                            if (!wait_bounded(&zempty[zb], (zph >> zb) & 1u, abort_flag, a.status,
-                                              kStatusTimeoutMma)) {
+                    jc_loaded = jc;
+                    return true;
+                };
+                for (int jc = 0; jc < njc && ok; ++jc) {
+                    const int ck = chunk_len(jc);
+                    // the first NR Y tiles of chunk jc need only work of chunk jc - 1,
+                    // so they are issued before the chunk swap
+                    const int64_t swap_at = issued + NR;
+                    bool b_pending = true;
+                    for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                        const int cP = (int)(pi / a.nQ);
+                        const int cQ = (int)(pi - (int64_t)cP * a.nQ);
+                        for (int q = 0; q < ck; ++q, ++issued, rr.next()) {
+                            if (b_pending && issued == swap_at) {
+                                b_pending = false;
+                                if (!load_b(jc)) {
+                                    ok = false;
+                                    break;
+                                }
+                            }
+                            if (rr.reused && !wait_bounded_inl(&raw_empty[rr.slot], rr.phase ^ 1u, abort_flag,
+                                                           a.status, kStatusTimeoutTma)) {
                                 ok = false;
                                 break;
                             }
-                            tc_fence_after();
-                        }
-                        // a group is kH2Group consecutive K-steps of one unit
-                        const bool gstart = q % kH2Group == 0;
-                        const bool gend = q % kH2Group == kH2Group - 1 || q == ck - 1;
-                        if (gstart) {
-                            if (!a_ready && !wait_bounded(&a_full[ag], aph, abort_flag, a.status, kStatusTimeoutMma)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                        }
-                        const uint32_t ta =
-                            tmem + kH2ACol0 + 32u * (uint32_t)(ag * kH2Group + q % kH2Group);
-                        const uint32_t dz = tmem + (uint32_t)(zb * BN);
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            const uint32_t adv = (uint32_t)kk * 2u;   // 16 fp16 = 32 bytes of B
-                            const uint32_t ac = (uint32_t)kk * 8u;    // 8 TMEM columns (16 fp16) of A
-                            mma_f16_ta(dz, ta + ac, bw + adv, idesc, (first && kk == 0) ? 0u : 1u);
-                            mma_f16_ta(dz, ta + ac, bw + kBLo + adv, idesc, 1u);
-                            mma_f16_ta(dz, ta + 16u + ac, bw + adv, idesc, 1u);
-                        }
-                        if (gend) mma_commit(&a_empty[ag]);
-                        if (last) {
-                            if (a.withhold_signal && zused == 0 && zb == 0) {
-                                // test hook: this buffer is never reported full
+                            const int ks = jc * CK + q;
+                            int role[kRoles];
+                            if (INNER) {
+                                role[kRoleJq] = ks * kBK2;
+                                role[kRoleJp] = 0;
                             } else {
-                                mma_commit(&zfull[zb]);
+                                const int jp = ks / a.jq_steps;
+                                role[kRoleJq] = (ks - jp * a.jq_steps) * kBK2;
+                                role[kRoleJp] = jp;
                             }
-                            if ((zused >> zb) & 1u) zph ^= 1u << zb;
-                            zused |= 1u << zb;
-                            zb ^= 1;
-                        }
-                        if (gend) {
-                            if (++ag == NG) {
-                                ag = 0;
-                                aph ^= 1u;
-                            }
-                            // non-blocking test of the next group; its answer is used at
-                            // the next group start, so its latency overlaps the bookkeeping
-                            a_ready = TC_PREFETCH && mbar_test_wait(&a_full[ag], aph) != 0;
+                            role[kRoleI] = (int)m0;
+                            role[kRolePP] = cP;
+                            role[kRolePQ] = cQ;
+                            int c[5];
+                            tma_coords(a.slot, role, c);
+                            mbar_arrive_expect_tx(&raw_full[rr.slot], a.y_box_bytes);
+                            tma_load(&a.ymap, a.rank, c, raw + rr.slot * L::kY, &raw_full[rr.slot]);
                         }
                     }
+                    if (ok && b_pending && !load_b(jc)) ok = false;
                 }
-                if (ok) mma_commit(bempty);
+                for (int64_t u = issued - 1; u >= 0 && u >= issued - NR; --u)
+                    wait_drain_inl(&raw_full[u % NR], (uint32_t)((u / NR) & 1), a.status);
+                if (jc_loaded >= 0) wait_drain_inl(bfull, (uint32_t)(jc_loaded & 1), a.status);
             }
-            mma_commit(mma_done);
-            wait_drain(mma_done, 0, a.status);
+        } else if (warp == kH2MmaWarp) {
+            // ------------------------- MMA issuer -------------------------
+            if (lane == 0) {
+                // kind::f16: fp16 A and B, fp32 accumulator
+                const uint32_t idesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+                const uint32_t b_w0 = sdesc_lo(smem_u32(bres));
+                constexpr uint32_t kBStep = (2 * L::kB) >> 4;
+                constexpr uint32_t kBLo = L::kB >> 4;
+                int ag = 0;             // A-slot group of the current K-step (ring of NG)
+                uint32_t aph = 0;
+                bool a_ready = false;   // a_full[ag] already observed complete (prefetched test)
+                int zb = 0;
+                uint32_t zph = 0;
+                uint32_t zused = 0;
+                bool ok = true;
+                for (int jc = 0; jc < njc && ok; ++jc) {
+                    const int ck = chunk_len(jc);
+                    if (!wait_bounded_inl(bfull, (uint32_t)(jc & 1), abort_flag, a.status, kStatusTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                        uint32_t bw = b_w0;
+                        for (int q = 0; q < ck; ++q, bw += kBStep) {
+                            const int qq = q % kChunkSteps2;
+                            const bool first = qq == 0;
+                            const bool last = qq == kChunkSteps2 - 1 || q == ck - 1;
+                            if (first && ((zused >> zb) & 1u)) {
+                                if (!wait_bounded_inl(&zempty[zb], (zph >> zb) & 1u, abort_flag, a.status,
+                                                  kStatusTimeoutMma)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                            }
+                            // a group is kH2Group consecutive K-steps of one unit
+                            const bool gstart = q % kH2Group == 0;
+                            const bool gend = q % kH2Group == kH2Group - 1 || q == ck - 1;
+                            if (gstart) {
+                                if (!a_ready && !wait_bounded_inl(&a_full[ag], aph, abort_flag, a.status, kStatusTimeoutMma)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                            }
+                            const uint32_t ta =
+                                tmem + kH2ACol0 + 32u * (uint32_t)(ag * kH2Group + q % kH2Group);
+                            const uint32_t dz = tmem + (uint32_t)(zb * BN);
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                const uint32_t adv = (uint32_t)kk * 2u;   // 16 fp16 = 32 bytes of B
+                                const uint32_t ac = (uint32_t)kk * 8u;    // 8 TMEM columns (16 fp16) of A
+                                mma_f16_ta(dz, ta + ac, bw + adv, idesc, (first && kk == 0) ? 0u : 1u);
+                                mma_f16_ta(dz, ta + ac, bw + kBLo + adv, idesc, 1u);
+                                mma_f16_ta(dz, ta + 16u + ac, bw + adv, idesc, 1u);
+                            }
+                            if (gend) mma_commit(&a_empty[ag]);
+                            if (last) {
+                                if (a.withhold_signal && zused == 0 && zb == 0) {
+                                    // test hook: this buffer is never reported full
+                                } else {
+                                    mma_commit(&zfull[zb]);
+                                }
+                                if ((zused >> zb) & 1u) zph ^= 1u << zb;
+                                zused |= 1u << zb;
+                                zb ^= 1;
+                            }
+                            if (gend) {
+                                if (++ag == NG) {
+                                    ag = 0;
+                                    aph ^= 1u;
+                                }
+                                // non-blocking test of the next group; its answer is used at
+                                // the next group start, so its latency overlaps the bookkeeping
+                                a_ready = TC_PREFETCH && mbar_test_wait(&a_full[ag], aph) != 0;
+                            }
+                        }
+                    }
+                    if (ok) mma_commit(bempty);
+                }
+                mma_commit(mma_done);
+                wait_drain_inl(mma_done, 0, a.status);
+            }
         }
-    } else if (warp < kTFirstEpi) {
+    } else if (prod_warp) {
+        h2_regs_dec<kH2RegsProd>();
         // --------------- operand producers: one TMEM lane quadrant each ---------------
         const int quad = warp & 3;
         const int r = 32 * quad + lane;   // tile row of this thread
@@ -1773,13 +1871,13 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
                 for (int q = 0; q < ck; ++q, rr.next()) {
                     const bool gstart = q % kH2Group == 0;
                     const bool gend = q % kH2Group == kH2Group - 1 || q == ck - 1;
-                    if (!warp_wait(&raw_full[rr.slot], rr.phase, abort_flag, a.status, kStatusTimeoutLo)) {
+                    if (!warp_wait_inl(&raw_full[rr.slot], rr.phase, abort_flag, a.status, kStatusTimeoutLo)) {
                         ok = false;
                         break;
                     }
                     if (gstart) {
                         // the group's slots were last read by the MMAs of group g - NG
-                        if (g >= NG && !warp_wait(&a_empty[ag], (uint32_t)(((g / NG) - 1) & 1), abort_flag,
+                        if (g >= NG && !warp_wait_inl(&a_empty[ag], (uint32_t)(((g / NG) - 1) & 1), abort_flag,
                                                   a.status, kStatusTimeoutLo)) {
                             ok = false;
                             break;
@@ -1841,13 +1939,14 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
             }
         }
     } else {
+        h2_regs_inc<kH2RegsEpi>();
         // ---------------------- epilogue (16 warps) ----------------------
         constexpr int kCols = BN / 4;
         const int quad = warp & 3;
-        const int part = (warp - kTFirstEpi) >> 2;
+        const int part = (warp - kH2FirstEpi) >> 2;
         const int64_t row = m0 + 32 * quad + lane;
         const int64_t c0 = r0 + part * kCols;
-        float* gw = gsm + (warp - kTFirstEpi) * 2 * kCols;
+        float* gw = gsm + (warp - kH2FirstEpi) * 2 * kCols;
         float acc[kCols];
 #pragma unroll
         for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
@@ -1875,7 +1974,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
                 fetch_g(pi + 1 < pre_hi ? pi + 1 : pre_lo, gb ^ 1);
                 const float* g_cur = gw + gb * kCols;
                 for (int q0 = 0; q0 < ck; q0 += kChunkSteps) {
-                    if (!warp_wait(&zfull[zb], (zph >> zb) & 1u, abort_flag, a.status, kStatusTimeoutEpi)) {
+                    if (!warp_wait_inl(&zfull[zb], (zph >> zb) & 1u, abort_flag, a.status, kStatusTimeoutEpi)) {
                         ok = false;
                         break;
                     }
@@ -1883,12 +1982,15 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
                     const uint32_t tbase =
                         tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
 #pragma unroll
-                    for (int cc = 0; cc < kCols; cc += 8) {
-                        uint32_t z[8];
-                        tmem_ld8(tbase + cc, z);
+                    for (int cc = 0; cc < kCols; cc += TC_H2_EPI_LD) {
+                        uint32_t z[TC_H2_EPI_LD];
+                        if constexpr (TC_H2_EPI_LD == 8)
+                            tmem_ld8(tbase + cc, z);
+                        else
+                            tmem_ld4(tbase + cc, z);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int q = 0; q < 2; ++q) {
+                        for (int q = 0; q < TC_H2_EPI_LD / 4; ++q) {
                             const float4 g = *reinterpret_cast<const float4*>(g_cur + cc + 4 * q);
                             acc[cc + 4 * q + 0] = fmaf(g.x, __uint_as_float(z[4 * q + 0]), acc[cc + 4 * q + 0]);
                             acc[cc + 4 * q + 1] = fmaf(g.y, __uint_as_float(z[4 * q + 1]), acc[cc + 4 * q + 1]);
@@ -1907,31 +2009,33 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_h2_kernel(const __grid_consta
         }
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         if (!*abort_flag && row < a.I) {
-            // undo the power-of-two scales of Y and of each Binner column
-            const float inv_y = pow2_unscale(*a.ymax_bits);
-#pragma unroll
-            for (int e = 0; e < kCols; ++e) {
-                const float cs = (c0 + e < a.R) ? a.colscale[c0 + e] : 1.f;
-                acc[e] = acc[e] * inv_y * (1.f / cs);
-            }
+            // undo the power-of-two scales of Y and of each Binner column (exact)
+            const float inv_y = pow2_recip(pow2_scale(*a.ymax_bits));
             float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride + row * a.R + c0;
             const bool vst = (a.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.dst) & 15) == 0);
 #pragma unroll
             for (int e = 0; e < kCols; e += 4) {
+                float v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float cs = (c0 + e + q < a.R) ? a.colscale[c0 + e + q] : 1.f;
+                    v[q] = acc[e + q] * inv_y * pow2_recip(cs);
+                }
                 if (vst && c0 + e + 4 <= a.R) {
-                    *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+                    *reinterpret_cast<float4*>(dst + e) = make_float4(v[0], v[1], v[2], v[3]);
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        if (c0 + e + q < a.R) dst[e + q] = acc[e + q];
+                        if (c0 + e + q < a.R) dst[e + q] = v[q];
                 }
+                asm volatile("" ::: "memory");   // keep one group of column scales in flight
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kH2MmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
     }
@@ -2264,12 +2368,20 @@ cudaError_t launch_h2(const TcArgs& args, dim3 grid, cudaStream_t s) {
     if (e0 != cudaSuccess) return e0;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
+        if (TC_H2_REGSPLIT) {
+            // setmaxnreg.inc waits until the pool allotted at launch can serve it:
+            // refuse a build whose launch allotment is below what the split assumes
+            cudaFuncAttributes fa;
+            cudaError_t e = cudaFuncGetAttributes(&fa, tc_h2_kernel<INNER>);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs < kH2RegsLaunch || fa.numRegs * kH2Threads > 65536) return cudaErrorInvalidConfiguration;
+        }
         cudaError_t e = cudaFuncSetAttribute(tc_h2_kernel<INNER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)SmemH2::kTotal);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    tc_h2_kernel<INNER><<<grid, kTThreads, SmemH2::kTotal, s>>>(args);
+    tc_h2_kernel<INNER><<<grid, kH2Threads, SmemH2::kTotal, s>>>(args);
     return cudaGetLastError();
 }
 
