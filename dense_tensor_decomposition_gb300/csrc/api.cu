@@ -132,6 +132,28 @@ void layout_workspace(ModePlan& mp) {
     mp.total = off;
 }
 
+// fp16 images of Y (tc_img modes): one region after every mode's own needs, so
+// that the images written for the first such mode of a call serve the others
+void place_images(Plan& p) {
+    size_t base = 0;
+    bool any = false;
+    for (int k = 0; k < p.d; ++k) {
+        if (p.mode[k].path == MTTKRP_PATH_TC && p.mode[k].tc_img) any = true;
+        if (p.mode[k].total > base) base = p.mode[k].total;
+    }
+    if (!any) return;
+    base = align256(base);
+    int64_t numel = 1;
+    for (int n = 0; n < p.d; ++n) numel *= p.dims[n];
+    const size_t img = 2 * align256((size_t)numel * 2);   // hi and lo, 2 bytes an element
+    for (int k = 0; k < p.d; ++k) {
+        ModePlan& mp = p.mode[k];
+        if (mp.path != MTTKRP_PATH_TC || !mp.tc_img) continue;
+        mp.off_img = base;
+        mp.total = base + img;
+    }
+}
+
 int plan_mode(Plan& p, int k, int path) {
     ModePlan& mp = p.mode[k];
     memset(&mp, 0, sizeof(mp));
@@ -370,6 +392,7 @@ int mttkrp_plan(int d, const int64_t* dims, int64_t R, mttkrp_plan_t* out) {
             return fail(rc, "planning mode %d failed", k);
         }
     }
+    place_images(*p);
     *out = reinterpret_cast<mttkrp_plan_t>(p);
     return MTTKRP_OK;
 }
@@ -388,6 +411,7 @@ int mttkrp_plan_set_path(mttkrp_plan_t h, int path) {
             return fail(rc, "mode %d cannot run on path %d", k, path);
         }
     }
+    place_images(*p);
     p->forced_path = path;
     return MTTKRP_OK;
 }
@@ -421,6 +445,7 @@ int mttkrp(mttkrp_plan_t h, const float* Y, const float* const* factors, int mod
     if (Y == nullptr || factors == nullptr || out == nullptr)
         return fail(MTTKRP_ERR_INVALID, "NULL tensor, factor array or output");
     p->ymax_ready = 0;
+    p->img_ready = 0;
     return run_mode(*p, Y, factors, mode, out, static_cast<cudaStream_t>(stream));
 }
 
@@ -436,6 +461,7 @@ int mttkrp_all_modes(mttkrp_plan_t h, const float* Y, const float* const* factor
         if (outs[k] == nullptr) return fail(MTTKRP_ERR_INVALID, "output %d is NULL", k);
     }
     p->ymax_ready = 0;   // one max |Y| pass serves every mode of this call
+    p->img_ready = 0;    // and one pass writing the fp16 images of Y
     for (int k = 0; k < p->d; ++k) {
         int rc = run_mode(*p, Y, factors, k, outs[k], static_cast<cudaStream_t>(stream));
         if (rc != MTTKRP_OK) return rc;
@@ -463,11 +489,11 @@ int mttkrp_plan_describe(mttkrp_plan_t h, int mode, char* buf, size_t len) {
     int n = snprintf(tmp, sizeof(tmp),
                      "mode=%d path=%s tile=%dx%d inner_group=[%s] J=%lld Jq=%lld pre_modes=[%s] "
                      "npre=%lld splits=%lld pre_per_split=%lld workspace=%zu tc_ksteps=%d tc_inner=%d tc_slots=%d "
-                     "tc_tmem_a=%d tc_fp16x2=%d",
+                     "tc_tmem_a=%d tc_fp16x2=%d tc_fp16_image=%d",
                      mode, mp.path == MTTKRP_PATH_TC ? "tc" : "simt", mp.bm, mp.bn, groups,
                      (long long)g.J, (long long)g.Jq, pres, (long long)g.npre,
                      (long long)mp.splits, (long long)mp.pre_per_split, mp.total, mp.tc_ks, mp.tc_inner,
-                     mp.tc_small ? mp.tc_ps : 1, mp.tc_tmem, mp.tc_h2);
+                     mp.tc_small ? mp.tc_ps : 1, mp.tc_tmem, mp.tc_h2 || mp.tc_img, mp.tc_img);
     if (buf != nullptr && len > 0) {
         strncpy(buf, tmp, len - 1);
         buf[len - 1] = 0;

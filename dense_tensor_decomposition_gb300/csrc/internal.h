@@ -60,9 +60,12 @@ struct ModePlan {
     int tc_ps;
     int tc_tmem;        // 1: A operand staged in tensor memory (128 x 224 tiles, large R)
     int tc_h2;          // 1: two-term fp16 split (kind::f16, K-steps of 32); implies tc_tmem
-    int tc_kw;          // contraction indices per K-step (16, or 32 with tc_h2)
+    int tc_kw;          // contraction indices per K-step (16; 32 with tc_h2; 64 with tc_img)
+    int tc_img;         // 1: two-term fp16 split from pre-split fp16 images of Y, both
+                        //    operands in shared memory (K-major modes, K-steps of 64)
     // workspace layout, byte offsets from the workspace base
     size_t off_partials, off_binner, off_gtab, off_base, total;
+    size_t off_img;     // tc_img: fp16 hi image of Y, then the lo image (shared by all modes)
 };
 
 struct Plan {
@@ -81,6 +84,8 @@ struct Plan {
     int64_t launches;  // kernels launched so far
     // max |Y| (fp16-split path) already computed for the current call's Y
     mutable int ymax_ready;
+    // fp16 images of Y (tc_img modes) already written for the current call's Y
+    mutable int img_ready;
     // benchmark timing: event pairs around the main kernel of each mode
     int timing;
     int ev_cap[kMaxD];

@@ -72,6 +72,7 @@ enum Role { kRoleJq = 0, kRoleI = 1, kRoleJp = 2, kRolePP = 3, kRolePQ = 4, kRol
 
 struct TcArgs {
     CUtensorMap ymap;
+    CUtensorMap ymap_lo;      // fp16-image kernel: the lo image (ymap holds the hi image)
     int rank;                 // tensor-map rank (2..5)
     int slot[kRoles];         // coordinate slot of each role, -1 if absent
     const float* bimg;        // B images [n-tile][K-step][hi|lo][BN rows x 64 B]
@@ -1523,6 +1524,12 @@ constexpr int kChunkSteps2 = 4;   // 128 contraction indices between TMEM drains
 #ifndef TC_H2_GROUP
 #define TC_H2_GROUP 1
 #endif
+#ifndef TC_IMG
+#define TC_IMG 1           // fp16-image kernel for K-major modes
+#endif
+#ifndef TC_IMG_MIN_R
+#define TC_IMG_MIN_R 128
+#endif
 #ifndef TC_H2_EPI_LD
 #define TC_H2_EPI_LD 8   // TMEM columns per epilogue load (4 or 8)
 #endif
@@ -2041,6 +2048,389 @@ __global__ void __launch_bounds__(kH2Threads, 1) tc_h2_kernel(const __grid_const
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Two-term fp16 split with both operands in shared memory.  Y is split once per
+// call into fp16 hi and lo images laid out like Y (split_image_kernel); the
+// kernel streams 128-row x 64-index tiles of both images with TMA (128-byte
+// swizzle) and issues, per 16 contraction indices, hi*Bhi + hi*Blo + lo*Bhi into
+// a TMEM accumulator.  Same arithmetic as tc_h2_kernel, but no producer warps:
+// the only hand-over per K-step (64 indices, twelve MMAs) is TMA -> MMA.
+// Roles: warp 0 TMA, warp 1 MMA, warps 2-3 idle (the control warpgroup, which
+// gives registers back), warps 4-19 epilogue (which take them).
+// ---------------------------------------------------------------------------
+constexpr int kBK4 = 64;          // contraction indices per K-step (128-byte fp16 rows)
+constexpr int kImgCK = 2;         // K-steps per B chunk and per TMEM drain (128 indices)
+constexpr int kImgEpiWarp0 = 4;
+constexpr int kImgThreads = (kImgEpiWarp0 + kEpiWarps) * 32;   // 640
+// registers a thread: the launch allots 96 (65536 / 640, in units of 8); the
+// split uses 128 x (48 + 4 x 104) = 59392 of the 61440 allotted
+constexpr int kImgRegsCtl = 48, kImgRegsEpi = 104, kImgRegsLaunch = 96;
+static_assert(128 * (kImgRegsCtl + 4 * kImgRegsEpi) <= kImgThreads * kImgRegsLaunch, "register split");
+
+// K-major, 128-byte swizzle descriptor: 8-row groups of 128-byte rows, 1024
+// bytes apart (high word; the low word is the start address >> 4 and LBO = 1)
+constexpr uint64_t kDescSw128Hi = ((uint64_t)1 << 16)            // leading byte offset (unused)
+                                | ((uint64_t)(1024 >> 4) << 32)  // stride byte offset: 8 rows x 128 B
+                                | ((uint64_t)1 << 46)            // descriptor version
+                                | ((uint64_t)2 << 61);           // 128-byte swizzle
+
+__device__ __forceinline__ uint32_t sdesc128_lo(uint32_t saddr) {
+    return (uint32_t)kDescSw128Hi | ((saddr & 0x3FFFFu) >> 4);
+}
+
+// D (+)= A * B, kind::f16, both operands by descriptor low word (128-byte swizzle)
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                           uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %3};\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"((uint32_t)(kDescSw128Hi >> 32)), "r"(idesc), "r"(acc));
+}
+
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int BN>
+struct SmemImg {
+    static constexpr uint32_t kA = kBM * 128;      // 16 KB: one image tile (128 rows x 64 fp16)
+    static constexpr uint32_t kStage = 2 * kA;     // hi and lo tiles
+    static constexpr uint32_t kB = BN * 128;       // one K-step of B (hi or lo)
+    static constexpr uint32_t kBRes = kImgCK * 2 * kB;
+    static constexpr uint32_t kBarBytes = 256;
+    static constexpr uint32_t kFree = 232448u - 1024u - kBarBytes - kBRes;
+    static constexpr int kStages = kFree / kStage > 6 ? 6 : (int)(kFree / kStage);
+    static constexpr uint32_t kOffA = kBRes;
+    static constexpr uint32_t kOffBars = kOffA + kStages * kStage;
+    static constexpr uint32_t kTotal = 1024 + kOffBars + kBarBytes;
+    static_assert(kStages >= 3, "operand ring depth");
+    static_assert(kTotal <= 232448, "shared memory budget");
+    static_assert(kB % 1024 == 0, "swizzle-atom alignment");
+    static_assert((2 * kStages + 7) * 8 + 8 <= kBarBytes, "barrier area");
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_constant__ TcArgs a) {
+    using L = SmemImg<BN>;
+    constexpr int NS = L::kStages;
+    constexpr int CK = kImgCK;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~(uintptr_t)1023);
+    uint8_t* bres = smem;
+    uint8_t* ring = smem + L::kOffA;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBars);
+    uint64_t* full = bars;                      // [NS] both image tiles of the stage landed
+    uint64_t* empty = full + NS;                // [NS] the MMAs that read the stage are done
+    uint64_t* zfull = empty + NS;               // [2]
+    uint64_t* zempty = zfull + 2;               // [2]
+    uint64_t* bfull = zempty + 2;               // [1]
+    uint64_t* bempty = bfull + 1;               // [1]
+    uint64_t* mma_done = bempty + 1;            // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int64_t m0 = (int64_t)blockIdx.y * kBM;
+    const int64_t r0 = (int64_t)blockIdx.x * BN;
+    const int64_t pre_lo = (int64_t)blockIdx.z * a.pre_per_split;
+    int64_t pre_hi = pre_lo + a.pre_per_split;
+    if (pre_hi > a.npre) pre_hi = a.npre;
+    const int KS = a.KS;
+    const int njc = (KS + CK - 1) / CK;
+    auto chunk_len = [&](int jc) { return min(CK, KS - jc * CK); };
+    constexpr uint32_t kTmemCols = 2 * BN;   // two accumulator buffers
+    static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
+                  "TMEM allocation: a power of two in [32, 512]");
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&zfull[b], 1);
+            mbar_init(&zempty[b], kEpiWarps);
+        }
+        mbar_init(bfull, 1);
+        mbar_init(bempty, 1);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < kImgEpiWarp0) {
+        regs_dec<kImgRegsCtl>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------- TMA producer -------------------------
+            const uint8_t* bimg = reinterpret_cast<const uint8_t*>(a.bimg);
+            Ring<NS> rr;
+            int64_t issued = 0;
+            int jc_loaded = -1;
+            bool ok = true;
+            auto load_b = [&](int jc) -> bool {
+                if (jc > 0 && !wait_bounded_inl(bempty, (uint32_t)((jc - 1) & 1), abort_flag, a.status,
+                                                kStatusTimeoutTma))
+                    return false;
+                const int ck = chunk_len(jc);
+                mbar_arrive_expect_tx(bfull, (uint32_t)(ck * 2 * L::kB));
+                for (int q = 0; q < ck; ++q) {
+                    const int ks = jc * CK + q;
+                    const uint8_t* src = bimg + ((int64_t)blockIdx.x * KS + ks) * (int64_t)(2 * L::kB);
+                    bulk_load(bres + q * 2 * L::kB, src, 2 * L::kB, bfull);
+                }
+                jc_loaded = jc;
+                return true;
+            };
+            for (int jc = 0; jc < njc && ok; ++jc) {
+                const int ck = chunk_len(jc);
+                // the first NS tiles of chunk jc need only work of chunk jc - 1,
+                // so they are issued before the chunk swap
+                const int64_t swap_at = issued + NS;
+                bool b_pending = true;
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                    const int cP = (int)(pi / a.nQ);
+                    const int cQ = (int)(pi - (int64_t)cP * a.nQ);
+                    for (int q = 0; q < ck; ++q, ++issued, rr.next()) {
+                        if (b_pending && issued == swap_at) {
+                            b_pending = false;
+                            if (!load_b(jc)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (rr.reused && !wait_bounded_inl(&empty[rr.slot], rr.phase ^ 1u, abort_flag,
+                                                           a.status, kStatusTimeoutTma)) {
+                            ok = false;
+                            break;
+                        }
+                        const int ks = jc * CK + q;
+                        const int jp = ks / a.jq_steps;
+                        int role[kRoles];
+                        role[kRoleJq] = (ks - jp * a.jq_steps) * kBK4;
+                        role[kRoleJp] = jp;
+                        role[kRoleI] = (int)m0;
+                        role[kRolePP] = cP;
+                        role[kRolePQ] = cQ;
+                        int c[5];
+                        tma_coords(a.slot, role, c);
+                        uint8_t* st = ring + rr.slot * L::kStage;
+                        mbar_arrive_expect_tx(&full[rr.slot], 2u * a.y_box_bytes);
+                        tma_load(&a.ymap, a.rank, c, st, &full[rr.slot]);
+                        tma_load(&a.ymap_lo, a.rank, c, st + L::kA, &full[rr.slot]);
+                    }
+                }
+                if (ok && b_pending && !load_b(jc)) ok = false;
+            }
+            for (int64_t u = issued - 1; u >= 0 && u >= issued - NS; --u)
+                wait_drain_inl(&full[u % NS], (uint32_t)((u / NS) & 1), a.status);
+            if (jc_loaded >= 0) wait_drain_inl(bfull, (uint32_t)(jc_loaded & 1), a.status);
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------- MMA issuer -------------------------
+            // kind::f16: fp16 A and B (both K-major), fp32 accumulator
+            const uint32_t idesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+            const uint32_t a_w0 = sdesc128_lo(smem_u32(ring));
+            const uint32_t b_w0 = sdesc128_lo(smem_u32(bres));
+            constexpr uint32_t kAStep = L::kStage >> 4;
+            constexpr uint32_t kALo = L::kA >> 4;
+            constexpr uint32_t kBStep = (2 * L::kB) >> 4;
+            constexpr uint32_t kBLo = L::kB >> 4;
+            Ring<NS> rr;
+            int zb = 0;
+            uint32_t zph = 0;
+            uint32_t zused = 0;
+            bool ok = true;
+            for (int jc = 0; jc < njc && ok; ++jc) {
+                const int ck = chunk_len(jc);
+                if (!wait_bounded_inl(bfull, (uint32_t)(jc & 1), abort_flag, a.status, kStatusTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                    uint32_t bw = b_w0;
+                    for (int q = 0; q < ck; ++q, bw += kBStep, rr.next()) {
+                        const bool first = q == 0;
+                        const bool last = q == ck - 1;
+                        if (first && ((zused >> zb) & 1u)) {
+                            if (!wait_bounded_inl(&zempty[zb], (zph >> zb) & 1u, abort_flag, a.status,
+                                                  kStatusTimeoutMma)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        if (!wait_bounded_inl(&full[rr.slot], rr.phase, abort_flag, a.status, kStatusTimeoutMma)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t aw = a_w0 + (uint32_t)rr.slot * kAStep;
+                        const uint32_t dz = tmem + (uint32_t)(zb * BN);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t adv = (uint32_t)kk * 2u;   // 16 fp16 = 32 bytes
+                            mma_f16_ss(dz, aw + adv, bw + adv, idesc, (first && kk == 0) ? 0u : 1u);
+                            mma_f16_ss(dz, aw + adv, bw + kBLo + adv, idesc, 1u);
+                            mma_f16_ss(dz, aw + kALo + adv, bw + adv, idesc, 1u);
+                        }
+                        mma_commit(&empty[rr.slot]);
+                        if (last) {
+                            if (a.withhold_signal && zused == 0 && zb == 0) {
+                                // test hook: this buffer is never reported full
+                            } else {
+                                mma_commit(&zfull[zb]);
+                            }
+                            if ((zused >> zb) & 1u) zph ^= 1u << zb;
+                            zused |= 1u << zb;
+                            zb ^= 1;
+                        }
+                    }
+                }
+                if (ok) mma_commit(bempty);
+            }
+            mma_commit(mma_done);
+            wait_drain_inl(mma_done, 0, a.status);
+        }
+    } else {
+        regs_inc<kImgRegsEpi>();
+        // ---------------------- epilogue (16 warps) ----------------------
+        constexpr int kCols = BN / 4;
+        constexpr int kGv = (kCols + 31) / 32;   // G values a lane holds
+        static_assert(kCols % 8 == 0, "8-column TMEM loads");
+        const int quad = warp & 3;
+        const int part = (warp - kImgEpiWarp0) >> 2;
+        const int64_t row = m0 + 32 * quad + lane;
+        const int64_t c0 = r0 + part * kCols;
+        float acc[kCols];
+#pragma unroll
+        for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
+        // G(pi, c0 + 32 u + lane) in lane `lane`, slot u; broadcast by shuffles
+        auto load_g = [&](int64_t pi, float* g) {
+#pragma unroll
+            for (int u = 0; u < kGv; ++u) {
+                const int e = 32 * u + lane;
+                g[u] = (e < kCols && c0 + e < a.R && pi < pre_hi) ? __ldg(a.gtab + pi * a.R + c0 + e) : 0.f;
+            }
+        };
+        float g_next[kGv];
+        load_g(pre_lo, g_next);
+        int zb = 0;
+        uint32_t zph = 0;
+        bool ok = true;
+        for (int jc = 0; jc < njc && ok; ++jc) {
+            for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                float g_cur[kGv];
+#pragma unroll
+                for (int u = 0; u < kGv; ++u) g_cur[u] = g_next[u];
+                load_g(pi + 1 < pre_hi ? pi + 1 : pre_lo, g_next);   // used at the next drain
+                if (!warp_wait_inl(&zfull[zb], (zph >> zb) & 1u, abort_flag, a.status, kStatusTimeoutEpi)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tbase =
+                    tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
+#pragma unroll
+                for (int cc = 0; cc < kCols; cc += 8) {
+                    uint32_t z[8];
+                    tmem_ld8(tbase + cc, z);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int e = cc + q;
+                        const float g = __shfl_sync(0xffffffffu, g_cur[e / 32], e % 32);
+                        acc[e] = fmaf(g, __uint_as_float(z[q]), acc[e]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&zempty[zb]);
+                zph ^= 1u << zb;
+                zb ^= 1;
+            }
+        }
+        if (!*abort_flag && row < a.I) {
+            // undo the power-of-two scales of Y and of each Binner column (exact)
+            const float inv_y = pow2_recip(pow2_scale(*a.ymax_bits));
+            float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride + row * a.R + c0;
+            const bool vst = (a.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.dst) & 15) == 0);
+#pragma unroll
+            for (int e = 0; e < kCols; e += 4) {
+                float v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float cs = (c0 + e + q < a.R) ? a.colscale[c0 + e + q] : 1.f;
+                    v[q] = acc[e + q] * inv_y * pow2_recip(cs);
+                }
+                if (vst && c0 + e + 4 <= a.R) {
+                    *reinterpret_cast<float4*>(dst + e) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (c0 + e + q < a.R) dst[e + q] = v[q];
+                }
+                asm volatile("" ::: "memory");   // keep one group of column scales in flight
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+// Split Y into the fp16 images the kernel above streams: with x = Y * s (s the
+// power of two that takes max |Y| into [2^13, 2^14)), hi = fp16(x) and
+// lo = fp16(x - hi) (the difference is exact in fp32), same layout as Y.
+__global__ void __launch_bounds__(256) split_image_kernel(const float* __restrict__ y, int64_t n,
+                                                          const uint32_t* __restrict__ ymax_bits,
+                                                          __half* __restrict__ hi, __half* __restrict__ lo) {
+    const float sy = pow2_scale(*ymax_bits);
+    const int64_t n4 = n / 4;   // y, hi and lo are 16-byte aligned
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int64_t i = t0; i < n4; i += stride) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(y) + i);
+        const float x0 = v.x * sy, x1 = v.y * sy, x2 = v.z * sy, x3 = v.w * sy;
+        const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+        const __half2 l01 = __floats2half2_rn(x0 - f01.x, x1 - f01.y);
+        const __half2 l23 = __floats2half2_rn(x2 - f23.x, x3 - f23.y);
+        reinterpret_cast<uint2*>(hi)[i] = make_uint2(half2_bits(h01), half2_bits(h23));
+        reinterpret_cast<uint2*>(lo)[i] = make_uint2(half2_bits(l01), half2_bits(l23));
+    }
+    for (int64_t i = 4 * n4 + t0; i < n; i += stride) {
+        const float x = y[i] * sy;
+        const __half h = __float2half_rn(x);
+        hi[i] = h;
+        lo[i] = __float2half_rn(x - __half2float(h));
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Prep: pre-swizzled hi/lo images of the inner Khatri-Rao table
 // ---------------------------------------------------------------------------
@@ -2158,34 +2548,39 @@ __global__ void __launch_bounds__(256) colscale_kernel(ColScaleArgs a) {
 }
 
 // fp16 hi|lo images of the scaled inner KRP table for the two-term fp16 split:
-// per (n-tile, K-step of 32): hi image [BN rows][32 fp16] then lo image, rows of
-// 64 bytes, 64-byte swizzled (16-byte chunk c of row n at (c ^ (n >> 1)) & 3).
-__global__ void tc_bimage_h2_kernel(BImgArgs a, const float* __restrict__ colscale) {
-    const int64_t per_block = 2LL * a.BN * kBK2;  // fp16 elements (hi + lo)
+// per (n-tile, K-step of KW): hi image [BN rows][KW fp16] then lo image.
+// KW = 32: rows of 64 bytes, 64-byte swizzled (16-byte chunk c of row n at
+// (c ^ (n >> 1)) & 3); KW = 64: rows of 128 bytes, 128-byte swizzled (chunk c
+// at (c ^ n) & 7).
+template <int KW>
+__global__ void tc_bimage_f16_kernel(BImgArgs a, const float* __restrict__ colscale) {
+    static_assert(KW == 32 || KW == 64, "64- or 128-byte rows");
+    constexpr uint32_t kRow = 2 * KW;              // bytes per row
+    const int64_t per_block = 2LL * a.BN * KW;    // fp16 elements (hi + lo)
     const int64_t n = a.nblocks * per_block;
     __half* out = reinterpret_cast<__half*>(a.out);
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (int64_t)gridDim.x * blockDim.x) {
         const int64_t blk = e / per_block;
         const int64_t w = e - blk * per_block;
-        const int half = (int)(w / (a.BN * kBK2));
-        const int64_t w2 = w - (int64_t)half * a.BN * kBK2;
+        const int half = (int)(w / (a.BN * KW));
+        const int64_t w2 = w - (int64_t)half * a.BN * KW;
         const uint32_t byte = (uint32_t)(w2 * 2);
-        const uint32_t row = byte / 64u;
-        const uint32_t chunk_pos = (byte % 64u) / 16u;
+        const uint32_t row = byte / kRow;
+        const uint32_t chunk_pos = (byte % kRow) / 16u;
         const uint32_t elem = (byte % 16u) / 2u;
-        const uint32_t kk = ((chunk_pos ^ (row >> 1)) & 3u) * 8u + elem;
+        const uint32_t kk = (KW == 32 ? ((chunk_pos ^ (row >> 1)) & 3u) : ((chunk_pos ^ row) & 7u)) * 8u + elem;
         const int64_t nt = blk / a.KS;
         const int ks = (int)(blk - nt * a.KS);
         const int64_t r = nt * a.BN + row;
         int64_t j;
         bool valid;
         if (a.inner) {
-            j = (int64_t)ks * kBK2 + kk;
+            j = (int64_t)ks * KW + kk;
             valid = j < a.J;
         } else {
             const int jp = ks / a.jq_steps;
-            const int64_t jq = (int64_t)(ks - jp * a.jq_steps) * kBK2 + kk;
+            const int64_t jq = (int64_t)(ks - jp * a.jq_steps) * KW + kk;
             valid = jq < a.Jq;
             j = (int64_t)jp * a.Jq + jq;
         }
@@ -2236,8 +2631,10 @@ struct MapGeom {
     uint32_t box[5];
 };
 
-// Tensor-map geometry of Y for mode plan mp; false if TMA cannot express it.
-bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides, int d, MapGeom& mg) {
+// Tensor-map geometry of Y (elements of esize bytes: 4 for Y itself, 2 for its
+// fp16 images) for mode plan mp; false if TMA cannot express it.
+bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides, int d, MapGeom& mg,
+                int esize) {
     const ModeGeom& g = mp.g;
     const int k = g.k;
     struct Dim {
@@ -2315,7 +2712,7 @@ bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides,
         mg.dim[t] = (uint64_t)dl[t].size;
         mg.stride_el[t] = (uint64_t)dl[t].stride;
         if (dl[t].size >= ((int64_t)1 << 31)) return false;
-        if (t > 0 && ((dl[t].stride * 4) % 16 != 0 || dl[t].stride * 4 >= ((int64_t)1 << 40)))
+        if (t > 0 && ((dl[t].stride * esize) % 16 != 0 || dl[t].stride * esize >= ((int64_t)1 << 40)))
             return false;
         mg.box[t] = 1;
     }
@@ -2385,6 +2782,29 @@ cudaError_t launch_h2(const TcArgs& args, dim3 grid, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <int BN>
+cudaError_t launch_img(const TcArgs& args, dim3 grid, cudaStream_t s) {
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        // setmaxnreg.inc waits until the pool allotted at launch can serve it:
+        // refuse a build whose launch allotment is below what the split assumes
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, tc_img_kernel<BN>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs < kImgRegsLaunch || fa.numRegs * kImgThreads > 65536) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(tc_img_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SmemImg<BN>::kTotal);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    tc_img_kernel<BN><<<grid, kImgThreads, SmemImg<BN>::kTotal, s>>>(args);
+    return cudaGetLastError();
+}
+
 template <bool INNER>
 cudaError_t launch_tmem(const TcArgs& args, dim3 grid, cudaStream_t s) {
     static bool attr_set[64] = {false};
@@ -2421,8 +2841,10 @@ cudaError_t launch_main(const TcArgs& args, dim3 grid, cudaStream_t s) {
 }
 
 size_t bimg_bytes(const ModePlan& mp) {
-    // per K-step: hi and lo images of bn rows x 64 bytes (16 fp32 or 32 fp16)
-    return (size_t)cdiv64(mp.g.R, mp.bn) * mp.tc_ks * 2 * (size_t)mp.bn * 64;
+    // per K-step: hi and lo images of bn rows x tc_kw elements (64-byte rows of
+    // 16 fp32 or 32 fp16; 128-byte rows of 64 fp16 for tc_img)
+    const size_t row = mp.tc_img ? 128 : 64;
+    return (size_t)cdiv64(mp.g.R, mp.bn) * mp.tc_ks * 2 * (size_t)mp.bn * row;
 }
 
 // fp16 split: the column scales follow the images
@@ -2438,7 +2860,7 @@ bool small_eligible(const ModeGeom& g) {
 }  // namespace
 
 size_t tc_binner_bytes(const ModePlan& mp) {
-    return mp.tc_h2 ? colscale_offset(mp) + (size_t)mp.g.R * sizeof(float) : bimg_bytes(mp);
+    return (mp.tc_h2 || mp.tc_img) ? colscale_offset(mp) + (size_t)mp.g.R * sizeof(float) : bimg_bytes(mp);
 }
 
 bool tc_prefer(const ModePlan& mp) {
@@ -2469,6 +2891,22 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
     mp.tc_kw = mp.tc_h2 ? kBK2 : kBK;
     mp.bm = kBM;
     mp.bn = mp.tc_h2 ? kH2BN : mp.tc_tmem ? kTBN : g.R >= 192 ? 256 : (g.R > 64 ? 128 : 64);
+    // K-major modes with a wide enough R: the fp16 split streamed from images of
+    // Y written once per call (no producer warps, both operands in shared
+    // memory, 128 x 256 or 128 x 128 tiles, K-steps of 64 indices); the q-block
+    // length must not be padded to K-steps by much
+    mp.tc_img = 0;
+    if (TC_IMG && !mp.tc_inner && !mp.tc_small && g.R >= TC_IMG_MIN_R &&
+        cdiv64(g.Jq, kBK4) * kBK4 * 8 <= g.Jq * 9) {
+        ModePlan t = mp;
+        t.tc_img = 1;
+        t.tc_h2 = 0;
+        t.tc_tmem = 0;
+        t.tc_kw = kBK4;
+        t.bn = cdiv64(g.R, 256) * 256 * 20 <= cdiv64(g.R, 128) * 128 * 23 ? 256 : 128;
+        MapGeom mgi;
+        if (y_map_geom(t, p.dims, p.strides, p.d, mgi, 2)) mp = t;
+    }
     if (mp.tc_inner) {
         if (g.J > g.Jq && g.Jq != 1) return false;
         mp.tc_jq_steps = 1;
@@ -2479,7 +2917,7 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
     }
     if ((!mp.tc_small && cdiv64(g.I, kBM) > 65535) || g.npre >= ((int64_t)1 << 31)) return false;
     MapGeom mg;
-    if (!y_map_geom(mp, p.dims, p.strides, p.d, mg)) return false;
+    if (!y_map_geom(mp, p.dims, p.strides, p.d, mg, mp.tc_img ? 2 : 4)) return false;
     // split count: fill whole waves of one CTA per SM, at least two drain
     // chunks per CTA where possible
     const int64_t tiles = (mp.tc_small ? 1 : cdiv64(g.I, kBM)) * cdiv64(g.R, mp.bn);
@@ -2511,7 +2949,7 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
         return MTTKRP_ERR_INVALID;
     }
     MapGeom mg;
-    if (!y_map_geom(mp, p.dims, p.strides, p.d, mg)) {
+    if (!y_map_geom(mp, p.dims, p.strides, p.d, mg, mp.tc_img ? 2 : 4)) {
         snprintf(errbuf, errlen, "mode %d: Y view not expressible as a TMA tensor map", g.k);
         return MTTKRP_ERR_UNSUPPORTED;
     }
@@ -2522,21 +2960,39 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     }
     TcArgs args;
     memset(&args, 0, sizeof(args));
+    // fp16 images of Y (tc_img): hi then lo, in the region every tc_img mode shares
+    uint8_t* ws_base = static_cast<uint8_t*>(binner_ws) - mp.off_binner;
+    int64_t numel = 1;
+    for (int t = 0; t < p.d; ++t) numel *= p.dims[t];
+    __half* img_hi = reinterpret_cast<__half*>(ws_base + mp.off_img);
+    __half* img_lo = reinterpret_cast<__half*>(ws_base + mp.off_img + ((size_t)numel * 2 + 255) / 256 * 256);
+    const size_t esize = mp.tc_img ? 2 : 4;
     cuuint64_t gdim[5], gstride[4];
     cuuint32_t box[5], estr[5];
     for (int t = 0; t < mg.rank; ++t) {
         gdim[t] = mg.dim[t];
         box[t] = mg.box[t];
         estr[t] = 1;
-        if (t > 0) gstride[t - 1] = mg.stride_el[t] * sizeof(float);
+        if (t > 0) gstride[t - 1] = mg.stride_el[t] * esize;
     }
-    CUresult cr = encode(&args.ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)mg.rank,
-                         const_cast<float*>(Y), gdim, gstride, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         mp.tc_inner ? CU_TENSOR_MAP_SWIZZLE_NONE
-                         : mp.tc_h2  ? CU_TENSOR_MAP_SWIZZLE_128B   // 32 fp32 = 128-byte rows
-                                     : CU_TENSOR_MAP_SWIZZLE_64B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult cr;
+    if (mp.tc_img) {
+        // 64 fp16 = 128-byte rows, 128-byte swizzle (the MMA descriptors' layout)
+        cr = encode(&args.ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)mg.rank, img_hi, gdim, gstride,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr == CUDA_SUCCESS)
+            cr = encode(&args.ymap_lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)mg.rank, img_lo, gdim,
+                        gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cr = encode(&args.ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)mg.rank, const_cast<float*>(Y),
+                    gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    mp.tc_inner ? CU_TENSOR_MAP_SWIZZLE_NONE
+                    : mp.tc_h2  ? CU_TENSOR_MAP_SWIZZLE_128B   // 32 fp32 = 128-byte rows
+                                : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (cr != CUDA_SUCCESS) {
         snprintf(errbuf, errlen, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
         return MTTKRP_ERR_CUDA;
@@ -2549,18 +3005,26 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     float* colscale = reinterpret_cast<float*>(static_cast<uint8_t*>(binner_ws) + colscale_offset(mp));
     // the first bytes of the workspace (reserved region) hold max |Y| as fp32 bits
     uint32_t* ymax = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(binner_ws) - mp.off_binner);
-    if (mp.tc_h2) {
+    if (mp.tc_h2 || mp.tc_img) {
         cudaError_t e = cudaSuccess;
         if (!p.ymax_ready) e = cudaMemsetAsync(ymax, 0, sizeof(uint32_t), stream);
         if (e == cudaSuccess && !p.ymax_ready) {
-            int64_t numel = 1;
-            for (int t = 0; t < p.d; ++t) numel *= p.dims[t];
             int64_t blocks = cdiv64(numel / 4 + 1, 256);
             if (blocks > 152 * 8) blocks = 152 * 8;
             absmax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, numel, ymax);
             e = cudaGetLastError();
             if (e == cudaSuccess) {
                 p.ymax_ready = 1;
+                ++*nlaunch;
+            }
+        }
+        if (e == cudaSuccess && mp.tc_img && !p.img_ready) {
+            int64_t blocks = cdiv64(numel / 4 + 1, 256);
+            if (blocks > 152 * 8) blocks = 152 * 8;
+            split_image_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, numel, ymax, img_hi, img_lo);
+            e = cudaGetLastError();
+            if (e == cudaSuccess) {
+                p.img_ready = 1;
                 ++*nlaunch;
             }
         }
@@ -2603,8 +3067,10 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
         const int64_t n = b.nblocks * 2 * mp.bn * mp.tc_kw;
         int64_t blocks = cdiv64(n, 256);
         if (blocks > 152 * 16) blocks = 152 * 16;
-        if (mp.tc_h2)
-            tc_bimage_h2_kernel<<<(unsigned)blocks, 256, 0, stream>>>(b, colscale);
+        if (mp.tc_img)
+            tc_bimage_f16_kernel<kBK4><<<(unsigned)blocks, 256, 0, stream>>>(b, colscale);
+        else if (mp.tc_h2)
+            tc_bimage_f16_kernel<kBK2><<<(unsigned)blocks, 256, 0, stream>>>(b, colscale);
         else
             tc_bimage_kernel<<<(unsigned)blocks, 256, 0, stream>>>(b);
         cudaError_t e = cudaGetLastError();
@@ -2632,7 +3098,8 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     args.jq_steps = mp.tc_jq_steps;
     args.ps = mp.tc_small ? mp.tc_ps : 1;
     args.batch_len = nQ > 1 ? nQ : g.npre;
-    args.y_box_bytes = (uint32_t)mp.tc_kw * 4u * (mp.tc_small ? (uint32_t)(g.I * mp.tc_ps) : (uint32_t)kBM);
+    args.y_box_bytes = mp.tc_img ? (uint32_t)kBK4 * 2u * (uint32_t)kBM   // one fp16 image tile
+                                 : (uint32_t)mp.tc_kw * 4u * (mp.tc_small ? (uint32_t)(g.I * mp.tc_ps) : (uint32_t)kBM);
     args.ymax_bits = ymax;
     args.colscale = colscale;
     {
@@ -2650,7 +3117,9 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     dim3 grid((unsigned)cdiv64(g.R, mp.bn), mp.tc_small ? 1u : (unsigned)cdiv64(g.I, kBM),
               (unsigned)mp.splits);
     cudaError_t e;
-    if (mp.tc_h2) {
+    if (mp.tc_img) {
+        e = mp.bn == 256 ? launch_img<256>(args, grid, stream) : launch_img<128>(args, grid, stream);
+    } else if (mp.tc_h2) {
         e = mp.tc_inner ? launch_h2<true>(args, grid, stream) : launch_h2<false>(args, grid, stream);
     } else if (mp.tc_tmem) {
         e = mp.tc_inner ? launch_tmem<true>(args, grid, stream) : launch_tmem<false>(args, grid, stream);

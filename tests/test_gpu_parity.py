@@ -156,6 +156,15 @@ EDGE = [
     # and innermost modes, row / column / contraction tails
     ((24, 40, 136), 460),
     ((130, 6, 7, 100), 500),
+    # K-major modes on the fp16-image kernel (Y split once into fp16 images):
+    # a contraction tail inside the last 64-index step, row and column tails,
+    # 128- and 256-column tiles, pre modes on one or both sides of the mode
+    ((136, 24, 120), 260),
+    ((200, 96, 64), 300),
+    ((160, 8, 16, 64), 200),
+    ((16, 130, 8, 64), 200),
+    ((4, 8, 136, 64), 160),
+    ((128, 64, 4, 64), 128),
 ]
 
 
@@ -286,7 +295,7 @@ def test_timing_events_and_launch_count(path):
 # value ranges for the fp16-split tensor-core kernel (power-of-two scaling)
 # ---------------------------------------------------------------------------
 
-H2_SHAPES = [((130, 40, 48), 300), ((40, 36, 128), 450)]
+H2_SHAPES = [((130, 40, 48), 300), ((40, 36, 128), 450), ((200, 96, 64), 300)]
 
 
 def h2_modes(plan, d):
@@ -315,7 +324,28 @@ def test_scaled_values(dims, R, yscale, ascale):
         assert rel_fro(got[k], ref) <= TOL, f"{dims} k={k} scales {yscale},{ascale}"
 
 
-@pytest.mark.parametrize("dims,R", H2_SHAPES)
+@pytest.mark.parametrize("yscale,ascale", [(1e20, 1e-12), (1e-25, 1e8), (3.0, 1e-11)])
+def test_scaled_values_two_pre_modes(yscale, ascale):
+    """The same with two pre modes on either side of the mode: the factor-product
+    table G multiplies two factor rows in fp32 on every path, so the scales are
+    chosen to keep those products within the fp32 normal range (with A scaled by
+    1e-20, as above, they would be about 1e-40 and lose bits to gradual
+    underflow before any kernel runs)."""
+    dims, R = (16, 130, 8, 64), 200
+    Y, A = synth.random_case(500 + R, dims, R)
+    Y = (Y.astype(np.float64) * yscale).astype(np.float32)
+    A = [(a.astype(np.float64) * ascale).astype(np.float32) for a in A]
+    plan = make_plan(dims, R, "auto")
+    modes = h2_modes(plan, len(dims))
+    assert 1 in modes
+    got = gpu_modes(Y, A, "auto", modes=modes, plan=plan)
+    for k in modes:
+        ref = oracle.mttkrp(Y, A, k)
+        assert np.isfinite(got[k]).all()
+        assert rel_fro(got[k], ref) <= TOL, f"{dims} k={k} scales {yscale},{ascale}"
+
+
+@pytest.mark.parametrize("dims,R", H2_SHAPES + [((16, 130, 8, 64), 200)])
 def test_outlier_zero_column_and_zero_tensor(dims, R):
     Y, A = synth.random_case(600 + R, dims, R)
     Y = Y.copy()
@@ -331,3 +361,14 @@ def test_outlier_zero_column_and_zero_tensor(dims, R):
     zero = gpu_modes(np.zeros_like(Y), A, "auto")
     for k in range(len(dims)):
         assert not zero[k].any()
+
+
+def test_image_kernel_is_planned_for_k_major_modes():
+    """The fp16-image kernel takes the K-major modes of these shapes (so the
+    edge cases above exercise it), and the innermost mode stays off it."""
+    cases = {((200, 96, 64), 300): [0, 1], ((16, 130, 8, 64), 200): [1], ((512, 512, 512), 2000): [0, 1],
+             ((128, 128, 128, 128), 256): [0, 1, 2]}
+    for (dims, R), modes in cases.items():
+        plan = make_plan(dims, R, "auto")
+        img = [k for k in range(len(dims)) if "tc_fp16_image=1" in plan.describe(k)]
+        assert img == modes, (dims, R, img)
