@@ -136,21 +136,31 @@ void layout_workspace(ModePlan& mp) {
 // that the images written for the first such mode of a call serve the others
 void place_images(Plan& p) {
     size_t base = 0;
-    bool any = false;
+    p.img_nat = p.img_t = 0;
     for (int k = 0; k < p.d; ++k) {
-        if (p.mode[k].path == MTTKRP_PATH_TC && p.mode[k].tc_img) any = true;
-        if (p.mode[k].total > base) base = p.mode[k].total;
+        const ModePlan& mp = p.mode[k];
+        if (mp.path == MTTKRP_PATH_TC && mp.tc_img) {
+            if (mp.tc_img_t)
+                p.img_t = 1;
+            else
+                p.img_nat = 1;
+        }
+        if (mp.total > base) base = mp.total;
     }
-    if (!any) return;
+    if (!p.img_nat && !p.img_t) return;
     base = align256(base);
     int64_t numel = 1;
     for (int n = 0; n < p.d; ++n) numel *= p.dims[n];
     const size_t img = 2 * align256((size_t)numel * 2);   // hi and lo, 2 bytes an element
+    const size_t off_nat = base;
+    const size_t off_t = base + (p.img_nat ? img : 0);
+    const size_t total = off_t + (p.img_t ? img : 0);
     for (int k = 0; k < p.d; ++k) {
         ModePlan& mp = p.mode[k];
         if (mp.path != MTTKRP_PATH_TC || !mp.tc_img) continue;
-        mp.off_img = base;
-        mp.total = base + img;
+        mp.off_img = off_nat;
+        mp.off_timg = off_t;
+        mp.total = total;
     }
 }
 
@@ -493,7 +503,7 @@ int mttkrp_plan_describe(mttkrp_plan_t h, int mode, char* buf, size_t len) {
                      mode, mp.path == MTTKRP_PATH_TC ? "tc" : "simt", mp.bm, mp.bn, groups,
                      (long long)g.J, (long long)g.Jq, pres, (long long)g.npre,
                      (long long)mp.splits, (long long)mp.pre_per_split, mp.total, mp.tc_ks, mp.tc_inner,
-                     mp.tc_small ? mp.tc_ps : 1, mp.tc_tmem, mp.tc_h2 || mp.tc_img, mp.tc_img);
+                     mp.tc_small ? mp.tc_ps : 1, mp.tc_tmem, mp.tc_h2 || mp.tc_img, mp.tc_img + mp.tc_img_t);
     if (buf != nullptr && len > 0) {
         strncpy(buf, tmp, len - 1);
         buf[len - 1] = 0;

@@ -62,10 +62,13 @@ struct ModePlan {
     int tc_h2;          // 1: two-term fp16 split (kind::f16, K-steps of 32); implies tc_tmem
     int tc_kw;          // contraction indices per K-step (16; 32 with tc_h2; 64 with tc_img)
     int tc_img;         // 1: two-term fp16 split from pre-split fp16 images of Y, both
-                        //    operands in shared memory (K-major modes, K-steps of 64)
+                        //    operands in shared memory (K-steps of 64)
+    int tc_img_t;       // tc_img for the innermost mode: from the transposed images
+                        //    (Y viewed as P x I_{d-1}, stored I_{d-1} x P)
     // workspace layout, byte offsets from the workspace base
     size_t off_partials, off_binner, off_gtab, off_base, total;
     size_t off_img;     // tc_img: fp16 hi image of Y, then the lo image (shared by all modes)
+    size_t off_timg;    // tc_img: the transposed hi and lo images
 };
 
 struct Plan {
@@ -86,6 +89,7 @@ struct Plan {
     mutable int ymax_ready;
     // fp16 images of Y (tc_img modes) already written for the current call's Y
     mutable int img_ready;
+    int img_nat, img_t;   // which images the plan's tc_img modes read (natural, transposed)
     // benchmark timing: event pairs around the main kernel of each mode
     int timing;
     int ev_cap[kMaxD];

@@ -1527,6 +1527,9 @@ constexpr int kChunkSteps2 = 4;   // 128 contraction indices between TMEM drains
 #ifndef TC_IMG
 #define TC_IMG 1           // fp16-image kernel for K-major modes
 #endif
+#ifndef TC_IMG_XPOSE
+#define TC_IMG_XPOSE 1     // the innermost mode from transposed fp16 images
+#endif
 #ifndef TC_IMG_MIN_R
 #define TC_IMG_MIN_R 128
 #endif
@@ -2431,6 +2434,94 @@ __global__ void __launch_bounds__(256) split_image_kernel(const float* __restric
     }
 }
 
+// The same split for the innermost mode: Y viewed as P x I (I = I_{d-1}, the
+// contiguous mode) is also written transposed, I x P, so that the innermost
+// mode's tiles are K-contiguous too.  One 64 (p) x 128 (i) tile per step: each
+// warp reads rows of 128 consecutive i (16-byte loads; scalar when I is not a
+// multiple of 4), converts, optionally writes the natural images (8-byte
+// stores), and parks (hi | lo << 16) in shared memory; then each warp writes
+// rows of 64 consecutive p of both transposed images (4-byte stores, P even).
+template <bool VEC>
+__global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restrict__ y, int64_t P, int64_t I,
+                                                            const uint32_t* __restrict__ ymax_bits,
+                                                            __half* __restrict__ hi, __half* __restrict__ lo,
+                                                            __half* __restrict__ thi, __half* __restrict__ tlo,
+                                                            int write_nat) {
+    constexpr int TP = 64, TI = 128;
+    __shared__ uint32_t sh[TI][TP + 1];   // [i][p]: hi in the low half, lo in the high half
+    const float sy = pow2_scale(*ymax_bits);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t np = (P + TP - 1) / TP, ni = (I + TI - 1) / TI;
+    for (int64_t t = blockIdx.x; t < np * ni; t += gridDim.x) {
+        const int64_t p0 = (t / ni) * TP, i0 = (t % ni) * TI;
+        const int64_t ib = i0 + 4 * lane;   // this lane's first i
+#pragma unroll 2
+        for (int r = warp; r < TP; r += 8) {
+            const int64_t pr = p0 + r;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            const int64_t e = pr * I + ib;
+            if (pr < P) {
+                if (VEC) {
+                    if (ib < I) {
+                        const float4 x = __ldcs(reinterpret_cast<const float4*>(y + e));
+                        v[0] = x.x;
+                        v[1] = x.y;
+                        v[2] = x.z;
+                        v[3] = x.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (ib + q < I) v[q] = __ldcs(y + e + q);
+                }
+            }
+            uint32_t hb[4], lb[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float x = v[q] * sy;
+                const __half h = __float2half_rn(x);
+                const __half l = __float2half_rn(x - __half2float(h));
+                hb[q] = __half_as_ushort(h);
+                lb[q] = __half_as_ushort(l);
+                sh[4 * lane + q][r] = hb[q] | (lb[q] << 16);
+            }
+            if (write_nat && pr < P) {
+                if (VEC) {
+                    if (ib < I) {
+                        reinterpret_cast<uint2*>(hi + e)[0] = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
+                        reinterpret_cast<uint2*>(lo + e)[0] = make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (ib + q < I) {
+                            hi[e + q] = __ushort_as_half((unsigned short)hb[q]);
+                            lo[e + q] = __ushort_as_half((unsigned short)lb[q]);
+                        }
+                }
+            }
+        }
+        __syncthreads();
+        for (int c = warp; c < TI; c += 8) {
+            const int64_t ic = i0 + c;
+            const int64_t pc = p0 + 2 * lane;
+            if (ic < I && pc < P) {
+                const uint32_t w0 = sh[c][2 * lane], w1 = sh[c][2 * lane + 1];
+                const int64_t e = ic * P + pc;
+                if (pc + 1 < P) {
+                    *reinterpret_cast<uint32_t*>(thi + e) = __byte_perm(w0, w1, 0x5410);
+                    *reinterpret_cast<uint32_t*>(tlo + e) = __byte_perm(w0, w1, 0x7632);
+                } else {
+                    thi[e] = __ushort_as_half((unsigned short)(w0 & 0xFFFFu));
+                    tlo[e] = __ushort_as_half((unsigned short)(w0 >> 16));
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Prep: pre-swizzled hi/lo images of the inner Khatri-Rao table
 // ---------------------------------------------------------------------------
@@ -2744,6 +2835,43 @@ bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides,
     return true;
 }
 
+// Tensor-map geometry of the transposed images for the innermost mode: element
+// (i, pi, j) at i * P + pi * J + j (P = npre * J); roles j (Jq, box 64), i (box
+// 128) and pi (PP); false if TMA cannot express it.
+bool timg_map_geom(const ModePlan& mp, MapGeom& mg) {
+    const ModeGeom& g = mp.g;
+    const int64_t P = g.npre * g.J;
+    if ((g.J * 2) % 16 != 0 || (P * 2) % 16 != 0 || P * 2 >= ((int64_t)1 << 40)) return false;
+    if (g.J >= ((int64_t)1 << 31) || g.I >= ((int64_t)1 << 31) || g.npre >= ((int64_t)1 << 31)) return false;
+    mg.rank = 3;
+    for (int q = 0; q < kRoles; ++q) mg.slot[q] = -1;
+    mg.slot[kRoleJq] = 0;
+    mg.slot[kRoleI] = 1;
+    mg.slot[kRolePP] = 2;
+    mg.dim[0] = (uint64_t)g.J;
+    mg.dim[1] = (uint64_t)g.I;
+    mg.dim[2] = (uint64_t)g.npre;
+    mg.stride_el[0] = 1;
+    mg.stride_el[1] = (uint64_t)P;
+    mg.stride_el[2] = (uint64_t)g.J;
+    mg.box[0] = (uint32_t)kBK4;
+    mg.box[1] = kBM;
+    mg.box[2] = 1;
+    return true;
+}
+
+// The innermost mode can read transposed images when its inner group is the run
+// of modes just before it and the pre modes are the modes before that (then
+// (pi, j) is contiguous in the transposed layout).
+bool timg_eligible(const ModeGeom& g, int d) {
+    if (g.k != d - 1 || g.ngroup < 1) return false;
+    for (int t = 0; t < g.ngroup; ++t)
+        if (g.group[t] != d - 1 - g.ngroup + t) return false;
+    for (int t = 0; t < g.npm; ++t)
+        if (g.pm[t] != t) return false;
+    return g.npm + g.ngroup == d - 1;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (fn == nullptr) {
@@ -2896,8 +3024,8 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
     // memory, 128 x 256 or 128 x 128 tiles, K-steps of 64 indices); the q-block
     // length must not be padded to K-steps by much
     mp.tc_img = 0;
-    if (TC_IMG && !mp.tc_inner && !mp.tc_small && g.R >= TC_IMG_MIN_R &&
-        cdiv64(g.Jq, kBK4) * kBK4 * 8 <= g.Jq * 9) {
+    mp.tc_img_t = 0;
+    if (TC_IMG && !mp.tc_small && g.R >= TC_IMG_MIN_R) {
         ModePlan t = mp;
         t.tc_img = 1;
         t.tc_h2 = 0;
@@ -2905,7 +3033,14 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
         t.tc_kw = kBK4;
         t.bn = cdiv64(g.R, 256) * 256 * 20 <= cdiv64(g.R, 128) * 128 * 23 ? 256 : 128;
         MapGeom mgi;
-        if (y_map_geom(t, p.dims, p.strides, p.d, mgi, 2)) mp = t;
+        if (!mp.tc_inner) {
+            if (cdiv64(g.Jq, kBK4) * kBK4 * 8 <= g.Jq * 9 && y_map_geom(t, p.dims, p.strides, p.d, mgi, 2)) mp = t;
+        } else if (TC_IMG_XPOSE && timg_eligible(g, p.d) && cdiv64(g.J, kBK4) * kBK4 * 8 <= g.J * 9) {
+            // the innermost mode from the transposed images (written in the same
+            // pass as the others); the K-steps run over j alone
+            t.tc_img_t = 1;
+            if (timg_map_geom(t, mgi)) mp = t;
+        }
     }
     if (mp.tc_inner) {
         if (g.J > g.Jq && g.Jq != 1) return false;
@@ -2915,9 +3050,11 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
         mp.tc_jq_steps = (int)cdiv64(g.Jq, mp.tc_kw);
         mp.tc_ks = (int)((g.J / g.Jq) * mp.tc_jq_steps);
     }
+    if (mp.tc_img_t) mp.tc_jq_steps = mp.tc_ks;   // the j role carries the whole K-step offset
     if ((!mp.tc_small && cdiv64(g.I, kBM) > 65535) || g.npre >= ((int64_t)1 << 31)) return false;
     MapGeom mg;
-    if (!y_map_geom(mp, p.dims, p.strides, p.d, mg, mp.tc_img ? 2 : 4)) return false;
+    if (mp.tc_img_t ? !timg_map_geom(mp, mg) : !y_map_geom(mp, p.dims, p.strides, p.d, mg, mp.tc_img ? 2 : 4))
+        return false;
     // split count: fill whole waves of one CTA per SM, at least two drain
     // chunks per CTA where possible
     const int64_t tiles = (mp.tc_small ? 1 : cdiv64(g.I, kBM)) * cdiv64(g.R, mp.bn);
@@ -2949,7 +3086,7 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
         return MTTKRP_ERR_INVALID;
     }
     MapGeom mg;
-    if (!y_map_geom(mp, p.dims, p.strides, p.d, mg, mp.tc_img ? 2 : 4)) {
+    if (mp.tc_img_t ? !timg_map_geom(mp, mg) : !y_map_geom(mp, p.dims, p.strides, p.d, mg, mp.tc_img ? 2 : 4)) {
         snprintf(errbuf, errlen, "mode %d: Y view not expressible as a TMA tensor map", g.k);
         return MTTKRP_ERR_UNSUPPORTED;
     }
@@ -2964,8 +3101,13 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     uint8_t* ws_base = static_cast<uint8_t*>(binner_ws) - mp.off_binner;
     int64_t numel = 1;
     for (int t = 0; t < p.d; ++t) numel *= p.dims[t];
+    const size_t img_half = ((size_t)numel * 2 + 255) / 256 * 256;
     __half* img_hi = reinterpret_cast<__half*>(ws_base + mp.off_img);
-    __half* img_lo = reinterpret_cast<__half*>(ws_base + mp.off_img + ((size_t)numel * 2 + 255) / 256 * 256);
+    __half* img_lo = reinterpret_cast<__half*>(ws_base + mp.off_img + img_half);
+    __half* timg_hi = reinterpret_cast<__half*>(ws_base + mp.off_timg);
+    __half* timg_lo = reinterpret_cast<__half*>(ws_base + mp.off_timg + img_half);
+    __half* map_hi = mp.tc_img_t ? timg_hi : img_hi;
+    __half* map_lo = mp.tc_img_t ? timg_lo : img_lo;
     const size_t esize = mp.tc_img ? 2 : 4;
     cuuint64_t gdim[5], gstride[4];
     cuuint32_t box[5], estr[5];
@@ -2978,11 +3120,11 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     CUresult cr;
     if (mp.tc_img) {
         // 64 fp16 = 128-byte rows, 128-byte swizzle (the MMA descriptors' layout)
-        cr = encode(&args.ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)mg.rank, img_hi, gdim, gstride,
+        cr = encode(&args.ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)mg.rank, map_hi, gdim, gstride,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (cr == CUDA_SUCCESS)
-            cr = encode(&args.ymap_lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)mg.rank, img_lo, gdim,
+            cr = encode(&args.ymap_lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)mg.rank, map_lo, gdim,
                         gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
@@ -3019,9 +3161,23 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
             }
         }
         if (e == cudaSuccess && mp.tc_img && !p.img_ready) {
-            int64_t blocks = cdiv64(numel / 4 + 1, 256);
-            if (blocks > 152 * 8) blocks = 152 * 8;
-            split_image_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, numel, ymax, img_hi, img_lo);
+            // every image the plan's tc_img modes read, in one pass over Y
+            if (p.img_t) {
+                const int64_t In = p.dims[p.d - 1];
+                const int64_t P = numel / In;
+                int64_t blocks = cdiv64(P, 64) * cdiv64(In, 128);
+                if (blocks > 152 * 16) blocks = 152 * 16;
+                if (In % 4 == 0)
+                    split_image_t_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(Y, P, In, ymax, img_hi, img_lo,
+                                                                                     timg_hi, timg_lo, p.img_nat);
+                else
+                    split_image_t_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(Y, P, In, ymax, img_hi, img_lo,
+                                                                                      timg_hi, timg_lo, p.img_nat);
+            } else {
+                int64_t blocks = cdiv64(numel / 4 + 1, 256);
+                if (blocks > 152 * 8) blocks = 152 * 8;
+                split_image_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, numel, ymax, img_hi, img_lo);
+            }
             e = cudaGetLastError();
             if (e == cudaSuccess) {
                 p.img_ready = 1;
@@ -3085,6 +3241,7 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     int64_t nQ = 1;
     for (int t = 0; t < g.npm; ++t)
         if (g.pm[t] > g.k) nQ *= p.dims[g.pm[t]];
+    if (mp.tc_img_t) nQ = 1;   // one pre dimension in the transposed layout
     args.bimg = bimg;
     args.gtab = gtab;
     args.dst = dst;

@@ -165,6 +165,11 @@ EDGE = [
     ((16, 130, 8, 64), 200),
     ((4, 8, 136, 64), 160),
     ((128, 64, 4, 64), 128),
+    # the innermost mode from the transposed images: row tails (I_{d-1} = 200,
+    # 130, 150), a contraction tail (J = 120), two inner-group modes
+    ((24, 120, 200), 300),
+    ((10, 128, 130), 256),
+    ((64, 8, 8, 150), 200),
 ]
 
 
@@ -295,7 +300,7 @@ def test_timing_events_and_launch_count(path):
 # value ranges for the fp16-split tensor-core kernel (power-of-two scaling)
 # ---------------------------------------------------------------------------
 
-H2_SHAPES = [((130, 40, 48), 300), ((40, 36, 128), 450), ((200, 96, 64), 300)]
+H2_SHAPES = [((130, 40, 48), 300), ((40, 36, 128), 450), ((200, 96, 64), 300), ((24, 120, 200), 300)]
 
 
 def h2_modes(plan, d):
@@ -363,12 +368,15 @@ def test_outlier_zero_column_and_zero_tensor(dims, R):
         assert not zero[k].any()
 
 
-def test_image_kernel_is_planned_for_k_major_modes():
-    """The fp16-image kernel takes the K-major modes of these shapes (so the
-    edge cases above exercise it), and the innermost mode stays off it."""
-    cases = {((200, 96, 64), 300): [0, 1], ((16, 130, 8, 64), 200): [1], ((512, 512, 512), 2000): [0, 1],
-             ((128, 128, 128, 128), 256): [0, 1, 2]}
-    for (dims, R), modes in cases.items():
+def test_image_kernel_is_planned():
+    """The fp16-image kernel takes the K-major modes of these shapes from the
+    natural images (tc_fp16_image=1) and the innermost mode from the transposed
+    images (=2), so the edge cases above exercise both."""
+    cases = {((200, 96, 64), 300): [1, 1, 0], ((16, 130, 8, 64), 200): [0, 1, 0, 0],
+             ((512, 512, 512), 2000): [1, 1, 2], ((128, 128, 128, 128), 256): [1, 1, 1, 2],
+             ((136, 24, 120), 260): [1, 0, 0], ((4, 8, 136, 64), 160): [0, 0, 1, 0],
+             ((24, 120, 200), 300): [0, 0, 2], ((64, 8, 8, 150), 200): [0, 0, 0, 2]}
+    for (dims, R), want in cases.items():
         plan = make_plan(dims, R, "auto")
-        img = [k for k in range(len(dims)) if "tc_fp16_image=1" in plan.describe(k)]
-        assert img == modes, (dims, R, img)
+        got = [int(plan.describe(k).split("tc_fp16_image=")[1].split()[0]) for k in range(len(dims))]
+        assert got == want, (dims, R, got)
