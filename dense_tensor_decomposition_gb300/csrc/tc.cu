@@ -2063,12 +2063,18 @@ __global__ void __launch_bounds__(kH2Threads, 1) tc_h2_kernel(const __grid_const
 // gives registers back), warps 4-19 epilogue (which take them).
 // ---------------------------------------------------------------------------
 constexpr int kBK4 = 64;          // contraction indices per K-step (128-byte fp16 rows)
-constexpr int kImgCK = 2;         // K-steps per B chunk and per TMEM drain (128 indices)
+#ifndef TC_IMG_EPI_LD
+#define TC_IMG_EPI_LD 16   // TMEM columns per epilogue load (8, 16 or 32)
+#endif
+#ifndef TC_IMG_CK
+#define TC_IMG_CK 2
+#endif
+constexpr int kImgCK = TC_IMG_CK;   // K-steps per B chunk and per TMEM drain (128 indices)
 constexpr int kImgEpiWarp0 = 4;
 constexpr int kImgThreads = (kImgEpiWarp0 + kEpiWarps) * 32;   // 640
 // registers a thread: the launch allots 96 (65536 / 640, in units of 8); the
-// split uses 128 x (48 + 4 x 104) = 59392 of the 61440 allotted
-constexpr int kImgRegsCtl = 48, kImgRegsEpi = 104, kImgRegsLaunch = 96;
+// split uses 128 x (56 + 4 x 104) = 60416 of the 61440 allotted
+constexpr int kImgRegsCtl = 56, kImgRegsEpi = 104, kImgRegsLaunch = 96;
 static_assert(128 * (kImgRegsCtl + 4 * kImgRegsEpi) <= kImgThreads * kImgRegsLaunch, "register split");
 
 // K-major, 128-byte swizzle descriptor: 8-row groups of 128-byte rows, 1024
@@ -2206,16 +2212,30 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                 jc_loaded = jc;
                 return true;
             };
+            // the pre index pi = (cP, cQ) in C order, advanced without divisions
+            const int64_t nQ = a.nQ;
+            const int cP0 = (int)(pre_lo / nQ), cQ0 = (int)(pre_lo - (int64_t)cP0 * nQ);
             for (int jc = 0; jc < njc && ok; ++jc) {
                 const int ck = chunk_len(jc);
                 // the first NS tiles of chunk jc need only work of chunk jc - 1,
                 // so they are issued before the chunk swap
                 const int64_t swap_at = issued + NS;
                 bool b_pending = true;
+                int cP = cP0, cQ = cQ0;
                 for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
-                    const int cP = (int)(pi / a.nQ);
-                    const int cQ = (int)(pi - (int64_t)cP * a.nQ);
                     for (int q = 0; q < ck; ++q, ++issued, rr.next()) {
+                        // box coordinates first: they do not depend on the slot, so
+                        // the copy is issued as soon as the slot is released
+                        const int ks = jc * CK + q;
+                        const int jp = ks / a.jq_steps;
+                        int role[kRoles];
+                        role[kRoleJq] = (ks - jp * a.jq_steps) * kBK4;
+                        role[kRoleJp] = jp;
+                        role[kRoleI] = (int)m0;
+                        role[kRolePP] = cP;
+                        role[kRolePQ] = cQ;
+                        int c[5];
+                        tma_coords(a.slot, role, c);
                         if (b_pending && issued == swap_at) {
                             b_pending = false;
                             if (!load_b(jc)) {
@@ -2228,20 +2248,14 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                             ok = false;
                             break;
                         }
-                        const int ks = jc * CK + q;
-                        const int jp = ks / a.jq_steps;
-                        int role[kRoles];
-                        role[kRoleJq] = (ks - jp * a.jq_steps) * kBK4;
-                        role[kRoleJp] = jp;
-                        role[kRoleI] = (int)m0;
-                        role[kRolePP] = cP;
-                        role[kRolePQ] = cQ;
-                        int c[5];
-                        tma_coords(a.slot, role, c);
                         uint8_t* st = ring + rr.slot * L::kStage;
                         mbar_arrive_expect_tx(&full[rr.slot], 2u * a.y_box_bytes);
                         tma_load(&a.ymap, a.rank, c, st, &full[rr.slot]);
                         tma_load(&a.ymap_lo, a.rank, c, st + L::kA, &full[rr.slot]);
+                    }
+                    if (++cQ == nQ) {
+                        cQ = 0;
+                        ++cP;
                     }
                 }
                 if (ok && b_pending && !load_b(jc)) ok = false;
@@ -2320,7 +2334,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
         // ---------------------- epilogue (16 warps) ----------------------
         constexpr int kCols = BN / 4;
         constexpr int kGv = (kCols + 31) / 32;   // G values a lane holds
-        static_assert(kCols % 8 == 0, "8-column TMEM loads");
+        static_assert(kCols % TC_IMG_EPI_LD == 0, "TMEM load width");
         const int quad = warp & 3;
         const int part = (warp - kImgEpiWarp0) >> 2;
         const int64_t row = m0 + 32 * quad + lane;
@@ -2355,12 +2369,12 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                 const uint32_t tbase =
                     tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
 #pragma unroll
-                for (int cc = 0; cc < kCols; cc += 8) {
-                    uint32_t z[8];
-                    tmem_ld8(tbase + cc, z);
+                for (int cc = 0; cc < kCols; cc += TC_IMG_EPI_LD) {
+                    uint32_t z[TC_IMG_EPI_LD];
+                    tmem_ld_cols<TC_IMG_EPI_LD>(tbase + cc, z);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
+                    for (int q = 0; q < TC_IMG_EPI_LD; ++q) {
                         const int e = cc + q;
                         const float g = __shfl_sync(0xffffffffu, g_cur[e / 32], e % 32);
                         acc[e] = fmaf(g, __uint_as_float(z[q]), acc[e]);
