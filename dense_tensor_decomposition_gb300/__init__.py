@@ -266,6 +266,57 @@ class Plan:
             m_h.copy_(m_d, non_blocking=True)
         return outs_host
 
+    def all_modes_pipelined(self, batches, dev_bufs, stream=None, copy_stream=None):
+        """End to end over a sequence of problems in pinned host memory, with the
+        copies overlapped with the computation.
+
+        batches = [(Y_host, [A_host...], [M_host...]), ...]; dev_bufs = two device
+        buffer sets (Y_dev, [A_dev...], [M_dev...]) used alternately.  The copy in of
+        problem t + 1 runs on a copy stream while problem t is computed on `stream`;
+        the outputs of problem t are copied out on the copy stream after its
+        computation.  Everything is enqueued; `stream` has waited for the last copy
+        out when this returns.
+        """
+        import torch
+        if len(dev_bufs) != 2:
+            raise ValueError("dev_bufs must hold two device buffer sets")
+        device = dev_bufs[0][0].device
+        comp = stream if stream is not None else torch.cuda.current_stream(device)
+        cs = copy_stream if copy_stream is not None else torch.cuda.Stream(device=device)
+        cs.wait_stream(comp)
+        n = len(batches)
+        ready, done = [None] * n, [None] * n
+
+        def copy_in(t):
+            Y_h, A_h, _ = batches[t]
+            Y_d, A_d, _ = dev_bufs[t % 2]
+            if t >= 2:
+                cs.wait_event(done[t - 2])   # the buffers' previous problem has been computed
+            with torch.cuda.stream(cs):
+                Y_d.copy_(Y_h, non_blocking=True)
+                for a_d, a_h in zip(A_d, A_h):
+                    a_d.copy_(a_h, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(cs)
+            return ev
+
+        if n:
+            ready[0] = copy_in(0)
+        for t in range(n):
+            if t + 1 < n:
+                ready[t + 1] = copy_in(t + 1)
+            Y_d, A_d, M_d = dev_bufs[t % 2]
+            comp.wait_event(ready[t])
+            self.all_modes(Y_d, A_d, outs=M_d, stream=comp)
+            done[t] = torch.cuda.Event()
+            done[t].record(comp)
+            cs.wait_event(done[t])
+            with torch.cuda.stream(cs):
+                for m_h, m_d in zip(batches[t][2], M_d):
+                    m_h.copy_(m_d, non_blocking=True)
+        comp.wait_stream(cs)
+        return [b[2] for b in batches]
+
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:
             self._lib.mttkrp_plan_destroy(self._h)

@@ -380,3 +380,22 @@ def test_image_kernel_is_planned():
         plan = make_plan(dims, R, "auto")
         got = [int(plan.describe(k).split("tc_fp16_image=")[1].split()[0]) for k in range(len(dims))]
         assert got == want, (dims, R, got)
+
+
+def test_pipelined_end_to_end_matches_device_calls():
+    """all_modes_pipelined: three different problems from pinned host memory, copies
+    overlapped with the computation on two buffer sets, equal (bitwise) to the
+    device-resident calls."""
+    dims, R = (136, 24, 120), 260
+    cases = [synth.random_case(900 + t, dims, R) for t in range(3)]
+    plan = make_plan(dims, R, "auto")
+    want = [[m.cpu().numpy() for m in plan.all_modes(dev(Y), [dev(a) for a in A])] for Y, A in cases]
+    batches = [(torch.from_numpy(Y).pin_memory(), [torch.from_numpy(a).pin_memory() for a in A],
+                [torch.empty(dims[k], R).pin_memory() for k in range(len(dims))]) for Y, A in cases]
+    bufs = tuple((torch.empty(dims, device="cuda"), [torch.empty(d, R, device="cuda") for d in dims],
+                  [torch.empty(d, R, device="cuda") for d in dims]) for _ in range(2))
+    got = plan.all_modes_pipelined(batches, bufs)
+    torch.cuda.synchronize()
+    for t in range(3):
+        for k in range(len(dims)):
+            assert np.array_equal(got[t][k].numpy(), want[t][k]), (t, k)
