@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cp-als", type=int, default=0, metavar="SWEEPS",
+                    help="instead: time SWEEPS CP-ALS sweeps (mttkrp_cp_als_sweep) on the workload's tensor")
+    ap.add_argument("--cp-rank", type=int, default=32, help="rank of the CP-ALS model (--cp-als)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target length of the oracle CPU-baseline sample")
     return ap.parse_args()
@@ -431,11 +434,54 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_cp_als(args, w):
+    """CP-ALS sweeps on the workload's tensor at rank --cp-rank from a seeded
+    random start: one JSON line with the time per sweep, the MTTKRP share of it
+    (CUDA events around the main kernels) and the fit reached."""
+    import numpy as np
+    import torch
+    import dense_tensor_decomposition_gb300 as mk
+    device = torch.device("cuda", 0)
+    Y = torch.from_numpy(synth.make_tensor(w)).to(device)
+    R = args.cp_rank
+    rng = np.random.default_rng(20261202)
+    A0 = [rng.standard_normal((n, R)).astype(np.float32) for n in w.dims]
+    plan = mk.Plan(w.dims, R, args.path)
+    A = [torch.from_numpy(a).to(device) for a in A0]
+    plan.cp_als(Y, A, sweeps=max(args.warmup, 1))          # warm-up (and first ||Y||^2)
+    A = [torch.from_numpy(a).to(device) for a in A0]
+    torch.cuda.synchronize(device)
+    plan.set_timing(True)
+    stream = torch.cuda.current_stream(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    lam, fits = plan.cp_als(Y, A, sweeps=args.cp_als)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / args.cp_als
+    mttkrp_ms = sum(sum(plan.kernel_times(k)) for k in range(w.d)) / args.cp_als
+    plan.set_timing(False)
+    print(json.dumps({
+        "metric": "CP-ALS time per sweep (every factor updated once, fit included)",
+        "value": round(ms, 4), "unit": "ms", "higher_is_better": False, "n_gpus": 1,
+        "steps": args.cp_als, "dtype": "fp16x2+f64" if plan.mode_path(0) == "tc" else "f32+f64",
+        "data": "synthetic", "impl": "ours",
+        "config": {"workload": w.name, "dims": list(w.dims), "R": R, "start": "seeded N(0,1) factors"},
+        "mttkrp_kernel_ms_per_sweep": round(mttkrp_ms, 4),
+        "mttkrp_share": round(mttkrp_ms / ms, 4),
+        "fit_first_last": [round(float(fits[0]), 6), round(float(fits[-1]), 6)],
+        "kernel_src": kernel_source_hash(),
+    }))
+
+
 def main():
     args = parse_args()
     w = workload_from_arg(args.workload)
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.cp_als > 0:
+        run_cp_als(args, w)
     else:
         run_ours(args, w)
 

@@ -79,6 +79,10 @@ def load_library():
         lib.mttkrp_last_error.restype = ctypes.c_char_p
         lib.mttkrp_version.argtypes = []
         lib.mttkrp_version.restype = ci
+        lib.mttkrp_cp_als_scratch_bytes.argtypes = [vp]
+        lib.mttkrp_cp_als_scratch_bytes.restype = sz
+        lib.mttkrp_cp_als_sweep.argtypes = [vp, vp, vp, vp, vp, ci, vp, vp, sz, vp]
+        lib.mttkrp_cp_als_sweep.restype = ci
         _lib = lib
         return lib
 
@@ -265,6 +269,32 @@ class Plan:
         for m_h, m_d in zip(outs_host, M_dev):
             m_h.copy_(m_d, non_blocking=True)
         return outs_host
+
+    def cp_als(self, Y, factors, sweeps: int = 1, stream=None):
+        """`sweeps` CP-ALS sweeps on device tensors (mttkrp_cp_als_sweep): the
+        factors are updated in place (normalised columns).  Returns (lambda, fits):
+        the last column norms (R fp32) and the fit after every sweep (fp64), both
+        on the device and not synchronised."""
+        import torch
+        if sweeps < 1:
+            raise ValueError("sweeps must be >= 1")
+        ptrs = self._check_inputs(Y, factors)
+        self.attach_workspace(Y.device)
+        need = int(self._lib.mttkrp_cp_als_scratch_bytes(self._h))
+        if getattr(self, "_cp_scratch", None) is None or self._cp_scratch.numel() < need \
+                or self._cp_scratch.device != Y.device:
+            self._cp_scratch = torch.empty(max(need, 256), dtype=torch.uint8, device=Y.device)
+        lam = torch.empty(self.R, dtype=torch.float32, device=Y.device)
+        fits = torch.empty(sweeps, dtype=torch.float64, device=Y.device)
+        norm = torch.empty(1, dtype=torch.float64, device=Y.device)
+        fptrs = (ctypes.c_void_p * self.d)(*[f.data_ptr() for f in factors])
+        for t in range(sweeps):
+            _check(self._lib.mttkrp_cp_als_sweep(
+                self._h, ctypes.c_void_p(Y.data_ptr()), fptrs, ctypes.c_void_p(lam.data_ptr()),
+                ctypes.c_void_p(norm.data_ptr()), int(t > 0), ctypes.c_void_p(fits.data_ptr() + 8 * t),
+                ctypes.c_void_p(self._cp_scratch.data_ptr()), self._cp_scratch.numel(),
+                _stream_handle(Y.device, stream)), "mttkrp_cp_als_sweep")
+        return lam, fits
 
     def all_modes_pipelined(self, batches, dev_bufs, stream=None, copy_stream=None):
         """End to end over a sequence of problems in pinned host memory, with the

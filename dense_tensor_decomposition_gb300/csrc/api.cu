@@ -479,6 +479,105 @@ int mttkrp_all_modes(mttkrp_plan_t h, const float* Y, const float* const* factor
     return MTTKRP_OK;
 }
 
+// CP-ALS scratch: Gram matrices of every mode, V (reused for the Hadamard
+// product of all Grams), the fp64 solve of the current mode, its fp32 MTTKRP,
+// the ||Y||^2 partials and the Cholesky status word.
+namespace {
+struct CpAlsLayout {
+    size_t grams, v, x, m, part, info, total;
+};
+CpAlsLayout cp_als_layout(const Plan& p) {
+    int64_t imax = 0;
+    for (int n = 0; n < p.d; ++n) imax = p.dims[n] > imax ? p.dims[n] : imax;
+    const size_t R = (size_t)p.R;
+    CpAlsLayout l;
+    size_t off = 0;
+    l.grams = off;
+    off = align256(off + (size_t)p.d * R * R * sizeof(double));
+    l.v = off;
+    off = align256(off + R * R * sizeof(double));
+    l.x = off;
+    off = align256(off + (size_t)imax * R * sizeof(double));
+    l.m = off;
+    off = align256(off + (size_t)imax * R * sizeof(float));
+    l.part = off;
+    off = align256(off + cpals_sumsq_scratch_bytes());
+    l.info = off;
+    off = align256(off + sizeof(int));
+    l.total = off;
+    return l;
+}
+}  // namespace
+
+size_t mttkrp_cp_als_scratch_bytes(mttkrp_plan_t h) {
+    Plan* p = as_plan(h);
+    return p == nullptr ? 0 : cp_als_layout(*p).total;
+}
+
+int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, float* lambda,
+                        double* norm_y2, int have_norm, double* fit, void* scratch, size_t scratch_bytes,
+                        void* stream) {
+    g_errmsg[0] = 0;
+    Plan* p = as_plan(h);
+    if (p == nullptr) return fail(MTTKRP_ERR_INVALID, "plan is NULL");
+    if (Y == nullptr || factors == nullptr || lambda == nullptr || norm_y2 == nullptr || fit == nullptr ||
+        scratch == nullptr)
+        return fail(MTTKRP_ERR_INVALID, "NULL tensor, factor array, lambda, norm, fit or scratch");
+    for (int n = 0; n < p->d; ++n)
+        if (factors[n] == nullptr) return fail(MTTKRP_ERR_INVALID, "factor %d is NULL", n);
+    if ((reinterpret_cast<uintptr_t>(scratch) & 255) != 0)
+        return fail(MTTKRP_ERR_INVALID, "scratch must be 256-byte aligned");
+    if (p->R > 65535) return fail(MTTKRP_ERR_UNSUPPORTED, "CP-ALS rank %lld above 65535", (long long)p->R);
+    const CpAlsLayout l = cp_als_layout(*p);
+    if (scratch_bytes < l.total)
+        return fail(MTTKRP_ERR_WORKSPACE, "CP-ALS scratch of %zu bytes is smaller than the %zu bytes needed",
+                    scratch_bytes, l.total);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(scratch);
+    double* G = reinterpret_cast<double*>(base + l.grams);
+    double* V = reinterpret_cast<double*>(base + l.v);
+    double* X = reinterpret_cast<double*>(base + l.x);
+    float* M = reinterpret_cast<float*>(base + l.m);
+    double* part = reinterpret_cast<double*>(base + l.part);
+    int* info = reinterpret_cast<int*>(base + l.info);
+    const int d = p->d;
+    const int R = (int)p->R;
+    const int64_t RR = (int64_t)R * R;
+    int64_t numel = 1;
+    for (int n = 0; n < d; ++n) numel *= p->dims[n];
+    cudaError_t e = cudaMemsetAsync(info, 0, sizeof(int), s);
+    if (e == cudaSuccess && !have_norm) {
+        e = cpals_sum_squares(Y, numel, part, norm_y2, s);
+        p->launches += 2;
+    }
+    for (int n = 0; n < d && e == cudaSuccess; ++n) {
+        e = cpals_gram(factors[n], p->dims[n], R, G + n * RR, s);
+        ++p->launches;
+    }
+    if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "CP-ALS setup: %s", cudaGetErrorString(e));
+    // one max |Y| pass and one image pass serve every mode of the sweep
+    p->ymax_ready = 0;
+    p->img_ready = 0;
+    for (int n = 0; n < d; ++n) {
+        if ((e = cpals_hadamard(G, d, n, R, V, s)) != cudaSuccess)
+            return fail(MTTKRP_ERR_CUDA, "CP-ALS Hadamard: %s", cudaGetErrorString(e));
+        ++p->launches;
+        int rc = run_mode(*p, Y, factors, n, M, s);
+        if (rc != MTTKRP_OK) return rc;
+        if ((e = cpals_cholesky(V, R, info, s)) == cudaSuccess &&
+            (e = cpals_solve(V, R, M, p->dims[n], X, s)) == cudaSuccess &&
+            (e = cpals_normalize(X, p->dims[n], R, factors[n], lambda, s)) == cudaSuccess)
+            e = cpals_gram(factors[n], p->dims[n], R, G + n * RR, s);
+        if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "CP-ALS update of mode %d: %s", n, cudaGetErrorString(e));
+        p->launches += 4;
+    }
+    if ((e = cpals_hadamard(G, d, -1, R, V, s)) == cudaSuccess)
+        e = cpals_fit(V, lambda, M, factors[d - 1], p->dims[d - 1], R, norm_y2, info, fit, s);
+    if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "CP-ALS fit: %s", cudaGetErrorString(e));
+    p->launches += 2;
+    return MTTKRP_OK;
+}
+
 int mttkrp_plan_mode_path(mttkrp_plan_t h, int mode) {
     Plan* p = as_plan(h);
     if (p == nullptr || mode < 0 || mode >= p->d) return -1;

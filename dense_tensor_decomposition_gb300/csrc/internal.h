@@ -126,6 +126,17 @@ struct SimtArgs {
 enum { kLoadScalar = 0, kLoadVecJ = 1, kLoadVecI = 2 };
 
 cudaError_t launch_prod_table(const ProdTableArgs& a, cudaStream_t s);
+
+// CP-ALS pieces (cpals.cu)
+cudaError_t cpals_gram(const float* A, int64_t I, int R, double* G, cudaStream_t s);
+cudaError_t cpals_hadamard(const double* G, int d, int skip, int R, double* V, cudaStream_t s);
+cudaError_t cpals_cholesky(double* V, int R, int* info, cudaStream_t s);
+cudaError_t cpals_solve(const double* L, int R, const float* M, int64_t I, double* X, cudaStream_t s);
+cudaError_t cpals_normalize(const double* X, int64_t I, int R, float* A, float* lam, cudaStream_t s);
+cudaError_t cpals_fit(const double* H, const float* lam, const float* M, const float* A, int64_t I, int R,
+                      const double* norm_y2, const int* info, double* fit, cudaStream_t s);
+size_t cpals_sumsq_scratch_bytes();
+cudaError_t cpals_sum_squares(const float* Y, int64_t n, double* part, double* out, cudaStream_t s);
 cudaError_t launch_reduce_splits(const float* part, int64_t splits, int64_t n, float* out,
                                  cudaStream_t s);
 cudaError_t launch_simt(int bm, int bn, int amode, bool bvec, const SimtArgs& a,

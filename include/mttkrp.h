@@ -18,15 +18,16 @@
  *            computed is not read and may be NULL.
  *   M_k      I_k x R row-major; overwritten (not accumulated into).
  *   workspace  caller-allocated device scratch of mttkrp_workspace_bytes()
- *            bytes, 256-byte aligned; holds split partial sums and small
- *            factor-product tables.  The library itself never allocates
- *            device memory.
+ *            bytes, 256-byte aligned; holds split partial sums, small
+ *            factor-product tables and, for tensor-core modes on the
+ *            fp16-image kernel, fp16 hi/lo images of Y (4 bytes an element
+ *            per layout).  The library itself never allocates device memory.
  *
  * Execution: every compute call only enqueues kernels on the given CUDA
  * stream (a cudaStream_t passed as void*; NULL = the legacy default stream)
  * and returns without synchronising.  Results are bitwise reproducible from
  * run to run for a given plan (no atomics; split partial sums are added in a
- * fixed order in fp64).  A plan and its workspace may be used by one stream
+ * fixed order, in fp64 or compensated fp32).  A plan and its workspace may be used by one stream
  * at a time; calls on one plan are not thread-safe.
  *
  * Errors: every int-returning call returns MTTKRP_OK (0) or one of the codes
@@ -60,7 +61,7 @@ enum mttkrp_status {
 enum mttkrp_path {
     MTTKRP_PATH_AUTO = 0,
     MTTKRP_PATH_SIMT = 1, /* fp32 FMA on the CUDA cores */
-    MTTKRP_PATH_TC = 2    /* tcgen05 tensor cores, 3xTF32 split, fp32-accurate */
+    MTTKRP_PATH_TC = 2    /* tcgen05 tensor cores, fp32-accurate split (fp16 two-term or 3xTF32) */
 };
 
 typedef struct mttkrp_plan_s* mttkrp_plan_t;
@@ -171,6 +172,40 @@ const char* mttkrp_last_error(void);
 #define MTTKRP_NOALLOC_SCRATCH_BYTES (32u << 20)
 int mttkrp_noalloc(int d, const int64_t* dims, int64_t R, const float* Y,
                    const float* const* factors, int mode, float* out, void* stream);
+
+/*
+ * CP-ALS sweep around the MTTKRP ("A Performance Portable Matrix Free Dense
+ * MTTKRP in GenTen", Fig. 5: CP-ALS = per mode an MTTKRP plus the other
+ * operations, an inner product and a Cholesky solve among them).  One call
+ * updates every factor in turn, n = 0 .. d-1, each update using the newest
+ * factors:
+ *     V   = Hadamard product over m != n of A_m^T A_m        (R x R, fp64)
+ *     M   = MTTKRP(Y, A, n)                                   (this plan)
+ *     A_n = M V^{-1}  (Cholesky factor of V, fp64), then lambda_r = ||A_n(:, r)||_2
+ *           and A_n(:, r) /= lambda_r (a zero column stays zero)
+ * and then writes
+ *     fit = 1 - ||Y - X||_F / ||Y||_F,  X = sum_r lambda_r a_r^(0) o ... o a_r^(d-1),
+ * from ||X||^2 = lambda^T (Hadamard product of all Grams) lambda and
+ * <Y, X> = sum_r lambda_r sum_i M(i, r) A_{d-1}(i, r) (M of the last mode).
+ *
+ * plan      a plan for Y's dims and the rank R; its workspace must be attached.
+ * Y         device tensor (as for mttkrp).
+ * factors   HOST array of d DEVICE pointers, each I_n x R fp32 row-major; all
+ *           are read and overwritten with the normalised updated factors.
+ * lambda    device, R fp32: the column norms of the last update (output).
+ * norm_y2   device, one double: ||Y||_F^2.  If have_norm is 0 the call
+ *           computes it first and stores it there (pass 1 afterwards).
+ * fit       device, one double (output); NaN if V was not positive definite.
+ * scratch   device scratch of mttkrp_cp_als_scratch_bytes(plan) bytes, 256-byte
+ *           aligned, caller-owned.
+ * Enqueues on `stream` and returns without synchronising.  Errors: as mttkrp,
+ * plus MTTKRP_ERR_WORKSPACE for a short scratch.  The Cholesky runs in one
+ * thread block: meant for the ranks CP-ALS is used at (up to a few hundred).
+ */
+size_t mttkrp_cp_als_scratch_bytes(mttkrp_plan_t plan);
+int mttkrp_cp_als_sweep(mttkrp_plan_t plan, const float* Y, float* const* factors, float* lambda,
+                        double* norm_y2, int have_norm, double* fit, void* scratch, size_t scratch_bytes,
+                        void* stream);
 
 /* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
 int mttkrp_version(void);
