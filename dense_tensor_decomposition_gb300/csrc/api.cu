@@ -484,7 +484,7 @@ int mttkrp_all_modes(mttkrp_plan_t h, const float* Y, const float* const* factor
 // the ||Y||^2 partials and the Cholesky status word.
 namespace {
 struct CpAlsLayout {
-    size_t grams, v, x, m, part, info, total;
+    size_t grams, v, dinv, x, m, gpart, part, info, total;
 };
 CpAlsLayout cp_als_layout(const Plan& p) {
     int64_t imax = 0;
@@ -496,10 +496,19 @@ CpAlsLayout cp_als_layout(const Plan& p) {
     off = align256(off + (size_t)p.d * R * R * sizeof(double));
     l.v = off;
     off = align256(off + R * R * sizeof(double));
+    l.dinv = off;
+    off = align256(off + R * sizeof(double));
     l.x = off;
     off = align256(off + (size_t)imax * R * sizeof(double));
     l.m = off;
     off = align256(off + (size_t)imax * R * sizeof(float));
+    int slabs = 1;
+    for (int n = 0; n < p.d; ++n) {
+        const int sn = cpals_gram_slabs(p.dims[n], (int)p.R);
+        slabs = sn > slabs ? sn : slabs;
+    }
+    l.gpart = off;
+    off = align256(off + (slabs > 1 ? (size_t)slabs * R * R * sizeof(double) : 0));
     l.part = off;
     off = align256(off + cpals_sumsq_scratch_bytes());
     l.info = off;
@@ -536,9 +545,11 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, 
     char* base = static_cast<char*>(scratch);
     double* G = reinterpret_cast<double*>(base + l.grams);
     double* V = reinterpret_cast<double*>(base + l.v);
+    double* dinv = reinterpret_cast<double*>(base + l.dinv);
     double* X = reinterpret_cast<double*>(base + l.x);
     float* M = reinterpret_cast<float*>(base + l.m);
     double* part = reinterpret_cast<double*>(base + l.part);
+    double* gpart = reinterpret_cast<double*>(base + l.gpart);
     int* info = reinterpret_cast<int*>(base + l.info);
     const int d = p->d;
     const int R = (int)p->R;
@@ -551,8 +562,8 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, 
         p->launches += 2;
     }
     for (int n = 0; n < d && e == cudaSuccess; ++n) {
-        e = cpals_gram(factors[n], p->dims[n], R, G + n * RR, s);
-        ++p->launches;
+        e = cpals_gram(factors[n], p->dims[n], R, G + n * RR, gpart, s);
+        p->launches += cpals_gram_slabs(p->dims[n], R) > 1 ? 2 : 1;
     }
     if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "CP-ALS setup: %s", cudaGetErrorString(e));
     // one max |Y| pass and one image pass serve every mode of the sweep
@@ -564,12 +575,12 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, 
         ++p->launches;
         int rc = run_mode(*p, Y, factors, n, M, s);
         if (rc != MTTKRP_OK) return rc;
-        if ((e = cpals_cholesky(V, R, info, s)) == cudaSuccess &&
-            (e = cpals_solve(V, R, M, p->dims[n], X, s)) == cudaSuccess &&
+        if ((e = cpals_cholesky(V, R, info, dinv, s)) == cudaSuccess &&
+            (e = cpals_solve(V, dinv, R, M, p->dims[n], X, s)) == cudaSuccess &&
             (e = cpals_normalize(X, p->dims[n], R, factors[n], lambda, s)) == cudaSuccess)
-            e = cpals_gram(factors[n], p->dims[n], R, G + n * RR, s);
+            e = cpals_gram(factors[n], p->dims[n], R, G + n * RR, gpart, s);
         if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "CP-ALS update of mode %d: %s", n, cudaGetErrorString(e));
-        p->launches += 4;
+        p->launches += 4 + cpals_cholesky_launches(R) + (cpals_gram_slabs(p->dims[n], R) > 1 ? 1 : 0);
     }
     if ((e = cpals_hadamard(G, d, -1, R, V, s)) == cudaSuccess)
         e = cpals_fit(V, lambda, M, factors[d - 1], p->dims[d - 1], R, norm_y2, info, fit, s);

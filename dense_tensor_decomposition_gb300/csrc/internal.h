@@ -128,10 +128,15 @@ enum { kLoadScalar = 0, kLoadVecJ = 1, kLoadVecI = 2 };
 cudaError_t launch_prod_table(const ProdTableArgs& a, cudaStream_t s);
 
 // CP-ALS pieces (cpals.cu)
-cudaError_t cpals_gram(const float* A, int64_t I, int R, double* G, cudaStream_t s);
+int cpals_gram_slabs(int64_t I, int R);   // partial Grams cpals_gram keeps (R x R fp64 each)
+cudaError_t cpals_gram(const float* A, int64_t I, int R, double* G, double* part, cudaStream_t s);
 cudaError_t cpals_hadamard(const double* G, int d, int skip, int R, double* V, cudaStream_t s);
-cudaError_t cpals_cholesky(double* V, int R, int* info, cudaStream_t s);
-cudaError_t cpals_solve(const double* L, int R, const float* M, int64_t I, double* X, cudaStream_t s);
+// lower Cholesky factor of V in place; dinv (R) receives the reciprocals of its diagonal
+cudaError_t cpals_cholesky(double* V, int R, int* info, double* dinv, cudaStream_t s);
+int cpals_cholesky_launches(int R);
+// X = M (L L^T)^{-1}; mirrors L into the strict upper triangle of its storage first
+cudaError_t cpals_solve(double* L, const double* dinv, int R, const float* M, int64_t I, double* X,
+                        cudaStream_t s);
 cudaError_t cpals_normalize(const double* X, int64_t I, int R, float* A, float* lam, cudaStream_t s);
 cudaError_t cpals_fit(const double* H, const float* lam, const float* M, const float* A, int64_t I, int R,
                       const double* norm_y2, const int* info, double* fit, cudaStream_t s);
