@@ -2430,8 +2430,7 @@ __global__ void __launch_bounds__(256) split_image_kernel(const float* __restric
     const int64_t n4 = n / 4;   // y, hi and lo are 16-byte aligned
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (int64_t i = t0; i < n4; i += stride) {
-        const float4 v = __ldcs(reinterpret_cast<const float4*>(y) + i);
+    auto split4 = [&](int64_t i, float4 v) {
         const float x0 = v.x * sy, x1 = v.y * sy, x2 = v.z * sy, x3 = v.w * sy;
         const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
         const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
@@ -2439,7 +2438,15 @@ __global__ void __launch_bounds__(256) split_image_kernel(const float* __restric
         const __half2 l23 = __floats2half2_rn(x2 - f23.x, x3 - f23.y);
         reinterpret_cast<uint2*>(hi)[i] = make_uint2(half2_bits(h01), half2_bits(h23));
         reinterpret_cast<uint2*>(lo)[i] = make_uint2(half2_bits(l01), half2_bits(l23));
+    };
+    int64_t i = t0;
+    for (; i + stride < n4; i += 2 * stride) {   // two 16-byte loads in flight
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(y) + i);
+        const float4 b = __ldcs(reinterpret_cast<const float4*>(y) + i + stride);
+        split4(i, a);
+        split4(i + stride, b);
     }
+    for (; i < n4; i += stride) split4(i, __ldcs(reinterpret_cast<const float4*>(y) + i));
     for (int64_t i = 4 * n4 + t0; i < n; i += stride) {
         const float x = y[i] * sy;
         const __half h = __float2half_rn(x);
@@ -2470,26 +2477,36 @@ __global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restr
     for (int64_t t = blockIdx.x; t < np * ni; t += gridDim.x) {
         const int64_t p0 = (t / ni) * TP, i0 = (t % ni) * TI;
         const int64_t ib = i0 + 4 * lane;   // this lane's first i
-#pragma unroll 2
-        for (int r = warp; r < TP; r += 8) {
-            const int64_t pr = p0 + r;
-            float v[4] = {0.f, 0.f, 0.f, 0.f};
+        // all eight rows' loads first (eight 16-byte loads in flight a thread)
+        float vv[TP / 8][4];
+#pragma unroll
+        for (int u = 0; u < TP / 8; ++u) {
+            const int64_t pr = p0 + warp + 8 * u;
             const int64_t e = pr * I + ib;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) vv[u][q] = 0.f;
             if (pr < P) {
                 if (VEC) {
                     if (ib < I) {
                         const float4 x = __ldcs(reinterpret_cast<const float4*>(y + e));
-                        v[0] = x.x;
-                        v[1] = x.y;
-                        v[2] = x.z;
-                        v[3] = x.w;
+                        vv[u][0] = x.x;
+                        vv[u][1] = x.y;
+                        vv[u][2] = x.z;
+                        vv[u][3] = x.w;
                     }
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        if (ib + q < I) v[q] = __ldcs(y + e + q);
+                        if (ib + q < I) vv[u][q] = __ldcs(y + e + q);
                 }
             }
+        }
+#pragma unroll
+        for (int u = 0; u < TP / 8; ++u) {
+            const int r = warp + 8 * u;
+            const int64_t pr = p0 + r;
+            const int64_t e = pr * I + ib;
+            const float* v = vv[u];
             uint32_t hb[4], lb[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -2632,19 +2649,21 @@ struct ColScaleArgs {
 };
 
 // one block per 32 columns: 8 row groups x 32 columns, reduced through shared memory
-__global__ void __launch_bounds__(256) colscale_kernel(ColScaleArgs a) {
-    __shared__ float red[8][33];
+__global__ void __launch_bounds__(1024) colscale_kernel(ColScaleArgs a) {
+    __shared__ float red[32][33];
     const int lc = threadIdx.x & 31, lr = threadIdx.x >> 5;
     const int64_t r = (int64_t)blockIdx.x * 32 + lc;
     float prod = 1.f;
     for (int t = 0; t < a.ngroup; ++t) {
         float m = 0.f;
-        if (r < a.R)
-            for (int64_t i = lr; i < a.gdim[t]; i += 8) m = fmaxf(m, fabsf(a.gfac[t][i * a.R + r]));
+        if (r < a.R) {
+#pragma unroll 4
+            for (int64_t i = lr; i < a.gdim[t]; i += 32) m = fmaxf(m, fabsf(a.gfac[t][i * a.R + r]));
+        }
         red[lr][lc] = m;
         __syncthreads();
         if (lr == 0) {
-            for (int q = 1; q < 8; ++q) m = fmaxf(m, red[q][lc]);
+            for (int q = 1; q < 32; ++q) m = fmaxf(m, red[q][lc]);
             prod *= m;
         }
         __syncthreads();
@@ -2660,17 +2679,16 @@ __global__ void __launch_bounds__(256) colscale_kernel(ColScaleArgs a) {
 template <int KW>
 __global__ void tc_bimage_f16_kernel(BImgArgs a, const float* __restrict__ colscale) {
     static_assert(KW == 32 || KW == 64, "64- or 128-byte rows");
-    constexpr uint32_t kRow = 2 * KW;              // bytes per row
-    const int64_t per_block = 2LL * a.BN * KW;    // fp16 elements (hi + lo)
+    constexpr uint32_t kRow = 2 * KW;                 // bytes per row
+    const int per_block = 2 * a.BN * KW;              // fp16 elements (hi + lo)
     const int64_t n = a.nblocks * per_block;
     __half* out = reinterpret_cast<__half*>(a.out);
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (int64_t)gridDim.x * blockDim.x) {
         const int64_t blk = e / per_block;
-        const int64_t w = e - blk * per_block;
-        const int half = (int)(w / (a.BN * KW));
-        const int64_t w2 = w - (int64_t)half * a.BN * KW;
-        const uint32_t byte = (uint32_t)(w2 * 2);
+        const uint32_t w = (uint32_t)(e - blk * per_block);
+        const uint32_t half = w / (uint32_t)(a.BN * KW);
+        const uint32_t byte = (w - half * (uint32_t)(a.BN * KW)) * 2u;
         const uint32_t row = byte / kRow;
         const uint32_t chunk_pos = (byte % kRow) / 16u;
         const uint32_t elem = (byte % 16u) / 2u;
@@ -2691,12 +2709,16 @@ __global__ void tc_bimage_f16_kernel(BImgArgs a, const float* __restrict__ colsc
         }
         float v = 0.f;
         if (valid && r < a.R) {
-            int64_t rem = j;
             v = colscale[r];
-            for (int m = a.ngroup - 1; m >= 0; --m) {
-                const int64_t idx = rem % a.gdim[m];
-                rem /= a.gdim[m];
-                v *= a.gfac[m][idx * a.R + r];
+            if (a.ngroup == 1) {
+                v *= a.gfac[0][j * a.R + r];   // the group's only mode: j is its index
+            } else {
+                int64_t rem = j;
+                for (int m = a.ngroup - 1; m >= 0; --m) {
+                    const int64_t idx = rem % a.gdim[m];
+                    rem /= a.gdim[m];
+                    v *= a.gfac[m][idx * a.R + r];
+                }
             }
         }
         const __half h = __float2half_rn(v);
@@ -3208,7 +3230,7 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
             }
             c.R = g.R;
             c.out = colscale;
-            colscale_kernel<<<(unsigned)cdiv64(g.R, 32), 256, 0, stream>>>(c);
+            colscale_kernel<<<(unsigned)cdiv64(g.R, 32), 1024, 0, stream>>>(c);
             e = cudaGetLastError();
         }
         if (e != cudaSuccess) {
