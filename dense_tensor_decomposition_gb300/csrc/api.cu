@@ -443,6 +443,7 @@ int mttkrp_set_workspace(mttkrp_plan_t h, void* dptr, size_t bytes) {
         return fail(MTTKRP_ERR_INVALID, "workspace must be 256-byte aligned");
     p->ws = dptr;
     p->ws_bytes = dptr ? bytes : 0;
+    p->sweep_left_images = 0;   // a new workspace holds none of the earlier results
     return MTTKRP_OK;
 }
 
@@ -456,6 +457,7 @@ int mttkrp(mttkrp_plan_t h, const float* Y, const float* const* factors, int mod
         return fail(MTTKRP_ERR_INVALID, "NULL tensor, factor array or output");
     p->ymax_ready = 0;
     p->img_ready = 0;
+    p->sweep_left_images = 0;
     return run_mode(*p, Y, factors, mode, out, static_cast<cudaStream_t>(stream));
 }
 
@@ -472,6 +474,7 @@ int mttkrp_all_modes(mttkrp_plan_t h, const float* Y, const float* const* factor
     }
     p->ymax_ready = 0;   // one max |Y| pass serves every mode of this call
     p->img_ready = 0;    // and one pass writing the fp16 images of Y
+    p->sweep_left_images = 0;
     for (int k = 0; k < p->d; ++k) {
         int rc = run_mode(*p, Y, factors, k, outs[k], static_cast<cudaStream_t>(stream));
         if (rc != MTTKRP_OK) return rc;
@@ -566,9 +569,13 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, 
         p->launches += cpals_gram_slabs(p->dims[n], R) > 1 ? 2 : 1;
     }
     if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "CP-ALS setup: %s", cudaGetErrorString(e));
-    // one max |Y| pass and one image pass serve every mode of the sweep
-    p->ymax_ready = 0;
-    p->img_ready = 0;
+    // one max |Y| pass and one image pass serve every mode of the sweep; a
+    // continuing sweep (have_norm: the same Y, no other call on the plan since
+    // the previous sweep) reuses the previous sweep's
+    const int reuse = have_norm && p->sweep_left_images;
+    p->ymax_ready = reuse;
+    p->img_ready = reuse;
+    p->sweep_left_images = 0;
     for (int n = 0; n < d; ++n) {
         if ((e = cpals_hadamard(G, d, n, R, V, s)) != cudaSuccess)
             return fail(MTTKRP_ERR_CUDA, "CP-ALS Hadamard: %s", cudaGetErrorString(e));
@@ -586,6 +593,7 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, 
         e = cpals_fit(V, lambda, M, factors[d - 1], p->dims[d - 1], R, norm_y2, info, fit, s);
     if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "CP-ALS fit: %s", cudaGetErrorString(e));
     p->launches += 2;
+    p->sweep_left_images = 1;
     return MTTKRP_OK;
 }
 

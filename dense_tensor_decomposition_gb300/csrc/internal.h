@@ -90,6 +90,9 @@ struct Plan {
     // fp16 images of Y (tc_img modes) already written for the current call's Y
     mutable int img_ready;
     int img_nat, img_t;   // which images the plan's tc_img modes read (natural, transposed)
+    // the last call on this plan was a CP-ALS sweep: max |Y| and the fp16 images
+    // in the workspace are those of that sweep's Y
+    int sweep_left_images;
     // benchmark timing: event pairs around the main kernel of each mode
     int timing;
     int ev_cap[kMaxD];

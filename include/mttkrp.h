@@ -194,13 +194,16 @@ int mttkrp_noalloc(int d, const int64_t* dims, int64_t R, const float* Y,
  *           are read and overwritten with the normalised updated factors.
  * lambda    device, R fp32: the column norms of the last update (output).
  * norm_y2   device, one double: ||Y||_F^2.  If have_norm is 0 the call
- *           computes it first and stores it there (pass 1 afterwards).
+ *           computes it first and stores it there.  have_norm = 1 states that
+ *           Y is unchanged since the previous sweep on this plan and that no
+ *           other call used the plan in between: the sweep then also reuses
+ *           the max |Y| and fp16 images of Y that the previous sweep left in
+ *           the plan's workspace.
  * fit       device, one double (output); NaN if V was not positive definite.
  * scratch   device scratch of mttkrp_cp_als_scratch_bytes(plan) bytes, 256-byte
  *           aligned, caller-owned.
  * Enqueues on `stream` and returns without synchronising.  Errors: as mttkrp,
- * plus MTTKRP_ERR_WORKSPACE for a short scratch.  The Cholesky runs in one
- * thread block: meant for the ranks CP-ALS is used at (up to a few hundred).
+ * plus MTTKRP_ERR_WORKSPACE for a short scratch.
  */
 size_t mttkrp_cp_als_scratch_bytes(mttkrp_plan_t plan);
 int mttkrp_cp_als_sweep(mttkrp_plan_t plan, const float* Y, float* const* factors, float* lambda,

@@ -91,3 +91,26 @@ def test_singular_normal_equations_report_nan_fit():
     _, fits = plan.cp_als(dev(Y), [dev(a) for a in A0], sweeps=1)
     assert np.isnan(float(fits[0]))
     assert mk.device_status() == 0
+
+
+def test_continuing_sweeps_reuse_images_without_changing_results():
+    """Sweeps after the first in one cp_als call reuse max |Y| and the fp16
+    images of Y (fp16-image modes); the results equal one-sweep calls that
+    recompute them."""
+    dims, R = (136, 130, 128), 128
+    Y, _ = synth.random_case(97, dims, R)
+    A0 = start(98, dims, R)
+    plan = mk.Plan(dims, R)
+    assert any("tc_fp16_image=1" in plan.describe(k) for k in range(3))
+    Yd = dev(Y)
+    Ad = [dev(a) for a in A0]
+    lam_a, fits_a = plan.cp_als(Yd, Ad, sweeps=3)
+    Bd = [dev(a) for a in A0]
+    fits_b = []
+    for _ in range(3):
+        lam_b, f = plan.cp_als(Yd, Bd, sweeps=1)
+        fits_b.append(float(f[0]))
+    for x, y in zip(Ad, Bd):
+        assert torch.equal(x, y)
+    assert torch.equal(lam_a, lam_b)
+    assert list(fits_a.cpu().numpy()) == fits_b
