@@ -1531,7 +1531,7 @@ constexpr int kChunkSteps2 = 4;   // 128 contraction indices between TMEM drains
 #define TC_IMG_XPOSE 1     // the innermost mode from transposed fp16 images
 #endif
 #ifndef TC_IMG_MIN_R
-#define TC_IMG_MIN_R 128
+#define TC_IMG_MIN_R 32
 #endif
 #ifndef TC_H2_EPI_LD
 #define TC_H2_EPI_LD 8   // TMEM columns per epilogue load (4 or 8)
@@ -3067,7 +3067,9 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
         t.tc_h2 = 0;
         t.tc_tmem = 0;
         t.tc_kw = kBK4;
-        t.bn = cdiv64(g.R, 256) * 256 * 20 <= cdiv64(g.R, 128) * 128 * 23 ? 256 : 128;
+        // 128 x 64 tiles for small R; else 256 or 128 columns, whichever wastes
+        // fewer (256 preferred within 15 %)
+        t.bn = g.R <= 64 ? 64 : (cdiv64(g.R, 256) * 256 * 20 <= cdiv64(g.R, 128) * 128 * 23 ? 256 : 128);
         MapGeom mgi;
         if (!mp.tc_inner) {
             if (cdiv64(g.Jq, kBK4) * kBK4 * 8 <= g.Jq * 9 && y_map_geom(t, p.dims, p.strides, p.d, mgi, 2)) mp = t;
@@ -3311,7 +3313,9 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
               (unsigned)mp.splits);
     cudaError_t e;
     if (mp.tc_img) {
-        e = mp.bn == 256 ? launch_img<256>(args, grid, stream) : launch_img<128>(args, grid, stream);
+        e = mp.bn == 256 ? launch_img<256>(args, grid, stream)
+          : mp.bn == 128 ? launch_img<128>(args, grid, stream)
+                         : launch_img<64>(args, grid, stream);
     } else if (mp.tc_h2) {
         e = mp.tc_inner ? launch_h2<true>(args, grid, stream) : launch_h2<false>(args, grid, stream);
     } else if (mp.tc_tmem) {
