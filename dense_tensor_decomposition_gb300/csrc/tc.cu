@@ -2109,7 +2109,7 @@ __device__ __forceinline__ void regs_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-template <int BN>
+template <int BN, bool SMALL = false>
 struct SmemImg {
     static constexpr uint32_t kA = kBM * 128;      // 16 KB: one image tile (128 rows x 64 fp16)
     static constexpr uint32_t kStage = 2 * kA;     // hi and lo tiles
@@ -2118,6 +2118,9 @@ struct SmemImg {
     static constexpr uint32_t kBarBytes = 256;
     static constexpr uint32_t kFree = 232448u - 1024u - kBarBytes - kBRes;
     static constexpr int kStages = kFree / kStage > 6 ? 6 : (int)(kFree / kStage);
+    // small I: the slot sums at the end go through a [128][BN + 4] fp32 buffer
+    // laid over the (then idle) B chunk and operand stages
+    static_assert(!SMALL || (uint32_t)(kBM * (BN + 4) * 4) <= kBRes + kStages * kStage, "slot-sum buffer");
     static constexpr uint32_t kOffA = kBRes;
     static constexpr uint32_t kOffBars = kOffA + kStages * kStage;
     static constexpr uint32_t kTotal = 1024 + kOffBars + kBarBytes;
@@ -2127,9 +2130,9 @@ struct SmemImg {
     static_assert((2 * kStages + 7) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
-template <int BN>
+template <int BN, bool SMALL>
 __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_constant__ TcArgs a) {
-    using L = SmemImg<BN>;
+    using L = SmemImg<BN, SMALL>;
     constexpr int NS = L::kStages;
     constexpr int CK = kImgCK;
     extern __shared__ uint8_t smem_raw[];
@@ -2188,6 +2191,16 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Work units: one pre index, or (small I) up to ps consecutive pre indices
+    // stacked in one 128-row tile (rows slot * I + i), never crossing a multiple
+    // of batch_len.
+    auto unit_next = [&](int64_t pi) -> int64_t {
+        if (!SMALL) return pi + 1;
+        int64_t e = pi + a.ps;
+        const int64_t row_end = (pi / a.batch_len + 1) * a.batch_len;
+        if (e > row_end) e = row_end;
+        return e < pre_hi ? e : pre_hi;
+    };
 
     if (warp < kImgEpiWarp0) {
         regs_dec<kImgRegsCtl>();
@@ -2222,7 +2235,11 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                 const int64_t swap_at = issued + NS;
                 bool b_pending = true;
                 int cP = cP0, cQ = cQ0;
-                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; pi = unit_next(pi)) {
+                    if (SMALL) {
+                        cP = (int)(pi / nQ);
+                        cQ = (int)(pi - (int64_t)cP * nQ);
+                    }
                     for (int q = 0; q < ck; ++q, ++issued, rr.next()) {
                         // box coordinates first: they do not depend on the slot, so
                         // the copy is issued as soon as the slot is released
@@ -2253,7 +2270,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                         tma_load(&a.ymap, a.rank, c, st, &full[rr.slot]);
                         tma_load(&a.ymap_lo, a.rank, c, st + L::kA, &full[rr.slot]);
                     }
-                    if (++cQ == nQ) {
+                    if (!SMALL && ++cQ == nQ) {
                         cQ = 0;
                         ++cP;
                     }
@@ -2284,7 +2301,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                     ok = false;
                     break;
                 }
-                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; pi = unit_next(pi)) {
                     uint32_t bw = b_w0;
                     for (int q = 0; q < ck; ++q, bw += kBStep, rr.next()) {
                         const bool first = q == 0;
@@ -2333,6 +2350,79 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
         regs_inc<kImgRegsEpi>();
         // ---------------------- epilogue (16 warps) ----------------------
         constexpr int kCols = BN / 4;
+        if constexpr (SMALL) {
+            // TMEM lane slot * I + i holds pre index pi_u + slot of the unit; each
+            // lane reads its own G row at every drain.  At the end the slots are
+            // summed through shared memory.
+            static_assert(kCols % TC_IMG_EPI_LD == 0, "TMEM load width");
+            const int quad = warp & 3;
+            const int part = (warp - kImgEpiWarp0) >> 2;
+            const int64_t c0 = r0 + part * kCols;
+            const int Iv = (int)a.I;
+            const int lg = 32 * quad + lane;
+            const int slot = lg / Iv;
+            float acc[kCols];
+#pragma unroll
+            for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
+            int zb = 0;
+            uint32_t zph = 0;
+            bool ok = true;
+            for (int jc = 0; jc < njc && ok; ++jc) {
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; pi = unit_next(pi)) {
+                    const int64_t pe = unit_next(pi);
+                    const bool live_row = slot < a.ps && pi + slot < pe;
+                    const float* grow = a.gtab + (pi + slot) * a.R + c0;
+                    if (!warp_wait_inl(&zfull[zb], (zph >> zb) & 1u, abort_flag, a.status, kStatusTimeoutEpi)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tbase =
+                        tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
+#pragma unroll
+                    for (int cc = 0; cc < kCols; cc += TC_IMG_EPI_LD) {
+                        float g[TC_IMG_EPI_LD];   // this row's G values for the group
+#pragma unroll
+                        for (int q = 0; q < TC_IMG_EPI_LD; ++q)
+                            g[q] = (live_row && c0 + cc + q < a.R) ? __ldg(grow + cc + q) : 0.f;
+                        uint32_t z[TC_IMG_EPI_LD];
+                        tmem_ld_cols<TC_IMG_EPI_LD>(tbase + cc, z);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < TC_IMG_EPI_LD; ++q)
+                            acc[cc + q] = fmaf(g[q], __uint_as_float(z[q]), acc[cc + q]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&zempty[zb]);
+                    zph ^= 1u << zb;
+                    zb ^= 1;
+                }
+            }
+            // sum the slots: rows slot * I + i of a [128][BN + 4] buffer over the
+            // (now idle) B chunk and operand stages
+            constexpr int kSP = BN + 4;
+            float* S = reinterpret_cast<float*>(smem);
+            const bool live = !*abort_flag;
+            if (live) {
+#pragma unroll
+                for (int e = 0; e < kCols; e += 4)
+                    *reinterpret_cast<float4*>(S + lg * kSP + part * kCols + e) =
+                        make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+            if (live) {
+                const float inv_y = pow2_recip(pow2_scale(*a.ymax_bits));
+                float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride;
+                for (int idx = tid - 32 * kImgEpiWarp0; idx < Iv * BN; idx += kEpiWarps * 32) {
+                    const int i = idx / BN, c = idx - i * BN;
+                    if (r0 + c >= a.R) continue;
+                    float sum = 0.f;
+                    for (int sl = 0; sl < a.ps; ++sl) sum += S[(sl * Iv + i) * kSP + c];
+                    dst[(int64_t)i * a.R + r0 + c] = sum * inv_y * pow2_recip(a.colscale[r0 + c]);
+                }
+            }
+        } else {
         constexpr int kGv = (kCols + 31) / 32;   // G values a lane holds
         static_assert(kCols % TC_IMG_EPI_LD == 0, "TMEM load width");
         const int quad = warp & 3;
@@ -2410,6 +2500,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                 asm volatile("" ::: "memory");   // keep one group of column scales in flight
             }
         }
+        }   // not SMALL
     }
 
     tc_fence_before();
@@ -2473,6 +2564,71 @@ __global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restr
     const float sy = pow2_scale(*ymax_bits);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    if (I < TI / 2) {
+        // short rows: TP consecutive p are one contiguous block of TP * I values,
+        // read (and written in the natural layout) flat, so that no lanes idle
+        const int Ii = (int)I;
+        const int64_t np = (P + TP - 1) / TP;
+        for (int64_t t = blockIdx.x; t < np; t += gridDim.x) {
+            const int64_t p0 = t * TP;
+            const int rows = (int)(P - p0 < TP ? P - p0 : TP);
+            const int nvals = rows * Ii;
+            const int64_t base = p0 * I;
+            for (int f = threadIdx.x; 4 * f < nvals; f += blockDim.x) {
+                float v[4] = {0.f, 0.f, 0.f, 0.f};
+                if (4 * f + 3 < nvals) {
+                    const float4 x = __ldcs(reinterpret_cast<const float4*>(y + base) + f);
+                    v[0] = x.x;
+                    v[1] = x.y;
+                    v[2] = x.z;
+                    v[3] = x.w;
+                } else {
+                    for (int q = 0; q < 4; ++q)
+                        if (4 * f + q < nvals) v[q] = __ldcs(y + base + 4 * f + q);
+                }
+                uint32_t hb[4], lb[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int idx = 4 * f + q;
+                    const float x = v[q] * sy;
+                    const __half h = __float2half_rn(x);
+                    const __half l = __float2half_rn(x - __half2float(h));
+                    hb[q] = __half_as_ushort(h);
+                    lb[q] = __half_as_ushort(l);
+                    if (idx < nvals) sh[idx % Ii][idx / Ii] = hb[q] | (lb[q] << 16);
+                }
+                if (write_nat) {
+                    if (4 * f + 3 < nvals) {
+                        reinterpret_cast<uint2*>(hi + base)[f] = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
+                        reinterpret_cast<uint2*>(lo + base)[f] = make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
+                    } else {
+                        for (int q = 0; q < 4; ++q)
+                            if (4 * f + q < nvals) {
+                                hi[base + 4 * f + q] = __ushort_as_half((unsigned short)hb[q]);
+                                lo[base + 4 * f + q] = __ushort_as_half((unsigned short)lb[q]);
+                            }
+                    }
+                }
+            }
+            __syncthreads();
+            for (int c = warp; c < Ii; c += 8) {
+                const int64_t pc = p0 + 2 * lane;
+                if (2 * lane < rows) {
+                    const uint32_t w0 = sh[c][2 * lane], w1 = sh[c][2 * lane + 1];
+                    const int64_t e = (int64_t)c * P + pc;
+                    if (2 * lane + 1 < rows) {
+                        *reinterpret_cast<uint32_t*>(thi + e) = __byte_perm(w0, w1, 0x5410);
+                        *reinterpret_cast<uint32_t*>(tlo + e) = __byte_perm(w0, w1, 0x7632);
+                    } else {
+                        thi[e] = __ushort_as_half((unsigned short)(w0 & 0xFFFFu));
+                        tlo[e] = __ushort_as_half((unsigned short)(w0 >> 16));
+                    }
+                }
+            }
+            __syncthreads();
+        }
+        return;
+    }
     const int64_t np = (P + TP - 1) / TP, ni = (I + TI - 1) / TI;
     for (int64_t t = blockIdx.x; t < np * ni; t += gridDim.x) {
         const int64_t p0 = (t / ni) * TP, i0 = (t % ni) * TI;
@@ -2893,6 +3049,12 @@ bool timg_map_geom(const ModePlan& mp, MapGeom& mg) {
     mg.box[0] = (uint32_t)kBK4;
     mg.box[1] = kBM;
     mg.box[2] = 1;
+    if (mp.tc_small) {
+        // ps consecutive pre indices, all I_k rows: tile rows slot * I_k + i
+        if (mp.tc_ps < 2 || mp.tc_ps > 256) return false;
+        mg.box[1] = (uint32_t)g.I;
+        mg.box[2] = (uint32_t)mp.tc_ps;
+    }
     return true;
 }
 
@@ -2946,7 +3108,7 @@ cudaError_t launch_h2(const TcArgs& args, dim3 grid, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int BN>
+template <int BN, bool SMALL = false>
 cudaError_t launch_img(const TcArgs& args, dim3 grid, cudaStream_t s) {
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -2957,15 +3119,15 @@ cudaError_t launch_img(const TcArgs& args, dim3 grid, cudaStream_t s) {
         // setmaxnreg.inc waits until the pool allotted at launch can serve it:
         // refuse a build whose launch allotment is below what the split assumes
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, tc_img_kernel<BN>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, tc_img_kernel<BN, SMALL>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs < kImgRegsLaunch || fa.numRegs * kImgThreads > 65536) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(tc_img_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SmemImg<BN>::kTotal);
+        e = cudaFuncSetAttribute(tc_img_kernel<BN, SMALL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SmemImg<BN, SMALL>::kTotal);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    tc_img_kernel<BN><<<grid, kImgThreads, SmemImg<BN>::kTotal, s>>>(args);
+    tc_img_kernel<BN, SMALL><<<grid, kImgThreads, SmemImg<BN, SMALL>::kTotal, s>>>(args);
     return cudaGetLastError();
 }
 
@@ -3061,7 +3223,7 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
     // length must not be padded to K-steps by much
     mp.tc_img = 0;
     mp.tc_img_t = 0;
-    if (TC_IMG && !mp.tc_small && g.R >= TC_IMG_MIN_R) {
+    if (TC_IMG && g.R >= TC_IMG_MIN_R) {
         ModePlan t = mp;
         t.tc_img = 1;
         t.tc_h2 = 0;
@@ -3070,6 +3232,7 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
         // 128 x 64 tiles for small R; else 256 or 128 columns, whichever wastes
         // fewer (256 preferred within 15 %)
         t.bn = g.R <= 64 ? 64 : (cdiv64(g.R, 256) * 256 * 20 <= cdiv64(g.R, 128) * 128 * 23 ? 256 : 128);
+        if (mp.tc_small && t.bn > 128) t.bn = 128;   // per-row G loads: 128-column tiles at most
         MapGeom mgi;
         if (!mp.tc_inner) {
             if (cdiv64(g.Jq, kBK4) * kBK4 * 8 <= g.Jq * 9 && y_map_geom(t, p.dims, p.strides, p.d, mgi, 2)) mp = t;
@@ -3205,6 +3368,8 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
                 const int64_t P = numel / In;
                 int64_t blocks = cdiv64(P, 64) * cdiv64(In, 128);
                 if (blocks > 152 * 16) blocks = 152 * 16;
+                // (I_{d-1} < 64: whole rows per tile, read flat; the 16-byte
+                // alignment of every tile start holds because tiles are 64 rows)
                 if (In % 4 == 0)
                     split_image_t_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(Y, P, In, ymax, img_hi, img_lo,
                                                                                      timg_hi, timg_lo, p.img_nat);
@@ -3293,7 +3458,8 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     args.jq_steps = mp.tc_jq_steps;
     args.ps = mp.tc_small ? mp.tc_ps : 1;
     args.batch_len = nQ > 1 ? nQ : g.npre;
-    args.y_box_bytes = mp.tc_img ? (uint32_t)kBK4 * 2u * (uint32_t)kBM   // one fp16 image tile
+    args.y_box_bytes = mp.tc_img ? (uint32_t)kBK4 * 2u *   // one fp16 image tile
+                                       (mp.tc_small ? (uint32_t)(g.I * mp.tc_ps) : (uint32_t)kBM)
                                  : (uint32_t)mp.tc_kw * 4u * (mp.tc_small ? (uint32_t)(g.I * mp.tc_ps) : (uint32_t)kBM);
     args.ymax_bits = ymax;
     args.colscale = colscale;
@@ -3313,9 +3479,12 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
               (unsigned)mp.splits);
     cudaError_t e;
     if (mp.tc_img) {
-        e = mp.bn == 256 ? launch_img<256>(args, grid, stream)
-          : mp.bn == 128 ? launch_img<128>(args, grid, stream)
-                         : launch_img<64>(args, grid, stream);
+        if (mp.tc_small)
+            e = mp.bn == 128 ? launch_img<128, true>(args, grid, stream) : launch_img<64, true>(args, grid, stream);
+        else
+            e = mp.bn == 256 ? launch_img<256>(args, grid, stream)
+              : mp.bn == 128 ? launch_img<128>(args, grid, stream)
+                             : launch_img<64>(args, grid, stream);
     } else if (mp.tc_h2) {
         e = mp.tc_inner ? launch_h2<true>(args, grid, stream) : launch_h2<false>(args, grid, stream);
     } else if (mp.tc_tmem) {
