@@ -3223,7 +3223,12 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
     // length must not be padded to K-steps by much
     mp.tc_img = 0;
     mp.tc_img_t = 0;
-    if (TC_IMG && g.R >= TC_IMG_MIN_R) {
+    // the images take 4 bytes an element per layout (natural, transposed); above
+    // 12 Gi elements (48 GiB of Y) they would crowd the tensor out of HBM, and
+    // the kernels that convert Y per CTA take over
+    int64_t numel = 1;
+    for (int t = 0; t < p.d; ++t) numel *= p.dims[t];
+    if (TC_IMG && g.R >= TC_IMG_MIN_R && numel <= ((int64_t)12 << 30)) {
         ModePlan t = mp;
         t.tc_img = 1;
         t.tc_h2 = 0;
