@@ -20,7 +20,7 @@ import threading
 
 from ._build import LIB as LIB_PATH, build  # noqa: F401
 
-__all__ = ["Plan", "mttkrp", "all_modes", "MttkrpError", "build", "load_library",
+__all__ = ["Plan", "mttkrp", "all_modes", "apply_rotations", "MttkrpError", "build", "load_library",
            "exported_symbols", "PATH_AUTO", "PATH_SIMT", "PATH_TC"]
 
 PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
@@ -79,6 +79,8 @@ def load_library():
         lib.mttkrp_last_error.restype = ctypes.c_char_p
         lib.mttkrp_version.argtypes = []
         lib.mttkrp_version.restype = ci
+        lib.mttkrp_apply_rotations.argtypes = [ci, vp, vp, ci, vp, vp, vp, ci, vp]
+        lib.mttkrp_apply_rotations.restype = ci
         lib.mttkrp_cp_als_scratch_bytes.argtypes = [vp]
         lib.mttkrp_cp_als_scratch_bytes.restype = sz
         lib.mttkrp_cp_als_sweep.argtypes = [vp, vp, vp, vp, vp, ci, vp, vp, sz, vp]
@@ -369,6 +371,26 @@ def mttkrp(Y, factors, mode: int, path="auto"):
 def all_modes(Y, factors, path="auto"):
     plan = Plan(tuple(Y.shape), factors[0].shape[1], path)
     return plan.all_modes(Y, factors)
+
+
+def apply_rotations(Y, mode: int, pairs, c, s, stream=None):
+    """In place: Y x_mode R^T for disjoint Givens pairs (mttkrp_apply_rotations).
+    pairs: int32 CUDA tensor (G, 2); c, s: float32 CUDA tensors (G,)."""
+    import torch
+    lib = load_library()
+    if not isinstance(Y, torch.Tensor) or not Y.is_cuda or Y.dtype != torch.float32 or not Y.is_contiguous():
+        raise TypeError("Y must be a contiguous float32 CUDA tensor")
+    G = int(pairs.shape[0]) if pairs is not None else 0
+    for t, dt in ((pairs, torch.int32), (c, torch.float32), (s, torch.float32)):
+        if t is not None and (not t.is_cuda or t.dtype != dt or not t.is_contiguous() or t.device != Y.device):
+            raise TypeError("pairs (int32), c and s (float32) must be contiguous CUDA tensors on Y's device")
+    if pairs is not None and tuple(pairs.shape) != (G, 2) or (G and (c.numel() != G or s.numel() != G)):
+        raise ValueError("pairs must be (G, 2), c and s (G,)")
+    dims = (ctypes.c_int64 * Y.dim())(*Y.shape)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() else None
+    _check(lib.mttkrp_apply_rotations(Y.dim(), dims, ctypes.c_void_p(Y.data_ptr()), mode, ptr(pairs), ptr(c),
+                                      ptr(s), G, _stream_handle(Y.device, stream)), "mttkrp_apply_rotations")
+    return Y
 
 
 def device_status() -> int:

@@ -521,6 +521,34 @@ CpAlsLayout cp_als_layout(const Plan& p) {
 }
 }  // namespace
 
+int mttkrp_apply_rotations(int d, const int64_t* dims, float* Y, int mode, const int32_t* pairs, const float* c,
+                           const float* s, int group_size, void* stream) {
+    g_errmsg[0] = 0;
+    if (d < 2 || d > kMaxD) return fail(MTTKRP_ERR_INVALID, "order d=%d outside [2, %d]", d, kMaxD);
+    if (dims == nullptr || Y == nullptr) return fail(MTTKRP_ERR_INVALID, "NULL dims or tensor");
+    if (mode < 0 || mode >= d) return fail(MTTKRP_ERR_INVALID, "mode %d outside [0, %d)", mode, d);
+    int64_t P = 1, Q = 1, numel = 1;
+    for (int n = 0; n < d; ++n) {
+        if (dims[n] < 1) return fail(MTTKRP_ERR_INVALID, "dims[%d]=%lld < 1", n, (long long)dims[n]);
+        if (dims[n] > kMaxNumel || numel > kMaxNumel / dims[n])
+            return fail(MTTKRP_ERR_INVALID, "tensor has more than 2^40 elements");
+        numel *= dims[n];
+        if (n < mode) P *= dims[n];
+        if (n > mode) Q *= dims[n];
+    }
+    const int64_t N = dims[mode];
+    if (N > INT32_MAX) return fail(MTTKRP_ERR_INVALID, "mode size %lld too large", (long long)N);
+    if (group_size < 0 || 2 * (int64_t)group_size > N)
+        return fail(MTTKRP_ERR_INVALID, "group of %d disjoint pairs does not fit mode size %lld", group_size,
+                    (long long)N);
+    if (group_size > 0 && (pairs == nullptr || c == nullptr || s == nullptr))
+        return fail(MTTKRP_ERR_INVALID, "NULL pairs, cosines or sines");
+    if ((reinterpret_cast<uintptr_t>(Y) & 3) != 0) return fail(MTTKRP_ERR_INVALID, "Y must be 4-byte aligned");
+    cudaError_t e = launch_rotations(Y, P, (int)N, Q, pairs, c, s, group_size, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "rotation launch: %s", cudaGetErrorString(e));
+    return MTTKRP_OK;
+}
+
 size_t mttkrp_cp_als_scratch_bytes(mttkrp_plan_t h) {
     Plan* p = as_plan(h);
     return p == nullptr ? 0 : cp_als_layout(*p).total;

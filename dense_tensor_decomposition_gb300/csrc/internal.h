@@ -130,6 +130,10 @@ enum { kLoadScalar = 0, kLoadVecJ = 1, kLoadVecI = 2 };
 
 cudaError_t launch_prod_table(const ProdTableArgs& a, cudaStream_t s);
 
+// Givens rotations along one mode (rotations.cu); Y viewed as [P, N, Q]
+cudaError_t launch_rotations(float* Y, int64_t P, int N, int64_t Q, const int* pairs, const float* c, const float* s,
+                             int G, cudaStream_t stream);
+
 // CP-ALS pieces (cpals.cu)
 int cpals_gram_slabs(int64_t I, int R);   // partial Grams cpals_gram keeps (R x R fp64 each)
 cudaError_t cpals_gram(const float* A, int64_t I, int R, double* G, double* part, cudaStream_t s);

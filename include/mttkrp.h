@@ -210,6 +210,30 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t plan, const float* Y, float* const* factor
                         double* norm_y2, int have_norm, double* fit, void* scratch, size_t scratch_bytes,
                         void* stream);
 
+/*
+ * Givens rotations along one mode ("Parallel Jacobi-type tensor
+ * diagonalization on GPUs", §2 and §4.3, "Application of Rotations"): Y is
+ * multiplied in place in mode `mode` by R^T, where R is the identity except
+ * for the 2 x 2 blocks [[c_g, -s_g], [s_g, c_g]] at rows and columns
+ * (p_g, q_g) of a group of disjoint pivot pairs; for every fibre along the
+ * mode,
+ *     new[p_g] = c_g * old[p_g] + s_g * old[q_g],
+ *     new[q_g] = c_g * old[q_g] - s_g * old[p_g],
+ * and entries whose mode index is in no pair are not touched.
+ *
+ * d, dims   the tensor's order and shape (as for mttkrp_plan); Y is C-order
+ *           fp32 device memory, 4-byte aligned (16-byte for vector access).
+ * pairs     device, 2 * group_size int32: p_0, q_0, p_1, q_1, ...; the pairs
+ *           must be disjoint (overlapping pairs race; indices out of range or
+ *           p == q are skipped).
+ * c, s      device, group_size fp32 each: cosine and sine of each rotation.
+ * fp32 arithmetic (one fused multiply-add per output).  Enqueues on `stream`.
+ * Errors: MTTKRP_ERR_INVALID for bad shapes, a mode out of range, a group
+ * larger than half the mode size or NULL pointers; MTTKRP_ERR_CUDA.
+ */
+int mttkrp_apply_rotations(int d, const int64_t* dims, float* Y, int mode, const int32_t* pairs, const float* c,
+                           const float* s, int group_size, void* stream);
+
 /* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
 int mttkrp_version(void);
 
