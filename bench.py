@@ -60,6 +60,9 @@ def parse_args():
     ap.add_argument("--cp-als", type=int, default=0, metavar="SWEEPS",
                     help="instead: time SWEEPS CP-ALS sweeps (mttkrp_cp_als_sweep) on the workload's tensor")
     ap.add_argument("--cp-rank", type=int, default=32, help="rank of the CP-ALS model (--cp-als)")
+    ap.add_argument("--ttm", type=int, default=-1, metavar="J",
+                    help="instead: time the dense mode-n product X x_k M_k along every mode with J x I_k "
+                         "matrices (J = 0: square, J = I_k)")
     ap.add_argument("--rotations", action="store_true",
                     help="instead: time Givens rotations (a full group of disjoint pairs) along every mode")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -537,6 +540,70 @@ def run_rotations(args, w):
     }))
 
 
+def run_ttm(args, w):
+    """The dense mode-n product along every mode of the workload's tensor per
+    step (mttkrp_ttm), each mode into its own preallocated result.  One JSON
+    line: TFLOP/s (2 J I_1..I_d flops per mode) against the fp32 FMA pipe, with
+    the HBM time of the algorithmic bytes beside it."""
+    import numpy as np
+    import torch
+    import dense_tensor_decomposition_gb300 as mk
+    device = torch.device("cuda", 0)
+    X = torch.from_numpy(synth.make_tensor(w)).to(device)
+    rng = np.random.default_rng(20261203)
+    numel = int(np.prod(w.dims))
+    Js = [n if args.ttm == 0 else args.ttm for n in w.dims]
+    Ms = [torch.from_numpy(rng.standard_normal((J, n)).astype(np.float32)).to(device) for J, n in zip(Js, w.dims)]
+    outs = [torch.empty(list(w.dims[:k]) + [Js[k]] + list(w.dims[k + 1:]), device=device) for k in range(w.d)]
+
+    def step():
+        for k in range(w.d):
+            mk.ttm(X, k, Ms[k], out=outs[k])
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    stream = torch.cuda.current_stream(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / args.steps
+    per_mode = []
+    for k in range(w.d):
+        e0.record(stream)
+        for _ in range(args.steps):
+            mk.ttm(X, k, Ms[k], out=outs[k])
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        per_mode.append(round(e0.elapsed_time(e1) / args.steps, 4))
+    flops = sum(2.0 * J * numel for J in Js)
+    moved = sum(4.0 * (numel + J * numel // n + J * n) for J, n in zip(Js, w.dims))
+    tflops = flops / (ms * 1e-3) / 1e12
+    peaks, src = measured_peaks()
+    props = torch.cuda.get_device_properties(device)
+    sm_mhz = peaks.get("sm_max_mhz", SM_MAX_MHZ_FALLBACK)
+    alu_peak = props.multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
+    print(json.dumps({
+        "metric": "dense mode-n product along every mode: TFLOP/s (2 J prod(I_n) per mode)",
+        "value": round(tflops, 3), "unit": "TFLOP/s", "higher_is_better": True, "n_gpus": 1,
+        "steps": args.steps, "ms_per_step": round(ms, 4), "dtype": "f32", "data": "synthetic", "impl": "ours",
+        "config": {"workload": w.name, "dims": list(w.dims), "J": Js,
+                   "l2": "tensor larger than L2" if 4 * numel > 129e6 else "fits L2"},
+        "roofline": {"bound": "alu", "achieved": round(tflops, 3), "peak": round(alu_peak, 3), "unit": "TFLOP/s",
+                     "frac": round(tflops / alu_peak, 4),
+                     "peak_source": f"fp32 FMA pipe: {props.multi_processor_count} SMs x 128 lanes x 2 flops x "
+                                    f"{sm_mhz:.0f} MHz (max SM clock)",
+                     "hbm_ms_at_algorithmic_bytes": round(moved / (peaks["hbm_gbs"] * 1e9) * 1e3, 4),
+                     "hbm_peak_source": src},
+        "ms_per_mode": per_mode,
+        "kernel_src": kernel_source_hash(),
+    }))
+
+
 def main():
     args = parse_args()
     w = workload_from_arg(args.workload)
@@ -544,6 +611,8 @@ def main():
         run_reference(args, w)
     elif args.rotations:
         run_rotations(args, w)
+    elif args.ttm >= 0:
+        run_ttm(args, w)
     elif args.cp_als > 0:
         run_cp_als(args, w)
     else:

@@ -20,7 +20,7 @@ import threading
 
 from ._build import LIB as LIB_PATH, build  # noqa: F401
 
-__all__ = ["Plan", "mttkrp", "all_modes", "apply_rotations", "MttkrpError", "build", "load_library",
+__all__ = ["Plan", "mttkrp", "all_modes", "apply_rotations", "ttm", "MttkrpError", "build", "load_library",
            "exported_symbols", "PATH_AUTO", "PATH_SIMT", "PATH_TC"]
 
 PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
@@ -81,6 +81,8 @@ def load_library():
         lib.mttkrp_version.restype = ci
         lib.mttkrp_apply_rotations.argtypes = [ci, vp, vp, ci, vp, vp, vp, ci, vp]
         lib.mttkrp_apply_rotations.restype = ci
+        lib.mttkrp_ttm.argtypes = [ci, vp, vp, ci, vp, i64, vp, vp]
+        lib.mttkrp_ttm.restype = ci
         lib.mttkrp_cp_als_scratch_bytes.argtypes = [vp]
         lib.mttkrp_cp_als_scratch_bytes.restype = sz
         lib.mttkrp_cp_als_sweep.argtypes = [vp, vp, vp, vp, vp, ci, vp, vp, sz, vp]
@@ -391,6 +393,31 @@ def apply_rotations(Y, mode: int, pairs, c, s, stream=None):
     _check(lib.mttkrp_apply_rotations(Y.dim(), dims, ctypes.c_void_p(Y.data_ptr()), mode, ptr(pairs), ptr(c),
                                       ptr(s), G, _stream_handle(Y.device, stream)), "mttkrp_apply_rotations")
     return Y
+
+
+def ttm(X, mode: int, M, out=None, stream=None):
+    """T = X x_mode M (mttkrp_ttm): M is a float32 CUDA matrix J x X.shape[mode];
+    returns T (X's shape with that mode's size replaced by J), written into
+    `out` when given (contiguous float32, not overlapping X or M)."""
+    import torch
+    lib = load_library()
+    for name, t in (("X", X), ("M", M)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous float32 CUDA tensor")
+    if M.device != X.device or M.dim() != 2 or not 0 <= mode < X.dim() or M.shape[1] != X.shape[mode]:
+        raise ValueError("M must be J x X.shape[mode] on X's device")
+    shape = list(X.shape)
+    shape[mode] = int(M.shape[0])
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float32, device=X.device)
+    elif (not isinstance(out, torch.Tensor) or out.device != X.device or out.dtype != torch.float32
+          or not out.is_contiguous() or list(out.shape) != shape):
+        raise ValueError(f"out must be a contiguous float32 CUDA tensor of shape {shape}")
+    dims = (ctypes.c_int64 * X.dim())(*X.shape)
+    _check(lib.mttkrp_ttm(X.dim(), dims, ctypes.c_void_p(X.data_ptr()), mode, ctypes.c_void_p(M.data_ptr()),
+                          int(M.shape[0]), ctypes.c_void_p(out.data_ptr()), _stream_handle(X.device, stream)),
+           "mttkrp_ttm")
+    return out
 
 
 def device_status() -> int:

@@ -549,6 +549,39 @@ int mttkrp_apply_rotations(int d, const int64_t* dims, float* Y, int mode, const
     return MTTKRP_OK;
 }
 
+int mttkrp_ttm(int d, const int64_t* dims, const float* X, int mode, const float* M, int64_t J, float* T,
+               void* stream) {
+    g_errmsg[0] = 0;
+    if (d < 1 || d > kMaxD) return fail(MTTKRP_ERR_INVALID, "order d=%d outside [1, %d]", d, kMaxD);
+    if (dims == nullptr || X == nullptr || M == nullptr || T == nullptr)
+        return fail(MTTKRP_ERR_INVALID, "NULL dims, tensor, matrix or result");
+    if (mode < 0 || mode >= d) return fail(MTTKRP_ERR_INVALID, "mode %d outside [0, %d)", mode, d);
+    if (J < 1 || J > ((int64_t)1 << 24))
+        return fail(MTTKRP_ERR_INVALID, "J=%lld outside [1, 2^24]", (long long)J);
+    int64_t P = 1, Q = 1, numel = 1;
+    for (int n = 0; n < d; ++n) {
+        if (dims[n] < 1) return fail(MTTKRP_ERR_INVALID, "dims[%d]=%lld < 1", n, (long long)dims[n]);
+        if (dims[n] > kMaxNumel || numel > kMaxNumel / dims[n])
+            return fail(MTTKRP_ERR_INVALID, "tensor has more than 2^40 elements");
+        numel *= dims[n];
+        if (n < mode) P *= dims[n];
+        if (n > mode) Q *= dims[n];
+    }
+    const int64_t N = dims[mode];
+    if (P * Q > kMaxNumel / J) return fail(MTTKRP_ERR_INVALID, "result has more than 2^40 elements");
+    if (ttm_tiles(P, Q, J) > INT32_MAX) return fail(MTTKRP_ERR_INVALID, "too many result tiles");
+    if (((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(M) | reinterpret_cast<uintptr_t>(T)) & 3) != 0)
+        return fail(MTTKRP_ERR_INVALID, "X, M and T must be 4-byte aligned");
+    const uintptr_t x0 = reinterpret_cast<uintptr_t>(X), x1 = x0 + (uintptr_t)numel * 4;
+    const uintptr_t t0 = reinterpret_cast<uintptr_t>(T), t1 = t0 + (uintptr_t)(P * J * Q) * 4;
+    const uintptr_t m0 = reinterpret_cast<uintptr_t>(M), m1 = m0 + (uintptr_t)(J * N) * 4;
+    if ((t0 < x1 && x0 < t1) || (t0 < m1 && m0 < t1))
+        return fail(MTTKRP_ERR_INVALID, "the result overlaps X or M");
+    cudaError_t e = launch_ttm(X, M, T, P, N, Q, J, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "mode-n product launch: %s", cudaGetErrorString(e));
+    return MTTKRP_OK;
+}
+
 size_t mttkrp_cp_als_scratch_bytes(mttkrp_plan_t h) {
     Plan* p = as_plan(h);
     return p == nullptr ? 0 : cp_als_layout(*p).total;

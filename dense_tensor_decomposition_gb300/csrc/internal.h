@@ -134,6 +134,12 @@ cudaError_t launch_prod_table(const ProdTableArgs& a, cudaStream_t s);
 cudaError_t launch_rotations(float* Y, int64_t P, int N, int64_t Q, const int* pairs, const float* c, const float* s,
                              int G, cudaStream_t stream);
 
+// dense mode-n product T = X x_n M (ttm.cu); X [P, N, Q], M [J, N], T [P, J, Q]
+int ttm_row_tile(int64_t J);
+int64_t ttm_tiles(int64_t P, int64_t Q, int64_t J);
+cudaError_t launch_ttm(const float* X, const float* M, float* T, int64_t P, int64_t N, int64_t Q, int64_t J,
+                       cudaStream_t s);
+
 // CP-ALS pieces (cpals.cu)
 int cpals_gram_slabs(int64_t I, int R);   // partial Grams cpals_gram keeps (R x R fp64 each)
 cudaError_t cpals_gram(const float* A, int64_t I, int R, double* G, double* part, cudaStream_t s);

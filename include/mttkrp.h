@@ -234,6 +234,30 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t plan, const float* Y, float* const* factor
 int mttkrp_apply_rotations(int d, const int64_t* dims, float* Y, int mode, const int32_t* pairs, const float* c,
                            const float* s, int group_size, void* stream);
 
+/*
+ * Dense mode-n product, TTM ("Parallel Jacobi-type tensor diagonalization on
+ * GPUs", §2, eq. (1)): T = X x_mode M for a matrix M of size J x I_mode,
+ *     T[i_0 .. i_{mode-1}, j, i_{mode+1} .. i_{d-1}]
+ *         = sum over i of X[i_0 .. i_{mode-1}, i, i_{mode+1} .. i_{d-1}] * M[j, i].
+ *
+ * d, dims   X's order (1 <= d <= 8) and shape; X is C-order fp32 device memory.
+ * M         device, J x dims[mode] fp32, row-major.
+ * J         rows of M, 1 <= J <= 2^24; T has the shape of X with dims[mode]
+ *           replaced by J (at most 2^40 elements, and at most 2^31 - 1 result
+ *           tiles of 128 columns (p, q) x 32, 64 or 128 rows j).
+ * T         device, caller-owned result buffer, C-order; must not overlap X or
+ *           M.  Every element is written.
+ * All pointers 4-byte aligned (16-byte alignment enables vector access).
+ * fp32 products with fp32 accumulation over i in index order (fused
+ * multiply-adds); the result does not depend on the launch configuration.
+ * Enqueues on `stream` and returns without synchronising.
+ * Errors: MTTKRP_ERR_INVALID for bad shapes, a mode out of range, J out of
+ * range, NULL or misaligned pointers, or a result overlapping X or M;
+ * MTTKRP_ERR_CUDA.
+ */
+int mttkrp_ttm(int d, const int64_t* dims, const float* X, int mode, const float* M, int64_t J, float* T,
+               void* stream);
+
 /* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
 int mttkrp_version(void);
 

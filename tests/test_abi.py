@@ -163,3 +163,34 @@ def test_image_kernel_planning_and_workspace():
     big = mk.Plan((4096, 4096, 1024), 256)
     assert image_flags(big, 3) == [0, 0, 0]
     assert big.workspace_bytes(-1) < 4096 * 4096 * 1024        # no image region
+
+
+def _fake(addr):
+    return ctypes.c_void_p(addr)
+
+
+@pytest.mark.parametrize("d,dims,mode,J,x,m,t,why", [
+    (0, (4,), 0, 2, 0x1000, 0x2000, 0x3000, "order"),
+    (9, (2,) * 9, 0, 2, 0x1000, 0x2000, 0x3000, "order"),
+    (3, (4, 5, 6), 3, 2, 0x1000, 0x2000, 0x3000, "mode"),
+    (3, (4, 5, 6), 1, 0, 0x1000, 0x2000, 0x3000, "J"),
+    (3, (4, 0, 6), 1, 2, 0x1000, 0x2000, 0x3000, "dims"),
+    (3, (4, 5, 6), 1, 2, 0, 0x2000, 0x3000, "NULL"),
+    (3, (4, 5, 6), 1, 2, 0x1000, 0x2000, 0x1002, "aligned"),
+    (3, (4, 5, 6), 1, 5, 0x1000, 0x100000, 0x1000 + 4 * 119, "overlap"),     # T's start inside X
+    (3, (4, 5, 6), 1, 2, 0x100000, 0x1000, 0x1000 + 4 * 9, "overlap"),       # T's start inside M
+])
+def test_ttm_rejects_invalid_before_any_launch(lib, d, dims, mode, J, x, m, t, why):
+    arr = (ctypes.c_int64 * len(dims))(*dims)
+    assert lib.mttkrp_ttm(d, arr, _fake(x), mode, _fake(m), J, _fake(t), None) == 1
+    assert why.lower() in lib.mttkrp_last_error().decode().lower()
+
+
+@pytest.mark.parametrize("d,dims,mode,G,why", [
+    (1, (4,), 0, 1, "order"), (3, (4, 5, 6), 3, 1, "mode"), (3, (4, 5, 6), 1, 3, "fit"),
+    (3, (4, -5, 6), 1, 1, "dims")])
+def test_rotations_reject_invalid_before_any_launch(lib, d, dims, mode, G, why):
+    arr = (ctypes.c_int64 * len(dims))(*dims)
+    f = _fake(0x1000)
+    assert lib.mttkrp_apply_rotations(d, arr, f, mode, f, f, f, G, None) == 1
+    assert why.lower() in lib.mttkrp_last_error().decode().lower()

@@ -1,0 +1,114 @@
+"""GPU dense mode-n product (mttkrp_ttm through the C ABI) against the fp64
+oracle on the same seeded inputs.
+
+Tolerance, from the arithmetic: every output is one fp32 fused multiply-add
+chain over the N = I_mode products in index order, so
+|T - T_exact| <= gamma_N * (|X| x_mode |M|) with gamma_N = N u / (1 - N u),
+u = 2^-24 (fp32 unit roundoff); the tests check that element-wise bound, and
+1e-5 relative Frobenius."""
+import numpy as np
+import pytest
+
+from conftest import rel_fro
+from oracle import ttm as ottm
+
+torch = pytest.importorskip("torch")
+import dense_tensor_decomposition_gb300 as mk  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+U = 2.0 ** -24
+
+
+def case(seed, dims, mode, J):
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal(dims).astype(np.float32)
+    M = rng.standard_normal((J, dims[mode])).astype(np.float32)
+    return X, M
+
+
+def check(got, X, mode, M):
+    want = ottm.ttm(X, mode, M)
+    N = X.shape[mode]
+    gamma = N * U / (1 - N * U)
+    bound = gamma * ottm.ttm(np.abs(X), mode, np.abs(M)) + 1e-30
+    assert rel_fro(got, want) <= 1e-5
+    assert np.all(np.abs(got.astype(np.float64) - want) <= bound)
+
+
+# Q = product of the modes after `mode`: float4 columns (Q % 4 == 0), scalar
+# columns (Q >= 32, odd), float4 along i (innermost, N % 4 == 0), scalar along
+# i (short or odd Q); J picks 32/64/128-row tiles, ragged in rows and columns;
+# float4 stores along columns, along rows (innermost, J % 4 == 0) and scalars.
+SHAPES = [((64, 48, 256), 0, 20), ((64, 48, 256), 1, 50), ((64, 48, 256), 2, 130), ((64, 48, 256), 2, 33),
+          ((7, 33, 9, 5), 0, 7), ((7, 33, 9, 5), 1, 64), ((7, 33, 9, 5), 2, 9), ((7, 33, 9, 5), 3, 200),
+          ((300, 257), 0, 300), ((300, 257), 1, 257), ((1000,), 0, 3), ((16, 16, 16, 16, 16), 2, 16),
+          ((3, 1, 5), 1, 4)]
+
+
+@pytest.mark.parametrize("dims,mode,J", SHAPES)
+def test_ttm_matches_oracle(dims, mode, J):
+    X, M = case(sum(dims) + 7 * mode + J, dims, mode, J)
+    T = mk.ttm(torch.from_numpy(X).cuda(), mode, torch.from_numpy(M).cuda())
+    assert tuple(T.shape) == tuple(dims[:mode]) + (J,) + tuple(dims[mode + 1:])
+    check(T.cpu().numpy(), X, mode, M)
+
+
+def test_tucker_reconstruction_chain_and_repeatability():
+    """Core x_0 U_0 x_1 U_1 x_2 U_2 (the full-tensor reconstruction of the
+    Jacobi page's Tucker setting), each product on the previous result."""
+    rng = np.random.default_rng(31)
+    core = rng.standard_normal((12, 10, 8)).astype(np.float32)
+    Us = [rng.standard_normal((n, r)).astype(np.float32) for n, r in ((40, 12), (36, 10), (44, 8))]
+    cur_d = torch.from_numpy(core).cuda()
+    cur_h = core
+    for k, Uk in enumerate(Us):
+        cur_d = mk.ttm(cur_d, k, torch.from_numpy(Uk).cuda())
+        got = cur_d.cpu().numpy()
+        check(got, cur_h, k, Uk)
+        cur_h = got                              # next step from the GPU's fp32 result
+    again = torch.from_numpy(core).cuda()
+    for k, Uk in enumerate(Us):
+        again = mk.ttm(again, k, torch.from_numpy(Uk).cuda())
+    assert torch.equal(again, cur_d)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_full_size_sampled(mode):
+    """512^3 with a square 512 x 512 matrix (the bench's launch
+    configuration), checked on 2000 sampled outputs computed one by one."""
+    rng = np.random.default_rng(40 + mode)
+    dims = (512, 512, 512)
+    Xd = torch.randn(dims, generator=torch.Generator().manual_seed(41 + mode)).cuda()
+    M = rng.standard_normal((512, 512)).astype(np.float32)
+    T = mk.ttm(Xd, mode, torch.from_numpy(M).cuda())
+    idx = [rng.integers(0, 512, 2000) for _ in range(3)]
+    got = T[idx[0], idx[1], idx[2]].cpu().numpy().astype(np.float64)
+    X = Xd.cpu().numpy()
+    want = np.empty(2000)
+    bound = np.empty(2000)
+    for s in range(2000):
+        at = [int(idx[0][s]), int(idx[1][s]), int(idx[2][s])]
+        j = at[mode]
+        at[mode] = slice(None)
+        x = X[tuple(at)].astype(np.float64)   # the fibre along `mode`
+        want[s] = x @ M[j].astype(np.float64)
+        bound[s] = np.abs(x) @ np.abs(M[j]).astype(np.float64)
+    assert np.all(np.abs(got - want) <= 512 * U / (1 - 512 * U) * bound + 1e-30)
+    del T, Xd
+    torch.cuda.empty_cache()
+
+
+def test_out_buffer_and_rejects_bad_arguments():
+    X = torch.randn((8, 6, 4), device="cuda")
+    M = torch.randn((6, 6), device="cuda")
+    out = torch.empty((8, 6, 4), device="cuda")
+    assert mk.ttm(X, 1, M, out=out) is out
+    with pytest.raises(mk.MttkrpError):
+        mk.ttm(X, 1, M, out=X)                   # the result may not overlap X
+    with pytest.raises(ValueError):
+        mk.ttm(X, 1, torch.randn((6, 5), device="cuda"))   # M has 5 columns, mode 1 has 6
+    with pytest.raises(ValueError):
+        mk.ttm(X, 3, M)                          # mode out of range
+    with pytest.raises(mk.MttkrpError):
+        mk.ttm(X, 1, torch.empty((0, 6), device="cuda"))   # J = 0
