@@ -62,42 +62,45 @@ __global__ void __launch_bounds__(256) rotate_items4_kernel(float4* __restrict__
 // short slabs (N * Q <= kSlab floats, e.g. the innermost mode): T whole
 // consecutive [N, Q] slabs are read flat into shared memory, rotated there and
 // written back flat, so every global access is coalesced.  With VEC the host
-// has chosen T so that every tile starts on a 16-byte boundary; the flat copies
-// then move float4s, eight in flight per thread, and the tail of the last tile
-// goes element by element.
+// has chosen T so that every tile starts on a 16-byte boundary: the tile is
+// loaded with cp.async 16-byte copies (straight into shared memory, no
+// registers, the whole tile in flight at once) and stored as float4s; the
+// tail of the last tile goes element by element.
 constexpr int kSlab = 8192;
 constexpr int kSlabThreads = 256;
-constexpr int kSlabUnroll = 8;
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+
+// waits for this thread's copies (a hardware wait, no polling)
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 template <bool VEC>
-__device__ __forceinline__ void slab_copy(float* __restrict__ dst, const float* __restrict__ src, int nv, bool to_smem) {
+__device__ __forceinline__ void slab_load(float* __restrict__ sm, const float* __restrict__ src, int nv) {
     int done = 0;
-    if (VEC) {
+    if constexpr (VEC) {
         const int nv4 = nv >> 2;
-        const float4* s4 = reinterpret_cast<const float4*>(src);
-        float4* d4 = reinterpret_cast<float4*>(dst);
-        for (int e0 = threadIdx.x; e0 < nv4; e0 += kSlabUnroll * kSlabThreads) {
-            float4 r[kSlabUnroll];
-#pragma unroll
-            for (int u = 0; u < kSlabUnroll; ++u) {
-                const int e = e0 + u * kSlabThreads;
-                if (e < nv4) r[u] = to_smem ? __ldcs(s4 + e) : s4[e];
-            }
-#pragma unroll
-            for (int u = 0; u < kSlabUnroll; ++u) {
-                const int e = e0 + u * kSlabThreads;
-                if (e < nv4) {
-                    if (to_smem) d4[e] = r[u];
-                    else __stcs(d4 + e, r[u]);
-                }
-            }
-        }
+        for (int e = threadIdx.x; e < nv4; e += kSlabThreads) cp_async16(sm + 4 * e, src + 4 * e);
         done = nv4 << 2;
     }
-    for (int e = done + threadIdx.x; e < nv; e += kSlabThreads) {
-        if (to_smem) dst[e] = __ldcs(src + e);
-        else __stcs(dst + e, src[e]);
+    for (int e = done + threadIdx.x; e < nv; e += kSlabThreads) sm[e] = __ldcs(src + e);
+    if constexpr (VEC) cp_async_wait_all();
+}
+
+template <bool VEC>
+__device__ __forceinline__ void slab_store(float* __restrict__ dst, const float* __restrict__ sm, int nv) {
+    int done = 0;
+    if constexpr (VEC) {
+        const int nv4 = nv >> 2;
+        const float4* s4 = reinterpret_cast<const float4*>(sm);
+        float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll 4
+        for (int e = threadIdx.x; e < nv4; e += kSlabThreads) __stcs(d4 + e, s4[e]);
+        done = nv4 << 2;
     }
+    for (int e = done + threadIdx.x; e < nv; e += kSlabThreads) __stcs(dst + e, sm[e]);
 }
 
 template <bool VEC>
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(kSlabThreads) rotate_slabs_kernel(float* __res
         const int64_t p0 = tile * T;
         const int nt = (int)(P - p0 < T ? P - p0 : T);
         const int nv = nt * S;
-        slab_copy<VEC>(sm, Y + p0 * S, nv, true);
+        slab_load<VEC>(sm, Y + p0 * S, nv);
         __syncthreads();
         for (int q = q0, g = g0, t = t0; t < nt;) {
             const int pg = pairs[2 * g], qg = pairs[2 * g + 1];
@@ -141,7 +144,7 @@ __global__ void __launch_bounds__(kSlabThreads) rotate_slabs_kernel(float* __res
             t += dt;
         }
         __syncthreads();
-        slab_copy<VEC>(Y + p0 * S, sm, nv, false);
+        slab_store<VEC>(Y + p0 * S, sm, nv);
         __syncthreads();
     }
 }
@@ -149,10 +152,16 @@ __global__ void __launch_bounds__(kSlabThreads) rotate_slabs_kernel(float* __res
 template <bool VEC>
 int slab_blocks_per_sm() {
     static int occ = 0;
-    if (occ == 0 &&
-        (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rotate_slabs_kernel<VEC>, kSlabThreads, 0) != cudaSuccess ||
-         occ < 1))
-        occ = 1;
+    if (occ == 0) {
+        // largest shared-memory carveout, so that shared memory is not what limits residency
+        cudaFuncSetAttribute(rotate_slabs_kernel<VEC>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rotate_slabs_kernel<VEC>, kSlabThreads, 0) !=
+                cudaSuccess ||
+            occ < 1)
+            occ = 1;
+        cudaGetLastError();
+    }
     return occ;
 }
 
