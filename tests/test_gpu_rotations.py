@@ -65,3 +65,35 @@ def test_rejects_bad_arguments():
         mk.apply_rotations(Y, 1, P, C, C)          # 4 pairs do not fit a mode of size 6
     with pytest.raises(mk.MttkrpError):
         mk.apply_rotations(Y, 3, P[:1], C[:1], C[:1])   # mode out of range
+
+
+@pytest.mark.parametrize("dims,mode", [((512, 512, 512), 0), ((512, 512, 512), 1), ((512, 512, 512), 2),
+                                       ((20,) * 6, 4), ((20,) * 6, 5)])
+def test_full_size_sampled_fibres(dims, mode):
+    """The bench's workloads and launch configurations (a full group of N/2
+    pairs): 400 fibres along the mode, each checked against the oracle's
+    rotation of the same fibre; fp32 bound per entry: 2^-22 (|c x| + |s y|)."""
+    rng = np.random.default_rng(60 + mode + len(dims))
+    N = dims[mode]
+    G = N // 2
+    pairs = rng.permutation(N)[: 2 * G].reshape(G, 2).astype(np.int32)
+    phi = rng.uniform(-np.pi, np.pi, G)
+    c, s = np.cos(phi).astype(np.float32), np.sin(phi).astype(np.float32)
+    Yh = torch.randn(dims, generator=torch.Generator().manual_seed(61 + mode)).numpy()
+    Yd = torch.from_numpy(Yh).cuda()
+    mk.apply_rotations(Yd, mode, torch.from_numpy(pairs).cuda(), torch.from_numpy(c).cuda(),
+                       torch.from_numpy(s).cuda())
+    got = Yd.cpu().numpy()
+    mag = np.zeros(N)
+    for k in range(400):
+        at = [int(rng.integers(0, n)) for n in dims]
+        at[mode] = slice(None)
+        x = Yh[tuple(at)]
+        want = orot.apply_rotations(x, 0, pairs, c, s)
+        mag[:] = np.abs(x)
+        for (p, q), cg, sg in zip(pairs, c, s):
+            mag[p] = abs(cg * x[p]) + abs(sg * x[q])
+            mag[q] = abs(cg * x[q]) + abs(sg * x[p])
+        assert np.all(np.abs(got[tuple(at)] - want) <= 2.0 ** -22 * mag), (k, at)
+    del Yd
+    torch.cuda.empty_cache()
