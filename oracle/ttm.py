@@ -13,7 +13,8 @@ sum as plain Python loops, for tiny inputs.
 
 Pins (tests/test_ttm_oracle.py): the loops on tiny inputs for every mode, the
 d = 2 cases as matrix products, the identity matrix, composition in one mode,
-commutation across two modes, the rank-one closed form, and planted mistakes.
+commutation across two modes, the rank-one closed form, the 2-way MTTKRP
+oracle on the permuted tensor, and planted mistakes.
 """
 from __future__ import annotations
 

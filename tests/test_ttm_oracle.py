@@ -56,3 +56,20 @@ def test_planted_mistakes_are_caught():
     assert not np.allclose(wrong_mode, want, atol=1e-6)
     with pytest.raises(ValueError):
         ottm.ttm(X, 0, M)                                           # I_0 = 4 does not match M's 5 columns
+
+
+@pytest.mark.parametrize("dims,mode,J", [((4, 5, 6), 0, 3), ((4, 5, 6), 1, 7), ((4, 5, 6), 2, 2),
+                                         ((3, 2, 4, 5), 2, 6)])
+def test_equals_two_way_mttkrp_of_the_permuted_tensor(dims, mode, J):
+    """With mode n moved last, Z[(p, q), i] = X[p, i, q]; the 2-way MTTKRP of Z
+    for mode 0 with the single factor M^T is sum_i Z[(p, q), i] M[j, i], i.e.
+    T[p, j, q] laid out as [(p, q), j].  Ties the mode-n product oracle to the
+    MTTKRP oracle (plain C, its own pins)."""
+    import oracle
+    X = rnd(20 + mode, *dims)
+    M = rnd(21 + J, J, dims[mode])
+    Z = np.ascontiguousarray(np.moveaxis(X, mode, -1).reshape(-1, dims[mode]))
+    A0 = np.zeros((Z.shape[0], J))                        # mode 0's own factor is not used
+    M0 = oracle.mttkrp(Z, [A0, np.ascontiguousarray(M.T)], 0)
+    want = np.moveaxis(M0.reshape(np.moveaxis(X, mode, -1).shape[:-1] + (J,)), -1, mode)
+    assert np.allclose(ottm.ttm(X, mode, M), want, rtol=1e-12, atol=1e-12)
