@@ -212,6 +212,82 @@ def oracle_sample(w, Y, A, seconds):
                       f"({rows}/{w.dims[k]} of one mode), {dt:.1f} s, fp64"}
 
 
+def _mode_sample(Yh, k, elems):
+    """Y cut to its first s indices along one mode other than k (mode 0, or
+    mode 1 when k == 0) so that it holds about `elems` elements; a view."""
+    d = Yh.ndim
+    if d == 1:
+        return Yh
+    m = 0 if k != 0 else 1
+    per = Yh.size // Yh.shape[m]
+    s = int(max(1, min(Yh.shape[m], elems // max(per, 1))))
+    return Yh[(slice(None),) * m + (slice(0, s),)]
+
+
+def _timed_samples(Yh, seconds, run_mode, units_of):
+    """Grow a per-mode sample until one pass over all modes takes about
+    `seconds`; returns (units processed, seconds, elements per mode sample)."""
+    elems = 1 << 18
+    while True:
+        t0 = time.perf_counter()
+        units = 0.0
+        for k in range(Yh.ndim):
+            sample = _mode_sample(Yh, k, elems)
+            run_mode(sample, k)
+            units += units_of(sample, k)
+        dt = time.perf_counter() - t0
+        if dt >= seconds / 4 or elems >= Yh.size:
+            return units, dt, elems
+        elems = int(min(Yh.size, elems * max(2.0, min(16.0, seconds / 2 / max(dt, 1e-3)))))
+
+
+def rotations_cpu_baseline(Yh, groups, seconds):
+    """The fp64 rotation oracle on slices of the tensor (one mode at a time,
+    a full group per mode), GB/s of rotated rows read and written."""
+    from oracle import rotations as orot
+
+    def run(sample, k):
+        orot.apply_rotations(sample, k, *groups[k])
+
+    def units(sample, k):
+        return 2.0 * 4 * (sample.size // sample.shape[k]) * 2 * len(groups[k][0])
+
+    moved, dt, elems = _timed_samples(Yh, seconds, run, units)
+    return {"value": moved / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"every mode on a slice of about {elems} elements (cut along another mode), "
+                      f"{dt:.1f} s, numpy fp64, one thread"}
+
+
+def ttm_cpu_baseline(Xh, Ms, seconds):
+    """The fp64 mode-n product oracle on slices of the tensor, TFLOP/s."""
+    from oracle import ttm as ottm
+
+    def run(sample, k):
+        ottm.ttm(sample, k, Ms[k])
+
+    def units(sample, k):
+        return 2.0 * Ms[k].shape[0] * sample.size
+
+    flops, dt, elems = _timed_samples(Xh, seconds, run, units)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"every mode on a slice of about {elems} elements (cut along another mode), "
+                      f"{dt:.1f} s, numpy fp64 matrix products (BLAS threads)"}
+
+
+def cp_als_cpu_baseline(Yh, A0):
+    """One fp64 oracle sweep on the whole tensor, ms per sweep."""
+    import numpy as np
+    import oracle
+    from oracle import cp_als as ocp
+    norm = float(np.sum(np.asarray(Yh, dtype=np.float64) ** 2))
+    t0 = time.perf_counter()
+    ocp.cp_als_sweep(Yh, A0, norm_y2=norm)
+    dt = time.perf_counter() - t0
+    return {"value": dt * 1e3, "unit": "ms", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"one sweep on the whole tensor ({dt:.1f} s; ||Y||^2 precomputed), "
+                      f"MTTKRP in the C oracle (OpenMP), the rest numpy fp64"}
+
+
 def run_reference(args, w):
     """--impl reference: the oracle on this host's cores, same metric and workload."""
     rank = int(os.environ.get("RANK", "0"))
@@ -457,7 +533,8 @@ def run_cp_als(args, w):
     import torch
     import dense_tensor_decomposition_gb300 as mk
     device = torch.device("cuda", 0)
-    Y = torch.from_numpy(synth.make_tensor(w)).to(device)
+    Yh = synth.make_tensor(w)
+    Y = torch.from_numpy(Yh).to(device)
     R = args.cp_rank
     rng = np.random.default_rng(20261202)
     A0 = [rng.standard_normal((n, R)).astype(np.float32) for n in w.dims]
@@ -477,6 +554,7 @@ def run_cp_als(args, w):
     ms = e0.elapsed_time(e1) / args.cp_als
     mttkrp_ms = sum(sum(plan.kernel_times(k)) for k in range(w.d)) / args.cp_als
     plan.set_timing(False)
+    cpu = None if args.no_cpu_baseline else cp_als_cpu_baseline(Yh, A0)
     print(json.dumps({
         "metric": "CP-ALS time per sweep (every factor updated once, fit included)",
         "value": round(ms, 4), "unit": "ms", "higher_is_better": False, "n_gpus": 1,
@@ -486,6 +564,7 @@ def run_cp_als(args, w):
         "mttkrp_kernel_ms_per_sweep": round(mttkrp_ms, 4),
         "mttkrp_share": round(mttkrp_ms / ms, 4),
         "fit_first_last": [round(float(fits[0]), 6), round(float(fits[-1]), 6)],
+        "cpu_baseline": cpu,
         "kernel_src": kernel_source_hash(),
     }))
 
@@ -498,15 +577,16 @@ def run_rotations(args, w):
     import torch
     import dense_tensor_decomposition_gb300 as mk
     device = torch.device("cuda", 0)
-    Y = torch.from_numpy(synth.make_tensor(w)).to(device)
+    Yh = synth.make_tensor(w)
+    Y = torch.from_numpy(Yh).to(device)
     rng = np.random.default_rng(20261202)
-    groups = []
+    groups, groups_h = [], []
     for n in w.dims:
         G = n // 2
         pairs = rng.permutation(n)[: 2 * G].reshape(G, 2).astype(np.int32)
         phi = rng.uniform(-np.pi, np.pi, G)
-        groups.append(tuple(torch.from_numpy(x).to(device) for x in
-                            (pairs, np.cos(phi).astype(np.float32), np.sin(phi).astype(np.float32))))
+        groups_h.append((pairs, np.cos(phi).astype(np.float32), np.sin(phi).astype(np.float32)))
+        groups.append(tuple(torch.from_numpy(x).to(device) for x in groups_h[-1]))
 
     def step():
         for k in range(w.d):
@@ -537,6 +617,7 @@ def run_rotations(args, w):
         moved += 2 * 4 * (int(np.prod(w.dims)) // n) * 2 * (n // 2)   # rotated rows read + written
     gbs = moved / (ms * 1e-3) / 1e9
     peaks, src = measured_peaks()
+    cpu = None if args.no_cpu_baseline else rotations_cpu_baseline(Yh, groups_h, args.cpu_seconds)
     print(json.dumps({
         "metric": "Givens rotations along every mode: GB/s of rotated rows read and written",
         "value": round(gbs, 1), "unit": "GB/s", "higher_is_better": True, "n_gpus": 1,
@@ -546,6 +627,7 @@ def run_rotations(args, w):
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": src},
         "ms_per_mode": per_mode,
+        "cpu_baseline": cpu,
         "kernel_src": kernel_source_hash(),
     }))
 
@@ -559,11 +641,13 @@ def run_ttm(args, w):
     import torch
     import dense_tensor_decomposition_gb300 as mk
     device = torch.device("cuda", 0)
-    X = torch.from_numpy(synth.make_tensor(w)).to(device)
+    Xh = synth.make_tensor(w)
+    X = torch.from_numpy(Xh).to(device)
     rng = np.random.default_rng(20261203)
     numel = int(np.prod(w.dims))
     Js = [n if args.ttm == 0 else args.ttm for n in w.dims]
-    Ms = [torch.from_numpy(rng.standard_normal((J, n)).astype(np.float32)).to(device) for J, n in zip(Js, w.dims)]
+    Ms_h = [rng.standard_normal((J, n)).astype(np.float32) for J, n in zip(Js, w.dims)]
+    Ms = [torch.from_numpy(m).to(device) for m in Ms_h]
     outs = [torch.empty(list(w.dims[:k]) + [Js[k]] + list(w.dims[k + 1:]), device=device) for k in range(w.d)]
 
     def step():
@@ -597,6 +681,7 @@ def run_ttm(args, w):
     props = torch.cuda.get_device_properties(device)
     sm_mhz = peaks.get("sm_max_mhz", SM_MAX_MHZ_FALLBACK)
     alu_peak = props.multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
+    cpu = None if args.no_cpu_baseline else ttm_cpu_baseline(Xh, Ms_h, args.cpu_seconds)
     print(json.dumps({
         "metric": "dense mode-n product along every mode: TFLOP/s (2 J prod(I_n) per mode)",
         "value": round(tflops, 3), "unit": "TFLOP/s", "higher_is_better": True, "n_gpus": 1,
@@ -610,6 +695,7 @@ def run_ttm(args, w):
                      "hbm_ms_at_algorithmic_bytes": round(moved / (peaks["hbm_gbs"] * 1e9) * 1e3, 4),
                      "hbm_peak_source": src},
         "ms_per_mode": per_mode,
+        "cpu_baseline": cpu,
         "kernel_src": kernel_source_hash(),
     }))
 
