@@ -1,0 +1,52 @@
+"""bench.py's host-side bookkeeping (no GPU): the source hashes that key the
+DRAM traffic records, the record lookup, and the fallback peaks."""
+import os
+import shutil
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+
+def fake_root(tmp_path):
+    """A copy of the CUDA sources and the traffic records under tmp_path."""
+    src = os.path.join(bench.ROOT, "dense_tensor_decomposition_gb300", "csrc")
+    dst = tmp_path / "dense_tensor_decomposition_gb300" / "csrc"
+    shutil.copytree(src, dst, ignore=shutil.ignore_patterns("*.o", "*.so"))
+    (tmp_path / "profiles").mkdir()
+    return tmp_path, dst
+
+
+def test_main_kernel_hash_ignores_the_other_kernels(tmp_path, monkeypatch):
+    root, csrc = fake_root(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    main = bench.MAIN_KERNEL_SOURCES["tc"]
+    h_main, h_all = bench.kernel_source_hash(main), bench.kernel_source_hash()
+    assert h_main != h_all
+    with open(csrc / "rotations.cu", "a") as f:          # another kernel changes
+        f.write("\n// edit\n")
+    assert bench.kernel_source_hash(main) == h_main
+    assert bench.kernel_source_hash() != h_all
+    with open(csrc / "tc.cu", "a") as f:                 # the main kernel changes
+        f.write("\n// edit\n")
+    assert bench.kernel_source_hash(main) != h_main
+
+
+def test_recorded_traffic_lookup(tmp_path, monkeypatch):
+    root, _ = fake_root(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    (root / "profiles" / "dram_traffic.txt").write_text(
+        "# comment line\n"
+        "workload=w1 path=tc src=aaaa bytes_per_launch=100 capture=x.md (note)\n"
+        "workload=w1 path=simt src=aaaa bytes_per_launch=200 capture=y.md\n"
+        "workload=w2 path=tc src=bbbb bytes_per_launch=300 capture=z.md\n")
+    assert bench.recorded_traffic("w1", "tc", "aaaa") == 100.0
+    assert bench.recorded_traffic("w1", "simt", "aaaa") == 200.0
+    assert bench.recorded_traffic("w1", "tc", "bbbb") is None      # other sources: no figure
+    assert bench.recorded_traffic("w3", "tc", "aaaa") is None
+
+
+def test_peaks_fall_back_when_unmeasured(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    peaks, src = bench.measured_peaks()
+    assert src == "fallback" and peaks["hbm_gbs"] == 6800.0 and peaks["bf16_tflops"] == 1900.0
