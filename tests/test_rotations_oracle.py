@@ -45,3 +45,26 @@ def test_planted_sign_mistake_is_caught():
     R = rot.rotation_matrix(8, pairs, c, s)
     wrong = np.moveaxis(np.tensordot(R, np.moveaxis(Y, 2, 0), axes=(1, 0)), 0, 2)   # R instead of R^T
     assert not np.allclose(rot.apply_rotations(Y, 2, pairs, c, s), wrong, atol=1e-6)
+
+
+def _mutant(Y, mode, pairs, c, s, kind):
+    out = np.moveaxis(np.array(Y, dtype=np.float64), mode, 0)
+    for (p, q), cg, sg in zip(pairs, c, s):
+        x, y = out[p].copy(), out[q].copy()
+        if kind == "sign":                 # sine sign flipped in both rows
+            out[p], out[q] = cg * x - sg * y, cg * y + sg * x
+        elif kind == "in_place":           # q updated from the already-updated p
+            out[p] = cg * x + sg * y
+            out[q] = cg * y - sg * out[p]
+        elif kind == "swap":               # p and q roles exchanged
+            out[q], out[p] = cg * y + sg * x, cg * x - sg * y
+    return np.moveaxis(out, 0, mode)
+
+
+@pytest.mark.parametrize("kind", ["sign", "in_place", "swap"])
+def test_plausible_mistakes_fail_the_dense_product_pin(kind):
+    Y, pairs, c, s = case(11, (6, 8, 5), 1, 3)
+    R = rot.rotation_matrix(8, pairs, c, s)
+    want = np.moveaxis(np.tensordot(R.T, np.moveaxis(Y, 1, 0), axes=(1, 0)), 0, 1)
+    assert np.allclose(rot.apply_rotations(Y, 1, pairs, c, s), want, rtol=1e-13, atol=1e-13)
+    assert not np.allclose(_mutant(Y, 1, pairs, c, s, kind), want, atol=1e-6)
