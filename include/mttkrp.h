@@ -30,6 +30,12 @@
  * fixed order, in fp64 or compensated fp32).  A plan and its workspace may be used by one stream
  * at a time; calls on one plan are not thread-safe.
  *
+ * Around the MTTKRP the library also provides one CP-ALS sweep on the device
+ * (mttkrp_cp_als_sweep, on a plan), and two dense kernels of the Jacobi-type
+ * Tucker diagonalization setting that take plain pointers and no plan: the
+ * mode-n product (mttkrp_ttm) and Givens rotations along a mode
+ * (mttkrp_apply_rotations).
+ *
  * Errors: every int-returning call returns MTTKRP_OK (0) or one of the codes
  * below; nothing is thrown across the ABI.  mttkrp_strerror() names a code and
  * mttkrp_last_error() gives the calling thread's last detailed message.
