@@ -21,10 +21,10 @@ import threading
 from ._build import LIB as LIB_PATH, build  # noqa: F401
 
 __all__ = ["Plan", "mttkrp", "all_modes", "apply_rotations", "ttm", "MttkrpError", "build", "load_library",
-           "exported_symbols", "PATH_AUTO", "PATH_SIMT", "PATH_TC"]
+           "exported_symbols", "PATH_AUTO", "PATH_SIMT", "PATH_TC", "PATH_TC_TF32"]
 
-PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
-_PATH_NAMES = {"auto": PATH_AUTO, "simt": PATH_SIMT, "tc": PATH_TC}
+PATH_AUTO, PATH_SIMT, PATH_TC, PATH_TC_TF32 = 0, 1, 2, 3
+_PATH_NAMES = {"auto": PATH_AUTO, "simt": PATH_SIMT, "tc": PATH_TC, "tc_tf32": PATH_TC_TF32}
 
 _lock = threading.Lock()
 _lib = None
@@ -152,8 +152,8 @@ class Plan:
         return {PATH_SIMT: "simt", PATH_TC: "tc"}.get(p, "invalid")
 
     def describe(self, mode: int) -> str:
-        buf = ctypes.create_string_buffer(512)
-        n = self._lib.mttkrp_plan_describe(self._h, mode, buf, 512)
+        buf = ctypes.create_string_buffer(1024)
+        n = self._lib.mttkrp_plan_describe(self._h, mode, buf, 1024)
         if n < 0:
             raise ValueError(f"invalid mode {mode}")
         return buf.value.decode()

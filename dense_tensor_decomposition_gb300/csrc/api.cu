@@ -168,11 +168,14 @@ int plan_mode(Plan& p, int k, int path) {
     ModePlan& mp = p.mode[k];
     memset(&mp, 0, sizeof(mp));
     classify(p, k, mp.g);
+    // MTTKRP_PATH_TC_TF32: the tensor-core kernels without the fp16 split
+    const bool allow_fp16 = path != MTTKRP_PATH_TC_TF32;
+    if (path == MTTKRP_PATH_TC_TF32) path = MTTKRP_PATH_TC;
     if (path == MTTKRP_PATH_AUTO) {
         path = MTTKRP_PATH_SIMT;
         if (tc_prefer(mp)) {
             ModePlan trial = mp;
-            if (tc_plan(p, trial)) path = MTTKRP_PATH_TC;
+            if (tc_plan(p, trial, true)) path = MTTKRP_PATH_TC;
         }
     }
     ModePlan& alt = p.simt_alt[k];
@@ -181,7 +184,7 @@ int plan_mode(Plan& p, int k, int path) {
     layout_workspace(alt);
     const bool simt_ok = cdiv(alt.g.I, alt.bm) <= 65535;  // row tiles run along gridDim.y
     if (path == MTTKRP_PATH_TC) {
-        if (!tc_plan(p, mp)) return MTTKRP_ERR_UNSUPPORTED;
+        if (!tc_plan(p, mp, allow_fp16)) return MTTKRP_ERR_UNSUPPORTED;
         layout_workspace(mp);
         if (simt_ok && alt.total > mp.total) mp.total = alt.total;
     } else {
@@ -410,7 +413,8 @@ int mttkrp_plan(int d, const int64_t* dims, int64_t R, mttkrp_plan_t* out) {
 int mttkrp_plan_set_path(mttkrp_plan_t h, int path) {
     Plan* p = as_plan(h);
     if (p == nullptr) return fail(MTTKRP_ERR_INVALID, "plan is NULL");
-    if (path != MTTKRP_PATH_AUTO && path != MTTKRP_PATH_SIMT && path != MTTKRP_PATH_TC)
+    if (path != MTTKRP_PATH_AUTO && path != MTTKRP_PATH_SIMT && path != MTTKRP_PATH_TC &&
+        path != MTTKRP_PATH_TC_TF32)
         return fail(MTTKRP_ERR_INVALID, "unknown path %d", path);
     ModePlan saved[kMaxD];
     memcpy(saved, p->mode, sizeof(saved));
@@ -674,12 +678,24 @@ int mttkrp_plan_describe(mttkrp_plan_t h, int mode, char* buf, size_t len) {
         snprintf(groups + strlen(groups), sizeof(groups) - strlen(groups), "%s%d", t ? "," : "", g.group[t]);
     for (int t = 0; t < g.npm; ++t)
         snprintf(pres + strlen(pres), sizeof(pres) - strlen(pres), "%s%d", t ? "," : "", g.pm[t]);
-    char tmp[512];
+    // kernel variant: family (simt; img = fp16 images, h2 = fp16 split in tensor
+    // memory, tf32 = 3xTF32 with A in shared memory, tf32tm = 3xTF32 with A in
+    // tensor memory), then the A layout (nat / t = transposed images, kmaj / inner
+    // = raw fp32 tiles), "small" for stacked pre indices, and the tile width
+    char kernel[64];
+    if (mp.path != MTTKRP_PATH_TC) {
+        snprintf(kernel, sizeof(kernel), "simt.bn%d", mp.bn);
+    } else {
+        const char* fam = mp.tc_img ? "img" : mp.tc_h2 ? "h2" : mp.tc_tmem ? "tf32tm" : "tf32";
+        const char* lay = mp.tc_img ? (mp.tc_img_t ? "t" : "nat") : (mp.tc_inner ? "inner" : "kmaj");
+        snprintf(kernel, sizeof(kernel), "%s.%s%s.bn%d", fam, lay, mp.tc_small ? ".small" : "", mp.bn);
+    }
+    char tmp[640];
     int n = snprintf(tmp, sizeof(tmp),
-                     "mode=%d path=%s tile=%dx%d inner_group=[%s] J=%lld Jq=%lld pre_modes=[%s] "
+                     "mode=%d path=%s kernel=%s tile=%dx%d inner_group=[%s] J=%lld Jq=%lld pre_modes=[%s] "
                      "npre=%lld splits=%lld pre_per_split=%lld workspace=%zu tc_ksteps=%d tc_inner=%d tc_slots=%d "
                      "tc_tmem_a=%d tc_fp16x2=%d tc_fp16_image=%d",
-                     mode, mp.path == MTTKRP_PATH_TC ? "tc" : "simt", mp.bm, mp.bn, groups,
+                     mode, mp.path == MTTKRP_PATH_TC ? "tc" : "simt", kernel, mp.bm, mp.bn, groups,
                      (long long)g.J, (long long)g.Jq, pres, (long long)g.npre,
                      (long long)mp.splits, (long long)mp.pre_per_split, mp.total, mp.tc_ks, mp.tc_inner,
                      mp.tc_small ? mp.tc_ps : 1, mp.tc_tmem, mp.tc_h2 || mp.tc_img, mp.tc_img + mp.tc_img_t);

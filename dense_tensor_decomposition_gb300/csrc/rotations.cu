@@ -1,5 +1,5 @@
-// Givens rotations along one mode ("Parallel Jacobi-type tensor
-// diagonalization on GPUs", §2 and §4.3, "Application of Rotations"): Y is
+// Givens rotations along one mode ("An HPC Approach to Accelerate Tensor
+// Decompositions", §2 and §4.3, "Application of Rotations"): Y is
 // multiplied in mode n by R^T, R the identity except for 2 x 2 blocks
 // [[c, -s], [s, c]] at rows and columns (p, q) of a group of disjoint pivot
 // pairs.  For every fibre along mode n and every pair g:

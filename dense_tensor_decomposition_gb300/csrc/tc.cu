@@ -3196,7 +3196,7 @@ bool tc_prefer(const ModePlan& mp) {
     return mp.g.R >= 32 && (mp.g.I >= 96 || small_eligible(mp.g));
 }
 
-bool tc_plan(const Plan& p, ModePlan& mp) {
+bool tc_plan(const Plan& p, ModePlan& mp, bool allow_fp16) {
     const ModeGeom& g = mp.g;
     mp.path = MTTKRP_PATH_TC;
     mp.tc_inner = (g.s_k == 1) ? 1 : 0;
@@ -3211,7 +3211,7 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
     {
         const int64_t h2_cols = cdiv64(g.R, kH2BN) * kH2BN * 10;
         const int64_t tf_cols = cdiv64(g.R, 256) * 256 * 14;
-        mp.tc_h2 = (!mp.tc_small && g.R >= TC_H2_MIN_R && h2_cols < tf_cols) ? 1 : 0;
+        mp.tc_h2 = (allow_fp16 && !mp.tc_small && g.R >= TC_H2_MIN_R && h2_cols < tf_cols) ? 1 : 0;
     }
     if (mp.tc_h2) mp.tc_tmem = 1;
     mp.tc_kw = mp.tc_h2 ? kBK2 : kBK;
@@ -3228,7 +3228,7 @@ bool tc_plan(const Plan& p, ModePlan& mp) {
     // the kernels that convert Y per CTA take over
     int64_t numel = 1;
     for (int t = 0; t < p.d; ++t) numel *= p.dims[t];
-    if (TC_IMG && g.R >= TC_IMG_MIN_R && numel <= ((int64_t)12 << 30)) {
+    if (allow_fp16 && TC_IMG && g.R >= TC_IMG_MIN_R && numel <= ((int64_t)12 << 30)) {
         ModePlan t = mp;
         t.tc_img = 1;
         t.tc_h2 = 0;

@@ -11,7 +11,8 @@ size_t tc_binner_bytes(const ModePlan& mp);
 // Whether the planner should choose the tensor-core path for this mode.
 bool tc_prefer(const ModePlan& mp);
 // Fill tiles and split counts for the tensor-core path; false if unsupported.
-bool tc_plan(const Plan& p, ModePlan& mp);
+// allow_fp16 = false keeps the mode on the 3xTF32 kernels.
+bool tc_plan(const Plan& p, ModePlan& mp, bool allow_fp16);
 // Enqueue the tensor-core work of one mode (tables are already built).
 // *nlaunch receives the number of kernels enqueued.  If start_ev is non-null,
 // *start_ev is re-recorded just before the main kernel (after the tensor-core

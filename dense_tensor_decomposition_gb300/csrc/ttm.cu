@@ -1,5 +1,5 @@
-// Dense mode-n product, TTM ("Parallel Jacobi-type tensor diagonalization on
-// GPUs", §2, eq. (1)): T = X x_n M for M of size J x N (N = I_n),
+// Dense mode-n product, TTM ("An HPC Approach to Accelerate Tensor
+// Decompositions", §2, eq. (1)): T = X x_n M for M of size J x N (N = I_n),
 //     T[p, j, q] = sum_i M[j, i] X[p, i, q],
 // with X viewed as [P, N, Q] (P: modes before n, Q: modes after) and T as
 // [P, J, Q].  All slabs form one fp32 SGEMM: rows j, columns c = p * Q + q,

@@ -66,8 +66,10 @@ enum mttkrp_status {
 /* Kernel family used for a mode.  AUTO lets the planner choose per mode. */
 enum mttkrp_path {
     MTTKRP_PATH_AUTO = 0,
-    MTTKRP_PATH_SIMT = 1, /* fp32 FMA on the CUDA cores */
-    MTTKRP_PATH_TC = 2    /* tcgen05 tensor cores, fp32-accurate split (fp16 two-term or 3xTF32) */
+    MTTKRP_PATH_SIMT = 1,   /* fp32 FMA on the CUDA cores */
+    MTTKRP_PATH_TC = 2,     /* tcgen05 tensor cores, fp32-accurate split (fp16 two-term or 3xTF32) */
+    MTTKRP_PATH_TC_TF32 = 3 /* tcgen05 tensor cores, 3xTF32 split only (no fp16): for tensors whose
+                               entries span more than the fp16 split's range (see mttkrp_plan) */
 };
 
 typedef struct mttkrp_plan_s* mttkrp_plan_t;
@@ -217,8 +219,8 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t plan, const float* Y, float* const* factor
                         void* stream);
 
 /*
- * Givens rotations along one mode ("Parallel Jacobi-type tensor
- * diagonalization on GPUs", §2 and §4.3, "Application of Rotations"): Y is
+ * Givens rotations along one mode ("An HPC Approach to Accelerate Tensor
+ * Decompositions", §2 and §4.3, "Application of Rotations"): Y is
  * multiplied in place in mode `mode` by R^T, where R is the identity except
  * for the 2 x 2 blocks [[c_g, -s_g], [s_g, c_g]] at rows and columns
  * (p_g, q_g) of a group of disjoint pivot pairs; for every fibre along the
@@ -241,8 +243,8 @@ int mttkrp_apply_rotations(int d, const int64_t* dims, float* Y, int mode, const
                            const float* s, int group_size, void* stream);
 
 /*
- * Dense mode-n product, TTM ("Parallel Jacobi-type tensor diagonalization on
- * GPUs", §2, eq. (1)): T = X x_mode M for a matrix M of size J x I_mode,
+ * Dense mode-n product, TTM ("An HPC Approach to Accelerate Tensor
+ * Decompositions", §2, eq. (1)): T = X x_mode M for a matrix M of size J x I_mode,
  *     T[i_0 .. i_{mode-1}, j, i_{mode+1} .. i_{d-1}]
  *         = sum over i of X[i_0 .. i_{mode-1}, i, i_{mode+1} .. i_{d-1}] * M[j, i].
  *

@@ -1,7 +1,7 @@
 """fp64 application of disjoint Givens rotations along one mode (TEST
 INFRASTRUCTURE ONLY: only tests/ and bench.py's CPU leg import it).
 
-"Parallel Jacobi-type tensor diagonalization on GPUs" (the page on the Jacobi
+"An HPC Approach to Accelerate Tensor Decompositions" (the page on the Jacobi
 method, §2 and §4.3, "Application of Rotations"): one step multiplies the tensor
 in mode n by R^T, where R differs from the identity only in 2 x 2 blocks
 [[c, -s], [s, c]] at rows and columns (p, q) of a group of disjoint pivot pairs.

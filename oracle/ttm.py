@@ -1,7 +1,7 @@
 """fp64 dense mode-n product, TTM (TEST INFRASTRUCTURE ONLY: only tests/ and
 bench.py's CPU leg import it).
 
-"Parallel Jacobi-type tensor diagonalization on GPUs", §2, eq. (1): for a
+"An HPC Approach to Accelerate Tensor Decompositions", §2, eq. (1): for a
 tensor X of size I_1 x ... x I_D and a matrix M of size J x I_n, the mode-n
 product T = X x_n M has size I_1 x ... x I_{n-1} x J x I_{n+1} x ... x I_D and
 

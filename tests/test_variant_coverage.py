@@ -1,0 +1,95 @@
+"""Every kernel variant the planner can choose is exercised by the GPU parity tests.
+
+The planner is host code (no GPU needed): for each (shape, path) that
+tests/test_gpu_parity.py runs, it reports the kernel of every mode
+(``kernel=`` in mttkrp_plan_describe).  Two checks:
+  * a sweep over many random shapes and ranks finds no variant outside the
+    known list (a new variant cannot appear untested);
+  * each known variant is planned for at least one mode of one shape that the
+    GPU parity tests run on the path that plans it.
+"""
+import itertools
+import math
+import random
+
+import pytest
+
+from parity_shapes import EDGE, H2_SHAPES
+
+mk = pytest.importorskip("dense_tensor_decomposition_gb300")
+
+# family.layout[.small].bn<columns>; families: simt, img (fp16 images of Y),
+# h2 (fp16 split in tensor memory), tf32 (3xTF32, A in shared memory),
+# tf32tm (3xTF32, A in tensor memory)
+KNOWN = {
+    "simt.bn64", "simt.bn128",
+    "img.nat.bn64", "img.nat.bn128", "img.nat.bn256", "img.nat.small.bn64", "img.nat.small.bn128",
+    "img.t.bn64", "img.t.bn128", "img.t.bn256", "img.t.small.bn64", "img.t.small.bn128",
+    "h2.kmaj.bn224", "h2.inner.bn224",
+    "tf32.kmaj.bn64", "tf32.kmaj.bn128", "tf32.kmaj.bn256",
+    "tf32.inner.bn64", "tf32.inner.bn128", "tf32.inner.bn256",
+    "tf32.kmaj.small.bn64", "tf32.kmaj.small.bn128", "tf32.kmaj.small.bn256",
+    "tf32.inner.small.bn64", "tf32.inner.small.bn128", "tf32.inner.small.bn256",
+    "tf32tm.inner.bn224",
+}
+PATHS = ("auto", "simt", "tc", "tc_tf32")
+
+# the five workloads and the fixed shapes of the other GPU parity tests
+WORKLOADS = [((32, 32, 32), 8), ((256, 256, 256), 64), ((128,) * 4, 256), ((512,) * 3, 2000),
+             ((20,) * 6, 128)]
+OTHER = [((7, 12, 36, 5), 37), ((300, 200), 48), ((24, 16, 32), 20), ((45, 36, 20), 19),
+         ((31, 22, 17, 9), 40), ((96, 80, 64), 64), ((16, 130, 8, 64), 200)]
+
+
+def kernels(dims, R, path):
+    try:
+        plan = mk.Plan(dims, R, path)
+    except mk.MttkrpError:
+        return []
+    out = []
+    for k in range(len(dims)):
+        field = [f for f in plan.describe(k).split() if f.startswith("kernel=")]
+        assert len(field) == 1
+        out.append(field[0][len("kernel="):])
+    return out
+
+
+def test_random_shapes_plan_only_known_variants():
+    rng = random.Random(2026)
+    sizes = [1, 2, 3, 4, 5, 7, 8, 12, 16, 17, 20, 24, 30, 32, 33, 36, 40, 44, 48, 60, 64, 65, 96, 100,
+             120, 128, 129, 130, 136, 150, 160, 200, 256, 300, 512]
+    ranks = [1, 3, 8, 17, 31, 32, 33, 48, 64, 65, 96, 100, 128, 130, 159, 160, 192, 200, 224, 256, 260,
+             300, 447, 448, 460, 500, 1000, 2000]
+    found = set()
+    for _ in range(1500):
+        d = rng.randint(2, 6)
+        dims = tuple(rng.choice(sizes) for _ in range(d))
+        if math.prod(dims) > 1 << 28:
+            continue
+        R = rng.choice(ranks)
+        for path in PATHS:
+            found.update(kernels(dims, R, path))
+    assert found <= KNOWN, sorted(found - KNOWN)
+
+
+def test_every_variant_is_gpu_tested():
+    """(shape, path) pairs as the GPU parity tests run them: the edge shapes and
+    workloads on every forced path, the value-range shapes on the planner's own
+    choice."""
+    planned = {}
+    for (dims, R), path in itertools.product(EDGE + WORKLOADS + OTHER, ("simt", "tc", "tc_tf32")):
+        for k, v in enumerate(kernels(dims, R, path)):
+            planned.setdefault(v, (dims, R, path, k))
+    for dims, R in H2_SHAPES:
+        for k, v in enumerate(kernels(dims, R, "auto")):
+            planned.setdefault(v, (dims, R, "auto", k))
+    missing = sorted(KNOWN - set(planned))
+    assert not missing, f"variants no GPU parity shape plans: {missing}"
+
+
+def test_headline_workload_kernels():
+    """The planner's choice on the largest workload, and the 3xTF32 kernels the
+    forced path takes there (the innermost mode with A in tensor memory)."""
+    assert kernels((512,) * 3, 2000, "auto") == ["img.nat.bn256", "img.nat.bn256", "img.t.bn256"]
+    assert kernels((512,) * 3, 2000, "tc_tf32") == ["tf32.kmaj.bn256", "tf32.kmaj.bn256",
+                                                     "tf32tm.inner.bn224"]

@@ -4,16 +4,17 @@ mttkrp_noalloc serves callers that must not allocate device memory (a library
 inside a program whose own allocator owns the GPU's memory, or a
 latency-critical path where cudaMalloc/cudaFree may block until the device is
 idle): its scratch is a fixed static device array inside the library.  Here its
-output is checked against the regular workspace-based entry point, within the
-1e-5 relative Frobenius tolerance of the other GPU tests, on two calls in a
-row (the second call reuses scratch the first one left behind).  This file is
-named so that pytest collects it last.
+output is checked against the fp64 oracle and against the regular
+workspace-based entry point, within the 1e-5 relative Frobenius tolerance of
+the other GPU tests, on two calls in a row (the second call reuses scratch the
+first one left behind).  This file is named so that pytest collects it last.
 """
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from conftest import rel_fro
 
@@ -50,7 +51,8 @@ def test_noalloc_matches_workspace_entry_point(dims, R):
     Ad = [torch.from_numpy(a).cuda() for a in A]
     plan = mk.Plan(dims, R, "simt")
     for k in range(len(dims)):
-        ref = plan.mttkrp(Yd, Ad, k).cpu().numpy()
+        ref = oracle.mttkrp(Y, A, k)
+        ws = plan.mttkrp(Yd, Ad, k).cpu().numpy()
         for call in range(2):
             out = torch.full((dims[k], R), float("nan"), device="cuda")
             rc = call_noalloc(fn, dims, R, Yd, Ad, k, out)
@@ -59,7 +61,9 @@ def test_noalloc_matches_workspace_entry_point(dims, R):
             got = out.cpu().numpy()
             assert np.isfinite(got).all()
             err = rel_fro(got, ref)
-            assert err <= TOL, f"{dims} R={R} mode {k} call {call}: {err:.3e}"
+            assert err <= TOL, f"{dims} R={R} mode {k} call {call}: {err:.3e} against the oracle"
+            err = rel_fro(got, ws)
+            assert err <= TOL, f"{dims} R={R} mode {k} call {call}: {err:.3e} against mttkrp()"
 
 
 def test_noalloc_rejects_problems_beyond_the_static_scratch():
