@@ -132,23 +132,36 @@ void layout_workspace(ModePlan& mp) {
     mp.total = off;
 }
 
-// fp16 images of Y (tc_img modes): one region after every mode's own needs, so
-// that the images written for the first such mode of a call serve the others
-void place_images(Plan& p) {
+// Plan-level workspace regions after every mode's own needs, shared by all
+// modes of a call: for fp16-split modes the largest |Y| of every slab of mode 0
+// (one slab when some fp16-split mode sums over mode 0 inside its tensor-memory
+// accumulation, i.e. has it in its inner group), then the fp16 images of Y
+// (tc_img modes) written for the first such mode of a call.
+void place_plan_regions(Plan& p) {
     size_t base = 0;
     p.img_nat = p.img_t = 0;
+    bool fp16 = false, slab_ok = true;
     for (int k = 0; k < p.d; ++k) {
         const ModePlan& mp = p.mode[k];
-        if (mp.path == MTTKRP_PATH_TC && mp.tc_img) {
-            if (mp.tc_img_t)
-                p.img_t = 1;
-            else
-                p.img_nat = 1;
+        if (mp.path == MTTKRP_PATH_TC && (mp.tc_img || mp.tc_h2)) {
+            fp16 = true;
+            if (k != 0 && !(mp.g.npm > 0 && mp.g.pm[0] == 0)) slab_ok = false;
+            if (mp.tc_img) {
+                if (mp.tc_img_t)
+                    p.img_t = 1;
+                else
+                    p.img_nat = 1;
+            }
         }
         if (mp.total > base) base = mp.total;
     }
-    if (!p.img_nat && !p.img_t) return;
+    p.slab_on = (fp16 && slab_ok && p.dims[0] > 1) ? 1 : 0;
+    p.nslab = p.slab_on ? p.dims[0] : 1;
+    p.off_slab = 0;
+    if (!fp16) return;
     base = align256(base);
+    p.off_slab = base;
+    base = align256(base + (size_t)p.nslab * sizeof(uint32_t));
     int64_t numel = 1;
     for (int n = 0; n < p.d; ++n) numel *= p.dims[n];
     const size_t img = 2 * align256((size_t)numel * 2);   // hi and lo, 2 bytes an element
@@ -157,7 +170,7 @@ void place_images(Plan& p) {
     const size_t total = off_t + (p.img_t ? img : 0);
     for (int k = 0; k < p.d; ++k) {
         ModePlan& mp = p.mode[k];
-        if (mp.path != MTTKRP_PATH_TC || !mp.tc_img) continue;
+        if (mp.path != MTTKRP_PATH_TC || !(mp.tc_img || mp.tc_h2)) continue;
         mp.off_img = off_nat;
         mp.off_timg = off_t;
         mp.total = total;
@@ -262,8 +275,17 @@ int run_mode(Plan& p, const float* Y, const float* const* factors, int k, float*
     float* gtab = reinterpret_cast<float*>(ws + mp.off_gtab);
     int64_t* basetab = reinterpret_cast<int64_t*>(ws + mp.off_base);
     cudaError_t err;
+    const bool fp16 = mp.path == MTTKRP_PATH_TC && (mp.tc_img || mp.tc_h2);
 
-    // 1. G table and base offsets of the pre indices
+    // 0. fp16 split: slab maxima of Y and the fp16 images (once per call)
+    if (fp16) {
+        int nlaunch = 0;
+        const int rc = tc_prepare(p, mp, Y, ws, stream, &nlaunch, g_errmsg, sizeof(g_errmsg));
+        p.launches += nlaunch;
+        if (rc != MTTKRP_OK) return rc;
+    }
+    // 1. G table and base offsets of the pre indices (fp16 split with per-slab
+    //    scales: rows scaled by s_global / s_slab, mode 0 being the first pre mode)
     {
         ProdTableArgs a;
         memset(&a, 0, sizeof(a));
@@ -277,6 +299,11 @@ int run_mode(Plan& p, const float* Y, const float* const* factors, int k, float*
         a.R = g.R;
         a.tab = gtab;
         a.base = basetab;
+        if (fp16 && p.slab_on && k != 0) {
+            a.slab_bits = reinterpret_cast<const uint32_t*>(ws + p.off_slab);
+            a.gmax_bits = reinterpret_cast<const uint32_t*>(ws);
+            a.slab_div = g.npre / p.nslab;
+        }
         if ((err = launch_prod_table(a, stream)) != cudaSuccess)
             return fail(MTTKRP_ERR_CUDA, "table launch: %s", cudaGetErrorString(err));
         ++p.launches;
@@ -405,7 +432,7 @@ int mttkrp_plan(int d, const int64_t* dims, int64_t R, mttkrp_plan_t* out) {
             return fail(rc, "planning mode %d failed", k);
         }
     }
-    place_images(*p);
+    place_plan_regions(*p);
     *out = reinterpret_cast<mttkrp_plan_t>(p);
     return MTTKRP_OK;
 }
@@ -425,7 +452,7 @@ int mttkrp_plan_set_path(mttkrp_plan_t h, int path) {
             return fail(rc, "mode %d cannot run on path %d", k, path);
         }
     }
-    place_images(*p);
+    place_plan_regions(*p);
     p->forced_path = path;
     return MTTKRP_OK;
 }

@@ -90,6 +90,13 @@ struct Plan {
     // fp16 images of Y (tc_img modes) already written for the current call's Y
     mutable int img_ready;
     int img_nat, img_t;   // which images the plan's tc_img modes read (natural, transposed)
+    // fp16 split: largest |Y| of every slab of mode 0 (fp32 bits) at off_slab in
+    // the workspace.  nslab = I_0 when every fp16-split mode of the plan takes
+    // per-slab scales (mode 0 is its output row or a pre mode), else 1 (one
+    // scale for the whole tensor).
+    int slab_on;
+    int64_t nslab;
+    size_t off_slab;
     // the last call on this plan was a CP-ALS sweep: max |Y| and the fp16 images
     // in the workspace are those of that sweep's Y
     int sweep_left_images;
@@ -113,6 +120,11 @@ struct ProdTableArgs {
     int64_t R;
     float* tab;
     int64_t* base;
+    // optional (fp16-split G tables with per-slab scales of Y): row t is also
+    // multiplied by s_global / s_slab(t / slab_div), a power of two <= 1
+    const uint32_t* slab_bits;
+    const uint32_t* gmax_bits;
+    int64_t slab_div;
 };
 
 struct SimtArgs {

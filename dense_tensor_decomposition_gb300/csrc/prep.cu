@@ -7,36 +7,49 @@
 //    when warps share the splits) and write the fp32 output; no atomics
 //    anywhere, so results are bitwise reproducible for a given plan.
 #include "internal.h"
+#include "scale.cuh"
 
 namespace mk {
 
-__global__ void prod_table_kernel(ProdTableArgs a) {
-    const int64_t n = a.rows * a.R;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t row = e / a.R;
-        const int64_t r = e - row * a.R;
-        int64_t rem = row;
-        int64_t base = 0;
-        float prod = 1.0f;
-        for (int m = a.nm - 1; m >= 0; --m) {
-            const int64_t idx = rem % a.dim[m];
-            rem /= a.dim[m];
-            prod *= a.fac[m][idx * a.R + r];
-            base += idx * a.ystride[m];
+// One warp per table row: the row's multi-index, Y offset and scale once, then
+// the R columns by the lanes (coalesced loads and stores).
+__global__ void __launch_bounds__(256) prod_table_kernel(ProdTableArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < a.rows;
+         row += nwarps) {
+        const float* frow[kMaxD];
+        int64_t rem = row, base = 0;
+#pragma unroll
+        for (int m = kMaxD - 1; m >= 0; --m) {
+            frow[m] = nullptr;
+            if (m < a.nm) {
+                const int64_t idx = rem % a.dim[m];
+                rem /= a.dim[m];
+                frow[m] = a.fac[m] + idx * a.R;
+                base += idx * a.ystride[m];
+            }
         }
-        a.tab[e] = prod;
-        if (a.base != nullptr && r == 0) a.base[row] = base;
+        float f = 1.f;
+        if (a.slab_bits != nullptr)
+            f = pow2_scale(*a.gmax_bits) * pow2_recip(slab_scale(a.slab_bits, row / a.slab_div, *a.gmax_bits));
+        float* out = a.tab + row * a.R;
+        for (int64_t r = lane; r < a.R; r += 32) {
+            float prod = 1.0f;
+#pragma unroll
+            for (int m = kMaxD - 1; m >= 0; --m)
+                if (m < a.nm) prod *= frow[m][r];
+            out[r] = prod * f;
+        }
+        if (a.base != nullptr && lane == 0) a.base[row] = base;
     }
 }
 
 cudaError_t launch_prod_table(const ProdTableArgs& a, cudaStream_t s) {
-    const int64_t n = a.rows * a.R;
-    if (n == 0) return cudaSuccess;
-    const int threads = 256;
-    int64_t blocks = (n + threads - 1) / threads;
+    if (a.rows * a.R == 0) return cudaSuccess;
+    int64_t blocks = (a.rows + 7) / 8;   // eight warps, one row each
     if (blocks > 152 * 16) blocks = 152 * 16;
-    prod_table_kernel<<<(unsigned)blocks, threads, 0, s>>>(a);
+    prod_table_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

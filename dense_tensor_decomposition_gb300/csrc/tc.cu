@@ -29,6 +29,7 @@
 #include <cstdio>
 #include <cstring>
 
+#include "scale.cuh"
 #include "tc.h"
 
 namespace mk {
@@ -91,6 +92,9 @@ struct TcArgs {
     int64_t batch_len;        // slots never cross a multiple of this pre index
     // two-term fp16 split only
     const uint32_t* ymax_bits;   // max |Y| as fp32 bits (device)
+    const uint32_t* slab_bits;   // max |Y| of every slab of mode 0 (one slab: the whole tensor)
+    int64_t slab_div;            // pre indices a slab (slab of pi = pi / slab_div)
+    int slab_rows;               // 1: the slab is the output row (mode 0, per-slab scales)
     const float* colscale;       // power-of-two scale of each Binner column (R)
     uint32_t* status;
 };
@@ -832,8 +836,8 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
                 // lo tile, elementwise at the same (swizzled) offsets as the raw tile
                 const float4* src = reinterpret_cast<const float4*>(st);
                 float4* dst = reinterpret_cast<float4*>(op);
-#pragma unroll
                 static_assert(INNER || (L::kY / 16) % kPT == 0, "whole rounds");
+#pragma unroll
                 for (int v = 0; v < (int)(L::kY / 16) / kPT; ++v) {
                     const int e = ptid + kPT * v;
                     const float4 x = src[e];
@@ -1603,25 +1607,17 @@ __device__ __forceinline__ uint32_t half2_bits(__half2 h) {
     return u;
 }
 
-// Power of two that maps the largest magnitude m (fp32 bits of a non-negative
-// value) into [2^13, 2^14): fp16 holds the scaled values with room to spare,
-// and their lo parts stay normal down to 2^-11 of the largest.  m = 0 or a
-// non-finite m: 1 (nothing to scale; non-finite values propagate).  Subnormal
-// m uses the exponent of its leading bit; the scale is clamped to the fp32 range.
-__device__ __forceinline__ float pow2_scale(uint32_t mbits) {
-    const uint32_t m = mbits & 0x7FFFFFFFu;
-    int e = (int)(m >> 23);                       // biased exponent
-    if (m == 0 || e == 255) return 1.f;
-    if (e == 0) e = 1 - (__clz((int)m) - 9);      // subnormal: leading bit of the mantissa
-    int se = 127 + 13 - (e - 127);               // biased exponent of 2^(13 - (e - 127))
-    se = se < 1 ? 1 : (se > 254 ? 254 : se);
-    return __uint_as_float((uint32_t)se << 23);
+// Scale of the Y entries of pre index pi, or of output row `row` when the slab
+// is the row; and the factor that undoes the scale of output row `row` at the
+// end (the global scale unless the slab is the row: G absorbs the rest).
+__device__ __forceinline__ float y_scale_pre(const TcArgs& a, int64_t pi) {
+    return slab_scale(a.slab_bits, pi / a.slab_div, *a.ymax_bits);
 }
-// 1 / x for x = 2^k with a biased exponent in [1, 254] (what pow2_scale
-// returns), exactly: 2^-k, subnormal (2^-127) for the largest x
-__device__ __forceinline__ float pow2_recip(float x) {
-    const uint32_t e = __float_as_uint(x) >> 23;
-    return __uint_as_float(e <= 253u ? (254u - e) << 23 : 0x00400000u);
+__device__ __forceinline__ float y_scale_row(const TcArgs& a, int64_t row) {
+    return slab_scale(a.slab_bits, row < a.I ? row : a.I - 1, *a.ymax_bits);
+}
+__device__ __forceinline__ float y_unscale(const TcArgs& a, int64_t row) {
+    return pow2_recip(a.slab_rows ? y_scale_row(a, row) : pow2_scale(*a.ymax_bits));
 }
 
 // D (+)= A * B, kind::f16, A (M=128 rows = lanes, 8 columns = 16 fp16 of K) in
@@ -1870,7 +1866,10 @@ __global__ void __launch_bounds__(kH2Threads, 1) tc_h2_kernel(const __grid_const
         // --------------- operand producers: one TMEM lane quadrant each ---------------
         const int quad = warp & 3;
         const int r = 32 * quad + lane;   // tile row of this thread
-        const float sy = pow2_scale(*a.ymax_bits);   // Y is scaled by this power of two
+        // Y is scaled by a power of two: per row (mode 0 with per-slab scales) or
+        // per pre index
+        const float sy_row = a.slab_rows ? y_scale_row(a, m0 + r) : 1.f;
+        float sy = sy_row;
         Ring<NR> rr;
         int ag = 0;          // A-slot group of the current K-step (ring of NG)
         int64_t g = 0;       // groups started so far
@@ -1878,6 +1877,7 @@ __global__ void __launch_bounds__(kH2Threads, 1) tc_h2_kernel(const __grid_const
         for (int jc = 0; jc < njc && ok; ++jc) {
             const int ck = chunk_len(jc);
             for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                if (!a.slab_rows) sy = y_scale_pre(a, pi);
                 for (int q = 0; q < ck; ++q, rr.next()) {
                     const bool gstart = q % kH2Group == 0;
                     const bool gend = q % kH2Group == kH2Group - 1 || q == ck - 1;
@@ -2020,7 +2020,7 @@ __global__ void __launch_bounds__(kH2Threads, 1) tc_h2_kernel(const __grid_const
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         if (!*abort_flag && row < a.I) {
             // undo the power-of-two scales of Y and of each Binner column (exact)
-            const float inv_y = pow2_recip(pow2_scale(*a.ymax_bits));
+            const float inv_y = y_unscale(a, row);
             float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride + row * a.R + c0;
             const bool vst = (a.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.dst) & 15) == 0);
 #pragma unroll
@@ -2412,14 +2412,13 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
             if (live) {
-                const float inv_y = pow2_recip(pow2_scale(*a.ymax_bits));
                 float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride;
                 for (int idx = tid - 32 * kImgEpiWarp0; idx < Iv * BN; idx += kEpiWarps * 32) {
                     const int i = idx / BN, c = idx - i * BN;
                     if (r0 + c >= a.R) continue;
                     float sum = 0.f;
                     for (int sl = 0; sl < a.ps; ++sl) sum += S[(sl * Iv + i) * kSP + c];
-                    dst[(int64_t)i * a.R + r0 + c] = sum * inv_y * pow2_recip(a.colscale[r0 + c]);
+                    dst[(int64_t)i * a.R + r0 + c] = sum * y_unscale(a, i) * pow2_recip(a.colscale[r0 + c]);
                 }
             }
         } else {
@@ -2479,7 +2478,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
         }
         if (!*abort_flag && row < a.I) {
             // undo the power-of-two scales of Y and of each Binner column (exact)
-            const float inv_y = pow2_recip(pow2_scale(*a.ymax_bits));
+            const float inv_y = y_unscale(a, row);
             float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride + row * a.R + c0;
             const bool vst = (a.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.dst) & 15) == 0);
 #pragma unroll
@@ -2511,38 +2510,63 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
     }
 }
 
-// Split Y into the fp16 images the kernel above streams: with x = Y * s (s the
-// power of two that takes max |Y| into [2^13, 2^14)), hi = fp16(x) and
-// lo = fp16(x - hi) (the difference is exact in fp32), same layout as Y.
-__global__ void __launch_bounds__(256) split_image_kernel(const float* __restrict__ y, int64_t n,
-                                                          const uint32_t* __restrict__ ymax_bits,
-                                                          __half* __restrict__ hi, __half* __restrict__ lo) {
-    const float sy = pow2_scale(*ymax_bits);
-    const int64_t n4 = n / 4;   // y, hi and lo are 16-byte aligned
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    auto split4 = [&](int64_t i, float4 v) {
-        const float x0 = v.x * sy, x1 = v.y * sy, x2 = v.z * sy, x3 = v.w * sy;
-        const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
-        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-        const __half2 l01 = __floats2half2_rn(x0 - f01.x, x1 - f01.y);
-        const __half2 l23 = __floats2half2_rn(x2 - f23.x, x3 - f23.y);
-        reinterpret_cast<uint2*>(hi)[i] = make_uint2(half2_bits(h01), half2_bits(h23));
-        reinterpret_cast<uint2*>(lo)[i] = make_uint2(half2_bits(l01), half2_bits(l23));
-    };
-    int64_t i = t0;
-    for (; i + stride < n4; i += 2 * stride) {   // two 16-byte loads in flight
-        const float4 a = __ldcs(reinterpret_cast<const float4*>(y) + i);
-        const float4 b = __ldcs(reinterpret_cast<const float4*>(y) + i + stride);
-        split4(i, a);
-        split4(i + stride, b);
+// Work units of the passes over Y that need a slab's scale: at most kSlabUnit
+// consecutive elements of one slab of mode 0 (nslab slabs of len elements; one
+// slab when the plan scales Y as a whole).  A block takes a contiguous run of
+// units, so it meets each slab in one stretch.
+constexpr int kSlabUnit = 8192;
+
+struct SlabUnits {
+    int64_t ups, u0, u1;   // units per slab, this block's units [u0, u1)
+    __device__ SlabUnits(int64_t nslab, int64_t len) {
+        ups = (len + kSlabUnit - 1) / kSlabUnit;
+        const int64_t n = nslab * ups;
+        const int64_t per = (n + gridDim.x - 1) / gridDim.x;
+        u0 = (int64_t)blockIdx.x * per;
+        u1 = u0 + per < n ? u0 + per : n;
     }
-    for (; i < n4; i += stride) split4(i, __ldcs(reinterpret_cast<const float4*>(y) + i));
-    for (int64_t i = 4 * n4 + t0; i < n; i += stride) {
-        const float x = y[i] * sy;
-        const __half h = __float2half_rn(x);
-        hi[i] = h;
-        lo[i] = __float2half_rn(x - __half2float(h));
+};
+
+// Split Y into the fp16 images the kernel above streams: with x = Y * s (s the
+// power of two of Y's slab of mode 0), hi = fp16(x) and lo = fp16(x - hi) (the
+// difference is exact in fp32), same layout as Y.  Units as in slabmax_kernel.
+__device__ __forceinline__ void split1(float v, float sy, __half& h, __half& l) {
+    const float x = v * sy;
+    h = __float2half_rn(x);
+    l = __float2half_rn(x - __half2float(h));
+}
+
+__global__ void __launch_bounds__(256) split_image_kernel(const float* __restrict__ y, int64_t nslab, int64_t len,
+                                                          const uint32_t* __restrict__ slab,
+                                                          const uint32_t* __restrict__ gmax,
+                                                          __half* __restrict__ hi, __half* __restrict__ lo) {
+    const SlabUnits su(nslab, len);
+    const uint32_t gbits = *gmax;
+    // y, hi and lo 16-byte aligned (the images are): whole units move as float4
+    const bool vec = (len % 4 == 0) && (reinterpret_cast<uintptr_t>(y) & 15) == 0;
+    for (int64_t u = su.u0; u < su.u1; ++u) {
+        const int64_t s = u / su.ups;
+        const float sy = slab_scale(slab, s, gbits);
+        const int64_t a0 = s * len + (u - s * su.ups) * kSlabUnit;
+        const int64_t a1 = min(a0 + kSlabUnit, (s + 1) * len);
+        if (vec && a1 - a0 == kSlabUnit) {
+            const int64_t f0 = a0 / 4 + threadIdx.x;
+            float4 v[kSlabUnit / 1024];
+#pragma unroll
+            for (int q = 0; q < kSlabUnit / 1024; ++q) v[q] = __ldcs(reinterpret_cast<const float4*>(y) + f0 + 256 * q);
+#pragma unroll
+            for (int q = 0; q < kSlabUnit / 1024; ++q) {
+                const float x0 = v[q].x * sy, x1 = v[q].y * sy, x2 = v[q].z * sy, x3 = v[q].w * sy;
+                const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+                const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                const __half2 l01 = __floats2half2_rn(x0 - f01.x, x1 - f01.y);
+                const __half2 l23 = __floats2half2_rn(x2 - f23.x, x3 - f23.y);
+                reinterpret_cast<uint2*>(hi)[f0 + 256 * q] = make_uint2(half2_bits(h01), half2_bits(h23));
+                reinterpret_cast<uint2*>(lo)[f0 + 256 * q] = make_uint2(half2_bits(l01), half2_bits(l23));
+            }
+        } else {
+            for (int64_t i = a0 + threadIdx.x; i < a1; i += blockDim.x) split1(__ldcs(y + i), sy, hi[i], lo[i]);
+        }
     }
 }
 
@@ -2553,17 +2577,32 @@ __global__ void __launch_bounds__(256) split_image_kernel(const float* __restric
 // multiple of 4), converts, optionally writes the natural images (8-byte
 // stores), and parks (hi | lo << 16) in shared memory; then each warp writes
 // rows of 64 consecutive p of both transposed images (4-byte stores, P even).
+// Rows p of the P x I view belong to slab p / rps of mode 0 (rps rows a slab).
 template <bool VEC>
 __global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restrict__ y, int64_t P, int64_t I,
-                                                            const uint32_t* __restrict__ ymax_bits,
+                                                            const uint32_t* __restrict__ slab,
+                                                            const uint32_t* __restrict__ gmax, int64_t rps,
                                                             __half* __restrict__ hi, __half* __restrict__ lo,
                                                             __half* __restrict__ thi, __half* __restrict__ tlo,
                                                             int write_nat) {
     constexpr int TP = 64, TI = 128;
     __shared__ uint32_t sh[TI][TP + 1];   // [i][p]: hi in the low half, lo in the high half
-    const float sy = pow2_scale(*ymax_bits);
+    const uint32_t gbits = *gmax;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // scale of row pr of the tile starting at row p0: a tile of TP rows meets at
+    // most two slabs when a slab has at least TP rows
+    int64_t s_b1 = 0;
+    float s_sy0 = 1.f, s_sy1 = 1.f;
+    auto tile_scales = [&](int64_t p0) {
+        const int64_t s0 = p0 / rps;
+        s_b1 = (s0 + 1) * rps;
+        s_sy0 = slab_scale(slab, s0, gbits);
+        s_sy1 = s_b1 < P ? slab_scale(slab, s0 + 1, gbits) : s_sy0;
+    };
+    auto row_scale = [&](int64_t pr) -> float {   // rows past P (tile padding) clamp to the last
+        return rps >= TP ? (pr >= s_b1 ? s_sy1 : s_sy0) : slab_scale(slab, (pr < P ? pr : P - 1) / rps, gbits);
+    };
     if (I < TI / 2) {
         // short rows: TP consecutive p are one contiguous block of TP * I values,
         // read (and written in the natural layout) flat, so that no lanes idle
@@ -2572,6 +2611,7 @@ __global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restr
         for (int64_t t = blockIdx.x; t < np; t += gridDim.x) {
             const int64_t p0 = t * TP;
             const int rows = (int)(P - p0 < TP ? P - p0 : TP);
+            tile_scales(p0);
             const int nvals = rows * Ii;
             const int64_t base = p0 * I;
             for (int f = threadIdx.x; 4 * f < nvals; f += blockDim.x) {
@@ -2590,7 +2630,7 @@ __global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restr
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int idx = 4 * f + q;
-                    const float x = v[q] * sy;
+                    const float x = v[q] * row_scale(p0 + idx / Ii);
                     const __half h = __float2half_rn(x);
                     const __half l = __float2half_rn(x - __half2float(h));
                     hb[q] = __half_as_ushort(h);
@@ -2633,6 +2673,7 @@ __global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restr
     for (int64_t t = blockIdx.x; t < np * ni; t += gridDim.x) {
         const int64_t p0 = (t / ni) * TP, i0 = (t % ni) * TI;
         const int64_t ib = i0 + 4 * lane;   // this lane's first i
+        tile_scales(p0);
         // all eight rows' loads first (eight 16-byte loads in flight a thread)
         float vv[TP / 8][4];
 #pragma unroll
@@ -2663,6 +2704,7 @@ __global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restr
             const int64_t pr = p0 + r;
             const int64_t e = pr * I + ib;
             const float* v = vv[u];
+            const float sy = row_scale(pr);
             uint32_t hb[4], lb[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -2765,32 +2807,65 @@ __global__ void tc_bimage_kernel(BImgArgs a) {
     }
 }
 
-// max |Y| over n fp32 values as fp32 bits (non-negative floats order like their
-// bits); *out must be zero before the launch.
-__global__ void __launch_bounds__(256) absmax_kernel(const float* __restrict__ y, int64_t n,
-                                                     uint32_t* __restrict__ out) {
-    uint32_t m = 0;
-    const bool vec = (reinterpret_cast<uintptr_t>(y) & 15) == 0;
-    const int64_t n4 = vec ? n / 4 : 0;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
-        const float4 v = __ldcs(reinterpret_cast<const float4*>(y) + i);
-        m = max(m, __float_as_uint(fabsf(v.x)));
-        m = max(m, __float_as_uint(fabsf(v.y)));
-        m = max(m, __float_as_uint(fabsf(v.z)));
-        m = max(m, __float_as_uint(fabsf(v.w)));
-    }
-    for (int64_t i = 4 * n4 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
-        m = max(m, __float_as_uint(fabsf(y[i])));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+// Largest magnitude of every slab of mode 0 (slab[s]) and of the whole tensor
+// (*gmax), as fp32 bits (non-negative floats order like their bits).  Each block
+// flushes its running maximum with one atomicMax per slab it touches and one on
+// *gmax at the end.  slab[] and *gmax must be zero before the launch.
+__global__ void __launch_bounds__(256) slabmax_kernel(const float* __restrict__ y, int64_t nslab, int64_t len,
+                                                      uint32_t* __restrict__ slab, uint32_t* __restrict__ gmax) {
     __shared__ uint32_t wm[8];
-    if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = max(m, wm[w]);
-        atomicMax(out, m);
+    const SlabUnits su(nslab, len);
+    const bool vec = (len % 4 == 0) && (reinterpret_cast<uintptr_t>(y) & 15) == 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t m = 0, g = 0;
+    auto block_max = [&](uint32_t v) -> uint32_t {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == 0) wm[warp] = v;
+        __syncthreads();
+        uint32_t r = wm[0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) r = max(r, wm[w]);
+        __syncthreads();
+        return r;
+    };
+    int64_t cur = -1;
+    for (int64_t u = su.u0; u < su.u1; ++u) {
+        const int64_t s = u / su.ups;   // the same for every thread of the block
+        if (s != cur) {
+            if (cur >= 0) {
+                const uint32_t b = block_max(m);
+                if (threadIdx.x == 0 && b) atomicMax(slab + cur, b);
+                g = max(g, b);
+            }
+            m = 0;
+            cur = s;
+        }
+        const int64_t a0 = s * len + (u - s * su.ups) * kSlabUnit;
+        const int64_t a1 = min(a0 + kSlabUnit, (s + 1) * len);
+        if (vec && a1 - a0 == kSlabUnit) {
+            // a whole unit: eight 16-byte loads in flight a thread
+            const float4* p = reinterpret_cast<const float4*>(y + a0) + threadIdx.x;
+            float4 v[kSlabUnit / 1024];
+#pragma unroll
+            for (int q = 0; q < kSlabUnit / 1024; ++q) v[q] = __ldcs(p + 256 * q);
+#pragma unroll
+            for (int q = 0; q < kSlabUnit / 1024; ++q) {
+                m = max(m, __float_as_uint(fabsf(v[q].x)));
+                m = max(m, __float_as_uint(fabsf(v[q].y)));
+                m = max(m, __float_as_uint(fabsf(v[q].z)));
+                m = max(m, __float_as_uint(fabsf(v[q].w)));
+            }
+        } else {
+            for (int64_t i = a0 + threadIdx.x; i < a1; i += blockDim.x) m = max(m, __float_as_uint(fabsf(y[i])));
+        }
     }
+    if (cur >= 0) {
+        const uint32_t b = block_max(m);
+        if (threadIdx.x == 0 && b) atomicMax(slab + cur, b);
+        g = max(g, b);
+    }
+    if (threadIdx.x == 0 && g) atomicMax(gmax, g);
 }
 
 // Power-of-two scale of each Binner column: max_j |Binner(j, r)| is the product
@@ -3281,6 +3356,76 @@ bool tc_plan(const Plan& p, ModePlan& mp, bool allow_fp16) {
     return true;
 }
 
+int tc_prepare(const Plan& p, const ModePlan& mp, const float* Y, void* ws, cudaStream_t stream, int* nlaunch,
+               char* errbuf, size_t errlen) {
+    *nlaunch = 0;
+    if (!(mp.tc_h2 || mp.tc_img)) return MTTKRP_OK;
+    if ((reinterpret_cast<uintptr_t>(Y) & 15) != 0) {
+        snprintf(errbuf, errlen, "tensor-core path needs a 16-byte aligned Y");
+        return MTTKRP_ERR_INVALID;
+    }
+    uint8_t* ws_base = static_cast<uint8_t*>(ws);
+    uint32_t* ymax = reinterpret_cast<uint32_t*>(ws_base);   // reserved first bytes
+    uint32_t* slab = reinterpret_cast<uint32_t*>(ws_base + p.off_slab);
+    int64_t numel = 1;
+    for (int t = 0; t < p.d; ++t) numel *= p.dims[t];
+    const int64_t slab_len = numel / p.nslab;
+    cudaError_t e = cudaSuccess;
+    if (!p.ymax_ready) {
+        // largest magnitude of every slab of mode 0 and of the whole tensor
+        e = cudaMemsetAsync(ymax, 0, sizeof(uint32_t), stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(slab, 0, (size_t)p.nslab * sizeof(uint32_t), stream);
+        if (e == cudaSuccess) {
+            int64_t blocks = cdiv64(cdiv64(slab_len, kSlabUnit) * p.nslab, 4);
+            if (blocks > 152 * 8) blocks = 152 * 8;
+            slabmax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, p.nslab, slab_len, slab, ymax);
+            e = cudaGetLastError();
+        }
+        if (e == cudaSuccess) {
+            p.ymax_ready = 1;
+            ++*nlaunch;
+        }
+    }
+    if (e == cudaSuccess && mp.tc_img && !p.img_ready) {
+        // every image the plan's tc_img modes read, in one pass over Y
+        const size_t img_half = ((size_t)numel * 2 + 255) / 256 * 256;
+        __half* img_hi = reinterpret_cast<__half*>(ws_base + mp.off_img);
+        __half* img_lo = reinterpret_cast<__half*>(ws_base + mp.off_img + img_half);
+        __half* timg_hi = reinterpret_cast<__half*>(ws_base + mp.off_timg);
+        __half* timg_lo = reinterpret_cast<__half*>(ws_base + mp.off_timg + img_half);
+        if (p.img_t) {
+            const int64_t In = p.dims[p.d - 1];
+            const int64_t P = numel / In;
+            int64_t blocks = cdiv64(P, 64) * cdiv64(In, 128);
+            if (blocks > 152 * 16) blocks = 152 * 16;
+            // (I_{d-1} < 64: whole rows per tile, read flat; the 16-byte
+            // alignment of every tile start holds because tiles are 64 rows)
+            const int64_t rps = P / p.nslab;
+            if (In % 4 == 0)
+                split_image_t_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(
+                    Y, P, In, slab, ymax, rps, img_hi, img_lo, timg_hi, timg_lo, p.img_nat);
+            else
+                split_image_t_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(
+                    Y, P, In, slab, ymax, rps, img_hi, img_lo, timg_hi, timg_lo, p.img_nat);
+        } else {
+            int64_t blocks = cdiv64(cdiv64(slab_len, kSlabUnit) * p.nslab, 4);
+            if (blocks > 152 * 8) blocks = 152 * 8;
+            split_image_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, p.nslab, slab_len, slab, ymax, img_hi,
+                                                                     img_lo);
+        }
+        e = cudaGetLastError();
+        if (e == cudaSuccess) {
+            p.img_ready = 1;
+            ++*nlaunch;
+        }
+    }
+    if (e != cudaSuccess) {
+        snprintf(errbuf, errlen, "fp16 split pass: %s", cudaGetErrorString(e));
+        return MTTKRP_ERR_CUDA;
+    }
+    return MTTKRP_OK;
+}
+
 int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const* factors,
            const float* gtab, const int64_t* basetab, void* binner_ws, float* dst,
            cudaStream_t stream, int* nlaunch, cudaEvent_t* start_ev, char* errbuf, size_t errlen) {
@@ -3352,59 +3497,19 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     float* bimg = static_cast<float*>(binner_ws);
     float* colscale = reinterpret_cast<float*>(static_cast<uint8_t*>(binner_ws) + colscale_offset(mp));
     // the first bytes of the workspace (reserved region) hold max |Y| as fp32 bits
-    uint32_t* ymax = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(binner_ws) - mp.off_binner);
+    uint32_t* ymax = reinterpret_cast<uint32_t*>(ws_base);
     if (mp.tc_h2 || mp.tc_img) {
-        cudaError_t e = cudaSuccess;
-        if (!p.ymax_ready) e = cudaMemsetAsync(ymax, 0, sizeof(uint32_t), stream);
-        if (e == cudaSuccess && !p.ymax_ready) {
-            int64_t blocks = cdiv64(numel / 4 + 1, 256);
-            if (blocks > 152 * 8) blocks = 152 * 8;
-            absmax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, numel, ymax);
-            e = cudaGetLastError();
-            if (e == cudaSuccess) {
-                p.ymax_ready = 1;
-                ++*nlaunch;
-            }
+        ColScaleArgs c;
+        memset(&c, 0, sizeof(c));
+        c.ngroup = g.ngroup;
+        for (int t = 0; t < g.ngroup; ++t) {
+            c.gdim[t] = p.dims[g.group[t]];
+            c.gfac[t] = factors[g.group[t]];
         }
-        if (e == cudaSuccess && mp.tc_img && !p.img_ready) {
-            // every image the plan's tc_img modes read, in one pass over Y
-            if (p.img_t) {
-                const int64_t In = p.dims[p.d - 1];
-                const int64_t P = numel / In;
-                int64_t blocks = cdiv64(P, 64) * cdiv64(In, 128);
-                if (blocks > 152 * 16) blocks = 152 * 16;
-                // (I_{d-1} < 64: whole rows per tile, read flat; the 16-byte
-                // alignment of every tile start holds because tiles are 64 rows)
-                if (In % 4 == 0)
-                    split_image_t_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(Y, P, In, ymax, img_hi, img_lo,
-                                                                                     timg_hi, timg_lo, p.img_nat);
-                else
-                    split_image_t_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(Y, P, In, ymax, img_hi, img_lo,
-                                                                                      timg_hi, timg_lo, p.img_nat);
-            } else {
-                int64_t blocks = cdiv64(numel / 4 + 1, 256);
-                if (blocks > 152 * 8) blocks = 152 * 8;
-                split_image_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, numel, ymax, img_hi, img_lo);
-            }
-            e = cudaGetLastError();
-            if (e == cudaSuccess) {
-                p.img_ready = 1;
-                ++*nlaunch;
-            }
-        }
-        if (e == cudaSuccess) {
-            ColScaleArgs c;
-            memset(&c, 0, sizeof(c));
-            c.ngroup = g.ngroup;
-            for (int t = 0; t < g.ngroup; ++t) {
-                c.gdim[t] = p.dims[g.group[t]];
-                c.gfac[t] = factors[g.group[t]];
-            }
-            c.R = g.R;
-            c.out = colscale;
-            colscale_kernel<<<(unsigned)cdiv64(g.R, 32), 1024, 0, stream>>>(c);
-            e = cudaGetLastError();
-        }
+        c.R = g.R;
+        c.out = colscale;
+        colscale_kernel<<<(unsigned)cdiv64(g.R, 32), 1024, 0, stream>>>(c);
+        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) {
             snprintf(errbuf, errlen, "scale launch: %s", cudaGetErrorString(e));
             return MTTKRP_ERR_CUDA;
@@ -3467,6 +3572,9 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
                                        (mp.tc_small ? (uint32_t)(g.I * mp.tc_ps) : (uint32_t)kBM)
                                  : (uint32_t)mp.tc_kw * 4u * (mp.tc_small ? (uint32_t)(g.I * mp.tc_ps) : (uint32_t)kBM);
     args.ymax_bits = ymax;
+    args.slab_bits = reinterpret_cast<const uint32_t*>(ws_base + p.off_slab);
+    args.slab_rows = (p.slab_on && g.k == 0) ? 1 : 0;
+    args.slab_div = (p.slab_on && g.k != 0) ? g.npre / p.nslab : g.npre;
     args.colscale = colscale;
     {
         int n = g_withhold_signal.load();

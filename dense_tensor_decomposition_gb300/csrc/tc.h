@@ -13,6 +13,12 @@ bool tc_prefer(const ModePlan& mp);
 // Fill tiles and split counts for the tensor-core path; false if unsupported.
 // allow_fp16 = false keeps the mode on the 3xTF32 kernels.
 bool tc_plan(const Plan& p, ModePlan& mp, bool allow_fp16);
+// Enqueue the passes over Y that an fp16-split mode needs before its tables are
+// built: the largest magnitude of every slab of mode 0 and of the whole tensor
+// (once per call), and the fp16 images of Y (tc_img modes, once per call).
+// ws is the workspace base; *nlaunch receives the number of kernels enqueued.
+int tc_prepare(const Plan& p, const ModePlan& mp, const float* Y, void* ws, cudaStream_t stream, int* nlaunch,
+               char* errbuf, size_t errlen);
 // Enqueue the tensor-core work of one mode (tables are already built).
 // *nlaunch receives the number of kernels enqueued.  If start_ev is non-null,
 // *start_ev is re-recorded just before the main kernel (after the tensor-core
