@@ -12,10 +12,17 @@ inputs resident in HBM.  Prints one JSON line (rank 0):
                of step t + 1 overlaps the computation of step t
                (serial_ms_per_step: one after another)
   roofline     the main contraction kernel: algorithmic flops per launch over its
-               average CUDA-event duration, against the pipe's peak
+               average CUDA-event duration, against the pipe's peak; call_frac:
+               the whole all-modes call against the same roofline
+  peaks_probe  fp32 FMA, tcgen05 kind::tf32 and kind::f16 rates measured in this
+               run by the library's probe kernels, with the SM clock seen
+  per_workload all five workloads (and the largest on the 3xTF32 kernels): per
+               mode the kernel, its time, GFLOP/s and roofline fraction
+               (t_roof = max(flops / that kernel's pipe peak, algorithmic bytes /
+               HBM bandwidth)), and the all-modes time and fraction
   cpu_baseline the fp64 oracle on a bounded sample, on this host's cores
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4] [--path auto|simt|tc]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4] [--path auto|simt|tc|tc_tf32]
   python bench.py --impl reference ...   # the oracle on the host cores, same metric
 
 N > 1 (torchrun): every rank runs the whole workload on its own GPU (replicas;
@@ -44,6 +51,7 @@ import synth  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 SM_MAX_MHZ_FALLBACK = 2070.0
 # nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): tf32 1.1 PFLOP/s
+# (used only when the tf32 probe could not run)
 TF32_OVER_BF16 = 1.1 / 2.25
 
 
@@ -54,7 +62,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="4")
-    ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc", "tc_tf32"])
+    ap.add_argument("--no-workload-sweep", action="store_true",
+                    help="skip the per-workload block (all five workloads, per mode)")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cp-als", type=int, default=0, metavar="SWEEPS",
@@ -63,6 +73,9 @@ def parse_args():
     ap.add_argument("--ttm", type=int, default=-1, metavar="J",
                     help="instead: time the dense mode-n product X x_k M_k along every mode with J x I_k "
                          "matrices (J = 0: square, J = I_k)")
+    ap.add_argument("--explicit-krp", action="store_true",
+                    help="instead: the matrix-based variant (explicit Khatri-Rao product) against the "
+                         "matrix-free one on several workloads: time per mode and workspace bytes")
     ap.add_argument("--rotations", action="store_true",
                     help="instead: time Givens rotations (a full group of disjoint pairs) along every mode")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -333,6 +346,141 @@ def run_reference(args, w):
 # GPU side
 # ---------------------------------------------------------------------------
 
+def kernel_name(plan, k):
+    """The planner's kernel for mode k (family.layout[.small].bn<columns>)."""
+    for tok in plan.describe(k).split():
+        if tok.startswith("kernel="):
+            return tok[len("kernel="):]
+    return "unknown"
+
+
+def kernel_kind(name):
+    """Arithmetic of a kernel: fp16x2 (two-term fp16 split on the tensor cores),
+    tf32x3 (3xTF32 on the tensor cores) or f32 (fp32 FMA on the CUDA cores)."""
+    return {"img": "fp16x2", "h2": "fp16x2", "tf32": "tf32x3", "tf32tm": "tf32x3"}.get(name.split(".")[0], "f32")
+
+
+def probe_peaks(device, sms):
+    """Rates of the library's probe kernels in this run (TFLOP/s), with the SM
+    clock sampled while they run: an fp32 FMA chain on every SM, and one CTA
+    per SM issuing tcgen05 MMAs (M128 N256) of kind::tf32 and kind::f16."""
+    import torch
+    import dense_tensor_decomposition_gb300 as mk
+    stream = torch.cuda.current_stream(device)
+    out = torch.empty(sms * 8 * 256, device=device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+
+    def rate(launch, flops, seconds=0.3):
+        launch()
+        torch.cuda.synchronize(device)
+        n = 1
+        while True:
+            e0.record(stream)
+            for _ in range(n):
+                launch()
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+            ms = e0.elapsed_time(e1)
+            if ms >= seconds * 1e3 or n >= 1 << 14:
+                return flops * n / (ms * 1e-3) / 1e12
+            n = int(min(1 << 14, n * max(2.0, seconds * 1e3 / max(ms, 1e-3))))
+
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    time.sleep(0.3)
+    fma_iters, mma_iters = 16384, 8192
+    res = {
+        "fp32_fma_tflops": rate(lambda: mk.probe_fma(sms * 8, fma_iters, out),
+                                16.0 * fma_iters * sms * 8 * 256),
+        "tf32_mma_tflops": rate(lambda: mk.probe_mma("tf32", sms, mma_iters, device),
+                                2.0 * 128 * 256 * 8 * mma_iters * sms),
+        "f16_mma_tflops": rate(lambda: mk.probe_mma("f16", sms, mma_iters, device),
+                               2.0 * 128 * 256 * 16 * mma_iters * sms),
+    }
+    res = {k: round(v, 2) for k, v in res.items()}
+    res["clocks"] = clocks.stop()
+    res["status"] = mk.device_status()
+    res["how"] = (f"fp32: {sms * 8} blocks x 256 threads x {fma_iters} iterations of 8 FMA chains; "
+                  f"tensor: {sms} CTAs (one per SM) x {mma_iters} back-to-back tcgen05.mma M128 N256 "
+                  f"(tf32 K8, f16 K16); CUDA events, about 0.3 s each")
+    return res
+
+
+def kind_peaks(peaks, probe, sms):
+    """TFLOP/s of one fp32-accurate product per kind: fp16x2 = the driver-measured
+    bf16 dense burst / 3 (fp16 and bf16 share the rate), tf32x3 = the tf32 probe
+    / 3, f32 = the FMA probe (fallbacks: bf16 x nominal 1.1/2.25 / 3, and
+    SMs x 128 x 2 x max clock)."""
+    fp16 = peaks["bf16_tflops"] / 3.0
+    tf32 = (probe["tf32_mma_tflops"] if probe else peaks["bf16_tflops"] * TF32_OVER_BF16) / 3.0
+    f32 = probe["fp32_fma_tflops"] if probe else sms * 128 * 2 * peaks.get("sm_max_mhz", SM_MAX_MHZ_FALLBACK) / 1e6
+    return {"fp16x2": fp16, "tf32x3": tf32, "f32": f32}
+
+
+def roofline_ms(w, k, kind, kpk, hbm_gbs):
+    """t_roof of mode k: the slower of its flops at its pipe's peak and its
+    algorithmic bytes at the HBM bandwidth; and which one it is."""
+    t_flop = w.flops_per_mode() / (kpk[kind] * 1e12) * 1e3
+    t_hbm = w.bytes_per_mode(k) / (hbm_gbs * 1e9) * 1e3
+    return max(t_flop, t_hbm), ("hbm" if t_hbm > t_flop else ("alu" if kind == "f32" else "tensor"))
+
+
+def workload_sweep(device, kpk, hbm_gbs, cases):
+    """Every mode of each (workload, path) in `cases`: the main kernel's CUDA-event
+    time (median over calls), GFLOP/s and roofline fraction per mode, and the
+    whole all-modes call (median of per-call events; workloads that fit in L2
+    get a 512 MiB L2 flush before every call)."""
+    import torch
+    import dense_tensor_decomposition_gb300 as mk
+    stream = torch.cuda.current_stream(device)
+    out = []
+    for idx, path in cases:
+        w = synth.workload(idx)
+        Y = torch.from_numpy(synth.make_tensor(w)).to(device)
+        A = [torch.from_numpy(a).to(device) for a in synth.make_factors(w)]
+        M = [torch.empty(n, w.R, device=device) for n in w.dims]
+        plan = mk.Plan(w.dims, w.R, path)
+        plan.attach_workspace(device)
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=device) if Y.numel() * 4 <= L2_BYTES else None
+        for _ in range(3):
+            plan.all_modes(Y, A, outs=M)
+        torch.cuda.synchronize(device)
+        reps = 20 if w.numel <= 1 << 24 else 5
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        plan.set_timing(True)
+        for r in range(reps):
+            if flush is not None:
+                flush.fill_(r & 255)
+            evs[r][0].record(stream)
+            plan.all_modes(Y, A, outs=M)
+            evs[r][1].record(stream)
+        torch.cuda.synchronize(device)
+        ms_all = statistics.median(a.elapsed_time(b) for a, b in evs)
+        modes, roof_sum, kern_sum = [], 0.0, 0.0
+        for k in range(w.d):
+            kt = statistics.median(plan.kernel_times(k))
+            name = kernel_name(plan, k)
+            kind = kernel_kind(name)
+            t_roof, bound = roofline_ms(w, k, kind, kpk, hbm_gbs)
+            roof_sum += t_roof
+            kern_sum += kt
+            modes.append({"mode": k, "kernel": name, "ms": round(kt, 4),
+                          "gflops": round(w.flops_per_mode() / (kt * 1e-3) / 1e9, 1),
+                          "t_roof_ms": round(t_roof, 4), "bound": bound, "frac": round(t_roof / kt, 3)})
+        plan.set_timing(False)
+        out.append({"workload": w.name, "path": path, "dims": list(w.dims), "R": w.R,
+                    "ms_all_modes": round(ms_all, 4),
+                    "gflops_all_modes": round(w.d * w.flops_per_mode() / (ms_all * 1e-3) / 1e9, 1),
+                    "frac_all_modes": round(roof_sum / ms_all, 3),
+                    "ms_main_kernels": round(kern_sum, 4),
+                    "l2": "flushed before every call" if flush is not None else "Y larger than L2",
+                    "modes": modes})
+        del Y, A, M, plan, flush
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -445,47 +593,46 @@ def run_ours(args, w):
             dist.destroy_process_group()
         return
 
-    # ---- roofline of the main contraction kernel ----
+    # ---- peaks measured in this run, roofline of the main contraction kernel ----
     peaks, peak_src = measured_peaks()
+    props = torch.cuda.get_device_properties(device)
+    sms = props.multi_processor_count
+    try:
+        probe = probe_peaks(device, sms)
+    except Exception as e:  # the probes are context; the bench line stands without them
+        probe = {"error": str(e)[:200]}
+    kpk = kind_peaks(peaks, probe if "error" not in probe else None, sms)
     path = plan.mode_path(0)
+    names = [kernel_name(plan, k) for k in range(w.d)]
+    kinds = [kernel_kind(n) for n in names]
     kern_ms = statistics.mean(kern) if kern else None
     achieved_tflops = (w.flops_per_mode() / (kern_ms * 1e-3) / 1e12) if kern_ms else None
-    props = torch.cuda.get_device_properties(device)
+    # the modes' pipes, flop-weighted (every mode has the same flops): the time
+    # all modes would take at their pipes' peaks, per mode
+    flops = w.flops_per_mode()
+    t_peak = sum(flops / (kpk[kd] * 1e12) for kd in kinds)
+    peak = w.d * flops / t_peak / 1e12
+    bound = "alu" if set(kinds) == {"f32"} else "tensor"
+    roof_ms = [roofline_ms(w, k, kinds[k], kpk, peaks["hbm_gbs"])[0] for k in range(w.d)]
+    call_frac = sum(roof_ms) / ms_per_step
     frac_sustained = None
-    # arithmetic of the tensor-core kernel each mode runs on
-    kinds = ["fp16x2" if "tc_fp16x2=1" in plan.describe(k) else "tf32x3" for k in range(w.d)]
-    if path == "tc":
-        # burst figure: the timed region is tens of milliseconds at full SM clock.
-        # fp16 split: 3 kind::f16 products per fp32-accurate product at the
-        # bf16/fp16 dense rate; tf32 split: 3 kind::tf32 products at the tf32
-        # rate (measured bf16 x nominal 1.1/2.25).  Mixed plans: flop-weighted.
-        def peak_of(kind, base):
-            return base / 3.0 if kind == "fp16x2" else base * TF32_OVER_BF16 / 3.0
-        flops = [w.flops_per_mode() for _ in range(w.d)]
-        def weighted(base):
-            t = sum(f / (peak_of(kd, base) * 1e12) for f, kd in zip(flops, kinds))
-            return sum(flops) / t / 1e12
-        peak = weighted(peaks["bf16_tflops"])
-        sustained = weighted(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
-        bound = "tensor"
-        peak_note = ("fp32-accurate products on tensor cores, per mode: "
-                     + ", ".join(kinds)
-                     + f"; fp16x2 = bf16 dense burst {peak_src} / 3 products, "
-                       f"tf32x3 = bf16 dense burst {peak_src} x 1.1/2.25 / 3 products")
-        if achieved_tflops:
-            frac_sustained = round(achieved_tflops / sustained, 4)
-    else:
-        sm_mhz = peaks.get("sm_max_mhz", SM_MAX_MHZ_FALLBACK)
-        peak = props.multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
-        bound = "alu"
-        peak_note = (f"fp32 FMA pipe: {props.multi_processor_count} SMs x 128 lanes x 2 flops x "
-                     f"{sm_mhz:.0f} MHz (max SM clock)")
+    if "fp16x2" in kinds and achieved_tflops:
+        sus = dict(kpk, fp16x2=peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) / 3.0)
+        frac_sustained = round(achieved_tflops / (w.d * flops / sum(flops / (sus[kd] * 1e12) for kd in kinds)
+                                                  / 1e12), 4)
+    peak_note = ("per mode " + ", ".join(f"{n} ({kd})" for n, kd in zip(names, kinds))
+                 + f"; fp16x2 = bf16 dense burst ({peak_src}) / 3 products; tf32x3 = tcgen05 kind::tf32 probe"
+                   f" / 3 products; f32 = fp32 FMA probe (peaks_probe; nominal fallbacks if it failed)")
     main_src = kernel_source_hash(MAIN_KERNEL_SOURCES.get(path, ()))
     traffic = recorded_traffic(w.name, path, main_src)
     roofline = {"bound": bound, "achieved": round(achieved_tflops, 3) if achieved_tflops else None,
                 "peak": round(peak, 3), "unit": "TFLOP/s",
                 "frac": round(achieved_tflops / peak, 4) if achieved_tflops else None,
                 "traffic": traffic, "peak_source": peak_note,
+                "call_frac": round(call_frac, 4),
+                "call_frac_note": "all-modes call (every kernel of the step) against the same roofline: "
+                                  "sum over modes of max(flops / pipe peak, algorithmic bytes / HBM) "
+                                  "over ms_per_step",
                 "frac_vs_sustained_peak": frac_sustained,
                 "kernel_ms_mean": round(kern_ms, 4) if kern_ms else None,
                 "kernel_launches_timed": len(kern),
@@ -493,6 +640,10 @@ def run_ours(args, w):
                 "hbm_gbs_at_algorithmic_bytes":
                     round(max(w.bytes_per_mode(k) for k in range(w.d)) / (kern_ms * 1e-3) / 1e9, 1)
                     if kern_ms else None}
+    sweep = None
+    if not args.no_workload_sweep:
+        sweep = workload_sweep(device, kpk, peaks["hbm_gbs"],
+                               [(i, "auto") for i in (1, 2, 3, 4, 5)] + [(w.index, "tc_tf32")])
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -503,7 +654,7 @@ def run_ours(args, w):
         "value": round(value, 2), "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("+".join(sorted(set(kinds))) if path == "tc" else "f32"), "data": "synthetic",
+        "dtype": "+".join(sorted(set(kinds))), "data": "synthetic",
         "config": {"workload": w.name, "dims": list(w.dims), "R": w.R, "modes": w.d,
                    "path": path, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 (Y {Y.nbytes >> 20} MiB > 129 MB)"
@@ -514,6 +665,8 @@ def run_ours(args, w):
                 "steps": args.e2e_steps, "copies": "overlapped with the previous step's compute",
                 "serial_ms_per_step": round(serial_ms, 3)},
         "roofline": roofline,
+        "peaks_probe": probe,
+        "per_workload": sweep,
         "cpu_baseline": cpu,
         "clocks": clk,
         "gpu_launches": launches,
@@ -700,11 +853,74 @@ def run_ttm(args, w):
     }))
 
 
+def run_explicit_krp(args):
+    """The matrix-based variant (MTTKRP_PATH_TC_EXPLICIT_KRP: the Khatri-Rao
+    product of every mode but k formed in the workspace, then multiplied on the
+    tensor cores) against the matrix-free planner choice, on 256^3, 128^4, 20^6
+    and 512^3: all-modes time, per-mode main-kernel time and workspace bytes by
+    purpose.  One JSON line."""
+    import torch
+    import dense_tensor_decomposition_gb300 as mk
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(device)
+    out = []
+    for idx in (2, 3, 5, 4):
+        w = synth.workload(idx)
+        Y = torch.from_numpy(synth.make_tensor(w)).to(device)
+        A = [torch.from_numpy(a).to(device) for a in synth.make_factors(w)]
+        M = [torch.empty(n, w.R, device=device) for n in w.dims]
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=device) if Y.numel() * 4 <= L2_BYTES else None
+        entry = {"workload": w.name, "dims": list(w.dims), "R": w.R,
+                 "krp_bytes_per_mode": [4 * w.R * (w.numel // n) for n in w.dims]}
+        for variant, path in (("matrix_free", "auto"), ("explicit_krp", "tc_explicit_krp")):
+            plan = mk.Plan(w.dims, w.R, path)
+            plan.attach_workspace(device)
+            for _ in range(max(args.warmup, 2)):
+                plan.all_modes(Y, A, outs=M)
+            torch.cuda.synchronize(device)
+            plan.set_timing(True)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+            for r, (e0, e1) in enumerate(evs):
+                if flush is not None:
+                    flush.fill_(r & 255)
+                e0.record(stream)
+                plan.all_modes(Y, A, outs=M)
+                e1.record(stream)
+            torch.cuda.synchronize(device)
+            fs = [dict(t.split("=", 1) for t in plan.describe(k).split() if "=" in t) for k in range(w.d)]
+            entry[variant] = {
+                "ms_all_modes": round(statistics.median(a.elapsed_time(b) for a, b in evs), 4),
+                "ms_main_kernel": [round(statistics.median(plan.kernel_times(k)), 4) for k in range(w.d)],
+                "kernels": [f["kernel"] for f in fs],
+                "workspace_bytes": plan.workspace_bytes(-1),
+                "ws_tables_max": max(int(f["ws_tables"]) for f in fs),
+                "ws_partials_max": max(int(f["ws_partials"]) for f in fs),
+                "ws_images": max(int(f["ws_images"]) for f in fs)}
+            plan.set_timing(False)
+            assert mk.device_status() == 0
+            del plan
+            torch.cuda.empty_cache()
+        mf, ex = entry["matrix_free"], entry["explicit_krp"]
+        entry["explicit_over_free_time"] = round(ex["ms_all_modes"] / mf["ms_all_modes"], 3)
+        entry["explicit_product_over_free_tables"] = round(max(entry["krp_bytes_per_mode"]) / mf["ws_tables_max"], 1)
+        out.append(entry)
+        del Y, A, M, flush
+        torch.cuda.empty_cache()
+    print(json.dumps({
+        "metric": "matrix-based (explicit Khatri-Rao product) vs matrix-free MTTKRP: ms per all-modes call "
+                  "and workspace bytes",
+        "unit": "ms", "higher_is_better": False, "n_gpus": 1, "data": "synthetic", "impl": "ours",
+        "dtype": "fp16x2 (tf32x3 where the fp16 images do not apply)",
+        "workloads": out, "kernel_src": kernel_source_hash()}))
+
+
 def main():
     args = parse_args()
     w = workload_from_arg(args.workload)
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.explicit_krp:
+        run_explicit_krp(args)
     elif args.rotations:
         run_rotations(args, w)
     elif args.ttm >= 0:

@@ -20,11 +20,13 @@ import threading
 
 from ._build import LIB as LIB_PATH, build  # noqa: F401
 
-__all__ = ["Plan", "mttkrp", "all_modes", "apply_rotations", "ttm", "MttkrpError", "build", "load_library",
-           "exported_symbols", "PATH_AUTO", "PATH_SIMT", "PATH_TC", "PATH_TC_TF32"]
+__all__ = ["Plan", "mttkrp", "all_modes", "apply_rotations", "ttm", "probe_fma", "probe_mma", "MttkrpError",
+           "build", "load_library",
+           "exported_symbols", "PATH_AUTO", "PATH_SIMT", "PATH_TC", "PATH_TC_TF32", "PATH_TC_EXPLICIT_KRP"]
 
-PATH_AUTO, PATH_SIMT, PATH_TC, PATH_TC_TF32 = 0, 1, 2, 3
-_PATH_NAMES = {"auto": PATH_AUTO, "simt": PATH_SIMT, "tc": PATH_TC, "tc_tf32": PATH_TC_TF32}
+PATH_AUTO, PATH_SIMT, PATH_TC, PATH_TC_TF32, PATH_TC_EXPLICIT_KRP = 0, 1, 2, 3, 4
+_PATH_NAMES = {"auto": PATH_AUTO, "simt": PATH_SIMT, "tc": PATH_TC, "tc_tf32": PATH_TC_TF32,
+               "tc_explicit_krp": PATH_TC_EXPLICIT_KRP}
 
 _lock = threading.Lock()
 _lib = None
@@ -87,6 +89,10 @@ def load_library():
         lib.mttkrp_cp_als_scratch_bytes.restype = sz
         lib.mttkrp_cp_als_sweep.argtypes = [vp, vp, vp, vp, vp, ci, vp, vp, sz, vp]
         lib.mttkrp_cp_als_sweep.restype = ci
+        lib.mttkrp_probe_fma.argtypes = [ci, ci, vp, vp]
+        lib.mttkrp_probe_fma.restype = ci
+        lib.mttkrp_probe_mma.argtypes = [ci, ci, ci, vp]
+        lib.mttkrp_probe_mma.restype = ci
         _lib = lib
         return lib
 
@@ -418,6 +424,23 @@ def ttm(X, mode: int, M, out=None, stream=None):
                           int(M.shape[0]), ctypes.c_void_p(out.data_ptr()), _stream_handle(X.device, stream)),
            "mttkrp_ttm")
     return out
+
+
+def probe_fma(blocks: int, iters: int, out, stream=None):
+    """Enqueue the fp32 FMA peak probe (mttkrp_probe_fma); out: float32 CUDA
+    tensor of blocks * 256 elements.  flops = 16 * iters * blocks * 256."""
+    _check(load_library().mttkrp_probe_fma(int(blocks), int(iters), ctypes.c_void_p(out.data_ptr()),
+                                           _stream_handle(out.device, stream)), "mttkrp_probe_fma")
+
+
+def probe_mma(kind: str, blocks: int, iters: int, device=None, stream=None):
+    """Enqueue the tensor-pipe peak probe (mttkrp_probe_mma) for kind "tf32" (K = 8)
+    or "f16" (K = 16).  flops = 2 * 128 * 256 * K * iters * blocks."""
+    import torch
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    k = {"tf32": 0, "f16": 1}[kind]
+    _check(load_library().mttkrp_probe_mma(k, int(blocks), int(iters), _stream_handle(device, stream)),
+           "mttkrp_probe_mma")
 
 
 def device_status() -> int:

@@ -97,6 +97,29 @@ void classify(const Plan& p, int k, ModeGeom& g) {
     }
 }
 
+// The matrix-based variant: every mode but k forms the inner group, so the B
+// operand is the whole Khatri-Rao product (J = prod_{n != k} I_n rows), with
+// one pre index.
+void classify_explicit(const Plan& p, int k, ModeGeom& g) {
+    g.k = k;
+    g.I = p.dims[k];
+    g.R = p.R;
+    g.s_k = p.strides[k];
+    g.J = 1;
+    g.Jq = 1;
+    for (int n = 0; n < p.d; ++n) {
+        if (n == k) continue;
+        g.J *= p.dims[n];
+        if (n > k) g.Jq *= p.dims[n];
+    }
+    g.IQ = (k > 0) ? p.strides[k - 1] : 0;
+    g.ngroup = 0;
+    g.npm = 0;
+    g.npre = 1;
+    for (int n = 0; n < p.d; ++n)
+        if (n != k) g.group[g.ngroup++] = n;
+}
+
 void plan_simt(ModePlan& mp) {
     const ModeGeom& g = mp.g;
     mp.path = MTTKRP_PATH_SIMT;
@@ -114,7 +137,7 @@ void plan_simt(ModePlan& mp) {
     mp.splits = cdiv(g.npre, mp.pre_per_split);
 }
 
-void layout_workspace(ModePlan& mp) {
+void layout_workspace(const Plan& p, ModePlan& mp) {
     const ModeGeom& g = mp.g;
     size_t off = 256;  // first 256 bytes reserved
     mp.off_partials = off;
@@ -129,6 +152,13 @@ void layout_workspace(ModePlan& mp) {
     off = align256(off + (size_t)g.npre * g.R * sizeof(float));
     mp.off_base = off;
     off = align256(off + (size_t)g.npre * sizeof(int64_t));
+    mp.off_t1 = off;
+    if (mp.explicit_krp) {
+        // product of the group's factors but the last: J / I_last rows of R
+        const int64_t rows = g.J / p.dims[g.group[g.ngroup - 1]];
+        off = align256(off + (size_t)rows * g.R * sizeof(float));
+    }
+    mp.off_end = off;
     mp.total = off;
 }
 
@@ -184,6 +214,20 @@ int plan_mode(Plan& p, int k, int path) {
     // MTTKRP_PATH_TC_TF32: the tensor-core kernels without the fp16 split
     const bool allow_fp16 = path != MTTKRP_PATH_TC_TF32;
     if (path == MTTKRP_PATH_TC_TF32) path = MTTKRP_PATH_TC;
+    if (path == MTTKRP_PATH_TC_EXPLICIT_KRP) {
+        // the matrix-based variant: tensor-core kernels over the explicit
+        // Khatri-Rao product; a misaligned Y runs the matrix-free SIMT plan
+        ModePlan& alt = p.simt_alt[k];
+        alt = mp;
+        plan_simt(alt);
+        layout_workspace(p, alt);
+        classify_explicit(p, k, mp.g);
+        mp.explicit_krp = 1;
+        if (!tc_plan(p, mp, true)) return MTTKRP_ERR_UNSUPPORTED;
+        layout_workspace(p, mp);
+        if (cdiv(alt.g.I, alt.bm) <= 65535 && alt.total > mp.total) mp.total = alt.total;
+        return MTTKRP_OK;
+    }
     if (path == MTTKRP_PATH_AUTO) {
         path = MTTKRP_PATH_SIMT;
         if (tc_prefer(mp)) {
@@ -194,11 +238,11 @@ int plan_mode(Plan& p, int k, int path) {
     ModePlan& alt = p.simt_alt[k];
     alt = mp;
     plan_simt(alt);
-    layout_workspace(alt);
+    layout_workspace(p, alt);
     const bool simt_ok = cdiv(alt.g.I, alt.bm) <= 65535;  // row tiles run along gridDim.y
     if (path == MTTKRP_PATH_TC) {
         if (!tc_plan(p, mp, allow_fp16)) return MTTKRP_ERR_UNSUPPORTED;
-        layout_workspace(mp);
+        layout_workspace(p, mp);
         if (simt_ok && alt.total > mp.total) mp.total = alt.total;
     } else {
         if (!simt_ok) return MTTKRP_ERR_UNSUPPORTED;
@@ -315,6 +359,24 @@ int run_mode(Plan& p, const float* Y, const float* const* factors, int k, float*
             return fail(MTTKRP_ERR_CUDA, "timing events: %s", cudaGetErrorString(err));
     }
 
+    if (mp.path == MTTKRP_PATH_TC && mp.explicit_krp) {
+        // explicit Khatri-Rao product: the table of the group's factors but the
+        // last one (the B-image kernel multiplies in the last factor)
+        ProdTableArgs a;
+        memset(&a, 0, sizeof(a));
+        a.nm = g.ngroup - 1;
+        for (int t = 0; t + 1 < g.ngroup; ++t) {
+            a.dim[t] = p.dims[g.group[t]];
+            a.ystride[t] = p.strides[g.group[t]];
+            a.fac[t] = factors[g.group[t]];
+        }
+        a.rows = g.J / p.dims[g.group[g.ngroup - 1]];
+        a.R = g.R;
+        a.tab = reinterpret_cast<float*>(ws + mp.off_t1);
+        if ((err = launch_prod_table(a, stream)) != cudaSuccess)
+            return fail(MTTKRP_ERR_CUDA, "table launch: %s", cudaGetErrorString(err));
+        ++p.launches;
+    }
     if (mp.path == MTTKRP_PATH_TC) {
         int nlaunch = 0;
         if (ev0) cudaEventRecord(ev0, stream);
@@ -441,7 +503,7 @@ int mttkrp_plan_set_path(mttkrp_plan_t h, int path) {
     Plan* p = as_plan(h);
     if (p == nullptr) return fail(MTTKRP_ERR_INVALID, "plan is NULL");
     if (path != MTTKRP_PATH_AUTO && path != MTTKRP_PATH_SIMT && path != MTTKRP_PATH_TC &&
-        path != MTTKRP_PATH_TC_TF32)
+        path != MTTKRP_PATH_TC_TF32 && path != MTTKRP_PATH_TC_EXPLICIT_KRP)
         return fail(MTTKRP_ERR_INVALID, "unknown path %d", path);
     ModePlan saved[kMaxD];
     memcpy(saved, p->mode, sizeof(saved));
@@ -717,15 +779,29 @@ int mttkrp_plan_describe(mttkrp_plan_t h, int mode, char* buf, size_t len) {
         const char* lay = mp.tc_img ? (mp.tc_img_t ? "t" : "nat") : (mp.tc_inner ? "inner" : "kmaj");
         snprintf(kernel, sizeof(kernel), "%s.%s%s.bn%d", fam, lay, mp.tc_small ? ".small" : "", mp.bn);
     }
+    // fp32 bytes of the explicit Khatri-Rao product of every mode but this one
+    // (what the matrix-based variant forms; the matrix-free one never does)
+    int64_t others = 1;
+    for (int t = 0; t < p->d; ++t)
+        if (t != mode) others *= p->dims[t];
+    const double krp_bytes = 4.0 * (double)p->R * (double)others;
+    // workspace by purpose: split partial sums; tables (factor products, the B
+    // operand images -- for the explicit variant the whole Khatri-Rao product);
+    // plan-wide fp16 images of Y and slab maxima (fp16-split modes)
+    const bool fp16 = mp.path == MTTKRP_PATH_TC && (mp.tc_img || mp.tc_h2);
+    const size_t ws_images = fp16 ? mp.total - p->off_slab : 0;
     char tmp[640];
     int n = snprintf(tmp, sizeof(tmp),
                      "mode=%d path=%s kernel=%s tile=%dx%d inner_group=[%s] J=%lld Jq=%lld pre_modes=[%s] "
                      "npre=%lld splits=%lld pre_per_split=%lld workspace=%zu tc_ksteps=%d tc_inner=%d tc_slots=%d "
-                     "tc_tmem_a=%d tc_fp16x2=%d tc_fp16_image=%d",
+                     "tc_tmem_a=%d tc_fp16x2=%d tc_fp16_image=%d krp=%s krp_bytes=%llu "
+                     "ws_partials=%zu ws_tables=%zu ws_images=%zu",
                      mode, mp.path == MTTKRP_PATH_TC ? "tc" : "simt", kernel, mp.bm, mp.bn, groups,
                      (long long)g.J, (long long)g.Jq, pres, (long long)g.npre,
                      (long long)mp.splits, (long long)mp.pre_per_split, mp.total, mp.tc_ks, mp.tc_inner,
-                     mp.tc_small ? mp.tc_ps : 1, mp.tc_tmem, mp.tc_h2 || mp.tc_img, mp.tc_img + mp.tc_img_t);
+                     mp.tc_small ? mp.tc_ps : 1, mp.tc_tmem, mp.tc_h2 || mp.tc_img, mp.tc_img + mp.tc_img_t,
+                     mp.explicit_krp ? "explicit" : "free", (unsigned long long)krp_bytes,
+                     mp.off_binner - mp.off_partials, mp.off_end - mp.off_binner, ws_images);
     if (buf != nullptr && len > 0) {
         strncpy(buf, tmp, len - 1);
         buf[len - 1] = 0;
@@ -791,6 +867,24 @@ const char* mttkrp_strerror(int code) {
 const char* mttkrp_last_error(void) { return g_errmsg; }
 
 int mttkrp_version(void) { return 100; }
+
+int mttkrp_probe_fma(int blocks, int iters, float* out, void* stream) {
+    g_errmsg[0] = 0;
+    if (blocks < 1 || blocks > 65535 || iters < 1 || out == nullptr)
+        return fail(MTTKRP_ERR_INVALID, "blocks in [1, 65535], iters >= 1 and a non-NULL out are required");
+    cudaError_t e = launch_fma_probe(blocks, iters, out, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "FMA probe launch: %s", cudaGetErrorString(e));
+    return MTTKRP_OK;
+}
+
+int mttkrp_probe_mma(int kind, int blocks, int iters, void* stream) {
+    g_errmsg[0] = 0;
+    if ((kind != 0 && kind != 1) || blocks < 1 || blocks > 65535 || iters < 1)
+        return fail(MTTKRP_ERR_INVALID, "kind 0 (tf32) or 1 (f16), blocks in [1, 65535] and iters >= 1 are required");
+    cudaError_t e = tc_launch_mma_probe(kind, blocks, iters, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "MMA probe launch: %s", cudaGetErrorString(e));
+    return MTTKRP_OK;
+}
 
 }  // extern "C"
 

@@ -65,8 +65,16 @@ struct ModePlan {
                         //    operands in shared memory (K-steps of 64)
     int tc_img_t;       // tc_img for the innermost mode: from the transposed images
                         //    (Y viewed as P x I_{d-1}, stored I_{d-1} x P)
+    // explicit Khatri-Rao product (the matrix-based comparison variant): the
+    // inner group is every mode but k (one pre index), the B images hold the
+    // whole product, and the contraction is split over B chunks, jc_per_split
+    // chunks a CTA
+    int explicit_krp;
+    int jc_per_split;
     // workspace layout, byte offsets from the workspace base
     size_t off_partials, off_binner, off_gtab, off_base, total;
+    size_t off_t1;      // explicit_krp: product of the inner group's factors but the last one
+    size_t off_end;     // end of the mode's own regions (before plan-level regions)
     size_t off_img;     // tc_img: fp16 hi image of Y, then the lo image (shared by all modes)
     size_t off_timg;    // tc_img: the transposed hi and lo images
 };
@@ -172,5 +180,7 @@ cudaError_t launch_reduce_splits(const float* part, int64_t splits, int64_t n, f
 cudaError_t launch_simt(int bm, int bn, int amode, bool bvec, const SimtArgs& a,
                         int64_t splits, cudaStream_t s);
 bool simt_tile_supported(int bm, int bn);
+// peak probe of the fp32 FMA pipe (blocks x 256 threads; out: blocks x 256 floats)
+cudaError_t launch_fma_probe(int blocks, int iters, float* out, cudaStream_t s);
 
 }  // namespace mk

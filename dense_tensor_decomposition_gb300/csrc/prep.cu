@@ -3,9 +3,8 @@
 //    Binner (inner group) that the main kernels combine into Khatri-Rao rows
 //    on the fly, plus the Y base offset of every pre index;
 //  * the split reductions add the per-split partial results in a fixed order
-//    (compensated fp32 when every thread sums all splits of its outputs, fp64
-//    when warps share the splits) and write the fp32 output; no atomics
-//    anywhere, so results are bitwise reproducible for a given plan.
+//    with compensated (Neumaier) fp32 additions and write the fp32 output; no
+//    atomics anywhere, so results are bitwise reproducible for a given plan.
 #include "internal.h"
 #include "scale.cuh"
 
@@ -34,12 +33,19 @@ __global__ void __launch_bounds__(256) prod_table_kernel(ProdTableArgs a) {
         if (a.slab_bits != nullptr)
             f = pow2_scale(*a.gmax_bits) * pow2_recip(slab_scale(a.slab_bits, row / a.slab_div, *a.gmax_bits));
         float* out = a.tab + row * a.R;
-        for (int64_t r = lane; r < a.R; r += 32) {
-            float prod = 1.0f;
+        for (int64_t r0 = lane; r0 < a.R; r0 += 128) {   // four columns a lane in flight
+            float prod[4];
 #pragma unroll
-            for (int m = kMaxD - 1; m >= 0; --m)
-                if (m < a.nm) prod *= frow[m][r];
-            out[r] = prod * f;
+            for (int u = 0; u < 4; ++u) {
+                const int64_t r = r0 + 32 * u;
+                prod[u] = 1.0f;
+#pragma unroll
+                for (int m = kMaxD - 1; m >= 0; --m)
+                    if (m < a.nm && r < a.R) prod[u] *= __ldg(frow[m] + r);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (r0 + 32 * u < a.R) out[r0 + 32 * u] = prod[u] * f;
         }
         if (a.base != nullptr && lane == 0) a.base[row] = base;
     }
@@ -53,20 +59,30 @@ cudaError_t launch_prod_table(const ProdTableArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// out[e] = (float) sum over s of (double) part[s * n + e].  Each block owns 32
-// groups of 4 consecutive outputs (one 16-byte group per lane); warp w adds the
-// partials of splits [w*S/8, (w+1)*S/8) in increasing s with several 16-byte
-// loads in flight, and the eight warp sums are added in warp order.  The order
-// depends only on (S, n), so results are bitwise reproducible; spreading the
-// splits over warps keeps enough loads in flight both for many outputs and few
-// splits and for few outputs and many splits.
+// Compensated fp32 addition (Neumaier): sum + c carries the exact running total
+// to about one fp32 rounding, independent of the number of terms; GB300's fp64
+// rate is too low for a bandwidth-bound sum of this size.
+__device__ __forceinline__ void kahan_add(float& sum, float& c, float x) {
+    const float t = sum + x;
+    c += fabsf(sum) >= fabsf(x) ? (sum - t) + x : (x - t) + sum;
+    sum = t;
+}
+
+// out[e] = sum over s of part[s * n + e].  Each block owns 32 groups of 4
+// consecutive outputs (one 16-byte group per lane); warp w adds the partials of
+// splits [w*S/8, (w+1)*S/8) in increasing s with several 16-byte loads in
+// flight (compensated fp32), and the eight warp sums are added in warp order
+// (compensated fp32 again).  The order depends only on (S, n), so results are
+// bitwise reproducible; spreading the splits over warps keeps enough loads in
+// flight both for many outputs and few splits and for few outputs and many
+// splits.
 constexpr int kRedWarps = 8;
 
 template <int V>   // V = 4: float4 groups; V = 1: scalars
 __global__ void __launch_bounds__(kRedWarps * 32)
     reduce_splits_kernel(const float* __restrict__ part, int64_t splits, int64_t n,
                          float* __restrict__ out) {
-    __shared__ double sums[kRedWarps][32][V];
+    __shared__ float sums[kRedWarps][32][V];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int64_t s0 = splits * warp / kRedWarps;
@@ -74,9 +90,9 @@ __global__ void __launch_bounds__(kRedWarps * 32)
     const int64_t ng = n / V;   // groups
     for (int64_t base = (int64_t)blockIdx.x * 32; base < ng; base += (int64_t)gridDim.x * 32) {
         const int64_t g = base + lane;
-        double acc[V];
+        float acc[V], cmp[V];
 #pragma unroll
-        for (int c = 0; c < V; ++c) acc[c] = 0.0;
+        for (int c = 0; c < V; ++c) acc[c] = cmp[c] = 0.f;
         if (g < ng) {
             int64_t sp = s0;
             for (; sp + 4 <= s1; sp += 4) {
@@ -97,48 +113,39 @@ __global__ void __launch_bounds__(kRedWarps * 32)
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
 #pragma unroll
-                    for (int c = 0; c < V; ++c) acc[c] += (double)v[u][c];
+                    for (int c = 0; c < V; ++c) kahan_add(acc[c], cmp[c], v[u][c]);
             }
             for (; sp < s1; ++sp) {
                 const float* p = part + sp * n + g * V;
                 if constexpr (V == 4) {
                     const float4 x = __ldcs(reinterpret_cast<const float4*>(p));
-                    acc[0] += (double)x.x;
-                    acc[1] += (double)x.y;
-                    acc[2] += (double)x.z;
-                    acc[3] += (double)x.w;
+                    kahan_add(acc[0], cmp[0], x.x);
+                    kahan_add(acc[1], cmp[1], x.y);
+                    kahan_add(acc[2], cmp[2], x.z);
+                    kahan_add(acc[3], cmp[3], x.w);
                 } else {
-                    acc[0] += (double)__ldcs(p);
+                    kahan_add(acc[0], cmp[0], __ldcs(p));
                 }
             }
         }
 #pragma unroll
-        for (int c = 0; c < V; ++c) sums[warp][lane][c] = acc[c];
+        for (int c = 0; c < V; ++c) sums[warp][lane][c] = acc[c] + cmp[c];
         __syncthreads();
         if (warp == 0 && g < ng) {
-            double t[V];
+            float t[V], tc[V];
 #pragma unroll
-            for (int c = 0; c < V; ++c) t[c] = 0.0;
+            for (int c = 0; c < V; ++c) t[c] = tc[c] = 0.f;
 #pragma unroll
             for (int w = 0; w < kRedWarps; ++w)
 #pragma unroll
-                for (int c = 0; c < V; ++c) t[c] += sums[w][lane][c];
+                for (int c = 0; c < V; ++c) kahan_add(t[c], tc[c], sums[w][lane][c]);
             if constexpr (V == 4)
-                reinterpret_cast<float4*>(out)[g] = make_float4((float)t[0], (float)t[1], (float)t[2], (float)t[3]);
+                reinterpret_cast<float4*>(out)[g] = make_float4(t[0] + tc[0], t[1] + tc[1], t[2] + tc[2], t[3] + tc[3]);
             else
-                out[g] = (float)t[0];
+                out[g] = t[0] + tc[0];
         }
         __syncthreads();
     }
-}
-
-// Compensated fp32 addition (Neumaier): sum + c carries the exact running total
-// to about one fp32 rounding, independent of the number of terms; GB300's fp64
-// rate is too low for a bandwidth-bound sum of this size.
-__device__ __forceinline__ void kahan_add(float& sum, float& c, float x) {
-    const float t = sum + x;
-    c += fabsf(sum) >= fabsf(x) ? (sum - t) + x : (x - t) + sum;
-    sum = t;
 }
 
 // One thread per 4 consecutive outputs, all splits in increasing s with four

@@ -274,6 +274,32 @@ bool simt_tile_supported(int bm, int bn) {
            (bn == 64 && (bm == 128 || bm == 64 || bm == 32));
 }
 
+// Peak probe of the fp32 FMA pipe: eight independent chains of fused
+// multiply-adds a thread (enough independent work to hide the pipe's latency
+// at 8 warps per scheduler); each thread stores its sum so nothing is dropped.
+// flops = 16 x iters x threads.
+__global__ void __launch_bounds__(256) fma_probe_kernel(int iters, float* __restrict__ out) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    float x[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) x[c] = 1.0f + 1e-3f * (float)(c + (t & 7));
+    const float m = 0.999999f, b = 1e-7f;
+#pragma unroll 4
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) x[c] = fmaf(x[c], m, b);
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) sum += x[c];
+    out[t] = sum;
+}
+
+cudaError_t launch_fma_probe(int blocks, int iters, float* out, cudaStream_t s) {
+    fma_probe_kernel<<<blocks, 256, 0, s>>>(iters, out);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_simt(int bm, int bn, int amode, bool bvec, const SimtArgs& a, int64_t splits,
                         cudaStream_t s) {
     if (bn == 128) {

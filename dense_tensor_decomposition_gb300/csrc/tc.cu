@@ -86,6 +86,8 @@ struct TcArgs {
     int KS;                   // K-steps per pi
     int jq_steps;             // K-steps per value of jp (K-contiguous variant)
     int withhold_signal;      // test hook: skip the first accumulator-ready commit
+    int jc_per_split;         // > 0: blockIdx.z splits the B chunks (this many a CTA), every
+                              // CTA takes all pre indices (explicit Khatri-Rao product)
     uint32_t y_box_bytes;     // bytes of one Y tile copy
     // small-I variant: ps pre indices share one 128-row tile (rows slot * I + i)
     int ps;                   // pre-index slots per tile (1 otherwise)
@@ -556,6 +558,30 @@ struct Ring {
     }
 };
 
+// This CTA's share of the contraction: a range of pre indices with every B chunk
+// (the contraction split over pre indices), or every pre index with a range of
+// B chunks (split over chunks: the explicit Khatri-Rao product has one pre
+// index).  The host makes every share non-empty.
+struct Share {
+    int64_t pre_lo, pre_hi;
+    int jc0, jc1;
+};
+__device__ __forceinline__ Share cta_share(const TcArgs& a, int njc) {
+    Share s;
+    if (a.jc_per_split > 0) {
+        s.pre_lo = 0;
+        s.pre_hi = a.npre;
+        s.jc0 = (int)blockIdx.z * a.jc_per_split;
+        s.jc1 = min(njc, s.jc0 + a.jc_per_split);
+    } else {
+        s.pre_lo = (int64_t)blockIdx.z * a.pre_per_split;
+        s.pre_hi = min(a.npre, s.pre_lo + a.pre_per_split);
+        s.jc0 = 0;
+        s.jc1 = njc;
+    }
+    return s;
+}
+
 template <int BN, bool INNER, bool SMALL>
 __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(const __grid_constant__ TcArgs a) {
     using L = Smem<BN, INNER, SMALL>;
@@ -591,12 +617,12 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
     const int lane = tid & 31;
     const int64_t m0 = (int64_t)blockIdx.y * kBM;
     const int64_t r0 = (int64_t)blockIdx.x * BN;
-    const int64_t pre_lo = (int64_t)blockIdx.z * a.pre_per_split;
-    int64_t pre_hi = pre_lo + a.pre_per_split;
-    if (pre_hi > a.npre) pre_hi = a.npre;
-    const int64_t npi = pre_hi > pre_lo ? pre_hi - pre_lo : 0;
     const int KS = a.KS;
     const int njc = (KS + CK - 1) / CK;           // B-chunks
+    const Share share = cta_share(a, njc);
+    const int64_t pre_lo = share.pre_lo, pre_hi = share.pre_hi;
+    const int jc0 = share.jc0, jc1 = share.jc1;
+    const int64_t npi = pre_hi > pre_lo ? pre_hi - pre_lo : 0;
     auto chunk_len = [&](int jc) { return min(CK, KS - jc * CK); };
     constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : 2 * BN;
 
@@ -641,7 +667,8 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
     } else {
         nunits = npi;
     }
-    const int64_t T = nunits * KS;  // K-steps of this CTA
+    // K-steps of this CTA: every unit runs the K-steps of the CTA's B chunks
+    const int64_t T = nunits * (int64_t)(min(KS, jc1 * CK) - jc0 * CK);
 
     if (warp == 0) {
         // ------------------------- TMA producer -------------------------
@@ -654,7 +681,7 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
             // Replace the resident B-chunk with chunk jc once the MMAs of chunk
             // jc - 1 are done.
             auto load_b = [&](int jc) -> bool {
-                if (jc > 0 && !wait_bounded(bempty, (uint32_t)((jc - 1) & 1), abort_flag, a.status,
+                if (jc > jc0 && !wait_bounded(bempty, (uint32_t)((jc - jc0 - 1) & 1), abort_flag, a.status,
                                             kStatusTimeoutTma))
                     return false;
                 const int ck = chunk_len(jc);
@@ -667,7 +694,7 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
                 jc_loaded = jc;
                 return true;
             };
-            for (int jc = 0; jc < njc && ok; ++jc) {
+            for (int jc = jc0; jc < jc1 && ok; ++jc) {
                 const int ck = chunk_len(jc);
                 // The first NR Y tiles of chunk jc only need stages freed by the
                 // MMAs of chunk jc - 1, so they are issued before the chunk swap
@@ -714,7 +741,7 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
             // wait (bounded) for copies still in flight before leaving
             for (int64_t u = issued - 1; u >= 0 && u >= issued - NR; --u)
                 wait_drain(&raw_full[u % NR], (uint32_t)((u / NR) & 1), a.status);
-            if (jc_loaded >= 0) wait_drain(bfull, (uint32_t)(jc_loaded & 1), a.status);
+            if (jc_loaded >= 0) wait_drain(bfull, (uint32_t)((jc_loaded - jc0) & 1), a.status);
         }
     } else if (warp == 1) {
         // ------------------------- MMA issuer -------------------------
@@ -758,9 +785,9 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
             uint32_t zph = 0;    // bit b: parity of the next release of buffer b
             uint32_t zused = 0;  // bit b: buffer b was used before
             bool ok = true;
-            for (int jc = 0; jc < njc && ok; ++jc) {
+            for (int jc = jc0; jc < jc1 && ok; ++jc) {
                 const int ck = chunk_len(jc);
-                if (!wait_w(bfull, (uint32_t)(jc & 1))) {
+                if (!wait_w(bfull, (uint32_t)((jc - jc0) & 1))) {
                     ok = false;
                     break;
                 }
@@ -945,7 +972,7 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
             int zb = 0;
             uint32_t zph = 0;
             bool ok = true;
-            for (int jc = 0; jc < njc && ok; ++jc) {
+            for (int jc = jc0; jc < jc1 && ok; ++jc) {
                 const int ck = chunk_len(jc);
                 for (int64_t pi = pre_lo; pi < pre_hi && ok; pi = unit_next(pi)) {
                     asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -1036,7 +1063,7 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
             int zb = 0;           // TMEM buffer of the next unit
             uint32_t zph = 0;     // bit b: parity of the next completion of zfull[b]
             bool ok = true;
-            for (int jc = 0; jc < njc && ok; ++jc) {
+            for (int jc = jc0; jc < jc1 && ok; ++jc) {
                 const int ck = chunk_len(jc);
                 for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
                     asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -2156,11 +2183,11 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
     const int lane = tid & 31;
     const int64_t m0 = (int64_t)blockIdx.y * kBM;
     const int64_t r0 = (int64_t)blockIdx.x * BN;
-    const int64_t pre_lo = (int64_t)blockIdx.z * a.pre_per_split;
-    int64_t pre_hi = pre_lo + a.pre_per_split;
-    if (pre_hi > a.npre) pre_hi = a.npre;
     const int KS = a.KS;
     const int njc = (KS + CK - 1) / CK;
+    const Share share = cta_share(a, njc);
+    const int64_t pre_lo = share.pre_lo, pre_hi = share.pre_hi;
+    const int jc0 = share.jc0, jc1 = share.jc1;
     auto chunk_len = [&](int jc) { return min(CK, KS - jc * CK); };
     constexpr uint32_t kTmemCols = 2 * BN;   // two accumulator buffers
     static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
@@ -2212,7 +2239,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             int jc_loaded = -1;
             bool ok = true;
             auto load_b = [&](int jc) -> bool {
-                if (jc > 0 && !wait_bounded_inl(bempty, (uint32_t)((jc - 1) & 1), abort_flag, a.status,
+                if (jc > jc0 && !wait_bounded_inl(bempty, (uint32_t)((jc - jc0 - 1) & 1), abort_flag, a.status,
                                                 kStatusTimeoutTma))
                     return false;
                 const int ck = chunk_len(jc);
@@ -2228,7 +2255,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             // the pre index pi = (cP, cQ) in C order, advanced without divisions
             const int64_t nQ = a.nQ;
             const int cP0 = (int)(pre_lo / nQ), cQ0 = (int)(pre_lo - (int64_t)cP0 * nQ);
-            for (int jc = 0; jc < njc && ok; ++jc) {
+            for (int jc = jc0; jc < jc1 && ok; ++jc) {
                 const int ck = chunk_len(jc);
                 // the first NS tiles of chunk jc need only work of chunk jc - 1,
                 // so they are issued before the chunk swap
@@ -2279,7 +2306,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             }
             for (int64_t u = issued - 1; u >= 0 && u >= issued - NS; --u)
                 wait_drain_inl(&full[u % NS], (uint32_t)((u / NS) & 1), a.status);
-            if (jc_loaded >= 0) wait_drain_inl(bfull, (uint32_t)(jc_loaded & 1), a.status);
+            if (jc_loaded >= 0) wait_drain_inl(bfull, (uint32_t)((jc_loaded - jc0) & 1), a.status);
         } else if (warp == 1 && lane == 0) {
             // ------------------------- MMA issuer -------------------------
             // kind::f16: fp16 A and B (both K-major), fp32 accumulator
@@ -2295,9 +2322,9 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             uint32_t zph = 0;
             uint32_t zused = 0;
             bool ok = true;
-            for (int jc = 0; jc < njc && ok; ++jc) {
+            for (int jc = jc0; jc < jc1 && ok; ++jc) {
                 const int ck = chunk_len(jc);
-                if (!wait_bounded_inl(bfull, (uint32_t)(jc & 1), abort_flag, a.status, kStatusTimeoutMma)) {
+                if (!wait_bounded_inl(bfull, (uint32_t)((jc - jc0) & 1), abort_flag, a.status, kStatusTimeoutMma)) {
                     ok = false;
                     break;
                 }
@@ -2367,7 +2394,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             int zb = 0;
             uint32_t zph = 0;
             bool ok = true;
-            for (int jc = 0; jc < njc && ok; ++jc) {
+            for (int jc = jc0; jc < jc1 && ok; ++jc) {
                 for (int64_t pi = pre_lo; pi < pre_hi && ok; pi = unit_next(pi)) {
                     const int64_t pe = unit_next(pi);
                     const bool live_row = slot < a.ps && pi + slot < pe;
@@ -2444,7 +2471,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
         int zb = 0;
         uint32_t zph = 0;
         bool ok = true;
-        for (int jc = 0; jc < njc && ok; ++jc) {
+        for (int jc = jc0; jc < jc1 && ok; ++jc) {
             for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
                 float g_cur[kGv];
 #pragma unroll
@@ -2600,17 +2627,24 @@ __global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restr
         s_sy0 = slab_scale(slab, s0, gbits);
         s_sy1 = s_b1 < P ? slab_scale(slab, s0 + 1, gbits) : s_sy0;
     };
-    auto row_scale = [&](int64_t pr) -> float {   // rows past P (tile padding) clamp to the last
-        return rps >= TP ? (pr >= s_b1 ? s_sy1 : s_sy0) : slab_scale(slab, (pr < P ? pr : P - 1) / rps, gbits);
+    auto row_scale = [&](int64_t pr, int64_t tile_rows) -> float {   // rows past P clamp to the last
+        return rps >= tile_rows ? (pr >= s_b1 ? s_sy1 : s_sy0)
+                                : slab_scale(slab, (pr < P ? pr : P - 1) / rps, gbits);
     };
     if (I < TI / 2) {
-        // short rows: TP consecutive p are one contiguous block of TP * I values,
-        // read (and written in the natural layout) flat, so that no lanes idle
+        // short rows: TPS consecutive p (as many as the shared array holds, a
+        // multiple of 64) are one contiguous block of TPS * I values, read (and
+        // written in the natural layout) flat, so that no lanes idle; staged as
+        // [i][p] with a row stride of TPS + 1 words
         const int Ii = (int)I;
-        const int64_t np = (P + TP - 1) / TP;
+        int tps = (TI * (TP + 1)) / Ii - 1;
+        tps = tps >= 1024 ? 1024 : (tps / TP) * TP;
+        const int stride = tps + 1;
+        uint32_t* shf = &sh[0][0];
+        const int64_t np = (P + tps - 1) / tps;
         for (int64_t t = blockIdx.x; t < np; t += gridDim.x) {
-            const int64_t p0 = t * TP;
-            const int rows = (int)(P - p0 < TP ? P - p0 : TP);
+            const int64_t p0 = t * tps;
+            const int rows = (int)(P - p0 < tps ? P - p0 : tps);
             tile_scales(p0);
             const int nvals = rows * Ii;
             const int64_t base = p0 * I;
@@ -2630,12 +2664,13 @@ __global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restr
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int idx = 4 * f + q;
-                    const float x = v[q] * row_scale(p0 + idx / Ii);
+                    const int row = idx / Ii;
+                    const float x = v[q] * row_scale(p0 + row, tps);
                     const __half h = __float2half_rn(x);
                     const __half l = __float2half_rn(x - __half2float(h));
                     hb[q] = __half_as_ushort(h);
                     lb[q] = __half_as_ushort(l);
-                    if (idx < nvals) sh[idx % Ii][idx / Ii] = hb[q] | (lb[q] << 16);
+                    if (idx < nvals) shf[(idx - row * Ii) * stride + row] = hb[q] | (lb[q] << 16);
                 }
                 if (write_nat) {
                     if (4 * f + 3 < nvals) {
@@ -2651,18 +2686,19 @@ __global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restr
                 }
             }
             __syncthreads();
-            for (int c = warp; c < Ii; c += 8) {
-                const int64_t pc = p0 + 2 * lane;
-                if (2 * lane < rows) {
-                    const uint32_t w0 = sh[c][2 * lane], w1 = sh[c][2 * lane + 1];
-                    const int64_t e = (int64_t)c * P + pc;
-                    if (2 * lane + 1 < rows) {
-                        *reinterpret_cast<uint32_t*>(thi + e) = __byte_perm(w0, w1, 0x5410);
-                        *reinterpret_cast<uint32_t*>(tlo + e) = __byte_perm(w0, w1, 0x7632);
-                    } else {
-                        thi[e] = __ushort_as_half((unsigned short)(w0 & 0xFFFFu));
-                        tlo[e] = __ushort_as_half((unsigned short)(w0 >> 16));
-                    }
+            // transposed: row c holds p0 .. p0 + rows - 1 at c * P + p, two p a lane
+            const int pairs = (rows + 1) / 2;
+            for (int w = threadIdx.x; w < Ii * pairs; w += blockDim.x) {
+                const int c = w / pairs, pp = 2 * (w - c * pairs);
+                const uint32_t w0 = shf[c * stride + pp];
+                const int64_t e = (int64_t)c * P + p0 + pp;
+                if (pp + 1 < rows) {
+                    const uint32_t w1 = shf[c * stride + pp + 1];
+                    *reinterpret_cast<uint32_t*>(thi + e) = __byte_perm(w0, w1, 0x5410);
+                    *reinterpret_cast<uint32_t*>(tlo + e) = __byte_perm(w0, w1, 0x7632);
+                } else {
+                    thi[e] = __ushort_as_half((unsigned short)(w0 & 0xFFFFu));
+                    tlo[e] = __ushort_as_half((unsigned short)(w0 >> 16));
                 }
             }
             __syncthreads();
@@ -2704,7 +2740,7 @@ __global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restr
             const int64_t pr = p0 + r;
             const int64_t e = pr * I + ib;
             const float* v = vv[u];
-            const float sy = row_scale(pr);
+            const float sy = row_scale(pr, TP);
             uint32_t hb[4], lb[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -2954,6 +2990,175 @@ __global__ void tc_bimage_f16_kernel(BImgArgs a, const float* __restrict__ colsc
         }
         const __half h = __float2half_rn(v);
         out[e] = half == 0 ? h : __float2half_rn(v - __half2float(h));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The explicit Khatri-Rao product (matrix-based comparison variant), written
+// as the B images the tensor-core kernels stream: row j of the product (j over
+// every mode but k, C order) is KRP(j, r) = T1(j / I_last, r) * A_last(j % I_last, r),
+// T1 being the product of the other group factors (a table built beforehand).
+// One block of the images per (column tile nt, K-step ks): the KW rows j of the
+// K-step are decoded once, the KW x BN values staged in shared memory (columns
+// r fastest, so the table and factor reads are coalesced), then written as hi
+// and lo images in the swizzled layout of the kernel that reads them:
+//   F16  (fp16-image kernel): KW = 64, 128-byte rows, chunk c of row n at
+//        (c ^ n) & 7, values scaled by the column's power of two,
+//        hi = fp16(v), lo = fp16(v - hi);
+//   fp32 (3xTF32 kernel):     KW = 16, 64-byte rows, chunk c of row n at
+//        (c ^ (n >> 1)) & 3, hi = v (the tensor core truncates it to tf32),
+//        lo = v - tf32(v).
+// ---------------------------------------------------------------------------
+struct KrpImgArgs {
+    const float* t1;        // (J / I_last) x R
+    const float* alast;     // I_last x R
+    int64_t ilast;
+    const float* colscale;  // R (F16 only)
+    int64_t R, J, Jq;
+    int BN, KS, jq_steps, inner;
+    int64_t nblocks;        // column tiles x KS
+    void* out;
+};
+
+constexpr int kKrpMaxBN = 256;
+
+template <int KW, bool F16>
+__global__ void __launch_bounds__(256) krp_image_kernel(KrpImgArgs a) {
+    extern __shared__ float vs[];           // [KW][BN]
+    __shared__ int64_t jrow1[KW], jrow2[KW];   // j / I_last and j % I_last, -1: padding
+    constexpr int kChunk = 16 / (F16 ? 2 : 4);     // values a 16-byte chunk holds
+    constexpr int kChunks = KW / kChunk;           // chunks a row
+    constexpr int kRow = KW * (F16 ? 2 : 4);       // bytes a row
+    const int BN = a.BN;
+    for (int64_t blk = blockIdx.x; blk < a.nblocks; blk += gridDim.x) {
+        const int64_t nt = blk / a.KS;
+        const int ks = (int)(blk - nt * a.KS);
+        if (threadIdx.x < KW) {
+            const int kk = threadIdx.x;
+            int64_t j;
+            bool valid;
+            if (a.inner) {
+                j = (int64_t)ks * KW + kk;
+                valid = j < a.J;
+            } else {
+                const int jp = ks / a.jq_steps;
+                const int64_t jq = (int64_t)(ks - jp * a.jq_steps) * KW + kk;
+                valid = jq < a.Jq;
+                j = (int64_t)jp * a.Jq + jq;
+            }
+            jrow1[kk] = valid ? j / a.ilast : -1;
+            jrow2[kk] = valid ? j - (j / a.ilast) * a.ilast : 0;
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < KW * BN; e += blockDim.x) {
+            const int kk = e / BN, c = e - kk * BN;
+            const int64_t r = nt * BN + c;
+            float v = 0.f;
+            if (jrow1[kk] >= 0 && r < a.R) {
+                v = __ldg(a.t1 + jrow1[kk] * a.R + r) * __ldg(a.alast + jrow2[kk] * a.R + r);
+                if constexpr (F16) v *= __ldg(a.colscale + r);
+            }
+            vs[e] = v;
+        }
+        __syncthreads();
+        uint8_t* base = static_cast<uint8_t*>(a.out) + blk * (int64_t)(2 * BN * kRow);
+        for (int t = threadIdx.x; t < BN * kChunks; t += blockDim.x) {
+            const int n = t / kChunks, cp = t - n * kChunks;
+            const int lc = F16 ? ((cp ^ n) & 7) : ((cp ^ (n >> 1)) & 3);   // logical chunk held at cp
+            float v[kChunk];
+#pragma unroll
+            for (int q = 0; q < kChunk; ++q) v[q] = vs[(lc * kChunk + q) * BN + n];
+            uint4 hw, lw;
+            if constexpr (F16) {
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const __half2 hh = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
+                    const float2 hf = __half22float2(hh);
+                    const __half2 ll = __floats2half2_rn(v[2 * q] - hf.x, v[2 * q + 1] - hf.y);
+                    h[q] = half2_bits(hh);
+                    l[q] = half2_bits(ll);
+                }
+                hw = make_uint4(h[0], h[1], h[2], h[3]);
+                lw = make_uint4(l[0], l[1], l[2], l[3]);
+            } else {
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    h[q] = __float_as_uint(v[q]);
+                    l[q] = __float_as_uint(v[q] - __uint_as_float(h[q] & kTf32Mask));
+                }
+                hw = make_uint4(h[0], h[1], h[2], h[3]);
+                lw = make_uint4(l[0], l[1], l[2], l[3]);
+            }
+            *reinterpret_cast<uint4*>(base + (int64_t)n * kRow + cp * 16) = hw;
+            *reinterpret_cast<uint4*>(base + (int64_t)(BN + n) * kRow + cp * 16) = lw;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Peak probe of the tensor pipe (measurement only).  One CTA per SM (the
+// dynamic shared memory keeps a second one off); one thread issues `iters`
+// M128 x N256 MMAs back to back -- kind::tf32 with K = 8, or kind::f16 with
+// K = 16 -- from zero-filled shared-memory operands (64-byte swizzled K-major
+// tiles) into one TMEM accumulator, then commits and waits (bounded).
+// flops per MMA: 2 x 128 x 256 x K.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kProbeSmem = 120 * 1024;
+
+template <bool F16>
+__global__ void __launch_bounds__(128, 1) mma_probe_kernel(int iters, uint32_t* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~(uintptr_t)1023);
+    constexpr uint32_t kA = 128 * 64, kB = 256 * 64;   // 64-byte rows
+    uint64_t* done = reinterpret_cast<uint64_t*>(smem + kA + kB);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    const int tid = threadIdx.x;
+    for (uint32_t o = 16u * tid; o < kA + kB; o += 16u * blockDim.x)
+        *reinterpret_cast<uint4*>(smem + o) = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0) {
+        mbar_init(done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid < 32) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(256));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    fence_proxy_async();   // the zero fill, seen by the tensor core's reads
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (tid == 0) {
+        const uint32_t a = sdesc_lo(smem_u32(smem)), b = sdesc_lo(smem_u32(smem + kA));
+        if constexpr (F16) {
+            const uint32_t idesc = (1u << 4) | ((uint32_t)(256 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+            for (int i = 0; i < iters; ++i)
+                asm volatile(
+                    "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+                    "mov.b64 da, {%1, %3};\n\t"
+                    "mov.b64 db, {%2, %3};\n\t"
+                    "setp.ne.b32 p, %5, 0;\n\t"
+                    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}\n" ::"r"(tmem),
+                    "r"(a), "r"(b), "r"((uint32_t)(kDescSw64Hi >> 32)), "r"(idesc), "r"(i > 0 ? 1u : 0u));
+        } else {
+            const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(256 >> 3) << 17) |
+                                   ((uint32_t)(128 >> 4) << 24);
+            for (int i = 0; i < iters; ++i) mma_tf32_w(tmem, a, b, idesc, i > 0 ? 1u : 0u);
+        }
+        mma_commit(done);
+        wait_drain(done, 0, status);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid < 32) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256));
     }
 }
 
@@ -3279,14 +3484,14 @@ bool tc_plan(const Plan& p, ModePlan& mp, bool allow_fp16) {
     mp.tc_ps = mp.tc_small ? (int)(kBM / g.I) : 1;
     // innermost mode with large R: A staged in tensor memory (the i-contiguous
     // tile is transposed on the way into TMEM, no shared-memory round trip)
-    mp.tc_tmem = (!mp.tc_small && g.R >= TC_TMEM_MIN_R && (mp.tc_inner || TC_TMEM_KMAJOR)) ? 1 : 0;
+    mp.tc_tmem = (!mp.explicit_krp && !mp.tc_small && g.R >= TC_TMEM_MIN_R && (mp.tc_inner || TC_TMEM_KMAJOR)) ? 1 : 0;
     // the two-term fp16 split in tensor memory (128 x 224 tiles) does a K-step
     // about 1.4 times faster than the tf32 kernel (128 x 256 tiles): it wins
     // unless its narrower tiles waste more columns than that
     {
         const int64_t h2_cols = cdiv64(g.R, kH2BN) * kH2BN * 10;
         const int64_t tf_cols = cdiv64(g.R, 256) * 256 * 14;
-        mp.tc_h2 = (allow_fp16 && !mp.tc_small && g.R >= TC_H2_MIN_R && h2_cols < tf_cols) ? 1 : 0;
+        mp.tc_h2 = (allow_fp16 && !mp.explicit_krp && !mp.tc_small && g.R >= TC_H2_MIN_R && h2_cols < tf_cols) ? 1 : 0;
     }
     if (mp.tc_h2) mp.tc_tmem = 1;
     mp.tc_kw = mp.tc_h2 ? kBK2 : kBK;
@@ -3340,6 +3545,29 @@ bool tc_plan(const Plan& p, ModePlan& mp, bool allow_fp16) {
     // chunks per CTA where possible
     const int64_t tiles = (mp.tc_small ? 1 : cdiv64(g.I, kBM)) * cdiv64(g.R, mp.bn);
     const int64_t sms = sm_count();
+    if (mp.explicit_krp) {
+        // one pre index: split the B chunks instead
+        if (cdiv64(g.R, mp.bn) > kKrpMaxBN || mp.bn > kKrpMaxBN) return false;
+        const int ck = mp.tc_img ? kImgCK
+                                 : (int)(((mp.tc_inner ? TC_BRES_INNER_KB : TC_BRES_KB) * 1024) /
+                                         (2 * mp.bn * kBK * 4));
+        const int64_t njc = cdiv64(mp.tc_ks, ck);
+        int64_t best = 1;
+        double best_eff = -1.0;
+        for (int64_t S = 1; S <= njc && S * tiles <= 8 * sms; ++S) {
+            const int64_t ctas = S * tiles;
+            const double eff = (double)ctas / (double)(cdiv64(ctas, sms) * sms);
+            if (eff > best_eff + 0.02) {
+                best_eff = eff;
+                best = S;
+            }
+        }
+        const int64_t jcps = cdiv64(njc, best);
+        mp.jc_per_split = (int)jcps;
+        mp.splits = cdiv64(njc, jcps);
+        mp.pre_per_split = 1;
+        return true;
+    }
     const int64_t smax = g.npre;
     int64_t best = 1;
     double best_eff = -1.0;
@@ -3516,7 +3744,41 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
         }
         ++*nlaunch;
     }
-    {
+    if (mp.explicit_krp) {
+        KrpImgArgs b;
+        memset(&b, 0, sizeof(b));
+        const int last = g.group[g.ngroup - 1];
+        b.t1 = reinterpret_cast<const float*>(ws_base + mp.off_t1);
+        b.alast = factors[last];
+        b.ilast = p.dims[last];
+        b.colscale = colscale;
+        b.R = g.R;
+        b.J = g.J;
+        b.Jq = g.Jq;
+        b.BN = mp.bn;
+        b.KS = mp.tc_ks;
+        b.jq_steps = mp.tc_jq_steps;
+        b.inner = mp.tc_inner;
+        b.nblocks = cdiv64(g.R, mp.bn) * mp.tc_ks;
+        b.out = bimg;
+        int64_t blocks = b.nblocks < 152 * 8 ? b.nblocks : 152 * 8;
+        const int kw = mp.tc_img ? kBK4 : kBK;
+        const size_t smem = (size_t)kw * mp.bn * sizeof(float);
+        cudaError_t e = cudaSuccess;
+        if (mp.tc_img) {
+            e = cudaFuncSetAttribute(krp_image_kernel<kBK4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(kBK4 * kKrpMaxBN * sizeof(float)));
+            if (e == cudaSuccess) krp_image_kernel<kBK4, true><<<(unsigned)blocks, 256, smem, stream>>>(b);
+        } else {
+            krp_image_kernel<kBK, false><<<(unsigned)blocks, 256, smem, stream>>>(b);
+        }
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            snprintf(errbuf, errlen, "Khatri-Rao image launch: %s", cudaGetErrorString(e));
+            return MTTKRP_ERR_CUDA;
+        }
+        ++*nlaunch;
+    } else {
         BImgArgs b;
         memset(&b, 0, sizeof(b));
         b.ngroup = g.ngroup;
@@ -3567,6 +3829,7 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     args.KS = mp.tc_ks;
     args.jq_steps = mp.tc_jq_steps;
     args.ps = mp.tc_small ? mp.tc_ps : 1;
+    args.jc_per_split = mp.explicit_krp ? mp.jc_per_split : 0;
     args.batch_len = nQ > 1 ? nQ : g.npre;
     args.y_box_bytes = mp.tc_img ? (uint32_t)kBK4 * 2u *   // one fp16 image tile
                                        (mp.tc_small ? (uint32_t)(g.I * mp.tc_ps) : (uint32_t)kBM)
@@ -3625,6 +3888,30 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     }
     ++*nlaunch;
     return MTTKRP_OK;
+}
+
+cudaError_t tc_launch_mma_probe(int kind, int blocks, int iters, cudaStream_t s) {
+    static bool attr_set[64][2] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    uint32_t* status = tc_status_ptr();
+    if (status == nullptr) return cudaErrorInvalidSymbol;
+    const int f16 = kind == 1 ? 1 : 0;
+    if (!attr_set[dev][f16]) {
+        e = f16 ? cudaFuncSetAttribute(mma_probe_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kProbeSmem)
+                : cudaFuncSetAttribute(mma_probe_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kProbeSmem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev][f16] = true;
+    }
+    if (f16)
+        mma_probe_kernel<true><<<blocks, 128, kProbeSmem, s>>>(iters, status);
+    else
+        mma_probe_kernel<false><<<blocks, 128, kProbeSmem, s>>>(iters, status);
+    return cudaGetLastError();
 }
 
 uint32_t* tc_status_ptr() {

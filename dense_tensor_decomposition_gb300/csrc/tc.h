@@ -26,6 +26,9 @@ int tc_prepare(const Plan& p, const ModePlan& mp, const float* Y, void* ws, cuda
 int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const* factors,
            const float* gtab, const int64_t* basetab, void* binner_ws, float* dst,
            cudaStream_t stream, int* nlaunch, cudaEvent_t* start_ev, char* errbuf, size_t errlen);
+// Peak probe of the tensor pipe: `blocks` CTAs (one per SM), each issuing `iters`
+// M128 x N256 MMAs of kind::tf32 (kind 0, K = 8) or kind::f16 (kind 1, K = 16).
+cudaError_t tc_launch_mma_probe(int kind, int blocks, int iters, cudaStream_t s);
 // Device address of the error word on the current device (null on failure).
 uint32_t* tc_status_ptr();
 // Arm the failure-detection test hook for the next `count` launches.

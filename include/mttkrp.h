@@ -68,8 +68,12 @@ enum mttkrp_path {
     MTTKRP_PATH_AUTO = 0,
     MTTKRP_PATH_SIMT = 1,   /* fp32 FMA on the CUDA cores */
     MTTKRP_PATH_TC = 2,     /* tcgen05 tensor cores, fp32-accurate split (fp16 two-term or 3xTF32) */
-    MTTKRP_PATH_TC_TF32 = 3 /* tcgen05 tensor cores, 3xTF32 split only (no fp16): for tensors whose
-                               entries span more than the fp16 split's range (see mttkrp_plan) */
+    MTTKRP_PATH_TC_TF32 = 3, /* tcgen05 tensor cores, 3xTF32 split only (no fp16): for tensors whose
+                                entries span more than the fp16 split's range (see mttkrp_plan) */
+    MTTKRP_PATH_TC_EXPLICIT_KRP = 4 /* the matrix-based variant, for comparison: the Khatri-Rao
+                                product of all modes but k is formed explicitly in the workspace
+                                (4 * R * prod_{n != k} I_n bytes, plus padding) and Y_(k) is
+                                multiplied by it on the tensor cores */
 };
 
 typedef struct mttkrp_plan_s* mttkrp_plan_t;
@@ -265,6 +269,24 @@ int mttkrp_apply_rotations(int d, const int64_t* dims, float* Y, int mode, const
  */
 int mttkrp_ttm(int d, const int64_t* dims, const float* X, int mode, const float* M, int64_t J, float* T,
                void* stream);
+
+/*
+ * Peak probes for the roofline of a benchmark (measurement only; the pages have
+ * no counterpart).  Both enqueue one kernel on `stream` and return; the caller
+ * times it with events.
+ *   mttkrp_probe_fma: `blocks` x 256 threads, each running `iters` iterations of
+ *     eight independent fp32 fused multiply-add chains; out (device, blocks x 256
+ *     floats) receives each thread's sum.  flops = 16 x iters x blocks x 256.
+ *   mttkrp_probe_mma: `blocks` CTAs (one per SM: launch as many as there are SMs),
+ *     each with one thread issuing `iters` tcgen05 MMAs of M = 128, N = 256 back to
+ *     back into tensor memory, kind::tf32 (kind 0, K = 8) or kind::f16 (kind 1,
+ *     K = 16), on zero operands.  flops = 2 x 128 x 256 x K x iters x blocks.
+ *     Its wait for the MMAs to finish is bounded (mttkrp_device_status reports
+ *     an expiry).
+ * Errors: MTTKRP_ERR_INVALID for bad counts or a NULL out; MTTKRP_ERR_CUDA.
+ */
+int mttkrp_probe_fma(int blocks, int iters, float* out, void* stream);
+int mttkrp_probe_mma(int kind, int blocks, int iters, void* stream);
 
 /* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
 int mttkrp_version(void);
