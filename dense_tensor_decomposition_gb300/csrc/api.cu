@@ -776,7 +776,8 @@ int mttkrp_plan_describe(mttkrp_plan_t h, int mode, char* buf, size_t len) {
         snprintf(kernel, sizeof(kernel), "simt.bn%d", mp.bn);
     } else {
         const char* fam = mp.tc_img ? "img" : mp.tc_h2 ? "h2" : mp.tc_tmem ? "tf32tm" : "tf32";
-        const char* lay = mp.tc_img ? (mp.tc_img_t ? "t" : "nat") : (mp.tc_inner ? "inner" : "kmaj");
+        const char* lay = mp.tc_img ? (mp.tc_img_t ? "t" : mp.tc_img_mn ? "mn" : "nat")
+                                    : (mp.tc_inner ? "inner" : "kmaj");
         snprintf(kernel, sizeof(kernel), "%s.%s%s.bn%d", fam, lay, mp.tc_small ? ".small" : "", mp.bn);
     }
     // fp32 bytes of the explicit Khatri-Rao product of every mode but this one
@@ -799,7 +800,8 @@ int mttkrp_plan_describe(mttkrp_plan_t h, int mode, char* buf, size_t len) {
                      mode, mp.path == MTTKRP_PATH_TC ? "tc" : "simt", kernel, mp.bm, mp.bn, groups,
                      (long long)g.J, (long long)g.Jq, pres, (long long)g.npre,
                      (long long)mp.splits, (long long)mp.pre_per_split, mp.total, mp.tc_ks, mp.tc_inner,
-                     mp.tc_small ? mp.tc_ps : 1, mp.tc_tmem, mp.tc_h2 || mp.tc_img, mp.tc_img + mp.tc_img_t,
+                     mp.tc_small ? mp.tc_ps : 1, mp.tc_tmem, mp.tc_h2 || mp.tc_img,
+                     mp.tc_img ? (mp.tc_img_t ? 2 : mp.tc_img_mn ? 3 : 1) : 0,
                      mp.explicit_krp ? "explicit" : "free", (unsigned long long)krp_bytes,
                      mp.off_binner - mp.off_partials, mp.off_end - mp.off_binner, ws_images);
     if (buf != nullptr && len > 0) {

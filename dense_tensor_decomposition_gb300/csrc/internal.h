@@ -65,6 +65,8 @@ struct ModePlan {
                         //    operands in shared memory (K-steps of 64)
     int tc_img_t;       // tc_img for the innermost mode: from the transposed images
                         //    (Y viewed as P x I_{d-1}, stored I_{d-1} x P)
+    int tc_img_mn;      // tc_img for the innermost mode: from the natural images, A read
+                        //    MN-major (i contiguous) by the tensor cores
     // explicit Khatri-Rao product (the matrix-based comparison variant): the
     // inner group is every mode but k (one pre index), the B images hold the
     // whole product, and the contraction is split over B chunks, jc_per_split

@@ -26,8 +26,12 @@ __device__ __forceinline__ float4 ldg4(const float* p) {
     return __ldg(reinterpret_cast<const float4*>(p));
 }
 
+// 128 x 128 tiles with vector loads of Y are held to 128 registers a thread, so
+// two CTAs (16 warps) share an SM: the extra warps hide the latency of the
+// shared-memory and global loads behind other warps' FMAs (no spills at that
+// bound; the scalar-load variants would spill and keep one CTA per SM).
 template <int BM, int BN, int BK, int AMODE, bool BVEC>
-__global__ void __launch_bounds__((BM / 8) * (BN / 8))
+__global__ void __launch_bounds__((BM / 8) * (BN / 8), (BM == 128 && BN == 128 && AMODE != kLoadScalar) ? 2 : 1)
     simt_kernel(const SimtArgs a) {
     constexpr int NT = (BM / 8) * (BN / 8);
     constexpr int APAD = 4;

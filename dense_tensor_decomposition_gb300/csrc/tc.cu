@@ -2157,8 +2157,19 @@ struct SmemImg {
     static_assert((2 * kStages + 7) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
-template <int BN, bool SMALL>
+// MN-major A operand (the innermost mode from the natural images, MN = true):
+// each image tile is two TMA boxes of 64 i (128 bytes, contiguous in the image)
+// x 64 contraction indices, 8 KB apart, which is the canonical MN-major layout
+// with a 128-byte swizzle: 8-row groups of K 1024 bytes apart (stride offset),
+// the two 64-row halves of M 8192 bytes apart (leading offset); a slice of 16
+// contraction indices advances the start address by 16 rows (2048 bytes).
+constexpr uint32_t kDescMnLo = (uint32_t)((8192 >> 4) << 16);   // leading byte offset: M halves
+
+__device__ __forceinline__ uint32_t sdesc128mn_lo(uint32_t saddr) { return kDescMnLo | ((saddr & 0x3FFFFu) >> 4); }
+
+template <int BN, bool SMALL, bool MN>
 __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_constant__ TcArgs a) {
+    static_assert(!(SMALL && MN), "stacked tiles read K-major images");
     using L = SmemImg<BN, SMALL>;
     constexpr int NS = L::kStages;
     constexpr int CK = kImgCK;
@@ -2294,8 +2305,19 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                         }
                         uint8_t* st = ring + rr.slot * L::kStage;
                         mbar_arrive_expect_tx(&full[rr.slot], 2u * a.y_box_bytes);
-                        tma_load(&a.ymap, a.rank, c, st, &full[rr.slot]);
-                        tma_load(&a.ymap_lo, a.rank, c, st + L::kA, &full[rr.slot]);
+                        if constexpr (MN) {
+                            // two 64-row halves of M per image
+                            int c2[5];
+                            role[kRoleI] = (int)m0 + 64;
+                            tma_coords(a.slot, role, c2);
+                            tma_load(&a.ymap, a.rank, c, st, &full[rr.slot]);
+                            tma_load(&a.ymap, a.rank, c2, st + L::kA / 2, &full[rr.slot]);
+                            tma_load(&a.ymap_lo, a.rank, c, st + L::kA, &full[rr.slot]);
+                            tma_load(&a.ymap_lo, a.rank, c2, st + L::kA + L::kA / 2, &full[rr.slot]);
+                        } else {
+                            tma_load(&a.ymap, a.rank, c, st, &full[rr.slot]);
+                            tma_load(&a.ymap_lo, a.rank, c, st + L::kA, &full[rr.slot]);
+                        }
                     }
                     if (!SMALL && ++cQ == nQ) {
                         cQ = 0;
@@ -2309,9 +2331,11 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             if (jc_loaded >= 0) wait_drain_inl(bfull, (uint32_t)((jc_loaded - jc0) & 1), a.status);
         } else if (warp == 1 && lane == 0) {
             // ------------------------- MMA issuer -------------------------
-            // kind::f16: fp16 A and B (both K-major), fp32 accumulator
-            const uint32_t idesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-            const uint32_t a_w0 = sdesc128_lo(smem_u32(ring));
+            // kind::f16: fp16 A and B (B K-major; A K-major, or MN-major with the
+            // transpose-A bit), fp32 accumulator
+            const uint32_t idesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24) |
+                                   (MN ? (1u << 15) : 0u);
+            const uint32_t a_w0 = MN ? sdesc128mn_lo(smem_u32(ring)) : sdesc128_lo(smem_u32(ring));
             const uint32_t b_w0 = sdesc128_lo(smem_u32(bres));
             constexpr uint32_t kAStep = L::kStage >> 4;
             constexpr uint32_t kALo = L::kA >> 4;
@@ -2351,9 +2375,11 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint32_t adv = (uint32_t)kk * 2u;   // 16 fp16 = 32 bytes
-                            mma_f16_ss(dz, aw + adv, bw + adv, idesc, (first && kk == 0) ? 0u : 1u);
-                            mma_f16_ss(dz, aw + adv, bw + kBLo + adv, idesc, 1u);
-                            mma_f16_ss(dz, aw + kALo + adv, bw + adv, idesc, 1u);
+                            // A: 32 bytes along a K-major row, or 16 rows of 128 bytes MN-major
+                            const uint32_t adva = MN ? (uint32_t)kk * 128u : adv;
+                            mma_f16_ss(dz, aw + adva, bw + adv, idesc, (first && kk == 0) ? 0u : 1u);
+                            mma_f16_ss(dz, aw + adva, bw + kBLo + adv, idesc, 1u);
+                            mma_f16_ss(dz, aw + kALo + adva, bw + adv, idesc, 1u);
                         }
                         mma_commit(&empty[rr.slot]);
                         if (last) {
@@ -3281,7 +3307,7 @@ bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides,
     }
     if (mp.tc_inner) {
         if (mg.slot[kRoleI] != 0) return false;   // i contiguous
-        mg.box[mg.slot[kRoleJq]] = (uint32_t)mp.tc_kw;
+        mg.box[mg.slot[kRoleJq]] = (uint32_t)(mp.tc_img_mn ? kBK4 : mp.tc_kw);
         if (mp.tc_small) {
             const int batch_role = sizeQ > 1 ? kRolePQ : kRolePP;
             if (mg.slot[batch_role] < 0 || mp.tc_ps < 2 || mp.tc_ps > 256 || (g.I * 4) % 16 != 0)
@@ -3289,7 +3315,7 @@ bool y_map_geom(const ModePlan& mp, const int64_t* dims, const int64_t* strides,
             mg.box[0] = (uint32_t)g.I;
             mg.box[mg.slot[batch_role]] = (uint32_t)mp.tc_ps;
         } else {
-            mg.box[0] = kBM;
+            mg.box[0] = mp.tc_img_mn ? 64u : (uint32_t)kBM;   // MN-major: two boxes of 64 rows
         }
     } else {
         if (mg.slot[kRoleJq] != 0) return false;
@@ -3388,7 +3414,7 @@ cudaError_t launch_h2(const TcArgs& args, dim3 grid, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int BN, bool SMALL = false>
+template <int BN, bool SMALL = false, bool MN = false>
 cudaError_t launch_img(const TcArgs& args, dim3 grid, cudaStream_t s) {
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -3399,15 +3425,15 @@ cudaError_t launch_img(const TcArgs& args, dim3 grid, cudaStream_t s) {
         // setmaxnreg.inc waits until the pool allotted at launch can serve it:
         // refuse a build whose launch allotment is below what the split assumes
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, tc_img_kernel<BN, SMALL>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, tc_img_kernel<BN, SMALL, MN>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs < kImgRegsLaunch || fa.numRegs * kImgThreads > 65536) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(tc_img_kernel<BN, SMALL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(tc_img_kernel<BN, SMALL, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)SmemImg<BN, SMALL>::kTotal);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    tc_img_kernel<BN, SMALL><<<grid, kImgThreads, SmemImg<BN, SMALL>::kTotal, s>>>(args);
+    tc_img_kernel<BN, SMALL, MN><<<grid, kImgThreads, SmemImg<BN, SMALL>::kTotal, s>>>(args);
     return cudaGetLastError();
 }
 
@@ -3521,7 +3547,13 @@ bool tc_plan(const Plan& p, ModePlan& mp, bool allow_fp16) {
         MapGeom mgi;
         if (!mp.tc_inner) {
             if (cdiv64(g.Jq, kBK4) * kBK4 * 8 <= g.Jq * 9 && y_map_geom(t, p.dims, p.strides, p.d, mgi, 2)) mp = t;
+        } else if (!mp.tc_small && cdiv64(g.J, kBK4) * kBK4 * 8 <= g.J * 9 &&
+                   (t.tc_img_mn = 1, y_map_geom(t, p.dims, p.strides, p.d, mgi, 2))) {
+            // the innermost mode from the natural images, A MN-major (boxes of
+            // 64 i x 64 j; the i stride of the image a 16-byte multiple)
+            mp = t;
         } else if (TC_IMG_XPOSE && timg_eligible(g, p.d) && cdiv64(g.J, kBK4) * kBK4 * 8 <= g.J * 9) {
+            t.tc_img_mn = 0;
             // the innermost mode from the transposed images (written in the same
             // pass as the others); the K-steps run over j alone
             t.tc_img_t = 1;
@@ -3536,7 +3568,7 @@ bool tc_plan(const Plan& p, ModePlan& mp, bool allow_fp16) {
         mp.tc_jq_steps = (int)cdiv64(g.Jq, mp.tc_kw);
         mp.tc_ks = (int)((g.J / g.Jq) * mp.tc_jq_steps);
     }
-    if (mp.tc_img_t) mp.tc_jq_steps = mp.tc_ks;   // the j role carries the whole K-step offset
+    if (mp.tc_img_t || mp.tc_img_mn) mp.tc_jq_steps = mp.tc_ks;   // the j role carries the whole K-step offset
     if ((!mp.tc_small && cdiv64(g.I, kBM) > 65535) || g.npre >= ((int64_t)1 << 31)) return false;
     MapGeom mg;
     if (mp.tc_img_t ? !timg_map_geom(mp, mg) : !y_map_geom(mp, p.dims, p.strides, p.d, mg, mp.tc_img ? 2 : 4))
@@ -3858,9 +3890,12 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
         if (mp.tc_small)
             e = mp.bn == 128 ? launch_img<128, true>(args, grid, stream) : launch_img<64, true>(args, grid, stream);
         else
-            e = mp.bn == 256 ? launch_img<256>(args, grid, stream)
-              : mp.bn == 128 ? launch_img<128>(args, grid, stream)
-                             : launch_img<64>(args, grid, stream);
+            e = mp.tc_img_mn ? (mp.bn == 256 ? launch_img<256, false, true>(args, grid, stream)
+                                : mp.bn == 128 ? launch_img<128, false, true>(args, grid, stream)
+                                               : launch_img<64, false, true>(args, grid, stream))
+                             : (mp.bn == 256 ? launch_img<256>(args, grid, stream)
+                                : mp.bn == 128 ? launch_img<128>(args, grid, stream)
+                                               : launch_img<64>(args, grid, stream));
     } else if (mp.tc_h2) {
         e = mp.tc_inner ? launch_h2<true>(args, grid, stream) : launch_h2<false>(args, grid, stream);
     } else if (mp.tc_tmem) {

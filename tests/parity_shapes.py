@@ -55,6 +55,11 @@ EDGE = [
     # 64-column image tiles with small I_k, natural and transposed images
     ((20, 3, 120), 48),
     ((8, 512, 20), 64),
+    # the innermost mode read MN-major from the natural images needs I_{d-1} a
+    # multiple of 8; at 4 mod 8 it takes the transposed images (128- and
+    # 256-column tiles) and the other modes the 3xTF32 kernels
+    ((64, 64, 132), 100),
+    ((64, 64, 132), 256),
 ]
 
 # shapes whose modes run on the fp16-split tensor-core kernels (value-range tests)

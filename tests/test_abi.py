@@ -149,17 +149,22 @@ def test_python_binding_rejects_cpu_tensors():
 
 def test_image_kernel_planning_and_workspace():
     """Host-only planner decisions for the fp16-image kernel: the K-major and
-    innermost modes of the headline shape take it, the workspace grows by the
-    two image layouts (hi + lo, 2 bytes an element each), and tensors above
-    12 Gi elements fall back to the kernels that need no images."""
+    innermost modes of the headline shape take it (the innermost mode reading
+    the natural images MN-major, flag 3), the workspace grows by one image
+    layout (hi + lo, 2 bytes an element each), a stacked small innermost mode
+    needs the transposed layout too (flag 2), and tensors above 12 Gi elements
+    fall back to the kernels that need no images."""
     def image_flags(p, d):
         return [int(p.describe(k).split("tc_fp16_image=")[1].split()[0]) for k in range(d)]
 
     p = mk.Plan((512, 512, 512), 2000)
-    assert image_flags(p, 3) == [1, 1, 2]
+    assert image_flags(p, 3) == [1, 1, 3]
     numel = 512 ** 3
-    assert p.workspace_bytes(-1) >= 2 * 2 * numel * 2          # natural + transposed, hi + lo
+    assert 2 * numel * 2 <= p.workspace_bytes(-1) < 2 * 2 * numel * 2   # natural only, hi + lo
     assert p.workspace_bytes(0) == p.workspace_bytes(-1)        # every image mode sees the region
+    q = mk.Plan((20,) * 6, 128)
+    assert image_flags(q, 6) == [1, 1, 1, 1, 0, 2]
+    assert q.workspace_bytes(-1) >= 2 * 2 * 20 ** 6 * 2         # natural + transposed
     big = mk.Plan((4096, 4096, 1024), 256)
     assert image_flags(big, 3) == [0, 0, 0]
     assert big.workspace_bytes(-1) < 4096 * 4096 * 1024        # no image region

@@ -319,14 +319,16 @@ def test_outlier_zero_column_and_zero_tensor(dims, R):
 
 def test_image_kernel_is_planned():
     """The fp16-image kernel takes the K-major modes of these shapes from the
-    natural images (tc_fp16_image=1) and the innermost mode from the transposed
-    images (=2), also with several pre indices stacked in a tile for small I_k,
-    so the edge cases above exercise all of these."""
+    natural images (tc_fp16_image=1), the innermost mode from the natural images
+    read MN-major (=3) or, for stacked small-I_k tiles and rows that are not a
+    multiple of 8, from the transposed images (=2), so the edge cases above
+    exercise all of these."""
     cases = {((200, 96, 64), 300): [1, 1, 0], ((16, 130, 8, 64), 200): [1, 1, 0, 0],
              ((20, 20, 20, 20, 20, 20), 128): [1, 1, 1, 1, 0, 2], ((16, 64, 40), 200): [0, 0, 2],
-             ((512, 512, 512), 2000): [1, 1, 2], ((128, 128, 128, 128), 256): [1, 1, 1, 2],
+             ((512, 512, 512), 2000): [1, 1, 3], ((128, 128, 128, 128), 256): [1, 1, 1, 3],
              ((136, 24, 120), 260): [1, 1, 0], ((4, 8, 136, 64), 160): [0, 0, 1, 0],
-             ((24, 120, 200), 300): [0, 0, 2], ((64, 8, 8, 150), 200): [0, 0, 0, 2]}
+             ((24, 120, 200), 300): [0, 0, 3], ((64, 8, 8, 150), 200): [0, 0, 0, 2],
+             ((64, 64, 132), 256): [0, 0, 2]}
     for (dims, R), want in cases.items():
         plan = make_plan(dims, R, "auto")
         got = [int(plan.describe(k).split("tc_fp16_image=")[1].split()[0]) for k in range(len(dims))]

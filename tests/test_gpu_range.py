@@ -31,7 +31,8 @@ TOL = 1e-5
 # (dims, R, fp16-split kernels the planner picks for some modes)
 SHAPES = [
     ((256, 96, 128), 256, {"img.nat.bn256"}),
-    ((256, 64, 128), 256, {"img.nat.bn256", "img.t.bn256"}),
+    ((256, 64, 128), 256, {"img.nat.bn256", "img.mn.bn256"}),
+    ((64, 64, 132), 256, {"img.t.bn256"}),
     ((130, 6, 7, 100), 500, {"h2.kmaj.bn224", "h2.inner.bn224"}),
     ((40, 36, 128), 450, {"img.nat.small.bn128", "h2.inner.bn224"}),
     ((48, 64, 40), 130, {"img.t.small.bn128"}),

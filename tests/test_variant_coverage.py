@@ -18,13 +18,15 @@ from parity_shapes import EDGE, H2_SHAPES
 
 mk = pytest.importorskip("dense_tensor_decomposition_gb300")
 
-# family.layout[.small].bn<columns>; families: simt, img (fp16 images of Y),
+# family.layout[.small].bn<columns>; families: simt, img (fp16 images of Y:
+# natural, transposed, or natural read MN-major),
 # h2 (fp16 split in tensor memory), tf32 (3xTF32, A in shared memory),
 # tf32tm (3xTF32, A in tensor memory)
 KNOWN = {
     "simt.bn64", "simt.bn128",
     "img.nat.bn64", "img.nat.bn128", "img.nat.bn256", "img.nat.small.bn64", "img.nat.small.bn128",
     "img.t.bn64", "img.t.bn128", "img.t.bn256", "img.t.small.bn64", "img.t.small.bn128",
+    "img.mn.bn64", "img.mn.bn128", "img.mn.bn256",
     "h2.kmaj.bn224", "h2.inner.bn224",
     "tf32.kmaj.bn64", "tf32.kmaj.bn128", "tf32.kmaj.bn256",
     "tf32.inner.bn64", "tf32.inner.bn128", "tf32.inner.bn256",
@@ -90,6 +92,6 @@ def test_every_variant_is_gpu_tested():
 def test_headline_workload_kernels():
     """The planner's choice on the largest workload, and the 3xTF32 kernels the
     forced path takes there (the innermost mode with A in tensor memory)."""
-    assert kernels((512,) * 3, 2000, "auto") == ["img.nat.bn256", "img.nat.bn256", "img.t.bn256"]
+    assert kernels((512,) * 3, 2000, "auto") == ["img.nat.bn256", "img.nat.bn256", "img.mn.bn256"]
     assert kernels((512,) * 3, 2000, "tc_tf32") == ["tf32.kmaj.bn256", "tf32.kmaj.bn256",
                                                      "tf32tm.inner.bn224"]
