@@ -20,7 +20,8 @@ import threading
 
 from ._build import LIB as LIB_PATH, build  # noqa: F401
 
-__all__ = ["Plan", "mttkrp", "all_modes", "apply_rotations", "ttm", "probe_fma", "probe_mma", "MttkrpError",
+__all__ = ["Plan", "mttkrp", "all_modes", "apply_rotations", "ttm", "ttm_workspace_bytes", "probe_fma", "probe_mma",
+           "MttkrpError",
            "build", "load_library",
            "exported_symbols", "PATH_AUTO", "PATH_SIMT", "PATH_TC", "PATH_TC_TF32", "PATH_TC_EXPLICIT_KRP"]
 
@@ -85,6 +86,10 @@ def load_library():
         lib.mttkrp_apply_rotations.restype = ci
         lib.mttkrp_ttm.argtypes = [ci, vp, vp, ci, vp, i64, vp, vp]
         lib.mttkrp_ttm.restype = ci
+        lib.mttkrp_ttm_workspace_bytes.argtypes = [ci, vp, ci, i64]
+        lib.mttkrp_ttm_workspace_bytes.restype = sz
+        lib.mttkrp_ttm_ws.argtypes = [ci, vp, vp, ci, vp, i64, vp, vp, sz, vp]
+        lib.mttkrp_ttm_ws.restype = ci
         lib.mttkrp_cp_als_scratch_bytes.argtypes = [vp]
         lib.mttkrp_cp_als_scratch_bytes.restype = sz
         lib.mttkrp_cp_als_sweep.argtypes = [vp, vp, vp, vp, vp, ci, vp, vp, sz, vp]
@@ -401,10 +406,19 @@ def apply_rotations(Y, mode: int, pairs, c, s, stream=None):
     return Y
 
 
-def ttm(X, mode: int, M, out=None, stream=None):
-    """T = X x_mode M (mttkrp_ttm): M is a float32 CUDA matrix J x X.shape[mode];
-    returns T (X's shape with that mode's size replaced by J), written into
-    `out` when given (contiguous float32, not overlapping X or M)."""
+def ttm_workspace_bytes(shape, mode: int, J: int) -> int:
+    """Workspace bytes of the tensor-core mode-n product (0: it does not take the shape)."""
+    dims = (ctypes.c_int64 * len(shape))(*shape)
+    return int(load_library().mttkrp_ttm_workspace_bytes(len(shape), dims, mode, int(J)))
+
+
+def ttm(X, mode: int, M, out=None, stream=None, path: str = "auto"):
+    """T = X x_mode M: M is a float32 CUDA matrix J x X.shape[mode]; returns T
+    (X's shape with that mode's size replaced by J), written into `out` when
+    given (contiguous float32, not overlapping X or M).  path "simt": the CUDA-core
+    kernel (mttkrp_ttm); "auto": the tensor cores when they take the shape
+    (mttkrp_ttm_ws with a PyTorch-allocated workspace), else the CUDA cores; "tc":
+    the tensor cores or an error."""
     import torch
     lib = load_library()
     for name, t in (("X", X), ("M", M)):
@@ -420,6 +434,17 @@ def ttm(X, mode: int, M, out=None, stream=None):
           or not out.is_contiguous() or list(out.shape) != shape):
         raise ValueError(f"out must be a contiguous float32 CUDA tensor of shape {shape}")
     dims = (ctypes.c_int64 * X.dim())(*X.shape)
+    if path not in ("auto", "simt", "tc"):
+        raise ValueError(f"unknown path {path!r}")
+    need = 0 if path == "simt" else int(lib.mttkrp_ttm_workspace_bytes(X.dim(), dims, mode, int(M.shape[0])))
+    if path == "tc" and need == 0:
+        raise MttkrpError(2, "ttm", "the tensor-core mode-n product does not take this shape")
+    if need > 0:
+        ws = torch.empty(need, dtype=torch.uint8, device=X.device)
+        _check(lib.mttkrp_ttm_ws(X.dim(), dims, ctypes.c_void_p(X.data_ptr()), mode, ctypes.c_void_p(M.data_ptr()),
+                                 int(M.shape[0]), ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+                                 need, _stream_handle(X.device, stream)), "mttkrp_ttm_ws")
+        return out
     _check(lib.mttkrp_ttm(X.dim(), dims, ctypes.c_void_p(X.data_ptr()), mode, ctypes.c_void_p(M.data_ptr()),
                           int(M.shape[0]), ctypes.c_void_p(out.data_ptr()), _stream_handle(X.device, stream)),
            "mttkrp_ttm")

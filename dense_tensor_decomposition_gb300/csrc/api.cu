@@ -642,9 +642,13 @@ int mttkrp_apply_rotations(int d, const int64_t* dims, float* Y, int mode, const
     return MTTKRP_OK;
 }
 
-int mttkrp_ttm(int d, const int64_t* dims, const float* X, int mode, const float* M, int64_t J, float* T,
-               void* stream) {
-    g_errmsg[0] = 0;
+}  // extern "C"
+
+namespace mk {
+namespace {
+// Argument checks of the mode-n product; P, N, Q of X viewed [P, N, Q].
+int ttm_check(int d, const int64_t* dims, const float* X, int mode, const float* M, int64_t J, const float* T,
+              int64_t* Pout, int64_t* Nout, int64_t* Qout) {
     if (d < 1 || d > kMaxD) return fail(MTTKRP_ERR_INVALID, "order d=%d outside [1, %d]", d, kMaxD);
     if (dims == nullptr || X == nullptr || M == nullptr || T == nullptr)
         return fail(MTTKRP_ERR_INVALID, "NULL dims, tensor, matrix or result");
@@ -670,7 +674,54 @@ int mttkrp_ttm(int d, const int64_t* dims, const float* X, int mode, const float
     const uintptr_t m0 = reinterpret_cast<uintptr_t>(M), m1 = m0 + (uintptr_t)(J * N) * 4;
     if ((t0 < x1 && x0 < t1) || (t0 < m1 && m0 < t1))
         return fail(MTTKRP_ERR_INVALID, "the result overlaps X or M");
+    *Pout = P;
+    *Nout = N;
+    *Qout = Q;
+    return MTTKRP_OK;
+}
+}  // namespace
+}  // namespace mk
+
+extern "C" {
+
+int mttkrp_ttm(int d, const int64_t* dims, const float* X, int mode, const float* M, int64_t J, float* T,
+               void* stream) {
+    g_errmsg[0] = 0;
+    int64_t P, N, Q;
+    const int rc = ttm_check(d, dims, X, mode, M, J, T, &P, &N, &Q);
+    if (rc != MTTKRP_OK) return rc;
     cudaError_t e = launch_ttm(X, M, T, P, N, Q, J, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "mode-n product launch: %s", cudaGetErrorString(e));
+    return MTTKRP_OK;
+}
+
+size_t mttkrp_ttm_workspace_bytes(int d, const int64_t* dims, int mode, int64_t J) {
+    if (d < 1 || d > kMaxD || dims == nullptr || mode < 0 || mode >= d || J < 1) return 0;
+    int64_t P = 1, Q = 1, numel = 1;
+    for (int n = 0; n < d; ++n) {
+        if (dims[n] < 1 || dims[n] > kMaxNumel || numel > kMaxNumel / dims[n]) return 0;
+        numel *= dims[n];
+        if (n < mode) P *= dims[n];
+        if (n > mode) Q *= dims[n];
+    }
+    return tc_ttm_workspace_bytes(P, dims[mode], Q, J);
+}
+
+int mttkrp_ttm_ws(int d, const int64_t* dims, const float* X, int mode, const float* M, int64_t J, float* T,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+    g_errmsg[0] = 0;
+    int64_t P, N, Q;
+    const int rc = ttm_check(d, dims, X, mode, M, J, T, &P, &N, &Q);
+    if (rc != MTTKRP_OK) return rc;
+    const size_t need = tc_ttm_workspace_bytes(P, N, Q, J);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (need > 0 && workspace != nullptr && workspace_bytes >= need &&
+        (reinterpret_cast<uintptr_t>(X) & 15) == 0 && (reinterpret_cast<uintptr_t>(workspace) & 255) == 0)
+        return tc_ttm_run(X, M, T, P, N, Q, J, workspace, s, g_errmsg, sizeof(g_errmsg));
+    if (need > 0 && workspace != nullptr && workspace_bytes < need)
+        return fail(MTTKRP_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes needed", workspace_bytes,
+                    need);
+    cudaError_t e = launch_ttm(X, M, T, P, N, Q, J, s);
     if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "mode-n product launch: %s", cudaGetErrorString(e));
     return MTTKRP_OK;
 }

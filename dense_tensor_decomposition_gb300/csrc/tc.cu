@@ -88,6 +88,8 @@ struct TcArgs {
     int withhold_signal;      // test hook: skip the first accumulator-ready commit
     int jc_per_split;         // > 0: blockIdx.z splits the B chunks (this many a CTA), every
                               // CTA takes all pre indices (explicit Khatri-Rao product)
+    int64_t ttm_q;            // > 0: mode-n product; tile row m is (p, q) = (m / ttm_q, m % ttm_q)
+                              // of X viewed [P, N, Q], and column j goes to T[p, j, q]
     uint32_t y_box_bytes;     // bytes of one Y tile copy
     // small-I variant: ps pre indices share one 128-row tile (rows slot * I + i)
     int ps;                   // pre-index slots per tile (1 otherwise)
@@ -2045,7 +2047,16 @@ __global__ void __launch_bounds__(kH2Threads, 1) tc_h2_kernel(const __grid_const
             }
         }
         asm volatile("cp.async.wait_group 0;" ::: "memory");
-        if (!*abort_flag && row < a.I) {
+        if (!*abort_flag && row < a.I && a.ttm_q > 0) {
+            // mode-n product: column j of row (p, q) is T[p, j, q]; the lanes of a
+            // warp hold consecutive q, so each store instruction writes 128 bytes
+            const float inv_y = y_unscale(a, row);
+            const int64_t p = row / a.ttm_q, q = row - p * a.ttm_q;
+            float* dst = a.dst + p * a.R * a.ttm_q + q;
+#pragma unroll
+            for (int e = 0; e < kCols; ++e)
+                if (c0 + e < a.R) dst[(c0 + e) * a.ttm_q] = acc[e] * inv_y * pow2_recip(a.colscale[c0 + e]);
+        } else if (!*abort_flag && row < a.I) {
             // undo the power-of-two scales of Y and of each Binner column (exact)
             const float inv_y = y_unscale(a, row);
             float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride + row * a.R + c0;
@@ -2266,6 +2277,15 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             // the pre index pi = (cP, cQ) in C order, advanced without divisions
             const int64_t nQ = a.nQ;
             const int cP0 = (int)(pre_lo / nQ), cQ0 = (int)(pre_lo - (int64_t)cP0 * nQ);
+            // mode-n product: (p, q) of the first row of each 64-row half
+            int ttm_q0 = 0, ttm_p0 = 0, ttm_q1 = 0, ttm_p1 = 0;
+            if (MN && a.ttm_q > 0) {
+                ttm_p0 = (int)(m0 / a.ttm_q);
+                ttm_q0 = (int)(m0 - (int64_t)ttm_p0 * a.ttm_q);
+                ttm_p1 = (int)((m0 + 64) / a.ttm_q);
+                ttm_q1 = (int)(m0 + 64 - (int64_t)ttm_p1 * a.ttm_q);
+            }
+            (void)ttm_q0; (void)ttm_p0; (void)ttm_q1; (void)ttm_p1;
             for (int jc = jc0; jc < jc1 && ok; ++jc) {
                 const int ck = chunk_len(jc);
                 // the first NS tiles of chunk jc need only work of chunk jc - 1,
@@ -2308,7 +2328,16 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                         if constexpr (MN) {
                             // two 64-row halves of M per image
                             int c2[5];
-                            role[kRoleI] = (int)m0 + 64;
+                            if (a.ttm_q > 0) {
+                                // mode-n product: each half is 64 consecutive q of one p
+                                role[kRoleI] = ttm_q0;
+                                role[kRolePP] = ttm_p0;
+                                tma_coords(a.slot, role, c);
+                                role[kRoleI] = ttm_q1;
+                                role[kRolePP] = ttm_p1;
+                            } else {
+                                role[kRoleI] = (int)m0 + 64;
+                            }
                             tma_coords(a.slot, role, c2);
                             tma_load(&a.ymap, a.rank, c, st, &full[rr.slot]);
                             tma_load(&a.ymap, a.rank, c2, st + L::kA / 2, &full[rr.slot]);
@@ -2529,7 +2558,16 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                 zb ^= 1;
             }
         }
-        if (!*abort_flag && row < a.I) {
+        if (!*abort_flag && row < a.I && a.ttm_q > 0) {
+            // mode-n product: column j of row (p, q) is T[p, j, q]; the lanes of a
+            // warp hold consecutive q, so each store instruction writes 128 bytes
+            const float inv_y = y_unscale(a, row);
+            const int64_t p = row / a.ttm_q, q = row - p * a.ttm_q;
+            float* dst = a.dst + p * a.R * a.ttm_q + q;
+#pragma unroll
+            for (int e = 0; e < kCols; ++e)
+                if (c0 + e < a.R) dst[(c0 + e) * a.ttm_q] = acc[e] * inv_y * pow2_recip(a.colscale[c0 + e]);
+        } else if (!*abort_flag && row < a.I) {
             // undo the power-of-two scales of Y and of each Binner column (exact)
             const float inv_y = y_unscale(a, row);
             float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride + row * a.R + c0;
@@ -3122,6 +3160,19 @@ __global__ void __launch_bounds__(256) krp_image_kernel(KrpImgArgs a) {
         }
         __syncthreads();
     }
+}
+
+// Mode-n product on the tensor cores: M^T (N x J, row-major) from M (J x N), the
+// inner table of the "2-way MTTKRP" the product is computed as, and a row of
+// J ones for its G table.
+__global__ void ttm_prep_kernel(const float* __restrict__ M, int64_t J, int64_t N, float* __restrict__ mt,
+                                float* __restrict__ ones) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < J * N; e += stride) {
+        const int64_t j = e / N, i = e - j * N;
+        mt[i * J + j] = M[e];
+    }
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < J; e += stride) ones[e] = 1.f;
 }
 
 // ---------------------------------------------------------------------------
@@ -3947,6 +3998,212 @@ cudaError_t tc_launch_mma_probe(int kind, int blocks, int iters, cudaStream_t s)
     else
         mma_probe_kernel<false><<<blocks, 128, kProbeSmem, s>>>(iters, status);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Mode-n product T = X x_n M on the tensor cores.  With X viewed [P, N, Q] and T
+// [P, J, Q], T[p, j, q] = sum_i X[p, i, q] M[j, i] is the mode-0 MTTKRP of the
+// two-way array Z[(p, q), i] with the single factor M^T (rank J): rows (p, q),
+// contraction over i, columns j, G a row of ones.  Z is read from the natural
+// fp16 images of X: K-major when Q = 1 (the innermost mode), else MN-major (q
+// contiguous, two 64-row halves of one p each, so Q must be a multiple of 64).
+// One scale for the whole of X (a single slab).
+// ---------------------------------------------------------------------------
+namespace {
+struct TtmLayout {
+    int bn, ks;
+    int64_t rows;
+    size_t off_mt, off_ones, off_bimg, off_colscale, off_img, total;
+};
+
+bool ttm_layout(int64_t P, int64_t N, int64_t Q, int64_t J, TtmLayout& l) {
+    const int64_t numel = P * N * Q;
+    l.rows = Q == 1 ? P : P * Q;
+    if (J < TC_IMG_MIN_R || J > 65536 || N < 16 || cdiv64(N, kBK4) * kBK4 > 2 * N) return false;
+    if (numel > ((int64_t)12 << 30) || cdiv64(l.rows, kBM) > 65535 || P >= ((int64_t)1 << 31)) return false;
+    if (Q == 1 ? (N % 8 != 0) : (Q % 64 != 0 || Q >= ((int64_t)1 << 31))) return false;
+    l.bn = J <= 64 ? 64 : (cdiv64(J, 256) * 256 * 20 <= cdiv64(J, 128) * 128 * 23 ? 256 : 128);
+    l.ks = (int)cdiv64(N, kBK4);
+    auto a256 = [](size_t x) { return (x + 255) / 256 * 256; };
+    size_t off = 512;   // max |X| at 0, the single slab maximum at 256
+    l.off_mt = off;
+    off = a256(off + (size_t)N * J * 4);
+    l.off_ones = off;
+    off = a256(off + (size_t)J * 4);
+    l.off_bimg = off;
+    off = a256(off + (size_t)cdiv64(J, l.bn) * l.ks * 2 * l.bn * 128);
+    l.off_colscale = off;
+    off = a256(off + (size_t)J * 4);
+    l.off_img = off;
+    off += 2 * a256((size_t)numel * 2);
+    l.total = off;
+    return true;
+}
+}  // namespace
+
+size_t tc_ttm_workspace_bytes(int64_t P, int64_t N, int64_t Q, int64_t J) {
+    TtmLayout l;
+    return ttm_layout(P, N, Q, J, l) ? l.total : 0;
+}
+
+int tc_ttm_run(const float* X, const float* M, float* T, int64_t P, int64_t N, int64_t Q, int64_t J, void* ws,
+               cudaStream_t stream, char* errbuf, size_t errlen) {
+    TtmLayout l;
+    if (!ttm_layout(P, N, Q, J, l)) {
+        snprintf(errbuf, errlen, "the tensor-core mode-n product does not take this shape");
+        return MTTKRP_ERR_UNSUPPORTED;
+    }
+    if ((reinterpret_cast<uintptr_t>(X) & 15) != 0 || (reinterpret_cast<uintptr_t>(ws) & 255) != 0) {
+        snprintf(errbuf, errlen, "the tensor-core mode-n product needs a 16-byte aligned X and a 256-byte aligned workspace");
+        return MTTKRP_ERR_INVALID;
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+    uint32_t* status = tc_status_ptr();
+    if (encode == nullptr || status == nullptr) {
+        snprintf(errbuf, errlen, "tensor-map encoder or status word unavailable");
+        return MTTKRP_ERR_CUDA;
+    }
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    uint32_t* ymax = reinterpret_cast<uint32_t*>(base);
+    uint32_t* slab = reinterpret_cast<uint32_t*>(base + 256);
+    float* mt = reinterpret_cast<float*>(base + l.off_mt);
+    float* ones = reinterpret_cast<float*>(base + l.off_ones);
+    float* bimg = reinterpret_cast<float*>(base + l.off_bimg);
+    float* colscale = reinterpret_cast<float*>(base + l.off_colscale);
+    const int64_t numel = P * N * Q;
+    const size_t img_half = ((size_t)numel * 2 + 255) / 256 * 256;
+    __half* img_hi = reinterpret_cast<__half*>(base + l.off_img);
+    __half* img_lo = reinterpret_cast<__half*>(base + l.off_img + img_half);
+    cudaError_t e = cudaMemsetAsync(base, 0, 512, stream);
+    if (e == cudaSuccess) {
+        int64_t blocks = cdiv64(J * N, 256);
+        if (blocks > 152 * 8) blocks = 152 * 8;
+        ttm_prep_kernel<<<(unsigned)blocks, 256, 0, stream>>>(M, J, N, mt, ones);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+        int64_t blocks = cdiv64(cdiv64(numel, kSlabUnit), 4);
+        if (blocks > 152 * 8) blocks = 152 * 8;
+        slabmax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(X, 1, numel, slab, ymax);
+        e = cudaGetLastError();
+        if (e == cudaSuccess) {
+            split_image_kernel<<<(unsigned)blocks, 256, 0, stream>>>(X, 1, numel, slab, ymax, img_hi, img_lo);
+            e = cudaGetLastError();
+        }
+    }
+    if (e == cudaSuccess) {
+        ColScaleArgs c;
+        memset(&c, 0, sizeof(c));
+        c.ngroup = 1;
+        c.gdim[0] = N;
+        c.gfac[0] = mt;
+        c.R = J;
+        c.out = colscale;
+        colscale_kernel<<<(unsigned)cdiv64(J, 32), 1024, 0, stream>>>(c);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+        BImgArgs b;
+        memset(&b, 0, sizeof(b));
+        b.ngroup = 1;
+        b.gdim[0] = N;
+        b.gfac[0] = mt;
+        b.R = J;
+        b.J = N;
+        b.Jq = N;
+        b.BN = l.bn;
+        b.KS = l.ks;
+        b.jq_steps = l.ks;
+        b.inner = 1;
+        b.nblocks = cdiv64(J, l.bn) * l.ks;
+        b.out = bimg;
+        int64_t blocks = cdiv64(b.nblocks * 2 * l.bn * kBK4, 256);
+        if (blocks > 152 * 16) blocks = 152 * 16;
+        tc_bimage_f16_kernel<kBK4><<<(unsigned)blocks, 256, 0, stream>>>(b, colscale);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) {
+        snprintf(errbuf, errlen, "mode-n product preparation: %s", cudaGetErrorString(e));
+        return MTTKRP_ERR_CUDA;
+    }
+    // tensor map of the natural images: (i, p) K-major for Q = 1, else (q, i, p)
+    TcArgs args;
+    memset(&args, 0, sizeof(args));
+    cuuint64_t gdim[5];
+    cuuint64_t gstride[4];
+    cuuint32_t box[5], estr[5] = {1, 1, 1, 1, 1};
+    int rank;
+    for (int q = 0; q < kRoles; ++q) args.slot[q] = -1;
+    if (Q == 1) {
+        rank = 2;
+        gdim[0] = (cuuint64_t)N;
+        gdim[1] = (cuuint64_t)P;
+        gstride[0] = (cuuint64_t)N * 2;
+        box[0] = kBK4;
+        box[1] = kBM;
+        args.slot[kRoleJq] = 0;
+        args.slot[kRoleI] = 1;
+    } else {
+        rank = 3;
+        gdim[0] = (cuuint64_t)Q;
+        gdim[1] = (cuuint64_t)N;
+        gdim[2] = (cuuint64_t)P;
+        gstride[0] = (cuuint64_t)Q * 2;
+        gstride[1] = (cuuint64_t)N * Q * 2;
+        box[0] = 64;
+        box[1] = kBK4;
+        box[2] = 1;
+        args.slot[kRoleI] = 0;
+        args.slot[kRoleJq] = 1;
+        args.slot[kRolePP] = 2;
+    }
+    CUresult cr = encode(&args.ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, img_hi, gdim, gstride, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr == CUDA_SUCCESS)
+        cr = encode(&args.ymap_lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, img_lo, gdim, gstride, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) {
+        snprintf(errbuf, errlen, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
+        return MTTKRP_ERR_CUDA;
+    }
+    args.rank = rank;
+    args.bimg = bimg;
+    args.gtab = ones;
+    args.dst = T;
+    args.dst_split_stride = 0;
+    args.I = l.rows;
+    args.R = J;
+    args.npre = 1;
+    args.pre_per_split = 1;
+    args.nQ = 1;
+    args.KS = l.ks;
+    args.jq_steps = l.ks;
+    args.ps = 1;
+    args.batch_len = 1;
+    args.y_box_bytes = (uint32_t)kBK4 * 2u * (uint32_t)kBM;
+    args.ymax_bits = ymax;
+    args.slab_bits = slab;
+    args.slab_div = 1;
+    args.slab_rows = 0;
+    args.colscale = colscale;
+    args.ttm_q = Q == 1 ? 0 : Q;
+    args.status = status;
+    dim3 grid((unsigned)cdiv64(J, l.bn), (unsigned)cdiv64(l.rows, kBM), 1u);
+    if (Q == 1)
+        e = l.bn == 256 ? launch_img<256>(args, grid, stream)
+          : l.bn == 128 ? launch_img<128>(args, grid, stream)
+                        : launch_img<64>(args, grid, stream);
+    else
+        e = l.bn == 256 ? launch_img<256, false, true>(args, grid, stream)
+          : l.bn == 128 ? launch_img<128, false, true>(args, grid, stream)
+                        : launch_img<64, false, true>(args, grid, stream);
+    if (e != cudaSuccess) {
+        snprintf(errbuf, errlen, "tensor-core mode-n product launch: %s", cudaGetErrorString(e));
+        return MTTKRP_ERR_CUDA;
+    }
+    return MTTKRP_OK;
 }
 
 uint32_t* tc_status_ptr() {

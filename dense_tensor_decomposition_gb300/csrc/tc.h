@@ -29,6 +29,11 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
 // Peak probe of the tensor pipe: `blocks` CTAs (one per SM), each issuing `iters`
 // M128 x N256 MMAs of kind::tf32 (kind 0, K = 8) or kind::f16 (kind 1, K = 16).
 cudaError_t tc_launch_mma_probe(int kind, int blocks, int iters, cudaStream_t s);
+// Mode-n product T = X x_n M on the tensor cores (X viewed [P, N, Q], M J x N, T
+// [P, J, Q]): workspace bytes it needs (0: the shape is not taken), and the run.
+size_t tc_ttm_workspace_bytes(int64_t P, int64_t N, int64_t Q, int64_t J);
+int tc_ttm_run(const float* X, const float* M, float* T, int64_t P, int64_t N, int64_t Q, int64_t J, void* ws,
+               cudaStream_t stream, char* errbuf, size_t errlen);
 // Device address of the error word on the current device (null on failure).
 uint32_t* tc_status_ptr();
 // Arm the failure-detection test hook for the next `count` launches.

@@ -271,6 +271,31 @@ int mttkrp_ttm(int d, const int64_t* dims, const float* X, int mode, const float
                void* stream);
 
 /*
+ * The same mode-n product on the tensor cores, with a caller-owned workspace.
+ * X viewed as [P, N, Q] (N = dims[mode]) and T as [P, J, Q]: T is computed as
+ * the mode-0 MTTKRP of the two-way array Z[(p, q), i] = X[p, i, q] with the
+ * single factor M^T (rank J) -- the fp16 two-term split of X (one power-of-two
+ * scale for the whole tensor) and of M^T (a scale per column j), three
+ * kind::f16 tensor-core products per fp32-accurate product, fp32 accumulation.
+ *
+ * mttkrp_ttm_workspace_bytes: device workspace bytes that path needs (about 4
+ * bytes an element of X for its fp16 images, plus M^T and small tables), or 0
+ * when it does not take the shape: J < 32, N < 16 or padded by more than half to
+ * a multiple of 64, Q a multiple of 64 unless the mode is the innermost one (then
+ * N a multiple of 8), more than 12 Gi elements, or more than 65535 x 128 rows
+ * (p, q).  Returns 0 for invalid arguments too.
+ * mttkrp_ttm_ws: arguments as mttkrp_ttm, plus workspace (device, 256-byte
+ * aligned, caller-owned) of workspace_bytes bytes.  Runs on the tensor cores when
+ * mttkrp_ttm_workspace_bytes() > 0, the workspace is that large and X is 16-byte
+ * aligned; otherwise (no workspace, a shape the path does not take, a misaligned
+ * X) it runs mttkrp_ttm's CUDA-core kernel.  Errors: as mttkrp_ttm, plus
+ * MTTKRP_ERR_WORKSPACE for a workspace that is given but too small.
+ */
+size_t mttkrp_ttm_workspace_bytes(int d, const int64_t* dims, int mode, int64_t J);
+int mttkrp_ttm_ws(int d, const int64_t* dims, const float* X, int mode, const float* M, int64_t J, float* T,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Peak probes for the roofline of a benchmark (measurement only; the pages have
  * no counterpart).  Both enqueue one kernel on `stream` and return; the caller
  * times it with events.

@@ -1,11 +1,19 @@
-"""GPU dense mode-n product (mttkrp_ttm through the C ABI) against the fp64
-oracle on the same seeded inputs.
+"""GPU dense mode-n product (mttkrp_ttm and mttkrp_ttm_ws through the C ABI)
+against the fp64 oracle on the same seeded inputs.
 
-Tolerance, from the arithmetic: every output is one fp32 fused multiply-add
-chain over the N = I_mode products in index order, so
-|T - T_exact| <= gamma_N * (|X| x_mode |M|) with gamma_N = N u / (1 - N u),
-u = 2^-24 (fp32 unit roundoff); the tests check that element-wise bound, and
-1e-5 relative Frobenius."""
+Tolerances, from the arithmetic (u = 2^-24, fp32 unit roundoff):
+  CUDA cores (mttkrp_ttm): every output is one fp32 fused multiply-add chain
+    over the N = I_mode products in index order, so
+    |T - T_exact| <= gamma_N * (|X| x_mode |M|), gamma_N = N u / (1 - N u).
+  Tensor cores (mttkrp_ttm_ws, the fp16 two-term split): each product x m is
+    formed from hi/lo parts with relative error <= 3 * 2^-22 plus the fp16
+    subnormal floor of each part (2^-25 of the scaled value: 2^-38 of the
+    largest |X|, or of the largest |M| in that row); tensor memory accumulates
+    the three products of each of at most Kd = min(128, N rounded up to 64)
+    indices toward zero (<= 2u a step, 3 Kd steps), and the drains are summed in
+    fp32 (gamma over N / 128 terms).  So
+    |T - T_exact| <= (6 Kd + 24 + N) u (|X| x_mode |M|) + 2^-36 N max|X| max|M|.
+Both also within 1e-5 relative Frobenius."""
 import numpy as np
 import pytest
 
@@ -27,11 +35,20 @@ def case(seed, dims, mode, J):
     return X, M
 
 
-def check(got, X, mode, M):
+def tc_coefficient(N):
+    kd = min(128, -(-N // 64) * 64)
+    return (6 * kd + 24 + N) * U
+
+
+def check(got, X, mode, M, tc=False):
     want = ottm.ttm(X, mode, M)
     N = X.shape[mode]
     gamma = N * U / (1 - N * U)
-    bound = gamma * ottm.ttm(np.abs(X), mode, np.abs(M)) + 1e-30
+    absprod = ottm.ttm(np.abs(X), mode, np.abs(M))
+    if tc:
+        bound = tc_coefficient(N) * absprod + 2.0 ** -36 * N * np.abs(X).max() * np.abs(M).max() + 1e-30
+    else:
+        bound = gamma * absprod + 1e-30
     assert rel_fro(got, want) <= 1e-5
     assert np.all(np.abs(got.astype(np.float64) - want) <= bound)
 
@@ -49,9 +66,39 @@ SHAPES = [((64, 48, 256), 0, 20), ((64, 48, 256), 1, 50), ((64, 48, 256), 2, 130
 @pytest.mark.parametrize("dims,mode,J", SHAPES)
 def test_ttm_matches_oracle(dims, mode, J):
     X, M = case(sum(dims) + 7 * mode + J, dims, mode, J)
-    T = mk.ttm(torch.from_numpy(X).cuda(), mode, torch.from_numpy(M).cuda())
+    T = mk.ttm(torch.from_numpy(X).cuda(), mode, torch.from_numpy(M).cuda(), path="simt")
     assert tuple(T.shape) == tuple(dims[:mode]) + (J,) + tuple(dims[mode + 1:])
     check(T.cpu().numpy(), X, mode, M)
+
+
+# shapes the tensor-core path takes: the innermost mode read K-major (row tail
+# P = 130), other modes MN-major with Q = 64, 512 and 8192, a half tile past the
+# last (p, q) row, contraction lengths 32, 40, 96, 128, 256 (padded to 64), J from
+# 32 (64-column tiles) to 300 (128- and 256-column tiles, ragged)
+TC_SHAPES = [((64, 48, 256), 2, 130), ((64, 48, 256), 2, 33), ((64, 128, 64), 1, 50), ((32, 64, 128), 0, 100),
+             ((16, 40, 8, 64), 1, 300), ((130, 96), 1, 200), ((3, 200, 64), 1, 64), ((2, 128, 40, 128), 2, 256)]
+
+
+@pytest.mark.parametrize("dims,mode,J", TC_SHAPES)
+def test_ttm_tensor_cores_match_oracle(dims, mode, J):
+    assert mk.ttm_workspace_bytes(dims, mode, J) > 0
+    X, M = case(5 + sum(dims) + 7 * mode + J, dims, mode, J)
+    T = mk.ttm(torch.from_numpy(X).cuda(), mode, torch.from_numpy(M).cuda(), path="tc")
+    check(T.cpu().numpy(), X, mode, M, tc=True)
+    assert mk.device_status() == 0
+
+
+def test_ttm_paths_agree_and_tc_is_deterministic():
+    dims, mode, J = (32, 64, 128), 1, 96
+    X, M = case(77, dims, mode, J)
+    Xd, Md = torch.from_numpy(X).cuda(), torch.from_numpy(M).cuda()
+    a = mk.ttm(Xd, mode, Md, path="tc")
+    b = mk.ttm(Xd, mode, Md, path="tc")
+    c = mk.ttm(Xd, mode, Md, path="simt")
+    assert torch.equal(a, b)
+    assert rel_fro(a.cpu().numpy(), c.cpu().numpy().astype(np.float64)) <= 2e-5
+    with pytest.raises(mk.MttkrpError):
+        mk.ttm(torch.zeros((5, 7, 3), device="cuda"), 1, torch.zeros((40, 7), device="cuda"), path="tc")
 
 
 def test_tucker_reconstruction_chain_and_repeatability():
@@ -63,25 +110,26 @@ def test_tucker_reconstruction_chain_and_repeatability():
     cur_d = torch.from_numpy(core).cuda()
     cur_h = core
     for k, Uk in enumerate(Us):
-        cur_d = mk.ttm(cur_d, k, torch.from_numpy(Uk).cuda())
+        cur_d = mk.ttm(cur_d, k, torch.from_numpy(Uk).cuda(), path="simt")
         got = cur_d.cpu().numpy()
         check(got, cur_h, k, Uk)
         cur_h = got                              # next step from the GPU's fp32 result
     again = torch.from_numpy(core).cuda()
     for k, Uk in enumerate(Us):
-        again = mk.ttm(again, k, torch.from_numpy(Uk).cuda())
+        again = mk.ttm(again, k, torch.from_numpy(Uk).cuda(), path="simt")
     assert torch.equal(again, cur_d)
 
 
+@pytest.mark.parametrize("path", ["simt", "tc"])
 @pytest.mark.parametrize("mode", [0, 1, 2])
-def test_full_size_sampled(mode):
+def test_full_size_sampled(mode, path):
     """512^3 with a square 512 x 512 matrix (the bench's launch
     configuration), checked on 2000 sampled outputs computed one by one."""
     rng = np.random.default_rng(40 + mode)
     dims = (512, 512, 512)
     Xd = torch.randn(dims, generator=torch.Generator().manual_seed(41 + mode)).cuda()
     M = rng.standard_normal((512, 512)).astype(np.float32)
-    T = mk.ttm(Xd, mode, torch.from_numpy(M).cuda())
+    T = mk.ttm(Xd, mode, torch.from_numpy(M).cuda(), path=path)
     idx = [rng.integers(0, 512, 2000) for _ in range(3)]
     got = T[idx[0], idx[1], idx[2]].cpu().numpy().astype(np.float64)
     X = Xd.cpu().numpy()
@@ -94,7 +142,12 @@ def test_full_size_sampled(mode):
         x = X[tuple(at)].astype(np.float64)   # the fibre along `mode`
         want[s] = x @ M[j].astype(np.float64)
         bound[s] = np.abs(x) @ np.abs(M[j]).astype(np.float64)
-    assert np.all(np.abs(got - want) <= 512 * U / (1 - 512 * U) * bound + 1e-30)
+    if path == "simt":
+        assert np.all(np.abs(got - want) <= 512 * U / (1 - 512 * U) * bound + 1e-30)
+    else:
+        floor = 2.0 ** -36 * 512 * float(np.abs(X).max()) * float(np.abs(M).max())
+        assert np.all(np.abs(got - want) <= tc_coefficient(512) * bound + floor)
+    assert mk.device_status() == 0
     del T, Xd
     torch.cuda.empty_cache()
 
