@@ -577,10 +577,12 @@ int mttkrp_all_modes(mttkrp_plan_t h, const float* Y, const float* const* factor
 
 // CP-ALS scratch: Gram matrices of every mode, V (reused for the Hadamard
 // product of all Grams), the fp64 solve of the current mode, its fp32 MTTKRP,
-// the ||Y||^2 partials and the Cholesky status word.
+// the ||Y||^2 and fit partials, the Cholesky status word, and for the
+// mixed-precision solve (R <= cpals_mixed_max_rank()) V's two fp32 words, the
+// fp32 factor and the fp32 first solution and residual.
 namespace {
 struct CpAlsLayout {
-    size_t grams, v, dinv, x, m, gpart, part, info, total;
+    size_t grams, v, dinv, x, m, gpart, part, info, vhi, vlo, l32, dinv32, x0, res, total;
 };
 CpAlsLayout cp_als_layout(const Plan& p) {
     int64_t imax = 0;
@@ -609,6 +611,19 @@ CpAlsLayout cp_als_layout(const Plan& p) {
     off = align256(off + cpals_sumsq_scratch_bytes());
     l.info = off;
     off = align256(off + sizeof(int));
+    const bool mixed = p.R <= cpals_mixed_max_rank();
+    l.vhi = off;
+    off = align256(off + (mixed ? R * R * sizeof(float) : 0));
+    l.vlo = off;
+    off = align256(off + (mixed ? R * R * sizeof(float) : 0));
+    l.l32 = off;
+    off = align256(off + (mixed ? R * R * sizeof(float) : 0));
+    l.dinv32 = off;
+    off = align256(off + (mixed ? R * sizeof(float) : 0));
+    l.x0 = off;
+    off = align256(off + (mixed ? (size_t)imax * R * sizeof(float) : 0));
+    l.res = off;
+    off = align256(off + (mixed ? (size_t)imax * R * sizeof(float) : 0));
     l.total = off;
     return l;
 }
@@ -762,6 +777,7 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, 
     const int d = p->d;
     const int R = (int)p->R;
     const int64_t RR = (int64_t)R * R;
+    const bool mixed = R <= cpals_mixed_max_rank();
     int64_t numel = 1;
     for (int n = 0; n < d; ++n) numel *= p->dims[n];
     cudaError_t e = cudaMemsetAsync(info, 0, sizeof(int), s);
@@ -787,17 +803,26 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, 
         ++p->launches;
         int rc = run_mode(*p, Y, factors, n, M, s);
         if (rc != MTTKRP_OK) return rc;
-        if ((e = cpals_cholesky(V, R, info, dinv, s)) == cudaSuccess &&
-            (e = cpals_solve(V, dinv, R, M, p->dims[n], X, s)) == cudaSuccess &&
-            (e = cpals_normalize(X, p->dims[n], R, factors[n], lambda, s)) == cudaSuccess)
+        if (mixed) {
+            e = cpals_solve_mixed(V, R, M, p->dims[n], X, reinterpret_cast<float*>(base + l.vhi),
+                                  reinterpret_cast<float*>(base + l.vlo), reinterpret_cast<float*>(base + l.l32),
+                                  reinterpret_cast<float*>(base + l.dinv32), reinterpret_cast<float*>(base + l.x0),
+                                  reinterpret_cast<float*>(base + l.res), info, s);
+            p->launches += cpals_mixed_launches(R);
+        } else {
+            if ((e = cpals_cholesky(V, R, info, dinv, s)) == cudaSuccess)
+                e = cpals_solve(V, dinv, R, M, p->dims[n], X, s);
+            p->launches += 2 + cpals_cholesky_launches(R);
+        }
+        if (e == cudaSuccess && (e = cpals_normalize(X, p->dims[n], R, factors[n], lambda, s)) == cudaSuccess)
             e = cpals_gram(factors[n], p->dims[n], R, G + n * RR, gpart, s);
         if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "CP-ALS update of mode %d: %s", n, cudaGetErrorString(e));
-        p->launches += 4 + cpals_cholesky_launches(R) + (cpals_gram_slabs(p->dims[n], R) > 1 ? 1 : 0);
+        p->launches += 2 + (cpals_gram_slabs(p->dims[n], R) > 1 ? 1 : 0);
     }
     if ((e = cpals_hadamard(G, d, -1, R, V, s)) == cudaSuccess)
-        e = cpals_fit(V, lambda, M, factors[d - 1], p->dims[d - 1], R, norm_y2, info, fit, s);
+        e = cpals_fit(V, lambda, M, factors[d - 1], p->dims[d - 1], R, norm_y2, info, fit, part, s);
     if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "CP-ALS fit: %s", cudaGetErrorString(e));
-    p->launches += 2;
+    p->launches += 3;
     p->sweep_left_images = 1;
     return MTTKRP_OK;
 }

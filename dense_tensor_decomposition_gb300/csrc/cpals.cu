@@ -6,38 +6,72 @@
 // after the sweep the fit from ||X||^2 = lambda^T (Hadamard of all Grams)
 // lambda and <Y, X> = sum_r lambda_r sum_i M(i, r) A_{d-1}(i, r).
 //
-// The R x R algebra runs in fp64 (Gram sums, Cholesky, the two triangular
-// solves, the fit); factors stay fp32.  Every reduction has a fixed order, so
-// a sweep is bitwise reproducible.
+// Precision.  GB300 runs fp64 at about 1/64 of its fp32 rate (two fused
+// multiply-adds a clock an SM), so the O(I R^2) steps use fp32 arithmetic
+// that keeps fp64-level accuracy, and fp64 is kept for the small O(R^2)
+// steps:
+//   * Gram matrices: exact fp32 products (p = a b and its rounding error
+//     fma(a, b, -p)) summed with compensation, stored in fp64;
+//   * A_n = M V^{-1}: V is factored in fp32 (blocked, 32-column panels), the
+//     rows are solved in fp32, and one refinement step solves for the residual
+//     M - X V, computed with V split into two fp32 words and compensated sums,
+//     so the result carries the accuracy of V (fp64) rather than of the fp32
+//     factor; it needs cond(V) well below 1 / 2^-24 (a failing fp32 pivot gives
+//     a NaN fit).  Above R = 1024 the factor and solves run in fp64.
+//   * Hadamard products, column norms and the fit in fp64.
+// Factors stay fp32.  Every reduction has a fixed order, so a sweep is bitwise
+// reproducible.
 #include "internal.h"
 
 namespace mk {
 namespace {
 
-// G = A^T A (R x R, fp64) for A (I x R, fp32 row-major): 16 x 16 output tiles,
-// 32-row slabs of the two column blocks staged in shared memory.  blockIdx.z
+// Compensated fp32 addition (Neumaier): sum + c carries the exact running total
+// to about one fp32 rounding.
+__device__ __forceinline__ void neumaier(float& sum, float& c, float x) {
+    const float t = sum + x;
+    c += fabsf(sum) >= fabsf(x) ? (sum - t) + x : (x - t) + sum;
+    sum = t;
+}
+
+// G = A^T A (R x R, fp64) for A (I x R, fp32 row-major): 16 x 16 output tiles of
+// the lower triangle (mirrored), 32-row slabs of the two column blocks staged in
+// shared memory.  Each product a b is split exactly into p = fl(a b) and
+// fma(a, b, -p); the p are summed with compensation and the small parts plainly,
+// which gives the Gram to about fp64 accuracy on the fp32 pipe.  blockIdx.z
 // takes every gridDim.z-th slab and writes its partial Gram to part[z]; the
 // partials are then added in z order (gram_sum_kernel).
 __global__ void __launch_bounds__(256) gram_kernel(const float* __restrict__ A, int64_t I, int R,
                                                    double* __restrict__ part) {
-    __shared__ double sa[32][17], sb[32][17];
+    if (blockIdx.x > blockIdx.y) return;   // upper tiles: mirrored from the lower ones
+    __shared__ float sa[32][17], sb[32][17];
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const int r0 = blockIdx.y * 16, c0 = blockIdx.x * 16;
     double* G = part + (int64_t)blockIdx.z * R * R;
-    double acc = 0.0;
+    float s = 0.f, c = 0.f, small = 0.f;
     for (int64_t i0 = 32 * (int64_t)blockIdx.z; i0 < I; i0 += 32 * (int64_t)gridDim.z) {
         for (int t = threadIdx.x; t < 32 * 16; t += 256) {
             const int ii = t / 16, cc = t % 16;
             const int64_t i = i0 + ii;
-            sa[ii][cc] = (i < I && r0 + cc < R) ? (double)A[i * R + r0 + cc] : 0.0;
-            sb[ii][cc] = (i < I && c0 + cc < R) ? (double)A[i * R + c0 + cc] : 0.0;
+            sa[ii][cc] = (i < I && r0 + cc < R) ? A[i * R + r0 + cc] : 0.f;
+            sb[ii][cc] = (i < I && c0 + cc < R) ? A[i * R + c0 + cc] : 0.f;
         }
         __syncthreads();
 #pragma unroll 8
-        for (int ii = 0; ii < 32; ++ii) acc = fma(sa[ii][ty], sb[ii][tx], acc);
+        for (int ii = 0; ii < 32; ++ii) {
+            const float a = sa[ii][ty], b = sb[ii][tx];
+            const float p = a * b;
+            small += fmaf(a, b, -p);
+            neumaier(s, c, p);
+        }
         __syncthreads();
     }
-    if (r0 + ty < R && c0 + tx < R) G[(int64_t)(r0 + ty) * R + c0 + tx] = acc;
+    const int r = r0 + ty, col = c0 + tx;
+    if (r < R && col < R) {
+        const double v = (double)s + ((double)c + (double)small);
+        G[(int64_t)r * R + col] = v;
+        G[(int64_t)col * R + r] = v;
+    }
 }
 
 __global__ void gram_sum_kernel(const double* __restrict__ part, int S, int R, double* __restrict__ G) {
@@ -67,9 +101,10 @@ __global__ void hadamard_kernel(const double* __restrict__ G, int d, int skip, i
 // j-th pivot is not positive (the factor then holds NaN from there on).
 constexpr int kChNB = 32;
 
-__global__ void __launch_bounds__(256) chol_diag_kernel(double* __restrict__ V, int R, int k0, int nb,
-                                                        int* __restrict__ info, double* __restrict__ dinv) {
-    __shared__ double a[kChNB][kChNB + 1];
+template <typename T>
+__global__ void __launch_bounds__(256) chol_diag_kernel(T* __restrict__ V, int R, int k0, int nb,
+                                                        int* __restrict__ info, T* __restrict__ dinv) {
+    __shared__ T a[kChNB][kChNB + 1];
     for (int t = threadIdx.x; t < nb * nb; t += blockDim.x) {
         const int i = t / nb, j = t % nb;
         a[i][j] = j <= i ? V[(int64_t)(k0 + i) * R + k0 + j] : 0.0;
@@ -77,12 +112,12 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(double* __restrict__ V, 
     __syncthreads();
     for (int j = 0; j < nb; ++j) {
         if (threadIdx.x == 0) {
-            const double p = a[j][j];
-            if (!(p > 0.0) && *info == 0) *info = k0 + j + 1;
+            const T p = a[j][j];
+            if (!(p > T(0)) && *info == 0) *info = k0 + j + 1;
             a[j][j] = sqrt(p);
         }
         __syncthreads();
-        const double inv = 1.0 / a[j][j];
+        const T inv = T(1) / a[j][j];
         if (threadIdx.x == 0) dinv[k0 + j] = inv;
         for (int i = j + 1 + threadIdx.x; i < nb; i += blockDim.x) a[i][j] *= inv;
         __syncthreads();
@@ -100,21 +135,22 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(double* __restrict__ V, 
 }
 
 // rows i >= k0 + nb of the panel: x = v L11^{-T} (forward substitution)
-__global__ void __launch_bounds__(256) chol_panel_kernel(double* __restrict__ V, int R, int k0, int nb,
-                                                         const double* __restrict__ dinv) {
-    __shared__ double l[kChNB][kChNB + 1];
+template <typename T>
+__global__ void __launch_bounds__(256) chol_panel_kernel(T* __restrict__ V, int R, int k0, int nb,
+                                                         const T* __restrict__ dinv) {
+    __shared__ T l[kChNB][kChNB + 1];
     for (int t = threadIdx.x; t < nb * nb; t += blockDim.x) {
         const int i = t / nb, j = t % nb;
         l[i][j] = j <= i ? V[(int64_t)(k0 + i) * R + k0 + j] : 0.0;
     }
     __syncthreads();
     for (int i = k0 + nb + blockIdx.x * blockDim.x + threadIdx.x; i < R; i += gridDim.x * blockDim.x) {
-        double x[kChNB];
-        double* v = V + (int64_t)i * R + k0;
+        T x[kChNB];
+        T* v = V + (int64_t)i * R + k0;
 #pragma unroll
         for (int j = 0; j < kChNB; ++j) {
             if (j < nb) {
-                double s = v[j];
+                T s = v[j];
 #pragma unroll
                 for (int t = 0; t < j; ++t) s -= x[t] * l[j][t];
                 x[j] = s * dinv[k0 + j];
@@ -125,21 +161,22 @@ __global__ void __launch_bounds__(256) chol_panel_kernel(double* __restrict__ V,
 }
 
 // trailing lower triangle: V[i][j] -= sum_t P[i][t] P[j][t], k0 + nb <= j <= i
-__global__ void __launch_bounds__(256) chol_update_kernel(double* __restrict__ V, int R, int k0, int nb) {
+template <typename T>
+__global__ void __launch_bounds__(256) chol_update_kernel(T* __restrict__ V, int R, int k0, int nb) {
     if (blockIdx.x > blockIdx.y) return;   // upper tiles
-    __shared__ double pi[kChNB][kChNB + 1], pj[kChNB][kChNB + 1];
+    __shared__ T pi[kChNB][kChNB + 1], pj[kChNB][kChNB + 1];
     const int i0 = k0 + nb + blockIdx.y * kChNB, j0 = k0 + nb + blockIdx.x * kChNB;
     for (int t = threadIdx.x; t < kChNB * kChNB; t += blockDim.x) {
         const int r = t / kChNB, c = t % kChNB;
-        pi[r][c] = (i0 + r < R && c < nb) ? V[(int64_t)(i0 + r) * R + k0 + c] : 0.0;
-        pj[r][c] = (j0 + r < R && c < nb) ? V[(int64_t)(j0 + r) * R + k0 + c] : 0.0;
+        pi[r][c] = (i0 + r < R && c < nb) ? V[(int64_t)(i0 + r) * R + k0 + c] : T(0);
+        pj[r][c] = (j0 + r < R && c < nb) ? V[(int64_t)(j0 + r) * R + k0 + c] : T(0);
     }
     __syncthreads();
     for (int t = threadIdx.x; t < kChNB * kChNB; t += blockDim.x) {
         const int r = t / kChNB, c = t % kChNB;
         const int i = i0 + r, j = j0 + c;
         if (i < R && j <= i) {
-            double s = 0.0;
+            T s = T(0);
 #pragma unroll 8
             for (int u = 0; u < kChNB; ++u) s = fma(pi[r][u], pj[c][u], s);
             V[(int64_t)i * R + j] -= s;
@@ -150,7 +187,8 @@ __global__ void __launch_bounds__(256) chol_update_kernel(double* __restrict__ V
 // Mirror the lower Cholesky factor into the strict upper triangle (V[j][k] =
 // L[k][j], j < k), so that both substitutions read L with consecutive lanes on
 // consecutive addresses.
-__global__ void mirror_lower_kernel(double* __restrict__ V, int R) {
+template <typename T>
+__global__ void mirror_lower_kernel(T* __restrict__ V, int R) {
     const int64_t n = (int64_t)R * R;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
         const int j = (int)(e / R), k = (int)(e % R);
@@ -212,6 +250,390 @@ __global__ void __launch_bounds__(256) solve_kernel(const double* __restrict__ L
     for (int k = lane; k < R; k += 32) X[row * R + k] = x[k];
 }
 
+constexpr int kChol32MaxR = 1024;
+
+// Small ranks (R <= kSmemMaxR): the factorisation and the solves keep the lower
+// triangle of the fp32 factor packed in shared memory (row i at i (i + 1) / 2).
+constexpr int kSmemMaxR = 288;
+
+__host__ __device__ __forceinline__ int tri(int i) { return i * (i + 1) / 2; }
+
+// One CTA factors V (fp32, only the lower triangle read) in shared memory in
+// 32-column panels: warp 0 factors the diagonal block in registers (lane i holds
+// row i), every thread forward-substitutes one row of the panel below it, and the
+// trailing lower triangle is updated in 4 x 4 register blocks from the panel.
+// Writes L (dense row-major: lower triangle and its mirror above) and
+// dinv[j] = 1 / L[j][j]; *info = j + 1 for the first pivot that is not positive.
+constexpr int kCholSmemThreads = 256;   // no register cap: the row arrays stay in registers
+__global__ void __launch_bounds__(kCholSmemThreads, 1) chol_smem_kernel(const float* __restrict__ V, int R,
+                                                            float* __restrict__ L, float* __restrict__ dinv,
+                                                            int* __restrict__ info) {
+    extern __shared__ float sm[];
+    float* a = sm;                         // packed lower triangle, tri(R) floats
+    float* panel = sm + tri(R);            // [R][33]
+    __shared__ float l11[32][33];
+    __shared__ float dv[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    for (int i = warp; i < R; i += nw)
+        for (int j = lane; j <= i; j += 32) a[tri(i) + j] = V[(int64_t)i * R + j];
+    __syncthreads();
+    for (int k0 = 0; k0 < R; k0 += 32) {
+        const int nb = R - k0 < 32 ? R - k0 : 32;
+        if (warp == 0) {
+            float r[32];
+#pragma unroll
+            for (int t = 0; t < 32; ++t) r[t] = (lane < nb && t <= lane) ? a[tri(k0 + lane) + k0 + t] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (j < nb) {
+                    const float piv = __shfl_sync(0xffffffffu, r[j], j);
+                    if (lane == 0 && !(piv > 0.f) && *info == 0) *info = k0 + j + 1;
+                    const float d = sqrtf(piv), inv = 1.f / d;
+                    if (lane == j) r[j] = d;
+                    if (lane > j) r[j] *= inv;
+                    if (lane == 0) dv[j] = inv;
+#pragma unroll
+                    for (int t = j + 1; t < 32; ++t) {
+                        const float ltj = __shfl_sync(0xffffffffu, r[j], t);
+                        if (t < nb && lane >= t) r[t] = fmaf(-r[j], ltj, r[t]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                l11[lane][t] = (t <= lane) ? r[t] : 0.f;
+                if (lane < nb && t <= lane) a[tri(k0 + lane) + k0 + t] = r[t];
+            }
+            __syncwarp();
+            if (lane < nb) dinv[k0 + lane] = dv[lane];
+        }
+        __syncthreads();
+        const int rest = R - k0 - nb;
+        for (int ii = tid; ii < rest; ii += blockDim.x) {
+            const int i = k0 + nb + ii;
+            float x[32];
+#pragma unroll
+            for (int t = 0; t < 32; ++t) x[t] = t < nb ? a[tri(i) + k0 + t] : 0.f;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                if (t < nb) {
+                    float v = x[t];
+#pragma unroll
+                    for (int u = 0; u < t; ++u) v = fmaf(-x[u], l11[t][u], v);
+                    x[t] = v * dv[t];
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                if (t < nb) a[tri(i) + k0 + t] = x[t];
+                panel[ii * 33 + t] = x[t];
+            }
+        }
+        __syncthreads();
+        const int nblk = (rest + 3) / 4;
+        const int pairs = nblk * (nblk + 1) / 2;
+        for (int pq = tid; pq < pairs; pq += blockDim.x) {
+            int bi = (int)((sqrtf(8.f * (float)pq + 1.f) - 1.f) * 0.5f);
+            while (bi * (bi + 1) / 2 > pq) --bi;
+            while ((bi + 1) * (bi + 2) / 2 <= pq) ++bi;
+            const int bk = pq - bi * (bi + 1) / 2;
+            float acc[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) acc[u][v] = 0.f;
+            for (int t = 0; t < nb; ++t) {
+                float pi[4], pk[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int ri = 4 * bi + u, rk = 4 * bk + u;
+                    pi[u] = ri < rest ? panel[ri * 33 + t] : 0.f;
+                    pk[u] = rk < rest ? panel[rk * 33 + t] : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(pi[u], pk[v], acc[u][v]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int ri = 4 * bi + u, rk = 4 * bk + v;
+                    if (ri < rest && rk <= ri) a[tri(k0 + nb + ri) + k0 + nb + rk] -= acc[u][v];
+                }
+        }
+        __syncthreads();
+    }
+    for (int i = warp; i < R; i += nw)
+        for (int j = lane; j < R; j += 32) L[(int64_t)i * R + j] = j <= i ? a[tri(i) + j] : a[tri(j) + i];
+}
+
+// Y(i, :) = B(i, :) (L L^T)^{-1} in fp32, one warp per row, 32 rows a CTA, the
+// packed lower triangle of L staged in shared memory (L dense, lower part read).
+// Blocks of 32 unknowns as in solve_kernel.  out32 / (add, out64) as in
+// solve32_kernel.
+__global__ void __launch_bounds__(1024, 1) solve_smem_kernel(const float* __restrict__ L,
+                                                             const float* __restrict__ dinv, int R,
+                                                             const float* __restrict__ B, int64_t I,
+                                                             float* __restrict__ out32,
+                                                             const float* __restrict__ add,
+                                                             double* __restrict__ out64) {
+    extern __shared__ float sm[];
+    float* lp = sm;                        // packed lower triangle
+    float* ds = sm + tri(R);               // the pivots' reciprocals (R)
+    float* xs = ds + R;                    // [32 warps][R]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    for (int i = warp; i < R; i += nw)
+        for (int j = lane; j <= i; j += 32) lp[tri(i) + j] = L[(int64_t)i * R + j];
+    for (int j = tid; j < R; j += blockDim.x) ds[j] = dinv[j];
+    const int64_t row = (int64_t)blockIdx.x * nw + warp;
+    float* x = xs + (int64_t)warp * R;
+    if (row < I)
+        for (int k = lane; k < R; k += 32) x[k] = B[row * R + k];
+    __syncthreads();
+    if (row >= I) return;
+    for (int k0 = 0; k0 < R; k0 += 32) {
+        const int k = k0 + lane;
+        const bool live = k < R;
+        float acc = live ? x[k] : 0.f;
+        if (live) {
+            const float* lk = lp + tri(k);
+            for (int j = 0; j < k0; ++j) acc = fmaf(-lk[j], x[j], acc);
+        }
+        const int nb = R - k0 < 32 ? R - k0 : 32;
+        for (int t = 0; t < nb; ++t) {
+            const float yt = __shfl_sync(0xffffffffu, acc, t) * ds[k0 + t];
+            if (lane == t)
+                acc = yt;
+            else if (lane > t && live)
+                acc = fmaf(-lp[tri(k) + k0 + t], yt, acc);
+        }
+        if (live) x[k] = acc;
+        __syncwarp();
+    }
+    for (int k0 = ((R - 1) / 32) * 32; k0 >= 0; k0 -= 32) {
+        const int k = k0 + lane;
+        const bool live = k < R;
+        float acc = live ? x[k] : 0.f;
+        if (live)
+            for (int j = k0 + 32; j < R; ++j) acc = fmaf(-lp[tri(j) + k], x[j], acc);
+        const int nb = R - k0 < 32 ? R - k0 : 32;
+        for (int t = nb - 1; t >= 0; --t) {
+            const float xt = __shfl_sync(0xffffffffu, acc, t) * ds[k0 + t];
+            if (lane == t)
+                acc = xt;
+            else if (lane < t && live)
+                acc = fmaf(-lp[tri(k0 + t) + k], xt, acc);
+        }
+        if (live) x[k] = acc;
+        __syncwarp();
+    }
+    for (int k = lane; k < R; k += 32) {
+        const int64_t e = row * R + k;
+        if (out32 != nullptr) out32[e] = x[k];
+        if (out64 != nullptr) out64[e] = (double)add[e] + (double)x[k];
+    }
+}
+
+// Y(i, :) = B(i, :) (L L^T)^{-1} in fp32 with the fp32 Cholesky factor (its
+// upper triangle mirrored).  One warp solves kSolveRows rows together, so every
+// load of L serves kSolveRows independent chains; lane l owns unknown k0 + l of
+// each row in blocks of 32 unknowns: the finished blocks' contributions are dot
+// products (loads of L issued eight at a time ahead of the arithmetic), and
+// within the block the unknowns are finished one by one and broadcast by
+// shuffles.  out32 (if non-null) receives the fp32 result; out64 (if non-null)
+// receives add + result in fp64.
+constexpr int kSolveRows = 1;
+__global__ void __launch_bounds__(32) solve32_kernel(const float* __restrict__ L, const float* __restrict__ dinv,
+                                                     int R, const float* __restrict__ B, int64_t I,
+                                                     float* __restrict__ out32, const float* __restrict__ add,
+                                                     double* __restrict__ out64) {
+    extern __shared__ float xs32[];   // [kSolveRows][R], then the staged block of L [R][33]
+    constexpr int NR = kSolveRows;
+    const int lane = threadIdx.x;
+    const int64_t row0 = (int64_t)blockIdx.x * NR;
+    float* x = xs32;
+    float* lst = xs32 + NR * R;
+    // lst[j][l] = L[j][k0 + l] for the rows j the block's dot products need (all
+    // loads issued before any use)
+    auto stage = [&](int j0, int j1, int k0) {
+        const bool in = k0 + lane < R;
+        int j = j0;
+        for (; j + 8 <= j1; j += 8) {   // eight loads in flight before their stores
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = in ? L[(int64_t)(j + q) * R + k0 + lane] : 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) lst[(j + q) * 33 + lane] = v[q];
+        }
+        for (; j < j1; ++j) lst[j * 33 + lane] = in ? L[(int64_t)j * R + k0 + lane] : 0.f;
+        __syncwarp();
+    };
+    for (int u = 0; u < NR; ++u)
+        for (int k = lane; k < R; k += 32) x[u * R + k] = row0 + u < I ? B[(row0 + u) * R + k] : 0.f;
+    __syncwarp();
+    // L y = b
+    for (int k0 = 0; k0 < R; k0 += 32) {
+        const int k = k0 + lane;
+        const bool live = k < R;
+        float acc[NR];
+#pragma unroll
+        for (int u = 0; u < NR; ++u) acc[u] = live ? x[u * R + k] : 0.f;
+        stage(0, k0, k0);   // upper mirror: L[j][k] = L[k][j]
+        if (live)
+            for (int j = 0; j < k0; ++j) {
+                const float l = lst[j * 33 + lane];
+#pragma unroll
+                for (int u = 0; u < NR; ++u) acc[u] = fmaf(-l, x[u * R + j], acc[u]);
+            }
+        __syncwarp();
+        const int nb = R - k0 < 32 ? R - k0 : 32;
+        float lb[32], db[32];   // this lane's row of the diagonal block, and the pivots' reciprocals
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            lb[t] = (live && t < nb && lane > t) ? L[(int64_t)k * R + k0 + t] : 0.f;
+            db[t] = t < nb ? dinv[k0 + t] : 0.f;
+        }
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            if (t < nb) {
+#pragma unroll
+                for (int u = 0; u < NR; ++u) {
+                    const float yt = __shfl_sync(0xffffffffu, acc[u], t) * db[t];
+                    if (lane == t)
+                        acc[u] = yt;
+                    else if (lane > t)
+                        acc[u] = fmaf(-lb[t], yt, acc[u]);
+                }
+            }
+        }
+        if (live)
+#pragma unroll
+            for (int u = 0; u < NR; ++u) x[u * R + k] = acc[u];
+        __syncwarp();
+    }
+    // L^T x = y
+    for (int k0 = ((R - 1) / 32) * 32; k0 >= 0; k0 -= 32) {
+        const int k = k0 + lane;
+        const bool live = k < R;
+        float acc[NR];
+#pragma unroll
+        for (int u = 0; u < NR; ++u) acc[u] = live ? x[u * R + k] : 0.f;
+        stage(k0 + 32 < R ? k0 + 32 : R, R, k0);
+        if (live)
+            for (int j = k0 + 32; j < R; ++j) {
+                const float l = lst[j * 33 + lane];
+#pragma unroll
+                for (int u = 0; u < NR; ++u) acc[u] = fmaf(-l, x[u * R + j], acc[u]);
+            }
+        __syncwarp();
+        const int nb = R - k0 < 32 ? R - k0 : 32;
+        float lb[32], db[32];   // column k of the diagonal block (L[k0 + t][k]), and the reciprocals
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            lb[t] = (live && t < nb && lane < t) ? L[(int64_t)(k0 + t) * R + k] : 0.f;
+            db[t] = t < nb ? dinv[k0 + t] : 0.f;
+        }
+#pragma unroll
+        for (int t = 31; t >= 0; --t) {
+            if (t < nb) {
+#pragma unroll
+                for (int u = 0; u < NR; ++u) {
+                    const float xt = __shfl_sync(0xffffffffu, acc[u], t) * db[t];
+                    if (lane == t)
+                        acc[u] = xt;
+                    else if (lane < t)
+                        acc[u] = fmaf(-lb[t], xt, acc[u]);
+                }
+            }
+        }
+        if (live)
+#pragma unroll
+            for (int u = 0; u < NR; ++u) x[u * R + k] = acc[u];
+        __syncwarp();
+    }
+    for (int u = 0; u < NR; ++u) {
+        if (row0 + u >= I) break;
+        for (int k = lane; k < R; k += 32) {
+            const int64_t e = (row0 + u) * R + k;
+            if (out32 != nullptr) out32[e] = x[u * R + k];
+            if (out64 != nullptr) out64[e] = (double)add[e] + (double)x[u * R + k];
+        }
+    }
+}
+
+// V (fp64) as two fp32 words, vhi = fl32(V) and vlo = fl32(V - vhi), which hold
+// it to about 2^-48 relative
+// (L receives a copy of vhi: the working matrix of the fp32 factorisation)
+__global__ void split_v_kernel(const double* __restrict__ V, int64_t n, float* __restrict__ vhi,
+                               float* __restrict__ vlo, float* __restrict__ L) {
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+        const double v = V[e];
+        const float h = (float)v;
+        vhi[e] = h;
+        vlo[e] = (float)(v - (double)h);
+        L[e] = h;
+    }
+}
+
+// Res = M - X V (I x R) with V = vhi + vlo: each product x vhi split exactly
+// (fma), summed with compensation; x vlo and the product errors summed plainly.
+// kResRows rows and kResCols columns a block (one column a thread).
+constexpr int kResRows = 2, kResCols = 128;
+__global__ void __launch_bounds__(kResCols) residual_kernel(const float* __restrict__ M, const float* __restrict__ X,
+                                                       const float* __restrict__ vhi_m, const float* __restrict__ vlo_m,
+                                                       int64_t I, int R, float* __restrict__ Res) {
+    extern __shared__ float xr[];   // [kResRows][R]
+    const int64_t i0 = (int64_t)blockIdx.y * kResRows;
+    for (int t = threadIdx.x; t < kResRows * R; t += blockDim.x) {
+        const int u = t / R;
+        xr[t] = i0 + u < I ? X[(i0 + u) * R + (t - u * R)] : 0.f;
+    }
+    __syncthreads();
+    {
+        const int j = blockIdx.x * kResCols + threadIdx.x;
+        if (j >= R) return;
+        float s[kResRows], c[kResRows], sm[kResRows];
+#pragma unroll
+        for (int u = 0; u < kResRows; ++u) s[u] = c[u] = sm[u] = 0.f;
+        int k = 0;
+        for (; k + 8 <= R; k += 8) {   // eight rows of V in flight
+            float vh[8], vl[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                vh[q] = vhi_m[(int64_t)(k + q) * R + j];
+                vl[q] = vlo_m[(int64_t)(k + q) * R + j];
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+#pragma unroll
+                for (int u = 0; u < kResRows; ++u) {
+                    const float x = xr[u * R + k + q];
+                    const float p = x * vh[q];
+                    sm[u] += fmaf(x, vh[q], -p) + x * vl[q];
+                    neumaier(s[u], c[u], p);
+                }
+        }
+        for (; k < R; ++k) {
+            const float vhi = vhi_m[(int64_t)k * R + j], vlo = vlo_m[(int64_t)k * R + j];
+#pragma unroll
+            for (int u = 0; u < kResRows; ++u) {
+                const float x = xr[u * R + k];
+                const float p = x * vhi;
+                sm[u] += fmaf(x, vhi, -p) + x * vlo;
+                neumaier(s[u], c[u], p);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kResRows; ++u)
+            if (i0 + u < I) {
+                const int64_t e = (i0 + u) * R + j;
+                Res[e] = (M[e] - s[u]) - (c[u] + sm[u]);
+            }
+    }
+}
+
 // lambda_r = ||X(:, r)||_2 and A(:, r) = X(:, r) / lambda_r (0 for a zero
 // column); one block per 32 columns, rows split over 32 warps in a fixed order.
 __global__ void __launch_bounds__(1024) normalize_kernel(const double* __restrict__ X, int64_t I, int R,
@@ -254,31 +676,42 @@ __device__ double block_sum(double v, double* sh) {
     return t;   // valid in thread 0
 }
 
-// fit = 1 - sqrt(max(||Y||^2 + lambda^T H lambda - 2 <Y, X>, 0)) / ||Y||, with
-// <Y, X> = sum_r lambda_r sum_i M(i, r) A(i, r); NaN if the Cholesky failed.
-__global__ void __launch_bounds__(1024) fit_kernel(const double* __restrict__ H, const float* __restrict__ lam,
-                                                   const float* __restrict__ M, const float* __restrict__ A,
-                                                   int64_t I, int R, const double* __restrict__ norm_y2,
-                                                   const int* __restrict__ info, double* __restrict__ fit) {
-    __shared__ double sh[32];
+// The fit over many blocks: block b takes rows r = b, b + B, ... of H for
+// lambda^T H lambda and rows i = b, b + B, ... of M and A for <Y, X>, and writes
+// its two partial sums; fit_final_kernel adds them in block order.
+constexpr int kFitBlocks = 128;
+__global__ void __launch_bounds__(256) fit_partial_kernel(const double* __restrict__ H, const float* __restrict__ lam,
+                                                          const float* __restrict__ M, const float* __restrict__ A,
+                                                          int64_t I, int R, double* __restrict__ part) {
+    __shared__ double sh[8];
     double x2 = 0.0, in = 0.0;
-    // thread t takes columns c = t mod 32 + 32 q and rows r = t / 32 + 32 p
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int c = lane; c < R; c += 32) {
-        const double lc = (double)lam[c];
-        for (int r = warp; r < R; r += 32) x2 += (double)lam[r] * H[(int64_t)r * R + c] * lc;
+    for (int r = blockIdx.x; r < R; r += gridDim.x) {
         double t = 0.0;
-        for (int64_t i = warp; i < I; i += 32) t += (double)M[i * R + c] * (double)A[i * R + c];
-        in += lc * t;
+        for (int c = threadIdx.x; c < R; c += blockDim.x) t += H[(int64_t)r * R + c] * (double)lam[c];
+        x2 += (double)lam[r] * t;
     }
+    for (int64_t i = blockIdx.x; i < I; i += gridDim.x)
+        for (int c = threadIdx.x; c < R; c += blockDim.x)
+            in += (double)lam[c] * ((double)M[i * R + c] * (double)A[i * R + c]);
     x2 = block_sum(x2, sh);
     in = block_sum(in, sh);
     if (threadIdx.x == 0) {
-        const double y2 = *norm_y2;
-        const double res2 = y2 + x2 - 2.0 * in;
-        *fit = (*info != 0) ? __longlong_as_double(0x7ff8000000000000ll)
-                            : 1.0 - sqrt(res2 > 0.0 ? res2 : 0.0) / sqrt(y2);
+        part[2 * blockIdx.x] = x2;
+        part[2 * blockIdx.x + 1] = in;
     }
+}
+
+__global__ void fit_final_kernel(const double* __restrict__ part, int nb, const double* __restrict__ norm_y2,
+                                 const int* __restrict__ info, double* __restrict__ fit) {
+    if (threadIdx.x != 0) return;
+    double x2 = 0.0, in = 0.0;
+    for (int b = 0; b < nb; ++b) {
+        x2 += part[2 * b];
+        in += part[2 * b + 1];
+    }
+    const double y2 = *norm_y2;
+    const double res2 = y2 + x2 - 2.0 * in;
+    *fit = (*info != 0) ? __longlong_as_double(0x7ff8000000000000ll) : 1.0 - sqrt(res2 > 0.0 ? res2 : 0.0) / sqrt(y2);
 }
 
 // ||Y||^2 in fp64: fixed-order block partials, then one block adds them
@@ -342,20 +775,27 @@ cudaError_t cpals_hadamard(const double* G, int d, int skip, int R, double* V, c
     return cudaGetLastError();
 }
 
-cudaError_t cpals_cholesky(double* V, int R, int* info, double* dinv, cudaStream_t s) {
+template <typename T>
+cudaError_t blocked_cholesky(T* V, int R, int* info, T* dinv, cudaStream_t s) {
     for (int k0 = 0; k0 < R; k0 += kChNB) {
         const int nb = R - k0 < kChNB ? R - k0 : kChNB;
-        chol_diag_kernel<<<1, 256, 0, s>>>(V, R, k0, nb, info, dinv);
+        chol_diag_kernel<T><<<1, 256, 0, s>>>(V, R, k0, nb, info, dinv);
         const int rest = R - k0 - nb;
         if (rest > 0) {
-            chol_panel_kernel<<<(unsigned)((rest + 255) / 256), 256, 0, s>>>(V, R, k0, nb, dinv);
+            // panel rows spread over CTAs of 32 threads, so that short panels still
+            // use several SMs
+            chol_panel_kernel<T><<<(unsigned)((rest + 31) / 32), 32, 0, s>>>(V, R, k0, nb, dinv);
             const unsigned nt = (unsigned)((rest + kChNB - 1) / kChNB);
-            chol_update_kernel<<<dim3(nt, nt), 256, 0, s>>>(V, R, k0, nb);
+            chol_update_kernel<T><<<dim3(nt, nt), 256, 0, s>>>(V, R, k0, nb);
         }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t cpals_cholesky(double* V, int R, int* info, double* dinv, cudaStream_t s) {
+    return blocked_cholesky<double>(V, R, info, dinv, s);
 }
 
 int cpals_cholesky_launches(int R) {
@@ -377,9 +817,57 @@ cudaError_t cpals_solve(double* L, const double* dinv, int R, const float* M, in
         const int64_t n = (int64_t)R * R;
         int64_t blocks = (n + 255) / 256;
         if (blocks > 152 * 8) blocks = 152 * 8;
-        mirror_lower_kernel<<<(unsigned)blocks, 256, 0, s>>>(L, R);
+        mirror_lower_kernel<double><<<(unsigned)blocks, 256, 0, s>>>(L, R);
     }
     solve_kernel<<<(unsigned)((I + warps - 1) / warps), warps * 32, smem, s>>>(L, dinv, R, M, I, X);
+    return cudaGetLastError();
+}
+
+int cpals_mixed_max_rank() { return kChol32MaxR; }
+
+int cpals_mixed_launches(int R) { return R <= kSmemMaxR ? 5 : 5 + cpals_cholesky_launches(R); }
+
+cudaError_t cpals_solve_mixed(const double* V, int R, const float* M, int64_t I, double* X, float* vhi, float* vlo,
+                              float* L, float* dinv, float* x0, float* res, int* info, cudaStream_t s) {
+    if (R > kChol32MaxR) return cudaErrorInvalidValue;
+    const int64_t n = (int64_t)R * R;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    split_v_kernel<<<(unsigned)blocks, 256, 0, s>>>(V, n, vhi, vlo, L);
+    cudaError_t e;
+    if (R <= kSmemMaxR) {
+        // the factor and the solves with the triangle in shared memory
+        const size_t csm = ((size_t)tri(R) + (size_t)R * 33) * sizeof(float);
+        e = cudaFuncSetAttribute(chol_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
+        if (e != cudaSuccess) return e;
+        chol_smem_kernel<<<1, kCholSmemThreads, csm, s>>>(vhi, R, L, dinv, info);
+        const size_t ssm = ((size_t)tri(R) + (size_t)33 * R) * sizeof(float);
+        e = cudaFuncSetAttribute(solve_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
+        if (e != cudaSuccess) return e;
+        const unsigned sb = (unsigned)((I + 31) / 32);
+        solve_smem_kernel<<<sb, 1024, ssm, s>>>(L, dinv, R, M, I, x0, nullptr, nullptr);
+        const size_t rsm = (size_t)kResRows * R * sizeof(float);
+        e = cudaFuncSetAttribute(residual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm);
+        if (e != cudaSuccess) return e;
+        residual_kernel<<<dim3((unsigned)((R + kResCols - 1) / kResCols), (unsigned)((I + kResRows - 1) / kResRows)),
+                          kResCols, rsm, s>>>(M, x0, vhi, vlo, I, R, res);
+        solve_smem_kernel<<<sb, 1024, ssm, s>>>(L, dinv, R, res, I, nullptr, x0, X);
+        return cudaGetLastError();
+    }
+    e = blocked_cholesky<float>(L, R, info, dinv, s);
+    if (e != cudaSuccess) return e;
+    mirror_lower_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(L, R);
+    const size_t ssm = ((size_t)kSolveRows * R + (size_t)R * 33) * sizeof(float);
+    e = cudaFuncSetAttribute(solve32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
+    if (e != cudaSuccess) return e;
+    const unsigned sblocks = (unsigned)((I + kSolveRows - 1) / kSolveRows);
+    solve32_kernel<<<sblocks, 32, ssm, s>>>(L, dinv, R, M, I, x0, nullptr, nullptr);
+    const size_t rsm = (size_t)kResRows * R * sizeof(float);
+    e = cudaFuncSetAttribute(residual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm);
+    if (e != cudaSuccess) return e;
+    residual_kernel<<<dim3((unsigned)((R + kResCols - 1) / kResCols), (unsigned)((I + kResRows - 1) / kResRows)),
+                      kResCols, rsm, s>>>(M, x0, vhi, vlo, I, R, res);
+    solve32_kernel<<<sblocks, 32, ssm, s>>>(L, dinv, R, res, I, nullptr, x0, X);
     return cudaGetLastError();
 }
 
@@ -389,12 +877,15 @@ cudaError_t cpals_normalize(const double* X, int64_t I, int R, float* A, float* 
 }
 
 cudaError_t cpals_fit(const double* H, const float* lam, const float* M, const float* A, int64_t I, int R,
-                      const double* norm_y2, const int* info, double* fit, cudaStream_t s) {
-    fit_kernel<<<1, 1024, 0, s>>>(H, lam, M, A, I, R, norm_y2, info, fit);
+                      const double* norm_y2, const int* info, double* fit, double* part, cudaStream_t s) {
+    fit_partial_kernel<<<kFitBlocks, 256, 0, s>>>(H, lam, M, A, I, R, part);
+    fit_final_kernel<<<1, 32, 0, s>>>(part, kFitBlocks, norm_y2, info, fit);
     return cudaGetLastError();
 }
 
-size_t cpals_sumsq_scratch_bytes() { return kSqBlocks * sizeof(double); }
+size_t cpals_sumsq_scratch_bytes() {
+    return (kSqBlocks > 2 * kFitBlocks ? kSqBlocks : 2 * kFitBlocks) * sizeof(double);
+}
 
 cudaError_t cpals_sum_squares(const float* Y, int64_t n, double* part, double* out, cudaStream_t s) {
     sumsq_partial_kernel<<<kSqBlocks, 256, 0, s>>>(Y, n, part);

@@ -173,8 +173,16 @@ int cpals_cholesky_launches(int R);
 cudaError_t cpals_solve(double* L, const double* dinv, int R, const float* M, int64_t I, double* X,
                         cudaStream_t s);
 cudaError_t cpals_normalize(const double* X, int64_t I, int R, float* A, float* lam, cudaStream_t s);
+// fit = 1 - ||Y - X|| / ||Y|| (part: cpals_sumsq_scratch_bytes() of fp64 scratch)
 cudaError_t cpals_fit(const double* H, const float* lam, const float* M, const float* A, int64_t I, int R,
-                      const double* norm_y2, const int* info, double* fit, cudaStream_t s);
+                      const double* norm_y2, const int* info, double* fit, double* part, cudaStream_t s);
+// X = M V^{-1} (fp64 out) for R <= cpals_mixed_max_rank(): V split into two fp32
+// words (vhi, vlo: R x R each), factored in fp32 (L: R x R, dinv: R), rows solved
+// in fp32 into x0 (I x R), residual M - x0 V (res: I x R) solved and added
+int cpals_mixed_max_rank();
+int cpals_mixed_launches(int R);
+cudaError_t cpals_solve_mixed(const double* V, int R, const float* M, int64_t I, double* X, float* vhi, float* vlo,
+                              float* L, float* dinv, float* x0, float* res, int* info, cudaStream_t s);
 size_t cpals_sumsq_scratch_bytes();
 cudaError_t cpals_sum_squares(const float* Y, int64_t n, double* part, double* out, cudaStream_t s);
 cudaError_t launch_reduce_splits(const float* part, int64_t splits, int64_t n, float* out,
