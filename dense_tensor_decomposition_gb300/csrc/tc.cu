@@ -1,26 +1,39 @@
-// Tensor-core (tcgen05 / TMEM) MTTKRP path: fp32-accurate 3xTF32 on the
-// 5th-generation tensor cores of sm_103a.
+// Tensor-core (tcgen05 / TMEM) kernels of the MTTKRP path on sm_103a, all
+// fp32-accurate: every operand is split into two low-precision terms whose
+// cross products the tensor cores accumulate in fp32, so the result matches an
+// fp32 contraction to within a few fp32 roundings of the sum of magnitudes.
 //
-// Per CTA: a 128 x BN tile of M_k (rows i, columns r) and a contiguous range of
-// pre indices pi.  For every pi the contraction over the inner-group index j
-// runs in K-steps of 16:
-//   * a TMA tensor copy brings the 128 x 16 tile of Y_(k) into shared memory
-//     (K-major, 64-byte swizzle; for the innermost mode it arrives i-major and
-//     is transposed by the producer warps);
-//   * one bulk copy brings the matching pre-swizzled BN x 16 tile of the inner
-//     Khatri-Rao table, as a "hi" and a "lo" image written by the prep kernel;
-//   * two producer warps write lo(y) = y - tf32(y) next to the raw tile;
-//   * one thread issues, per 8-wide k-slice, the three products
-//     hi*hi + hi*lo + lo*hi with tcgen05.mma.kind::tf32 into a TMEM accumulator.
-// The tensor cores read fp32 operands as tf32 by truncation, so the raw fp32
-// tile serves as its own "hi" part.  TMEM accumulation rounds toward zero, so
-// after at most 8 K-steps (128 indices, 48 MMAs) the accumulator is drained:
-// eight epilogue warps read it with tcgen05.ld and add G(pi, r) * z into fp32
-// registers (round to nearest), while the MMAs continue into the second TMEM
-// buffer.  At the end each thread writes its row segment of the tile (or of
-// its split's partial).  Every wait on an mbarrier is bounded in time; on
-// expiry the kernel records an error word, stops issuing work, waits (bounded)
-// for its own copies and MMAs and frees its TMEM before returning.
+// Common structure.  A CTA owns a 128 x BN tile of M_k (rows i, columns r) and
+// a contiguous range of pre indices pi; for every pi the contraction over the
+// inner-group index j runs in K-steps.  A TMA warp brings tiles of Y_(k)
+// (tensor maps over the natural layout of Y, or over its fp16 images) into a
+// ring of shared-memory stages, one elected thread issues tcgen05.mma into a
+// double-buffered TMEM accumulator, and epilogue warps drain it with
+// tcgen05.ld after a bounded number of K-steps (TMEM accumulation truncates),
+// scale each column by the pre-mode factor product G(pi, r) and add it into
+// fp32 registers.  Every mbarrier wait is bounded in time; on expiry the
+// kernel records an error word, stops issuing, waits (bounded) for its own
+// copies and MMAs and frees its TMEM before returning.
+//
+// The main kernels:
+//  * tc_img_kernel: kind::f16 on a two-term fp16 split of Y (hi and lo images
+//    written once per call, with a power-of-two scale per slab of mode 0) and
+//    of the inner Khatri-Rao rows; products hi*hi + hi*lo + lo*hi.  Modes
+//    other than the innermost read K-major images; the innermost one reads its
+//    natural (i-fastest) image directly as an MN-major A operand, or a
+//    transposed image where the MN-major form does not apply.  A SMALL form
+//    stacks several pre indices in one tile for short inner groups.
+//  * tc_h2_kernel: the same split formed in TMEM by producer warps from raw
+//    fp32 tiles (large R; register split between warpgroups).
+//  * tc_mttkrp_kernel: kind::tf32, 3xTF32 split (raw fp32 tile as hi,
+//    producer warps write lo = y - tf32(y)); K-major and innermost forms.
+//  * tc_tmem_kernel: the 3xTF32 kernel with A in TMEM, for large R on the
+//    innermost mode.
+// Helpers: the per-slab max|Y| pass and the fp16 image splits of Y (natural
+// and transposed), the pre-swizzled B images of the inner Khatri-Rao table
+// (tf32 and fp16, with per-column scales), the explicit Khatri-Rao image
+// builder, the mode-n-product operand preparation, and the tensor-pipe
+// throughput probe.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -44,16 +57,10 @@ constexpr int kBM = 128;
 constexpr int kBK = 16;           // contraction indices per K-step (64-byte rows)
 constexpr int kChunkSteps = 8;    // at most this many K-steps accumulate in TMEM between drains
 constexpr int kEpiWarps = 16;  // 4 per TMEM lane quadrant
-#ifndef TC_PROD_WARPS
-#define TC_PROD_WARPS 2
-#endif
-#ifndef TC_PROD_WARPS_INNER
-#define TC_PROD_WARPS_INNER 2
-#endif
 // Warp roles: 0 TMA, 1 MMA, then the operand-producer warps, then the epilogue.
 template <bool INNER>
 struct Roles {
-    static constexpr int kProdWarps = INNER ? TC_PROD_WARPS_INNER : TC_PROD_WARPS;
+    static constexpr int kProdWarps = 2;
     static constexpr int kProdThreads = kProdWarps * 32;
     static constexpr int kFirstEpi = 2 + kProdWarps;
     static constexpr int kThreads = (kFirstEpi + kEpiWarps) * 32;
@@ -174,14 +181,6 @@ __device__ __forceinline__ uint32_t mbar_test_wait(uint64_t* bar, uint32_t parit
 
 // Slow path of wait_bounded: suspend-and-retry until the phase completes, the
 // CTA is aborted, or kWaitNs pass (then the CTA is aborted and `code` recorded).
-#ifndef TC_WAIT_INLINE
-#define TC_WAIT_INLINE 0
-#endif
-#if TC_WAIT_INLINE
-#define TC_WAIT_SLOW_ATTR __forceinline__
-#else
-#define TC_WAIT_SLOW_ATTR __noinline__
-#endif
 // The clock is first read after one suspension has run out without the phase
 // completing, so a wait that ends within the first suspension (the common case)
 // costs no timer read; the bound is kWaitNs plus one suspension.
@@ -202,7 +201,7 @@ __device__ __forceinline__ bool wait_slow_body(uint64_t* bar, uint32_t parity, v
         }
     }
 }
-__device__ TC_WAIT_SLOW_ATTR bool wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+__device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                        uint32_t* status, uint32_t code) {
     return wait_slow_body(bar, parity, abort_flag, status, code);
 }
@@ -464,44 +463,38 @@ __device__ __forceinline__ uint32_t sw64_off(uint32_t row, uint32_t chunk) {
 }
 
 // ---------------------------------------------------------------------------
-// Main kernel
+// 3xTF32 kernel
 // ---------------------------------------------------------------------------
+//
+// Per K-step of 16 indices: a TMA tensor copy brings the 128 x 16 tile of
+// Y_(k) (K-major, 64-byte swizzle; for the innermost mode it arrives i-major
+// and the producer warps transpose it), one bulk copy brings the matching
+// pre-swizzled BN x 16 hi and lo images of the inner Khatri-Rao table, the
+// producer warps write lo(y) = y - tf32(y) next to the raw tile, and one
+// thread issues per 8-wide k-slice hi*hi + hi*lo + lo*hi (the tensor cores
+// read fp32 as tf32 by truncation, so the raw tile is its own hi part).  The
+// accumulator is drained after at most 8 K-steps (48 MMAs) while the MMAs
+// continue into the second TMEM buffer.
 //
 // Order of work in a CTA: the inner index range is cut into B-chunks of CK
 // K-steps whose hi|lo images stay resident in shared memory; for each chunk the
 // CTA walks all of its pi, streaming only Y tiles.  TMEM is drained after every
 // "unit" of at most kChunkSteps K-steps of one (chunk, pi) pair.
 
-#ifndef TC_STAGES
-#define TC_STAGES 5
-#endif
-#ifndef TC_STAGES_INNER
-#define TC_STAGES_INNER 3
-#endif
-#ifndef TC_BRES_KB
-#define TC_BRES_KB 128
-#endif
-#ifndef TC_INNER_XPOSE
-#define TC_INNER_XPOSE 1
-#endif
-#ifndef TC_TMEM_KMAJOR
-#define TC_TMEM_KMAJOR 0
-#endif
-#ifndef TC_H2_MIN_R
-#define TC_H2_MIN_R 160
-#endif
-#ifndef TC_TMEM_MIN_R
-#define TC_TMEM_MIN_R 448
-#endif
-#ifndef TC_MMA_WARP
-#define TC_MMA_WARP 1
-#endif
-#ifndef TC_EPI_LD
-#define TC_EPI_LD 8
-#endif
-#ifndef TC_BRES_INNER_KB
-#define TC_BRES_INNER_KB 128
-#endif
+
+// 3xTF32 kernel parameters: operand stages (K-major, innermost), resident
+// B-chunk kilobytes, TMEM columns per epilogue load, and the ranks from which
+// the fp16 split in tensor memory and the tf32 kernel with A in tensor memory
+// take over
+constexpr int kStages = 5, kStagesInner = 3;
+constexpr int kBResKB = 128, kBResInnerKB = 128;
+constexpr int kEpiLd = 8;
+constexpr int kH2MinR = 160, kTmemMinR = 448;
+// TMEM columns per epilogue load of the fp16-split kernels (register-resident
+// accumulators in the split-in-TMEM kernel, G-scaled rows in the image kernel)
+// and the smallest rank the fp16-image kernel takes
+constexpr int kH2EpiLd = 8, kImgEpiLd = 16;
+constexpr int kImgMinR = 32;
 
 template <int BN, bool INNER, bool SMALL = false>
 struct Smem {
@@ -509,11 +502,11 @@ struct Smem {
     static constexpr uint32_t kA = kBM * kBK * 4;      // 8 KB: one K-major A operand tile
     static constexpr uint32_t kB = BN * kBK * 4;       // BN x 64 B, one K-step of B
     static constexpr uint32_t kBRes =
-        (uint32_t)(SMALL ? 96 : INNER ? TC_BRES_INNER_KB : TC_BRES_KB) * 1024;  // resident B-chunk
+        (uint32_t)(SMALL ? 96 : INNER ? kBResInnerKB : kBResKB) * 1024;  // resident B-chunk
     static constexpr int kCK = (int)(kBRes / (2 * kB));  // K-steps per B-chunk
     // stages: raw Y tile + on-chip operand tile(s); one producer arrival, one
     // MMA wait and one MMA commit per stage
-    static constexpr int kRaw = INNER ? TC_STAGES_INNER : TC_STAGES;
+    static constexpr int kRaw = INNER ? kStagesInner : kStages;
     static constexpr int kOps = kRaw;
     static constexpr uint32_t kOp = INNER ? 2 * kA : kA;  // lo (and transposed hi if INNER)
     // per-warp G rows, double-buffered (small-I variant: up to 3 rows per warp)
@@ -751,9 +744,9 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
         // tensor pipe's duty cycle (six MMAs of BN / 2 cycles each per step), so
         // the loop is kept short: one wait and one commit per stage, and the
         // descriptors' low words advance incrementally (high word constant).
-        // TC_MMA_WARP: the whole warp runs the loop (warp-uniform values; lane 0
-        // issues through a predicate), otherwise lane 0 alone
-        constexpr bool kWarpIssue = TC_MMA_WARP != 0;
+        // The whole warp runs the loop (warp-uniform values; lane 0 issues
+        // through a predicate): measured faster than lane 0 alone
+        constexpr bool kWarpIssue = true;
         const uint32_t leader = lane == 0 ? 1u : 0u;
         auto mma_w = [&](uint32_t d, uint32_t aw, uint32_t bw_, uint32_t idesc_, uint32_t acc) {
             if constexpr (kWarpIssue) mma_tf32_wl(d, aw, bw_, idesc_, acc, leader);
@@ -917,11 +910,11 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
                                             make_float4(col[0].w, col[1].w, col[2].w, col[3].w)};
 #pragma unroll
                     for (int p = 0; p < 4; ++p) {
-                        // TC_INNER_XPOSE == 1: row 4 ib + p is stored at tile row
+                        // Row 4 ib + p is stored at tile row
                         // 4 ib + (p ^ (ib & 1)), so that the 8 lanes of a quarter-warp
                         // (two i-blocks of opposite parity) hit 8 distinct bank groups;
                         // the epilogue undoes the swap
-                        const int prow = TC_INNER_XPOSE == 1 ? (p ^ (ib & 1)) : p;
+                        const int prow = p ^ (ib & 1);
                         const uint32_t off = sw64_off(4 * ib + prow, jc);
                         *reinterpret_cast<float4*>(hi + off) = rows[p];
                         *reinterpret_cast<float4*>(lo + off) =
@@ -942,7 +935,7 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
             // unit are copied (cp.async) while the current one is drained; at the
             // end the slots are summed through shared memory.
             constexpr int kCols = BN / 4;
-            constexpr int kLd = TC_EPI_LD < kCols ? TC_EPI_LD : kCols;  // TMEM columns per wait
+            constexpr int kLd = kEpiLd < kCols ? kEpiLd : kCols;  // TMEM columns per wait
             constexpr int kW = 3;
             const int quad = warp & 3;
             const int part = (warp - kFE) >> 2;
@@ -1039,11 +1032,11 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
             // copied into the warp's second G buffer (cp.async, no registers) while
             // the current pair is drained.
             constexpr int kCols = BN / 4;
-            constexpr int kLd = TC_EPI_LD < kCols ? TC_EPI_LD : kCols;  // TMEM columns per wait
+            constexpr int kLd = kEpiLd < kCols ? kEpiLd : kCols;  // TMEM columns per wait
             const int quad = warp & 3;
             const int part = (warp - kFE) >> 2;
             const int lr = 32 * quad + lane;   // TMEM lane = tile row
-            const int64_t row = m0 + ((INNER && TC_INNER_XPOSE == 1) ? (lr ^ ((lr >> 2) & 1)) : lr);
+            const int64_t row = m0 + (INNER ? (lr ^ ((lr >> 2) & 1)) : lr);
             const int64_t c0 = r0 + part * kCols;
             float* gw = gsm + (warp - kFE) * 2 * kCols;   // this warp's two G rows
             float acc[kCols];
@@ -1145,28 +1138,19 @@ __global__ void __launch_bounds__(Roles<INNER>::kThreads, 1) tc_mttkrp_kernel(co
 // read it, so the TMA ring is decoupled from the MMAs and runs far ahead.
 // TMEM: accumulators at columns [0, BN) and [BN, 2 BN); A slots of 32 columns
 // (hi 16 | lo 16) from column 2 BN.
-#ifndef TC_T_BN
-#define TC_T_BN 224
-#endif
-#ifndef TC_T_ASLOTS
-#define TC_T_ASLOTS 2
-#endif
-constexpr int kTBN = TC_T_BN;
-constexpr int kTASlots = TC_T_ASLOTS;
+constexpr int kTBN = 224;
+constexpr int kTASlots = 2;
 constexpr uint32_t kTACol0 = 2 * kTBN;
 constexpr int kTProdWarps = 4;
 constexpr int kTFirstEpi = 2 + kTProdWarps;
 constexpr int kTThreads = (kTFirstEpi + kEpiWarps) * 32;
-#ifndef TC_T_STAGES
-#define TC_T_STAGES 12
-#endif
 
 struct SmemT {
     static constexpr uint32_t kY = kBM * kBK * 4;      // 8 KB raw Y tile
     static constexpr uint32_t kB = kTBN * kBK * 4;     // 14 KB: one K-step of B (hi or lo)
     static constexpr int kCK = 4;                      // K-steps per B-chunk
     static constexpr uint32_t kBRes = kCK * 2 * kB;    // 112 KB resident B-chunk
-    static constexpr int kRaw = TC_T_STAGES;
+    static constexpr int kRaw = 12;
     static constexpr uint32_t kG = kEpiWarps * 2 * (kTBN / 4) * 4;
     static constexpr uint32_t kBarBytes = 512;
     static constexpr uint32_t kOffRaw = kBRes;
@@ -1538,12 +1522,6 @@ __global__ void __launch_bounds__(kTThreads, 1) tc_tmem_kernel(const __grid_cons
 constexpr int kBK2 = 32;
 constexpr int kChunkSteps2 = 4;   // 128 contraction indices between TMEM drains
 
-#ifndef TC_PREFETCH
-#define TC_PREFETCH 1
-#endif
-#ifndef TC_H2_STAGES
-#define TC_H2_STAGES 6
-#endif
 // Tile 128 x kH2BN; TMEM: accumulators at [0, BN) and [BN, 2 BN), then kH2Slots
 // A slots of 32 columns (hi 16 | lo 16, one K-step each).  Producers and MMAs
 // hand the slots over in groups of kH2Group K-steps (one barrier round trip per
@@ -1551,25 +1529,7 @@ constexpr int kChunkSteps2 = 4;   // 128 contraction indices between TMEM drains
 // 128 x 224 with single-step groups (two slots) is the fastest per output
 // column; 128 x 192 with four slots, in groups of one or two K-steps, was 9-11 %
 // slower per column (the MMA issuer's per-step cost does not shrink with N).
-#ifndef TC_H2_BN
-#define TC_H2_BN 224
-#endif
-#ifndef TC_H2_GROUP
-#define TC_H2_GROUP 1
-#endif
-#ifndef TC_IMG
-#define TC_IMG 1           // fp16-image kernel for K-major modes
-#endif
-#ifndef TC_IMG_XPOSE
-#define TC_IMG_XPOSE 1     // the innermost mode from transposed fp16 images
-#endif
-#ifndef TC_IMG_MIN_R
-#define TC_IMG_MIN_R 32
-#endif
-#ifndef TC_H2_EPI_LD
-#define TC_H2_EPI_LD 8   // TMEM columns per epilogue load (4 or 8)
-#endif
-// Warp roles.  With the register split (default) the CTA is six warpgroups:
+// Warp roles.  The CTA is six warpgroups:
 // producers (warps 0-3, one per TMEM lane quadrant), control (TMA warp 4, MMA
 // warp 5, two idle warps), and four epilogue warpgroups (warps 8-23).  The
 // control and producer warpgroups give registers back (setmaxnreg.dec) and the
@@ -1577,39 +1537,26 @@ constexpr int kChunkSteps2 = 4;   // 128 contraction indices between TMEM drains
 // register-resident accumulators do not spill.  The launch allots 80 registers
 // a thread (768 threads); the split uses 128 x (56 + 72 + 4 x 88) = 61440 of
 // the 61440 allotted, and the host refuses the launch if the kernel was built
-// with fewer than 80.  Without the split: TMA warp 0, MMA warp 1, producers
-// 2-5, epilogue 6-21.
-#ifndef TC_H2_REGSPLIT
-#define TC_H2_REGSPLIT 1
-#endif
-#if TC_H2_REGSPLIT
+// with fewer than 80.
 constexpr int kH2ProdWarp0 = 0, kH2TmaWarp = 4, kH2MmaWarp = 5, kH2FirstEpi = 8;
-#else
-constexpr int kH2ProdWarp0 = 2, kH2TmaWarp = 0, kH2MmaWarp = 1, kH2FirstEpi = 6;
-#endif
 constexpr int kH2Threads = (kH2FirstEpi + kEpiWarps) * 32;
 constexpr int kH2RegsCtl = 56, kH2RegsProd = 72, kH2RegsEpi = 88;
 constexpr int kH2RegsLaunch = 80;   // registers a thread the split needs at launch
-static_assert(!TC_H2_REGSPLIT ||
-                  128 * (kH2RegsCtl + kH2RegsProd + 4 * kH2RegsEpi) <= kH2Threads * kH2RegsLaunch,
+static_assert(128 * (kH2RegsCtl + kH2RegsProd + 4 * kH2RegsEpi) <= kH2Threads * kH2RegsLaunch,
               "register split exceeds the launch allotment");
-static_assert(!TC_H2_REGSPLIT || kH2Threads == 768, "six warpgroups");
+static_assert(kH2Threads == 768, "six warpgroups");
 
 template <int N>
 __device__ __forceinline__ void h2_regs_dec() {
-#if TC_H2_REGSPLIT
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-#endif
 }
 template <int N>
 __device__ __forceinline__ void h2_regs_inc() {
-#if TC_H2_REGSPLIT
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-#endif
 }
-constexpr int kH2BN = TC_H2_BN;
+constexpr int kH2BN = 224;
 constexpr int kH2Slots = (512 - 2 * kH2BN) / 32 < 4 ? (512 - 2 * kH2BN) / 32 : 4;
-constexpr int kH2Group = TC_H2_GROUP;
+constexpr int kH2Group = 1;
 constexpr uint32_t kH2ACol0 = 2 * kH2BN;
 static_assert(kH2Slots >= 2 * kH2Group, "two A-slot groups in flight");
 
@@ -1618,7 +1565,7 @@ struct SmemH2 {
     static constexpr uint32_t kB = kH2BN * kBK2 * 2;   // one K-step of B (hi or lo, fp16): BN x 64 B
     static constexpr int kCK = 4;                      // K-steps per B-chunk
     static constexpr uint32_t kBRes = kCK * 2 * kB;    // 112 KB resident B-chunk
-    static constexpr int kRaw = TC_H2_STAGES;
+    static constexpr int kRaw = 6;
     static constexpr uint32_t kG = kEpiWarps * 2 * (kH2BN / 4) * 4;
     static constexpr uint32_t kBarBytes = 512;
     static constexpr uint32_t kOffRaw = kBRes;
@@ -1730,12 +1677,9 @@ __global__ void __launch_bounds__(kH2Threads, 1) tc_h2_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int64_t T = npi * KS;  // K-steps of this CTA
-
     const bool prod_warp = warp >= kH2ProdWarp0 && warp < kH2ProdWarp0 + kTProdWarps;
     if (!prod_warp && warp < kH2FirstEpi) {
-        // control warpgroup: TMA warp, MMA warp (and, with the register split,
-        // two idle warps)
+        // control warpgroup: TMA warp, MMA warp and two idle warps
         h2_regs_dec<kH2RegsCtl>();
         if (warp == kH2TmaWarp) {
             // ------------------------- TMA producer -------------------------
@@ -1880,7 +1824,7 @@ __global__ void __launch_bounds__(kH2Threads, 1) tc_h2_kernel(const __grid_const
                                 }
                                 // non-blocking test of the next group; its answer is used at
                                 // the next group start, so its latency overlaps the bookkeeping
-                                a_ready = TC_PREFETCH && mbar_test_wait(&a_full[ag], aph) != 0;
+                                a_ready = mbar_test_wait(&a_full[ag], aph) != 0;
                             }
                         }
                     }
@@ -2021,15 +1965,15 @@ __global__ void __launch_bounds__(kH2Threads, 1) tc_h2_kernel(const __grid_const
                     const uint32_t tbase =
                         tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
 #pragma unroll
-                    for (int cc = 0; cc < kCols; cc += TC_H2_EPI_LD) {
-                        uint32_t z[TC_H2_EPI_LD];
-                        if constexpr (TC_H2_EPI_LD == 8)
+                    for (int cc = 0; cc < kCols; cc += kH2EpiLd) {
+                        uint32_t z[kH2EpiLd];
+                        if constexpr (kH2EpiLd == 8)
                             tmem_ld8(tbase + cc, z);
                         else
                             tmem_ld4(tbase + cc, z);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int q = 0; q < TC_H2_EPI_LD / 4; ++q) {
+                        for (int q = 0; q < kH2EpiLd / 4; ++q) {
                             const float4 g = *reinterpret_cast<const float4*>(g_cur + cc + 4 * q);
                             acc[cc + 4 * q + 0] = fmaf(g.x, __uint_as_float(z[4 * q + 0]), acc[cc + 4 * q + 0]);
                             acc[cc + 4 * q + 1] = fmaf(g.y, __uint_as_float(z[4 * q + 1]), acc[cc + 4 * q + 1]);
@@ -2101,13 +2045,7 @@ __global__ void __launch_bounds__(kH2Threads, 1) tc_h2_kernel(const __grid_const
 // gives registers back), warps 4-19 epilogue (which take them).
 // ---------------------------------------------------------------------------
 constexpr int kBK4 = 64;          // contraction indices per K-step (128-byte fp16 rows)
-#ifndef TC_IMG_EPI_LD
-#define TC_IMG_EPI_LD 16   // TMEM columns per epilogue load (8, 16 or 32)
-#endif
-#ifndef TC_IMG_CK
-#define TC_IMG_CK 2
-#endif
-constexpr int kImgCK = TC_IMG_CK;   // K-steps per B chunk and per TMEM drain (128 indices)
+constexpr int kImgCK = 2;   // K-steps per B chunk and per TMEM drain (128 indices)
 constexpr int kImgEpiWarp0 = 4;
 constexpr int kImgThreads = (kImgEpiWarp0 + kEpiWarps) * 32;   // 640
 // registers a thread: the launch allots 96 (65536 / 640, in units of 8); the
@@ -2436,7 +2374,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             // TMEM lane slot * I + i holds pre index pi_u + slot of the unit; each
             // lane reads its own G row at every drain.  At the end the slots are
             // summed through shared memory.
-            static_assert(kCols % TC_IMG_EPI_LD == 0, "TMEM load width");
+            static_assert(kCols % kImgEpiLd == 0, "TMEM load width");
             const int quad = warp & 3;
             const int part = (warp - kImgEpiWarp0) >> 2;
             const int64_t c0 = r0 + part * kCols;
@@ -2462,16 +2400,16 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                     const uint32_t tbase =
                         tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
 #pragma unroll
-                    for (int cc = 0; cc < kCols; cc += TC_IMG_EPI_LD) {
-                        float g[TC_IMG_EPI_LD];   // this row's G values for the group
+                    for (int cc = 0; cc < kCols; cc += kImgEpiLd) {
+                        float g[kImgEpiLd];   // this row's G values for the group
 #pragma unroll
-                        for (int q = 0; q < TC_IMG_EPI_LD; ++q)
+                        for (int q = 0; q < kImgEpiLd; ++q)
                             g[q] = (live_row && c0 + cc + q < a.R) ? __ldg(grow + cc + q) : 0.f;
-                        uint32_t z[TC_IMG_EPI_LD];
-                        tmem_ld_cols<TC_IMG_EPI_LD>(tbase + cc, z);
+                        uint32_t z[kImgEpiLd];
+                        tmem_ld_cols<kImgEpiLd>(tbase + cc, z);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int q = 0; q < TC_IMG_EPI_LD; ++q)
+                        for (int q = 0; q < kImgEpiLd; ++q)
                             acc[cc + q] = fmaf(g[q], __uint_as_float(z[q]), acc[cc + q]);
                     }
                     tc_fence_before();
@@ -2505,7 +2443,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             }
         } else {
         constexpr int kGv = (kCols + 31) / 32;   // G values a lane holds
-        static_assert(kCols % TC_IMG_EPI_LD == 0, "TMEM load width");
+        static_assert(kCols % kImgEpiLd == 0, "TMEM load width");
         const int quad = warp & 3;
         const int part = (warp - kImgEpiWarp0) >> 2;
         const int64_t row = m0 + 32 * quad + lane;
@@ -2540,12 +2478,12 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                 const uint32_t tbase =
                     tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(zb * BN + part * kCols);
 #pragma unroll
-                for (int cc = 0; cc < kCols; cc += TC_IMG_EPI_LD) {
-                    uint32_t z[TC_IMG_EPI_LD];
-                    tmem_ld_cols<TC_IMG_EPI_LD>(tbase + cc, z);
+                for (int cc = 0; cc < kCols; cc += kImgEpiLd) {
+                    uint32_t z[kImgEpiLd];
+                    tmem_ld_cols<kImgEpiLd>(tbase + cc, z);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < TC_IMG_EPI_LD; ++q) {
+                    for (int q = 0; q < kImgEpiLd; ++q) {
                         const int e = cc + q;
                         const float g = __shfl_sync(0xffffffffu, g_cur[e / 32], e % 32);
                         acc[e] = fmaf(g, __uint_as_float(z[q]), acc[e]);
@@ -3448,7 +3386,7 @@ cudaError_t launch_h2(const TcArgs& args, dim3 grid, cudaStream_t s) {
     if (e0 != cudaSuccess) return e0;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        if (TC_H2_REGSPLIT) {
+        {
             // setmaxnreg.inc waits until the pool allotted at launch can serve it:
             // refuse a build whose launch allotment is below what the split assumes
             cudaFuncAttributes fa;
@@ -3561,14 +3499,14 @@ bool tc_plan(const Plan& p, ModePlan& mp, bool allow_fp16) {
     mp.tc_ps = mp.tc_small ? (int)(kBM / g.I) : 1;
     // innermost mode with large R: A staged in tensor memory (the i-contiguous
     // tile is transposed on the way into TMEM, no shared-memory round trip)
-    mp.tc_tmem = (!mp.explicit_krp && !mp.tc_small && g.R >= TC_TMEM_MIN_R && (mp.tc_inner || TC_TMEM_KMAJOR)) ? 1 : 0;
+    mp.tc_tmem = (!mp.explicit_krp && !mp.tc_small && g.R >= kTmemMinR && mp.tc_inner) ? 1 : 0;
     // the two-term fp16 split in tensor memory (128 x 224 tiles) does a K-step
     // about 1.4 times faster than the tf32 kernel (128 x 256 tiles): it wins
     // unless its narrower tiles waste more columns than that
     {
         const int64_t h2_cols = cdiv64(g.R, kH2BN) * kH2BN * 10;
         const int64_t tf_cols = cdiv64(g.R, 256) * 256 * 14;
-        mp.tc_h2 = (allow_fp16 && !mp.explicit_krp && !mp.tc_small && g.R >= TC_H2_MIN_R && h2_cols < tf_cols) ? 1 : 0;
+        mp.tc_h2 = (allow_fp16 && !mp.explicit_krp && !mp.tc_small && g.R >= kH2MinR && h2_cols < tf_cols) ? 1 : 0;
     }
     if (mp.tc_h2) mp.tc_tmem = 1;
     mp.tc_kw = mp.tc_h2 ? kBK2 : kBK;
@@ -3585,7 +3523,7 @@ bool tc_plan(const Plan& p, ModePlan& mp, bool allow_fp16) {
     // the kernels that convert Y per CTA take over
     int64_t numel = 1;
     for (int t = 0; t < p.d; ++t) numel *= p.dims[t];
-    if (allow_fp16 && TC_IMG && g.R >= TC_IMG_MIN_R && numel <= ((int64_t)12 << 30)) {
+    if (allow_fp16 && g.R >= kImgMinR && numel <= ((int64_t)12 << 30)) {
         ModePlan t = mp;
         t.tc_img = 1;
         t.tc_h2 = 0;
@@ -3603,7 +3541,7 @@ bool tc_plan(const Plan& p, ModePlan& mp, bool allow_fp16) {
             // the innermost mode from the natural images, A MN-major (boxes of
             // 64 i x 64 j; the i stride of the image a 16-byte multiple)
             mp = t;
-        } else if (TC_IMG_XPOSE && timg_eligible(g, p.d) && cdiv64(g.J, kBK4) * kBK4 * 8 <= g.J * 9) {
+        } else if (timg_eligible(g, p.d) && cdiv64(g.J, kBK4) * kBK4 * 8 <= g.J * 9) {
             t.tc_img_mn = 0;
             // the innermost mode from the transposed images (written in the same
             // pass as the others); the K-steps run over j alone
@@ -3632,7 +3570,7 @@ bool tc_plan(const Plan& p, ModePlan& mp, bool allow_fp16) {
         // one pre index: split the B chunks instead
         if (cdiv64(g.R, mp.bn) > kKrpMaxBN || mp.bn > kKrpMaxBN) return false;
         const int ck = mp.tc_img ? kImgCK
-                                 : (int)(((mp.tc_inner ? TC_BRES_INNER_KB : TC_BRES_KB) * 1024) /
+                                 : (int)(((mp.tc_inner ? kBResInnerKB : kBResKB) * 1024) /
                                          (2 * mp.bn * kBK * 4));
         const int64_t njc = cdiv64(mp.tc_ks, ck);
         int64_t best = 1;
@@ -4019,7 +3957,7 @@ struct TtmLayout {
 bool ttm_layout(int64_t P, int64_t N, int64_t Q, int64_t J, TtmLayout& l) {
     const int64_t numel = P * N * Q;
     l.rows = Q == 1 ? P : P * Q;
-    if (J < TC_IMG_MIN_R || J > 65536 || N < 16 || cdiv64(N, kBK4) * kBK4 > 2 * N) return false;
+    if (J < kImgMinR || J > 65536 || N < 16 || cdiv64(N, kBK4) * kBK4 > 2 * N) return false;
     if (numel > ((int64_t)12 << 30) || cdiv64(l.rows, kBM) > 65535 || P >= ((int64_t)1 << 31)) return false;
     if (Q == 1 ? (N % 8 != 0) : (Q % 64 != 0 || Q >= ((int64_t)1 << 31))) return false;
     l.bn = J <= 64 ? 64 : (cdiv64(J, 256) * 256 * 20 <= cdiv64(J, 128) * 128 * 23 ? 256 : 128);
