@@ -582,7 +582,7 @@ int mttkrp_all_modes(mttkrp_plan_t h, const float* Y, const float* const* factor
 // fp32 factor and the fp32 first solution and residual.
 namespace {
 struct CpAlsLayout {
-    size_t grams, v, dinv, x, m, gpart, part, info, vhi, vlo, l32, dinv32, x0, res, total;
+    size_t grams, v, dinv, x, m, gpart, part, npart, info, vhi, vlo, l32, dinv32, dblk, x0, res, total;
 };
 CpAlsLayout cp_als_layout(const Plan& p) {
     int64_t imax = 0;
@@ -609,6 +609,8 @@ CpAlsLayout cp_als_layout(const Plan& p) {
     off = align256(off + (slabs > 1 ? (size_t)slabs * R * R * sizeof(double) : 0));
     l.part = off;
     off = align256(off + cpals_sumsq_scratch_bytes());
+    l.npart = off;
+    off = align256(off + cpals_normalize_scratch_bytes((int)p.R));
     l.info = off;
     off = align256(off + sizeof(int));
     const bool mixed = p.R <= cpals_mixed_max_rank();
@@ -620,6 +622,8 @@ CpAlsLayout cp_als_layout(const Plan& p) {
     off = align256(off + (mixed ? R * R * sizeof(float) : 0));
     l.dinv32 = off;
     off = align256(off + (mixed ? R * sizeof(float) : 0));
+    l.dblk = off;
+    off = align256(off + (mixed ? cpals_mixed_block_bytes((int)p.R) : 0));
     l.x0 = off;
     off = align256(off + (mixed ? (size_t)imax * R * sizeof(float) : 0));
     l.res = off;
@@ -798,7 +802,9 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, 
     p->img_ready = reuse;
     p->sweep_left_images = 0;
     for (int n = 0; n < d; ++n) {
-        if ((e = cpals_hadamard(G, d, n, R, V, s)) != cudaSuccess)
+        float* vhi = mixed ? reinterpret_cast<float*>(base + l.vhi) : nullptr;
+        float* vlo = mixed ? reinterpret_cast<float*>(base + l.vlo) : nullptr;
+        if ((e = cpals_hadamard(G, d, n, R, V, vhi, vlo, s)) != cudaSuccess)
             return fail(MTTKRP_ERR_CUDA, "CP-ALS Hadamard: %s", cudaGetErrorString(e));
         ++p->launches;
         int rc = run_mode(*p, Y, factors, n, M, s);
@@ -806,7 +812,8 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, 
         if (mixed) {
             e = cpals_solve_mixed(V, R, M, p->dims[n], X, reinterpret_cast<float*>(base + l.vhi),
                                   reinterpret_cast<float*>(base + l.vlo), reinterpret_cast<float*>(base + l.l32),
-                                  reinterpret_cast<float*>(base + l.dinv32), reinterpret_cast<float*>(base + l.x0),
+                                  reinterpret_cast<float*>(base + l.dinv32), reinterpret_cast<float*>(base + l.dblk),
+                                  reinterpret_cast<float*>(base + l.x0),
                                   reinterpret_cast<float*>(base + l.res), info, s);
             p->launches += cpals_mixed_launches(R);
         } else {
@@ -814,12 +821,14 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, 
                 e = cpals_solve(V, dinv, R, M, p->dims[n], X, s);
             p->launches += 2 + cpals_cholesky_launches(R);
         }
-        if (e == cudaSuccess && (e = cpals_normalize(X, p->dims[n], R, factors[n], lambda, s)) == cudaSuccess)
+        if (e == cudaSuccess &&
+            (e = cpals_normalize(X, p->dims[n], R, factors[n], lambda, reinterpret_cast<double*>(base + l.npart), s)) ==
+                cudaSuccess)
             e = cpals_gram(factors[n], p->dims[n], R, G + n * RR, gpart, s);
         if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "CP-ALS update of mode %d: %s", n, cudaGetErrorString(e));
-        p->launches += 2 + (cpals_gram_slabs(p->dims[n], R) > 1 ? 1 : 0);
+        p->launches += cpals_normalize_launches() + 1 + (cpals_gram_slabs(p->dims[n], R) > 1 ? 1 : 0);
     }
-    if ((e = cpals_hadamard(G, d, -1, R, V, s)) == cudaSuccess)
+    if ((e = cpals_hadamard(G, d, -1, R, V, nullptr, nullptr, s)) == cudaSuccess)
         e = cpals_fit(V, lambda, M, factors[d - 1], p->dims[d - 1], R, norm_y2, info, fit, part, s);
     if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "CP-ALS fit: %s", cudaGetErrorString(e));
     p->launches += 3;

@@ -83,14 +83,22 @@ __global__ void gram_sum_kernel(const double* __restrict__ part, int S, int R, d
     }
 }
 
-// V = Hadamard product of G[m] over m != skip (skip < 0: all d)
-__global__ void hadamard_kernel(const double* __restrict__ G, int d, int skip, int R, double* __restrict__ V) {
+// V = Hadamard product of G[m] over m != skip (skip < 0: all d); with vhi
+// non-null also V as two fp32 words, vhi = fl32(V) and vlo = fl32(V - vhi),
+// which hold it to about 2^-48 relative
+__global__ void hadamard_kernel(const double* __restrict__ G, int d, int skip, int R, double* __restrict__ V,
+                                float* __restrict__ vhi, float* __restrict__ vlo) {
     const int64_t n = (int64_t)R * R;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
         double v = 1.0;
         for (int m = 0; m < d; ++m)
             if (m != skip) v *= G[m * n + e];
         V[e] = v;
+        if (vhi != nullptr) {
+            const float h = (float)v;
+            vhi[e] = h;
+            vlo[e] = (float)(v - (double)h);
+        }
     }
 }
 
@@ -252,187 +260,387 @@ __global__ void __launch_bounds__(256) solve_kernel(const double* __restrict__ L
 
 constexpr int kChol32MaxR = 1024;
 
-// Small ranks (R <= kSmemMaxR): the factorisation and the solves keep the lower
-// triangle of the fp32 factor packed in shared memory (row i at i (i + 1) / 2).
+// Small ranks (R <= kSmemMaxR) take the single-launch factorisation and the
+// multi-CTA row solves below; larger ranks the blocked multi-launch factor.
 constexpr int kSmemMaxR = 288;
+constexpr int kChB = 32;   // panel width = diagonal block size
 
 __host__ __device__ __forceinline__ int tri(int i) { return i * (i + 1) / 2; }
+__host__ __device__ __forceinline__ int round4(int x) { return (x + 3) & ~3; }
 
-// One CTA factors V (fp32, only the lower triangle read) in shared memory in
-// 32-column panels: warp 0 factors the diagonal block in registers (lane i holds
-// row i), every thread forward-substitutes one row of the panel below it, and the
-// trailing lower triangle is updated in 4 x 4 register blocks from the panel.
-// Writes L (dense row-major: lower triangle and its mirror above) and
-// dinv[j] = 1 / L[j][j]; *info = j + 1 for the first pivot that is not positive.
-constexpr int kCholSmemThreads = 256;   // no register cap: the row arrays stay in registers
-__global__ void __launch_bounds__(kCholSmemThreads, 1) chol_smem_kernel(const float* __restrict__ V, int R,
-                                                            float* __restrict__ L, float* __restrict__ dinv,
-                                                            int* __restrict__ info) {
-    extern __shared__ float sm[];
-    float* a = sm;                         // packed lower triangle, tri(R) floats
-    float* panel = sm + tri(R);            // [R][33]
-    __shared__ float l11[32][33];
-    __shared__ float dv[32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-    for (int i = warp; i < R; i += nw)
-        for (int j = lane; j <= i; j += 32) a[tri(i) + j] = V[(int64_t)i * R + j];
+// The fp32 factor L L^T of vhi = fl32(V) by one CTA, right-looking in 32-column
+// panels with the packed lower triangle in shared memory:
+//   A. warp 0 factors the diagonal block in registers (lane i holds row i; the
+//      pivot's 1 / sqrt from rsqrtf refined by one Newton-Raphson step, no
+//      division) and inverts it (lane c computes column c of the inverse);
+//   B. four threads a row of the panel below (one warp, eight rows): L21 =
+//      A21 L11^{-T} as a product with the inverse (no substitution chain),
+//      kept transposed in shared memory beside the triangle;
+//   C. the trailing lower triangle is updated in 4 x 4 register blocks from
+//      the transposed panel (16-byte loads).
+// Outputs: Lm (R x R: L in the lower triangle, its mirror above), Dm (the
+// inverse of every diagonal block, 32 x 32 row-major, zero above the diagonal
+// and outside the block), dinv[j] = 1 / L[j][j]; *info = j + 1 for the first
+// pivot that is not positive (the factor then holds NaN from there on).
+constexpr int kChol2Threads = 512;   // 128 registers a thread: no spills
+
+size_t chol2_smem_bytes(int R) { return ((size_t)round4(tri(R)) + (size_t)kChB * round4(R)) * sizeof(float); }
+
+__device__ __forceinline__ void cp_async4(float* smem, const float* gmem) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async16(float* smem, const float* gmem) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+__global__ void __launch_bounds__(kChol2Threads, 1)
+    chol2_kernel(const float* __restrict__ vhi, int R, float* __restrict__ Lm, float* __restrict__ Dm,
+                 float* __restrict__ dinv, int* __restrict__ info) {
+    extern __shared__ __align__(16) float sm[];
+    const int Rp = round4(R);
+    float* a = sm;                       // packed lower triangle (row i at tri(i))
+    float* P = sm + round4(tri(R));      // transposed panel [32][Rp]
+    __shared__ __align__(16) float l11[kChB][kChB + 4];    // rows 16-byte aligned
+    __shared__ __align__(16) float linv[kChB][kChB + 4];
+    __shared__ float colb[kChB], dvs[kChB];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = warp; i < R; i += kChol2Threads / 32)
+        for (int j = lane; j <= i; j += 32) cp_async4(a + tri(i) + j, vhi + (int64_t)i * R + j);
+    cp_async_wait_all();
     __syncthreads();
-    for (int k0 = 0; k0 < R; k0 += 32) {
-        const int nb = R - k0 < 32 ? R - k0 : 32;
+    int first_bad = -1;   // warp 0: first pivot that is not positive
+    for (int k0 = 0; k0 < R; k0 += kChB) {
+        const int nb = R - k0 < kChB ? R - k0 : kChB;
+        const int r0 = k0 + nb, rest = R - r0;
         if (warp == 0) {
-            float r[32];
+            // A. the diagonal block
+            float r[kChB];
 #pragma unroll
-            for (int t = 0; t < 32; ++t) r[t] = (lane < nb && t <= lane) ? a[tri(k0 + lane) + k0 + t] : 0.f;
+            for (int t = 0; t < kChB; ++t) r[t] = (lane < nb && t <= lane) ? a[tri(k0 + lane) + k0 + t] : 0.f;
+            float dl = 0.f;   // 1 / L[k0 + lane][k0 + lane]
+            // column j of the block goes through shared memory: lane j posts the
+            // pivot, every lane scales its entry and posts it, every lane updates
+            // its row from the posted column
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < kChB; ++j) {
                 if (j < nb) {
-                    const float piv = __shfl_sync(0xffffffffu, r[j], j);
-                    if (lane == 0 && !(piv > 0.f) && *info == 0) *info = k0 + j + 1;
-                    const float d = sqrtf(piv), inv = 1.f / d;
-                    if (lane == j) r[j] = d;
-                    if (lane > j) r[j] *= inv;
-                    if (lane == 0) dv[j] = inv;
+                    if (lane == j) colb[j] = r[j];
+                    __syncwarp();
+                    const float piv = colb[j];
+                    first_bad = (first_bad < 0 && !(piv > 0.f)) ? k0 + j : first_bad;
+                    float inv = rsqrtf(piv);
+                    inv = inv * fmaf(-0.5f * piv * inv, inv, 1.5f);   // Newton-Raphson step for 1 / sqrt
+                    const float dj = piv * inv;
+                    dl = lane == j ? inv : dl;
+                    r[j] = lane == j ? dj : (lane > j ? r[j] * inv : r[j]);
+                    __syncwarp();
+                    colb[lane] = r[j];   // L[lane][j] (zero above the diagonal)
+                    __syncwarp();
 #pragma unroll
-                    for (int t = j + 1; t < 32; ++t) {
-                        const float ltj = __shfl_sync(0xffffffffu, r[j], t);
-                        if (t < nb && lane >= t) r[t] = fmaf(-r[j], ltj, r[t]);
-                    }
+                    for (int t = j + 1; t < kChB; ++t) r[t] = lane >= t ? fmaf(-r[j], colb[t], r[t]) : r[t];
+                    __syncwarp();
                 }
             }
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                l11[lane][t] = (t <= lane) ? r[t] : 0.f;
+            for (int t = 0; t < kChB; ++t) {
+                l11[lane][t] = t <= lane ? r[t] : 0.f;
                 if (lane < nb && t <= lane) a[tri(k0 + lane) + k0 + t] = r[t];
             }
+            if (lane < nb) dinv[k0 + lane] = dl;
+            dvs[lane] = dl;
             __syncwarp();
-            if (lane < nb) dinv[k0 + lane] = dv[lane];
-        }
-        __syncthreads();
-        const int rest = R - k0 - nb;
-        for (int ii = tid; ii < rest; ii += blockDim.x) {
-            const int i = k0 + nb + ii;
-            float x[32];
+            // inverse of the block, lane c = column c: z[i] = Linv[i][c]
+            float z[kChB];
 #pragma unroll
-            for (int t = 0; t < 32; ++t) x[t] = t < nb ? a[tri(i) + k0 + t] : 0.f;
+            for (int i = 0; i < kChB; ++i) {
+                float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                if (t < nb) {
-                    float v = x[t];
-#pragma unroll
-                    for (int u = 0; u < t; ++u) v = fmaf(-x[u], l11[t][u], v);
-                    x[t] = v * dv[t];
+                for (int k = 0; k + 4 <= i; k += 4) {
+                    const float4 l = *reinterpret_cast<const float4*>(&l11[i][k]);
+                    s0 = fmaf(l.x, z[k], s0);
+                    s1 = fmaf(l.y, z[k + 1], s1);
+                    s0 = fmaf(l.z, z[k + 2], s0);
+                    s1 = fmaf(l.w, z[k + 3], s1);
                 }
-            }
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                if (t < nb) a[tri(i) + k0 + t] = x[t];
-                panel[ii * 33 + t] = x[t];
+                for (int k = i & ~3; k < i; ++k) s0 = fmaf(l11[i][k], z[k], s0);
+                const float di = dvs[i];
+                z[i] = i == lane ? di : (i > lane ? -(s0 + s1) * di : 0.f);
+            }
+            float* dblk = Dm + (int64_t)(k0 / kChB) * kChB * kChB;
+#pragma unroll
+            for (int i = 0; i < kChB; ++i) {
+                linv[i][lane] = z[i];   // z[i] = 0 above the diagonal
+                dblk[i * kChB + lane] = z[i];
+            }
+        }
+        __syncthreads();   // linv ready
+        // B. the panel below the block: item (row ii, tq) forms L21[ii][t] for
+        // t = tq, tq + 4, ..., tq + 28; a row's four items are in one warp, so a
+        // warp barrier orders its reads before its in-place writes
+        const int items = (4 * round4(rest) + 31) & ~31;   // whole warps: the loop is warp-uniform
+        for (int it = tid; it < items; it += kChol2Threads) {
+            const int ii = it >> 2, tq = it & 3;
+            const bool act = ii < rest;
+            float x[kChB];
+            if (act) {
+                const float* arow = a + tri(r0 + ii) + k0;
+#pragma unroll
+                for (int u = 0; u < kChB; ++u) x[u] = u < nb ? arow[u] : 0.f;
+            }
+            __syncwarp();
+            if (act) {
+                float* arow = a + tri(r0 + ii) + k0;
+#pragma unroll
+                for (int c = 0; c < kChB / 4; ++c) {
+                    const int t = tq + 4 * c;
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int u = 0; u < kChB; u += 4) {
+                        if (u <= 4 * c + 3) {   // linv[t][u..u+3] is zero beyond t
+                            const float4 l = *reinterpret_cast<const float4*>(&linv[t][u]);
+                            s0 = fmaf(x[u], l.x, s0);
+                            s1 = fmaf(x[u + 1], l.y, s1);
+                            s0 = fmaf(x[u + 2], l.z, s0);
+                            s1 = fmaf(x[u + 3], l.w, s1);
+                        }
+                    }
+                    const float v = s0 + s1;
+                    P[t * Rp + ii] = v;
+                    if (t < nb) arow[t] = v;
+                }
+            } else if (ii < round4(rest)) {
+#pragma unroll
+                for (int c = 0; c < kChB / 4; ++c) P[(tq + 4 * c) * Rp + ii] = 0.f;
             }
         }
         __syncthreads();
+        // C. trailing update: a[r0 + i][r0 + k] -= sum_t L21[i][t] L21[k][t], k <= i
         const int nblk = (rest + 3) / 4;
         const int pairs = nblk * (nblk + 1) / 2;
         for (int pq = tid; pq < pairs; pq += blockDim.x) {
             int bi = (int)((sqrtf(8.f * (float)pq + 1.f) - 1.f) * 0.5f);
-            while (bi * (bi + 1) / 2 > pq) --bi;
-            while ((bi + 1) * (bi + 2) / 2 <= pq) ++bi;
-            const int bk = pq - bi * (bi + 1) / 2;
+            while (tri(bi) > pq) --bi;
+            while (tri(bi + 1) <= pq) ++bi;
+            const int bk = pq - tri(bi);
             float acc[4][4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
 #pragma unroll
                 for (int v = 0; v < 4; ++v) acc[u][v] = 0.f;
             for (int t = 0; t < nb; ++t) {
-                float pi[4], pk[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int ri = 4 * bi + u, rk = 4 * bk + u;
-                    pi[u] = ri < rest ? panel[ri * 33 + t] : 0.f;
-                    pk[u] = rk < rest ? panel[rk * 33 + t] : 0.f;
-                }
+                const float4 pi = *reinterpret_cast<const float4*>(P + t * Rp + 4 * bi);
+                const float4 pk = *reinterpret_cast<const float4*>(P + t * Rp + 4 * bk);
+                const float vi[4] = {pi.x, pi.y, pi.z, pi.w}, vk[4] = {pk.x, pk.y, pk.z, pk.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(pi[u], pk[v], acc[u][v]);
+                    for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(vi[u], vk[v], acc[u][v]);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u)
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     const int ri = 4 * bi + u, rk = 4 * bk + v;
-                    if (ri < rest && rk <= ri) a[tri(k0 + nb + ri) + k0 + nb + rk] -= acc[u][v];
+                    if (ri < rest && rk <= ri) a[tri(r0 + ri) + r0 + rk] -= acc[u][v];
                 }
         }
         __syncthreads();
     }
-    for (int i = warp; i < R; i += nw)
-        for (int j = lane; j < R; j += 32) L[(int64_t)i * R + j] = j <= i ? a[tri(i) + j] : a[tri(j) + i];
+    if (warp == 0 && lane == 0 && first_bad >= 0 && *info == 0) *info = first_bad + 1;
+    for (int i = warp; i < R; i += kChol2Threads / 32)
+        for (int j = lane; j < R; j += 32) Lm[(int64_t)i * R + j] = j <= i ? a[tri(i) + j] : a[tri(j) + i];
 }
 
-// Y(i, :) = B(i, :) (L L^T)^{-1} in fp32, one warp per row, 32 rows a CTA, the
-// packed lower triangle of L staged in shared memory (L dense, lower part read).
-// Blocks of 32 unknowns as in solve_kernel.  out32 / (add, out64) as in
-// solve32_kernel.
-__global__ void __launch_bounds__(1024, 1) solve_smem_kernel(const float* __restrict__ L,
-                                                             const float* __restrict__ dinv, int R,
-                                                             const float* __restrict__ B, int64_t I,
-                                                             float* __restrict__ out32,
-                                                             const float* __restrict__ add,
-                                                             double* __restrict__ out64) {
-    extern __shared__ float sm[];
-    float* lp = sm;                        // packed lower triangle
-    float* ds = sm + tri(R);               // the pivots' reciprocals (R)
-    float* xs = ds + R;                    // [32 warps][R]
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-    for (int i = warp; i < R; i += nw)
-        for (int j = lane; j <= i; j += 32) lp[tri(i) + j] = L[(int64_t)i * R + j];
-    for (int j = tid; j < R; j += blockDim.x) ds[j] = dinv[j];
-    const int64_t row = (int64_t)blockIdx.x * nw + warp;
-    float* x = xs + (int64_t)warp * R;
-    if (row < I)
-        for (int k = lane; k < R; k += 32) x[k] = B[row * R + k];
+// X(i, :) = B(i, :) (L L^T)^{-1} in fp32 for R <= kSmemMaxR: y L^T = b, then
+// x L = y, row by row in blocks of 32 unknowns (lane l owns unknown k0 + l).
+// The finished blocks enter as dot products with columns of the factor, the
+// block itself as the product with the inverse of its diagonal block, so no
+// step waits on a substitution chain.  Each CTA stages the parts of the
+// mirrored factor Lm that a pass reads (the strip above every diagonal block
+// for the forward pass, below it for the backward pass) and Dm (rows padded to
+// 33 floats: read along rows and along columns without bank conflicts) in
+// shared memory with asynchronous copies; kSv2Warps warps of kSv2Rows rows
+// each.
+// out32 (if non-null) receives the result; out64 (if non-null) add + result in
+// fp64.
+constexpr int kSv2Warps = 4, kSv2Rows = 1;
+
+__host__ __device__ __forceinline__ int64_t sv2_strip_floats(int R) {
+    const int nb = (R + kChB - 1) / kChB;
+    int64_t f = 0, b = 0;
+    for (int kb = 0; kb < nb; ++kb) {
+        f += (int64_t)kChB * kb * kChB;
+        const int rows = R - kChB * (kb + 1);
+        b += rows > 0 ? (int64_t)rows * kChB : 0;
+    }
+    return f > b ? f : b;
+}
+size_t sv2_smem_bytes(int R) {
+    const int nb = (R + kChB - 1) / kChB;
+    return ((size_t)sv2_strip_floats(R) + (size_t)nb * kChB * (kChB + 1) + (size_t)kSv2Warps * kSv2Rows * nb * kChB) *
+           sizeof(float);
+}
+
+template <bool VEC>   // VEC: R % 4 == 0 and Lm 16-byte aligned (16-byte copies)
+__global__ void __launch_bounds__(kSv2Warps * 32)
+    solve2_kernel(const float* __restrict__ Lm, const float* __restrict__ Dm, int R, const float* __restrict__ B,
+                  int64_t I, float* __restrict__ out32, const float* __restrict__ add, double* __restrict__ out64) {
+    extern __shared__ __align__(16) float sm[];
+    constexpr int NR = kSv2Rows;
+    const int nblk = (R + kChB - 1) / kChB, Rb = nblk * kChB;
+    float* strip = sm;
+    float* dsm = sm + sv2_strip_floats(R);                 // [nblk][32][33]
+    float* ys = dsm + (int64_t)nblk * kChB * (kChB + 1);    // [warps][NR][Rb]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float* y = ys + (int64_t)warp * NR * Rb;
+    const int64_t row0 = ((int64_t)blockIdx.x * kSv2Warps + warp) * NR;
+
+    // stage rows [j0, j1) of columns [k0, k0 + 32) of Lm at dst (32 floats a
+    // row; columns at or beyond R read as 0)
+    auto stage = [&](float* dst, int j0, int j1, int k0) {
+        const int n = (j1 - j0) * (VEC ? kChB / 4 : kChB);
+        for (int e = tid; e < n; e += blockDim.x) {
+            if (VEC) {
+                const int j = j0 + e / (kChB / 4), c = 4 * (e % (kChB / 4));
+                float* d = dst + (int64_t)(j - j0) * kChB + c;
+                if (k0 + c < R)
+                    cp_async16(d, Lm + (int64_t)j * R + k0 + c);
+                else
+                    *reinterpret_cast<float4*>(d) = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+                const int j = j0 + e / kChB, c = e % kChB;
+                float* d = dst + (int64_t)(j - j0) * kChB + c;
+                if (k0 + c < R)
+                    cp_async4(d, Lm + (int64_t)j * R + k0 + c);
+                else
+                    *d = 0.f;
+            }
+        }
+    };
+    // forward strips: block kb at 1024 * kb (kb - 1) / 2 floats, rows j < 32 kb
+    for (int kb = 1; kb < nblk; ++kb) stage(strip + (int64_t)kChB * kChB * kb * (kb - 1) / 2, 0, kChB * kb, kChB * kb);
+    for (int e = tid; e < nblk * kChB * kChB; e += blockDim.x) cp_async4(dsm + e + e / kChB, Dm + e);
+    for (int u = 0; u < NR; ++u)
+        for (int k = lane; k < Rb; k += 32) y[u * Rb + k] = (row0 + u < I && k < R) ? B[(row0 + u) * R + k] : 0.f;
+    cp_async_wait_all();
     __syncthreads();
-    if (row >= I) return;
-    for (int k0 = 0; k0 < R; k0 += 32) {
-        const int k = k0 + lane;
-        const bool live = k < R;
-        float acc = live ? x[k] : 0.f;
-        if (live) {
-            const float* lk = lp + tri(k);
-            for (int j = 0; j < k0; ++j) acc = fmaf(-lk[j], x[j], acc);
+
+    // y L^T = b
+    for (int kb = 0; kb < nblk; ++kb) {
+        const int k0 = kb * kChB, k = k0 + lane;
+        const float* s = strip + (int64_t)kChB * kChB * kb * (kb - 1) / 2 + lane;   // s[j * 32] = L[k][j]
+        float acc[NR], acc2[NR];
+#pragma unroll
+        for (int u = 0; u < NR; ++u) {
+            acc[u] = y[u * Rb + k];
+            acc2[u] = 0.f;
         }
-        const int nb = R - k0 < 32 ? R - k0 : 32;
-        for (int t = 0; t < nb; ++t) {
-            const float yt = __shfl_sync(0xffffffffu, acc, t) * ds[k0 + t];
-            if (lane == t)
-                acc = yt;
-            else if (lane > t && live)
-                acc = fmaf(-lp[tri(k) + k0 + t], yt, acc);
+#pragma unroll 4
+        for (int j = 0; j < k0; j += 4) {
+            const float l0 = s[(j + 0) * kChB], l1 = s[(j + 1) * kChB], l2 = s[(j + 2) * kChB],
+                        l3 = s[(j + 3) * kChB];
+#pragma unroll
+            for (int u = 0; u < NR; ++u) {
+                const float4 yv = *reinterpret_cast<const float4*>(y + u * Rb + j);
+                acc[u] = fmaf(-l0, yv.x, acc[u]);
+                acc2[u] = fmaf(-l1, yv.y, acc2[u]);
+                acc[u] = fmaf(-l2, yv.z, acc[u]);
+                acc2[u] = fmaf(-l3, yv.w, acc2[u]);
+            }
         }
-        if (live) x[k] = acc;
+#pragma unroll
+        for (int u = 0; u < NR; ++u) acc[u] += acc2[u];
+        const float* drow = dsm + kb * kChB * (kChB + 1) + lane * (kChB + 1);   // drow[t] = Linv[lane][t]
+        float out[NR];
+#pragma unroll
+        for (int u = 0; u < NR; ++u) out[u] = 0.f;
+#pragma unroll
+        for (int t = 0; t < kChB; ++t) {
+            const float dv = drow[t];   // zero for t > lane
+#pragma unroll
+            for (int u = 0; u < NR; ++u) out[u] = fmaf(dv, __shfl_sync(0xffffffffu, acc[u], t), out[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < NR; ++u) y[u * Rb + k] = out[u];   // 0 beyond R: Dm is zero there
         __syncwarp();
     }
-    for (int k0 = ((R - 1) / 32) * 32; k0 >= 0; k0 -= 32) {
-        const int k = k0 + lane;
-        const bool live = k < R;
-        float acc = live ? x[k] : 0.f;
-        if (live)
-            for (int j = k0 + 32; j < R; ++j) acc = fmaf(-lp[tri(j) + k], x[j], acc);
-        const int nb = R - k0 < 32 ? R - k0 : 32;
-        for (int t = nb - 1; t >= 0; --t) {
-            const float xt = __shfl_sync(0xffffffffu, acc, t) * ds[k0 + t];
-            if (lane == t)
-                acc = xt;
-            else if (lane < t && live)
-                acc = fmaf(-lp[tri(k0 + t) + k], xt, acc);
+    __syncthreads();   // every warp done with the forward strips
+    // backward strips: block kb holds rows j >= 32 (kb + 1)
+    {
+        int64_t off = 0;
+        for (int kb = 0; kb < nblk; ++kb) {
+            const int j0 = kChB * (kb + 1);
+            if (j0 < R) {
+                stage(strip + off, j0, R, kChB * kb);
+                off += (int64_t)(R - j0) * kChB;
+            }
         }
-        if (live) x[k] = acc;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    // x L = y
+    int64_t off_end = 0;
+    for (int kb = 0; kb < nblk; ++kb) {
+        const int j0 = kChB * (kb + 1);
+        if (j0 < R) off_end += (int64_t)(R - j0) * kChB;
+    }
+    for (int kb = nblk - 1; kb >= 0; --kb) {
+        const int k0 = kb * kChB, k = k0 + lane, j0 = k0 + kChB;
+        const int rows = j0 < R ? R - j0 : 0;
+        off_end -= (int64_t)rows * kChB;
+        const float* s = strip + off_end + lane;   // s[(j - j0) * 32] = L[j][k]
+        float acc[NR], acc2[NR];
+#pragma unroll
+        for (int u = 0; u < NR; ++u) {
+            acc[u] = y[u * Rb + k];
+            acc2[u] = 0.f;
+        }
+        int j = 0;
+#pragma unroll 4
+        for (; j + 4 <= rows; j += 4) {
+            const float l0 = s[(j + 0) * kChB], l1 = s[(j + 1) * kChB], l2 = s[(j + 2) * kChB],
+                        l3 = s[(j + 3) * kChB];
+#pragma unroll
+            for (int u = 0; u < NR; ++u) {
+                const float4 yv = *reinterpret_cast<const float4*>(y + u * Rb + j0 + j);
+                acc[u] = fmaf(-l0, yv.x, acc[u]);
+                acc2[u] = fmaf(-l1, yv.y, acc2[u]);
+                acc[u] = fmaf(-l2, yv.z, acc[u]);
+                acc2[u] = fmaf(-l3, yv.w, acc2[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NR; ++u) acc[u] += acc2[u];
+        for (; j < rows; ++j) {
+            const float l = s[j * kChB];
+#pragma unroll
+            for (int u = 0; u < NR; ++u) acc[u] = fmaf(-l, y[u * Rb + j0 + j], acc[u]);
+        }
+        const float* dcol = dsm + kb * kChB * (kChB + 1) + lane;   // dcol[t * 33] = Linv[t][lane]
+        float out[NR];
+#pragma unroll
+        for (int u = 0; u < NR; ++u) out[u] = 0.f;
+#pragma unroll
+        for (int t = 0; t < kChB; ++t) {
+            const float dv = dcol[t * (kChB + 1)];   // zero for t < lane
+#pragma unroll
+            for (int u = 0; u < NR; ++u) out[u] = fmaf(dv, __shfl_sync(0xffffffffu, acc[u], t), out[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < NR; ++u) y[u * Rb + k] = out[u];
         __syncwarp();
     }
-    for (int k = lane; k < R; k += 32) {
-        const int64_t e = row * R + k;
-        if (out32 != nullptr) out32[e] = x[k];
-        if (out64 != nullptr) out64[e] = (double)add[e] + (double)x[k];
+    for (int u = 0; u < NR; ++u) {
+        if (row0 + u >= I) break;
+        for (int k = lane; k < R; k += 32) {
+            const int64_t e = (row0 + u) * R + k;
+            if (out32 != nullptr) out32[e] = y[u * Rb + k];
+            if (out64 != nullptr) out64[e] = (double)add[e] + (double)y[u * Rb + k];
+        }
     }
 }
 
@@ -579,88 +787,163 @@ __global__ void split_v_kernel(const double* __restrict__ V, int64_t n, float* _
 
 // Res = M - X V (I x R) with V = vhi + vlo: each product x vhi split exactly
 // (fma), summed with compensation; x vlo and the product errors summed plainly.
-// kResRows rows and kResCols columns a block (one column a thread).
-constexpr int kResRows = 2, kResCols = 128;
-__global__ void __launch_bounds__(kResCols) residual_kernel(const float* __restrict__ M, const float* __restrict__ X,
-                                                       const float* __restrict__ vhi_m, const float* __restrict__ vlo_m,
-                                                       int64_t I, int R, float* __restrict__ Res) {
-    extern __shared__ float xr[];   // [kResRows][R]
-    const int64_t i0 = (int64_t)blockIdx.y * kResRows;
-    for (int t = threadIdx.x; t < kResRows * R; t += blockDim.x) {
-        const int u = t / R;
-        xr[t] = i0 + u < I ? X[(i0 + u) * R + (t - u * R)] : 0.f;
-    }
-    __syncthreads();
-    {
-        const int j = blockIdx.x * kResCols + threadIdx.x;
-        if (j >= R) return;
-        float s[kResRows], c[kResRows], sm[kResRows];
-#pragma unroll
-        for (int u = 0; u < kResRows; ++u) s[u] = c[u] = sm[u] = 0.f;
-        int k = 0;
-        for (; k + 8 <= R; k += 8) {   // eight rows of V in flight
-            float vh[8], vl[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                vh[q] = vhi_m[(int64_t)(k + q) * R + j];
-                vl[q] = vlo_m[(int64_t)(k + q) * R + j];
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-#pragma unroll
-                for (int u = 0; u < kResRows; ++u) {
-                    const float x = xr[u * R + k + q];
-                    const float p = x * vh[q];
-                    sm[u] += fmaf(x, vh[q], -p) + x * vl[q];
-                    neumaier(s[u], c[u], p);
+// A CTA takes a tile of kRes2Rows rows x kRes2Cols columns: the rows of X staged
+// in shared memory once, V's column block streamed through shared memory in
+// chunks of kResKC rows with asynchronous copies (double-buffered); a thread
+// takes one row and four adjacent columns.
+constexpr int kRes2Rows = 8, kRes2Cols = 64, kResKC = 32;
+
+size_t res2_smem_bytes(int R) {
+    return ((size_t)kRes2Rows * (R + 1) + (size_t)2 * 2 * kResKC * kRes2Cols) * sizeof(float);
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+
+template <bool VEC>   // VEC: R % 4 == 0 and vhi, vlo 16-byte aligned
+__global__ void __launch_bounds__(kRes2Rows * kRes2Cols / 4)
+    residual2_kernel(const float* __restrict__ M, const float* __restrict__ X, const float* __restrict__ vhi_m,
+                     const float* __restrict__ vlo_m, int64_t I, int R, float* __restrict__ Res) {
+    extern __shared__ __align__(16) float rs[];
+    float* vb = rs;                                          // [2 buffers][hi|lo][kResKC][kRes2Cols]
+    float* xr = rs + 2 * 2 * kResKC * kRes2Cols;             // [kRes2Rows][R + 1]
+    constexpr int kThreads = kRes2Rows * kRes2Cols / 4;
+    const int stride = R + 1;
+    const int tid = threadIdx.x;
+    const int64_t i0 = (int64_t)blockIdx.y * kRes2Rows;
+    const int jb = blockIdx.x * kRes2Cols;
+    // chunk c of V's column block into buffer b (columns at or beyond R, rows at
+    // or beyond R read as 0)
+    auto stage = [&](int c, int b) {
+        float* dh = vb + (size_t)b * 2 * kResKC * kRes2Cols;
+        float* dl = dh + kResKC * kRes2Cols;
+        const int k0 = c * kResKC;
+        if (VEC) {
+            for (int e = tid; e < kResKC * kRes2Cols / 4; e += kThreads) {
+                const int kk = e / (kRes2Cols / 4), cc = 4 * (e % (kRes2Cols / 4));
+                const int k = k0 + kk, j = jb + cc;
+                float* h = dh + kk * kRes2Cols + cc;
+                float* l = dl + kk * kRes2Cols + cc;
+                if (k < R && j < R) {
+                    cp_async16(h, vhi_m + (int64_t)k * R + j);
+                    cp_async16(l, vlo_m + (int64_t)k * R + j);
+                } else {
+                    *reinterpret_cast<float4*>(h) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    *reinterpret_cast<float4*>(l) = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-        }
-        for (; k < R; ++k) {
-            const float vhi = vhi_m[(int64_t)k * R + j], vlo = vlo_m[(int64_t)k * R + j];
-#pragma unroll
-            for (int u = 0; u < kResRows; ++u) {
-                const float x = xr[u * R + k];
-                const float p = x * vhi;
-                sm[u] += fmaf(x, vhi, -p) + x * vlo;
-                neumaier(s[u], c[u], p);
+            }
+        } else {
+            for (int e = tid; e < kResKC * kRes2Cols; e += kThreads) {
+                const int kk = e / kRes2Cols, cc = e % kRes2Cols;
+                const int k = k0 + kk, j = jb + cc;
+                if (k < R && j < R) {
+                    cp_async4(dh + e, vhi_m + (int64_t)k * R + j);
+                    cp_async4(dl + e, vlo_m + (int64_t)k * R + j);
+                } else {
+                    dh[e] = 0.f;
+                    dl[e] = 0.f;
+                }
             }
         }
+        cp_async_commit();
+    };
+    const int nch = (R + kResKC - 1) / kResKC;
+    stage(0, 0);
+    for (int t = tid; t < kRes2Rows * R; t += kThreads) {
+        const int u = t / R, k = t - u * R;
+        xr[u * stride + k] = i0 + u < I ? X[(i0 + u) * R + k] : 0.f;
+    }
+    const int r = tid / (kRes2Cols / 4), cq = 4 * (tid % (kRes2Cols / 4));
+    const float* xrow = xr + r * stride;
+    float s[4], c[4], sm[4];
 #pragma unroll
-        for (int u = 0; u < kResRows; ++u)
-            if (i0 + u < I) {
-                const int64_t e = (i0 + u) * R + j;
-                Res[e] = (M[e] - s[u]) - (c[u] + sm[u]);
+    for (int q = 0; q < 4; ++q) s[q] = c[q] = sm[q] = 0.f;
+    for (int ch = 0; ch < nch; ++ch) {
+        if (ch + 1 < nch)
+            stage(ch + 1, (ch + 1) & 1);
+        else
+            cp_async_commit();   // an empty group keeps the wait count uniform
+        cp_async_wait_prev();
+        __syncthreads();
+        const float* hh = vb + (size_t)(ch & 1) * 2 * kResKC * kRes2Cols + cq;
+        const float* ll = hh + kResKC * kRes2Cols;
+        const int k0 = ch * kResKC;
+#pragma unroll 8
+        for (int kk = 0; kk < kResKC; ++kk) {
+            const float x = k0 + kk < R ? xrow[k0 + kk] : 0.f;
+            const float4 h4 = *reinterpret_cast<const float4*>(hh + kk * kRes2Cols);
+            const float4 l4 = *reinterpret_cast<const float4*>(ll + kk * kRes2Cols);
+            const float vh[4] = {h4.x, h4.y, h4.z, h4.w}, vl[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float p = x * vh[q];
+                sm[q] += fmaf(x, vh[q], -p);
+                sm[q] = fmaf(x, vl[q], sm[q]);
+                neumaier(s[q], c[q], p);
             }
+        }
+        __syncthreads();   // the buffer is refilled two chunks later
+    }
+    if (i0 + r < I) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = jb + cq + q;
+            if (j < R) {
+                const int64_t e = (i0 + r) * R + j;
+                Res[e] = (M[e] - s[q]) - (c[q] + sm[q]);
+            }
+        }
     }
 }
 
 // lambda_r = ||X(:, r)||_2 and A(:, r) = X(:, r) / lambda_r (0 for a zero
-// column); one block per 32 columns, rows split over 32 warps in a fixed order.
-__global__ void __launch_bounds__(1024) normalize_kernel(const double* __restrict__ X, int64_t I, int R,
-                                                         float* __restrict__ A, float* __restrict__ lam) {
-    __shared__ double part[32][32];
-    __shared__ double norm[32];
+// column), in fp64.  colsq_partial_kernel: block (cb, s) sums the squares of
+// rows [I s / S, I (s + 1) / S) of 32 columns (eight warps, then the warps in
+// order); normalize_apply_kernel: block (cb, rc) forms the 32 norms from the S
+// partials (in s order) once and scales its rows.
+constexpr int kNormSplits = 16, kNormRowsPerBlock = 64;
+
+__global__ void __launch_bounds__(256) colsq_partial_kernel(const double* __restrict__ X, int64_t I, int R,
+                                                            double* __restrict__ part) {
+    __shared__ double ws[8][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = blockIdx.x * 32 + lane;
-    double s = 0.0;
+    const int64_t i0 = I * blockIdx.y / kNormSplits, i1 = I * (blockIdx.y + 1) / kNormSplits;
+    double t = 0.0;
     if (r < R)
-        for (int64_t i = warp; i < I; i += 32) {
+        for (int64_t i = i0 + warp; i < i1; i += 8) {
             const double v = X[i * R + r];
-            s = fma(v, v, s);
+            t = fma(v, v, t);
         }
-    part[warp][lane] = s;
+    ws[warp][lane] = t;
     __syncthreads();
+    if (warp == 0 && r < R) {
+        double u = 0.0;
+        for (int w = 0; w < 8; ++w) u += ws[w][lane];
+        part[(int64_t)blockIdx.y * R + r] = u;
+    }
+}
+
+__global__ void __launch_bounds__(256) normalize_apply_kernel(const double* __restrict__ X, int64_t I, int R,
+                                                              const double* __restrict__ part,
+                                                              float* __restrict__ A, float* __restrict__ lam) {
+    __shared__ double inv[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = blockIdx.x * 32 + lane;
     if (warp == 0) {
-        double t = 0.0;
-        for (int w = 0; w < 32; ++w) t += part[w][lane];
-        norm[lane] = sqrt(t);
-        if (r < R) lam[r] = (float)norm[lane];
+        double n2 = 0.0;
+        if (r < R)
+            for (int sp = 0; sp < kNormSplits; ++sp) n2 += part[(int64_t)sp * R + r];
+        const double nr = sqrt(n2);
+        inv[lane] = nr > 0.0 ? 1.0 / nr : 0.0;
+        if (r < R && blockIdx.y == 0) lam[r] = (float)nr;
     }
     __syncthreads();
-    const double nr = norm[lane];
-    const double inv = nr > 0.0 ? 1.0 / nr : 0.0;
-    if (r < R)
-        for (int64_t i = warp; i < I; i += 32) A[i * R + r] = (float)(X[i * R + r] * inv);
+    if (r >= R) return;
+    const double v = inv[lane];
+    const int64_t i0 = (int64_t)blockIdx.y * kNormRowsPerBlock;
+    const int64_t i1 = i0 + kNormRowsPerBlock < I ? i0 + kNormRowsPerBlock : I;
+    for (int64_t i = i0 + warp; i < i1; i += 8) A[i * R + r] = (float)(X[i * R + r] * v);
 }
 
 __device__ double block_sum(double v, double* sh) {
@@ -767,11 +1050,12 @@ cudaError_t cpals_gram(const float* A, int64_t I, int R, double* G, double* part
     return cudaGetLastError();
 }
 
-cudaError_t cpals_hadamard(const double* G, int d, int skip, int R, double* V, cudaStream_t s) {
+cudaError_t cpals_hadamard(const double* G, int d, int skip, int R, double* V, float* vhi, float* vlo,
+                           cudaStream_t s) {
     const int64_t n = (int64_t)R * R;
     int64_t blocks = (n + 255) / 256;
     if (blocks > 152 * 8) blocks = 152 * 8;
-    hadamard_kernel<<<(unsigned)blocks, 256, 0, s>>>(G, d, skip, R, V);
+    hadamard_kernel<<<(unsigned)blocks, 256, 0, s>>>(G, d, skip, R, V, vhi, vlo);
     return cudaGetLastError();
 }
 
@@ -825,35 +1109,64 @@ cudaError_t cpals_solve(double* L, const double* dinv, int R, const float* M, in
 
 int cpals_mixed_max_rank() { return kChol32MaxR; }
 
-int cpals_mixed_launches(int R) { return R <= kSmemMaxR ? 5 : 5 + cpals_cholesky_launches(R); }
+int cpals_mixed_launches(int R) { return R <= kSmemMaxR ? 4 : 5 + cpals_cholesky_launches(R); }
+
+size_t cpals_mixed_block_bytes(int R) { return (size_t)((R + kChB - 1) / kChB) * kChB * kChB * sizeof(float); }
+
+namespace {
+cudaError_t launch_residual(const float* M, const float* x0, const float* vhi, const float* vlo, int64_t I, int R,
+                            float* res, cudaStream_t s) {
+    const size_t rsm = res2_smem_bytes(R);
+    const dim3 grid((unsigned)((R + kRes2Cols - 1) / kRes2Cols), (unsigned)((I + kRes2Rows - 1) / kRes2Rows));
+    constexpr int threads = kRes2Rows * kRes2Cols / 4;
+    cudaError_t e;
+    if (R % 4 == 0 && ((reinterpret_cast<uintptr_t>(vhi) | reinterpret_cast<uintptr_t>(vlo)) & 15) == 0) {
+        e = cudaFuncSetAttribute(residual2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm);
+        if (e != cudaSuccess) return e;
+        residual2_kernel<true><<<grid, threads, rsm, s>>>(M, x0, vhi, vlo, I, R, res);
+    } else {
+        e = cudaFuncSetAttribute(residual2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm);
+        if (e != cudaSuccess) return e;
+        residual2_kernel<false><<<grid, threads, rsm, s>>>(M, x0, vhi, vlo, I, R, res);
+    }
+    return cudaGetLastError();
+}
+}  // namespace
 
 cudaError_t cpals_solve_mixed(const double* V, int R, const float* M, int64_t I, double* X, float* vhi, float* vlo,
-                              float* L, float* dinv, float* x0, float* res, int* info, cudaStream_t s) {
+                              float* L, float* dinv, float* dblk, float* x0, float* res, int* info, cudaStream_t s) {
     if (R > kChol32MaxR) return cudaErrorInvalidValue;
+    cudaError_t e;
+    if (R <= kSmemMaxR) {
+        // one launch for the split and the factor, the row solves with the
+        // inverted diagonal blocks
+        const size_t csm = chol2_smem_bytes(R);
+        e = cudaFuncSetAttribute(chol2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
+        if (e != cudaSuccess) return e;
+        chol2_kernel<<<1, kChol2Threads, csm, s>>>(vhi, R, L, dblk, dinv, info);
+        const size_t ssm = sv2_smem_bytes(R);
+        const unsigned sb = (unsigned)((I + kSv2Warps * kSv2Rows - 1) / (kSv2Warps * kSv2Rows));
+        const bool vec = R % 4 == 0 && (reinterpret_cast<uintptr_t>(L) & 15) == 0;
+        if (vec) {
+            e = cudaFuncSetAttribute(solve2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
+            if (e != cudaSuccess) return e;
+            solve2_kernel<true><<<sb, kSv2Warps * 32, ssm, s>>>(L, dblk, R, M, I, x0, nullptr, nullptr);
+        } else {
+            e = cudaFuncSetAttribute(solve2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
+            if (e != cudaSuccess) return e;
+            solve2_kernel<false><<<sb, kSv2Warps * 32, ssm, s>>>(L, dblk, R, M, I, x0, nullptr, nullptr);
+        }
+        if ((e = launch_residual(M, x0, vhi, vlo, I, R, res, s)) != cudaSuccess) return e;
+        if (vec)
+            solve2_kernel<true><<<sb, kSv2Warps * 32, ssm, s>>>(L, dblk, R, res, I, nullptr, x0, X);
+        else
+            solve2_kernel<false><<<sb, kSv2Warps * 32, ssm, s>>>(L, dblk, R, res, I, nullptr, x0, X);
+        return cudaGetLastError();
+    }
     const int64_t n = (int64_t)R * R;
     int64_t blocks = (n + 255) / 256;
     if (blocks > 152 * 8) blocks = 152 * 8;
     split_v_kernel<<<(unsigned)blocks, 256, 0, s>>>(V, n, vhi, vlo, L);
-    cudaError_t e;
-    if (R <= kSmemMaxR) {
-        // the factor and the solves with the triangle in shared memory
-        const size_t csm = ((size_t)tri(R) + (size_t)R * 33) * sizeof(float);
-        e = cudaFuncSetAttribute(chol_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
-        if (e != cudaSuccess) return e;
-        chol_smem_kernel<<<1, kCholSmemThreads, csm, s>>>(vhi, R, L, dinv, info);
-        const size_t ssm = ((size_t)tri(R) + (size_t)33 * R) * sizeof(float);
-        e = cudaFuncSetAttribute(solve_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
-        if (e != cudaSuccess) return e;
-        const unsigned sb = (unsigned)((I + 31) / 32);
-        solve_smem_kernel<<<sb, 1024, ssm, s>>>(L, dinv, R, M, I, x0, nullptr, nullptr);
-        const size_t rsm = (size_t)kResRows * R * sizeof(float);
-        e = cudaFuncSetAttribute(residual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm);
-        if (e != cudaSuccess) return e;
-        residual_kernel<<<dim3((unsigned)((R + kResCols - 1) / kResCols), (unsigned)((I + kResRows - 1) / kResRows)),
-                          kResCols, rsm, s>>>(M, x0, vhi, vlo, I, R, res);
-        solve_smem_kernel<<<sb, 1024, ssm, s>>>(L, dinv, R, res, I, nullptr, x0, X);
-        return cudaGetLastError();
-    }
     e = blocked_cholesky<float>(L, R, info, dinv, s);
     if (e != cudaSuccess) return e;
     mirror_lower_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(L, R);
@@ -862,17 +1175,20 @@ cudaError_t cpals_solve_mixed(const double* V, int R, const float* M, int64_t I,
     if (e != cudaSuccess) return e;
     const unsigned sblocks = (unsigned)((I + kSolveRows - 1) / kSolveRows);
     solve32_kernel<<<sblocks, 32, ssm, s>>>(L, dinv, R, M, I, x0, nullptr, nullptr);
-    const size_t rsm = (size_t)kResRows * R * sizeof(float);
-    e = cudaFuncSetAttribute(residual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm);
-    if (e != cudaSuccess) return e;
-    residual_kernel<<<dim3((unsigned)((R + kResCols - 1) / kResCols), (unsigned)((I + kResRows - 1) / kResRows)),
-                      kResCols, rsm, s>>>(M, x0, vhi, vlo, I, R, res);
+    if ((e = launch_residual(M, x0, vhi, vlo, I, R, res, s)) != cudaSuccess) return e;
     solve32_kernel<<<sblocks, 32, ssm, s>>>(L, dinv, R, res, I, nullptr, x0, X);
     return cudaGetLastError();
 }
 
-cudaError_t cpals_normalize(const double* X, int64_t I, int R, float* A, float* lam, cudaStream_t s) {
-    normalize_kernel<<<(unsigned)((R + 31) / 32), 1024, 0, s>>>(X, I, R, A, lam);
+size_t cpals_normalize_scratch_bytes(int R) { return (size_t)kNormSplits * R * sizeof(double); }
+
+int cpals_normalize_launches() { return 2; }
+
+cudaError_t cpals_normalize(const double* X, int64_t I, int R, float* A, float* lam, double* part, cudaStream_t s) {
+    const unsigned cb = (unsigned)((R + 31) / 32);
+    colsq_partial_kernel<<<dim3(cb, kNormSplits), 256, 0, s>>>(X, I, R, part);
+    const int64_t rb = (I + kNormRowsPerBlock - 1) / kNormRowsPerBlock;
+    normalize_apply_kernel<<<dim3(cb, (unsigned)(rb > 0 ? rb : 1)), 256, 0, s>>>(X, I, R, part, A, lam);
     return cudaGetLastError();
 }
 

@@ -165,24 +165,33 @@ cudaError_t launch_ttm(const float* X, const float* M, float* T, int64_t P, int6
 // CP-ALS pieces (cpals.cu)
 int cpals_gram_slabs(int64_t I, int R);   // partial Grams cpals_gram keeps (R x R fp64 each)
 cudaError_t cpals_gram(const float* A, int64_t I, int R, double* G, double* part, cudaStream_t s);
-cudaError_t cpals_hadamard(const double* G, int d, int skip, int R, double* V, cudaStream_t s);
+// V = Hadamard product of the Grams but skip's; vhi, vlo (nullable): V as two fp32 words
+cudaError_t cpals_hadamard(const double* G, int d, int skip, int R, double* V, float* vhi, float* vlo,
+                           cudaStream_t s);
 // lower Cholesky factor of V in place; dinv (R) receives the reciprocals of its diagonal
 cudaError_t cpals_cholesky(double* V, int R, int* info, double* dinv, cudaStream_t s);
 int cpals_cholesky_launches(int R);
 // X = M (L L^T)^{-1}; mirrors L into the strict upper triangle of its storage first
 cudaError_t cpals_solve(double* L, const double* dinv, int R, const float* M, int64_t I, double* X,
                         cudaStream_t s);
-cudaError_t cpals_normalize(const double* X, int64_t I, int R, float* A, float* lam, cudaStream_t s);
+// A(:, r) = X(:, r) / ||X(:, r)||, lam[r] = ||X(:, r)|| (part: cpals_normalize_scratch_bytes(R))
+size_t cpals_normalize_scratch_bytes(int R);
+int cpals_normalize_launches();
+cudaError_t cpals_normalize(const double* X, int64_t I, int R, float* A, float* lam, double* part, cudaStream_t s);
 // fit = 1 - ||Y - X|| / ||Y|| (part: cpals_sumsq_scratch_bytes() of fp64 scratch)
 cudaError_t cpals_fit(const double* H, const float* lam, const float* M, const float* A, int64_t I, int R,
                       const double* norm_y2, const int* info, double* fit, double* part, cudaStream_t s);
-// X = M V^{-1} (fp64 out) for R <= cpals_mixed_max_rank(): V split into two fp32
-// words (vhi, vlo: R x R each), factored in fp32 (L: R x R, dinv: R), rows solved
-// in fp32 into x0 (I x R), residual M - x0 V (res: I x R) solved and added
+// X = M V^{-1} (fp64 out) for R <= cpals_mixed_max_rank(): V and its two fp32
+// words (vhi, vlo: R x R each, as cpals_hadamard wrote them), factored in fp32
+// (L: R x R, dinv: R; dblk:
+// cpals_mixed_block_bytes(R), the inverted diagonal blocks, 16-byte aligned),
+// rows solved in fp32 into x0 (I x R), residual M - x0 V (res: I x R) solved and
+// added
 int cpals_mixed_max_rank();
 int cpals_mixed_launches(int R);
+size_t cpals_mixed_block_bytes(int R);
 cudaError_t cpals_solve_mixed(const double* V, int R, const float* M, int64_t I, double* X, float* vhi, float* vlo,
-                              float* L, float* dinv, float* x0, float* res, int* info, cudaStream_t s);
+                              float* L, float* dinv, float* dblk, float* x0, float* res, int* info, cudaStream_t s);
 size_t cpals_sumsq_scratch_bytes();
 cudaError_t cpals_sum_squares(const float* Y, int64_t n, double* part, double* out, cudaStream_t s);
 cudaError_t launch_reduce_splits(const float* part, int64_t splits, int64_t n, float* out,

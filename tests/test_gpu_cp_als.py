@@ -48,7 +48,8 @@ def sweep_conditions(A0, A1):
 
 
 @pytest.mark.parametrize("dims,R", [((40, 36, 50), 12), ((130, 140, 150), 128), ((20, 24, 18, 22), 16),
-                                    ((150, 160, 170), 100), ((300, 310, 320), 256)])
+                                    ((150, 160, 170), 100), ((300, 310, 320), 256),
+                                    ((300, 290, 310), 288), ((330, 320, 310), 300)])
 def test_one_sweep_matches_oracle(dims, R):
     Y, _ = synth.random_case(70 + R, dims, R)
     A0 = start(80 + R, dims, R)
