@@ -789,7 +789,12 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, 
         e = cpals_sum_squares(Y, numel, part, norm_y2, s);
         p->launches += 2;
     }
-    for (int n = 0; n < d && e == cudaSuccess; ++n) {
+    // the Gram matrix of every factor; a continuing sweep on the same scratch and
+    // factors finds them where the previous sweep left them (each computed right
+    // after its factor's last update)
+    bool grams_ready = have_norm && p->sweep_left_images && p->sweep_scratch == scratch;
+    for (int n = 0; n < d; ++n) grams_ready = grams_ready && p->sweep_factors[n] == factors[n];
+    for (int n = 0; n < d && e == cudaSuccess && !grams_ready; ++n) {
         e = cpals_gram(factors[n], p->dims[n], R, G + n * RR, gpart, s);
         p->launches += cpals_gram_slabs(p->dims[n], R) > 1 ? 2 : 1;
     }
@@ -833,6 +838,8 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, 
     if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "CP-ALS fit: %s", cudaGetErrorString(e));
     p->launches += 3;
     p->sweep_left_images = 1;
+    p->sweep_scratch = scratch;
+    for (int n = 0; n < d; ++n) p->sweep_factors[n] = factors[n];
     return MTTKRP_OK;
 }
 

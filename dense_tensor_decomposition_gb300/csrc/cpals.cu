@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kChol2Threads, 1)
     float* P = sm + round4(tri(R));      // transposed panel [32][Rp]
     __shared__ __align__(16) float l11[kChB][kChB + 4];    // rows 16-byte aligned
     __shared__ __align__(16) float linv[kChB][kChB + 4];
-    __shared__ float colb[kChB], dvs[kChB];
+    __shared__ float dvs[kChB];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = warp; i < R; i += kChol2Threads / 32)
         for (int j = lane; j <= i; j += 32) cp_async4(a + tri(i) + j, vhi + (int64_t)i * R + j);
@@ -321,27 +321,22 @@ __global__ void __launch_bounds__(kChol2Threads, 1)
 #pragma unroll
             for (int t = 0; t < kChB; ++t) r[t] = (lane < nb && t <= lane) ? a[tri(k0 + lane) + k0 + t] : 0.f;
             float dl = 0.f;   // 1 / L[k0 + lane][k0 + lane]
-            // column j of the block goes through shared memory: lane j posts the
-            // pivot, every lane scales its entry and posts it, every lane updates
-            // its row from the posted column
+            // Every lane updates all of its row unconditionally: what lands above
+            // the diagonal (t > lane) is never read by the lower part (pivots come
+            // from the diagonal, shuffled column entries from lanes below) and is
+            // masked when the block is stored; no per-lane selects in the loop,
+            // which measured several times faster.
 #pragma unroll
             for (int j = 0; j < kChB; ++j) {
                 if (j < nb) {
-                    if (lane == j) colb[j] = r[j];
-                    __syncwarp();
-                    const float piv = colb[j];
+                    const float piv = __shfl_sync(0xffffffffu, r[j], j);
                     first_bad = (first_bad < 0 && !(piv > 0.f)) ? k0 + j : first_bad;
                     float inv = rsqrtf(piv);
                     inv = inv * fmaf(-0.5f * piv * inv, inv, 1.5f);   // Newton-Raphson step for 1 / sqrt
-                    const float dj = piv * inv;
                     dl = lane == j ? inv : dl;
-                    r[j] = lane == j ? dj : (lane > j ? r[j] * inv : r[j]);
-                    __syncwarp();
-                    colb[lane] = r[j];   // L[lane][j] (zero above the diagonal)
-                    __syncwarp();
+                    r[j] = lane == j ? piv * inv : r[j] * inv;
 #pragma unroll
-                    for (int t = j + 1; t < kChB; ++t) r[t] = lane >= t ? fmaf(-r[j], colb[t], r[t]) : r[t];
-                    __syncwarp();
+                    for (int t = j + 1; t < kChB; ++t) r[t] = fmaf(-r[j], __shfl_sync(0xffffffffu, r[j], t), r[t]);
                 }
             }
 #pragma unroll
@@ -352,23 +347,23 @@ __global__ void __launch_bounds__(kChol2Threads, 1)
             if (lane < nb) dinv[k0 + lane] = dl;
             dvs[lane] = dl;
             __syncwarp();
-            // inverse of the block, lane c = column c: z[i] = Linv[i][c]
+            // inverse of the block, lane c = column c: L z = e_c by substitution,
+            // z[i] = (delta_ic - sum_{k<i} L[i][k] z[k]) / L[i][i] (zero for i < c)
             float z[kChB];
 #pragma unroll
             for (int i = 0; i < kChB; ++i) {
-                float s0 = 0.f, s1 = 0.f;
+                float s0 = i == lane ? 1.f : 0.f, s1 = 0.f;
 #pragma unroll
                 for (int k = 0; k + 4 <= i; k += 4) {
                     const float4 l = *reinterpret_cast<const float4*>(&l11[i][k]);
-                    s0 = fmaf(l.x, z[k], s0);
-                    s1 = fmaf(l.y, z[k + 1], s1);
-                    s0 = fmaf(l.z, z[k + 2], s0);
-                    s1 = fmaf(l.w, z[k + 3], s1);
+                    s0 = fmaf(-l.x, z[k], s0);
+                    s1 = fmaf(-l.y, z[k + 1], s1);
+                    s0 = fmaf(-l.z, z[k + 2], s0);
+                    s1 = fmaf(-l.w, z[k + 3], s1);
                 }
 #pragma unroll
-                for (int k = i & ~3; k < i; ++k) s0 = fmaf(l11[i][k], z[k], s0);
-                const float di = dvs[i];
-                z[i] = i == lane ? di : (i > lane ? -(s0 + s1) * di : 0.f);
+                for (int k = i & ~3; k < i; ++k) s0 = fmaf(-l11[i][k], z[k], s0);
+                z[i] = (s0 + s1) * dvs[i];
             }
             float* dblk = Dm + (int64_t)(k0 / kChB) * kChB * kChB;
 #pragma unroll
@@ -984,16 +979,25 @@ __global__ void __launch_bounds__(256) fit_partial_kernel(const double* __restri
     }
 }
 
-__global__ void fit_final_kernel(const double* __restrict__ part, int nb, const double* __restrict__ norm_y2,
-                                 const int* __restrict__ info, double* __restrict__ fit) {
-    if (threadIdx.x != 0) return;
-    double x2 = 0.0, in = 0.0;
-    for (int b = 0; b < nb; ++b) {
-        x2 += part[2 * b];
-        in += part[2 * b + 1];
+__global__ void __launch_bounds__(kFitBlocks) fit_final_kernel(const double* __restrict__ part, int nb,
+                                                            const double* __restrict__ norm_y2,
+                                                            const int* __restrict__ info, double* __restrict__ fit) {
+    // pairwise tree over the block partials (fixed order); nb <= kFitBlocks
+    __shared__ double x2s[kFitBlocks], ins[kFitBlocks];
+    const int t = threadIdx.x;
+    x2s[t] = t < nb ? part[2 * t] : 0.0;
+    ins[t] = t < nb ? part[2 * t + 1] : 0.0;
+    __syncthreads();
+    for (int h = kFitBlocks / 2; h > 0; h >>= 1) {
+        if (t < h) {
+            x2s[t] += x2s[t + h];
+            ins[t] += ins[t + h];
+        }
+        __syncthreads();
     }
+    if (t != 0) return;
     const double y2 = *norm_y2;
-    const double res2 = y2 + x2 - 2.0 * in;
+    const double res2 = y2 + x2s[0] - 2.0 * ins[0];
     *fit = (*info != 0) ? __longlong_as_double(0x7ff8000000000000ll) : 1.0 - sqrt(res2 > 0.0 ? res2 : 0.0) / sqrt(y2);
 }
 
@@ -1195,7 +1199,7 @@ cudaError_t cpals_normalize(const double* X, int64_t I, int R, float* A, float* 
 cudaError_t cpals_fit(const double* H, const float* lam, const float* M, const float* A, int64_t I, int R,
                       const double* norm_y2, const int* info, double* fit, double* part, cudaStream_t s) {
     fit_partial_kernel<<<kFitBlocks, 256, 0, s>>>(H, lam, M, A, I, R, part);
-    fit_final_kernel<<<1, 32, 0, s>>>(part, kFitBlocks, norm_y2, info, fit);
+    fit_final_kernel<<<1, kFitBlocks, 0, s>>>(part, kFitBlocks, norm_y2, info, fit);
     return cudaGetLastError();
 }
 

@@ -110,6 +110,10 @@ struct Plan {
     // the last call on this plan was a CP-ALS sweep: max |Y| and the fp16 images
     // in the workspace are those of that sweep's Y
     int sweep_left_images;
+    // and its scratch and factor pointers: a continuing sweep with the same ones
+    // reuses the Gram matrices that sweep left in the scratch
+    const void* sweep_scratch;
+    const float* sweep_factors[kMaxD];
     // benchmark timing: event pairs around the main kernel of each mode
     int timing;
     int ev_cap[kMaxD];

@@ -210,7 +210,9 @@ int mttkrp_noalloc(int d, const int64_t* dims, int64_t R, const float* Y,
  *           Y is unchanged since the previous sweep on this plan and that no
  *           other call used the plan in between: the sweep then also reuses
  *           the max |Y| and fp16 images of Y that the previous sweep left in
- *           the plan's workspace.
+ *           the plan's workspace, and, when it gets the same factor pointers
+ *           and scratch as that sweep, the Gram matrices of the factors that
+ *           sweep left in the scratch (so neither may change in between).
  * fit       device, one double (output); NaN if V was not positive definite.
  * scratch   device scratch of mttkrp_cp_als_scratch_bytes(plan) bytes, 256-byte
  *           aligned, caller-owned.
