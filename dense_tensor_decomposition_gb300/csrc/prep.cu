@@ -11,52 +11,84 @@
 namespace mk {
 
 // One warp per table row: the row's multi-index, Y offset and scale once, then
-// the R columns by the lanes (coalesced loads and stores).
+// the R columns by the lanes (coalesced loads and stores; 16-byte ones when R
+// is a multiple of 4 and every factor is 16-byte aligned).  NM = the number of
+// factors in the product (a template argument, so that the per-column loop
+// holds only its loads and multiplies).
+template <int NM, bool V4>
 __global__ void __launch_bounds__(256) prod_table_kernel(ProdTableArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < a.rows;
          row += nwarps) {
-        const float* frow[kMaxD];
+        const float* frow[NM > 0 ? NM : 1];
         int64_t rem = row, base = 0;
 #pragma unroll
-        for (int m = kMaxD - 1; m >= 0; --m) {
-            frow[m] = nullptr;
-            if (m < a.nm) {
-                const int64_t idx = rem % a.dim[m];
-                rem /= a.dim[m];
-                frow[m] = a.fac[m] + idx * a.R;
-                base += idx * a.ystride[m];
-            }
+        for (int m = NM - 1; m >= 0; --m) {
+            const int64_t idx = rem % a.dim[m];
+            rem /= a.dim[m];
+            frow[m] = a.fac[m] + idx * a.R;
+            base += idx * a.ystride[m];
         }
         float f = 1.f;
         if (a.slab_bits != nullptr)
             f = pow2_scale(*a.gmax_bits) * pow2_recip(slab_scale(a.slab_bits, row / a.slab_div, *a.gmax_bits));
         float* out = a.tab + row * a.R;
-        for (int64_t r0 = lane; r0 < a.R; r0 += 128) {   // four columns a lane in flight
-            float prod[4];
+        if (V4) {
+            const int64_t R4 = a.R / 4;
+            for (int64_t c = lane; c < R4; c += 32) {
+                float4 p = make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t r = r0 + 32 * u;
-                prod[u] = 1.0f;
-#pragma unroll
-                for (int m = kMaxD - 1; m >= 0; --m)
-                    if (m < a.nm && r < a.R) prod[u] *= __ldg(frow[m] + r);
+                for (int m = NM - 1; m >= 0; --m) {
+                    const float4 v = __ldg(reinterpret_cast<const float4*>(frow[m]) + c);
+                    p.x *= v.x;
+                    p.y *= v.y;
+                    p.z *= v.z;
+                    p.w *= v.w;
+                }
+                reinterpret_cast<float4*>(out)[c] = make_float4(p.x * f, p.y * f, p.z * f, p.w * f);
             }
+        } else {
+            for (int64_t r = lane; r < a.R; r += 32) {
+                float p = 1.f;
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (r0 + 32 * u < a.R) out[r0 + 32 * u] = prod[u] * f;
+                for (int m = NM - 1; m >= 0; --m) p *= __ldg(frow[m] + r);
+                out[r] = p * f;
+            }
         }
         if (a.base != nullptr && lane == 0) a.base[row] = base;
     }
+}
+
+template <int NM>
+cudaError_t launch_prod_table_nm(const ProdTableArgs& a, bool v4, unsigned blocks, cudaStream_t s) {
+    if (v4)
+        prod_table_kernel<NM, true><<<blocks, 256, 0, s>>>(a);
+    else
+        prod_table_kernel<NM, false><<<blocks, 256, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_prod_table(const ProdTableArgs& a, cudaStream_t s) {
     if (a.rows * a.R == 0) return cudaSuccess;
     int64_t blocks = (a.rows + 7) / 8;   // eight warps, one row each
     if (blocks > 152 * 16) blocks = 152 * 16;
-    prod_table_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    bool v4 = a.R % 4 == 0 && (reinterpret_cast<uintptr_t>(a.tab) & 15) == 0;
+    for (int m = 0; m < a.nm; ++m) v4 = v4 && (reinterpret_cast<uintptr_t>(a.fac[m]) & 15) == 0;
+    const unsigned b = (unsigned)blocks;
+    static_assert(kMaxD == 8, "one instantiation per factor count");
+    switch (a.nm) {
+        case 0: return launch_prod_table_nm<0>(a, v4, b, s);
+        case 1: return launch_prod_table_nm<1>(a, v4, b, s);
+        case 2: return launch_prod_table_nm<2>(a, v4, b, s);
+        case 3: return launch_prod_table_nm<3>(a, v4, b, s);
+        case 4: return launch_prod_table_nm<4>(a, v4, b, s);
+        case 5: return launch_prod_table_nm<5>(a, v4, b, s);
+        case 6: return launch_prod_table_nm<6>(a, v4, b, s);
+        case 7: return launch_prod_table_nm<7>(a, v4, b, s);
+        case 8: return launch_prod_table_nm<8>(a, v4, b, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 // Compensated fp32 addition (Neumaier): sum + c carries the exact running total
@@ -68,28 +100,27 @@ __device__ __forceinline__ void kahan_add(float& sum, float& c, float x) {
     sum = t;
 }
 
-// out[e] = sum over s of part[s * n + e].  Each block owns 32 groups of 4
-// consecutive outputs (one 16-byte group per lane); warp w adds the partials of
-// splits [w*S/8, (w+1)*S/8) in increasing s with several 16-byte loads in
-// flight (compensated fp32), and the eight warp sums are added in warp order
-// (compensated fp32 again).  The order depends only on (S, n), so results are
-// bitwise reproducible; spreading the splits over warps keeps enough loads in
-// flight both for many outputs and few splits and for few outputs and many
-// splits.
-constexpr int kRedWarps = 8;
+// out[e] = sum over s of part[s * n + e].  A block of 256 threads owns G
+// groups of V consecutive outputs (one 16-byte group per thread when V = 4)
+// and cuts the splits into Q = 256 / G contiguous slices: thread (slice q,
+// group g) adds the partials of splits [q S / Q, (q + 1) S / Q) in increasing s
+// with several loads in flight (compensated fp32), and the Q slice sums are
+// added in slice order (compensated fp32 again).  The order depends only on
+// (S, n, G), so results are bitwise reproducible; many slices keep enough
+// loads in flight when there are few outputs and many splits.
+constexpr int kRedThreads = 256;
 
-template <int V>   // V = 4: float4 groups; V = 1: scalars
-__global__ void __launch_bounds__(kRedWarps * 32)
-    reduce_splits_kernel(const float* __restrict__ part, int64_t splits, int64_t n,
-                         float* __restrict__ out) {
-    __shared__ float sums[kRedWarps][32][V];
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int64_t s0 = splits * warp / kRedWarps;
-    const int64_t s1 = splits * (warp + 1) / kRedWarps;
+template <int V, int G>   // V = 4: float4 groups; V = 1: scalars
+__global__ void __launch_bounds__(kRedThreads)
+    reduce_splits_kernel(const float* __restrict__ part, int64_t splits, int64_t n, float* __restrict__ out) {
+    constexpr int Q = kRedThreads / G;
+    __shared__ float sums[Q][G][V];
+    const int gl = threadIdx.x % G, q = threadIdx.x / G;
+    const int64_t s0 = splits * q / Q;
+    const int64_t s1 = splits * (q + 1) / Q;
     const int64_t ng = n / V;   // groups
-    for (int64_t base = (int64_t)blockIdx.x * 32; base < ng; base += (int64_t)gridDim.x * 32) {
-        const int64_t g = base + lane;
+    for (int64_t base = (int64_t)blockIdx.x * G; base < ng; base += (int64_t)gridDim.x * G) {
+        const int64_t g = base + gl;
         float acc[V], cmp[V];
 #pragma unroll
         for (int c = 0; c < V; ++c) acc[c] = cmp[c] = 0.f;
@@ -129,16 +160,15 @@ __global__ void __launch_bounds__(kRedWarps * 32)
             }
         }
 #pragma unroll
-        for (int c = 0; c < V; ++c) sums[warp][lane][c] = acc[c] + cmp[c];
+        for (int c = 0; c < V; ++c) sums[q][gl][c] = acc[c] + cmp[c];
         __syncthreads();
-        if (warp == 0 && g < ng) {
+        if (q == 0 && g < ng) {
             float t[V], tc[V];
 #pragma unroll
             for (int c = 0; c < V; ++c) t[c] = tc[c] = 0.f;
+            for (int w = 0; w < Q; ++w)
 #pragma unroll
-            for (int w = 0; w < kRedWarps; ++w)
-#pragma unroll
-                for (int c = 0; c < V; ++c) kahan_add(t[c], tc[c], sums[w][lane][c]);
+                for (int c = 0; c < V; ++c) kahan_add(t[c], tc[c], sums[w][gl][c]);
             if constexpr (V == 4)
                 reinterpret_cast<float4*>(out)[g] = make_float4(t[0] + tc[0], t[1] + tc[1], t[2] + tc[2], t[3] + tc[3]);
             else
@@ -195,12 +225,20 @@ cudaError_t launch_reduce_splits(const float* part, int64_t splits, int64_t n, f
                                                                    groups, reinterpret_cast<float4*>(out));
         return cudaGetLastError();
     }
-    int64_t blocks = (groups + 31) / 32;
+    // many splits: 32 slices of eight groups a block; few: 8 slices of 32 groups
+    const bool wide = splits >= 64;
+    const int G = wide ? 8 : 32;
+    int64_t blocks = (groups + G - 1) / G;
     if (blocks > 152 * 16) blocks = 152 * 16;
-    if (vec)
-        reduce_splits_kernel<4><<<(unsigned)blocks, kRedWarps * 32, 0, s>>>(part, splits, n, out);
+    const unsigned b = (unsigned)blocks;
+    if (vec && wide)
+        reduce_splits_kernel<4, 8><<<b, kRedThreads, 0, s>>>(part, splits, n, out);
+    else if (vec)
+        reduce_splits_kernel<4, 32><<<b, kRedThreads, 0, s>>>(part, splits, n, out);
+    else if (wide)
+        reduce_splits_kernel<1, 8><<<b, kRedThreads, 0, s>>>(part, splits, n, out);
     else
-        reduce_splits_kernel<1><<<(unsigned)blocks, kRedWarps * 32, 0, s>>>(part, splits, n, out);
+        reduce_splits_kernel<1, 32><<<b, kRedThreads, 0, s>>>(part, splits, n, out);
     return cudaGetLastError();
 }
 

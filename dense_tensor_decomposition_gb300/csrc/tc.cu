@@ -1642,7 +1642,6 @@ __global__ void __launch_bounds__(kH2Threads, 1) tc_h2_kernel(const __grid_const
     const int64_t pre_lo = (int64_t)blockIdx.z * a.pre_per_split;
     int64_t pre_hi = pre_lo + a.pre_per_split;
     if (pre_hi > a.npre) pre_hi = a.npre;
-    const int64_t npi = pre_hi > pre_lo ? pre_hi - pre_lo : 0;
     const int KS = a.KS;
     const int njc = (KS + CK - 1) / CK;
     auto chunk_len = [&](int jc) { return min(CK, KS - jc * CK); };
