@@ -97,6 +97,9 @@ struct TcArgs {
                               // CTA takes all pre indices (explicit Khatri-Rao product)
     int64_t ttm_q;            // > 0: mode-n product; tile row m is (p, q) = (m / ttm_q, m % ttm_q)
                               // of X viewed [P, N, Q], and column j goes to T[p, j, q]
+    int64_t tiles_y;          // > 0 (image kernel, not stacked): row tiles, taken by the CTAs of
+                              // one grid column in turn (blockIdx.y, + gridDim.y, ...); 0: one
+                              // row tile a CTA, blockIdx.y
     uint32_t y_box_bytes;     // bytes of one Y tile copy
     // small-I variant: ps pre indices share one 128-row tile (rows slot * I + i)
     int ps;                   // pre-index slots per tile (1 otherwise)
@@ -2140,7 +2143,6 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int64_t m0 = (int64_t)blockIdx.y * kBM;
     const int64_t r0 = (int64_t)blockIdx.x * BN;
     const int KS = a.KS;
     const int njc = (KS + CK - 1) / CK;
@@ -2148,6 +2150,11 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
     const int64_t pre_lo = share.pre_lo, pre_hi = share.pre_hi;
     const int jc0 = share.jc0, jc1 = share.jc1;
     auto chunk_len = [&](int jc) { return min(CK, KS - jc * CK); };
+    // row tiles of this CTA: blockIdx.y alone, or (persistent) every gridDim.y-th
+    // one; every role walks the same sequence, and the pipeline (operand ring,
+    // accumulator buffers, B chunks) runs on across tiles
+    const int64_t ty_end = (a.tiles_y > 0 && !SMALL) ? a.tiles_y : (int64_t)blockIdx.y + 1;
+    const int64_t ty_step = (a.tiles_y > 0 && !SMALL) ? (int64_t)gridDim.y : 1;
     constexpr uint32_t kTmemCols = 2 * BN;   // two accumulator buffers
     static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
                   "TMEM allocation: a power of two in [32, 512]");
@@ -2195,11 +2202,11 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             const uint8_t* bimg = reinterpret_cast<const uint8_t*>(a.bimg);
             Ring<NS> rr;
             int64_t issued = 0;
-            int jc_loaded = -1;
+            uint32_t nbl = 0;   // B chunks loaded so far (the B barriers' phases)
             bool ok = true;
             auto load_b = [&](int jc) -> bool {
-                if (jc > jc0 && !wait_bounded_inl(bempty, (uint32_t)((jc - jc0 - 1) & 1), abort_flag, a.status,
-                                                kStatusTimeoutTma))
+                if (nbl > 0 && !wait_bounded_inl(bempty, (nbl - 1) & 1u, abort_flag, a.status,
+                                                 kStatusTimeoutTma))
                     return false;
                 const int ck = chunk_len(jc);
                 mbar_arrive_expect_tx(bfull, (uint32_t)(ck * 2 * L::kB));
@@ -2208,12 +2215,14 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                     const uint8_t* src = bimg + ((int64_t)blockIdx.x * KS + ks) * (int64_t)(2 * L::kB);
                     bulk_load(bres + q * 2 * L::kB, src, 2 * L::kB, bfull);
                 }
-                jc_loaded = jc;
+                ++nbl;
                 return true;
             };
             // the pre index pi = (cP, cQ) in C order, advanced without divisions
             const int64_t nQ = a.nQ;
             const int cP0 = (int)(pre_lo / nQ), cQ0 = (int)(pre_lo - (int64_t)cP0 * nQ);
+            for (int64_t ty = blockIdx.y; ty < ty_end && ok; ty += ty_step) {
+            const int64_t m0 = ty * kBM;
             // mode-n product: (p, q) of the first row of each 64-row half
             int ttm_q0 = 0, ttm_p0 = 0, ttm_q1 = 0, ttm_p1 = 0;
             if (MN && a.ttm_q > 0) {
@@ -2292,9 +2301,10 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                 }
                 if (ok && b_pending && !load_b(jc)) ok = false;
             }
+            }   // row tiles
             for (int64_t u = issued - 1; u >= 0 && u >= issued - NS; --u)
                 wait_drain_inl(&full[u % NS], (uint32_t)((u / NS) & 1), a.status);
-            if (jc_loaded >= 0) wait_drain_inl(bfull, (uint32_t)((jc_loaded - jc0) & 1), a.status);
+            if (nbl > 0) wait_drain_inl(bfull, (nbl - 1) & 1u, a.status);
         } else if (warp == 1 && lane == 0) {
             // ------------------------- MMA issuer -------------------------
             // kind::f16: fp16 A and B (B K-major; A K-major, or MN-major with the
@@ -2311,13 +2321,16 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             int zb = 0;
             uint32_t zph = 0;
             uint32_t zused = 0;
+            uint32_t nbu = 0;   // B chunks used so far
             bool ok = true;
+            for (int64_t ty = blockIdx.y; ty < ty_end && ok; ty += ty_step)
             for (int jc = jc0; jc < jc1 && ok; ++jc) {
                 const int ck = chunk_len(jc);
-                if (!wait_bounded_inl(bfull, (uint32_t)((jc - jc0) & 1), abort_flag, a.status, kStatusTimeoutMma)) {
+                if (!wait_bounded_inl(bfull, nbu & 1u, abort_flag, a.status, kStatusTimeoutMma)) {
                     ok = false;
                     break;
                 }
+                ++nbu;
                 for (int64_t pi = pre_lo; pi < pre_hi && ok; pi = unit_next(pi)) {
                     uint32_t bw = b_w0;
                     for (int q = 0; q < ck; ++q, bw += kBStep, rr.next()) {
@@ -2445,8 +2458,12 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
         static_assert(kCols % kImgEpiLd == 0, "TMEM load width");
         const int quad = warp & 3;
         const int part = (warp - kImgEpiWarp0) >> 2;
-        const int64_t row = m0 + 32 * quad + lane;
         const int64_t c0 = r0 + part * kCols;
+        int zb = 0;
+        uint32_t zph = 0;
+        bool ok = true;
+        for (int64_t ty = blockIdx.y; ty < ty_end && ok; ty += ty_step) {
+        const int64_t row = ty * kBM + 32 * quad + lane;
         float acc[kCols];
 #pragma unroll
         for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
@@ -2460,9 +2477,6 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
         };
         float g_next[kGv];
         load_g(pre_lo, g_next);
-        int zb = 0;
-        uint32_t zph = 0;
-        bool ok = true;
         for (int jc = jc0; jc < jc1 && ok; ++jc) {
             for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
                 float g_cur[kGv];
@@ -2527,6 +2541,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                 asm volatile("" ::: "memory");   // keep one group of column scales in flight
             }
         }
+        }   // row tiles
         }   // not SMALL
     }
 
@@ -4127,7 +4142,16 @@ int tc_ttm_run(const float* X, const float* M, float* T, int64_t P, int64_t N, i
     args.colscale = colscale;
     args.ttm_q = Q == 1 ? 0 : Q;
     args.status = status;
-    dim3 grid((unsigned)cdiv64(J, l.bn), (unsigned)cdiv64(l.rows, kBM), 1u);
+    // persistent: one CTA per SM, the row tiles of a column tile dealt out in
+    // turn (the column tiles of one row tile run side by side and share its A
+    // tiles through L2); the per-CTA start-up and the last tile's drain are paid
+    // once per CTA instead of once per tile
+    const int64_t gx = cdiv64(J, l.bn), ntiles = cdiv64(l.rows, kBM);
+    int64_t gy = sm_count() / gx;
+    if (gy < 1) gy = 1;
+    if (gy > ntiles) gy = ntiles;
+    args.tiles_y = ntiles;
+    dim3 grid((unsigned)gx, (unsigned)gy, 1u);
     if (Q == 1)
         e = l.bn == 256 ? launch_img<256>(args, grid, stream)
           : l.bn == 128 ? launch_img<128>(args, grid, stream)

@@ -76,7 +76,10 @@ def test_ttm_matches_oracle(dims, mode, J):
 # last (p, q) row, contraction lengths 32, 40, 96, 128, 256 (padded to 64), J from
 # 32 (64-column tiles) to 300 (128- and 256-column tiles, ragged)
 TC_SHAPES = [((64, 48, 256), 2, 130), ((64, 48, 256), 2, 33), ((64, 128, 64), 1, 50), ((32, 64, 128), 0, 100),
-             ((16, 40, 8, 64), 1, 300), ((130, 96), 1, 200), ((3, 200, 64), 1, 64), ((2, 128, 40, 128), 2, 256)]
+             ((16, 40, 8, 64), 1, 300), ((130, 96), 1, 200), ((3, 200, 64), 1, 64), ((2, 128, 40, 128), 2, 256),
+             # several row tiles a CTA (the kernel walks row tiles persistently), column
+             # and row tails
+             ((300, 64, 64), 1, 600), ((8000, 96), 1, 520)]
 
 
 @pytest.mark.parametrize("dims,mode,J", TC_SHAPES)
