@@ -1032,9 +1032,11 @@ __global__ void __launch_bounds__(256) sumsq_final_kernel(const double* __restri
 }  // namespace
 
 int cpals_gram_slabs(int64_t I, int R) {
-    // enough CTAs to fill the GPU, at least one 32-row slab each
-    const int64_t tiles = (int64_t)((R + 15) / 16) * ((R + 15) / 16);
-    int64_t S = (152 * 4 + tiles - 1) / tiles;
+    // about eight working CTAs an SM (the lower-triangle tiles; the others exit
+    // at once), at least one 32-row slab each: the slab loop is latency-bound
+    const int64_t nt = (R + 15) / 16;
+    const int64_t tiles = nt * (nt + 1) / 2;
+    int64_t S = (152 * 8 + tiles - 1) / tiles;
     const int64_t slabs = (I + 31) / 32;
     if (S > slabs) S = slabs;
     if (S > 64) S = 64;

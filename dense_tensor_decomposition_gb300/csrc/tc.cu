@@ -2622,7 +2622,7 @@ __global__ void __launch_bounds__(256) split_image_kernel(const float* __restric
 // rows of 64 consecutive p of both transposed images (4-byte stores, P even).
 // Rows p of the P x I view belong to slab p / rps of mode 0 (rps rows a slab).
 template <bool VEC>
-__global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restrict__ y, int64_t P, int64_t I,
+__global__ void __launch_bounds__(256, 3) split_image_t_kernel(const float* __restrict__ y, int64_t P, int64_t I,
                                                             const uint32_t* __restrict__ slab,
                                                             const uint32_t* __restrict__ gmax, int64_t rps,
                                                             __half* __restrict__ hi, __half* __restrict__ lo,
@@ -2664,40 +2664,57 @@ __global__ void __launch_bounds__(256) split_image_t_kernel(const float* __restr
             tile_scales(p0);
             const int nvals = rows * Ii;
             const int64_t base = p0 * I;
-            for (int f = threadIdx.x; 4 * f < nvals; f += blockDim.x) {
-                float v[4] = {0.f, 0.f, 0.f, 0.f};
-                if (4 * f + 3 < nvals) {
-                    const float4 x = __ldcs(reinterpret_cast<const float4*>(y + base) + f);
-                    v[0] = x.x;
-                    v[1] = x.y;
-                    v[2] = x.z;
-                    v[3] = x.w;
-                } else {
-                    for (int q = 0; q < 4; ++q)
-                        if (4 * f + q < nvals) v[q] = __ldcs(y + base + 4 * f + q);
-                }
-                uint32_t hb[4], lb[4];
+            // eight 16-byte loads in flight a thread before any conversion
+            constexpr int kU = 8;
+            for (int f0 = 0; 4 * f0 < nvals; f0 += kU * 256) {
+                float4 vv[kU];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int idx = 4 * f + q;
-                    const int row = idx / Ii;
-                    const float x = v[q] * row_scale(p0 + row, tps);
-                    const __half h = __float2half_rn(x);
-                    const __half l = __float2half_rn(x - __half2float(h));
-                    hb[q] = __half_as_ushort(h);
-                    lb[q] = __half_as_ushort(l);
-                    if (idx < nvals) shf[(idx - row * Ii) * stride + row] = hb[q] | (lb[q] << 16);
-                }
-                if (write_nat) {
+                for (int u = 0; u < kU; ++u) {
+                    const int f = f0 + threadIdx.x + 256 * u;
+                    vv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (4 * f + 3 < nvals) {
-                        reinterpret_cast<uint2*>(hi + base)[f] = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
-                        reinterpret_cast<uint2*>(lo + base)[f] = make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
-                    } else {
+                        vv[u] = __ldcs(reinterpret_cast<const float4*>(y + base) + f);
+                    } else if (4 * f < nvals) {
+                        float t[4] = {0.f, 0.f, 0.f, 0.f};
                         for (int q = 0; q < 4; ++q)
-                            if (4 * f + q < nvals) {
-                                hi[base + 4 * f + q] = __ushort_as_half((unsigned short)hb[q]);
-                                lo[base + 4 * f + q] = __ushort_as_half((unsigned short)lb[q]);
-                            }
+                            if (4 * f + q < nvals) t[q] = __ldcs(y + base + 4 * f + q);
+                        vv[u] = make_float4(t[0], t[1], t[2], t[3]);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int f = f0 + threadIdx.x + 256 * u;
+                    if (4 * f >= nvals) continue;
+                    const float v[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
+                    uint32_t hb[4], lb[4];
+                    int row = (4 * f) / Ii, col = 4 * f - row * Ii;   // (row, col) of value 4 f
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int idx = 4 * f + q;
+                        const float x = v[q] * row_scale(p0 + row, tps);
+                        const __half h = __float2half_rn(x);
+                        const __half l = __float2half_rn(x - __half2float(h));
+                        hb[q] = __half_as_ushort(h);
+                        lb[q] = __half_as_ushort(l);
+                        if (idx < nvals) shf[col * stride + row] = hb[q] | (lb[q] << 16);
+                        if (++col == Ii) {
+                            col = 0;
+                            ++row;
+                        }
+                    }
+                    if (write_nat) {
+                        if (4 * f + 3 < nvals) {
+                            reinterpret_cast<uint2*>(hi + base)[f] =
+                                make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
+                            reinterpret_cast<uint2*>(lo + base)[f] =
+                                make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
+                        } else {
+                            for (int q = 0; q < 4; ++q)
+                                if (4 * f + q < nvals) {
+                                    hi[base + 4 * f + q] = __ushort_as_half((unsigned short)hb[q]);
+                                    lo[base + 4 * f + q] = __ushort_as_half((unsigned short)lb[q]);
+                                }
+                        }
                     }
                 }
             }
