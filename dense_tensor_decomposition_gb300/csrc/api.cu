@@ -191,7 +191,7 @@ void place_plan_regions(Plan& p) {
     if (!fp16) return;
     base = align256(base);
     p.off_slab = base;
-    base = align256(base + (size_t)p.nslab * sizeof(uint32_t));
+    base = align256(base + (size_t)(p.nslab + 1) * sizeof(uint32_t));   // + the image pass's out-of-range flag
     int64_t numel = 1;
     for (int n = 0; n < p.d; ++n) numel *= p.dims[n];
     const size_t img = 2 * align256((size_t)numel * 2);   // hi and lo, 2 bytes an element

@@ -2579,12 +2579,22 @@ __device__ __forceinline__ void split1(float v, float sy, __half& h, __half& l) 
     l = __float2half_rn(x - __half2float(h));
 }
 
+// With ovf non-null, a scaled value outside the fp16 range (|x| >= 65504, or
+// not a number) sets *ovf: the scales came from sampled maxima that missed a
+// larger entry, and the exact pass that follows redoes maxima and images.  With
+// enable non-null the kernel runs only if *enable is set (that exact pass).
+__device__ __forceinline__ bool fp16_out_of_range(float x) { return !(fabsf(x) < 65504.f); }
+
 __global__ void __launch_bounds__(256) split_image_kernel(const float* __restrict__ y, int64_t nslab, int64_t len,
                                                           const uint32_t* __restrict__ slab,
                                                           const uint32_t* __restrict__ gmax,
-                                                          __half* __restrict__ hi, __half* __restrict__ lo) {
+                                                          __half* __restrict__ hi, __half* __restrict__ lo,
+                                                          uint32_t* __restrict__ ovf,
+                                                          const uint32_t* __restrict__ enable) {
+    if (enable != nullptr && *enable == 0) return;
     const SlabUnits su(nslab, len);
     const uint32_t gbits = *gmax;
+    bool bad = false;
     // y, hi and lo 16-byte aligned (the images are): whole units move as float4
     const bool vec = (len % 4 == 0) && (reinterpret_cast<uintptr_t>(y) & 15) == 0;
     for (int64_t u = su.u0; u < su.u1; ++u) {
@@ -2600,6 +2610,8 @@ __global__ void __launch_bounds__(256) split_image_kernel(const float* __restric
 #pragma unroll
             for (int q = 0; q < kSlabUnit / 1024; ++q) {
                 const float x0 = v[q].x * sy, x1 = v[q].y * sy, x2 = v[q].z * sy, x3 = v[q].w * sy;
+                bad |= fp16_out_of_range(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)))) ||
+                       x0 != x0 || x1 != x1 || x2 != x2 || x3 != x3;
                 const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
                 const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
                 const __half2 l01 = __floats2half2_rn(x0 - f01.x, x1 - f01.y);
@@ -2608,9 +2620,14 @@ __global__ void __launch_bounds__(256) split_image_kernel(const float* __restric
                 reinterpret_cast<uint2*>(lo)[f0 + 256 * q] = make_uint2(half2_bits(l01), half2_bits(l23));
             }
         } else {
-            for (int64_t i = a0 + threadIdx.x; i < a1; i += blockDim.x) split1(__ldcs(y + i), sy, hi[i], lo[i]);
+            for (int64_t i = a0 + threadIdx.x; i < a1; i += blockDim.x) {
+                const float v = __ldcs(y + i);
+                bad |= fp16_out_of_range(v * sy);
+                split1(v, sy, hi[i], lo[i]);
+            }
         }
     }
+    if (ovf != nullptr && __syncthreads_or(bad) && threadIdx.x == 0) atomicOr(ovf, 1u);
 }
 
 // The same split for the innermost mode: Y viewed as P x I (I = I_{d-1}, the
@@ -2627,7 +2644,10 @@ __global__ void __launch_bounds__(256, 3) split_image_t_kernel(const float* __re
                                                             const uint32_t* __restrict__ gmax, int64_t rps,
                                                             __half* __restrict__ hi, __half* __restrict__ lo,
                                                             __half* __restrict__ thi, __half* __restrict__ tlo,
-                                                            int write_nat) {
+                                                            int write_nat, uint32_t* __restrict__ ovf,
+                                                            const uint32_t* __restrict__ enable) {
+    if (enable != nullptr && *enable == 0) return;
+    bool bad = false;
     constexpr int TP = 64, TI = 128;
     __shared__ uint32_t sh[TI][TP + 1];   // [i][p]: hi in the low half, lo in the high half
     const uint32_t gbits = *gmax;
@@ -2692,6 +2712,7 @@ __global__ void __launch_bounds__(256, 3) split_image_t_kernel(const float* __re
                     for (int q = 0; q < 4; ++q) {
                         const int idx = 4 * f + q;
                         const float x = v[q] * row_scale(p0 + row, tps);
+                        bad |= fp16_out_of_range(x);
                         const __half h = __float2half_rn(x);
                         const __half l = __float2half_rn(x - __half2float(h));
                         hb[q] = __half_as_ushort(h);
@@ -2736,6 +2757,7 @@ __global__ void __launch_bounds__(256, 3) split_image_t_kernel(const float* __re
             }
             __syncthreads();
         }
+        if (ovf != nullptr && __syncthreads_or(bad) && threadIdx.x == 0) atomicOr(ovf, 1u);
         return;
     }
     const int64_t np = (P + TP - 1) / TP, ni = (I + TI - 1) / TI;
@@ -2778,6 +2800,7 @@ __global__ void __launch_bounds__(256, 3) split_image_t_kernel(const float* __re
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float x = v[q] * sy;
+                bad |= fp16_out_of_range(x);
                 const __half h = __float2half_rn(x);
                 const __half l = __float2half_rn(x - __half2float(h));
                 hb[q] = __half_as_ushort(h);
@@ -2818,6 +2841,7 @@ __global__ void __launch_bounds__(256, 3) split_image_t_kernel(const float* __re
         }
         __syncthreads();
     }
+    if (ovf != nullptr && __syncthreads_or(bad) && threadIdx.x == 0) atomicOr(ovf, 1u);
 }
 
 // ---------------------------------------------------------------------------
@@ -2879,9 +2903,13 @@ __global__ void tc_bimage_kernel(BImgArgs a) {
 // Largest magnitude of every slab of mode 0 (slab[s]) and of the whole tensor
 // (*gmax), as fp32 bits (non-negative floats order like their bits).  Each block
 // flushes its running maximum with one atomicMax per slab it touches and one on
-// *gmax at the end.  slab[] and *gmax must be zero before the launch.
+// *gmax at the end.  slab[] and *gmax must be zero, or hold lower bounds of the
+// maxima (the sampled ones), before the launch.  With enable non-null the
+// kernel runs only if *enable is set.
 __global__ void __launch_bounds__(256) slabmax_kernel(const float* __restrict__ y, int64_t nslab, int64_t len,
-                                                      uint32_t* __restrict__ slab, uint32_t* __restrict__ gmax) {
+                                                      uint32_t* __restrict__ slab, uint32_t* __restrict__ gmax,
+                                                      const uint32_t* __restrict__ enable) {
+    if (enable != nullptr && *enable == 0) return;
     __shared__ uint32_t wm[8];
     const SlabUnits su(nslab, len);
     const bool vec = (len % 4 == 0) && (reinterpret_cast<uintptr_t>(y) & 15) == 0;
@@ -2935,6 +2963,58 @@ __global__ void __launch_bounds__(256) slabmax_kernel(const float* __restrict__ 
         g = max(g, b);
     }
     if (threadIdx.x == 0 && g) atomicMax(gmax, g);
+}
+
+// Sampled maxima: every kSampleEvery-th chunk of kSampleChunk consecutive
+// elements of each slab (all of a slab of at most kSampleEvery chunks), a lower
+// bound of the slab's largest magnitude, stored (atomicMax) as at least the
+// smallest subnormal's bits, so that no sampled slab reads as all-zero: a scale
+// from a lower bound is at least the exact one (every value keeps at least the
+// exact path's precision), and a value it pushes out of the fp16 range is caught
+// by the split (which then calls for the exact maxima and images).  A warp takes
+// a chunk; one atomicMax on *gmax a block.  slab[] and *gmax zero before.
+constexpr int64_t kSampleChunk = 512, kSampleEvery = 16;
+
+__global__ void __launch_bounds__(256) slabsample_kernel(const float* __restrict__ y, int64_t nslab, int64_t len,
+                                                         uint32_t* __restrict__ slab, uint32_t* __restrict__ gmax) {
+    __shared__ uint32_t wm[8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t nch = (len + kSampleChunk - 1) / kSampleChunk;   // chunks a slab
+    const int64_t every = nch > kSampleEvery ? kSampleEvery : 1;
+    const int64_t per = (nch + every - 1) / every;                 // sampled chunks a slab
+    const int64_t total = nslab * per;
+    const bool vec = (len % 4 == 0) && (reinterpret_cast<uintptr_t>(y) & 15) == 0;
+    uint32_t bm = 0;
+    for (int64_t w = (int64_t)blockIdx.x * 8 + warp; w < total; w += (int64_t)gridDim.x * 8) {
+        const int64_t s = w / per, c = (w - s * per) * every;
+        const int64_t a0 = s * len + c * kSampleChunk;
+        const int64_t a1 = min(a0 + kSampleChunk, (s + 1) * len);
+        uint32_t m = 0;
+        if (vec && a1 - a0 == kSampleChunk) {
+            const float4* p = reinterpret_cast<const float4*>(y + a0) + lane;
+            float4 v[kSampleChunk / 128];
+#pragma unroll
+            for (int q = 0; q < kSampleChunk / 128; ++q) v[q] = __ldcs(p + 32 * q);
+#pragma unroll
+            for (int q = 0; q < kSampleChunk / 128; ++q)
+                m = max(m, max(max(__float_as_uint(fabsf(v[q].x)), __float_as_uint(fabsf(v[q].y))),
+                               max(__float_as_uint(fabsf(v[q].z)), __float_as_uint(fabsf(v[q].w)))));
+        } else {
+            for (int64_t i = a0 + lane; i < a1; i += 32) m = max(m, __float_as_uint(fabsf(y[i])));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        m = m > 0u ? m : 1u;
+        if (lane == 0) atomicMax(slab + s, m);
+        bm = max(bm, m);
+    }
+    if (lane == 0) wm[warp] = bm;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t t = 0;
+        for (int q = 0; q < 8; ++q) t = max(t, wm[q]);
+        if (t) atomicMax(gmax, t);
+    }
 }
 
 // Power-of-two scale of each Binner column: max_j |Binner(j, r)| is the product
@@ -3651,14 +3731,29 @@ int tc_prepare(const Plan& p, const ModePlan& mp, const float* Y, void* ws, cuda
     for (int t = 0; t < p.d; ++t) numel *= p.dims[t];
     const int64_t slab_len = numel / p.nslab;
     cudaError_t e = cudaSuccess;
+    // The maxima of a call that also writes the images (the common case) are
+    // sampled; the image pass checks every scaled value and, if one left the
+    // fp16 range, a second max pass (over all of Y, on top of the samples) and
+    // a second image pass run; otherwise those two launches return at once.
+    // Plans whose first fp16 mode converts per CTA take the exact maxima.
+    uint32_t* ovf = slab + p.nslab;   // the image pass's out-of-range flag
+    const bool sampled = !p.ymax_ready && mp.tc_img && !p.img_ready;
+    int64_t max_blocks = cdiv64(cdiv64(slab_len, kSlabUnit) * p.nslab, 4);
+    if (max_blocks > 152 * 8) max_blocks = 152 * 8;
     if (!p.ymax_ready) {
         // largest magnitude of every slab of mode 0 and of the whole tensor
         e = cudaMemsetAsync(ymax, 0, sizeof(uint32_t), stream);
-        if (e == cudaSuccess) e = cudaMemsetAsync(slab, 0, (size_t)p.nslab * sizeof(uint32_t), stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(slab, 0, (size_t)(p.nslab + 1) * sizeof(uint32_t), stream);
         if (e == cudaSuccess) {
-            int64_t blocks = cdiv64(cdiv64(slab_len, kSlabUnit) * p.nslab, 4);
-            if (blocks > 152 * 8) blocks = 152 * 8;
-            slabmax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, p.nslab, slab_len, slab, ymax);
+            if (sampled) {
+                const int64_t nch = cdiv64(slab_len, kSampleChunk);
+                const int64_t per = cdiv64(nch, nch > kSampleEvery ? kSampleEvery : 1);
+                int64_t blocks = cdiv64(per * p.nslab, 8);
+                if (blocks > 152 * 8) blocks = 152 * 8;
+                slabsample_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, p.nslab, slab_len, slab, ymax);
+            } else {
+                slabmax_kernel<<<(unsigned)max_blocks, 256, 0, stream>>>(Y, p.nslab, slab_len, slab, ymax, nullptr);
+            }
             e = cudaGetLastError();
         }
         if (e == cudaSuccess) {
@@ -3673,31 +3768,39 @@ int tc_prepare(const Plan& p, const ModePlan& mp, const float* Y, void* ws, cuda
         __half* img_lo = reinterpret_cast<__half*>(ws_base + mp.off_img + img_half);
         __half* timg_hi = reinterpret_cast<__half*>(ws_base + mp.off_timg);
         __half* timg_lo = reinterpret_cast<__half*>(ws_base + mp.off_timg + img_half);
-        if (p.img_t) {
-            const int64_t In = p.dims[p.d - 1];
-            const int64_t P = numel / In;
-            int64_t blocks = cdiv64(P, 64) * cdiv64(In, 128);
-            if (blocks > 152 * 16) blocks = 152 * 16;
-            // (I_{d-1} < 64: whole rows per tile, read flat; the 16-byte
-            // alignment of every tile start holds because tiles are 64 rows)
-            const int64_t rps = P / p.nslab;
-            if (In % 4 == 0)
-                split_image_t_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(
-                    Y, P, In, slab, ymax, rps, img_hi, img_lo, timg_hi, timg_lo, p.img_nat);
-            else
-                split_image_t_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(
-                    Y, P, In, slab, ymax, rps, img_hi, img_lo, timg_hi, timg_lo, p.img_nat);
-        } else {
-            int64_t blocks = cdiv64(cdiv64(slab_len, kSlabUnit) * p.nslab, 4);
-            if (blocks > 152 * 8) blocks = 152 * 8;
-            split_image_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, p.nslab, slab_len, slab, ymax, img_hi,
-                                                                     img_lo);
+        // pass 0: with the maxima as they are, flagging out-of-range values when
+        // they were sampled; pass 1 (sampled maxima only): the exact redo, which
+        // runs only if the flag is set
+        for (int pass = 0; pass < (sampled ? 2 : 1) && e == cudaSuccess; ++pass) {
+            uint32_t* flag_out = (sampled && pass == 0) ? ovf : nullptr;
+            const uint32_t* enable = pass == 1 ? ovf : nullptr;
+            if (pass == 1) {
+                slabmax_kernel<<<(unsigned)max_blocks, 256, 0, stream>>>(Y, p.nslab, slab_len, slab, ymax, enable);
+                if ((e = cudaGetLastError()) != cudaSuccess) break;
+                ++*nlaunch;
+            }
+            if (p.img_t) {
+                const int64_t In = p.dims[p.d - 1];
+                const int64_t P = numel / In;
+                int64_t blocks = cdiv64(P, 64) * cdiv64(In, 128);
+                if (blocks > 152 * 16) blocks = 152 * 16;
+                // (I_{d-1} < 64: whole rows per tile, read flat; the 16-byte
+                // alignment of every tile start holds because tiles are 64 rows)
+                const int64_t rps = P / p.nslab;
+                if (In % 4 == 0)
+                    split_image_t_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(
+                        Y, P, In, slab, ymax, rps, img_hi, img_lo, timg_hi, timg_lo, p.img_nat, flag_out, enable);
+                else
+                    split_image_t_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(
+                        Y, P, In, slab, ymax, rps, img_hi, img_lo, timg_hi, timg_lo, p.img_nat, flag_out, enable);
+            } else {
+                split_image_kernel<<<(unsigned)max_blocks, 256, 0, stream>>>(Y, p.nslab, slab_len, slab, ymax,
+                                                                            img_hi, img_lo, flag_out, enable);
+            }
+            e = cudaGetLastError();
+            if (e == cudaSuccess) ++*nlaunch;
         }
-        e = cudaGetLastError();
-        if (e == cudaSuccess) {
-            p.img_ready = 1;
-            ++*nlaunch;
-        }
+        if (e == cudaSuccess) p.img_ready = 1;
     }
     if (e != cudaSuccess) {
         snprintf(errbuf, errlen, "fp16 split pass: %s", cudaGetErrorString(e));
@@ -4051,12 +4154,28 @@ int tc_ttm_run(const float* X, const float* M, float* T, int64_t P, int64_t N, i
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) {
+        // sampled maximum, image pass with the out-of-range check, exact redo
+        // only if the check fired (as in tc_prepare)
+        uint32_t* ovf = slab + 1;
         int64_t blocks = cdiv64(cdiv64(numel, kSlabUnit), 4);
         if (blocks > 152 * 8) blocks = 152 * 8;
-        slabmax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(X, 1, numel, slab, ymax);
+        const int64_t nch = cdiv64(numel, kSampleChunk);
+        int64_t sblocks = cdiv64(cdiv64(nch, nch > kSampleEvery ? kSampleEvery : 1), 8);
+        if (sblocks > 152 * 8) sblocks = 152 * 8;
+        slabsample_kernel<<<(unsigned)sblocks, 256, 0, stream>>>(X, 1, numel, slab, ymax);
         e = cudaGetLastError();
         if (e == cudaSuccess) {
-            split_image_kernel<<<(unsigned)blocks, 256, 0, stream>>>(X, 1, numel, slab, ymax, img_hi, img_lo);
+            split_image_kernel<<<(unsigned)blocks, 256, 0, stream>>>(X, 1, numel, slab, ymax, img_hi, img_lo, ovf,
+                                                                     nullptr);
+            e = cudaGetLastError();
+        }
+        if (e == cudaSuccess) {
+            slabmax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(X, 1, numel, slab, ymax, ovf);
+            e = cudaGetLastError();
+        }
+        if (e == cudaSuccess) {
+            split_image_kernel<<<(unsigned)blocks, 256, 0, stream>>>(X, 1, numel, slab, ymax, img_hi, img_lo, nullptr,
+                                                                     ovf);
             e = cudaGetLastError();
         }
     }

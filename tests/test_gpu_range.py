@@ -93,3 +93,53 @@ def test_halves_along_last_mode_every_row(dims, R, path):
     for k in range(len(dims)):
         err = worst_row_error(got[k], oracle.mttkrp(Y, A, k))
         assert err <= TOL, f"{dims} R={R} mode {k} path {path}: worst row {err:.3e}"
+
+
+# Sampled maxima.  The maxima that set the fp16 scales are taken from every
+# 16th chunk of 512 consecutive elements of each slab of mode 0; the image pass
+# checks every scaled value and, when one leaves the fp16 range, the exact
+# maxima and images are recomputed before any kernel reads them.  These tensors
+# put a large entry where the sample does not look (element 1000 of a slab of
+# 32768: chunk 1), so the sampled maximum is far below the true one.
+
+@pytest.mark.parametrize("dims,R,factor,path", [
+    ((4, 64, 512), 64, 1e6, "auto"),     # out of range: the exact redo runs
+    ((4, 64, 512), 64, 3.0, "auto"),     # within range: kept, larger scale
+    ((4, 64, 512), 256, 1e6, "auto"),
+    ((64, 64, 132), 256, 1e6, "auto"),   # the transposed-image pass (img.t)
+])
+def test_sampled_maxima_unsampled_outlier_every_row(dims, R, factor, path):
+    rng = np.random.default_rng(int(factor) + R + sum(dims))
+    Y = rng.uniform(0.5, 1.0, size=dims).astype(np.float32)
+    flat = Y.reshape(dims[0], -1)
+    flat[1, 1000] *= np.float32(factor)
+    A = [rng.uniform(0.0, 1.0, size=(n, R)).astype(np.float32) for n in dims]
+    plan = mk.Plan(dims, R, path)
+    assert any(k.startswith("img.") for k in kernels(plan, len(dims)))
+    got = run(Y, A, plan)
+    assert mk.device_status() == 0
+    for k in range(len(dims)):
+        err = worst_row_error(got[k], oracle.mttkrp(Y, A, k))
+        assert err <= TOL, f"{dims} R={R} factor={factor} mode {k}: worst row {err:.3e}"
+
+
+def test_sampled_maxima_zero_slab_and_nonfinite():
+    """A slab that is all zero next to ordinary ones; then an Inf that the sample
+    misses (the exact redo then takes scale 1, as the exact maxima always did)."""
+    dims, R = (4, 64, 512), 64
+    rng = np.random.default_rng(5)
+    Y = rng.uniform(-1.0, 1.0, size=dims).astype(np.float32)
+    Y[2] = 0.0
+    A = [rng.uniform(-1.0, 1.0, size=(n, R)).astype(np.float32) for n in dims]
+    plan = mk.Plan(dims, R)
+    got = run(Y, A, plan)
+    for k in range(3):
+        ref = oracle.mttkrp(Y, A, k)
+        assert np.linalg.norm(got[k] - ref) <= TOL * np.linalg.norm(ref)
+        if k == 0:
+            assert np.all(got[0][2] == 0.0)
+    Y.reshape(4, -1)[1, 1000] = np.inf
+    got = run(Y, A, plan)
+    assert mk.device_status() == 0
+    assert not np.isfinite(got[0][1]).all()     # the Inf reaches its row
+    assert np.isfinite(got[0][0]).all() and np.isfinite(got[0][3]).all()
