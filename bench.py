@@ -841,7 +841,9 @@ def run_ttm(args, w):
         probe = {"error": str(e)[:200]}
     kpk = kind_peaks(peaks, probe if "error" not in probe else None, props.multi_processor_count)
     # per mode: the tensor cores (fp16 split) where they take the shape, else the FMA pipe
-    kinds = ["fp16x2" if mk.ttm_workspace_bytes(w.dims, k, Js[k]) > 0 else "f32" for k in range(w.d)]
+    # the path mk.ttm(path="auto") takes: tensor cores when they take the shape and J >= 64
+    kinds = ["fp16x2" if Js[k] >= 64 and mk.ttm_workspace_bytes(w.dims, k, Js[k]) > 0 else "f32"
+             for k in range(w.d)]
     t_peak = sum(2.0 * J * numel / (kpk[kd] * 1e12) for J, kd in zip(Js, kinds))
     peak = flops / t_peak / 1e12
     cpu = None if args.no_cpu_baseline else ttm_cpu_baseline(Xh, Ms_h, args.cpu_seconds)

@@ -416,9 +416,10 @@ def ttm(X, mode: int, M, out=None, stream=None, path: str = "auto"):
     """T = X x_mode M: M is a float32 CUDA matrix J x X.shape[mode]; returns T
     (X's shape with that mode's size replaced by J), written into `out` when
     given (contiguous float32, not overlapping X or M).  path "simt": the CUDA-core
-    kernel (mttkrp_ttm); "auto": the tensor cores when they take the shape
-    (mttkrp_ttm_ws with a PyTorch-allocated workspace), else the CUDA cores; "tc":
-    the tensor cores or an error."""
+    kernel (mttkrp_ttm); "auto": the tensor cores when they take the shape and
+    J >= 64 (mttkrp_ttm_ws with a PyTorch-allocated workspace; below that the two
+    passes over X that the tensor-core path needs cost more than the CUDA cores'
+    arithmetic), else the CUDA cores; "tc": the tensor cores or an error."""
     import torch
     lib = load_library()
     for name, t in (("X", X), ("M", M)):
@@ -436,7 +437,8 @@ def ttm(X, mode: int, M, out=None, stream=None, path: str = "auto"):
     dims = (ctypes.c_int64 * X.dim())(*X.shape)
     if path not in ("auto", "simt", "tc"):
         raise ValueError(f"unknown path {path!r}")
-    need = 0 if path == "simt" else int(lib.mttkrp_ttm_workspace_bytes(X.dim(), dims, mode, int(M.shape[0])))
+    use_tc = path == "tc" or (path == "auto" and int(M.shape[0]) >= 64)
+    need = int(lib.mttkrp_ttm_workspace_bytes(X.dim(), dims, mode, int(M.shape[0]))) if use_tc else 0
     if path == "tc" and need == 0:
         raise MttkrpError(2, "ttm", "the tensor-core mode-n product does not take this shape")
     if need > 0:
