@@ -3106,6 +3106,96 @@ __global__ void tc_bimage_f16_kernel(BImgArgs a, const float* __restrict__ colsc
     }
 }
 
+// The same images built 32 rows (columns r) of one (n-tile, K-step) block at a
+// time: the KW x 32 values are formed in shared memory with the columns r
+// fastest (coalesced reads of the column scales and the group factors), then
+// each thread writes one 16-byte chunk of 8 values of a row of both images in
+// its swizzled place.  Grid: image blocks x (BN / 32) row groups.
+constexpr int kBimgRows = 32;
+
+template <int KW>
+__global__ void __launch_bounds__(256) tc_bimage_f16_tile_kernel(BImgArgs a, const float* __restrict__ colscale) {
+    static_assert(KW == 32 || KW == 64, "64- or 128-byte rows");
+    constexpr int kChunks = KW / 8;
+    constexpr int S = kBimgRows + 1;
+    __shared__ float vs[KW * S];   // [kk][row in the group]
+    const int BN = a.BN;
+    const int groups = BN / kBimgRows;
+    const int64_t total = a.nblocks * groups;
+    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+        const int64_t blk = t / groups;
+        const int rg = (int)(t - blk * groups);
+        const int64_t nt = blk / a.KS;
+        const int ks = (int)(blk - nt * a.KS);
+        for (int e = threadIdx.x; e < KW * kBimgRows; e += blockDim.x) {
+            const int kk = e / kBimgRows, rl = e - kk * kBimgRows;
+            const int64_t r = nt * BN + rg * kBimgRows + rl;
+            int64_t j;
+            bool valid;
+            if (a.inner) {
+                j = (int64_t)ks * KW + kk;
+                valid = j < a.J;
+            } else {
+                const int jp = ks / a.jq_steps;
+                const int64_t jq = (int64_t)(ks - jp * a.jq_steps) * KW + kk;
+                valid = jq < a.Jq;
+                j = (int64_t)jp * a.Jq + jq;
+            }
+            float v = 0.f;
+            if (valid && r < a.R) {
+                v = colscale[r];
+                if (a.ngroup == 1) {
+                    v *= a.gfac[0][j * a.R + r];
+                } else {
+                    int64_t rem = j;
+                    for (int m = a.ngroup - 1; m >= 0; --m) {
+                        const int64_t idx = rem % a.gdim[m];
+                        rem /= a.gdim[m];
+                        v *= a.gfac[m][idx * a.R + r];
+                    }
+                }
+            }
+            vs[kk * S + rl] = v;
+        }
+        __syncthreads();
+        __half* out = reinterpret_cast<__half*>(a.out) + blk * (int64_t)(2 * BN * KW);
+        for (int w = threadIdx.x; w < kBimgRows * kChunks; w += blockDim.x) {
+            const int rl = w / kChunks, c = w - rl * kChunks;
+            const int rr = rg * kBimgRows + rl;
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float v0 = vs[(8 * c + 2 * q) * S + rl], v1 = vs[(8 * c + 2 * q + 1) * S + rl];
+                const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+                const __half l0 = __float2half_rn(v0 - __half2float(h0)), l1 = __float2half_rn(v1 - __half2float(h1));
+                hw[q] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+                lw[q] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+            }
+            const int pos = KW == 32 ? ((c ^ (rr >> 1)) & 3) : ((c ^ rr) & 7);
+            *reinterpret_cast<uint4*>(out + (int64_t)rr * KW + pos * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(out + (int64_t)BN * KW + (int64_t)rr * KW + pos * 8) =
+                make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        __syncthreads();
+    }
+}
+
+// launch helper: the tile kernel for tiles of whole 32-row groups, else the
+// element-wise one
+template <int KW>
+cudaError_t launch_bimage_f16(const BImgArgs& b, const float* colscale, cudaStream_t stream) {
+    if (b.BN % kBimgRows == 0 && (reinterpret_cast<uintptr_t>(b.out) & 15) == 0) {
+        int64_t blocks = b.nblocks * (b.BN / kBimgRows);
+        if (blocks > 152 * 8) blocks = 152 * 8;
+        tc_bimage_f16_tile_kernel<KW><<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, stream>>>(b, colscale);
+        return cudaGetLastError();
+    }
+    int64_t blocks = (b.nblocks * 2 * b.BN * KW + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    tc_bimage_f16_kernel<KW><<<(unsigned)blocks, 256, 0, stream>>>(b, colscale);
+    return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------------------
 // The explicit Khatri-Rao product (matrix-based comparison variant), written
 // as the B images the tensor-core kernels stream: row j of the product (j over
@@ -3953,13 +4043,15 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
         const int64_t n = b.nblocks * 2 * mp.bn * mp.tc_kw;
         int64_t blocks = cdiv64(n, 256);
         if (blocks > 152 * 16) blocks = 152 * 16;
-        if (mp.tc_img)
-            tc_bimage_f16_kernel<kBK4><<<(unsigned)blocks, 256, 0, stream>>>(b, colscale);
-        else if (mp.tc_h2)
-            tc_bimage_f16_kernel<kBK2><<<(unsigned)blocks, 256, 0, stream>>>(b, colscale);
-        else
+        cudaError_t e;
+        if (mp.tc_img) {
+            e = launch_bimage_f16<kBK4>(b, colscale, stream);
+        } else if (mp.tc_h2) {
+            e = launch_bimage_f16<kBK2>(b, colscale, stream);
+        } else {
             tc_bimage_kernel<<<(unsigned)blocks, 256, 0, stream>>>(b);
-        cudaError_t e = cudaGetLastError();
+            e = cudaGetLastError();
+        }
         if (e != cudaSuccess) {
             snprintf(errbuf, errlen, "B image launch: %s", cudaGetErrorString(e));
             return MTTKRP_ERR_CUDA;
@@ -4205,10 +4297,7 @@ int tc_ttm_run(const float* X, const float* M, float* T, int64_t P, int64_t N, i
         b.inner = 1;
         b.nblocks = cdiv64(J, l.bn) * l.ks;
         b.out = bimg;
-        int64_t blocks = cdiv64(b.nblocks * 2 * l.bn * kBK4, 256);
-        if (blocks > 152 * 16) blocks = 152 * 16;
-        tc_bimage_f16_kernel<kBK4><<<(unsigned)blocks, 256, 0, stream>>>(b, colscale);
-        e = cudaGetLastError();
+        e = launch_bimage_f16<kBK4>(b, colscale, stream);
     }
     if (e != cudaSuccess) {
         snprintf(errbuf, errlen, "mode-n product preparation: %s", cudaGetErrorString(e));
