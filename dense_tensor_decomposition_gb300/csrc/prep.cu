@@ -10,17 +10,24 @@
 
 namespace mk {
 
-// One warp per table row: the row's multi-index, Y offset and scale once, then
-// the R columns by the lanes (coalesced loads and stores; 16-byte ones when R
-// is a multiple of 4 and every factor is 16-byte aligned).  NM = the number of
-// factors in the product (a template argument, so that the per-column loop
-// holds only its loads and multiplies).
+// One warp per (table row, run of 128 columns): the row's multi-index, Y offset
+// and scale, then its columns by the lanes (coalesced; 16-byte loads and stores
+// when R is a multiple of 4 and every factor is 16-byte aligned: a run is then
+// 128 float4).  Splitting rows into runs keeps tables of few long rows (a single
+// pre mode at a large rank) spread over the GPU.  NM = the number of factors in
+// the product (a template argument, so that the per-column loop holds only its
+// loads and multiplies).
 template <int NM, bool V4>
 __global__ void __launch_bounds__(256) prod_table_kernel(ProdTableArgs a) {
     const int lane = threadIdx.x & 31;
+    constexpr int64_t kRun = 128;   // float4 groups (V4) or columns a run
+    const int64_t units = V4 ? a.R / 4 : a.R;
+    const int64_t runs = (units + kRun - 1) / kRun;
+    const int64_t tasks = a.rows * runs;
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < a.rows;
-         row += nwarps) {
+    for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < tasks;
+         task += nwarps) {
+        const int64_t row = task / runs, run = task - row * runs;
         const float* frow[NM > 0 ? NM : 1];
         int64_t rem = row, base = 0;
 #pragma unroll
@@ -34,9 +41,9 @@ __global__ void __launch_bounds__(256) prod_table_kernel(ProdTableArgs a) {
         if (a.slab_bits != nullptr)
             f = pow2_scale(*a.gmax_bits) * pow2_recip(slab_scale(a.slab_bits, row / a.slab_div, *a.gmax_bits));
         float* out = a.tab + row * a.R;
+        const int64_t u1 = (run + 1) * kRun < units ? (run + 1) * kRun : units;
         if (V4) {
-            const int64_t R4 = a.R / 4;
-            for (int64_t c = lane; c < R4; c += 32) {
+            for (int64_t c = run * kRun + lane; c < u1; c += 32) {
                 float4 p = make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
                 for (int m = NM - 1; m >= 0; --m) {
@@ -49,14 +56,14 @@ __global__ void __launch_bounds__(256) prod_table_kernel(ProdTableArgs a) {
                 reinterpret_cast<float4*>(out)[c] = make_float4(p.x * f, p.y * f, p.z * f, p.w * f);
             }
         } else {
-            for (int64_t r = lane; r < a.R; r += 32) {
+            for (int64_t r = run * kRun + lane; r < u1; r += 32) {
                 float p = 1.f;
 #pragma unroll
                 for (int m = NM - 1; m >= 0; --m) p *= __ldg(frow[m] + r);
                 out[r] = p * f;
             }
         }
-        if (a.base != nullptr && lane == 0) a.base[row] = base;
+        if (a.base != nullptr && run == 0 && lane == 0) a.base[row] = base;
     }
 }
 
@@ -71,10 +78,11 @@ cudaError_t launch_prod_table_nm(const ProdTableArgs& a, bool v4, unsigned block
 
 cudaError_t launch_prod_table(const ProdTableArgs& a, cudaStream_t s) {
     if (a.rows * a.R == 0) return cudaSuccess;
-    int64_t blocks = (a.rows + 7) / 8;   // eight warps, one row each
-    if (blocks > 152 * 16) blocks = 152 * 16;
     bool v4 = a.R % 4 == 0 && (reinterpret_cast<uintptr_t>(a.tab) & 15) == 0;
     for (int m = 0; m < a.nm; ++m) v4 = v4 && (reinterpret_cast<uintptr_t>(a.fac[m]) & 15) == 0;
+    const int64_t units = v4 ? a.R / 4 : a.R;
+    int64_t blocks = (a.rows * ((units + 127) / 128) + 7) / 8;   // eight warps, one (row, run) each
+    if (blocks > 152 * 16) blocks = 152 * 16;
     const unsigned b = (unsigned)blocks;
     static_assert(kMaxD == 8, "one instantiation per factor count");
     switch (a.nm) {
@@ -178,7 +186,7 @@ __global__ void __launch_bounds__(kRedThreads)
     }
 }
 
-// One thread per 4 consecutive outputs, all splits in increasing s with four
+// One thread per 4 consecutive outputs, all splits in increasing s with eight
 // 16-byte loads in flight (used when there are enough outputs to fill the GPU
 // this way; no shared memory, no block barriers).
 __global__ void __launch_bounds__(256)
@@ -189,12 +197,12 @@ __global__ void __launch_bounds__(256)
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
         const float4* p = part + e;
         int64_t sp = 0;
-        for (; sp + 4 <= splits; sp += 4) {
-            float4 v[4];
+        for (; sp + 8 <= splits; sp += 8) {   // eight 16-byte loads in flight
+            float4 v[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = __ldcs(p + (sp + u) * n4);
+            for (int u = 0; u < 8; ++u) v[u] = __ldcs(p + (sp + u) * n4);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 kahan_add(s0, c0, v[u].x);
                 kahan_add(s1, c1, v[u].y);
                 kahan_add(s2, c2, v[u].z);
