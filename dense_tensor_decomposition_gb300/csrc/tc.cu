@@ -3941,23 +3941,34 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
         estr[t] = 1;
         if (t > 0) gstride[t - 1] = mg.stride_el[t] * esize;
     }
+    // L2 promotion: a copy's L2 fills are widened to 256 bytes, which prefetches
+    // the next K-step of the same rows when rows and strides are 256-byte
+    // multiples; with shorter or unaligned rows (e.g. 800-byte rows of 400
+    // fp16) the widened fills straddle rows and the data is fetched about twice,
+    // so the fill width follows the alignment of the row length and strides
+    uint64_t align = (uint64_t)gdim[0] * esize;
+    for (int t = 0; t + 1 < mg.rank; ++t) align |= (uint64_t)gstride[t];
+    const CUtensorMapL2promotion promo = (align % 256 == 0)   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                         : (align % 128 == 0) ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                         : (align % 64 == 0)  ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B
+                                                              : CU_TENSOR_MAP_L2_PROMOTION_NONE;
     CUresult cr;
     if (mp.tc_img) {
         // 64 fp16 = 128-byte rows, 128-byte swizzle (the MMA descriptors' layout)
         cr = encode(&args.ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)mg.rank, map_hi, gdim, gstride,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (cr == CUDA_SUCCESS)
             cr = encode(&args.ymap_lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)mg.rank, map_lo, gdim,
-                        gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
         cr = encode(&args.ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)mg.rank, const_cast<float*>(Y),
                     gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     mp.tc_inner ? CU_TENSOR_MAP_SWIZZLE_NONE
                     : mp.tc_h2  ? CU_TENSOR_MAP_SWIZZLE_128B   // 32 fp32 = 128-byte rows
                                 : CU_TENSOR_MAP_SWIZZLE_64B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (cr != CUDA_SUCCESS) {
         snprintf(errbuf, errlen, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
