@@ -790,9 +790,12 @@ def run_rotations(args, w):
 
 def run_ttm(args, w):
     """The dense mode-n product along every mode of the workload's tensor per
-    step (mttkrp_ttm), each mode into its own preallocated result.  One JSON
-    line: TFLOP/s (2 J I_1..I_d flops per mode) against the fp32 FMA pipe, with
-    the HBM time of the algorithmic bytes beside it."""
+    step, one mttkrp_ttm_multi call (the tensor-core products share one pass
+    that writes the fp16 images of X), each mode into its own preallocated
+    result.  One JSON line: TFLOP/s (2 J I_1..I_d flops per mode) against the
+    flop-weighted peak of the pipes the products run on, with the HBM time of
+    the algorithmic bytes beside it; ms_per_mode times each product alone
+    (mttkrp_ttm_ws, its own image pass included)."""
     import numpy as np
     import torch
     import dense_tensor_decomposition_gb300 as mk
@@ -806,9 +809,12 @@ def run_ttm(args, w):
     Ms = [torch.from_numpy(m).to(device) for m in Ms_h]
     outs = [torch.empty(list(w.dims[:k]) + [Js[k]] + list(w.dims[k + 1:]), device=device) for k in range(w.d)]
 
+    modes = list(range(w.d))
+    need = mk.ttm_multi_workspace_bytes(w.dims, modes, Js) if max(Js) >= 64 else 0
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+
     def step():
-        for k in range(w.d):
-            mk.ttm(X, k, Ms[k], out=outs[k])
+        mk.ttm_multi(X, modes, Ms, outs=outs, workspace=ws if need else None)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -840,9 +846,10 @@ def run_ttm(args, w):
     except Exception as e:
         probe = {"error": str(e)[:200]}
     kpk = kind_peaks(peaks, probe if "error" not in probe else None, props.multi_processor_count)
-    # per mode: the tensor cores (fp16 split) where they take the shape, else the FMA pipe
-    # the path mk.ttm(path="auto") takes: tensor cores when they take the shape and J >= 64
-    kinds = ["fp16x2" if Js[k] >= 64 and mk.ttm_workspace_bytes(w.dims, k, Js[k]) > 0 else "f32"
+    # per mode: the tensor cores (fp16 split) where they take the shape, else the
+    # FMA pipe; ttm_multi(path="auto") takes them for every product they take
+    # once some J >= 64
+    kinds = ["fp16x2" if need and mk.ttm_workspace_bytes(w.dims, k, Js[k]) > 0 else "f32"
              for k in range(w.d)]
     t_peak = sum(2.0 * J * numel / (kpk[kd] * 1e12) for J, kd in zip(Js, kinds))
     peak = flops / t_peak / 1e12

@@ -20,7 +20,8 @@ import threading
 
 from ._build import LIB as LIB_PATH, build  # noqa: F401
 
-__all__ = ["Plan", "mttkrp", "all_modes", "apply_rotations", "ttm", "ttm_workspace_bytes", "probe_fma", "probe_mma",
+__all__ = ["Plan", "mttkrp", "all_modes", "apply_rotations", "ttm", "ttm_workspace_bytes", "ttm_multi",
+           "ttm_multi_workspace_bytes", "probe_fma", "probe_mma",
            "MttkrpError",
            "build", "load_library",
            "exported_symbols", "PATH_AUTO", "PATH_SIMT", "PATH_TC", "PATH_TC_TF32", "PATH_TC_EXPLICIT_KRP"]
@@ -90,6 +91,10 @@ def load_library():
         lib.mttkrp_ttm_workspace_bytes.restype = sz
         lib.mttkrp_ttm_ws.argtypes = [ci, vp, vp, ci, vp, i64, vp, vp, sz, vp]
         lib.mttkrp_ttm_ws.restype = ci
+        lib.mttkrp_ttm_multi_workspace_bytes.argtypes = [ci, vp, ci, vp, vp]
+        lib.mttkrp_ttm_multi_workspace_bytes.restype = sz
+        lib.mttkrp_ttm_multi.argtypes = [ci, vp, vp, ci, vp, vp, vp, vp, vp, sz, vp]
+        lib.mttkrp_ttm_multi.restype = ci
         lib.mttkrp_cp_als_scratch_bytes.argtypes = [vp]
         lib.mttkrp_cp_als_scratch_bytes.restype = sz
         lib.mttkrp_cp_als_sweep.argtypes = [vp, vp, vp, vp, vp, ci, vp, vp, sz, vp]
@@ -451,6 +456,81 @@ def ttm(X, mode: int, M, out=None, stream=None, path: str = "auto"):
                           int(M.shape[0]), ctypes.c_void_p(out.data_ptr()), _stream_handle(X.device, stream)),
            "mttkrp_ttm")
     return out
+
+
+def ttm_multi_workspace_bytes(shape, modes, Js) -> int:
+    """Workspace bytes of several tensor-core mode-n products of one tensor (the
+    images of X once plus the largest per-product region; 0: none is taken)."""
+    n = len(modes)
+    dims = (ctypes.c_int64 * len(shape))(*shape)
+    cm = (ctypes.c_int * n)(*[int(m) for m in modes])
+    cj = (ctypes.c_int64 * n)(*[int(j) for j in Js])
+    return int(load_library().mttkrp_ttm_multi_workspace_bytes(len(shape), dims, n, cm, cj))
+
+
+def ttm_multi(X, modes, Ms, outs=None, stream=None, path: str = "auto", workspace=None):
+    """T_t = X x_{modes[t]} Ms[t] for every t (mttkrp_ttm_multi): the products a
+    Tucker form takes of one tensor, the tensor-core ones sharing one pass that
+    writes X's fp16 images.  Ms: float32 CUDA matrices J_t x X.shape[modes[t]];
+    returns the list of results (written into `outs` when given).  path "simt":
+    every product on the CUDA cores; "auto": the tensor cores for every product
+    they take when some J_t >= 64, else the CUDA cores; "tc": the tensor cores
+    for every product or an error.  workspace: a uint8 CUDA tensor of at least
+    ttm_multi_workspace_bytes() bytes to use instead of a fresh allocation."""
+    import torch
+    lib = load_library()
+    modes = [int(m) for m in modes]
+    Ms = list(Ms)
+    n = len(modes)
+    if n < 1 or len(Ms) != n:
+        raise ValueError("modes and Ms must be non-empty and of the same length")
+    if not isinstance(X, torch.Tensor) or not X.is_cuda or X.dtype != torch.float32 or not X.is_contiguous():
+        raise TypeError("X must be a contiguous float32 CUDA tensor")
+    shapes = []
+    for t, (m, M) in enumerate(zip(modes, Ms)):
+        if not isinstance(M, torch.Tensor) or not M.is_cuda or M.dtype != torch.float32 or not M.is_contiguous():
+            raise TypeError(f"Ms[{t}] must be a contiguous float32 CUDA tensor")
+        if M.device != X.device or M.dim() != 2 or not 0 <= m < X.dim() or M.shape[1] != X.shape[m]:
+            raise ValueError(f"Ms[{t}] must be J x X.shape[{m}] on X's device")
+        shape = list(X.shape)
+        shape[m] = int(M.shape[0])
+        shapes.append(shape)
+    if outs is None:
+        outs = [torch.empty(sh, dtype=torch.float32, device=X.device) for sh in shapes]
+    else:
+        outs = list(outs)
+        if len(outs) != n:
+            raise ValueError("outs must hold one tensor per product")
+        for t, (o, sh) in enumerate(zip(outs, shapes)):
+            if (not isinstance(o, torch.Tensor) or o.device != X.device or o.dtype != torch.float32
+                    or not o.is_contiguous() or list(o.shape) != sh):
+                raise ValueError(f"outs[{t}] must be a contiguous float32 CUDA tensor of shape {sh}")
+    if path not in ("auto", "simt", "tc"):
+        raise ValueError(f"unknown path {path!r}")
+    Js = [int(M.shape[0]) for M in Ms]
+    dims = (ctypes.c_int64 * X.dim())(*X.shape)
+    cm = (ctypes.c_int * n)(*modes)
+    cj = (ctypes.c_int64 * n)(*Js)
+    cM = (ctypes.c_void_p * n)(*[M.data_ptr() for M in Ms])
+    cT = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
+    use_tc = path == "tc" or (path == "auto" and max(Js) >= 64)
+    need = int(lib.mttkrp_ttm_multi_workspace_bytes(X.dim(), dims, n, cm, cj)) if use_tc else 0
+    if path == "tc":
+        for t in range(n):
+            if int(lib.mttkrp_ttm_workspace_bytes(X.dim(), dims, modes[t], Js[t])) == 0:
+                raise MttkrpError(2, "ttm_multi", f"the tensor-core mode-n product does not take product {t}")
+    if need > 0 and workspace is not None:
+        if (not isinstance(workspace, torch.Tensor) or workspace.device != X.device
+                or workspace.dtype != torch.uint8 or not workspace.is_contiguous()):
+            raise TypeError("workspace must be a contiguous uint8 CUDA tensor on X's device")
+        ws, ws_bytes = workspace, workspace.numel()
+    else:
+        ws = torch.empty(need, dtype=torch.uint8, device=X.device) if need > 0 else None
+        ws_bytes = need
+    _check(lib.mttkrp_ttm_multi(X.dim(), dims, ctypes.c_void_p(X.data_ptr()), n, cm, cM, cj, cT,
+                                ctypes.c_void_p(ws.data_ptr()) if ws is not None else None, ws_bytes,
+                                _stream_handle(X.device, stream)), "mttkrp_ttm_multi")
+    return outs
 
 
 def probe_fma(blocks: int, iters: int, out, stream=None):

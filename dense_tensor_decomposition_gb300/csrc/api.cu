@@ -745,6 +745,69 @@ int mttkrp_ttm_ws(int d, const int64_t* dims, const float* X, int mode, const fl
     return MTTKRP_OK;
 }
 
+size_t mttkrp_ttm_multi_workspace_bytes(int d, const int64_t* dims, int nmodes, const int* modes,
+                                        const int64_t* Js) {
+    if (nmodes < 1 || nmodes > 64 || modes == nullptr || Js == nullptr) return 0;
+    size_t need = 0;
+    for (int t = 0; t < nmodes; ++t) {
+        const size_t b = mttkrp_ttm_workspace_bytes(d, dims, modes[t], Js[t]);
+        if (b > need) need = b;   // images at the same offsets for every product of one X
+    }
+    return need;
+}
+
+int mttkrp_ttm_multi(int d, const int64_t* dims, const float* X, int nmodes, const int* modes,
+                     const float* const* Ms, const int64_t* Js, float* const* Ts, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+    g_errmsg[0] = 0;
+    if (nmodes < 1 || nmodes > 64) return fail(MTTKRP_ERR_INVALID, "nmodes=%d outside [1, 64]", nmodes);
+    if (modes == nullptr || Ms == nullptr || Js == nullptr || Ts == nullptr)
+        return fail(MTTKRP_ERR_INVALID, "NULL modes, matrices, row counts or results");
+    int64_t P[64], N[64], Q[64];
+    size_t need[64];
+    for (int t = 0; t < nmodes; ++t) {
+        const int rc = ttm_check(d, dims, X, modes[t], Ms[t], Js[t], Ts[t], &P[t], &N[t], &Q[t]);
+        if (rc != MTTKRP_OK) return rc;
+        need[t] = tc_ttm_workspace_bytes(P[t], N[t], Q[t], Js[t]);
+    }
+    // a later product must not overwrite an earlier one's result or matrix
+    for (int t = 0; t < nmodes; ++t) {
+        const uintptr_t t0 = reinterpret_cast<uintptr_t>(Ts[t]), t1 = t0 + (uintptr_t)(P[t] * Js[t] * Q[t]) * 4;
+        for (int u = 0; u < nmodes; ++u) {
+            if (u == t) continue;
+            const uintptr_t u0 = reinterpret_cast<uintptr_t>(Ts[u]), u1 = u0 + (uintptr_t)(P[u] * Js[u] * Q[u]) * 4;
+            const uintptr_t m0 = reinterpret_cast<uintptr_t>(Ms[u]), m1 = m0 + (uintptr_t)(Js[u] * N[u]) * 4;
+            if ((t0 < u1 && u0 < t1) || (t0 < m1 && m0 < t1))
+                return fail(MTTKRP_ERR_INVALID, "result %d overlaps result or matrix %d", t, u);
+        }
+    }
+    size_t need_all = 0;
+    for (int t = 0; t < nmodes; ++t) need_all = need[t] > need_all ? need[t] : need_all;
+    if (workspace != nullptr && need_all > 0 && workspace_bytes < need_all)
+        return fail(MTTKRP_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes needed", workspace_bytes,
+                    need_all);
+    const bool tc_ok = workspace != nullptr && (reinterpret_cast<uintptr_t>(X) & 15) == 0 &&
+                       (reinterpret_cast<uintptr_t>(workspace) & 255) == 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool images = false;
+    for (int t = 0; t < nmodes; ++t) {
+        if (tc_ok && need[t] > 0) {
+            if (!images) {
+                const int rc = tc_ttm_images(X, P[t] * N[t] * Q[t], workspace, s, g_errmsg, sizeof(g_errmsg));
+                if (rc != MTTKRP_OK) return rc;
+                images = true;
+            }
+            const int rc = tc_ttm_product(Ms[t], Ts[t], P[t], N[t], Q[t], Js[t], workspace, s, g_errmsg,
+                                          sizeof(g_errmsg));
+            if (rc != MTTKRP_OK) return rc;
+        } else {
+            cudaError_t e = launch_ttm(X, Ms[t], Ts[t], P[t], N[t], Q[t], Js[t], s);
+            if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "mode-n product launch: %s", cudaGetErrorString(e));
+        }
+    }
+    return MTTKRP_OK;
+}
+
 size_t mttkrp_cp_als_scratch_bytes(mttkrp_plan_t h) {
     Plan* p = as_plan(h);
     return p == nullptr ? 0 : cp_als_layout(*p).total;

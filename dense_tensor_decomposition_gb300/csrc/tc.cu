@@ -4200,7 +4200,12 @@ bool ttm_layout(int64_t P, int64_t N, int64_t Q, int64_t J, TtmLayout& l) {
     l.bn = J <= 64 ? 64 : (cdiv64(J, 256) * 256 * 20 <= cdiv64(J, 128) * 128 * 23 ? 256 : 128);
     l.ks = (int)cdiv64(N, kBK4);
     auto a256 = [](size_t x) { return (x + 255) / 256 * 256; };
-    size_t off = 512;   // max |X| at 0, the single slab maximum at 256
+    // [max |X| at 0, the single slab maximum and the range flag at 256]
+    // [fp16 images of X: shared by every product of one X] [this product's M^T,
+    // ones, B images, column scales]
+    size_t off = 512;
+    l.off_img = off;
+    off += 2 * a256((size_t)numel * 2);
     l.off_mt = off;
     off = a256(off + (size_t)N * J * 4);
     l.off_ones = off;
@@ -4209,8 +4214,6 @@ bool ttm_layout(int64_t P, int64_t N, int64_t Q, int64_t J, TtmLayout& l) {
     off = a256(off + (size_t)cdiv64(J, l.bn) * l.ks * 2 * l.bn * 128);
     l.off_colscale = off;
     off = a256(off + (size_t)J * 4);
-    l.off_img = off;
-    off += 2 * a256((size_t)numel * 2);
     l.total = off;
     return true;
 }
@@ -4221,45 +4224,23 @@ size_t tc_ttm_workspace_bytes(int64_t P, int64_t N, int64_t Q, int64_t J) {
     return ttm_layout(P, N, Q, J, l) ? l.total : 0;
 }
 
-int tc_ttm_run(const float* X, const float* M, float* T, int64_t P, int64_t N, int64_t Q, int64_t J, void* ws,
-               cudaStream_t stream, char* errbuf, size_t errlen) {
-    TtmLayout l;
-    if (!ttm_layout(P, N, Q, J, l)) {
-        snprintf(errbuf, errlen, "the tensor-core mode-n product does not take this shape");
-        return MTTKRP_ERR_UNSUPPORTED;
-    }
+// The fp16 images of X (hi and lo at 512 and 512 + half) with one power-of-two
+// scale from the sampled maximum, checked, redone exactly if the check fired
+// (as in tc_prepare).  Shared by every product of one X.
+int tc_ttm_images(const float* X, int64_t numel, void* ws, cudaStream_t stream, char* errbuf, size_t errlen) {
     if ((reinterpret_cast<uintptr_t>(X) & 15) != 0 || (reinterpret_cast<uintptr_t>(ws) & 255) != 0) {
         snprintf(errbuf, errlen, "the tensor-core mode-n product needs a 16-byte aligned X and a 256-byte aligned workspace");
         return MTTKRP_ERR_INVALID;
     }
-    PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
-    uint32_t* status = tc_status_ptr();
-    if (encode == nullptr || status == nullptr) {
-        snprintf(errbuf, errlen, "tensor-map encoder or status word unavailable");
-        return MTTKRP_ERR_CUDA;
-    }
     uint8_t* base = static_cast<uint8_t*>(ws);
     uint32_t* ymax = reinterpret_cast<uint32_t*>(base);
     uint32_t* slab = reinterpret_cast<uint32_t*>(base + 256);
-    float* mt = reinterpret_cast<float*>(base + l.off_mt);
-    float* ones = reinterpret_cast<float*>(base + l.off_ones);
-    float* bimg = reinterpret_cast<float*>(base + l.off_bimg);
-    float* colscale = reinterpret_cast<float*>(base + l.off_colscale);
-    const int64_t numel = P * N * Q;
+    uint32_t* ovf = slab + 1;
     const size_t img_half = ((size_t)numel * 2 + 255) / 256 * 256;
-    __half* img_hi = reinterpret_cast<__half*>(base + l.off_img);
-    __half* img_lo = reinterpret_cast<__half*>(base + l.off_img + img_half);
+    __half* img_hi = reinterpret_cast<__half*>(base + 512);
+    __half* img_lo = reinterpret_cast<__half*>(base + 512 + img_half);
     cudaError_t e = cudaMemsetAsync(base, 0, 512, stream);
     if (e == cudaSuccess) {
-        int64_t blocks = cdiv64(J * N, 256);
-        if (blocks > 152 * 8) blocks = 152 * 8;
-        ttm_prep_kernel<<<(unsigned)blocks, 256, 0, stream>>>(M, J, N, mt, ones);
-        e = cudaGetLastError();
-    }
-    if (e == cudaSuccess) {
-        // sampled maximum, image pass with the out-of-range check, exact redo
-        // only if the check fired (as in tc_prepare)
-        uint32_t* ovf = slab + 1;
         int64_t blocks = cdiv64(cdiv64(numel, kSlabUnit), 4);
         if (blocks > 152 * 8) blocks = 152 * 8;
         const int64_t nch = cdiv64(numel, kSampleChunk);
@@ -4281,6 +4262,58 @@ int tc_ttm_run(const float* X, const float* M, float* T, int64_t P, int64_t N, i
                                                                      ovf);
             e = cudaGetLastError();
         }
+    }
+    if (e != cudaSuccess) {
+        snprintf(errbuf, errlen, "mode-n product image pass: %s", cudaGetErrorString(e));
+        return MTTKRP_ERR_CUDA;
+    }
+    return MTTKRP_OK;
+}
+
+int tc_ttm_run(const float* X, const float* M, float* T, int64_t P, int64_t N, int64_t Q, int64_t J, void* ws,
+               cudaStream_t stream, char* errbuf, size_t errlen) {
+    TtmLayout l;
+    if (!ttm_layout(P, N, Q, J, l)) {
+        snprintf(errbuf, errlen, "the tensor-core mode-n product does not take this shape");
+        return MTTKRP_ERR_UNSUPPORTED;
+    }
+    const int rc = tc_ttm_images(X, P * N * Q, ws, stream, errbuf, errlen);
+    if (rc != MTTKRP_OK) return rc;
+    return tc_ttm_product(M, T, P, N, Q, J, ws, stream, errbuf, errlen);
+}
+
+// One product on images tc_ttm_images wrote into ws: M^T and its B images, then
+// the image kernel with the mode-n-product epilogue.
+int tc_ttm_product(const float* M, float* T, int64_t P, int64_t N, int64_t Q, int64_t J, void* ws,
+                   cudaStream_t stream, char* errbuf, size_t errlen) {
+    TtmLayout l;
+    if (!ttm_layout(P, N, Q, J, l)) {
+        snprintf(errbuf, errlen, "the tensor-core mode-n product does not take this shape");
+        return MTTKRP_ERR_UNSUPPORTED;
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+    uint32_t* status = tc_status_ptr();
+    if (encode == nullptr || status == nullptr) {
+        snprintf(errbuf, errlen, "tensor-map encoder or status word unavailable");
+        return MTTKRP_ERR_CUDA;
+    }
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    uint32_t* ymax = reinterpret_cast<uint32_t*>(base);
+    uint32_t* slab = reinterpret_cast<uint32_t*>(base + 256);
+    float* mt = reinterpret_cast<float*>(base + l.off_mt);
+    float* ones = reinterpret_cast<float*>(base + l.off_ones);
+    float* bimg = reinterpret_cast<float*>(base + l.off_bimg);
+    float* colscale = reinterpret_cast<float*>(base + l.off_colscale);
+    const int64_t numel = P * N * Q;
+    const size_t img_half = ((size_t)numel * 2 + 255) / 256 * 256;
+    __half* img_hi = reinterpret_cast<__half*>(base + l.off_img);
+    __half* img_lo = reinterpret_cast<__half*>(base + l.off_img + img_half);
+    cudaError_t e;
+    {
+        int64_t blocks = cdiv64(J * N, 256);
+        if (blocks > 152 * 8) blocks = 152 * 8;
+        ttm_prep_kernel<<<(unsigned)blocks, 256, 0, stream>>>(M, J, N, mt, ones);
+        e = cudaGetLastError();
     }
     if (e == cudaSuccess) {
         ColScaleArgs c;

@@ -34,6 +34,14 @@ cudaError_t tc_launch_mma_probe(int kind, int blocks, int iters, cudaStream_t s)
 size_t tc_ttm_workspace_bytes(int64_t P, int64_t N, int64_t Q, int64_t J);
 int tc_ttm_run(const float* X, const float* M, float* T, int64_t P, int64_t N, int64_t Q, int64_t J, void* ws,
                cudaStream_t stream, char* errbuf, size_t errlen);
+// The same in two parts, so that several products of one X share the first:
+// tc_ttm_images writes the fp16 images of X (numel elements) and their scale at
+// the start of ws; tc_ttm_product runs one product on them.  Every product of
+// one X places the images at the same offset, so the workspace of several is
+// the largest tc_ttm_workspace_bytes among them.
+int tc_ttm_images(const float* X, int64_t numel, void* ws, cudaStream_t stream, char* errbuf, size_t errlen);
+int tc_ttm_product(const float* M, float* T, int64_t P, int64_t N, int64_t Q, int64_t J, void* ws,
+                   cudaStream_t stream, char* errbuf, size_t errlen);
 // Device address of the error word on the current device (null on failure).
 uint32_t* tc_status_ptr();
 // Arm the failure-detection test hook for the next `count` launches.

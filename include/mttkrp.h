@@ -298,6 +298,36 @@ int mttkrp_ttm_ws(int d, const int64_t* dims, const float* X, int mode, const fl
                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Several mode-n products of one tensor: T_t = X x_{modes[t]} Ms[t] for t <
+ * nmodes (a Tucker form applies one product per mode, "An HPC Approach to
+ * Accelerate Tensor Decompositions", §2, eq. (2)).  Each product is the one
+ * mttkrp_ttm defines; the tensor-core products share one pass that writes the
+ * fp16 images of X (and its scale), which is where the saving lies.
+ *   mttkrp_ttm_multi_workspace_bytes: workspace bytes (device) for the products
+ *     the tensor-core path takes: the images of X once plus the largest
+ *     per-product region.  0 when none of them is taken, or for invalid
+ *     arguments.
+ *   mttkrp_ttm_multi: d, dims, X as mttkrp_ttm; modes (host, nmodes entries, each
+ *     in [0, d), repeats allowed), Ms (host array of nmodes device pointers, Ms[t]
+ *     Js[t] x dims[modes[t]] row-major), Js (host, nmodes entries >= 1), Ts (host
+ *     array of nmodes device pointers, Ts[t] the result of product t, laid out as
+ *     mttkrp_ttm's T; no T may overlap X, any M or another T).  workspace and
+ *     workspace_bytes as mttkrp_ttm_ws: a product the tensor-core path takes runs
+ *     there when the workspace is given and large enough and X is 16-byte aligned;
+ *     every other product runs mttkrp_ttm's CUDA-core kernel.  The products are
+ *     enqueued in order on `stream`; the call returns without waiting.
+ * Errors: MTTKRP_ERR_INVALID (nmodes < 1 or above 64, NULL arrays, any product's
+ * arguments as mttkrp_ttm checks them, overlapping results; nothing is enqueued),
+ * MTTKRP_ERR_WORKSPACE (a workspace given but smaller than the bytes needed;
+ * nothing is enqueued), MTTKRP_ERR_CUDA.
+ */
+size_t mttkrp_ttm_multi_workspace_bytes(int d, const int64_t* dims, int nmodes, const int* modes,
+                                        const int64_t* Js);
+int mttkrp_ttm_multi(int d, const int64_t* dims, const float* X, int nmodes, const int* modes,
+                     const float* const* Ms, const int64_t* Js, float* const* Ts, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
  * Peak probes for the roofline of a benchmark (measurement only; the pages have
  * no counterpart).  Both enqueue one kernel on `stream` and return; the caller
  * times it with events.

@@ -199,3 +199,50 @@ def test_rotations_reject_invalid_before_any_launch(lib, d, dims, mode, G, why):
     f = _fake(0x1000)
     assert lib.mttkrp_apply_rotations(d, arr, f, mode, f, f, f, G, None) == 1
     assert why.lower() in lib.mttkrp_last_error().decode().lower()
+
+
+def _ttm_multi_rc(lib, dims, modes, Ms, Js, Ts, x=0x1000, ws=None, ws_bytes=0):
+    n = len(modes)
+    arr = (ctypes.c_int64 * len(dims))(*dims)
+    cm = (ctypes.c_int * n)(*modes)
+    cj = (ctypes.c_int64 * n)(*Js)
+    cM = (ctypes.c_void_p * n)(*Ms)
+    cT = (ctypes.c_void_p * n)(*Ts)
+    return lib.mttkrp_ttm_multi(len(dims), arr, _fake(x), n, cm, cM, cj, cT, _fake(ws) if ws else None,
+                                ws_bytes, None)
+
+
+@pytest.mark.parametrize("modes,Ms,Js,Ts,why", [
+    ((0, 3), (0x100000, 0x200000), (4, 4), (0x300000, 0x400000), "mode"),
+    ((0, 1), (0x100000, 0x200000), (4, 0), (0x300000, 0x400000), "J"),
+    ((0, 1), (0x100000, 0), (4, 4), (0x300000, 0x400000), "NULL"),
+    ((0, 1), (0x100000, 0x200000), (4, 4), (0x300000, 0x300000 + 16), "overlaps result"),
+    ((0, 1), (0x100000, 0x300000 + 64), (4, 4), (0x300000, 0x400000), "overlaps result or matrix"),
+])
+def test_ttm_multi_rejects_invalid_before_any_launch(lib, modes, Ms, Js, Ts, why):
+    assert _ttm_multi_rc(lib, (4, 5, 6), modes, Ms, Js, Ts) == 1
+    assert why.lower() in lib.mttkrp_last_error().decode().lower()
+
+
+def test_ttm_multi_rejects_bad_counts_and_small_workspace(lib):
+    arr = (ctypes.c_int64 * 3)(4, 5, 6)
+    assert lib.mttkrp_ttm_multi(3, arr, _fake(0x1000), 0, None, None, None, None, None, 0, None) == 1
+    assert lib.mttkrp_ttm_multi(3, arr, _fake(0x1000), 65, None, None, None, None, None, 0, None) == 1
+    dims = (256, 128, 64)
+    need = mk.ttm_multi_workspace_bytes(dims, (0, 1, 2), (64, 64, 64))
+    assert need > 0
+    rc = _ttm_multi_rc(lib, dims, (0, 1, 2), (0x100000, 0x200000, 0x300000), (64, 64, 64),
+                       (0x10000000, 0x20000000, 0x30000000), x=0x40000000, ws=0x50000000, ws_bytes=need - 256)
+    assert rc == 3 and b"workspace" in lib.mttkrp_last_error()
+
+
+def test_ttm_multi_workspace_is_largest_single_product(lib):
+    dims = (256, 128, 64)
+    single = [mk.ttm_workspace_bytes(dims, m, J) for m, J in ((0, 64), (1, 256), (2, 96), (1, 8))]
+    assert single[3] == 0 and min(single[:3]) > 0
+    assert mk.ttm_multi_workspace_bytes(dims, (0, 1, 2, 1), (64, 256, 96, 8)) == max(single)
+    assert mk.ttm_multi_workspace_bytes(dims, (1,), (8,)) == 0
+    # the images of X come first and are the same for every product: more
+    # than 4 bytes an element, less than 4 bytes plus the largest M^T region
+    numel = 256 * 128 * 64
+    assert 4 * numel < max(single) < 4 * numel + 8 * 1024 * 1024

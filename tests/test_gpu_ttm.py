@@ -168,3 +168,84 @@ def test_out_buffer_and_rejects_bad_arguments():
         mk.ttm(X, 3, M)                          # mode out of range
     with pytest.raises(mk.MttkrpError):
         mk.ttm(X, 1, torch.empty((0, 6), device="cuda"))   # J = 0
+
+
+def test_ttm_multi_matches_single_products_bitwise():
+    """Several products of one X (mttkrp_ttm_multi): the tensor-core products
+    share one image pass and must equal the single-product calls bit for bit
+    (same images, same kernels); a product the tensor cores do not take (J = 8)
+    runs on the CUDA cores, placed first so that the image pass follows it."""
+    dims = (32, 64, 128)
+    rng = np.random.default_rng(501)
+    X = rng.standard_normal(dims).astype(np.float32)
+    spec = [(1, 8), (0, 96), (1, 64), (2, 130), (1, 300)]
+    Ms = [rng.standard_normal((J, dims[m])).astype(np.float32) for m, J in spec]
+    Xd = torch.from_numpy(X).cuda()
+    Md = [torch.from_numpy(M).cuda() for M in Ms]
+    outs = mk.ttm_multi(Xd, [m for m, _ in spec], Md)
+    for (m, J), M, T, Mt in zip(spec, Ms, outs, Md):
+        single = mk.ttm(Xd, m, Mt, path="tc" if J >= 32 else "simt")
+        assert torch.equal(T, single), (m, J)
+        check(T.cpu().numpy(), X, m, M, tc=J >= 32)
+    assert mk.device_status() == 0
+    simt = mk.ttm_multi(Xd, [m for m, _ in spec], Md, path="simt")
+    for (m, _), M, T, Mt in zip(spec, Ms, simt, Md):
+        assert torch.equal(T, mk.ttm(Xd, m, Mt, path="simt"))
+
+
+def test_ttm_multi_scaled_tensor_and_outs():
+    """Values far from 1 (the shared images carry one power-of-two scale) and
+    caller-given result buffers."""
+    dims = (64, 128, 64)
+    rng = np.random.default_rng(502)
+    X = (rng.standard_normal(dims) * 3e5).astype(np.float32)
+    X[5, 7, 9] = 4e7                                 # one outlier sets the scale
+    Ms = [rng.standard_normal((n, n)).astype(np.float32) * 1e-3 for n in dims]   # square: T_k has X's shape
+    Xd = torch.from_numpy(X).cuda()
+    outs = [torch.empty(dims, device="cuda") for _ in range(3)]
+    got = mk.ttm_multi(Xd, (0, 1, 2), [torch.from_numpy(M).cuda() for M in Ms], outs=outs, path="tc")
+    for k in range(3):
+        assert got[k] is outs[k]
+        check(outs[k].cpu().numpy(), X, k, Ms[k], tc=True)
+    assert mk.device_status() == 0
+
+
+def test_ttm_multi_full_size_sampled():
+    """512^3 with square 512 x 512 matrices for all three modes in one call (the
+    bench's launch configuration), 600 sampled outputs a mode."""
+    rng = np.random.default_rng(503)
+    dims = (512, 512, 512)
+    Xd = torch.randn(dims, generator=torch.Generator().manual_seed(504)).cuda()
+    Ms = [rng.standard_normal((512, 512)).astype(np.float32) for _ in range(3)]
+    outs = mk.ttm_multi(Xd, (0, 1, 2), [torch.from_numpy(M).cuda() for M in Ms])
+    X = Xd.cpu().numpy()
+    floor = 2.0 ** -36 * 512 * float(np.abs(X).max()) * max(float(np.abs(M).max()) for M in Ms)
+    for mode in range(3):
+        idx = [rng.integers(0, 512, 600) for _ in range(3)]
+        got = outs[mode][idx[0], idx[1], idx[2]].cpu().numpy().astype(np.float64)
+        for s in range(600):
+            at = [int(idx[0][s]), int(idx[1][s]), int(idx[2][s])]
+            j = at[mode]
+            at[mode] = slice(None)
+            x = X[tuple(at)].astype(np.float64)
+            want = x @ Ms[mode][j].astype(np.float64)
+            bound = np.abs(x) @ np.abs(Ms[mode][j]).astype(np.float64)
+            assert abs(got[s] - want) <= tc_coefficient(512) * bound + floor
+    assert mk.device_status() == 0
+    del outs, Xd
+    torch.cuda.empty_cache()
+
+
+def test_ttm_multi_rejects_bad_arguments():
+    X = torch.randn((32, 64, 128), device="cuda")
+    M0, M1 = torch.randn((64, 32), device="cuda"), torch.randn((64, 64), device="cuda")
+    shared = torch.empty((32, 64, 128), device="cuda")
+    with pytest.raises(mk.MttkrpError):     # two results in one buffer
+        mk.ttm_multi(X, (1, 1), (M1, M1), outs=(shared, shared))
+    with pytest.raises(mk.MttkrpError):     # J = 8 is not taken by the tensor cores
+        mk.ttm_multi(X, (0, 1), (M0, torch.randn((8, 64), device="cuda")), path="tc")
+    with pytest.raises(ValueError):
+        mk.ttm_multi(X, (0, 1), (M1, M1))   # M for mode 0 has 64 columns, mode 0 has 32
+    with pytest.raises(ValueError):
+        mk.ttm_multi(X, (), ())
+    assert mk.device_status() == 0
