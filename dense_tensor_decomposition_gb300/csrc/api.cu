@@ -170,6 +170,7 @@ void layout_workspace(const Plan& p, ModePlan& mp) {
 void place_plan_regions(Plan& p) {
     size_t base = 0;
     p.img_nat = p.img_t = 0;
+    p.fuse_mode = -1;
     bool fp16 = false, slab_ok = true;
     for (int k = 0; k < p.d; ++k) {
         const ModePlan& mp = p.mode[k];
@@ -205,6 +206,7 @@ void place_plan_regions(Plan& p) {
         mp.off_timg = off_t;
         mp.total = total;
     }
+    p.fuse_mode = tc_pick_fuse_mode(p);
 }
 
 int plan_mode(Plan& p, int k, int path) {
@@ -330,7 +332,8 @@ int run_mode(Plan& p, const float* Y, const float* const* factors, int k, float*
     }
     // 1. G table and base offsets of the pre indices (fp16 split with per-slab
     //    scales: rows scaled by s_global / s_slab, mode 0 being the first pre mode)
-    {
+    const bool g_scaled = fp16 && p.slab_on && k != 0;
+    auto build_g = [&](const uint32_t* enable) -> int {
         ProdTableArgs a;
         memset(&a, 0, sizeof(a));
         a.nm = g.npm;
@@ -343,14 +346,20 @@ int run_mode(Plan& p, const float* Y, const float* const* factors, int k, float*
         a.R = g.R;
         a.tab = gtab;
         a.base = basetab;
-        if (fp16 && p.slab_on && k != 0) {
+        if (g_scaled) {
             a.slab_bits = reinterpret_cast<const uint32_t*>(ws + p.off_slab);
             a.gmax_bits = reinterpret_cast<const uint32_t*>(ws);
             a.slab_div = g.npre / p.nslab;
         }
-        if ((err = launch_prod_table(a, stream)) != cudaSuccess)
-            return fail(MTTKRP_ERR_CUDA, "table launch: %s", cudaGetErrorString(err));
+        a.enable = enable;
+        cudaError_t e = launch_prod_table(a, stream);
+        if (e != cudaSuccess) return fail(MTTKRP_ERR_CUDA, "table launch: %s", cudaGetErrorString(e));
         ++p.launches;
+        return MTTKRP_OK;
+    };
+    {
+        const int rc = build_g(nullptr);
+        if (rc != MTTKRP_OK) return rc;
     }
     float* dst = mp.splits > 1 ? partials : out;
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
@@ -383,10 +392,29 @@ int run_mode(Plan& p, const float* Y, const float* const* factors, int k, float*
         int rc = tc_run(p, mp, Y, factors, gtab, basetab, ws + mp.off_binner, dst, stream, &nlaunch,
                         ev0 ? &ev0 : nullptr, g_errmsg, sizeof(g_errmsg));
         p.launches += nlaunch;
-        if (rc != MTTKRP_OK) return rc;
+        if (rc != MTTKRP_OK) {
+            p.fuse_pending = 0;
+            return rc;
+        }
         if (ev1) {
             cudaEventRecord(ev1, stream);
             ++p.ev_n[k];
+        }
+        if (p.fuse_pending) {
+            // the main kernel converted Y with sampled scales and wrote the
+            // images; if a value left the fp16 range, the exact maxima, images,
+            // this mode's G table (when it carries slab scales) and its result
+            // follow (launches that otherwise return at once)
+            rc = tc_redo_images(p, mp, Y, ws, stream, &nlaunch, g_errmsg, sizeof(g_errmsg));
+            p.launches += nlaunch;
+            if (rc == MTTKRP_OK && g_scaled) rc = build_g(tc_redo_flag(p, ws));
+            if (rc == MTTKRP_OK) {
+                rc = tc_redo_main(p, mp, Y, factors, gtab, basetab, ws + mp.off_binner, dst, stream, &nlaunch,
+                                  g_errmsg, sizeof(g_errmsg));
+                p.launches += nlaunch;
+            }
+            p.fuse_pending = 0;
+            if (rc != MTTKRP_OK) return rc;
         }
     } else {
         // 2. Binner (only for an inner group of several modes; else the factor itself)
@@ -550,6 +578,7 @@ int mttkrp(mttkrp_plan_t h, const float* Y, const float* const* factors, int mod
         return fail(MTTKRP_ERR_INVALID, "NULL tensor, factor array or output");
     p->ymax_ready = 0;
     p->img_ready = 0;
+    p->fuse_pending = 0;
     p->sweep_left_images = 0;
     return run_mode(*p, Y, factors, mode, out, static_cast<cudaStream_t>(stream));
 }
@@ -567,8 +596,14 @@ int mttkrp_all_modes(mttkrp_plan_t h, const float* Y, const float* const* factor
     }
     p->ymax_ready = 0;   // one max |Y| pass serves every mode of this call
     p->img_ready = 0;    // and one pass writing the fp16 images of Y
+    p->fuse_pending = 0;
     p->sweep_left_images = 0;
-    for (int k = 0; k < p->d; ++k) {
+    // the mode that converts Y and writes the images (if any) first, then the
+    // others in order (each mode's result does not depend on the order)
+    const int first = p->fuse_mode;
+    for (int t = -1; t < p->d; ++t) {
+        const int k = t < 0 ? first : t;
+        if (k < 0 || (t >= 0 && k == first)) continue;
         int rc = run_mode(*p, Y, factors, k, outs[k], static_cast<cudaStream_t>(stream));
         if (rc != MTTKRP_OK) return rc;
     }
@@ -868,6 +903,7 @@ int mttkrp_cp_als_sweep(mttkrp_plan_t h, const float* Y, float* const* factors, 
     const int reuse = have_norm && p->sweep_left_images;
     p->ymax_ready = reuse;
     p->img_ready = reuse;
+    p->fuse_pending = 0;
     p->sweep_left_images = 0;
     for (int n = 0; n < d; ++n) {
         float* vhi = mixed ? reinterpret_cast<float*>(base + l.vhi) : nullptr;
@@ -951,14 +987,15 @@ int mttkrp_plan_describe(mttkrp_plan_t h, int mode, char* buf, size_t len) {
                      "mode=%d path=%s kernel=%s tile=%dx%d inner_group=[%s] J=%lld Jq=%lld pre_modes=[%s] "
                      "npre=%lld splits=%lld pre_per_split=%lld workspace=%zu tc_ksteps=%d tc_inner=%d tc_slots=%d "
                      "tc_tmem_a=%d tc_fp16x2=%d tc_fp16_image=%d krp=%s krp_bytes=%llu "
-                     "ws_partials=%zu ws_tables=%zu ws_images=%zu",
+                     "ws_partials=%zu ws_tables=%zu ws_images=%zu tc_convert=%d",
                      mode, mp.path == MTTKRP_PATH_TC ? "tc" : "simt", kernel, mp.bm, mp.bn, groups,
                      (long long)g.J, (long long)g.Jq, pres, (long long)g.npre,
                      (long long)mp.splits, (long long)mp.pre_per_split, mp.total, mp.tc_ks, mp.tc_inner,
                      mp.tc_small ? mp.tc_ps : 1, mp.tc_tmem, mp.tc_h2 || mp.tc_img,
                      mp.tc_img ? (mp.tc_img_t ? 2 : mp.tc_img_mn ? 3 : 1) : 0,
                      mp.explicit_krp ? "explicit" : "free", (unsigned long long)krp_bytes,
-                     mp.off_binner - mp.off_partials, mp.off_end - mp.off_binner, ws_images);
+                     mp.off_binner - mp.off_partials, mp.off_end - mp.off_binner, ws_images,
+                     mode == p->fuse_mode ? 1 : 0);
     if (buf != nullptr && len > 0) {
         strncpy(buf, tmp, len - 1);
         buf[len - 1] = 0;
@@ -1117,6 +1154,7 @@ extern "C" int mttkrp_noalloc(int d, const int64_t* dims, int64_t R, const float
     p.strides[d - 1] = 1;
     for (int n = d - 2; n >= 0; --n) p.strides[n] = p.strides[n + 1] * p.dims[n + 1];
     p.forced_path = MTTKRP_PATH_SIMT;
+    p.fuse_mode = -1;
     int rc = plan_mode(p, mode, MTTKRP_PATH_SIMT);
     if (rc != MTTKRP_OK) return fail(rc, "mode %d cannot be planned on the SIMT path", mode);
     const size_t need = p.mode[mode].total;

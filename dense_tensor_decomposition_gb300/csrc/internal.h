@@ -99,6 +99,12 @@ struct Plan {
     mutable int ymax_ready;
     // fp16 images of Y (tc_img modes) already written for the current call's Y
     mutable int img_ready;
+    // the next tensor-core launch converts Y in place and writes the images
+    // (set by tc_prepare, cleared once the launch and its exact redo are enqueued)
+    mutable int fuse_pending;
+    // the mode whose main kernel converts Y when it is the first fp16 mode of a
+    // call (-1: none); an all-modes call computes it first
+    int fuse_mode;
     int img_nat, img_t;   // which images the plan's tc_img modes read (natural, transposed)
     // fp16 split: largest |Y| of every slab of mode 0 (fp32 bits) at off_slab in
     // the workspace.  nslab = I_0 when every fp16-split mode of the plan takes
@@ -139,6 +145,8 @@ struct ProdTableArgs {
     const uint32_t* slab_bits;
     const uint32_t* gmax_bits;
     int64_t slab_div;
+    // non-null: the kernel runs only if *enable is set
+    const uint32_t* enable;
 };
 
 struct SimtArgs {

@@ -19,6 +19,7 @@ namespace mk {
 // loads and multiplies).
 template <int NM, bool V4>
 __global__ void __launch_bounds__(256) prod_table_kernel(ProdTableArgs a) {
+    if (a.enable != nullptr && *a.enable == 0) return;
     const int lane = threadIdx.x & 31;
     constexpr int64_t kRun = 128;   // float4 groups (V4) or columns a run
     const int64_t units = V4 ? a.R / 4 : a.R;

@@ -111,6 +111,14 @@ struct TcArgs {
     int slab_rows;               // 1: the slab is the output row (mode 0, per-slab scales)
     const float* colscale;       // power-of-two scale of each Binner column (R)
     uint32_t* status;
+    // image kernel converting in place (mode 0, the first mode of a call): fp32
+    // Y tiles (yfmap: two 32-index boxes a K-step; ymap and ymap_lo then map the
+    // images it stores); the out-of-range flag the conversion sets
+    CUtensorMap yfmap;
+    uint32_t* ovf;
+    // non-null: the kernel runs only if *enable is set (the exact redo after a
+    // converting launch whose sampled scales were too small)
+    const uint32_t* enable;
 };
 
 // ---------------------------------------------------------------------------
@@ -313,6 +321,60 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Tensor store of one box from shared memory (bulk-group completion): the
+// shared-memory writes it reads are fenced to the async proxy first; the group
+// is committed, and its reads waited for before the buffer is written again.
+__device__ __forceinline__ void tma_store(const CUtensorMap* map, int rank, const int* c, const void* src) {
+    const uint64_t m = reinterpret_cast<uint64_t>(map);
+    const uint32_t sa = smem_u32(src);
+    switch (rank) {
+        case 2:
+            asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(m),
+                         "r"(sa), "r"(c[0]), "r"(c[1])
+                         : "memory");
+            break;
+        case 3:
+            asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(m),
+                         "r"(sa), "r"(c[0]), "r"(c[1]), "r"(c[2])
+                         : "memory");
+            break;
+        case 4:
+            asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                             m),
+                         "r"(sa), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3])
+                         : "memory");
+            break;
+        default:
+            asm volatile(
+                "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(m),
+                "r"(sa), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4])
+                : "memory");
+            break;
+    }
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+// largest magnitude of two values, NaN if either is NaN
+__device__ __forceinline__ float absmax_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(fabsf(a)), "f"(fabsf(b)));
+    return d;
 }
 
 // K-major, 64-byte swizzle shared-memory matrix descriptor: 8-row groups of
@@ -2053,7 +2115,11 @@ constexpr int kImgThreads = (kImgEpiWarp0 + kEpiWarps) * 32;   // 640
 // registers a thread: the launch allots 96 (65536 / 640, in units of 8); the
 // split uses 128 x (56 + 4 x 104) = 60416 of the 61440 allotted
 constexpr int kImgRegsCtl = 56, kImgRegsEpi = 104, kImgRegsLaunch = 96;
+// with in-place conversion the control warpgroup holds the converter warps: 64
+// registers, which uses the whole allotment
+constexpr int kImgRegsCtlCvt = 64;
 static_assert(128 * (kImgRegsCtl + 4 * kImgRegsEpi) <= kImgThreads * kImgRegsLaunch, "register split");
+static_assert(128 * (kImgRegsCtlCvt + 4 * kImgRegsEpi) <= kImgThreads * kImgRegsLaunch, "register split");
 
 // K-major, 128-byte swizzle descriptor: 8-row groups of 128-byte rows, 1024
 // bytes apart (high word; the low word is the start address >> 4 and LBO = 1)
@@ -2093,7 +2159,9 @@ struct SmemImg {
     static constexpr uint32_t kStage = 2 * kA;     // hi and lo tiles
     static constexpr uint32_t kB = BN * 128;       // one K-step of B (hi or lo)
     static constexpr uint32_t kBRes = kImgCK * 2 * kB;
-    static constexpr uint32_t kBarBytes = 256;
+    // barriers in the first 512 bytes, then (in-place conversion) the scales of
+    // the row tile's 128 rows
+    static constexpr uint32_t kBarBytes = 1024;
     static constexpr uint32_t kFree = 232448u - 1024u - kBarBytes - kBRes;
     static constexpr int kStages = kFree / kStage > 6 ? 6 : (int)(kFree / kStage);
     // small I: the slot sums at the end go through a [128][BN + 4] fp32 buffer
@@ -2105,7 +2173,7 @@ struct SmemImg {
     static_assert(kStages >= 3, "operand ring depth");
     static_assert(kTotal <= 232448, "shared memory budget");
     static_assert(kB % 1024 == 0, "swizzle-atom alignment");
-    static_assert((2 * kStages + 7) * 8 + 8 <= kBarBytes, "barrier area");
+    static_assert((3 * kStages + 7) * 8 + 8 <= 512, "barrier area");
 };
 
 // MN-major A operand (the innermost mode from the natural images, MN = true):
@@ -2118,9 +2186,23 @@ constexpr uint32_t kDescMnLo = (uint32_t)((8192 >> 4) << 16);   // leading byte 
 
 __device__ __forceinline__ uint32_t sdesc128mn_lo(uint32_t saddr) { return kDescMnLo | ((saddr & 0x3FFFFu) >> 4); }
 
-template <int BN, bool SMALL, bool MN>
+// CVT = true: the operand stages are filled from fp32 Y instead of the images
+// (mode 0 as the first mode of a call, which then also writes the images).
+// The TMA warp loads each K-step as two 32-index fp32 boxes (128-byte swizzle)
+// into the stage; warps 2 and 3 (64 rows each) convert it in place into the hi
+// and lo tiles, with the same split and scales as split_image_kernel, and
+// release it to the MMA warp; the TMA warp stores the converted tiles to the
+// images (column tile 0 only; other column tiles read the same Y) one stage
+// behind its loads, and waits for a store's reads before it refills that
+// stage.  Every row's fp32 bytes and its hi and lo bytes lie in that row's
+// 128-byte lines of the two halves of the stage, so one warp owns all the
+// bytes of its rows and loads them before it stores.  A scaled value outside
+// the fp16 range sets *a.ovf.
+template <int BN, bool SMALL, bool MN, bool CVT = false>
 __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_constant__ TcArgs a) {
     static_assert(!(SMALL && MN), "stacked tiles read K-major images");
+    static_assert(!CVT || (!SMALL && !MN), "in-place conversion: natural K-major tiles");
+    if (a.enable != nullptr && *a.enable == 0) return;
     using L = SmemImg<BN, SMALL>;
     constexpr int NS = L::kStages;
     constexpr int CK = kImgCK;
@@ -2139,6 +2221,8 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
     uint64_t* mma_done = bempty + 1;            // [1]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint64_t* yfull = mma_done + 2;             // [NS] (CVT) the fp32 boxes of the stage landed
+    float* sscale = reinterpret_cast<float*>(smem + L::kOffBars + 512);   // [128] (CVT) row scales
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -2161,8 +2245,9 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], CVT ? 2 : 1);   // CVT: both converter warps
             mbar_init(&empty[s], 1);
+            if (CVT) mbar_init(&yfull[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&zfull[b], 1);
@@ -2196,7 +2281,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
     };
 
     if (warp < kImgEpiWarp0) {
-        regs_dec<kImgRegsCtl>();
+        regs_dec<CVT ? kImgRegsCtlCvt : kImgRegsCtl>();
         if (warp == 0 && lane == 0) {
             // ------------------------- TMA producer -------------------------
             const uint8_t* bimg = reinterpret_cast<const uint8_t*>(a.bimg);
@@ -2216,6 +2301,22 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                     bulk_load(bres + q * 2 * L::kB, src, 2 * L::kB, bfull);
                 }
                 ++nbl;
+                return true;
+            };
+            // CVT: image coordinates of the tile in each stage, and the tiles
+            // stored so far (tile u is stored once converted, from stage u % NS)
+            const bool store = CVT && blockIdx.x == 0;
+            int cst[CVT ? NS : 1][5];
+            int64_t stored = 0;
+            auto store_tile = [&](int64_t u) -> bool {
+                const int sl = (int)(u % NS);
+                if (!wait_bounded_inl(&full[sl], (uint32_t)((u / NS) & 1), abort_flag, a.status, kStatusTimeoutTma))
+                    return false;
+                const uint8_t* src = ring + sl * L::kStage;
+                tma_store(&a.ymap, a.rank, cst[CVT ? sl : 0], src);
+                tma_store(&a.ymap_lo, a.rank, cst[CVT ? sl : 0], src + L::kA);
+                bulk_commit();
+                stored = u + 1;
                 return true;
             };
             // the pre index pi = (cP, cQ) in C order, advanced without divisions
@@ -2269,9 +2370,28 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                             ok = false;
                             break;
                         }
+                        if (store && rr.reused) {
+                            // the stage's previous tile: stored, and its store's reads done
+                            while (ok && stored <= issued - NS) ok = store_tile(stored);
+                            if (!ok) break;
+                            bulk_wait_read_all();
+                        }
                         uint8_t* st = ring + rr.slot * L::kStage;
-                        mbar_arrive_expect_tx(&full[rr.slot], 2u * a.y_box_bytes);
-                        if constexpr (MN) {
+                        mbar_arrive_expect_tx(CVT ? &yfull[rr.slot] : &full[rr.slot], 2u * a.y_box_bytes);
+                        if constexpr (CVT) {
+#pragma unroll
+                            for (int t = 0; t < 5; ++t) cst[rr.slot][t] = c[t];
+                            // indices 0-31 of the K-step, then 32-63 (x is slot 0)
+                            tma_load(&a.yfmap, a.rank, c, st, &yfull[rr.slot]);
+                            c[0] += 32;
+                            tma_load(&a.yfmap, a.rank, c, st + L::kA, &yfull[rr.slot]);
+                            // the tile loaded NS - 1 loads ago is converted by now, or
+                            // will be before the stage it holds can be refilled
+                            if (store) {
+                                while (ok && stored <= issued - (NS - 1)) ok = store_tile(stored);
+                                if (!ok) break;
+                            }
+                        } else if constexpr (MN) {
                             // two 64-row halves of M per image
                             int c2[5];
                             if (a.ttm_q > 0) {
@@ -2302,9 +2422,96 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
                 if (ok && b_pending && !load_b(jc)) ok = false;
             }
             }   // row tiles
+            if (store) {
+                for (int64_t u = stored; u < issued && ok; ++u) ok = store_tile(u);
+                bulk_wait_all();
+            }
             for (int64_t u = issued - 1; u >= 0 && u >= issued - NS; --u)
-                wait_drain_inl(&full[u % NS], (uint32_t)((u / NS) & 1), a.status);
+                wait_drain_inl(CVT ? &yfull[u % NS] : &full[u % NS], (uint32_t)((u / NS) & 1), a.status);
             if (nbl > 0) wait_drain_inl(bfull, (nbl - 1) & 1u, a.status);
+        } else if (CVT && warp >= 2) {
+            // ----------------------- converters (CVT) -----------------------
+            // warp 2 converts rows 0-63 of each tile, warp 3 rows 64-127; lane
+            // (g, rw) = (lane / 8, lane % 8) takes row 8 G + rw of row group G and
+            // the 8-index groups g and g + 4 (fp32 chunks 2g, 2g + 1 of box 0 and
+            // of box 1; hi and lo chunks g and g + 4).  The eight lanes of a
+            // shared-memory phase take eight rows, whose swizzled chunks differ.
+            // The loads of group G + 1 are issued before group G is converted.
+            const int cw = warp - 2;
+            const int g = lane >> 3, rw = lane & 7;
+            const uint32_t ring_u = smem_u32(ring);
+            Ring<NS> rr;
+            bool ok = true;
+            float big = 0.f;   // largest scaled magnitude (NaN if any was NaN)
+            for (int64_t ty = blockIdx.y; ty < ty_end && ok; ty += ty_step) {
+                const int64_t m0 = ty * kBM;
+                // per-row slab scales of this warp's 64 rows (mode 0: the slab is the row)
+                __syncwarp();
+                if (a.slab_rows) {
+                    sscale[64 * cw + lane] = y_scale_row(a, m0 + 64 * cw + lane);
+                    sscale[64 * cw + 32 + lane] = y_scale_row(a, m0 + 64 * cw + 32 + lane);
+                }
+                __syncwarp();
+                for (int jc = jc0; jc < jc1 && ok; ++jc) {
+                    const int ck = chunk_len(jc);
+                    for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                        const float sy_pre = a.slab_rows ? 1.f : y_scale_pre(a, pi);
+                        for (int q = 0; q < ck; ++q, rr.next()) {
+                            if (!warp_wait_inl(&yfull[rr.slot], rr.phase, abort_flag, a.status, kStatusTimeoutLo)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t st = ring_u + (uint32_t)rr.slot * L::kStage;
+                            // box h of row group G: this lane's two fp32 chunks (8 indices)
+                            auto load = [&](int G, int h, float4* w) {
+                                const uint32_t base = st + (uint32_t)h * L::kA + (uint32_t)(64 * cw + 8 * G + rw) * 128u;
+                                w[0] = lds128(base + (uint32_t)(((2 * g) ^ rw) << 4));
+                                w[1] = lds128(base + (uint32_t)(((2 * g + 1) ^ rw) << 4));
+                            };
+                            // split 8 scaled values into hi and lo words
+                            auto split8 = [&](const float4* w, float sy, uint32_t* hw, uint32_t* lw) {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float4 f = w[e >> 1];
+                                    const float x0 = ((e & 1) ? f.z : f.x) * sy;
+                                    const float x1 = ((e & 1) ? f.w : f.y) * sy;
+                                    big = absmax_nan(big, absmax_nan(x0, x1));
+                                    const __half2 hh = __floats2half2_rn(x0, x1);
+                                    const float2 hf = __half22float2(hh);
+                                    hw[e] = half2_bits(hh);
+                                    lw[e] = half2_bits(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+                                }
+                            };
+                            auto put = [&](int G, int h, const uint32_t* hw, const uint32_t* lw) {
+                                const uint32_t off =
+                                    (uint32_t)(64 * cw + 8 * G + rw) * 128u + (uint32_t)(((g + 4 * h) ^ rw) << 4);
+                                sts128(st + off, hw[0], hw[1], hw[2], hw[3]);
+                                sts128(st + L::kA + off, lw[0], lw[1], lw[2], lw[3]);
+                            };
+                            // box 0 of group G + 1 is loaded while group G is split; every
+                            // load of group G's rows (both boxes) precedes its stores
+                            float4 a0[2], a1[2];
+                            load(0, 0, a0);
+#pragma unroll
+                            for (int G = 0; G < 8; ++G) {
+                                load(G, 1, a1);
+                                const float sy = a.slab_rows ? sscale[64 * cw + 8 * G + rw] : sy_pre;
+                                uint32_t hw[4], lw[4];
+                                split8(a0, sy, hw, lw);
+                                if (G + 1 < 8) load(G + 1, 0, a0);
+                                __syncwarp();
+                                put(G, 0, hw, lw);
+                                split8(a1, sy, hw, lw);
+                                put(G, 1, hw, lw);
+                            }
+                            fence_proxy_async();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&full[rr.slot]);
+                        }
+                    }
+                }
+            }
+            if (__any_sync(0xffffffffu, !(big < 65504.f)) && lane == 0) atomicOr(a.ovf, 1u);
         } else if (warp == 1 && lane == 0) {
             // ------------------------- MMA issuer -------------------------
             // kind::f16: fp16 A and B (B K-major; A K-major, or MN-major with the
@@ -3604,7 +3811,7 @@ cudaError_t launch_h2(const TcArgs& args, dim3 grid, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int BN, bool SMALL = false, bool MN = false>
+template <int BN, bool SMALL = false, bool MN = false, bool CVT = false>
 cudaError_t launch_img(const TcArgs& args, dim3 grid, cudaStream_t s) {
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -3615,15 +3822,15 @@ cudaError_t launch_img(const TcArgs& args, dim3 grid, cudaStream_t s) {
         // setmaxnreg.inc waits until the pool allotted at launch can serve it:
         // refuse a build whose launch allotment is below what the split assumes
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, tc_img_kernel<BN, SMALL, MN>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, tc_img_kernel<BN, SMALL, MN, CVT>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs < kImgRegsLaunch || fa.numRegs * kImgThreads > 65536) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(tc_img_kernel<BN, SMALL, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(tc_img_kernel<BN, SMALL, MN, CVT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)SmemImg<BN, SMALL>::kTotal);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    tc_img_kernel<BN, SMALL, MN><<<grid, kImgThreads, SmemImg<BN, SMALL>::kTotal, s>>>(args);
+    tc_img_kernel<BN, SMALL, MN, CVT><<<grid, kImgThreads, SmemImg<BN, SMALL>::kTotal, s>>>(args);
     return cudaGetLastError();
 }
 
@@ -3828,6 +4035,9 @@ int tc_prepare(const Plan& p, const ModePlan& mp, const float* Y, void* ws, cuda
     // Plans whose first fp16 mode converts per CTA take the exact maxima.
     uint32_t* ovf = slab + p.nslab;   // the image pass's out-of-range flag
     const bool sampled = !p.ymax_ready && mp.tc_img && !p.img_ready;
+    // the mode's own main kernel can write the images while it converts its
+    // tiles (then it sets the flag, and the gated redo launches follow it)
+    const bool fuse = sampled && mp.g.k == p.fuse_mode && tc_fuse_eligible(p, mp);
     int64_t max_blocks = cdiv64(cdiv64(slab_len, kSlabUnit) * p.nslab, 4);
     if (max_blocks > 152 * 8) max_blocks = 152 * 8;
     if (!p.ymax_ready) {
@@ -3851,7 +4061,10 @@ int tc_prepare(const Plan& p, const ModePlan& mp, const float* Y, void* ws, cuda
             ++*nlaunch;
         }
     }
-    if (e == cudaSuccess && mp.tc_img && !p.img_ready) {
+    if (e == cudaSuccess && mp.tc_img && !p.img_ready && fuse) {
+        p.img_ready = 1;
+        p.fuse_pending = 1;
+    } else if (e == cudaSuccess && mp.tc_img && !p.img_ready) {
         // every image the plan's tc_img modes read, in one pass over Y
         const size_t img_half = ((size_t)numel * 2 + 255) / 256 * 256;
         __half* img_hi = reinterpret_cast<__half*>(ws_base + mp.off_img);
@@ -3899,9 +4112,35 @@ int tc_prepare(const Plan& p, const ModePlan& mp, const float* Y, void* ws, cuda
     return MTTKRP_OK;
 }
 
-int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const* factors,
-           const float* gtab, const int64_t* basetab, void* binner_ws, float* dst,
-           cudaStream_t stream, int* nlaunch, cudaEvent_t* start_ev, char* errbuf, size_t errlen) {
+bool tc_fuse_eligible(const Plan& p, const ModePlan& mp) {
+    if (mp.path != MTTKRP_PATH_TC || !mp.tc_img || mp.tc_img_mn || mp.tc_img_t || mp.tc_small || mp.explicit_krp ||
+        mp.bn != 256 || p.img_t || !p.img_nat || mp.g.J != mp.g.Jq || mp.g.Jq % kBK4 != 0)
+        return false;
+    // one column tile: with several, each would convert the same Y tiles
+    if (cdiv64(mp.g.R, mp.bn) != 1) return false;
+    MapGeom mg;
+    return y_map_geom(mp, p.dims, p.strides, p.d, mg, 4) && y_map_geom(mp, p.dims, p.strides, p.d, mg, 2);
+}
+
+int tc_pick_fuse_mode(const Plan& p) {
+    int first = -1;
+    for (int k = 0; k < p.d; ++k) {
+        const ModePlan& mp = p.mode[k];
+        if (!tc_fuse_eligible(p, mp)) continue;
+        if (mp.g.s_k == mp.g.Jq) return k;   // 128 rows x Jq of one pre index: one contiguous block
+        if (first < 0) first = k;
+    }
+    return first;
+}
+
+namespace {
+// phase 0: the mode as planned; 1: the main kernel converts Y in place and
+// writes the images (p.fuse_pending); 2: the exact redo of phase 1's main
+// kernel, run only if its conversion flagged a value (the Binner scales and B
+// images of phase 1 are still in place)
+int tc_run_phase(const Plan& p, const ModePlan& mp, const float* Y, const float* const* factors,
+                 const float* gtab, const int64_t* basetab, void* binner_ws, float* dst, cudaStream_t stream,
+                 int* nlaunch, cudaEvent_t* start_ev, char* errbuf, size_t errlen, int phase) {
     (void)basetab;
     *nlaunch = 0;
     const ModeGeom& g = mp.g;
@@ -3970,6 +4209,30 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
                                 : CU_TENSOR_MAP_SWIZZLE_64B,
                     promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
+    if (cr == CUDA_SUCCESS && phase == 1) {
+        // fp32 Y in 32-index boxes (128-byte rows, the 128-byte swizzle)
+        MapGeom mf;
+        if (!y_map_geom(mp, p.dims, p.strides, p.d, mf, 4)) {
+            snprintf(errbuf, errlen, "mode %d: Y view not expressible as an fp32 TMA tensor map", g.k);
+            return MTTKRP_ERR_UNSUPPORTED;
+        }
+        cuuint64_t fdim[5], fstride[4];
+        cuuint32_t fbox[5];
+        for (int t = 0; t < mf.rank; ++t) {
+            fdim[t] = mf.dim[t];
+            fbox[t] = mf.box[t];
+            if (t > 0) fstride[t - 1] = mf.stride_el[t] * 4;
+        }
+        fbox[0] = 32;
+        uint64_t falign = (uint64_t)fdim[0] * 4;
+        for (int t = 0; t + 1 < mf.rank; ++t) falign |= (uint64_t)fstride[t];
+        const CUtensorMapL2promotion fpromo = (falign % 256 == 0)   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                              : (falign % 128 == 0) ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                                                    : CU_TENSOR_MAP_L2_PROMOTION_NONE;
+        cr = encode(&args.yfmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)mf.rank, const_cast<float*>(Y), fdim,
+                    fstride, fbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, fpromo,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (cr != CUDA_SUCCESS) {
         snprintf(errbuf, errlen, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
         return MTTKRP_ERR_CUDA;
@@ -3982,7 +4245,7 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     float* colscale = reinterpret_cast<float*>(static_cast<uint8_t*>(binner_ws) + colscale_offset(mp));
     // the first bytes of the workspace (reserved region) hold max |Y| as fp32 bits
     uint32_t* ymax = reinterpret_cast<uint32_t*>(ws_base);
-    if (mp.tc_h2 || mp.tc_img) {
+    if ((mp.tc_h2 || mp.tc_img) && phase != 2) {
         ColScaleArgs c;
         memset(&c, 0, sizeof(c));
         c.ngroup = g.ngroup;
@@ -4000,7 +4263,9 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
         }
         ++*nlaunch;
     }
-    if (mp.explicit_krp) {
+    if (phase == 2) {
+        // B images as phase 1 left them
+    } else if (mp.explicit_krp) {
         KrpImgArgs b;
         memset(&b, 0, sizeof(b));
         const int last = g.group[g.ngroup - 1];
@@ -4108,11 +4373,16 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
         snprintf(errbuf, errlen, "device status word unavailable");
         return MTTKRP_ERR_CUDA;
     }
+    uint32_t* ovf = reinterpret_cast<uint32_t*>(ws_base + p.off_slab) + p.nslab;
+    if (phase == 1) args.ovf = ovf;
+    if (phase == 2) args.enable = ovf;
     if (start_ev) cudaEventRecord(*start_ev, stream);
     dim3 grid((unsigned)cdiv64(g.R, mp.bn), mp.tc_small ? 1u : (unsigned)cdiv64(g.I, kBM),
               (unsigned)mp.splits);
     cudaError_t e;
-    if (mp.tc_img) {
+    if (phase == 1) {
+        e = launch_img<256, false, false, true>(args, grid, stream);
+    } else if (mp.tc_img) {
         if (mp.tc_small)
             e = mp.bn == 128 ? launch_img<128, true>(args, grid, stream) : launch_img<64, true>(args, grid, stream);
         else
@@ -4149,6 +4419,56 @@ int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const
     }
     ++*nlaunch;
     return MTTKRP_OK;
+}
+}  // namespace
+
+int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const* factors,
+           const float* gtab, const int64_t* basetab, void* binner_ws, float* dst,
+           cudaStream_t stream, int* nlaunch, cudaEvent_t* start_ev, char* errbuf, size_t errlen) {
+    return tc_run_phase(p, mp, Y, factors, gtab, basetab, binner_ws, dst, stream, nlaunch, start_ev, errbuf, errlen,
+                        p.fuse_pending ? 1 : 0);
+}
+
+const uint32_t* tc_redo_flag(const Plan& p, void* ws) {
+    return reinterpret_cast<const uint32_t*>(static_cast<uint8_t*>(ws) + p.off_slab) + p.nslab;
+}
+
+int tc_redo_images(const Plan& p, const ModePlan& mp, const float* Y, void* ws, cudaStream_t stream, int* nlaunch,
+                   char* errbuf, size_t errlen) {
+    *nlaunch = 0;
+    uint8_t* ws_base = static_cast<uint8_t*>(ws);
+    uint32_t* ymax = reinterpret_cast<uint32_t*>(ws_base);
+    uint32_t* slab = reinterpret_cast<uint32_t*>(ws_base + p.off_slab);
+    const uint32_t* ovf = tc_redo_flag(p, ws);
+    int64_t numel = 1;
+    for (int t = 0; t < p.d; ++t) numel *= p.dims[t];
+    const int64_t slab_len = numel / p.nslab;
+    const size_t img_half = ((size_t)numel * 2 + 255) / 256 * 256;
+    __half* img_hi = reinterpret_cast<__half*>(ws_base + mp.off_img);
+    __half* img_lo = reinterpret_cast<__half*>(ws_base + mp.off_img + img_half);
+    int64_t blocks = cdiv64(cdiv64(slab_len, kSlabUnit) * p.nslab, 4);
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    slabmax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, p.nslab, slab_len, slab, ymax, ovf);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) {
+        split_image_kernel<<<(unsigned)blocks, 256, 0, stream>>>(Y, p.nslab, slab_len, slab, ymax, img_hi, img_lo,
+                                                                 nullptr, ovf);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) {
+        snprintf(errbuf, errlen, "fp16 split redo: %s", cudaGetErrorString(e));
+        return MTTKRP_ERR_CUDA;
+    }
+    *nlaunch = 2;
+    return MTTKRP_OK;
+}
+
+int tc_redo_main(const Plan& p, const ModePlan& mp, const float* Y, const float* const* factors,
+                 const float* gtab, const int64_t* basetab, void* binner_ws, float* dst,
+                 cudaStream_t stream, int* nlaunch, char* errbuf, size_t errlen) {
+    p.fuse_pending = 0;
+    return tc_run_phase(p, mp, Y, factors, gtab, basetab, binner_ws, dst, stream, nlaunch, nullptr, errbuf, errlen,
+                        2);
 }
 
 cudaError_t tc_launch_mma_probe(int kind, int blocks, int iters, cudaStream_t s) {

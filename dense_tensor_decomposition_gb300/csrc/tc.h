@@ -23,9 +23,30 @@ int tc_prepare(const Plan& p, const ModePlan& mp, const float* Y, void* ws, cuda
 // *nlaunch receives the number of kernels enqueued.  If start_ev is non-null,
 // *start_ev is re-recorded just before the main kernel (after the tensor-core
 // path's own preparation kernels) so that timing covers the main kernel only.
+// With p.fuse_pending the main kernel converts Y in place and writes the images.
 int tc_run(const Plan& p, const ModePlan& mp, const float* Y, const float* const* factors,
            const float* gtab, const int64_t* basetab, void* binner_ws, float* dst,
            cudaStream_t stream, int* nlaunch, cudaEvent_t* start_ev, char* errbuf, size_t errlen);
+// After a converting launch (p.fuse_pending), each a launch that returns at
+// once unless the conversion flagged a scaled value outside the fp16 range:
+// tc_redo_images takes the exact maxima and writes the images; (the caller
+// then rebuilds the mode's G table if it carries slab scales, gated on
+// tc_redo_flag) tc_redo_main runs the mode's main kernel again on the images
+// and clears p.fuse_pending.  The inputs are those of the tc_run they follow.
+int tc_redo_images(const Plan& p, const ModePlan& mp, const float* Y, void* ws, cudaStream_t stream, int* nlaunch,
+                   char* errbuf, size_t errlen);
+const uint32_t* tc_redo_flag(const Plan& p, void* ws);
+int tc_redo_main(const Plan& p, const ModePlan& mp, const float* Y, const float* const* factors,
+                 const float* gtab, const int64_t* basetab, void* binner_ws, float* dst,
+                 cudaStream_t stream, int* nlaunch, char* errbuf, size_t errlen);
+// Whether a mode's main kernel can convert Y in place (natural K-major image
+// tiles, 256 columns in one column tile, an inner group of whole modes after
+// it, no transposed images in the plan).
+bool tc_fuse_eligible(const Plan& p, const ModePlan& mp);
+// The mode the plan converts in (p.fuse_mode): among the eligible modes, one
+// whose tiles cover contiguous memory (stride of the mode = inner-group size),
+// else the first; -1 if none.
+int tc_pick_fuse_mode(const Plan& p);
 // Peak probe of the tensor pipe: `blocks` CTAs (one per SM), each issuing `iters`
 // M128 x N256 MMAs of kind::tf32 (kind 0, K = 8) or kind::f16 (kind 1, K = 16).
 cudaError_t tc_launch_mma_probe(int kind, int blocks, int iters, cudaStream_t s);

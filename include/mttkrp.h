@@ -120,8 +120,10 @@ int mttkrp_all_modes(mttkrp_plan_t plan, const float* Y, const float* const* fac
 int mttkrp_plan_mode_path(mttkrp_plan_t plan, int mode);
 
 /* Human-readable planner decisions for `mode` (tiles, split count, inner
- * group) written into buf (NUL-terminated, truncated to len).  Returns the
- * length the full text needs, or -1 for an invalid plan or mode. */
+ * group; tc_convert=1: when the mode is the first of a call to need the fp16
+ * images of Y, its main kernel converts Y itself and writes the images, with
+ * no separate pass) written into buf (NUL-terminated, truncated to len).
+ * Returns the length the full text needs, or -1 for an invalid plan or mode. */
 int mttkrp_plan_describe(mttkrp_plan_t plan, int mode, char* buf, size_t len);
 
 /* Kernel timing for benchmarks.  When enabled (enable != 0), every call

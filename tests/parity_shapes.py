@@ -64,3 +64,17 @@ EDGE = [
 
 # shapes whose modes run on the fp16-split tensor-core kernels (value-range tests)
 H2_SHAPES = [((130, 40, 48), 300), ((40, 36, 128), 450), ((200, 96, 64), 300), ((24, 120, 200), 300)]
+
+# shapes with a mode whose main kernel converts Y in place and stores the fp16
+# images (tc_convert=1; it runs first in an all-modes call), and that mode:
+# mode 0 (slab scales by output row) with two row tiles, a 2-row tail, a column
+# tail (R = 200 of 256); mode 1 and mode 2 (slab scales carried by G) with row
+# and column tails and a 4-way tensor
+CONVERT_SHAPES = [
+    ((256, 64, 128), 256, 0),
+    ((130, 40, 128), 256, 0),
+    ((384, 16, 64), 200, 0),
+    ((16, 256, 128), 256, 1),
+    ((24, 200, 128), 230, 1),
+    ((3, 4, 256, 128), 256, 2),
+]

@@ -14,7 +14,7 @@ import random
 
 import pytest
 
-from parity_shapes import EDGE, H2_SHAPES
+from parity_shapes import CONVERT_SHAPES, EDGE, H2_SHAPES
 
 mk = pytest.importorskip("dense_tensor_decomposition_gb300")
 
@@ -95,3 +95,16 @@ def test_headline_workload_kernels():
     assert kernels((512,) * 3, 2000, "auto") == ["img.nat.bn256", "img.nat.bn256", "img.mn.bn256"]
     assert kernels((512,) * 3, 2000, "tc_tf32") == ["tf32.kmaj.bn256", "tf32.kmaj.bn256",
                                                      "tf32tm.inner.bn224"]
+
+
+def test_converting_mode_is_gpu_tested():
+    """The shapes tests/test_gpu_convert.py runs convert Y in the mode listed
+    with them (tc_convert=1) and in no other; the 128^4 workload converts in
+    mode 2 (its 128 x 128 tiles of one pre index are contiguous); no mode of the
+    512^3, R = 2000 workload does (eight column tiles would each convert)."""
+    for dims, R, mode in CONVERT_SHAPES + [((128,) * 4, 256, 2)]:
+        plan = mk.Plan(dims, R)
+        flags = ["tc_convert=1" in plan.describe(k) for k in range(len(dims))]
+        assert flags == [k == mode for k in range(len(dims))], (dims, R, flags)
+    plan = mk.Plan((512,) * 3, 2000)
+    assert not any("tc_convert=1" in plan.describe(k) for k in range(3))
