@@ -2115,11 +2115,16 @@ constexpr int kImgThreads = (kImgEpiWarp0 + kEpiWarps) * 32;   // 640
 // registers a thread: the launch allots 96 (65536 / 640, in units of 8); the
 // split uses 128 x (56 + 4 x 104) = 60416 of the 61440 allotted
 constexpr int kImgRegsCtl = 56, kImgRegsEpi = 104, kImgRegsLaunch = 96;
-// with in-place conversion the control warpgroup holds the converter warps: 64
-// registers, which uses the whole allotment
-constexpr int kImgRegsCtlCvt = 64;
 static_assert(128 * (kImgRegsCtl + 4 * kImgRegsEpi) <= kImgThreads * kImgRegsLaunch, "register split");
-static_assert(128 * (kImgRegsCtlCvt + 4 * kImgRegsEpi) <= kImgThreads * kImgRegsLaunch, "register split");
+// in-place conversion adds a warpgroup of four converter warps (warps 4-7; the
+// epilogue moves to warps 8-23): 768 threads, 80 registers a thread at launch,
+// split 56 (control) + 40 (converters) + 4 x 96 (epilogue), 61440 in all
+constexpr int kCvtEpiWarp0 = 8;
+constexpr int kCvtThreads = (kCvtEpiWarp0 + kEpiWarps) * 32;   // 768
+constexpr int kCvtRegsCtl = 56, kCvtRegsCvt = 40, kCvtRegsEpi = 96, kCvtRegsLaunch = 80;
+static_assert(128 * (kCvtRegsCtl + kCvtRegsCvt + 4 * kCvtRegsEpi) <= kCvtThreads * kCvtRegsLaunch,
+              "register split");
+static_assert(kCvtThreads * kCvtRegsLaunch <= 65536, "register file");
 
 // K-major, 128-byte swizzle descriptor: 8-row groups of 128-byte rows, 1024
 // bytes apart (high word; the low word is the start address >> 4 and LBO = 1)
@@ -2187,11 +2192,11 @@ constexpr uint32_t kDescMnLo = (uint32_t)((8192 >> 4) << 16);   // leading byte 
 __device__ __forceinline__ uint32_t sdesc128mn_lo(uint32_t saddr) { return kDescMnLo | ((saddr & 0x3FFFFu) >> 4); }
 
 // CVT = true: the operand stages are filled from fp32 Y instead of the images
-// (mode 0 as the first mode of a call, which then also writes the images).
-// The TMA warp loads each K-step as two 32-index fp32 boxes (128-byte swizzle)
-// into the stage; warps 2 and 3 (64 rows each) convert it in place into the hi
-// and lo tiles, with the same split and scales as split_image_kernel, and
-// release it to the MMA warp; the TMA warp stores the converted tiles to the
+// (the first mode of a call, which then also writes the images).  The TMA warp
+// loads each K-step as two 32-index fp32 boxes (128-byte swizzle) into the
+// stage; warps 4-7 (32 rows each) convert it in place into the hi and lo
+// tiles, with the same split and scales as split_image_kernel, and release it
+// to the MMA warp; the TMA warp stores the converted tiles to the
 // images (column tile 0 only; other column tiles read the same Y) one stage
 // behind its loads, and waits for a store's reads before it refills that
 // stage.  Every row's fp32 bytes and its hi and lo bytes lie in that row's
@@ -2199,7 +2204,8 @@ __device__ __forceinline__ uint32_t sdesc128mn_lo(uint32_t saddr) { return kDesc
 // bytes of its rows and loads them before it stores.  A scaled value outside
 // the fp16 range sets *a.ovf.
 template <int BN, bool SMALL, bool MN, bool CVT = false>
-__global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(CVT ? kCvtThreads : kImgThreads, 1) tc_img_kernel(const __grid_constant__ TcArgs a) {
+    constexpr int EW0 = CVT ? kCvtEpiWarp0 : kImgEpiWarp0;   // first epilogue warp
     static_assert(!(SMALL && MN), "stacked tiles read K-major images");
     static_assert(!CVT || (!SMALL && !MN), "in-place conversion: natural K-major tiles");
     if (a.enable != nullptr && *a.enable == 0) return;
@@ -2245,7 +2251,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(&full[s], CVT ? 2 : 1);   // CVT: both converter warps
+            mbar_init(&full[s], CVT ? 4 : 1);   // CVT: the four converter warps
             mbar_init(&empty[s], 1);
             if (CVT) mbar_init(&yfull[s], 1);
         }
@@ -2280,8 +2286,88 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
         return e < pre_hi ? e : pre_hi;
     };
 
-    if (warp < kImgEpiWarp0) {
-        regs_dec<CVT ? kImgRegsCtlCvt : kImgRegsCtl>();
+    if (CVT && warp >= 4 && warp < EW0) {
+        regs_dec<kCvtRegsCvt>();
+        // ----------------------- converters (CVT) -----------------------
+        // warp 4 + cw converts rows 32 cw .. 32 cw + 31 of each tile; lane (g, rw)
+        // = (lane / 8, lane % 8) takes row 8 G + rw of row group G and the
+        // 8-index groups g and g + 4 (fp32 chunks 2g, 2g + 1 of box 0 and of box
+        // 1; hi and lo chunks g and g + 4).  The eight lanes of a shared-memory
+        // phase take eight rows, whose swizzled chunks differ.  Box 0 of group
+        // G + 1 is loaded while group G is split.
+        const int cw = warp - 4;
+        const int g = lane >> 3, rw = lane & 7;
+        const uint32_t ring_u = smem_u32(ring);
+        Ring<NS> rr;
+        bool ok = true;
+        float big = 0.f;   // largest scaled magnitude (NaN if any was NaN)
+        for (int64_t ty = blockIdx.y; ty < ty_end && ok; ty += ty_step) {
+            const int64_t m0 = ty * kBM;
+            // per-row slab scales of this warp's 32 rows (mode 0: the slab is the row)
+            __syncwarp();
+            if (a.slab_rows) sscale[32 * cw + lane] = y_scale_row(a, m0 + 32 * cw + lane);
+            __syncwarp();
+            for (int jc = jc0; jc < jc1 && ok; ++jc) {
+                const int ck = chunk_len(jc);
+                for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
+                    const float sy_pre = a.slab_rows ? 1.f : y_scale_pre(a, pi);
+                    for (int q = 0; q < ck; ++q, rr.next()) {
+                        if (!warp_wait_inl(&yfull[rr.slot], rr.phase, abort_flag, a.status, kStatusTimeoutLo)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t st = ring_u + (uint32_t)rr.slot * L::kStage;
+                        // box h of row group G: this lane's two fp32 chunks (8 indices)
+                        auto load = [&](int G, int h, float4* w) {
+                            const uint32_t base = st + (uint32_t)h * L::kA + (uint32_t)(32 * cw + 8 * G + rw) * 128u;
+                            w[0] = lds128(base + (uint32_t)(((2 * g) ^ rw) << 4));
+                            w[1] = lds128(base + (uint32_t)(((2 * g + 1) ^ rw) << 4));
+                        };
+                        // split 8 scaled values into hi and lo words
+                        auto split8 = [&](const float4* w, float sy, uint32_t* hw, uint32_t* lw) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float4 f = w[e >> 1];
+                                const float x0 = ((e & 1) ? f.z : f.x) * sy;
+                                const float x1 = ((e & 1) ? f.w : f.y) * sy;
+                                big = absmax_nan(big, absmax_nan(x0, x1));
+                                const __half2 hh = __floats2half2_rn(x0, x1);
+                                const float2 hf = __half22float2(hh);
+                                hw[e] = half2_bits(hh);
+                                lw[e] = half2_bits(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+                            }
+                        };
+                        auto put = [&](int G, int h, const uint32_t* hw, const uint32_t* lw) {
+                            const uint32_t off =
+                                (uint32_t)(32 * cw + 8 * G + rw) * 128u + (uint32_t)(((g + 4 * h) ^ rw) << 4);
+                            sts128(st + off, hw[0], hw[1], hw[2], hw[3]);
+                            sts128(st + L::kA + off, lw[0], lw[1], lw[2], lw[3]);
+                        };
+                        // every load of group G's rows (both boxes) precedes its stores
+                        float4 a0[2], a1[2];
+                        load(0, 0, a0);
+#pragma unroll
+                        for (int G = 0; G < 4; ++G) {
+                            load(G, 1, a1);
+                            const float sy = a.slab_rows ? sscale[32 * cw + 8 * G + rw] : sy_pre;
+                            uint32_t hw[4], lw[4];
+                            split8(a0, sy, hw, lw);
+                            if (G + 1 < 4) load(G + 1, 0, a0);
+                            __syncwarp();
+                            put(G, 0, hw, lw);
+                            split8(a1, sy, hw, lw);
+                            put(G, 1, hw, lw);
+                        }
+                        fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&full[rr.slot]);
+                    }
+                }
+            }
+        }
+        if (__any_sync(0xffffffffu, !(big < 65504.f)) && lane == 0) atomicOr(a.ovf, 1u);
+    } else if (warp < 4) {
+        regs_dec<CVT ? kCvtRegsCtl : kImgRegsCtl>();
         if (warp == 0 && lane == 0) {
             // ------------------------- TMA producer -------------------------
             const uint8_t* bimg = reinterpret_cast<const uint8_t*>(a.bimg);
@@ -2429,89 +2515,6 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             for (int64_t u = issued - 1; u >= 0 && u >= issued - NS; --u)
                 wait_drain_inl(CVT ? &yfull[u % NS] : &full[u % NS], (uint32_t)((u / NS) & 1), a.status);
             if (nbl > 0) wait_drain_inl(bfull, (nbl - 1) & 1u, a.status);
-        } else if (CVT && warp >= 2) {
-            // ----------------------- converters (CVT) -----------------------
-            // warp 2 converts rows 0-63 of each tile, warp 3 rows 64-127; lane
-            // (g, rw) = (lane / 8, lane % 8) takes row 8 G + rw of row group G and
-            // the 8-index groups g and g + 4 (fp32 chunks 2g, 2g + 1 of box 0 and
-            // of box 1; hi and lo chunks g and g + 4).  The eight lanes of a
-            // shared-memory phase take eight rows, whose swizzled chunks differ.
-            // The loads of group G + 1 are issued before group G is converted.
-            const int cw = warp - 2;
-            const int g = lane >> 3, rw = lane & 7;
-            const uint32_t ring_u = smem_u32(ring);
-            Ring<NS> rr;
-            bool ok = true;
-            float big = 0.f;   // largest scaled magnitude (NaN if any was NaN)
-            for (int64_t ty = blockIdx.y; ty < ty_end && ok; ty += ty_step) {
-                const int64_t m0 = ty * kBM;
-                // per-row slab scales of this warp's 64 rows (mode 0: the slab is the row)
-                __syncwarp();
-                if (a.slab_rows) {
-                    sscale[64 * cw + lane] = y_scale_row(a, m0 + 64 * cw + lane);
-                    sscale[64 * cw + 32 + lane] = y_scale_row(a, m0 + 64 * cw + 32 + lane);
-                }
-                __syncwarp();
-                for (int jc = jc0; jc < jc1 && ok; ++jc) {
-                    const int ck = chunk_len(jc);
-                    for (int64_t pi = pre_lo; pi < pre_hi && ok; ++pi) {
-                        const float sy_pre = a.slab_rows ? 1.f : y_scale_pre(a, pi);
-                        for (int q = 0; q < ck; ++q, rr.next()) {
-                            if (!warp_wait_inl(&yfull[rr.slot], rr.phase, abort_flag, a.status, kStatusTimeoutLo)) {
-                                ok = false;
-                                break;
-                            }
-                            const uint32_t st = ring_u + (uint32_t)rr.slot * L::kStage;
-                            // box h of row group G: this lane's two fp32 chunks (8 indices)
-                            auto load = [&](int G, int h, float4* w) {
-                                const uint32_t base = st + (uint32_t)h * L::kA + (uint32_t)(64 * cw + 8 * G + rw) * 128u;
-                                w[0] = lds128(base + (uint32_t)(((2 * g) ^ rw) << 4));
-                                w[1] = lds128(base + (uint32_t)(((2 * g + 1) ^ rw) << 4));
-                            };
-                            // split 8 scaled values into hi and lo words
-                            auto split8 = [&](const float4* w, float sy, uint32_t* hw, uint32_t* lw) {
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float4 f = w[e >> 1];
-                                    const float x0 = ((e & 1) ? f.z : f.x) * sy;
-                                    const float x1 = ((e & 1) ? f.w : f.y) * sy;
-                                    big = absmax_nan(big, absmax_nan(x0, x1));
-                                    const __half2 hh = __floats2half2_rn(x0, x1);
-                                    const float2 hf = __half22float2(hh);
-                                    hw[e] = half2_bits(hh);
-                                    lw[e] = half2_bits(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
-                                }
-                            };
-                            auto put = [&](int G, int h, const uint32_t* hw, const uint32_t* lw) {
-                                const uint32_t off =
-                                    (uint32_t)(64 * cw + 8 * G + rw) * 128u + (uint32_t)(((g + 4 * h) ^ rw) << 4);
-                                sts128(st + off, hw[0], hw[1], hw[2], hw[3]);
-                                sts128(st + L::kA + off, lw[0], lw[1], lw[2], lw[3]);
-                            };
-                            // box 0 of group G + 1 is loaded while group G is split; every
-                            // load of group G's rows (both boxes) precedes its stores
-                            float4 a0[2], a1[2];
-                            load(0, 0, a0);
-#pragma unroll
-                            for (int G = 0; G < 8; ++G) {
-                                load(G, 1, a1);
-                                const float sy = a.slab_rows ? sscale[64 * cw + 8 * G + rw] : sy_pre;
-                                uint32_t hw[4], lw[4];
-                                split8(a0, sy, hw, lw);
-                                if (G + 1 < 8) load(G + 1, 0, a0);
-                                __syncwarp();
-                                put(G, 0, hw, lw);
-                                split8(a1, sy, hw, lw);
-                                put(G, 1, hw, lw);
-                            }
-                            fence_proxy_async();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&full[rr.slot]);
-                        }
-                    }
-                }
-            }
-            if (__any_sync(0xffffffffu, !(big < 65504.f)) && lane == 0) atomicOr(a.ovf, 1u);
         } else if (warp == 1 && lane == 0) {
             // ------------------------- MMA issuer -------------------------
             // kind::f16: fp16 A and B (B K-major; A K-major, or MN-major with the
@@ -2586,7 +2589,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             wait_drain_inl(mma_done, 0, a.status);
         }
     } else {
-        regs_inc<kImgRegsEpi>();
+        regs_inc<CVT ? kCvtRegsEpi : kImgRegsEpi>();
         // ---------------------- epilogue (16 warps) ----------------------
         constexpr int kCols = BN / 4;
         if constexpr (SMALL) {
@@ -2595,7 +2598,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             // summed through shared memory.
             static_assert(kCols % kImgEpiLd == 0, "TMEM load width");
             const int quad = warp & 3;
-            const int part = (warp - kImgEpiWarp0) >> 2;
+            const int part = (warp - EW0) >> 2;
             const int64_t c0 = r0 + part * kCols;
             const int Iv = (int)a.I;
             const int lg = 32 * quad + lane;
@@ -2652,7 +2655,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
             asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
             if (live) {
                 float* dst = a.dst + (int64_t)blockIdx.z * a.dst_split_stride;
-                for (int idx = tid - 32 * kImgEpiWarp0; idx < Iv * BN; idx += kEpiWarps * 32) {
+                for (int idx = tid - 32 * EW0; idx < Iv * BN; idx += kEpiWarps * 32) {
                     const int i = idx / BN, c = idx - i * BN;
                     if (r0 + c >= a.R) continue;
                     float sum = 0.f;
@@ -2664,7 +2667,7 @@ __global__ void __launch_bounds__(kImgThreads, 1) tc_img_kernel(const __grid_con
         constexpr int kGv = (kCols + 31) / 32;   // G values a lane holds
         static_assert(kCols % kImgEpiLd == 0, "TMEM load width");
         const int quad = warp & 3;
-        const int part = (warp - kImgEpiWarp0) >> 2;
+        const int part = (warp - EW0) >> 2;
         const int64_t c0 = r0 + part * kCols;
         int zb = 0;
         uint32_t zph = 0;
@@ -3824,13 +3827,14 @@ cudaError_t launch_img(const TcArgs& args, dim3 grid, cudaStream_t s) {
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, tc_img_kernel<BN, SMALL, MN, CVT>);
         if (e != cudaSuccess) return e;
-        if (fa.numRegs < kImgRegsLaunch || fa.numRegs * kImgThreads > 65536) return cudaErrorInvalidConfiguration;
+        const int need = CVT ? kCvtRegsLaunch : kImgRegsLaunch, threads = CVT ? kCvtThreads : kImgThreads;
+        if (fa.numRegs < need || fa.numRegs * threads > 65536) return cudaErrorInvalidConfiguration;
         e = cudaFuncSetAttribute(tc_img_kernel<BN, SMALL, MN, CVT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)SmemImg<BN, SMALL>::kTotal);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    tc_img_kernel<BN, SMALL, MN, CVT><<<grid, kImgThreads, SmemImg<BN, SMALL>::kTotal, s>>>(args);
+    tc_img_kernel<BN, SMALL, MN, CVT><<<grid, CVT ? kCvtThreads : kImgThreads, SmemImg<BN, SMALL>::kTotal, s>>>(args);
     return cudaGetLastError();
 }
 
