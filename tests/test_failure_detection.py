@@ -26,15 +26,19 @@ import dense_tensor_decomposition_gb300 as mk  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 
-def test_expired_wait_sets_status_and_context_survives():
+# one CTA (one row tile, one column tile, few pre indices); and the kernel that
+# converts Y in place (64 CTAs, with its converter warps and image stores)
+@pytest.mark.parametrize("dims,R,path,convert", [((128, 16, 32), 64, "tc", False),
+                                                 ((256, 64, 128), 256, "auto", True)])
+def test_expired_wait_sets_status_and_context_survives(dims, R, path, convert):
     lib = mk.load_library()
     lib.mttkrp_test_withhold_signal.argtypes = [ctypes.c_int]
     lib.mttkrp_test_withhold_signal.restype = ctypes.c_int
-    dims, R = (128, 16, 32), 64   # one CTA: one row tile, one column tile, few pre indices
     try:
-        plan = mk.Plan(dims, R, "tc")
+        plan = mk.Plan(dims, R, path)
     except mk.MttkrpError:
         pytest.skip("tensor-core path unavailable")
+    assert ("tc_convert=1" in plan.describe(0)) == convert
     Y, A = synth.random_case(808, dims, R)
     Yd = torch.from_numpy(Y).cuda()
     Ad = [torch.from_numpy(a).cuda() for a in A]
