@@ -119,6 +119,7 @@ struct TcArgs {
     // non-null: the kernel runs only if *enable is set (the exact redo after a
     // converting launch whose sampled scales were too small)
     const uint32_t* enable;
+    int g_ones;               // every G entry is 1 (mode-n product): the epilogue adds Z as is
 };
 
 // ---------------------------------------------------------------------------
@@ -2165,8 +2166,8 @@ struct SmemImg {
     static constexpr uint32_t kB = BN * 128;       // one K-step of B (hi or lo)
     static constexpr uint32_t kBRes = kImgCK * 2 * kB;
     // barriers in the first 512 bytes, then (in-place conversion) the scales of
-    // the row tile's 128 rows
-    static constexpr uint32_t kBarBytes = 1024;
+    // the row tile's 128 rows, then the reciprocals of the tile's column scales
+    static constexpr uint32_t kBarBytes = 2048;
     static constexpr uint32_t kFree = 232448u - 1024u - kBarBytes - kBRes;
     static constexpr int kStages = kFree / kStage > 6 ? 6 : (int)(kFree / kStage);
     // small I: the slot sums at the end go through a [128][BN + 4] fp32 buffer
@@ -2229,6 +2230,8 @@ __global__ void __launch_bounds__(CVT ? kCvtThreads : kImgThreads, 1) tc_img_ker
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     uint64_t* yfull = mma_done + 2;             // [NS] (CVT) the fp32 boxes of the stage landed
     float* sscale = reinterpret_cast<float*>(smem + L::kOffBars + 512);   // [128] (CVT) row scales
+    float* colinv = reinterpret_cast<float*>(smem + L::kOffBars + 1024);  // [BN] 1 / column scale
+    static_assert(BN * 4 <= 1024, "column-scale area");
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -2669,6 +2672,11 @@ __global__ void __launch_bounds__(CVT ? kCvtThreads : kImgThreads, 1) tc_img_ker
         const int quad = warp & 3;
         const int part = (warp - EW0) >> 2;
         const int64_t c0 = r0 + part * kCols;
+        // reciprocals of the column tile's scales, once a CTA (exact powers of two)
+        for (int c = tid - 32 * EW0; c < BN; c += kEpiWarps * 32)
+            colinv[c] = r0 + c < a.R ? pow2_recip(a.colscale[r0 + c]) : 0.f;
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+        const float* cinv = colinv + part * kCols;
         int zb = 0;
         uint32_t zph = 0;
         bool ok = true;
@@ -2682,7 +2690,8 @@ __global__ void __launch_bounds__(CVT ? kCvtThreads : kImgThreads, 1) tc_img_ker
 #pragma unroll
             for (int u = 0; u < kGv; ++u) {
                 const int e = 32 * u + lane;
-                g[u] = (e < kCols && c0 + e < a.R && pi < pre_hi) ? __ldg(a.gtab + pi * a.R + c0 + e) : 0.f;
+                g[u] = (!a.g_ones && e < kCols && c0 + e < a.R && pi < pre_hi) ? __ldg(a.gtab + pi * a.R + c0 + e)
+                                                                                : 0.f;
             }
         };
         float g_next[kGv];
@@ -2705,11 +2714,16 @@ __global__ void __launch_bounds__(CVT ? kCvtThreads : kImgThreads, 1) tc_img_ker
                     uint32_t z[kImgEpiLd];
                     tmem_ld_cols<kImgEpiLd>(tbase + cc, z);
                     tmem_ld_wait();
+                    if (a.g_ones) {
 #pragma unroll
-                    for (int q = 0; q < kImgEpiLd; ++q) {
-                        const int e = cc + q;
-                        const float g = __shfl_sync(0xffffffffu, g_cur[e / 32], e % 32);
-                        acc[e] = fmaf(g, __uint_as_float(z[q]), acc[e]);
+                        for (int q = 0; q < kImgEpiLd; ++q) acc[cc + q] += __uint_as_float(z[q]);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < kImgEpiLd; ++q) {
+                            const int e = cc + q;
+                            const float g = __shfl_sync(0xffffffffu, g_cur[e / 32], e % 32);
+                            acc[e] = fmaf(g, __uint_as_float(z[q]), acc[e]);
+                        }
                     }
                 }
                 tc_fence_before();
@@ -2727,7 +2741,7 @@ __global__ void __launch_bounds__(CVT ? kCvtThreads : kImgThreads, 1) tc_img_ker
             float* dst = a.dst + p * a.R * a.ttm_q + q;
 #pragma unroll
             for (int e = 0; e < kCols; ++e)
-                if (c0 + e < a.R) dst[(c0 + e) * a.ttm_q] = acc[e] * inv_y * pow2_recip(a.colscale[c0 + e]);
+                if (c0 + e < a.R) dst[(c0 + e) * a.ttm_q] = acc[e] * inv_y * cinv[e];
         } else if (!*abort_flag && row < a.I) {
             // undo the power-of-two scales of Y and of each Binner column (exact)
             const float inv_y = y_unscale(a, row);
@@ -2735,12 +2749,9 @@ __global__ void __launch_bounds__(CVT ? kCvtThreads : kImgThreads, 1) tc_img_ker
             const bool vst = (a.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.dst) & 15) == 0);
 #pragma unroll
             for (int e = 0; e < kCols; e += 4) {
-                float v[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float cs = (c0 + e + q < a.R) ? a.colscale[c0 + e + q] : 1.f;
-                    v[q] = acc[e + q] * inv_y * pow2_recip(cs);
-                }
+                const float4 ci = *reinterpret_cast<const float4*>(cinv + e);
+                const float v[4] = {acc[e] * inv_y * ci.x, acc[e + 1] * inv_y * ci.y, acc[e + 2] * inv_y * ci.z,
+                                    acc[e + 3] * inv_y * ci.w};
                 if (vst && c0 + e + 4 <= a.R) {
                     *reinterpret_cast<float4*>(dst + e) = make_float4(v[0], v[1], v[2], v[3]);
                 } else {
@@ -2748,7 +2759,6 @@ __global__ void __launch_bounds__(CVT ? kCvtThreads : kImgThreads, 1) tc_img_ker
                     for (int q = 0; q < 4; ++q)
                         if (c0 + e + q < a.R) dst[e + q] = v[q];
                 }
-                asm volatile("" ::: "memory");   // keep one group of column scales in flight
             }
         }
         }   // row tiles
@@ -4734,6 +4744,7 @@ int tc_ttm_product(const float* M, float* T, int64_t P, int64_t N, int64_t Q, in
     args.slab_rows = 0;
     args.colscale = colscale;
     args.ttm_q = Q == 1 ? 0 : Q;
+    args.g_ones = 1;
     args.status = status;
     // persistent: one CTA per SM, the row tiles of a column tile dealt out in
     // turn (the column tiles of one row tile run side by side and share its A
