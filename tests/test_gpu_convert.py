@@ -90,3 +90,25 @@ def test_converting_mode_repeated_calls():
     for a, b in zip(first, second):
         assert torch.equal(a, b)
     assert mk.device_status() == 0
+
+
+def test_converting_plan_with_misaligned_tensor():
+    """Y only 4-byte aligned: the tensor maps cannot address it, so every mode
+    (the converting one included) runs its SIMT plan; then an aligned call on the
+    same plan converts again."""
+    dims, R, mode = CONVERT_SHAPES[3]
+    Y, A = inputs(dims, R, 610)
+    ybuf = torch.zeros(Y.size + 1, device="cuda")
+    ybuf[1:] = torch.from_numpy(Y.ravel()).cuda()
+    Ym = ybuf[1:].view(dims)
+    Ad = [torch.from_numpy(a).cuda() for a in A]
+    plan = mk.Plan(dims, R)
+    assert "tc_convert=1" in plan.describe(mode)
+    outs = plan.all_modes(Ym, Ad)
+    aligned = plan.all_modes(torch.from_numpy(Y).cuda(), Ad)
+    torch.cuda.synchronize()
+    assert mk.device_status() == 0
+    for k in range(len(dims)):
+        ref = oracle.mttkrp(Y, A, k)
+        assert rel_fro(outs[k].cpu().numpy(), ref) <= TOL, f"misaligned, mode {k}"
+        assert rel_fro(aligned[k].cpu().numpy(), ref) <= TOL, f"aligned, mode {k}"
