@@ -2904,8 +2904,12 @@ __global__ void __launch_bounds__(256, 3) split_image_t_kernel(const float* __re
             tile_scales(p0);
             const int nvals = rows * Ii;
             const int64_t base = p0 * I;
-            // eight 16-byte loads in flight a thread before any conversion
-            constexpr int kU = 8;
+            // four 16-byte loads in flight a thread before any conversion; the
+            // (row, col) of a thread's value 4 f is stepped from one division
+            constexpr int kU = 4;
+            const int step_r = (4 * 256) / Ii, step_c = (4 * 256) - step_r * Ii;   // 4 * 256 values
+            int row0 = (4 * (int)threadIdx.x) / Ii;
+            int col0 = 4 * (int)threadIdx.x - row0 * Ii;
             for (int f0 = 0; 4 * f0 < nvals; f0 += kU * 256) {
                 float4 vv[kU];
 #pragma unroll
@@ -2924,10 +2928,16 @@ __global__ void __launch_bounds__(256, 3) split_image_t_kernel(const float* __re
 #pragma unroll
                 for (int u = 0; u < kU; ++u) {
                     const int f = f0 + threadIdx.x + 256 * u;
+                    int row = row0, col = col0;   // (row, col) of value 4 f
+                    row0 += step_r;
+                    col0 += step_c;
+                    if (col0 >= Ii) {
+                        col0 -= Ii;
+                        ++row0;
+                    }
                     if (4 * f >= nvals) continue;
                     const float v[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
                     uint32_t hb[4], lb[4];
-                    int row = (4 * f) / Ii, col = 4 * f - row * Ii;   // (row, col) of value 4 f
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int idx = 4 * f + q;
@@ -2960,10 +2970,19 @@ __global__ void __launch_bounds__(256, 3) split_image_t_kernel(const float* __re
                 }
             }
             __syncthreads();
-            // transposed: row c holds p0 .. p0 + rows - 1 at c * P + p, two p a lane
+            // transposed: row c holds p0 .. p0 + rows - 1 at c * P + p, two p a lane;
+            // (c, pair) of item w stepped from one division
             const int pairs = (rows + 1) / 2;
+            const int sc = (int)blockDim.x / pairs, sp = (int)blockDim.x - sc * pairs;
+            int c_w = (int)threadIdx.x / pairs, p_w = (int)threadIdx.x - c_w * pairs;
             for (int w = threadIdx.x; w < Ii * pairs; w += blockDim.x) {
-                const int c = w / pairs, pp = 2 * (w - c * pairs);
+                const int c = c_w, pp = 2 * p_w;
+                c_w += sc;
+                p_w += sp;
+                if (p_w >= pairs) {
+                    p_w -= pairs;
+                    ++c_w;
+                }
                 const uint32_t w0 = shf[c * stride + pp];
                 const int64_t e = (int64_t)c * P + p0 + pp;
                 if (pp + 1 < rows) {
