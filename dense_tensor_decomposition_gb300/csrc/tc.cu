@@ -4147,7 +4147,7 @@ int tc_prepare(const Plan& p, const ModePlan& mp, const float* Y, void* ws, cuda
 
 bool tc_fuse_eligible(const Plan& p, const ModePlan& mp) {
     if (mp.path != MTTKRP_PATH_TC || !mp.tc_img || mp.tc_img_mn || mp.tc_img_t || mp.tc_small || mp.explicit_krp ||
-        mp.bn != 256 || p.img_t || !p.img_nat || mp.g.J != mp.g.Jq || mp.g.Jq % kBK4 != 0)
+        p.img_t || !p.img_nat || mp.g.J != mp.g.Jq || mp.g.Jq % kBK4 != 0)
         return false;
     // one column tile: with several, each would convert the same Y tiles
     if (cdiv64(mp.g.R, mp.bn) != 1) return false;
@@ -4414,7 +4414,9 @@ int tc_run_phase(const Plan& p, const ModePlan& mp, const float* Y, const float*
               (unsigned)mp.splits);
     cudaError_t e;
     if (phase == 1) {
-        e = launch_img<256, false, false, true>(args, grid, stream);
+        e = mp.bn == 256 ? launch_img<256, false, false, true>(args, grid, stream)
+          : mp.bn == 128 ? launch_img<128, false, false, true>(args, grid, stream)
+                         : launch_img<64, false, false, true>(args, grid, stream);
     } else if (mp.tc_img) {
         if (mp.tc_small)
             e = mp.bn == 128 ? launch_img<128, true>(args, grid, stream) : launch_img<64, true>(args, grid, stream);

@@ -40,7 +40,7 @@ int tc_redo_main(const Plan& p, const ModePlan& mp, const float* Y, const float*
                  const float* gtab, const int64_t* basetab, void* binner_ws, float* dst,
                  cudaStream_t stream, int* nlaunch, char* errbuf, size_t errlen);
 // Whether a mode's main kernel can convert Y in place (natural K-major image
-// tiles, 256 columns in one column tile, an inner group of whole modes after
+// tiles in one column tile, an inner group of whole modes after
 // it, no transposed images in the plan).
 bool tc_fuse_eligible(const Plan& p, const ModePlan& mp);
 // The mode the plan converts in (p.fuse_mode): among the eligible modes, one

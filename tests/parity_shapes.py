@@ -69,7 +69,7 @@ H2_SHAPES = [((130, 40, 48), 300), ((40, 36, 128), 450), ((200, 96, 64), 300), (
 # images (tc_convert=1; it runs first in an all-modes call), and that mode:
 # mode 0 (slab scales by output row) with two row tiles, a 2-row tail, a column
 # tail (R = 200 of 256); mode 1 and mode 2 (slab scales carried by G) with row
-# and column tails and a 4-way tensor
+# and column tails and a 4-way tensor; 128-column (R = 100) and 64-column tiles
 CONVERT_SHAPES = [
     ((256, 64, 128), 256, 0),
     ((130, 40, 128), 256, 0),
@@ -77,4 +77,6 @@ CONVERT_SHAPES = [
     ((16, 256, 128), 256, 1),
     ((24, 200, 128), 230, 1),
     ((3, 4, 256, 128), 256, 2),
+    ((256, 64, 128), 100, 0),
+    ((192, 64, 128), 64, 0),
 ]

@@ -52,7 +52,7 @@ def test_converting_mode_and_stored_images(dims, R, mode):
 
 
 @pytest.mark.parametrize("factor", [1e6, 3.0])
-@pytest.mark.parametrize("shape", [0, 3], ids=["mode0", "mode1"])
+@pytest.mark.parametrize("shape", [0, 3, 7], ids=["mode0", "mode1", "bn64"])
 def test_converting_mode_unsampled_outlier(factor, shape):
     """Element 1000 of slab 1 lies in a chunk the maxima sample skips: 1e6
     leaves the fp16 range once scaled (the redo runs), 3.0 stays within it."""

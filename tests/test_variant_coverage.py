@@ -102,7 +102,7 @@ def test_converting_mode_is_gpu_tested():
     with them (tc_convert=1) and in no other; the 128^4 workload converts in
     mode 2 (its 128 x 128 tiles of one pre index are contiguous); no mode of the
     512^3, R = 2000 workload does (eight column tiles would each convert)."""
-    for dims, R, mode in CONVERT_SHAPES + [((128,) * 4, 256, 2)]:
+    for dims, R, mode in CONVERT_SHAPES + [((128,) * 4, 256, 2), ((256,) * 3, 64, 1)]:
         plan = mk.Plan(dims, R)
         flags = ["tc_convert=1" in plan.describe(k) for k in range(len(dims))]
         assert flags == [k == mode for k in range(len(dims))], (dims, R, flags)
