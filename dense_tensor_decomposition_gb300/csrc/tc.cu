@@ -2107,7 +2107,9 @@ __global__ void __launch_bounds__(kH2Threads, 1) tc_h2_kernel(const __grid_const
 // a TMEM accumulator.  Same arithmetic as tc_h2_kernel, but no producer warps:
 // the only hand-over per K-step (64 indices, twelve MMAs) is TMA -> MMA.
 // Roles: warp 0 TMA, warp 1 MMA, warps 2-3 idle (the control warpgroup, which
-// gives registers back), warps 4-19 epilogue (which take them).
+// gives registers back), warps 4-19 epilogue (which take them); the variant
+// that converts Y in place adds converter warps 4-7 and moves the epilogue to
+// warps 8-23.
 // ---------------------------------------------------------------------------
 constexpr int kBK4 = 64;          // contraction indices per K-step (128-byte fp16 rows)
 constexpr int kImgCK = 2;   // K-steps per B chunk and per TMEM drain (128 indices)
@@ -2197,10 +2199,10 @@ __device__ __forceinline__ uint32_t sdesc128mn_lo(uint32_t saddr) { return kDesc
 // loads each K-step as two 32-index fp32 boxes (128-byte swizzle) into the
 // stage; warps 4-7 (32 rows each) convert it in place into the hi and lo
 // tiles, with the same split and scales as split_image_kernel, and release it
-// to the MMA warp; the TMA warp stores the converted tiles to the
-// images (column tile 0 only; other column tiles read the same Y) one stage
-// behind its loads, and waits for a store's reads before it refills that
-// stage.  Every row's fp32 bytes and its hi and lo bytes lie in that row's
+// to the MMA warp; the TMA warp stores each converted tile to the images
+// (column tile 0 only; other column tiles read the same Y) once it is
+// converted, checking the tile it loaded NS - 1 loads earlier after each load,
+// and waits for a store's reads before it refills that stage.  Every row's fp32 bytes and its hi and lo bytes lie in that row's
 // 128-byte lines of the two halves of the stage, so one warp owns all the
 // bytes of its rows and loads them before it stores.  A scaled value outside
 // the fp16 range sets *a.ovf.
