@@ -788,14 +788,39 @@ def run_rotations(args, w):
     }))
 
 
+def ttm_roofline(flops, nbytes, kinds, kind_peak, hbm_gbs, ms):
+    """Roofline of a step of mode-n products: per product the slower of its flops
+    at the pipe it runs on (kind_peak[kind], TFLOP/s) and its algorithmic bytes
+    at HBM (hbm_gbs).  When the HBM times of the step add up to more than the
+    pipe times the line is reported as HBM-bound (GB/s, bytes over the step's
+    time), else against the flop-weighted pipe peak (TFLOP/s); t_roof_ms sums
+    the per-product maxima."""
+    t_pipe = [f / (kind_peak[k] * 1e12) for f, k in zip(flops, kinds)]
+    t_hbm = [b / (hbm_gbs * 1e9) for b in nbytes]
+    t_roof = sum(max(a, b) for a, b in zip(t_pipe, t_hbm))
+    if sum(t_hbm) > sum(t_pipe):
+        achieved = sum(nbytes) / (ms * 1e-3) / 1e9
+        out = {"bound": "hbm", "achieved": round(achieved, 1), "peak": round(hbm_gbs, 1), "unit": "GB/s",
+               "frac": round(achieved / hbm_gbs, 4)}
+    else:
+        achieved = sum(flops) / (ms * 1e-3) / 1e12
+        peak = sum(flops) / sum(t_pipe) / 1e12
+        out = {"bound": "alu" if set(kinds) == {"f32"} else "tensor", "achieved": round(achieved, 3),
+               "peak": round(peak, 3), "unit": "TFLOP/s", "frac": round(achieved / peak, 4)}
+    out["t_roof_ms"] = round(t_roof * 1e3, 4)
+    out["frac_of_t_roof"] = round(t_roof * 1e3 / ms, 4)
+    return out
+
+
 def run_ttm(args, w):
     """The dense mode-n product along every mode of the workload's tensor per
     step, one mttkrp_ttm_multi call (the tensor-core products share one pass
     that writes the fp16 images of X), each mode into its own preallocated
-    result.  One JSON line: TFLOP/s (2 J I_1..I_d flops per mode) against the
-    flop-weighted peak of the pipes the products run on, with the HBM time of
-    the algorithmic bytes beside it; ms_per_mode times each product alone
-    (mttkrp_ttm_ws, its own image pass included)."""
+    result.  One JSON line: TFLOP/s (2 J I_1..I_d flops per mode); the
+    roofline against the flop-weighted peak of the pipes the products run on,
+    or against HBM when the algorithmic bytes take longer (ttm_roofline);
+    ms_per_mode times each product alone (mttkrp_ttm_ws, its own image pass
+    included)."""
     import numpy as np
     import torch
     import dense_tensor_decomposition_gb300 as mk
@@ -851,8 +876,13 @@ def run_ttm(args, w):
     # once some J >= 64
     kinds = ["fp16x2" if need and mk.ttm_workspace_bytes(w.dims, k, Js[k]) > 0 else "f32"
              for k in range(w.d)]
-    t_peak = sum(2.0 * J * numel / (kpk[kd] * 1e12) for J, kd in zip(Js, kinds))
-    peak = flops / t_peak / 1e12
+    roof = ttm_roofline([2.0 * J * numel for J in Js],
+                        [4.0 * (numel + J * numel // n + J * n) for J, n in zip(Js, w.dims)],
+                        kinds, kpk, peaks["hbm_gbs"], ms)
+    roof.update({"peak_source": "per mode: fp16x2 = bf16 dense burst (" + src + ") / 3 products, "
+                                "f32 = fp32 FMA probe; flop-weighted; HBM: measured copy bandwidth",
+                 "hbm_ms_at_algorithmic_bytes": round(moved / (peaks["hbm_gbs"] * 1e9) * 1e3, 4),
+                 "hbm_peak_source": src})
     cpu = None if args.no_cpu_baseline else ttm_cpu_baseline(Xh, Ms_h, args.cpu_seconds)
     print(json.dumps({
         "metric": "dense mode-n product along every mode: TFLOP/s (2 J prod(I_n) per mode)",
@@ -861,12 +891,7 @@ def run_ttm(args, w):
         "impl": "ours",
         "config": {"workload": w.name, "dims": list(w.dims), "J": Js, "kinds": kinds,
                    "l2": "tensor larger than L2" if 4 * numel > 129e6 else "fits L2"},
-        "roofline": {"bound": "alu" if set(kinds) == {"f32"} else "tensor", "achieved": round(tflops, 3),
-                     "peak": round(peak, 3), "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
-                     "peak_source": "per mode: fp16x2 = bf16 dense burst (" + src + ") / 3 products, "
-                                    "f32 = fp32 FMA probe; flop-weighted",
-                     "hbm_ms_at_algorithmic_bytes": round(moved / (peaks["hbm_gbs"] * 1e9) * 1e3, 4),
-                     "hbm_peak_source": src},
+        "roofline": roof,
         "ms_per_mode": per_mode,
         "peaks_probe": probe,
         "cpu_baseline": cpu,

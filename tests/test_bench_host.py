@@ -50,3 +50,30 @@ def test_peaks_fall_back_when_unmeasured(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     peaks, src = bench.measured_peaks()
     assert src == "fallback" and peaks["hbm_gbs"] == 6800.0 and peaks["bf16_tflops"] == 1900.0
+
+
+def test_ttm_roofline_picks_the_slower_limit():
+    import bench
+    peaks = {"fp16x2": 659.3, "f32": 71.0}
+    # 512^3 square products: flops dominate (tensor-bound line in TFLOP/s)
+    n = 512 ** 3
+    flops = [2.0 * 512 * n] * 3
+    nbytes = [4.0 * (2 * n + 512 * 512)] * 3
+    r = bench.ttm_roofline(flops, nbytes, ["fp16x2"] * 3, peaks, 6780.7, 1.4)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - sum(flops) / 1.4e-3 / 1e12) < 1e-2
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    t_f = flops[0] / 659.3e12
+    assert abs(r["t_roof_ms"] - 3 * t_f * 1e3) < 1e-3
+    # 128^4 with J = 128: bytes dominate (HBM-bound line in GB/s)
+    n = 128 ** 4
+    flops = [2.0 * 128 * n] * 4
+    nbytes = [4.0 * (2 * n + 128 * 128)] * 4
+    r = bench.ttm_roofline(flops, nbytes, ["fp16x2"] * 4, peaks, 6780.7, 2.2)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6780.7
+    assert abs(r["achieved"] - sum(nbytes) / 2.2e-3 / 1e9) < 0.1
+    assert abs(r["t_roof_ms"] - sum(nbytes) / 6780.7e9 * 1e3) < 1e-3
+    assert abs(r["frac_of_t_roof"] - r["t_roof_ms"] / 2.2) < 1e-3
+    # the CUDA-core kernel on every mode
+    r = bench.ttm_roofline([1e9], [1e3], ["f32"], peaks, 6780.7, 1.0)
+    assert r["bound"] == "alu"
