@@ -2,8 +2,8 @@
 every 64-bit offset the kernels and the host planner form is exercised past
 the 32-bit range.  Every mode on the planner's path (fp16-image kernels; mode 1
 converts Y in place and writes the images, mode 2 reads them MN-major with a
-K-step tail) and on the SIMT path, and the tensor-core mode-n product of
-mode 1, against fp64 values computed from slices of the same tensor: output
+K-step tail) and on the SIMT path, and the mode-n product of mode 1 on the
+tensor cores and on the CUDA cores, against fp64 values computed from slices of the same tensor: output
 rows (the first, the middle, the last -- whose terms reach the end of Y) and
 sampled mode-n-product outputs.  Y is drawn on the device from a seeded
 generator; the checks copy only the slices they need."""
@@ -68,13 +68,14 @@ def test_mttkrp_past_2_31_elements(big, path):
     torch.cuda.empty_cache()
 
 
-def test_mode_n_product_past_2_31_elements(big):
+@pytest.mark.parametrize("path", ["tc", "simt"])
+def test_mode_n_product_past_2_31_elements(big, path):
     Y, _ = big
     J, mode, N = 64, 1, DIMS[1]
     assert mk.ttm_workspace_bytes(DIMS, mode, J) > 0
     rng = np.random.default_rng(2313)
     M = rng.standard_normal((J, N)).astype(np.float32)
-    T = mk.ttm(Y, mode, torch.from_numpy(M).cuda(), path="tc")
+    T = mk.ttm(Y, mode, torch.from_numpy(M).cuda(), path=path)
     torch.cuda.synchronize()
     assert mk.device_status() == 0
     p = torch.from_numpy(np.concatenate([[DIMS[0] - 1], rng.integers(0, DIMS[0], 199)])).cuda()
@@ -84,8 +85,11 @@ def test_mode_n_product_past_2_31_elements(big):
     got = T[p, torch.from_numpy(j).cuda(), q].double().cpu().numpy()
     want = np.einsum("sn,sn->s", x, M[j].astype(np.float64))
     bound = np.einsum("sn,sn->s", np.abs(x), np.abs(M[j]).astype(np.float64))
-    kd = min(128, -(-N // 64) * 64)
-    floor = 2.0 ** -36 * N * float(Y.abs().max()) * float(np.abs(M).max())
-    assert np.all(np.abs(got - want) <= (6 * kd + 24 + N) * U * bound + floor)
+    if path == "tc":
+        kd = min(128, -(-N // 64) * 64)
+        floor = 2.0 ** -36 * N * float(Y.abs().max()) * float(np.abs(M).max())
+        assert np.all(np.abs(got - want) <= (6 * kd + 24 + N) * U * bound + floor)
+    else:   # one fp32 fused multiply-add chain over the N products
+        assert np.all(np.abs(got - want) <= N * U / (1 - N * U) * bound + 1e-30)
     del T
     torch.cuda.empty_cache()
