@@ -352,3 +352,19 @@ def test_pipelined_end_to_end_matches_device_calls():
     for t in range(3):
         for k in range(len(dims)):
             assert np.array_equal(got[t][k].numpy(), want[t][k]), (t, k)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_largest_rank(path):
+    """R = 4096, the largest rank the planner is sized for (16 column tiles of
+    256; the stacked small-I_k kernel with 32 of 128), every mode against the
+    oracle on sampled output rows."""
+    dims, R = (160, 40, 64), 4096
+    Y, A = synth.random_case(4096, dims, R)
+    got = gpu_modes(Y, A, path)
+    for k in range(3):
+        rows = sample_rows(dims[k], seed=40 + k, n=4)
+        ref = oracle.mttkrp(Y, A, k, rows=rows)
+        err = rel_fro(got[k][rows], ref)
+        assert err <= TOL, f"R=4096 mode {k} path {path}: rel err {err:.3e}"
+    assert mk.device_status() == 0
