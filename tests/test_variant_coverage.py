@@ -108,3 +108,35 @@ def test_converting_mode_is_gpu_tested():
         assert flags == [k == mode for k in range(len(dims))], (dims, R, flags)
     plan = mk.Plan((512,) * 3, 2000)
     assert not any("tc_convert=1" in plan.describe(k) for k in range(3))
+
+
+def test_converting_mode_rules_on_random_shapes():
+    """Over random shapes and ranks: at most one mode converts Y in place; it is a
+    natural K-major image mode (kernel img.nat.bn*) with one column tile and an
+    inner group of whole modes after it (J = Jq, a multiple of 64); and no plan
+    with a transposed-image mode converts."""
+    rng = random.Random(7)
+    sizes = [2, 3, 8, 16, 20, 32, 40, 64, 96, 100, 128, 130, 200, 256, 512]
+    ranks = [8, 32, 48, 64, 100, 128, 200, 256, 300, 1000]
+    seen = 0
+    for _ in range(800):
+        d = rng.randint(2, 5)
+        dims = tuple(rng.choice(sizes) for _ in range(d))
+        if math.prod(dims) > 1 << 27:
+            continue
+        R = rng.choice(ranks)
+        plan = mk.Plan(dims, R)
+        descs = [dict(f.split("=", 1) for f in plan.describe(k).split() if "=" in f) for k in range(d)]
+        conv = [k for k in range(d) if descs[k]["tc_convert"] == "1"]
+        assert len(conv) <= 1, (dims, R, conv)
+        if not conv:
+            continue
+        seen += 1
+        k = conv[0]
+        f = descs[k]
+        assert f["kernel"].startswith("img.nat.bn") and ".small" not in f["kernel"], (dims, R, f["kernel"])
+        bn = int(f["kernel"].split("bn")[1])
+        assert -(-R // bn) == 1, (dims, R, bn)
+        assert f["J"] == f["Jq"] and int(f["J"]) % 64 == 0, (dims, R, f["J"], f["Jq"])
+        assert all(x["tc_fp16_image"] != "2" for x in descs), (dims, R)
+    assert seen >= 20, seen
