@@ -197,25 +197,22 @@ __global__ void __launch_bounds__(256)
          e += (int64_t)gridDim.x * blockDim.x) {
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
         const float4* p = part + e;
-        int64_t sp = 0;
-        for (; sp + 8 <= splits; sp += 8) {   // eight 16-byte loads in flight
+        // up to eight 16-byte loads in flight (the last batch predicated), then
+        // the compensated sums in split order
+        for (int64_t sp = 0; sp < splits; sp += 8) {
+            const int nb = splits - sp < 8 ? (int)(splits - sp) : 8;
             float4 v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldcs(p + (sp + u) * n4);
+            for (int u = 0; u < 8; ++u)
+                if (u < nb) v[u] = __ldcs(p + (sp + u) * n4);
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
+                if (u >= nb) break;
                 kahan_add(s0, c0, v[u].x);
                 kahan_add(s1, c1, v[u].y);
                 kahan_add(s2, c2, v[u].z);
                 kahan_add(s3, c3, v[u].w);
             }
-        }
-        for (; sp < splits; ++sp) {
-            const float4 v = __ldcs(p + sp * n4);
-            kahan_add(s0, c0, v.x);
-            kahan_add(s1, c1, v.y);
-            kahan_add(s2, c2, v.z);
-            kahan_add(s3, c3, v.w);
         }
         out[e] = make_float4(s0 + c0, s1 + c1, s2 + c2, s3 + c3);
     }
